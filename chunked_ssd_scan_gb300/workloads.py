@@ -1,0 +1,168 @@
+"""Seeded synthetic inputs for the SSD scan and the selective scan.
+
+This module only draws random numbers in the shapes, dtypes and distributions of the workloads;
+it holds none of the scan's arithmetic.  Tests and the benchmark feed the same tensors to the
+CUDA library and to the CPU oracle.
+
+Recipe (one torch CPU ``Generator`` per call, seeded):
+- SSD draw order x, B, C, dt, A_h, theta, init_state; all drawn in fp32 and then cast to the
+  I/O dtype (x, B, C, y share it; dA, theta and the states stay fp32).
+    x ~ N(0,1) * x_scale;  B, C ~ N(0,1) * bc_scale
+    dt = softplus(N(0,1) - 2)  [b,T,H];  A_h = -exp(U(0, ln 16))  [H];  dA = dt * A_h
+    "slow decay" variant: dA = -U(0, 0.01)  (so the chunk-to-chunk state carry stays visible)
+    theta ~ U(-0.1, 0.1)  [b,T,H,N/2];  init_state ~ N(0,1)  [b,H,P,N] when requested
+- Selective scan draw order u, delta, A, B, C, skip:
+    u ~ N(0,1);  delta = softplus(N(0,1));  A = -U(0.5, 2)  [D,N];  B, C ~ N(0,1)  [b,T,N];
+    skip ~ N(0,1)  [D]
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+from typing import Optional
+
+import torch
+
+
+@dataclasses.dataclass(frozen=True)
+class SSDConfig:
+    name: str
+    batch: int
+    seqlen: int
+    nheads: int
+    headdim: int
+    dstate: int
+    chunk_len: int
+    mimo_rank: int
+    ngroups: int
+    dtype: str            # "f32" or "bf16": the dtype of x, B, C and y
+    theta: bool = False
+    x_scale: float = 1.0
+    bc_scale: float = 1.0
+
+    @property
+    def torch_dtype(self) -> torch.dtype:
+        return torch.float32 if self.dtype == "f32" else torch.bfloat16
+
+    @property
+    def tokens(self) -> int:
+        """Tokens per call: one per (batch, time step); MIMO ranks do not multiply it."""
+        return self.batch * self.seqlen
+
+    def with_(self, **kw) -> "SSDConfig":
+        return dataclasses.replace(self, **kw)
+
+    def io_bytes(self) -> int:
+        """Algorithmic HBM bytes: every input read once and every output written once."""
+        e = 4 if self.dtype == "f32" else 2
+        b, T, R, H, P, N, G = (self.batch, self.seqlen, self.mimo_rank, self.nheads, self.headdim,
+                               self.dstate, self.ngroups)
+        nbytes = b * T * R * H * P * e * 2          # x read, y written
+        nbytes += b * T * R * G * N * e * 2         # B, C read
+        nbytes += b * T * H * 4                     # dA read
+        nbytes += b * H * P * N * 4                 # final state written
+        if self.theta:
+            nbytes += b * T * H * (N // 2) * 4      # theta read
+        return nbytes
+
+    def causal_flops(self) -> int:
+        """Contraction FLOPs of the chunked method, counting only the causal part of each chunk."""
+        b, T, R, H, P, N, G, l = (self.batch, self.seqlen, self.mimo_rank, self.nheads,
+                                  self.headdim, self.dstate, self.ngroups, self.chunk_len)
+        nch = -(-T // l)
+        L = l * R
+        pairs = R * R * l * (l + 1) // 2                     # causal (i, j) pairs per chunk
+        cb = 2 * pairs * N * b * nch * G                     # K2, once per B/C group
+        diag = 2 * pairs * P * b * nch * H                   # K5 intra-chunk
+        state = 2 * P * N * L * b * nch * H                  # K3
+        off = 2 * L * N * P * b * nch * H                    # K5 inter-chunk
+        return cb + diag + state + off
+
+
+@dataclasses.dataclass(frozen=True)
+class SelectiveScanConfig:
+    name: str
+    batch: int
+    seqlen: int
+    d_model: int
+    d_state: int
+
+    @property
+    def tokens(self) -> int:
+        return self.batch * self.seqlen
+
+    def io_bytes(self) -> int:
+        b, T, D, N = self.batch, self.seqlen, self.d_model, self.d_state
+        return 4 * (3 * b * T * D + 2 * b * T * N + D * N + D)
+
+    def with_(self, **kw) -> "SelectiveScanConfig":
+        return dataclasses.replace(self, **kw)
+
+
+# The five workloads: four SSD problems and one selective scan.
+TINY_SISO_F32 = SSDConfig("tiny_siso_f32", 1, 256, 2, 16, 16, 64, 1, 2, "f32")
+MAMBA2_SISO_BF16 = SSDConfig("mamba2_siso_bf16", 4, 4096, 32, 64, 128, 256, 1, 1, "bf16")
+MAMBA3_MIMO_BF16 = SSDConfig("mamba3_mimo_bf16", 2, 8192, 32, 64, 128, 64, 4, 32, "bf16",
+                             bc_scale=1.0 / math.sqrt(128))
+LONG_ROT_F32 = SSDConfig("long_rotation_f32", 1, 131072, 24, 64, 64, 256, 1, 24, "f32",
+                         theta=True)
+SELECTIVE_SCAN_F32 = SelectiveScanConfig("selective_scan_f32", 4, 4096, 512, 16)
+
+SSD_CONFIGS = [TINY_SISO_F32, MAMBA2_SISO_BF16, MAMBA3_MIMO_BF16, LONG_ROT_F32]
+
+
+def make_ssd_inputs(cfg: SSDConfig, seed: int = 0, *, slow_decay: bool = False,
+                    init_state: bool = False, device: Optional[str] = None) -> dict:
+    """Draw one problem for ``cfg`` on the CPU (then optionally move it to ``device``)."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed)
+    b, T, R, H, P, N, G = (cfg.batch, cfg.seqlen, cfg.mimo_rank, cfg.nheads, cfg.headdim,
+                           cfg.dstate, cfg.ngroups)
+    f32 = torch.float32
+    x = torch.randn((b, T, R, H, P), generator=g, dtype=f32)
+    if cfg.x_scale != 1.0:
+        x.mul_(cfg.x_scale)
+    B = torch.randn((b, T, R, G, N), generator=g, dtype=f32)
+    C = torch.randn((b, T, R, G, N), generator=g, dtype=f32)
+    if cfg.bc_scale != 1.0:
+        B.mul_(cfg.bc_scale)
+        C.mul_(cfg.bc_scale)
+    dt = torch.nn.functional.softplus(torch.randn((b, T, H), generator=g, dtype=f32) - 2.0)
+    A_h = -torch.exp(torch.rand((H,), generator=g, dtype=f32) * math.log(16.0))
+    if slow_decay:
+        dA = -torch.rand((b, T, H), generator=g, dtype=f32) * 0.01
+    else:
+        dA = dt * A_h
+    theta = None
+    if cfg.theta:
+        theta = (torch.rand((b, T, H, N // 2), generator=g, dtype=f32) * 0.2 - 0.1)
+    init = torch.randn((b, H, P, N), generator=g, dtype=f32) if init_state else None
+    out = {
+        "x": x.to(cfg.torch_dtype),
+        "dA": dA.contiguous(),
+        "B": B.to(cfg.torch_dtype),
+        "C": C.to(cfg.torch_dtype),
+        "theta": theta,
+        "init_state": init,
+    }
+    if device is not None:
+        out = {k: (v.to(device) if v is not None else None) for k, v in out.items()}
+    return out
+
+
+def make_selective_scan_inputs(cfg: SelectiveScanConfig, seed: int = 0,
+                               device: Optional[str] = None) -> dict:
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed)
+    b, T, D, N = cfg.batch, cfg.seqlen, cfg.d_model, cfg.d_state
+    f32 = torch.float32
+    u = torch.randn((b, T, D), generator=g, dtype=f32)
+    delta = torch.nn.functional.softplus(torch.randn((b, T, D), generator=g, dtype=f32))
+    A = -(torch.rand((D, N), generator=g, dtype=f32) * 1.5 + 0.5)
+    B = torch.randn((b, T, N), generator=g, dtype=f32)
+    C = torch.randn((b, T, N), generator=g, dtype=f32)
+    skip = torch.randn((D,), generator=g, dtype=f32)
+    out = {"u": u, "delta": delta, "A": A, "B": B, "C": C, "skip": skip}
+    if device is not None:
+        out = {k: v.to(device) for k, v in out.items()}
+    return out

@@ -1,0 +1,135 @@
+"""numpy fp64 restatement of the pages' chunked algorithm (TEST INFRASTRUCTURE ONLY).
+
+This is the algebra the GPU kernels are built on, written step by step in the pages' order so
+that the pin tests can check the sequential oracle (``oracle.ssd``) against it:
+
+- ``segsum``: the segsum.rs page (burn_mamba modules/misc/segsum.rs), ``segsum`` doc comment:
+  out[..., i, j] = cumsum(x)[i] - cumsum(x)[j] for i >= j, -inf above the diagonal, so that
+  exp(segsum) is the causal 1-semiseparable decay mask.
+- ``k1_chunk_cumsum`` .. ``k5_chunk_scan``: the serial.rs page (burn_mamba mamba3/ssd/serial.rs),
+  functions k1_ssd_chunk_cumsum, k2_ssd_bmm, k3_ssd_chunk_state, k4_ssd_state_passing,
+  k5_ssd_chunk_scan, on rank-fused tensors (fused index i = t*R + r, time-major).
+- ``rotate_pairs`` / cumulative angles: the scan.py page (steertts mamba3/scan.py),
+  cumulative_angles and rotate_by; the rotation is absorbed as B~ = R(-Phi_t) B, C~ = R(-Phi_t) C
+  and the final state is turned back by R(Phi_{T-1}) (module docstring, "THE TRICK").
+- Ragged T: zero padding with dA = 0 and x = 0 (moments.rs page, module header: pads are
+  identity decay and zero write, so the carried state passes through unchanged).
+
+It is deliberately unfused and unblocked: every intermediate of the pages is materialised.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+
+def segsum(x: np.ndarray) -> np.ndarray:
+    """[..., T] -> [..., T, T]; lower triangle = sum_{k=j+1..i} x_k, strict upper = -inf."""
+    T = x.shape[-1]
+    cs = np.cumsum(x, axis=-1)
+    out = cs[..., :, None] - cs[..., None, :]
+    upper = np.triu(np.ones((T, T), dtype=bool), k=1)
+    out = np.where(upper, -np.inf, out)
+    return out
+
+
+def rotate_pairs(v: np.ndarray, ang: np.ndarray) -> np.ndarray:
+    """Turn interleaved pairs (v[...,2k], v[...,2k+1]) of the last axis by +ang[...,k]."""
+    a, b = v[..., 0::2], v[..., 1::2]
+    c, s = np.cos(ang), np.sin(ang)
+    out = np.empty_like(v)
+    out[..., 0::2] = c * a - s * b
+    out[..., 1::2] = s * a + c * b
+    return out
+
+
+def k1_chunk_cumsum(da_bnlh: np.ndarray):
+    """K1: intra-chunk prefix sums [b,H,n,l] and the per-chunk totals [b,H,n]."""
+    cum = np.cumsum(np.transpose(da_bnlh, (0, 3, 1, 2)), axis=3)
+    return cum, cum[..., -1]
+
+
+def k2_bmm(c_bnLhn: np.ndarray, b_bnLhn: np.ndarray) -> np.ndarray:
+    """K2: CB[b,n,h,i,j] = sum_s C[i,s] B[j,s] on rank-fused tensors."""
+    return np.einsum("bnihs,bnjhs->bnhij", c_bnLhn, b_bnLhn)
+
+
+def k3_chunk_state(v_bnLhp, b_bnLhn, cum_fused_bhnL):
+    """K3: chunk-end state from zero: sum_i exp(cum_last - cum[i//R]) V[i,:]^T B[i,:] -> [b,n,h,p,s]."""
+    last = cum_fused_bhnL[..., -1:]
+    decay = np.exp(last - cum_fused_bhnL)                        # [b,h,n,L]
+    dv = v_bnLhp * np.transpose(decay, (0, 2, 3, 1))[..., None]  # [b,n,L,h,p]
+    return np.einsum("bnihp,bnihs->bnhps", dv, b_bnLhn)
+
+
+def k4_state_passing(states_bnhps, chunk_end_bhn, init_bhps):
+    """K4: sequential h <- exp(chunk_end[c]) h + S[c]; returns per-chunk input states and final."""
+    nch = states_bnhps.shape[1]
+    h = init_bhps.copy()
+    ins = []
+    for c in range(nch):
+        ins.append(h.copy())
+        h = np.exp(chunk_end_bhn[:, :, c])[:, :, None, None] * h + states_bnhps[:, c]
+    return np.stack(ins, axis=1), h
+
+
+def k5_chunk_scan(cum_fused_bhnL, da_bhnl, v_bnLhp, c_bnLhn, cb_bnhLL, hin_bnhps, R):
+    """K5: y = (L_mimo o CB) V + exp(cum[i//R]) C[i] h_in.
+
+    L_mimo is exp(segsum(dA)) of the unfused chunk, expanded so that
+    L[i, j] = exp(cum[i//R] - cum[j//R]) when i//R >= j//R and 0 otherwise.
+    """
+    b, n, L, H, P = v_bnLhp.shape
+    l = L // R
+    cum = np.transpose(cum_fused_bhnL, (0, 2, 1, 3))               # [b,n,h,L]
+    # off-diagonal ("blue") part: exp(cum_i) * C_i . h_in
+    blue = np.exp(cum)[..., None] * np.einsum("bnihs,bnhps->bnhip", c_bnLhn, hin_bnhps)
+    # diagonal ("orange") part
+    seg = segsum(np.transpose(da_bhnl, (0, 2, 1, 3)))             # [b,n,h,l,l]
+    seg_f = np.repeat(np.repeat(seg, R, axis=-2), R, axis=-1)      # [b,n,h,L,L]
+    orange = np.einsum("bnhij,bnjhp->bnhip", np.exp(seg_f) * cb_bnhLL, v_bnLhp)
+    y = blue + orange                                              # [b,n,h,L,p]
+    return np.transpose(y, (0, 1, 3, 2, 4)).reshape(b, n, l, R, H, P)
+
+
+def chunked_forward(x, dA, B, C, theta=None, init_state=None, chunk_len=64):
+    """K1..K5 on [b,T,R,H,P] inputs; returns (y [b,T,R,H,P], final [b,H,P,N])."""
+    x = np.asarray(x, np.float64)
+    dA = np.asarray(dA, np.float64)
+    B = np.asarray(B, np.float64)
+    C = np.asarray(C, np.float64)
+    b, T, R, H, P = x.shape
+    G, N = B.shape[3], B.shape[4]
+    hpg = H // G
+    # per-head B/C (expand groups)
+    Bh = np.repeat(B, hpg, axis=3)
+    Ch = np.repeat(C, hpg, axis=3)
+    phi = None
+    if theta is not None:
+        phi = np.cumsum(np.asarray(theta, np.float64), axis=1)     # [b,T,H,N/2]
+        Bh = rotate_pairs(Bh, -phi[:, :, None, :, :])
+        Ch = rotate_pairs(Ch, -phi[:, :, None, :, :])
+    init = np.zeros((b, H, P, N)) if init_state is None else np.asarray(init_state, np.float64)
+    if T == 0:
+        return np.zeros((b, 0, R, H, P)), init.copy()
+    l = int(chunk_len)
+    nch = -(-T // l)
+    pad = nch * l - T
+    if pad:
+        x = np.concatenate([x, np.zeros((b, pad, R, H, P))], axis=1)
+        dA = np.concatenate([dA, np.zeros((b, pad, H))], axis=1)
+        Bh = np.concatenate([Bh, np.zeros((b, pad, R, H, N))], axis=1)
+        Ch = np.concatenate([Ch, np.zeros((b, pad, R, H, N))], axis=1)
+    L = l * R
+    v = x.reshape(b, nch, L, H, P)
+    bf = Bh.reshape(b, nch, L, H, N)
+    cf = Ch.reshape(b, nch, L, H, N)
+    da_bnlh = dA.reshape(b, nch, l, H)
+    cum, chunk_end = k1_chunk_cumsum(da_bnlh)
+    cum_fused = np.repeat(cum, R, axis=3)                          # [b,h,n,L]
+    cb = k2_bmm(cf, bf)
+    states = k3_chunk_state(v, bf, cum_fused)
+    hin, final = k4_state_passing(states, chunk_end, init)
+    y = k5_chunk_scan(cum_fused, np.transpose(da_bnlh, (0, 3, 1, 2)), v, cf, cb, hin, R).reshape(b, nch * l, R, H, P)[:, :T]
+    if phi is not None:
+        final = rotate_pairs(final, phi[:, T - 1][:, :, None, :])
+    return y, final

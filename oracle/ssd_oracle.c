@@ -1,0 +1,282 @@
+/*
+ * Plain fp64 CPU oracle for the chunked SSD scan and the diagonal-A selective scan.
+ *
+ * TEST INFRASTRUCTURE ONLY.  This file is the slow, obviously-correct statement of what the
+ * GPU library computes.  Only the test suite, the smoke check and the benchmark's CPU-baseline
+ * leg load it.  It shares no code, header or constant with the CUDA library and includes
+ * nothing from it.
+ *
+ * What it computes (the plain definition; the chunked GPU method reaches the same result up to
+ * rounding order):
+ *
+ *   SSD recurrence, one independent problem per (batch b, head h):
+ *     h_{-1}      = init_state[b,h]                        (zeros when no init is given)
+ *     h_t         = exp(dA[b,t,h]) * R(theta_t) h_{t-1} + sum_r x[b,t,r,h,:] (outer) B[b,t,r,g,:]
+ *     y[b,t,r,h,p]= sum_n C[b,t,r,g,n] * h_t[p,n]
+ *     final[b,h]  = h_{T-1}
+ *   with g = h / (H/G) the B/C group of head h.
+ *   - The decay/write form is the recurrence that the serial.rs page (burn_mamba,
+ *     mamba3/ssd/serial.rs) decomposes into K1..K5: K3 sums the rank-fused writes V^T B with the
+ *     decay exp(cumA_last - cumA), K4 is h <- exp(da_chunk_end) h + s, and K5's MIMO mask
+ *     (i//R >= j//R) means y at step t sees all R writes of step t.  V ("x" here) is pre-scaled:
+ *     there is no dt factor, and no D-skip term ("No D skip is applied").
+ *   - R(theta) is the optional Mamba-3 data-dependent rotation (scan.py page, steertts
+ *     mamba3/scan.py, module docstring "THE TRICK" and rotate_by): it turns each interleaved
+ *     pair (h[2k], h[2k+1]) of the state axis by +theta[b,t,h,k]:
+ *         (a, b) -> (cos*a - sin*b, sin*a + cos*b).
+ *     The oracle applies this rotation to the state directly at every step (the rotated
+ *     recurrence itself), never the absorbed cumulative-angle form the GPU uses.
+ *
+ *   Selective scan (SSM Selective Scan page, problem statement), one problem per (b, d):
+ *     h_{-1}[n] = 0
+ *     h_t[n]    = exp(delta[b,t,d] * A[d,n]) * h_{t-1}[n] + delta[b,t,d] * B[b,t,n] * u[b,t,d]
+ *     y[b,t,d]  = sum_n C[b,t,n] * h_t[n] + skip[d] * u[b,t,d]
+ *
+ * All arithmetic is fp64; inputs arrive as fp64 arrays (the caller upcasts the exact values the
+ * GPU sees, e.g. bf16-rounded data).  Independent (b,h) or (b,d) problems are split across
+ * POSIX threads; each problem is evaluated sequentially in time, so the thread count does not
+ * change any result bit.
+ *
+ * `mutation` exists only so the test suite can show that its pins catch plausible mistakes; it
+ * is 0 in every real use.  Non-zero values plant one deliberate error (see oracle_ssd_ex).
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+typedef struct {
+  const double *x, *dA, *B, *C, *theta, *init;
+  double *y, *final_state;
+  int64_t batch, T, R, H, G, P, N;
+  int mutation;
+  int64_t nthreads;
+  int64_t tid;
+} ssd_job;
+
+/* Planted-mistake codes, used only by the oracle's own pin tests. */
+enum {
+  MUT_NONE = 0,
+  MUT_NO_DECAY = 1,        /* drops the exp(dA) factor                        */
+  MUT_DECAY_AFTER = 2,     /* applies the decay to the new write as well       */
+  MUT_SWAP_BC = 3,         /* reads B where C belongs and C where B belongs    */
+  MUT_RANK_LOCAL = 4,      /* y_{t,r} only sees the writes of ranks <= r       */
+  MUT_ROT_SIGN = 5,        /* rotates by -theta instead of +theta              */
+  MUT_GROUP_INDEX = 6,     /* maps head h to group h % G instead of h / (H/G)  */
+  MUT_SS_NO_SKIP = 7,      /* selective scan: drops the skip term              */
+  MUT_SS_DELTA_B = 8,      /* selective scan: forgets the delta factor on B    */
+};
+
+static void ssd_one(const ssd_job* j, int64_t b, int64_t hh, double* h) {
+  const int64_t T = j->T, R = j->R, H = j->H, G = j->G, P = j->P, N = j->N;
+  const int64_t heads_per_group = H / G;
+  const int64_t g = (j->mutation == MUT_GROUP_INDEX) ? (hh % G) : (hh / heads_per_group);
+  const double* Bsrc = (j->mutation == MUT_SWAP_BC) ? j->C : j->B;
+  const double* Csrc = (j->mutation == MUT_SWAP_BC) ? j->B : j->C;
+
+  if (j->init) {
+    memcpy(h, j->init + ((b * H + hh) * P) * N, sizeof(double) * P * N);
+  } else {
+    memset(h, 0, sizeof(double) * P * N);
+  }
+  for (int64_t t = 0; t < T; ++t) {
+    const double a = (j->mutation == MUT_NO_DECAY) ? 1.0 : exp(j->dA[(b * T + t) * H + hh]);
+    if (j->theta) {
+      const double* th = j->theta + ((b * T + t) * H + hh) * (N / 2);
+      for (int64_t k = 0; k < N / 2; ++k) {
+        const double ang = (j->mutation == MUT_ROT_SIGN) ? -th[k] : th[k];
+        const double c = cos(ang), s = sin(ang);
+        for (int64_t p = 0; p < P; ++p) {
+          double* hp = h + p * N;
+          const double e = hp[2 * k], o = hp[2 * k + 1];
+          hp[2 * k] = c * e - s * o;
+          hp[2 * k + 1] = s * e + c * o;
+        }
+      }
+    }
+    for (int64_t p = 0; p < P; ++p) {
+      for (int64_t n = 0; n < N; ++n) {
+        double w = 0.0;
+        for (int64_t r = 0; r < R; ++r) {
+          const double xv = j->x[(((b * T + t) * R + r) * H + hh) * P + p];
+          const double bv = Bsrc[(((b * T + t) * R + r) * G + g) * N + n];
+          w += xv * bv;
+        }
+        if (j->mutation == MUT_DECAY_AFTER) {
+          h[p * N + n] = a * (h[p * N + n] + w);
+        } else {
+          h[p * N + n] = a * h[p * N + n] + w;
+        }
+      }
+    }
+    for (int64_t r = 0; r < R; ++r) {
+      const double* cv = Csrc + (((b * T + t) * R + r) * G + g) * N;
+      for (int64_t p = 0; p < P; ++p) {
+        double acc = 0.0;
+        if (j->mutation == MUT_RANK_LOCAL) {
+          /* Recompute the state as if only ranks 0..r had written at step t. */
+          for (int64_t n = 0; n < N; ++n) {
+            double hv = h[p * N + n];
+            for (int64_t r2 = r + 1; r2 < R; ++r2) {
+              hv -= j->x[(((b * T + t) * R + r2) * H + hh) * P + p] *
+                    Bsrc[(((b * T + t) * R + r2) * G + g) * N + n];
+            }
+            acc += cv[n] * hv;
+          }
+        } else {
+          for (int64_t n = 0; n < N; ++n) acc += cv[n] * h[p * N + n];
+        }
+        j->y[(((b * T + t) * R + r) * H + hh) * P + p] = acc;
+      }
+    }
+  }
+  if (j->final_state) {
+    memcpy(j->final_state + ((b * H + hh) * P) * N, h, sizeof(double) * P * N);
+  }
+}
+
+static void* ssd_worker(void* arg) {
+  const ssd_job* j = (const ssd_job*)arg;
+  double* h = (double*)malloc(sizeof(double) * j->P * j->N);
+  if (!h) return (void*)1;
+  for (int64_t idx = j->tid; idx < j->batch * j->H; idx += j->nthreads) {
+    ssd_one(j, idx / j->H, idx % j->H, h);
+  }
+  free(h);
+  return NULL;
+}
+
+static int64_t clamp_threads(int64_t nthreads, int64_t work) {
+  if (nthreads < 1) nthreads = 1;
+  if (nthreads > work) nthreads = work;
+  if (nthreads > 512) nthreads = 512;
+  return nthreads < 1 ? 1 : nthreads;
+}
+
+/* Returns 0 on success, a negative value on invalid arguments or allocation failure. */
+int oracle_ssd_ex(const double* x, const double* dA, const double* B, const double* C,
+                  const double* theta, const double* init_state, double* y, double* final_state,
+                  int64_t batch, int64_t T, int64_t R, int64_t H, int64_t G, int64_t P, int64_t N,
+                  int64_t nthreads, int mutation) {
+  if (!x || !dA || !B || !C || !y) return -1;
+  if (batch < 0 || T < 0 || R < 1 || H < 1 || G < 1 || P < 1 || N < 1) return -2;
+  if (H % G != 0) return -3;
+  if (theta && (N % 2 != 0)) return -4;
+  if (batch == 0 || T == 0) {
+    if (final_state) {
+      for (int64_t i = 0; i < batch * H * P * N; ++i)
+        final_state[i] = init_state ? init_state[i] : 0.0;
+    }
+    return 0;
+  }
+  const int64_t nt = clamp_threads(nthreads, batch * H);
+  ssd_job* jobs = (ssd_job*)calloc((size_t)nt, sizeof(ssd_job));
+  pthread_t* th = (pthread_t*)calloc((size_t)nt, sizeof(pthread_t));
+  if (!jobs || !th) {
+    free(jobs);
+    free(th);
+    return -5;
+  }
+  int rc = 0;
+  for (int64_t i = 0; i < nt; ++i) {
+    ssd_job j = {x, dA, B, C, theta, init_state, y, final_state, batch, T, R, H, G, P, N,
+                 mutation, nt, i};
+    jobs[i] = j;
+  }
+  for (int64_t i = 1; i < nt; ++i) pthread_create(&th[i], NULL, ssd_worker, &jobs[i]);
+  if (ssd_worker(&jobs[0]) != NULL) rc = -5;
+  for (int64_t i = 1; i < nt; ++i) {
+    void* ret = NULL;
+    pthread_join(th[i], &ret);
+    if (ret != NULL) rc = -5;
+  }
+  free(jobs);
+  free(th);
+  return rc;
+}
+
+int oracle_ssd(const double* x, const double* dA, const double* B, const double* C,
+               const double* theta, const double* init_state, double* y, double* final_state,
+               int64_t batch, int64_t T, int64_t R, int64_t H, int64_t G, int64_t P, int64_t N,
+               int64_t nthreads) {
+  return oracle_ssd_ex(x, dA, B, C, theta, init_state, y, final_state, batch, T, R, H, G, P, N,
+                       nthreads, MUT_NONE);
+}
+
+/* ---------------------------------------------------------------------------------------- */
+/* Selective scan                                                                            */
+/* ---------------------------------------------------------------------------------------- */
+
+typedef struct {
+  const double *u, *delta, *A, *B, *C, *skip;
+  double* y;
+  int64_t batch, T, D, N;
+  int mutation;
+  int64_t nthreads, tid;
+} ss_job;
+
+static void* ss_worker(void* arg) {
+  const ss_job* j = (const ss_job*)arg;
+  const int64_t T = j->T, D = j->D, N = j->N;
+  double* h = (double*)malloc(sizeof(double) * N);
+  if (!h) return (void*)1;
+  for (int64_t idx = j->tid; idx < j->batch * D; idx += j->nthreads) {
+    const int64_t b = idx / D, d = idx % D;
+    for (int64_t n = 0; n < N; ++n) h[n] = 0.0;
+    const double sk = (j->skip && j->mutation != MUT_SS_NO_SKIP) ? j->skip[d] : 0.0;
+    for (int64_t t = 0; t < T; ++t) {
+      const double dt = j->delta[(b * T + t) * D + d];
+      const double uv = j->u[(b * T + t) * D + d];
+      double acc = 0.0;
+      for (int64_t n = 0; n < N; ++n) {
+        const double abar = exp(dt * j->A[d * N + n]);
+        const double bbar =
+            (j->mutation == MUT_SS_DELTA_B) ? j->B[(b * T + t) * N + n] : dt * j->B[(b * T + t) * N + n];
+        h[n] = abar * h[n] + bbar * uv;
+        acc += j->C[(b * T + t) * N + n] * h[n];
+      }
+      j->y[(b * T + t) * D + d] = acc + sk * uv;
+    }
+  }
+  free(h);
+  return NULL;
+}
+
+int oracle_selective_scan_ex(const double* u, const double* delta, const double* A,
+                             const double* B, const double* C, const double* skip, double* y,
+                             int64_t batch, int64_t T, int64_t D, int64_t N, int64_t nthreads,
+                             int mutation) {
+  if (!u || !delta || !A || !B || !C || !y) return -1;
+  if (batch < 0 || T < 0 || D < 1 || N < 1) return -2;
+  if (batch == 0 || T == 0) return 0;
+  const int64_t nt = clamp_threads(nthreads, batch * D);
+  ss_job* jobs = (ss_job*)calloc((size_t)nt, sizeof(ss_job));
+  pthread_t* th = (pthread_t*)calloc((size_t)nt, sizeof(pthread_t));
+  if (!jobs || !th) {
+    free(jobs);
+    free(th);
+    return -5;
+  }
+  int rc = 0;
+  for (int64_t i = 0; i < nt; ++i) {
+    ss_job j = {u, delta, A, B, C, skip, y, batch, T, D, N, mutation, nt, i};
+    jobs[i] = j;
+  }
+  for (int64_t i = 1; i < nt; ++i) pthread_create(&th[i], NULL, ss_worker, &jobs[i]);
+  if (ss_worker(&jobs[0]) != NULL) rc = -5;
+  for (int64_t i = 1; i < nt; ++i) {
+    void* ret = NULL;
+    pthread_join(th[i], &ret);
+    if (ret != NULL) rc = -5;
+  }
+  free(jobs);
+  free(th);
+  return rc;
+}
+
+int oracle_selective_scan(const double* u, const double* delta, const double* A, const double* B,
+                          const double* C, const double* skip, double* y, int64_t batch,
+                          int64_t T, int64_t D, int64_t N, int64_t nthreads) {
+  return oracle_selective_scan_ex(u, delta, A, B, C, skip, y, batch, T, D, N, nthreads, MUT_NONE);
+}

@@ -1,0 +1,254 @@
+"""Checks that tie the fp64 oracle to facts fixed by the pages and by plain mathematics.
+
+Each ``pin_*`` function runs the oracle (optionally with one planted mistake, ``mutation``) on
+small seeded inputs and returns a list of ``(check name, error, tolerance)``.  With
+``mutation=0`` every error must be within tolerance; with each planted mistake at least one
+check must fail, which shows that the pins would notice that kind of error.
+
+None of these checks re-types the oracle's own loop: they compare it with printed values, closed
+forms, a differently organised computation (the pages' chunked algebra in
+``oracle.chunked_ref``), superposition identities, or exact invariants.
+"""
+from __future__ import annotations
+
+import math
+import os
+
+import numpy as np
+
+import oracle
+from oracle import chunked_ref
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def _rng(seed):
+    return np.random.default_rng(seed)
+
+
+def _problem(seed, b, T, R, H, G, P, N, *, theta=False, init=False, decay=(0.0, 0.5)):
+    r = _rng(seed)
+    x = r.standard_normal((b, T, R, H, P))
+    dA = -r.uniform(decay[0], decay[1], (b, T, H))
+    B = r.standard_normal((b, T, R, G, N))
+    C = r.standard_normal((b, T, R, G, N))
+    th = r.uniform(-0.4, 0.4, (b, T, H, N // 2)) if theta else None
+    h0 = r.standard_normal((b, H, P, N)) if init else None
+    return x, dA, B, C, th, h0
+
+
+def _maxerr(a, b):
+    a = np.asarray(a, np.float64)
+    b = np.asarray(b, np.float64)
+    if a.size == 0 and b.size == 0:
+        return 0.0
+    return float(np.max(np.abs(a - b)))
+
+
+def load_golden(name):
+    vals = {}
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            k, v = line.split(":", 1)
+            vals[k.strip()] = [float(t) for t in v.split()]
+    return vals
+
+
+# --------------------------------------------------------------------------------------------
+# Selective scan
+# --------------------------------------------------------------------------------------------
+
+def pin_worked_example(mutation=0):
+    """The SSM Selective Scan page's worked example (section 示例), to its 3 printed decimals."""
+    g = load_golden("selective_scan_worked_example.txt")
+    b, T, D, N = (int(g[k][0]) for k in ("batch", "seq_len", "d_model", "d_state"))
+    u = np.array(g["u"]).reshape(b, T, D)
+    delta = np.array(g["delta"]).reshape(b, T, D)
+    A = np.array(g["A"]).reshape(D, N)
+    B = np.array(g["B"]).reshape(b, T, N)
+    C = np.array(g["C"]).reshape(b, T, N)
+    skip = np.array(g["skip"])
+    tol = g["tolerance"][0] + 1e-9
+    y = oracle.selective_scan(u, delta, A, B, C, skip, mutation=mutation)
+    # A_bar is printed for delta = 1: exp(1 * A).  A single step from h = e_n isolates it.
+    abar = []
+    for d in range(D):
+        for n in range(N):
+            uu = np.zeros((1, 2, D)); uu[0, 0, d] = 1.0
+            dd = np.ones((1, 2, D))
+            BB = np.zeros((1, 2, N)); BB[0, 0, n] = 1.0
+            CC = np.zeros((1, 2, N)); CC[0, 1, n] = 1.0
+            yy = oracle.selective_scan(uu, dd, A, BB, CC, None, mutation=mutation)
+            abar.append(yy[0, 1, d])
+    return [
+        ("worked_example_y", _maxerr(y.reshape(-1), g["y"]), tol),
+        ("worked_example_A_bar", _maxerr(abar, g["A_bar"]), tol),
+    ]
+
+
+def pin_selective_scan_superposition(mutation=0):
+    """A diagonal-A selective scan is N independent scalar recurrences per channel, each of them
+    an SSD problem with one state (heads = channels, P = N = 1, x = delta*u, dA = delta*A[:,n]),
+    plus the skip term: y = sum_n SSD_n + skip*u."""
+    r = _rng(11)
+    b, T, D, N = 2, 23, 5, 4
+    u = r.standard_normal((b, T, D))
+    delta = np.log1p(np.exp(r.standard_normal((b, T, D))))
+    A = -r.uniform(0.5, 2.0, (D, N))
+    B = r.standard_normal((b, T, N))
+    C = r.standard_normal((b, T, N))
+    skip = r.standard_normal((D,))
+    y = oracle.selective_scan(u, delta, A, B, C, skip, mutation=mutation)
+    ref = skip[None, None, :] * u
+    for n in range(N):
+        x = (delta * u)[:, :, None, :, None]                     # [b,T,1,D,1]
+        dA = delta * A[None, None, :, n]                          # [b,T,D]
+        Bn = np.broadcast_to(B[:, :, None, None, n:n + 1], (b, T, 1, 1, 1))
+        Cn = np.broadcast_to(C[:, :, None, None, n:n + 1], (b, T, 1, 1, 1))
+        yn, _ = oracle.ssd(x, dA, Bn, Cn)
+        ref = ref + yn[:, :, 0, :, 0]
+    return [("selective_scan_vs_scalar_ssd_sum", _maxerr(y, ref), 1e-11)]
+
+
+# --------------------------------------------------------------------------------------------
+# SSD
+# --------------------------------------------------------------------------------------------
+
+def pin_closed_form(mutation=0):
+    """scan.py page, module docstring "THE SCAN": g_t = A_t * (g_-1 + sum_{s<=t} w_s / A_s) with
+    A_t = prod_{r<=t} alpha_r, evaluated by brute force on tiny inputs (alpha in [0.5, 1))."""
+    out = []
+    for seed, T in ((1, 1), (2, 7), (3, 16)):
+        r = _rng(seed)
+        alpha = r.uniform(0.5, 1.0, T)
+        w = r.standard_normal(T)
+        g0 = r.standard_normal()
+        ref = []
+        for t in range(T):
+            At = math.prod(alpha[: t + 1])
+            ref.append(At * (g0 + sum(w[s] / math.prod(alpha[: s + 1]) for s in range(t + 1))))
+        x = w.reshape(1, T, 1, 1, 1)
+        dA = np.log(alpha).reshape(1, T, 1)
+        one = np.ones((1, T, 1, 1, 1))
+        y, fin = oracle.ssd(x, dA, one, one, init_state=np.full((1, 1, 1, 1), g0),
+                            mutation=mutation)
+        out.append((f"closed_form_T{T}", _maxerr(y.reshape(-1), ref), 1e-12))
+        out.append((f"closed_form_final_T{T}", _maxerr(fin.reshape(-1), ref[-1:]), 1e-12))
+    return out
+
+
+def pin_special_cases(mutation=0):
+    """Cases that reduce to textbook forms: no decay (dA = 0) with one state and one channel is a
+    prefix sum y_t = C_t * sum_{s<=t} x_s B_s; a single step is y = C . (exp(dA) h0 + x (x) B)."""
+    r = _rng(5)
+    T = 19
+    x, B, C = r.standard_normal(T), r.standard_normal(T), r.standard_normal(T)
+    y, _ = oracle.ssd(x.reshape(1, T, 1, 1, 1), np.zeros((1, T, 1)), B.reshape(1, T, 1, 1, 1),
+                      C.reshape(1, T, 1, 1, 1), mutation=mutation)
+    res = [("prefix_sum", _maxerr(y.reshape(-1), C * np.cumsum(x * B)), 1e-12)]
+    P, N = 3, 4
+    x1 = r.standard_normal((1, 1, 1, 1, P))
+    B1 = r.standard_normal((1, 1, 1, 1, N))
+    C1 = r.standard_normal((1, 1, 1, 1, N))
+    dA1 = np.array([[[-0.3]]])
+    h0 = r.standard_normal((1, 1, P, N))
+    y1, f1 = oracle.ssd(x1, dA1, B1, C1, init_state=h0, mutation=mutation)
+    h1 = math.exp(-0.3) * h0[0, 0] + np.outer(x1.reshape(P), B1.reshape(N))
+    res.append(("single_step_y", _maxerr(y1.reshape(P), h1 @ C1.reshape(N)), 1e-13))
+    res.append(("single_step_final", _maxerr(f1[0, 0], h1), 1e-13))
+    return res
+
+
+def pin_chunk_invariance(mutation=0):
+    """The serial.rs page's K1..K5 decomposition (restated in oracle.chunked_ref) computed at
+    chunk lengths 1, 8, 16, 64 and T must equal the sequential recurrence: chunking is exact.
+    Same pattern as the scan.py page's verify() (chunks 8/16/64, a ragged length 37)."""
+    res = []
+    cases = [
+        dict(seed=21, b=2, T=64, R=1, H=2, G=2, P=4, N=6, init=False),
+        dict(seed=22, b=1, T=37, R=1, H=4, G=2, P=3, N=4, init=True),      # ragged, groups
+        dict(seed=23, b=2, T=40, R=3, H=2, G=1, P=3, N=4, init=True),      # MIMO, shared B/C
+    ]
+    for c in cases:
+        x, dA, B, C, th, h0 = _problem(c["seed"], c["b"], c["T"], c["R"], c["H"], c["G"], c["P"],
+                                       c["N"], init=c["init"])
+        y, fin = oracle.ssd(x, dA, B, C, init_state=h0, mutation=mutation)
+        for l in (1, 8, 16, 64, c["T"]):
+            y2, f2 = chunked_ref.chunked_forward(x, dA, B, C, None, h0, l)
+            res.append((f"chunk{l}_seed{c['seed']}_y", _maxerr(y, y2), 1e-10))
+            res.append((f"chunk{l}_seed{c['seed']}_final", _maxerr(fin, f2), 1e-10))
+    return res
+
+
+def pin_rotation(mutation=0):
+    """The scan.py page's rotation identity (module docstring "THE TRICK"): the rotated
+    recurrence equals the plain scan with B~ = R(-Phi_t) B, C~ = R(-Phi_t) C and the state turned
+    back by R(Phi_{T-1}).  Plus two exact facts: theta = 0 changes nothing, and with no writes
+    and no decay the state is the initial state turned by the summed angle (rotate_by's
+    convention: (a, b) -> (c a - s b, s a + c b))."""
+    res = []
+    x, dA, B, C, th, h0 = _problem(31, 2, 45, 2, 2, 1, 3, 6, theta=True, init=True)
+    y, fin = oracle.ssd(x, dA, B, C, th, h0, mutation=mutation)
+    for l in (1, 16, 45):
+        y2, f2 = chunked_ref.chunked_forward(x, dA, B, C, th, h0, l)
+        res.append((f"rotation_absorbed_chunk{l}_y", _maxerr(y, y2), 1e-10))
+        res.append((f"rotation_absorbed_chunk{l}_final", _maxerr(fin, f2), 1e-10))
+    y0, f0 = oracle.ssd(x, dA, B, C, np.zeros_like(th), h0, mutation=mutation)
+    yn, fn = oracle.ssd(x, dA, B, C, None, h0, mutation=mutation)
+    res.append(("theta_zero_is_identity", max(_maxerr(y0, yn), _maxerr(f0, fn)), 0.0))
+    T = 9
+    r = _rng(32)
+    ang = r.uniform(-0.5, 0.5, (1, T, 1, 1))
+    h0 = np.array([1.0, 0.0]).reshape(1, 1, 1, 2)
+    _, f = oracle.ssd(np.zeros((1, T, 1, 1, 1)), np.zeros((1, T, 1)), np.zeros((1, T, 1, 1, 2)),
+                      np.zeros((1, T, 1, 1, 2)), ang, h0, mutation=mutation)
+    tot = float(ang.sum())
+    res.append(("pure_rotation", _maxerr(f.reshape(2), [math.cos(tot), math.sin(tot)]), 1e-13))
+    return res
+
+
+def pin_mimo_superposition(mutation=0):
+    """MIMO: every rank's write of step t lands before y_{t,r} is read (the serial.rs page's K5
+    mask i//R >= j//R).  By linearity the rank-R output is the sum over writing ranks r' of
+    rank-1 runs: y[:, :, r] = sum_{r'} SSD(x_{r'}, B_{r'}, C_r), the initial state counted once."""
+    b, T, R, H, G, P, N = 2, 21, 3, 2, 2, 3, 4
+    x, dA, B, C, th, h0 = _problem(41, b, T, R, H, G, P, N, theta=True, init=True)
+    y, fin = oracle.ssd(x, dA, B, C, th, h0, mutation=mutation)
+    yref = np.zeros_like(y)
+    fref = np.zeros_like(fin)
+    for rp in range(R):
+        for r in range(R):
+            ys, fs = oracle.ssd(x[:, :, rp:rp + 1], dA, B[:, :, rp:rp + 1], C[:, :, r:r + 1], th,
+                                h0 if rp == 0 else None)
+            yref[:, :, r] += ys[:, :, 0]
+            if r == 0:
+                fref += fs
+    return [("mimo_superposition_y", _maxerr(y, yref), 1e-11),
+            ("mimo_superposition_final", _maxerr(fin, fref), 1e-11)]
+
+
+def pin_causality_and_continuation(mutation=0):
+    """Causality (scan.py page, verify(): appended large noise must not change earlier outputs)
+    and continuation (the serial.rs page's initial_state / final_state hand-off): two calls
+    chained through the final state equal one call."""
+    b, T, R, H, G, P, N = 2, 40, 2, 2, 1, 3, 4
+    x, dA, B, C, th, h0 = _problem(51, b, T + 9, R, H, G, P, N, theta=True, init=True)
+    x2 = x.copy()
+    x2[:, T:] *= 50.0
+    ya, _ = oracle.ssd(x[:, :T], dA[:, :T], B[:, :T], C[:, :T], th[:, :T], h0, mutation=mutation)
+    yb, _ = oracle.ssd(x2, dA, B, C, th, h0, mutation=mutation)
+    res = [("causality", _maxerr(ya, yb[:, :T]), 0.0)]
+    yf, ff = oracle.ssd(x, dA, B, C, th, h0, mutation=mutation)
+    y1, f1 = oracle.ssd(x[:, :T], dA[:, :T], B[:, :T], C[:, :T], th[:, :T], h0, mutation=mutation)
+    y2, f2 = oracle.ssd(x[:, T:], dA[:, T:], B[:, T:], C[:, T:], th[:, T:], f1, mutation=mutation)
+    res.append(("continuation_y", _maxerr(yf, np.concatenate([y1, y2], axis=1)), 1e-12))
+    res.append(("continuation_final", _maxerr(ff, f2), 1e-12))
+    return res
+
+
+SSD_PINS = [pin_closed_form, pin_special_cases, pin_chunk_invariance, pin_rotation,
+            pin_mimo_superposition, pin_causality_and_continuation]
+SS_PINS = [pin_worked_example, pin_selective_scan_superposition]
