@@ -1,0 +1,472 @@
+#!/usr/bin/env python3
+"""Benchmark of the chunked SSD forward scan on GB300.
+
+One step = one ssd_chunked_forward call (the whole K1..K5 path) over one batch of the
+Mamba-2-shape SISO workload (batch 4, T 4096, 32 heads, P 64, N 128, chunk 256, bf16 x/B/C,
+B/C shared by all heads), inputs already resident in HBM.  Prints ONE JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+Under torchrun (N > 1) every rank runs an independent replica on its own GPU (the problems are
+independent; there is no collective on the data path); the time is the max over ranks and the
+value counts the tokens of all ranks (weak scaling).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+METRIC = "SSD forward tokens/s and % of roofline (HBM GB/s / tensor-pipe) at 1 GB300"
+L2_FLUSH_BYTES = 256 << 20
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+# dram__bytes_read.sum + dram__bytes_write.sum per launch of the dominant kernel, from the ncu
+# capture summarised under profiles/ (None until captured for the current kernel).
+NCU_TRAFFIC_BYTES = {}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="mamba2_siso_bf16")
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-clocks", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", str(rank)))
+    return rank, world, local
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
+
+
+def workload(name):
+    from chunked_ssd_scan_gb300 import workloads as wl
+    for c in wl.SSD_CONFIGS:
+        if c.name == name:
+            return c
+    if name == wl.SELECTIVE_SCAN_F32.name:
+        return wl.SELECTIVE_SCAN_F32
+    raise SystemExit(f"unknown workload {name}")
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples taken while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.t = threading.Thread(target=self._read, daemon=True)
+        self.t.start()
+        time.sleep(0.3)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        if self.t:
+            self.t.join(timeout=2)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+def timed_steps(fn, steps, warmup, stream, flush):
+    """Warm up, then time each step with CUDA events on `stream`, flushing L2 between steps."""
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(steps):
+        flush.fill_(1)
+        s = torch.cuda.Event(enable_timing=True)
+        e = torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        fn()
+        e.record(stream)
+        times.append((s, e))
+    torch.cuda.synchronize()
+    return [s.elapsed_time(e) for s, e in times]
+
+
+def run_ours(args, rank, world, local):
+    import chunked_ssd_scan_gb300 as pkg
+    from chunked_ssd_scan_gb300 import workloads as wl
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    cfg = workload(args.workload)
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    is_ss = isinstance(cfg, wl.SelectiveScanConfig)
+
+    if is_ss:
+        host = wl.make_selective_scan_inputs(cfg, seed=0)
+        d = {k: v.to(dev) for k, v in host.items()}
+        y = torch.empty_like(d["u"])
+        ws = torch.empty(pkg.selective_scan_workspace_bytes(cfg.batch, cfg.seqlen, cfg.d_model,
+                                                            cfg.d_state), dtype=torch.uint8,
+                         device=dev)
+        fn = lambda: pkg.selective_scan_forward(d["u"], d["delta"], d["A"], d["B"], d["C"],
+                                                d["skip"], y=y, workspace=ws)
+        launches_per_call = 3
+        variant = "selective_scan"
+        dtype = "f32"
+        io_bytes = cfg.io_bytes()
+        flops = 0
+    else:
+        host = wl.make_ssd_inputs(cfg, seed=0)
+        d = {k: (v.to(dev) if v is not None else None) for k, v in host.items()}
+        y = torch.empty_like(d["x"])
+        fin = torch.empty((cfg.batch, cfg.nheads, cfg.headdim, cfg.dstate), dtype=torch.float32,
+                          device=dev)
+        shape = pkg.shape_of(d["x"], d["B"], cfg.chunk_len, cfg.theta)
+        ws = torch.empty(pkg.ssd_chunked_workspace_bytes(shape), dtype=torch.uint8, device=dev)
+        fn = lambda: pkg.ssd_chunked_forward(d["x"], d["dA"], d["B"], d["C"],
+                                             chunk_len=cfg.chunk_len, theta=d["theta"],
+                                             init_state=d["init_state"], y=y, final_state=fin,
+                                             workspace=ws)
+        variant = pkg.ssd_chunked_variant(shape)
+        launches_per_call = {"generic": 3 + (2 if cfg.theta else 0)}.get(variant, 1)
+        dtype = cfg.dtype
+        io_bytes = cfg.io_bytes()
+        flops = cfg.causal_flops()
+
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = ClockSampler(local) if (rank == 0 and not args.no_clocks) else None
+    if clocks:
+        clocks.start()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    step_ms = timed_steps(fn, args.steps, args.warmup, stream, flush)
+    if world > 1:
+        torch.distributed.barrier()
+    clk = clocks.stop() if clocks else None
+    ms = sum(step_ms) / len(step_ms)
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+
+    tokens = cfg.tokens * world
+    hbm, tf, peak_src = measured_peaks()
+    achieved = io_bytes / (ms * 1e-3) / 1e9
+    roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
+            "frac": round(achieved / hbm, 4), "traffic": NCU_TRAFFIC_BYTES.get(variant),
+            "peak_source": peak_src, "kernel": f"ssd_chunked_forward[{variant}]",
+            "algorithmic_bytes_per_launch": io_bytes}
+    if flops:
+        roof["tensor_tflops"] = round(flops / (ms * 1e-3) / 1e12, 2)
+        roof["tensor_frac_of_bf16_peak"] = round(flops / (ms * 1e-3) / 1e12 / tf, 4)
+        t_roof = max(io_bytes / (hbm * 1e9), flops / (tf * 1e12))
+        roof["roofline_frac"] = round(t_roof / (ms * 1e-3), 4)
+
+    out = {
+        "metric": METRIC if not is_ss else "selective scan tokens/s at 1 GB300",
+        "value": round(tokens / (ms * 1e-3), 1),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": dtype,
+        "data": "synthetic (seeded; distributions of the workload definition)",
+        "config": config_dict(cfg, is_ss),
+        "roofline": roof,
+        "gpu_launches": launches_per_call * args.steps,
+        "variant": variant,
+        "step_ms_min": round(min(step_ms), 5),
+        "step_ms_median": round(statistics.median(step_ms), 5),
+    }
+    if clk:
+        out["clocks"] = clk
+    if not args.no_e2e:
+        try:
+            out["e2e"] = e2e_measure(args, cfg, is_ss, host, dev, stream)
+        except Exception as ex:  # pragma: no cover
+            out["e2e"] = {"error": repr(ex)}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        try:
+            out["cpu_baseline"] = cpu_baseline(cfg, is_ss, host)
+        except Exception as ex:  # pragma: no cover
+            out["cpu_baseline"] = {"error": repr(ex)}
+    return out
+
+
+def config_dict(cfg, is_ss):
+    if is_ss:
+        c = {"workload": cfg.name, "batch": cfg.batch, "seq_len": cfg.seqlen,
+             "d_model": cfg.d_model, "d_state": cfg.d_state}
+    else:
+        c = {"workload": cfg.name, "batch": cfg.batch, "seq_len": cfg.seqlen,
+             "nheads": cfg.nheads, "headdim": cfg.headdim, "dstate": cfg.dstate,
+             "chunk_len": cfg.chunk_len, "mimo_rank": cfg.mimo_rank, "ngroups": cfg.ngroups,
+             "io_dtype": cfg.dtype, "theta": cfg.theta}
+    c["l2"] = "flushed between timed steps (256 MiB write, outside the timed events)"
+    c["cuda_graph"] = False
+    return c
+
+
+def e2e_measure(args, cfg, is_ss, host, dev, stream):
+    """Same metric through the public API with pinned host buffers: every step copies the
+    step's inputs host->device, runs the call, and reads the outputs back device->host."""
+    import chunked_ssd_scan_gb300 as pkg
+
+    pin = {k: (v.pin_memory() if v is not None else None) for k, v in host.items()}
+    dbuf = {k: (torch.empty_like(v, device=dev) if v is not None else None)
+            for k, v in host.items()}
+    if is_ss:
+        y = torch.empty_like(dbuf["u"])
+        y_h = torch.empty_like(pin["u"]).pin_memory()
+        outs = [(y, y_h)]
+
+        def call():
+            pkg.selective_scan_forward(dbuf["u"], dbuf["delta"], dbuf["A"], dbuf["B"],
+                                       dbuf["C"], dbuf["skip"], y=y)
+    else:
+        y = torch.empty_like(dbuf["x"])
+        fin = torch.empty((cfg.batch, cfg.nheads, cfg.headdim, cfg.dstate),
+                          dtype=torch.float32, device=dev)
+        outs = [(y, torch.empty(y.shape, dtype=y.dtype).pin_memory()),
+                (fin, torch.empty(fin.shape, dtype=fin.dtype).pin_memory())]
+        shape = pkg.shape_of(dbuf["x"], dbuf["B"], cfg.chunk_len, cfg.theta)
+        ws = torch.empty(pkg.ssd_chunked_workspace_bytes(shape), dtype=torch.uint8, device=dev)
+
+        def call():
+            pkg.ssd_chunked_forward(dbuf["x"], dbuf["dA"], dbuf["B"], dbuf["C"],
+                                    chunk_len=cfg.chunk_len, theta=dbuf["theta"],
+                                    init_state=dbuf["init_state"], y=y, final_state=fin,
+                                    workspace=ws)
+
+    h2d = sum(v.numel() * v.element_size() for v in pin.values() if v is not None)
+    d2h = sum(o.numel() * o.element_size() for o, _ in outs)
+
+    def step():
+        for k, v in pin.items():
+            if v is not None:
+                dbuf[k].copy_(v, non_blocking=True)
+        call()
+        for o, oh in outs:
+            oh.copy_(o, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    s = torch.cuda.Event(enable_timing=True)
+    e = torch.cuda.Event(enable_timing=True)
+    n = max(1, min(args.steps, 10))
+    s.record(stream)
+    for _ in range(n):
+        step()
+    e.record(stream)
+    torch.cuda.synchronize()
+    ms = s.elapsed_time(e) / n
+    return {"value": round(cfg.tokens / (ms * 1e-3), 1), "unit": "tokens/s",
+            "ms_per_step": round(ms, 4), "h2d_bytes_per_step": int(h2d),
+            "d2h_bytes_per_step": int(d2h), "steps": n}
+
+
+def _ssd_sample(cfg, host, heads, batches=1):
+    """Batches 0..batches-1, heads 0..heads-1 of the workload as fp64 arrays (independent
+    (batch, head) problems; a sub-problem of the workload with the same per-problem size)."""
+    import numpy as np
+
+    hpg = cfg.nheads // cfg.ngroups
+    if cfg.ngroups > 1 and hpg > 1:
+        heads = max(hpg, heads // hpg * hpg)
+    groups = 1 if cfg.ngroups == 1 else -(-heads // hpg)
+    f = lambda v: None if v is None else v.to(torch.float64).numpy()
+    a = {k: f(v) for k, v in host.items()}
+    nb = batches
+    sub = {
+        "x": a["x"][:nb, :, :, :heads], "dA": a["dA"][:nb, :, :heads],
+        "B": a["B"][:nb, :, :, :groups], "C": a["C"][:nb, :, :, :groups],
+        "theta": None if a["theta"] is None else a["theta"][:nb, :, :heads],
+        "init_state": None if a["init_state"] is None else a["init_state"][:nb, :heads],
+    }
+    sub = {k: (None if v is None else np.ascontiguousarray(v)) for k, v in sub.items()}
+    return sub, heads
+
+
+def _time_oracle_ssd(sub, nthr):
+    import oracle
+
+    t0 = time.perf_counter()
+    oracle.ssd(sub["x"], sub["dA"], sub["B"], sub["C"], sub["theta"], sub["init_state"],
+               nthreads=nthr)
+    return time.perf_counter() - t0
+
+
+def _time_oracle_ss(cfg, host, nthr, channels):
+    import oracle
+
+    f = lambda v: v.to(torch.float64).numpy()
+    u, dl = f(host["u"])[0:1, :, :channels], f(host["delta"])[0:1, :, :channels]
+    A, sk = f(host["A"])[:channels], f(host["skip"])[:channels]
+    B, C = f(host["B"])[0:1], f(host["C"])[0:1]
+    import numpy as np
+    u, dl, A, sk = (np.ascontiguousarray(v) for v in (u, dl, A, sk))
+    t0 = time.perf_counter()
+    oracle.selective_scan(u, dl, A, B, C, sk, nthreads=nthr)
+    return time.perf_counter() - t0
+
+
+def oracle_sampler(cfg, is_ss, host, target_s):
+    """Returns (step callable -> seconds, sampled fraction of the workload, cores, description):
+    the oracle as it stands over whole independent problems of batch 0, sized to ~target_s."""
+    import oracle
+
+    nthr = oracle.default_threads()
+    if is_ss:
+        D = cfg.d_model
+        t1 = _time_oracle_ss(cfg, host, nthr, min(D, 64))
+        per_ch = t1 / min(D, 64)
+        ch = int(max(1, min(D, target_s / max(per_ch, 1e-9))))
+        frac = ch / (D * cfg.batch)
+        desc = f"batch 0, channels 0..{ch - 1} of {D}, full T (independent problems)"
+        return (lambda: _time_oracle_ss(cfg, host, nthr, ch)), frac, min(nthr, ch), desc
+    sub1, _ = _ssd_sample(cfg, host, 1)
+    t1 = _time_oracle_ssd(sub1, nthr)                # one (batch, head) problem, one thread
+    problems = int(max(1, (target_s * nthr) / max(t1, 1e-9)))
+    if problems >= cfg.nheads:
+        batches, heads = int(min(cfg.batch, problems // cfg.nheads)), cfg.nheads
+    else:
+        batches, heads = 1, problems
+    sub, heads = _ssd_sample(cfg, host, heads, batches)
+    frac = heads * batches / (cfg.nheads * cfg.batch)
+    desc = (f"batches 0..{batches - 1} of {cfg.batch}, heads 0..{heads - 1} of {cfg.nheads} "
+            f"(each a full-T independent (batch, head) problem); value scaled by the sampled "
+            f"fraction {frac:.4g}")
+    return (lambda: _time_oracle_ssd(sub, nthr)), frac, min(nthr, heads * batches), desc
+
+
+def cpu_baseline(cfg, is_ss, host, target_s: float = 12.0):
+    """The fp64 oracle as it stands, on this host's cores, over a bounded sample of the workload,
+    scaled to tokens/s of the full workload."""
+    step, frac, cores, desc = oracle_sampler(cfg, is_ss, host, target_s)
+    dt = step()
+    return {"value": round(cfg.tokens * frac / dt, 1), "unit": "tokens/s", "cores": cores,
+            "kind": "oracle", "sample": desc + f"; {dt:.2f} s wall"}
+
+
+def run_reference(args, rank, world):
+    """Reference arm: the fp64 oracle on the host cores, W untimed and K timed steps, each step a
+    bounded sample of the same workload; same metric and unit as our arm."""
+    cfg = workload(args.workload)
+    from chunked_ssd_scan_gb300 import workloads as wl
+    is_ss = isinstance(cfg, wl.SelectiveScanConfig)
+    host = (wl.make_selective_scan_inputs(cfg, seed=0) if is_ss else wl.make_ssd_inputs(cfg, 0))
+    per_step = max(0.5, min(20.0, 150.0 / max(1, args.steps + args.warmup)))
+    step, frac, cores, desc = oracle_sampler(cfg, is_ss, host, per_step)
+    for _ in range(args.warmup):
+        step()
+    times = [step() for _ in range(args.steps)]
+    sec = sum(times) / len(times)
+    val = round(cfg.tokens * frac / sec, 1)
+    return {
+        "impl": "reference",
+        "metric": METRIC if not is_ss else "selective scan tokens/s at 1 GB300",
+        "value": val, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(cfg.tokens / val * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": config_dict(cfg, is_ss),
+        "cpu_baseline": {"value": val, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": desc + f"; {sec:.2f} s wall per step"},
+        "e2e": {"value": val, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    args = parse_args()
+    rank, world, local = dist_env()
+    if world > 1 and not torch.distributed.is_initialized():
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        torch.distributed.init_process_group(backend)
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args, rank, world)))
+        return
+    out = run_ours(args, rank, world, local)
+    if rank == 0:
+        print(json.dumps(out))
+    if world > 1:
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,217 @@
+"""chunked_ssd_scan_gb300 -- chunked SSD scan and selective scan on GB300 (sm_103a).
+
+Thin Python binding over the C ABI in include/ssdscan.h (libssdscan.so, built in-tree by
+``_build.build()``).  PyTorch supplies device memory and the current stream; every step of the
+computation runs in the library's CUDA kernels.  If the shared library is missing this module
+raises: there is no Python or CPU fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+from . import workloads  # noqa: F401  (seeded synthetic inputs; no scan arithmetic)
+
+__all__ = [
+    "SSDError", "load_library", "ssd_shape", "ssd_chunked_workspace_bytes", "ssd_chunked_variant",
+    "ssd_chunked_forward", "selective_scan_workspace_bytes", "selective_scan_forward",
+    "workspace_status", "STATUS", "VARIANTS",
+]
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libssdscan.so")
+
+STATUS = {0: "SSD_OK", 1: "SSD_ERR_INVALID_ARG", 2: "SSD_ERR_UNSUPPORTED", 3: "SSD_ERR_CUDA",
+          4: "SSD_ERR_WORKSPACE", 5: "SSD_ERR_TIMEOUT"}
+VARIANTS = {0: "none", 1: "generic", 2: "tc_bf16", 3: "tc_tf32"}
+SSD_F32, SSD_BF16 = 0, 1
+
+
+class SSDError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = int(status)
+        super().__init__(f"{what}: {STATUS.get(int(status), status)}")
+
+
+class ssd_shape(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int64), ("seqlen", ctypes.c_int64), ("nheads", ctypes.c_int64),
+                ("headdim", ctypes.c_int64), ("dstate", ctypes.c_int64),
+                ("ngroups", ctypes.c_int64), ("mimo_rank", ctypes.c_int64),
+                ("chunk_len", ctypes.c_int64), ("io_dtype", ctypes.c_int32),
+                ("has_theta", ctypes.c_int32)]
+
+
+_LIB = None
+_VP = ctypes.c_void_p
+_I64 = ctypes.c_int64
+
+
+def load_library(path: Optional[str] = None):
+    """Load libssdscan.so (raises if it has not been built)."""
+    global _LIB
+    if _LIB is not None and path is None:
+        return _LIB
+    p = path or LIB_PATH
+    if not os.path.exists(p):
+        raise RuntimeError(f"libssdscan.so not found at {p}; build it with "
+                           "`python -c 'import __graft_entry__ as g; g.build()'`")
+    lib = ctypes.CDLL(p)
+    SP = ctypes.POINTER(ssd_shape)
+    lib.ssd_chunked_workspace_bytes.restype = ctypes.c_size_t
+    lib.ssd_chunked_workspace_bytes.argtypes = [SP]
+    lib.ssd_chunked_variant.restype = ctypes.c_int32
+    lib.ssd_chunked_variant.argtypes = [SP]
+    lib.ssd_chunked_forward.restype = ctypes.c_int
+    lib.ssd_chunked_forward.argtypes = [SP] + [_VP] * 9 + [ctypes.c_size_t, _VP]
+    lib.selective_scan_workspace_bytes.restype = ctypes.c_size_t
+    lib.selective_scan_workspace_bytes.argtypes = [_I64] * 4
+    lib.selective_scan_forward.restype = ctypes.c_int
+    lib.selective_scan_forward.argtypes = [_VP] * 7 + [_I64] * 4 + [_VP, ctypes.c_size_t, _VP]
+    lib.ssd_workspace_status.restype = ctypes.c_int
+    lib.ssd_workspace_status.argtypes = [_VP, _VP, ctypes.POINTER(ctypes.c_int64)]
+    lib.ssd_status_string.restype = ctypes.c_char_p
+    lib.ssd_status_string.argtypes = [ctypes.c_int]
+    lib.ssd_abi_version.restype = ctypes.c_int32
+    lib.ssd_abi_version.argtypes = []
+    if path is None:
+        _LIB = lib
+    return lib
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_handle(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check_cuda(name, t, dtype=None, shape=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must have dtype {dtype}, got {t.dtype}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+
+
+def make_shape(batch, seqlen, nheads, headdim, dstate, ngroups, mimo_rank, chunk_len,
+               io_dtype, has_theta) -> ssd_shape:
+    return ssd_shape(batch, seqlen, nheads, headdim, dstate, ngroups, mimo_rank, chunk_len,
+                     SSD_BF16 if io_dtype in (torch.bfloat16, SSD_BF16, "bf16") else SSD_F32,
+                     1 if has_theta else 0)
+
+
+def ssd_chunked_workspace_bytes(shape: ssd_shape) -> int:
+    return int(load_library().ssd_chunked_workspace_bytes(ctypes.byref(shape)))
+
+
+def ssd_chunked_variant(shape: ssd_shape) -> str:
+    return VARIANTS.get(int(load_library().ssd_chunked_variant(ctypes.byref(shape))), "none")
+
+
+def shape_of(x: torch.Tensor, B: torch.Tensor, chunk_len: int, has_theta: bool) -> ssd_shape:
+    b, T, R, H, P = x.shape
+    G, N = B.shape[3], B.shape[4]
+    return make_shape(b, T, H, P, N, G, R, chunk_len, x.dtype, has_theta)
+
+
+def ssd_chunked_forward(x: torch.Tensor, dA: torch.Tensor, B: torch.Tensor, C: torch.Tensor, *,
+                        chunk_len: int, theta: Optional[torch.Tensor] = None,
+                        init_state: Optional[torch.Tensor] = None,
+                        y: Optional[torch.Tensor] = None,
+                        final_state: Optional[torch.Tensor] = None,
+                        return_final_state: bool = True,
+                        workspace: Optional[torch.Tensor] = None, stream=None):
+    """Chunked SSD forward scan through ``ssd_chunked_forward``.
+
+    x [b,T,R,H,P], B/C [b,T,R,G,N] (all f32 or all bf16), dA [b,T,H] f32, theta [b,T,H,N/2] f32,
+    init_state [b,H,P,N] f32.  Returns (y, final_state) (final_state None if not requested).
+    """
+    if x.dim() != 5 or B.dim() != 5:
+        raise ValueError("x must be [b,T,R,H,P] and B/C [b,T,R,G,N]")
+    b, T, R, H, P = x.shape
+    G, N = B.shape[3], B.shape[4]
+    _check_cuda("x", x)
+    if x.dtype not in (torch.float32, torch.bfloat16):
+        raise ValueError("x/B/C must be float32 or bfloat16")
+    _check_cuda("B", B, x.dtype, (b, T, R, G, N))
+    _check_cuda("C", C, x.dtype, (b, T, R, G, N))
+    _check_cuda("dA", dA, torch.float32, (b, T, H))
+    if theta is not None:
+        _check_cuda("theta", theta, torch.float32, (b, T, H, N // 2))
+    if init_state is not None:
+        _check_cuda("init_state", init_state, torch.float32, (b, H, P, N))
+    shape = shape_of(x, B, chunk_len, theta is not None)
+    lib = load_library()
+    if y is None:
+        y = torch.empty_like(x)
+    _check_cuda("y", y, x.dtype, x.shape)
+    if final_state is None and return_final_state:
+        final_state = torch.empty((b, H, P, N), dtype=torch.float32, device=x.device)
+    if final_state is not None:
+        _check_cuda("final_state", final_state, torch.float32, (b, H, P, N))
+    need = int(lib.ssd_chunked_workspace_bytes(ctypes.byref(shape)))
+    if need == 0:
+        raise SSDError(2, "ssd_chunked_workspace_bytes (shape not supported)")
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
+    _check_cuda("workspace", workspace, torch.uint8)
+    st = lib.ssd_chunked_forward(ctypes.byref(shape), _ptr(x), _ptr(dA), _ptr(B), _ptr(C),
+                                 _ptr(theta), _ptr(init_state), _ptr(y), _ptr(final_state),
+                                 _ptr(workspace), ctypes.c_size_t(workspace.numel()),
+                                 _stream_handle(stream))
+    if st != 0:
+        raise SSDError(st, "ssd_chunked_forward")
+    return y, final_state
+
+
+def selective_scan_workspace_bytes(batch, seqlen, d_model, d_state) -> int:
+    return int(load_library().selective_scan_workspace_bytes(batch, seqlen, d_model, d_state))
+
+
+def selective_scan_forward(u, delta, A, B, C, skip=None, *, y=None, workspace=None, stream=None):
+    """Diagonal-A selective scan through ``selective_scan_forward`` (all f32).  Returns y."""
+    b, T, D = u.shape
+    N = A.shape[1]
+    f32 = torch.float32
+    _check_cuda("u", u, f32)
+    _check_cuda("delta", delta, f32, (b, T, D))
+    _check_cuda("A", A, f32, (D, N))
+    _check_cuda("B", B, f32, (b, T, N))
+    _check_cuda("C", C, f32, (b, T, N))
+    if skip is not None:
+        _check_cuda("skip", skip, f32, (D,))
+    lib = load_library()
+    if y is None:
+        y = torch.empty_like(u)
+    _check_cuda("y", y, f32, (b, T, D))
+    need = int(lib.selective_scan_workspace_bytes(b, T, D, N))
+    if need == 0:
+        raise SSDError(2, "selective_scan_workspace_bytes (sizes not supported)")
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=u.device)
+    _check_cuda("workspace", workspace, torch.uint8)
+    st = lib.selective_scan_forward(_ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(skip),
+                                    _ptr(y), b, T, D, N, _ptr(workspace),
+                                    ctypes.c_size_t(workspace.numel()), _stream_handle(stream))
+    if st != 0:
+        raise SSDError(st, "selective_scan_forward")
+    return y
+
+
+def workspace_status(workspace: torch.Tensor, stream=None):
+    """(status name, detail) of the device-side error word of ``workspace`` (syncs the stream)."""
+    detail = ctypes.c_int64(0)
+    st = load_library().ssd_workspace_status(_ptr(workspace), _stream_handle(stream),
+                                             ctypes.byref(detail))
+    return STATUS.get(int(st), str(st)), int(detail.value)

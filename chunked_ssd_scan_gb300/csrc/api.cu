@@ -1,0 +1,219 @@
+// C ABI of the library: argument validation, workspace layout and kernel launches.
+// Declarations and the contract of every entry point are in include/ssdscan.h.
+#include <string.h>
+
+#include "common.cuh"
+#include "ssd_internal.h"
+
+using namespace ssd;
+
+namespace {
+
+constexpr int64_t kMaxElems = (int64_t)1 << 40;
+
+struct SsdLayout {
+  size_t states = 0, cend = 0, phi = 0, phisum = 0, total = 0;
+};
+
+bool mul_ok(int64_t a, int64_t b, int64_t* out) {
+  if (a < 0 || b < 0) return false;
+  if (a != 0 && b > kMaxElems / a) return false;
+  *out = a * b;
+  return true;
+}
+
+ssd_status check_shape(const ssd_shape* s) {
+  if (!s) return SSD_ERR_INVALID_ARG;
+  if (s->batch < 1 || s->seqlen < 1 || s->nheads < 1 || s->headdim < 1 || s->dstate < 1 ||
+      s->ngroups < 1 || s->mimo_rank < 1 || s->chunk_len < 1)
+    return SSD_ERR_INVALID_ARG;
+  if (s->nheads % s->ngroups != 0) return SSD_ERR_INVALID_ARG;
+  if (s->io_dtype != SSD_F32 && s->io_dtype != SSD_BF16) return SSD_ERR_INVALID_ARG;
+  if (s->has_theta != 0 && s->has_theta != 1) return SSD_ERR_INVALID_ARG;
+  if (s->has_theta && (s->dstate % 2) != 0) return SSD_ERR_INVALID_ARG;
+  int64_t t;
+  if (!mul_ok(s->batch, s->seqlen, &t) || !mul_ok(t, s->mimo_rank, &t) ||
+      !mul_ok(t, s->nheads, &t) || !mul_ok(t, s->headdim, &t))
+    return SSD_ERR_INVALID_ARG;
+  if (!mul_ok(s->batch, s->seqlen, &t) || !mul_ok(t, s->mimo_rank, &t) ||
+      !mul_ok(t, s->ngroups, &t) || !mul_ok(t, s->dstate, &t))
+    return SSD_ERR_INVALID_ARG;
+  if (!mul_ok(s->batch, s->nheads, &t) || !mul_ok(t, s->headdim, &t) || !mul_ok(t, s->dstate, &t))
+    return SSD_ERR_INVALID_ARG;
+  if (s->seqlen % s->chunk_len != 0) return SSD_ERR_UNSUPPORTED;
+  if (s->batch > 65535 || s->nheads > 65535) return SSD_ERR_UNSUPPORTED;   // grid limits
+  if (!generic_supported(s->chunk_len, s->mimo_rank, s->headdim, s->dstate, s->has_theta != 0))
+    return SSD_ERR_UNSUPPORTED;
+  return SSD_OK;
+}
+
+SsdLayout ssd_layout(const ssd_shape* s) {
+  SsdLayout L;
+  const int64_t nch = s->seqlen / s->chunk_len;
+  size_t off = sizeof(WsHeader);
+  L.states = off;
+  off = align_up(off + sizeof(float) * (size_t)(s->batch * nch * s->nheads * s->headdim * s->dstate),
+                 kWsAlign);
+  L.cend = off;
+  off = align_up(off + sizeof(float) * (size_t)(s->batch * nch * s->nheads), kWsAlign);
+  if (s->has_theta) {
+    L.phi = off;
+    off = align_up(off + sizeof(double) * (size_t)(s->batch * (nch + 1) * s->nheads * (s->dstate / 2)),
+                   kWsAlign);
+    L.phisum = off;
+    off = align_up(off + sizeof(double) * (size_t)(s->batch * nch * s->nheads * (s->dstate / 2)),
+                   kWsAlign);
+  }
+  L.total = off;
+  return L;
+}
+
+bool al16(const void* p) { return p == nullptr || aligned16(p); }
+
+}  // namespace
+
+extern "C" {
+
+size_t ssd_chunked_workspace_bytes(const ssd_shape* shape) {
+  if (check_shape(shape) != SSD_OK) return 0;
+  return ssd_layout(shape).total;
+}
+
+int32_t ssd_chunked_variant(const ssd_shape* shape) {
+  if (check_shape(shape) != SSD_OK) return SSD_VARIANT_NONE;
+  return SSD_VARIANT_GENERIC;
+}
+
+ssd_status ssd_chunked_forward(const ssd_shape* shape, const void* x, const float* dA,
+                               const void* B, const void* C, const float* theta,
+                               const float* init_state, void* y, float* final_state,
+                               void* workspace, size_t workspace_bytes, void* stream) {
+  const ssd_status sc = check_shape(shape);
+  if (sc != SSD_OK) return sc;
+  if (!x || !dA || !B || !C || !y) return SSD_ERR_INVALID_ARG;
+  if ((shape->has_theta != 0) != (theta != nullptr)) return SSD_ERR_INVALID_ARG;
+  if (!al16(x) || !al16(dA) || !al16(B) || !al16(C) || !al16(y) || !al16(theta) ||
+      !al16(init_state) || !al16(final_state))
+    return SSD_ERR_INVALID_ARG;
+  const SsdLayout lay = ssd_layout(shape);
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) % kWsAlign) != 0 ||
+      workspace_bytes < lay.total)
+    return SSD_ERR_WORKSPACE;
+
+  char* ws = static_cast<char*>(workspace);
+  GenericParams p;
+  memset(&p, 0, sizeof(p));
+  p.x = x;
+  p.dA = dA;
+  p.B = B;
+  p.C = C;
+  p.theta = theta;
+  p.init = init_state;
+  p.y = y;
+  p.final_state = final_state;
+  p.batch = shape->batch;
+  p.T = shape->seqlen;
+  p.H = shape->nheads;
+  p.P = shape->headdim;
+  p.N = shape->dstate;
+  p.G = shape->ngroups;
+  p.R = shape->mimo_rank;
+  p.l = shape->chunk_len;
+  p.nch = shape->seqlen / shape->chunk_len;
+  p.states = reinterpret_cast<float*>(ws + lay.states);
+  p.cend = reinterpret_cast<float*>(ws + lay.cend);
+  p.phi = theta ? reinterpret_cast<double*>(ws + lay.phi) : nullptr;
+  p.phisum = theta ? reinterpret_cast<double*>(ws + lay.phisum) : nullptr;
+  p.hdr = reinterpret_cast<WsHeader*>(ws);
+  const cudaError_t e = generic_forward(p, shape->io_dtype == SSD_BF16,
+                                        static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
+}
+
+size_t selective_scan_workspace_bytes(int64_t batch, int64_t seqlen, int64_t d_model,
+                                      int64_t d_state) {
+  if (batch < 1 || seqlen < 1 || d_model < 1 || d_state < 1 || d_state > 64) return 0;
+  int64_t t;
+  if (!mul_ok(batch, seqlen, &t) || !mul_ok(t, d_model, &t)) return 0;
+  const int64_t seg = ss_segment_length(seqlen);
+  const int64_t nseg = (seqlen + seg - 1) / seg;
+  size_t off = sizeof(WsHeader);
+  off = align_up(off + sizeof(float) * (size_t)(batch * nseg * d_state * d_model), kWsAlign);
+  off = align_up(off + sizeof(float) * (size_t)(batch * nseg * d_model), kWsAlign);
+  return off;
+}
+
+ssd_status selective_scan_forward(const float* u, const float* delta, const float* A,
+                                  const float* B, const float* C, const float* skip, float* y,
+                                  int64_t batch, int64_t seqlen, int64_t d_model,
+                                  int64_t d_state, void* workspace, size_t workspace_bytes,
+                                  void* stream) {
+  if (batch < 1 || seqlen < 1 || d_model < 1 || d_state < 1) return SSD_ERR_INVALID_ARG;
+  if (d_state > 64 || batch > 65535 || d_model > ((int64_t)65535 * 128)) return SSD_ERR_UNSUPPORTED;
+  int64_t t;
+  if (!mul_ok(batch, seqlen, &t) || !mul_ok(t, d_model, &t)) return SSD_ERR_INVALID_ARG;
+  if (!u || !delta || !A || !B || !C || !y) return SSD_ERR_INVALID_ARG;
+  if (!al16(u) || !al16(delta) || !al16(A) || !al16(B) || !al16(C) || !al16(skip) || !al16(y))
+    return SSD_ERR_INVALID_ARG;
+  const size_t need = selective_scan_workspace_bytes(batch, seqlen, d_model, d_state);
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) % kWsAlign) != 0 ||
+      workspace_bytes < need)
+    return SSD_ERR_WORKSPACE;
+  SelectiveScanParams p;
+  memset(&p, 0, sizeof(p));
+  p.u = u;
+  p.delta = delta;
+  p.A = A;
+  p.B = B;
+  p.C = C;
+  p.skip = skip;
+  p.y = y;
+  p.batch = batch;
+  p.T = seqlen;
+  p.D = d_model;
+  p.N = d_state;
+  p.seg_len = ss_segment_length(seqlen);
+  p.nseg = (seqlen + p.seg_len - 1) / p.seg_len;
+  char* ws = static_cast<char*>(workspace);
+  size_t off = sizeof(WsHeader);
+  p.agg_h = reinterpret_cast<float*>(ws + off);
+  off = align_up(off + sizeof(float) * (size_t)(batch * p.nseg * d_state * d_model), kWsAlign);
+  p.agg_dt = reinterpret_cast<float*>(ws + off);
+  p.hdr = reinterpret_cast<WsHeader*>(ws);
+  const cudaError_t e = selective_scan_launch(p, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
+}
+
+ssd_status ssd_workspace_status(void* workspace, void* stream, int64_t* detail) {
+  if (detail) *detail = 0;
+  if (!workspace) return SSD_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(st) != cudaSuccess) return SSD_ERR_CUDA;
+  WsHeader h;
+  if (cudaMemcpy(&h, workspace, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return SSD_ERR_CUDA;
+  if (h.error != 0) {
+    if (detail) *detail = h.detail;
+    const int64_t zero[2] = {0, 0};
+    if (cudaMemcpy(workspace, zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
+      return SSD_ERR_CUDA;
+    return static_cast<ssd_status>(h.error);
+  }
+  return SSD_OK;
+}
+
+const char* ssd_status_string(ssd_status status) {
+  switch (status) {
+    case SSD_OK: return "SSD_OK";
+    case SSD_ERR_INVALID_ARG: return "SSD_ERR_INVALID_ARG";
+    case SSD_ERR_UNSUPPORTED: return "SSD_ERR_UNSUPPORTED";
+    case SSD_ERR_CUDA: return "SSD_ERR_CUDA";
+    case SSD_ERR_WORKSPACE: return "SSD_ERR_WORKSPACE";
+    case SSD_ERR_TIMEOUT: return "SSD_ERR_TIMEOUT";
+  }
+  return "SSD_ERR_UNKNOWN";
+}
+
+int32_t ssd_abi_version(void) { return 1; }
+
+}  // extern "C"

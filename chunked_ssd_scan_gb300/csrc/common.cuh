@@ -1,0 +1,58 @@
+// Shared device/host helpers of the ssdscan library (not part of the public ABI).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/ssdscan.h"
+
+namespace ssd {
+
+// ----------------------------------------------------------------------------------------------
+// Workspace header: the first 256 bytes of every workspace.  Kernels latch device-side errors
+// here instead of trapping, and the fused kernel keeps its work-ticket counters here.
+// ----------------------------------------------------------------------------------------------
+struct WsHeader {
+  int32_t error;     // 0 = ok, otherwise an ssd_status value latched by a kernel
+  int32_t pad0;
+  int64_t detail;    // kernel-specific detail word of the first latched error
+  uint32_t ticket;   // dynamic work-ticket counter (fused kernel)
+  uint32_t done;     // finished-CTA counter (fused kernel)
+  uint32_t reserved[58];
+};
+static_assert(sizeof(WsHeader) == 256, "workspace header must be 256 bytes");
+
+constexpr size_t kWsAlign = 256;
+
+__host__ __device__ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// Latch the first error of a call into the workspace header (never traps).
+__device__ inline void latch_error(WsHeader* hdr, int32_t code, int64_t detail) {
+  if (atomicCAS(&hdr->error, 0, code) == 0) {
+    hdr->detail = detail;
+  }
+}
+
+// Load one element of an I/O tensor as fp32.
+template <typename T>
+__device__ __forceinline__ float ld_f32(const T* p);
+template <>
+__device__ __forceinline__ float ld_f32<float>(const float* p) { return __ldg(p); }
+template <>
+__device__ __forceinline__ float ld_f32<__nv_bfloat16>(const __nv_bfloat16* p) {
+  return __bfloat162float(*p);
+}
+
+template <typename T>
+__device__ __forceinline__ void st_from_f32(T* p, float v);
+template <>
+__device__ __forceinline__ void st_from_f32<float>(float* p, float v) { *p = v; }
+template <>
+__device__ __forceinline__ void st_from_f32<__nv_bfloat16>(__nv_bfloat16* p, float v) {
+  *p = __float2bfloat16_rn(v);
+}
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace ssd

@@ -1,0 +1,54 @@
+// Internal declarations shared by the library's translation units (not part of the ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace ssd {
+
+struct WsHeader;
+
+// Arguments of the generic CUDA-core chunk pipeline.
+struct GenericParams {
+  const void* x;
+  const float* dA;
+  const void* B;
+  const void* C;
+  const float* theta;
+  const float* init;
+  void* y;
+  float* final_state;
+  int64_t batch, T, H, P, N, G, R, l, nch;
+  float* states;    // [b, nch, H, P, N]: chunk states, overwritten with chunk-input states
+  float* cend;      // [b, nch, H]: chunk-end cumulative log-decay
+  double* phi;      // [b, nch+1, H, N/2]: chunk-start angles (mod 2 pi); the last one is Phi_{T-1}
+  double* phisum;   // [b, nch, H, N/2]: per-chunk angle sums
+  WsHeader* hdr;
+};
+
+size_t generic_state_smem(int64_t l, int64_t P, int64_t N, bool theta);
+size_t generic_scan_smem(int64_t l, int64_t P, int64_t N, bool theta);
+bool generic_supported(int64_t l, int64_t R, int64_t P, int64_t N, bool theta);
+cudaError_t generic_forward(const GenericParams& p, bool bf16, cudaStream_t st);
+
+// Selective scan.
+struct SelectiveScanParams {
+  const float* u;
+  const float* delta;
+  const float* A;
+  const float* B;
+  const float* C;
+  const float* skip;
+  float* y;
+  int64_t batch, T, D, N;
+  int64_t seg_len, nseg;
+  float* agg_h;     // [b, nseg, N, D]: segment-local end states, then segment-input states
+  float* agg_dt;    // [b, nseg, D]: summed delta per segment
+  WsHeader* hdr;
+};
+
+int64_t ss_segment_length(int64_t T);
+cudaError_t selective_scan_launch(const SelectiveScanParams& p, cudaStream_t st);
+
+}  // namespace ssd

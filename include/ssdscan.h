@@ -1,0 +1,144 @@
+/*
+ * ssdscan.h -- C ABI of the GB300 (sm_103a) chunked SSD scan and diagonal-A selective scan.
+ *
+ * Every function is extern "C", takes plain pointers and integer sizes, throws nothing, and
+ * returns an ssd_status (or a size / string).  Pointers named as device pointers must be
+ * device-accessible memory of the current CUDA device; the caller owns every buffer.  Compute
+ * entry points are asynchronous on the given stream (a cudaStream_t passed as void*, NULL for
+ * the legacy default stream) and never synchronise the device; they allocate no device memory.
+ *
+ * Sources of the operations (web pages, cited by title and section):
+ *  - serial.rs (burn_mamba mamba3/ssd/serial.rs): the SSD chunk pipeline K1..K5 on rank-fused
+ *    tensors -- K1 intra-chunk cumsum of dA, K2 C.B^T, K3 chunk states from pre-scaled V,
+ *    K4 sequential state passing, K5 y = (L o CB) V + exp(cumA) C h_in.
+ *  - segsum.rs (burn_mamba modules/misc/segsum.rs): the stable segment sum behind the causal mask.
+ *  - scan.py (steertts mamba3/scan.py): cumulative angles Phi_t = sum_{s<=t} theta_s and the
+ *    pairwise rotation rotate_by; the data-dependent rotation is absorbed into B and C.
+ *  - SSM Selective Scan (LeetGPU write-up): the diagonal-A selective scan with skip term.
+ *
+ * Layouts (row-major, contiguous, innermost index last):
+ *   x, y          [batch, seqlen, mimo_rank, nheads, headdim]     io dtype
+ *   dA            [batch, seqlen, nheads]                         f32  (log-decay dt*A)
+ *   B, C          [batch, seqlen, mimo_rank, ngroups, dstate]     io dtype
+ *   theta         [batch, seqlen, nheads, dstate/2]               f32
+ *   init_state    [batch, nheads, headdim, dstate]                f32
+ *   final_state   [batch, nheads, headdim, dstate]                f32
+ * Head h reads B/C group h / (nheads/ngroups).  x, B, C and y share io_dtype (f32 or bf16).
+ */
+#ifndef SSDSCAN_H
+#define SSDSCAN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum ssd_status {
+  SSD_OK = 0,
+  SSD_ERR_INVALID_ARG = 1, /* null pointer, non-positive size, bad divisibility, misalignment */
+  SSD_ERR_UNSUPPORTED = 2, /* valid arguments outside what the kernels implement             */
+  SSD_ERR_CUDA = 3,        /* a CUDA runtime call or kernel launch failed                    */
+  SSD_ERR_WORKSPACE = 4,   /* workspace missing, misaligned or smaller than required         */
+  SSD_ERR_TIMEOUT = 5      /* a device-side wait gave up (latched in the workspace)          */
+} ssd_status;
+
+typedef enum ssd_dtype { SSD_F32 = 0, SSD_BF16 = 1 } ssd_dtype;
+
+typedef struct ssd_shape {
+  int64_t batch;     /* b >= 1                                                   */
+  int64_t seqlen;    /* T >= 1                                                   */
+  int64_t nheads;    /* H >= 1                                                   */
+  int64_t headdim;   /* P                                                        */
+  int64_t dstate;    /* N (even when theta is given)                             */
+  int64_t ngroups;   /* G, divides H                                             */
+  int64_t mimo_rank; /* R >= 1; the fused chunk length is L = chunk_len * R      */
+  int64_t chunk_len; /* l; T must be a multiple of l                             */
+  int32_t io_dtype;  /* ssd_dtype of x, B, C and y                               */
+  int32_t has_theta; /* 1 when theta will be passed (changes the workspace size) */
+} ssd_shape;
+
+/* Kernel families that ssd_chunked_forward may run for a shape. */
+typedef enum ssd_kernel_variant {
+  SSD_VARIANT_NONE = 0,    /* shape not supported                                    */
+  SSD_VARIANT_GENERIC = 1, /* CUDA-core fp32 chunk pipeline (any supported shape)    */
+  SSD_VARIANT_TC_BF16 = 2, /* fused tcgen05/TMEM kernel, bf16 operands, fp32 accum.  */
+  SSD_VARIANT_TC_TF32 = 3  /* fused tcgen05/TMEM kernel, split-tf32 operands (f32 io) */
+} ssd_kernel_variant;
+
+/*
+ * Bytes of device workspace ssd_chunked_forward needs for `shape` (0 if the shape is invalid).
+ * The workspace must be 256-byte aligned.  Its contents need no initialisation: every call
+ * resets what it uses, on the stream, before reading it.  One workspace must not be used by
+ * two calls that can run concurrently.
+ */
+size_t ssd_chunked_workspace_bytes(const ssd_shape* shape);
+
+/* Which kernel family ssd_chunked_forward will use for `shape` (SSD_VARIANT_NONE if none). */
+int32_t ssd_chunked_variant(const ssd_shape* shape);
+
+/*
+ * Chunked SSD forward scan (serial.rs: ssd_serial and K1..K5; scan.py: rotation absorption).
+ *
+ * Per (batch b, head h), with g = h / (H/G), Phi_t = sum_{s<=t} theta[b,s,h,:]:
+ *   state_{-1} = init_state[b,h] (zeros if init_state is NULL)
+ *   state_t    = exp(dA[b,t,h]) * Rot(theta_t) state_{t-1} + sum_r x[b,t,r,h,:] (outer) B[b,t,r,g,:]
+ *   y[b,t,r,h,:] = state_t . C[b,t,r,g,:]                   (sum over dstate)
+ *   final_state[b,h] = state_{T-1}  (physical frame: rotations applied, not the absorbed frame)
+ * Rot(theta) turns each interleaved pair (2k, 2k+1) of the dstate axis by +theta[...,k].
+ * x is the pre-scaled value (no dt factor) and no skip term is added, as in K3/K5.
+ * The result equals the sequential recurrence above for any chunk_len; chunk_len sets how the
+ * kernels tile time (K1..K5 granularity) and must divide seqlen.
+ *
+ * Arguments: x, B, C, y are device pointers of io_dtype; dA, theta, init_state, final_state are
+ * device f32.  theta may be NULL only if shape->has_theta == 0 (and must be non-NULL otherwise);
+ * init_state and final_state may be NULL.  x, B, C, y, dA, final_state must be 16-byte aligned.
+ * workspace: device memory of at least ssd_chunked_workspace_bytes(shape), 256-byte aligned.
+ * stream: cudaStream_t as void*.
+ * Errors: INVALID_ARG / UNSUPPORTED / WORKSPACE are detected on the host before any launch and
+ * leave every output untouched; CUDA reports a failed launch.  Device-side waits that give up
+ * are latched in the workspace and reported by ssd_workspace_status.
+ */
+ssd_status ssd_chunked_forward(const ssd_shape* shape, const void* x, const float* dA,
+                               const void* B, const void* C, const float* theta,
+                               const float* init_state, void* y, float* final_state,
+                               void* workspace, size_t workspace_bytes, void* stream);
+
+/* Bytes of device workspace selective_scan_forward needs (0 if the sizes are invalid). */
+size_t selective_scan_workspace_bytes(int64_t batch, int64_t seqlen, int64_t d_model,
+                                      int64_t d_state);
+
+/*
+ * Diagonal-A selective scan (SSM Selective Scan page, problem statement), all f32:
+ *   h_{-1} = 0;  h_t[n] = exp(delta[b,t,d] A[d,n]) h_{t-1}[n] + delta[b,t,d] B[b,t,n] u[b,t,d]
+ *   y[b,t,d] = sum_n C[b,t,n] h_t[n] + skip[d] u[b,t,d]
+ * Layouts: u, delta, y [batch, seqlen, d_model]; A [d_model, d_state]; B, C [batch, seqlen,
+ * d_state]; skip [d_model] (NULL = no skip term).  All device pointers, 16-byte aligned.
+ * 1 <= d_state <= 64.  Same asynchrony, workspace and error rules as ssd_chunked_forward.
+ */
+ssd_status selective_scan_forward(const float* u, const float* delta, const float* A,
+                                  const float* B, const float* C, const float* skip, float* y,
+                                  int64_t batch, int64_t seqlen, int64_t d_model,
+                                  int64_t d_state, void* workspace, size_t workspace_bytes,
+                                  void* stream);
+
+/*
+ * Reads (and clears) the device-side error word of a workspace after synchronising `stream`.
+ * Returns SSD_OK, or SSD_ERR_TIMEOUT if a device wait of an earlier call on this workspace gave
+ * up, or SSD_ERR_CUDA if the read itself failed.  *detail (if non-NULL) receives the
+ * device-recorded detail word (0 when none).
+ */
+ssd_status ssd_workspace_status(void* workspace, void* stream, int64_t* detail);
+
+/* Human-readable name of a status code (static storage). */
+const char* ssd_status_string(ssd_status status);
+
+/* ABI version of this library (incremented on incompatible changes). */
+int32_t ssd_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SSDSCAN_H */

@@ -1,0 +1,61 @@
+"""Helpers shared by the GPU parity tests: run the library and the oracle on the same inputs."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import chunked_ssd_scan_gb300 as pkg
+import oracle
+from chunked_ssd_scan_gb300 import workloads as wl
+
+# Element-wise gates: |got - ref| <= tol * (1 + |ref|) on y and on the final state.
+TOL = {"f32": 1e-4, "bf16": 2e-2}
+
+
+def to_np(t):
+    return None if t is None else t.detach().to("cpu", torch.float64).numpy()
+
+
+def gpu_ssd(inp: dict, chunk_len: int, dev: str = "cuda", final: bool = True):
+    d = {k: (v.to(dev) if v is not None else None) for k, v in inp.items()}
+    y, fin = pkg.ssd_chunked_forward(d["x"], d["dA"], d["B"], d["C"], chunk_len=chunk_len,
+                                     theta=d["theta"], init_state=d["init_state"],
+                                     return_final_state=final)
+    torch.cuda.synchronize()
+    return to_np(y), to_np(fin)
+
+
+def oracle_ssd(inp: dict):
+    return oracle.ssd(to_np(inp["x"]), to_np(inp["dA"]), to_np(inp["B"]), to_np(inp["C"]),
+                      to_np(inp["theta"]), to_np(inp["init_state"]))
+
+
+def check_close(got, ref, tol, what):
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    assert got.shape == ref.shape, f"{what}: shape {got.shape} != {ref.shape}"
+    assert np.all(np.isfinite(got)), f"{what}: non-finite output"
+    err = np.abs(got - ref)
+    bound = tol * (1.0 + np.abs(ref))
+    bad = err > bound
+    if np.any(bad):
+        idx = np.unravel_index(np.argmax(err - bound), err.shape)
+        raise AssertionError(
+            f"{what}: {int(bad.sum())} of {bad.size} elements outside tol {tol}: worst at {idx} "
+            f"got {got[idx]:.6g} ref {ref[idx]:.6g} (max abs err {err.max():.3e})")
+    nrel = float(np.linalg.norm(got - ref) / max(np.linalg.norm(ref), 1e-300))
+    return float(err.max()), nrel
+
+
+def slice_heads(inp: dict, cfg: wl.SSDConfig, b: int, h: int) -> dict:
+    """The independent (batch b, head h) sub-problem, as a batch-1, one-head, one-group problem."""
+    g = h // (cfg.nheads // cfg.ngroups)
+    return {
+        "x": inp["x"][b:b + 1, :, :, h:h + 1].contiguous(),
+        "dA": inp["dA"][b:b + 1, :, h:h + 1].contiguous(),
+        "B": inp["B"][b:b + 1, :, :, g:g + 1].contiguous(),
+        "C": inp["C"][b:b + 1, :, :, g:g + 1].contiguous(),
+        "theta": None if inp["theta"] is None else inp["theta"][b:b + 1, :, h:h + 1].contiguous(),
+        "init_state": (None if inp["init_state"] is None
+                       else inp["init_state"][b:b + 1, h:h + 1].contiguous()),
+    }

@@ -1,0 +1,128 @@
+"""CUDA SSD path vs the fp64 oracle, element by element, through the C ABI (GPU)."""
+import numpy as np
+import pytest
+import torch
+
+import chunked_ssd_scan_gb300 as pkg
+from chunked_ssd_scan_gb300 import workloads as wl
+from tests.parity_util import TOL, check_close, gpu_ssd, oracle_ssd, slice_heads
+
+pytestmark = pytest.mark.gpu
+
+# Reduced-T versions of the four SSD workloads: several chunks and tiles, oracle in seconds.
+REDUCED = [
+    wl.TINY_SISO_F32,
+    wl.MAMBA2_SISO_BF16.with_(batch=2, seqlen=1024),
+    wl.MAMBA3_MIMO_BF16.with_(batch=1, seqlen=512),
+    wl.LONG_ROT_F32.with_(seqlen=2048),
+]
+
+
+@pytest.mark.parametrize("cfg", REDUCED, ids=lambda c: c.name)
+@pytest.mark.parametrize("variant", ["stated", "slow_decay_init", "seed1", "seed2"])
+def test_reduced_workloads(cfg, variant):
+    kw = dict(slow_decay=True, init_state=True) if variant == "slow_decay_init" else {}
+    seed = {"seed1": 1, "seed2": 2}.get(variant, 0)
+    inp = wl.make_ssd_inputs(cfg, seed=seed, **kw)
+    y, fin = gpu_ssd(inp, cfg.chunk_len)
+    yr, fr = oracle_ssd(inp)
+    check_close(y, yr, TOL[cfg.dtype], f"{cfg.name}/{variant} y")
+    check_close(fin, fr, TOL[cfg.dtype], f"{cfg.name}/{variant} final_state")
+
+
+FULL = [wl.MAMBA2_SISO_BF16, wl.MAMBA3_MIMO_BF16, wl.LONG_ROT_F32]
+SAMPLES = {"mamba2_siso_bf16": [(0, 0), (3, 31), (2, 17)],
+           "mamba3_mimo_bf16": [(0, 5), (1, 30)],
+           "long_rotation_f32": [(0, 0), (0, 23)]}
+
+
+@pytest.mark.parametrize("cfg", FULL, ids=lambda c: c.name)
+def test_full_size_sampled_heads(cfg):
+    """Full workload sizes in the benchmark's launch configuration; the oracle recomputes a few
+    independent (batch, head) problems in full and compares every one of their outputs."""
+    inp = wl.make_ssd_inputs(cfg, seed=0)
+    y, fin = gpu_ssd(inp, cfg.chunk_len)
+    assert np.all(np.isfinite(y)) and np.all(np.isfinite(fin))
+    for (b, h) in SAMPLES[cfg.name]:
+        sub = slice_heads(inp, cfg, b, h)
+        yr, fr = oracle_ssd(sub)
+        check_close(y[b:b + 1, :, :, h:h + 1], yr, TOL[cfg.dtype], f"{cfg.name} y[b={b},h={h}]")
+        check_close(fin[b:b + 1, h:h + 1], fr, TOL[cfg.dtype], f"{cfg.name} final[b={b},h={h}]")
+
+
+EDGE = [
+    # single chunk, one head, tiny dims
+    wl.SSDConfig("one_chunk_f32", 1, 64, 1, 8, 8, 64, 1, 1, "f32"),
+    wl.SSDConfig("one_chunk_bf16", 1, 256, 2, 64, 128, 256, 1, 1, "bf16"),
+    # chunk_len 1 (every step is a chunk) and T == 1
+    wl.SSDConfig("chunk1_f32", 1, 24, 2, 4, 6, 1, 1, 2, "f32"),
+    wl.SSDConfig("T1_f32", 2, 1, 3, 5, 4, 1, 2, 3, "f32", theta=True),
+    # odd head/state sizes, groups, MIMO with ragged fused tiles (L = 3*40 = 120)
+    wl.SSDConfig("odd_dims_f32", 2, 120, 6, 5, 6, 40, 3, 2, "f32", theta=True),
+    wl.SSDConfig("odd_dims_bf16", 1, 96, 4, 24, 40, 32, 2, 2, "bf16"),
+    # shared B/C across all heads with rotation (per-head rotation of shared B/C)
+    wl.SSDConfig("shared_bc_theta_f32", 1, 512, 8, 16, 32, 128, 1, 1, "f32", theta=True),
+    # largest tile shapes of the bf16 path with several chunks
+    wl.SSDConfig("p128_n128_bf16", 1, 512, 2, 128, 128, 128, 1, 2, "bf16"),
+]
+
+
+@pytest.mark.parametrize("cfg", EDGE, ids=lambda c: c.name)
+def test_edge_shapes(cfg):
+    inp = wl.make_ssd_inputs(cfg, seed=3, slow_decay=True, init_state=True)
+    y, fin = gpu_ssd(inp, cfg.chunk_len)
+    yr, fr = oracle_ssd(inp)
+    check_close(y, yr, TOL[cfg.dtype], f"{cfg.name} y")
+    check_close(fin, fr, TOL[cfg.dtype], f"{cfg.name} final_state")
+
+
+def test_final_state_optional_and_y_unchanged():
+    cfg = wl.TINY_SISO_F32
+    inp = wl.make_ssd_inputs(cfg, seed=4, init_state=True)
+    y1, _ = gpu_ssd(inp, cfg.chunk_len, final=False)
+    y2, _ = gpu_ssd(inp, cfg.chunk_len, final=True)
+    assert np.array_equal(y1, y2)
+
+
+def test_chunk_length_invariance_on_gpu():
+    """The result does not depend on chunk_len (the serial.rs page's decomposition is exact)."""
+    cfg = wl.SSDConfig("inv", 1, 512, 4, 16, 32, 64, 1, 2, "f32", theta=True)
+    inp = wl.make_ssd_inputs(cfg, seed=5, slow_decay=True, init_state=True)
+    yr, fr = oracle_ssd(inp)
+    for l in (16, 64, 128, 256, 512):
+        y, fin = gpu_ssd(inp, l)
+        check_close(y, yr, TOL["f32"], f"chunk_len {l} y")
+        check_close(fin, fr, TOL["f32"], f"chunk_len {l} final")
+
+
+def test_continuation_through_final_state():
+    cfg = wl.SSDConfig("cont", 1, 512, 4, 16, 32, 64, 2, 2, "f32")
+    inp = wl.make_ssd_inputs(cfg, seed=6, slow_decay=True, init_state=True)
+    yf, ff = gpu_ssd(inp, 64)
+    first = {k: (v[:, :256].contiguous() if (v is not None and k != "init_state") else v)
+             for k, v in inp.items()}
+    y1, f1 = gpu_ssd(first, 64)
+    second = {k: (v[:, 256:].contiguous() if (v is not None and k != "init_state") else v)
+              for k, v in inp.items()}
+    second["init_state"] = torch.from_numpy(f1).float()
+    y2, f2 = gpu_ssd(second, 64)
+    check_close(np.concatenate([y1, y2], axis=1), yf, 1e-5, "continuation y")
+    check_close(f2, ff, 1e-5, "continuation final")
+
+
+def test_deterministic_bitwise():
+    cfg = wl.MAMBA2_SISO_BF16.with_(batch=1, seqlen=1024, nheads=8)
+    inp = wl.make_ssd_inputs(cfg, seed=7, init_state=True)
+    a = gpu_ssd(inp, cfg.chunk_len)
+    b = gpu_ssd(inp, cfg.chunk_len)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+def test_host_rejections_with_real_buffers():
+    cfg = wl.TINY_SISO_F32
+    d = wl.make_ssd_inputs(cfg, seed=0, device="cuda")
+    with pytest.raises(pkg.SSDError) as e:
+        pkg.ssd_chunked_forward(d["x"], d["dA"], d["B"], d["C"], chunk_len=48)
+    assert e.value.status == 2
+    with pytest.raises(ValueError):
+        pkg.ssd_chunked_forward(d["x"].cpu(), d["dA"], d["B"], d["C"], chunk_len=64)
