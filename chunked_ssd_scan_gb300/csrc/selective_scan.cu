@@ -10,6 +10,8 @@
 // d_state states in registers; loads of u/delta/y are coalesced over d.
 #include <math.h>
 
+#include <mutex>
+
 #include "common.cuh"
 #include "ssd_internal.h"
 
@@ -121,3 +123,84 @@ cudaError_t selective_scan_launch(const SelectiveScanParams& p, cudaStream_t st)
 }
 
 }  // namespace ssd
+
+// ------------------------------------------------------------------------------------------------
+// Allocation-free selective scan: the same three kernels, with their scratch (segment end states
+// and summed deltas) in a fixed device array owned by this library instead of a caller
+// workspace.  It exists for callers that cannot allocate device memory -- for example code
+// that is handed only its input and output buffers through a fixed plugin interface, or code on
+// a path where cudaMalloc (and the device synchronisation it can imply) is not allowed.
+// ------------------------------------------------------------------------------------------------
+namespace {
+
+constexpr size_t kNoAllocScratchFloats = SSD_NOALLOC_SCRATCH_BYTES / sizeof(float);
+
+// Every GPU that loads this library holds this array until the process exits.
+static __device__ __align__(256) float g_noalloc_scratch[kNoAllocScratchFloats];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mu;
+float* g_noalloc_ptr[kMaxDevices] = {};
+
+// Device address of g_noalloc_scratch on the current device, looked up once per device (the
+// array's name in host code is only a host-side stand-in, never a device address).
+cudaError_t noalloc_scratch(float** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (g_noalloc_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return e;
+    g_noalloc_ptr[dev] = static_cast<float*>(p);
+  }
+  *out = g_noalloc_ptr[dev];
+  return cudaSuccess;
+}
+
+}  // namespace
+
+extern "C" ssd_status selective_scan_forward_noalloc(const float* u, const float* delta,
+                                                     const float* A, const float* B,
+                                                     const float* C, const float* skip, float* y,
+                                                     int64_t batch, int64_t seqlen,
+                                                     int64_t d_model, int64_t d_state,
+                                                     void* stream) {
+  if (batch < 1 || seqlen < 1 || d_model < 1 || d_state < 1) return SSD_ERR_INVALID_ARG;
+  if (d_state > 64 || batch > 65535 || d_model > ((int64_t)65535 * 128)) return SSD_ERR_UNSUPPORTED;
+  if (!u || !delta || !A || !B || !C || !y) return SSD_ERR_INVALID_ARG;
+  const void* ptrs[] = {u, delta, A, B, C, skip, y};
+  for (const void* q : ptrs)
+    if (q && !ssd::aligned16(q)) return SSD_ERR_INVALID_ARG;
+  const int64_t seg = ssd::ss_segment_length(seqlen);
+  const int64_t nseg = (seqlen + seg - 1) / seg;
+  // scratch: segment end states [b, nseg, N, D] then summed deltas [b, nseg, D]
+  if (batch > (int64_t)kNoAllocScratchFloats || nseg > (int64_t)kNoAllocScratchFloats ||
+      d_model > (int64_t)kNoAllocScratchFloats)
+    return SSD_ERR_UNSUPPORTED;
+  const int64_t rows = batch * nseg * d_model;
+  if (rows > (int64_t)kNoAllocScratchFloats / (d_state + 1)) return SSD_ERR_UNSUPPORTED;
+  float* scratch = nullptr;
+  if (noalloc_scratch(&scratch) != cudaSuccess) return SSD_ERR_CUDA;
+  ssd::SelectiveScanParams p{};
+  p.u = u;
+  p.delta = delta;
+  p.A = A;
+  p.B = B;
+  p.C = C;
+  p.skip = skip;
+  p.y = y;
+  p.batch = batch;
+  p.T = seqlen;
+  p.D = d_model;
+  p.N = d_state;
+  p.seg_len = seg;
+  p.nseg = nseg;
+  p.agg_h = scratch;
+  p.agg_dt = scratch + rows * d_state;
+  p.hdr = nullptr;
+  const cudaError_t e = ssd::selective_scan_launch(p, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
+}

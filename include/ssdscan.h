@@ -123,6 +123,33 @@ ssd_status selective_scan_forward(const float* u, const float* delta, const floa
                                   int64_t d_state, void* workspace, size_t workspace_bytes,
                                   void* stream);
 
+/* Size of the fixed device scratch array behind selective_scan_forward_noalloc. */
+#define SSD_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
+
+/*
+ * Allocation-free variant of selective_scan_forward.  The pages have no counterpart: this entry
+ * point exists for callers that cannot allocate device memory (for example code that receives
+ * only its input and output buffers through a fixed plugin interface, or code on a path where
+ * cudaMalloc and the device synchronisation it can imply are not allowed).  It computes exactly
+ * what selective_scan_forward computes, with the same kernels, but takes no workspace: its
+ * scratch lives in one fixed device array of SSD_NOALLOC_SCRATCH_BYTES (16 MiB) inside this
+ * library, which every GPU that loads the library holds until the process exits.
+ *   - Limit: (d_state + 1) * batch * ceil(seqlen / 64) * d_model floats must fit the array
+ *     (the 4 x 4096 x 512 x 16 workload uses 8.9 MB); larger sizes return SSD_ERR_UNSUPPORTED
+ *     before any launch.  Other argument errors are reported as in selective_scan_forward.
+ *   - The first call on each device looks up the array's device address (cudaGetSymbolAddress)
+ *     with that device current; make that first call before any stream capture.
+ *   - All calls on a device share the one array and it keeps the last call's contents.  Nothing
+ *     in it has to start at zero (every call writes its scratch before reading it), but calls
+ *     that can overlap on the GPU (different streams, or concurrent host threads) race on it and
+ *     must be serialised by the caller.
+ *   - It never calls cudaMalloc, cudaFree or any allocating routine.
+ */
+ssd_status selective_scan_forward_noalloc(const float* u, const float* delta, const float* A,
+                                          const float* B, const float* C, const float* skip,
+                                          float* y, int64_t batch, int64_t seqlen,
+                                          int64_t d_model, int64_t d_state, void* stream);
+
 /*
  * Reads (and clears) the device-side error word of a workspace after synchronising `stream`.
  * Returns SSD_OK, or SSD_ERR_TIMEOUT if a device wait of an earlier call on this workspace gave
