@@ -47,8 +47,19 @@ ssd_status check_shape(const ssd_shape* s) {
   return SSD_OK;
 }
 
+int32_t pick_variant(const ssd_shape* s) {
+  if (fused_bf16_supported(s->seqlen, s->nheads, s->headdim, s->dstate, s->mimo_rank,
+                           s->chunk_len, s->io_dtype == SSD_BF16, s->has_theta != 0))
+    return SSD_VARIANT_TC_BF16;
+  return SSD_VARIANT_GENERIC;
+}
+
 SsdLayout ssd_layout(const ssd_shape* s) {
   SsdLayout L;
+  if (pick_variant(s) == SSD_VARIANT_TC_BF16) {   // the fused kernel keeps its state on chip
+    L.total = sizeof(WsHeader);
+    return L;
+  }
   const int64_t nch = s->seqlen / s->chunk_len;
   size_t off = sizeof(WsHeader);
   L.states = off;
@@ -81,7 +92,7 @@ size_t ssd_chunked_workspace_bytes(const ssd_shape* shape) {
 
 int32_t ssd_chunked_variant(const ssd_shape* shape) {
   if (check_shape(shape) != SSD_OK) return SSD_VARIANT_NONE;
-  return SSD_VARIANT_GENERIC;
+  return pick_variant(shape);
 }
 
 ssd_status ssd_chunked_forward(const ssd_shape* shape, const void* x, const float* dA,
@@ -125,8 +136,12 @@ ssd_status ssd_chunked_forward(const ssd_shape* shape, const void* x, const floa
   p.phi = theta ? reinterpret_cast<double*>(ws + lay.phi) : nullptr;
   p.phisum = theta ? reinterpret_cast<double*>(ws + lay.phisum) : nullptr;
   p.hdr = reinterpret_cast<WsHeader*>(ws);
-  const cudaError_t e = generic_forward(p, shape->io_dtype == SSD_BF16,
-                                        static_cast<cudaStream_t>(stream));
+  cudaError_t e;
+  if (pick_variant(shape) == SSD_VARIANT_TC_BF16) {
+    e = fused_bf16_forward(p, static_cast<cudaStream_t>(stream));
+  } else {
+    e = generic_forward(p, shape->io_dtype == SSD_BF16, static_cast<cudaStream_t>(stream));
+  }
   return e == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
 }
 

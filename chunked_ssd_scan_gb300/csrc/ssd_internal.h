@@ -49,6 +49,11 @@ struct SelectiveScanParams {
 };
 
 int64_t ss_segment_length(int64_t T);
+
+// Fused tcgen05 kernel for bf16 I/O.
+bool fused_bf16_supported(int64_t T, int64_t H, int64_t P, int64_t N, int64_t R, int64_t l,
+                          bool bf16, bool theta);
+cudaError_t fused_bf16_forward(const GenericParams& p, cudaStream_t st);
 cudaError_t selective_scan_launch(const SelectiveScanParams& p, cudaStream_t st);
 
 }  // namespace ssd

@@ -64,7 +64,18 @@ EDGE = [
     wl.SSDConfig("shared_bc_theta_f32", 1, 512, 8, 16, 32, 128, 1, 1, "f32", theta=True),
     # largest tile shapes of the bf16 path with several chunks
     wl.SSDConfig("p128_n128_bf16", 1, 512, 2, 128, 128, 128, 1, 2, "bf16"),
+    # fused tensor-core path: one tile; rank 2 with 2 groups; rank 8 (16 steps per tile)
+    wl.SSDConfig("fused_one_tile", 1, 128, 4, 64, 128, 128, 1, 1, "bf16"),
+    wl.SSDConfig("fused_r2_g2", 2, 320, 8, 64, 128, 64, 2, 2, "bf16"),
+    wl.SSDConfig("fused_r8_g4", 1, 256, 4, 64, 128, 16, 8, 4, "bf16"),
 ]
+
+
+def test_bf16_workloads_use_the_fused_kernel():
+    for cfg in (wl.MAMBA2_SISO_BF16, wl.MAMBA3_MIMO_BF16, EDGE[-1], EDGE[-2], EDGE[-3]):
+        shape = pkg.make_shape(cfg.batch, cfg.seqlen, cfg.nheads, cfg.headdim, cfg.dstate,
+                               cfg.ngroups, cfg.mimo_rank, cfg.chunk_len, cfg.dtype, cfg.theta)
+        assert pkg.ssd_chunked_variant(shape) == "tc_bf16", cfg.name
 
 
 @pytest.mark.parametrize("cfg", EDGE, ids=lambda c: c.name)
