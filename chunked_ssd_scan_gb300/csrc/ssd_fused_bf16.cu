@@ -3,26 +3,35 @@
 // One CTA owns one (batch, head) sequence and walks it in tiles of 128 rank-fused rows
 // (fused row i = t*R + r, as in the serial.rs page's K2 reshape), carrying the state on chip
 // from tile to tile, so the inter-chunk state of K4 never goes to HBM.  Per tile:
-//   K1  tile-local inclusive cumsum of dA (fp64-accumulated, kept as hi+lo floats)
+//   K1  tile-local inclusive cumsum of dA (double-float), decay factors
 //   K2  CB = C B^T                                   tcgen05.mma  M128 N128 K128 -> TMEM
-//   K5a Mcb = (L o CB) with L[i,j] = exp(cum[i/R]-cum[j/R]) for j/R <= i/R, else 0
-//       (mask applied before the exponential; segsum.rs / scan.py pages), bf16 -> SMEM
-//       Yd = Mcb X                                   tcgen05.mma  M128 N64  K128 -> TMEM
-//   K3  S^T = (dec o B)^T X,  dec_i = exp(cum_last - cum[i/R])
-//                                                    tcgen05.mma  M128 N64  K128 -> TMEM
-//   K5b Yo = C h_in                                  tcgen05.mma  M128 N64  K128 -> TMEM
-//       y  = Yd + exp(cum[i/R]) Yo  -> bf16 -> global
+//   K5a (L o CB), L[i,j] = exp(cum[i/R] - cum[j/R]) for j/R <= i/R else 0, split into bf16
+//       hi + lo and written back to TMEM;  Yd = (L o CB) x     tcgen05.mma (A from TMEM)
+//   K3  S^T = B^T (dec o x), dec_i = exp(cum_last - cum[i/R]), (dec o x) split hi + lo
+//   K5b Yo = C h_in, h_in split hi + lo;  y = Yd + exp(cum[i/R]) Yo -> bf16 -> global
 //   K4  h_out = exp(cum_last) h_in + S               (fp32, in registers)
 // The serial.rs page runs K1..K5 per chunk with the K4 loop across chunks; a 128-row tile is a
 // sub-block of a chunk, and the part of a chunk's 1-semiseparable mask below a tile's diagonal
 // block has rank one (exp(cum_i - cum_j) = exp(cum_i) exp(-cum_j)), which is exactly what the
 // tile-boundary state carries.  The result is the same recurrence for every chunk_len.
+// Inside a tile the same structure is used once more: below the diagonal 32 x 32 blocks of L
+// are rank one, L[i,j] = exp(cum_i - cum_ref) exp(cum_ref - cum_j) with cum_ref taken at the
+// end of the column block, so only the diagonal blocks need one exponential per element.
 //
-// Warp roles (320 threads): warp 0 TMA producer, warp 1 MMA issuer (and TMEM owner),
-// warps 2-5 "mask group" (K1, mask, dec o B), warps 6-9 "state group" (K4, h_in for K5b,
-// output).  Operands are staged by TMA in 128-byte swizzled layouts; the two stages of x/B/C
-// are double-buffered.  Every wait is bounded; a wait that gives up latches SSD_ERR_TIMEOUT in
-// the workspace header and the CTA stops issuing work.
+// Operands that are products of inputs ((L o CB), dec o x and h_in) are carried as two bf16
+// terms (hi + lo, ~16 mantissa bits): one bf16 rounding of them is far too coarse for the
+// 2e-2 (1 + |y|) bound when decay is slow and y cancels.  Products of two bf16 inputs are exact
+// in the fp32 accumulators.
+//
+// Warp roles (352 threads):
+//   warp 0      TMA producer (x, B, C, dA tiles; two stages)
+//   warp 1      MMA issuer and TMEM owner; per tile: Yd_t, CB_{t+1}, Yo_t, K3_t
+//   warp 2      K1 for each tile as soon as its dA lands (runs ahead of the math warps)
+//   warps 3-10  math: two groups of four warps, each group covering all 128 TMEM lanes; the
+//               groups split every element-wise phase in halves (columns or P).  Per tile
+//               they run  dec o x (t), mask (t+1), output (t), state update (t).
+// Every wait is bounded; a wait that gives up latches SSD_ERR_TIMEOUT in the workspace header
+// and the CTA stops issuing work.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <math.h>
@@ -43,51 +52,54 @@ using namespace tc;
 constexpr int kTileRows = 128;
 constexpr int kP = 64;
 constexpr int kN = 128;
-constexpr int kThreadsFused = 320;
+constexpr int kThreadsFused = 352;
+constexpr int kMathWarps = 8;
 constexpr uint64_t kWaitNs = 2000000000ull;   // 2 s per wait before giving up
+constexpr float kLog2e = 1.4426950408889634f;
 
-// Shared-memory map (offsets from a 1024-aligned base).
+// Shared-memory map (offsets from the 1024-aligned dynamic shared window).
 constexpr uint32_t kXBytes = kTileRows * kP * 2;          // 16 KB per stage
 constexpr uint32_t kBCBytes = kTileRows * kN * 2;         // 32 KB per stage (two 64-col blocks)
-constexpr uint32_t kOffX = 0;                              // 2 stages (x, then dec o x hi part)
-constexpr uint32_t kOffXlo = kOffX + 2 * kXBytes;          // dec o x, lo part
+constexpr uint32_t kOffX = 0;                              // 2 stages (x, then (dec o x) hi)
+constexpr uint32_t kOffXlo = kOffX + 2 * kXBytes;          // (dec o x) lo
 constexpr uint32_t kOffB = kOffXlo + kXBytes;              // 2 stages
 constexpr uint32_t kOffC = kOffB + 2 * kBCBytes;           // 2 stages
-constexpr uint32_t kOffHhi = kOffC + 2 * kBCBytes;         // h_in, hi part  [N rows][P]
-constexpr uint32_t kOffHlo = kOffHhi + kN * kP * 2;        // h_in, lo part
-constexpr uint32_t kOffDA = kOffHlo + kN * kP * 2;         // 2 stages x 128 steps x 4 floats
-constexpr uint32_t kDABytes = kTileRows * 16;
-constexpr uint32_t kOffInfo = kOffDA + 2 * kDABytes;       // per-stage tile info
+constexpr uint32_t kOffHhi = kOffC + 2 * kBCBytes;         // h_in hi  [N rows][P]
+constexpr uint32_t kOffHlo = kOffHhi + kN * kP * 2;        // h_in lo
+constexpr int kInfoSlots = 4;                             // K1 runs up to this many tiles ahead
+constexpr uint32_t kOffInfo = kOffHlo + kN * kP * 2;       // ring of per-tile K1 results
 struct TileInfo {
-  float cum_hi[kTileRows];   // log2-scaled prefix sum of dA at fused row j (step j/R), hi part
-  float cum_lo[kTileRows];   // ... lo part (hi + lo carries ~48 bits)
-  float expcum[kTileRows];   // exp(cum) at fused row j
-  float dec[kTileRows];      // exp(cum_last - cum) at fused row j
+  float cum_hi[kTileRows];   // log2-scaled prefix sum of dA at fused row j (hi part)
+  float cum_lo[kTileRows];   // ... lo part
+  float qf[kTileRows];       // exp(cum_ref(block of j) - cum_j), cum_ref at the block's end
+  float last_hi, last_lo;    // log2-scaled total of the tile
   float etile;               // exp(cum_last)
-  float pad[31];
+  int monotone;              // 1 if every dA of the tile is <= 0 (factorized mask is safe)
+  float pad[28];
 };
-constexpr uint32_t kOffBar = kOffInfo + 2 * sizeof(TileInfo);
+constexpr uint32_t kOffBar = kOffInfo + kInfoSlots * sizeof(TileInfo);
 constexpr uint32_t kSmemUsed = kOffBar + 256;
 constexpr uint32_t kSmemAlloc = kSmemUsed;
 static_assert(kSmemAlloc <= 232448, "exceeds the 227 KB shared-memory limit per CTA");
 
 // TMEM columns (128 lanes x 512 columns of 32 bit).
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColCB = 0;      // CB fp32 [0,128); after masking, (L o CB) hi part packed
-                                    // two bf16 per column in [0,64)
-constexpr uint32_t kColMlo = 128;   // (L o CB) lo part, packed, [128,192)
-constexpr uint32_t kColYd = 192;    // Yd  [192,256)
+constexpr uint32_t kColCB = 0;      // CB fp32 [0,128); after masking, (L o CB) hi packed two
+                                    // bf16 per column in [0,64)
+constexpr uint32_t kColMlo = 128;   // (L o CB) lo, packed, [128,192)
+constexpr uint32_t kColYd = 192;    // Yd [192,256)
 constexpr uint32_t kColYo = 256;    // Yo from h_hi [256,320) and from h_lo [320,384)
 constexpr uint32_t kColS = 384;     // S^T from (dec o x)_hi [384,448) and _lo [448,512)
 
 struct Bars {
-  uint64_t full[2], empty[2], info_ready[2];
-  uint64_t cb_full, eg0_done, xs_ready, yd_full, yd_empty, yo_full, yo_empty, s_full, s_empty,
-      hb_full;
+  uint64_t full[2], empty[2], info_ready[kInfoSlots], info_empty[kInfoSlots];
+  uint64_t cb_full, cb_read, eg_done, xs_ready, yd_full, yd_empty, yo_full, yo_empty, s_full,
+      s_empty, hb_full;
 };
 static_assert(sizeof(Bars) + 8 <= 256, "barrier block");
 
 struct FusedArgs {
+  const float* dA;
   const float* init;
   float* final_state;
   __nv_bfloat16* y;
@@ -126,18 +138,15 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
 }
 
 __device__ __forceinline__ float2 unpack_bf16(uint32_t u) {
-  __nv_bfloat162 v = *reinterpret_cast<__nv_bfloat162*>(&u);
-  return __bfloat1622float2(v);
+  return make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xffff0000u));
 }
 
 // v = hi + lo with hi = bf16(v) and lo = bf16(v - hi): two bf16 terms carry ~16 mantissa bits.
 // Packs the pair (a, b) of each into one 32-bit word (a in the low half).
 __device__ __forceinline__ void split_pack(float a, float b, uint32_t& hi, uint32_t& lo) {
-  const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
-  const float2 hf = __bfloat1622float2(h);
-  const __nv_bfloat162 l = __floats2bfloat162_rn(a - hf.x, b - hf.y);
-  hi = *reinterpret_cast<const uint32_t*>(&h);
-  lo = *reinterpret_cast<const uint32_t*>(&l);
+  hi = pack_bf16(a, b);
+  const float2 hf = unpack_bf16(hi);
+  lo = pack_bf16(a - hf.x, b - hf.y);
 }
 
 // Double-float arithmetic (unevaluated sum hi + lo of two floats), from Knuth's TwoSum: the
@@ -161,12 +170,14 @@ __device__ __forceinline__ DF df_add(DF x, DF y) {
 __device__ __forceinline__ DF df_shfl_up(DF v, int off) {
   return {__shfl_up_sync(0xffffffffu, v.hi, off), __shfl_up_sync(0xffffffffu, v.lo, off)};
 }
+__device__ __forceinline__ DF df_shfl(DF v, int src) {
+  return {__shfl_sync(0xffffffffu, v.hi, src), __shfl_sync(0xffffffffu, v.lo, src)};
+}
 
 __global__ void __launch_bounds__(kThreadsFused, 1)
     ssd_fused_bf16_kernel(FusedArgs a, const __grid_constant__ CUtensorMap tm_x,
                           const __grid_constant__ CUtensorMap tm_b,
-                          const __grid_constant__ CUtensorMap tm_c,
-                          const __grid_constant__ CUtensorMap tm_da) {
+                          const __grid_constant__ CUtensorMap tm_c) {
   // The dynamic shared window is declared 1024-byte aligned (required by the 128-byte swizzle
   // atoms) and addressed directly, so every access stays a shared-memory access.
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -191,11 +202,15 @@ __global__ void __launch_bounds__(kThreadsFused, 1)
     s_abort = 0;
     for (int s = 0; s < 2; ++s) {
       mbar_init(&bars->full[s], 1);
-      mbar_init(&bars->empty[s], 5);        // MMA commit + the four state-group warps
-      mbar_init(&bars->info_ready[s], 1);
+      mbar_init(&bars->empty[s], 1);                // MMA commit after the stage's last MMA
+    }
+    for (int k = 0; k < kInfoSlots; ++k) {
+      mbar_init(&bars->info_ready[k], 1);
+      mbar_init(&bars->info_empty[k], 4);   // group B, after the tile's last use of its info
     }
     mbar_init(&bars->cb_full, 1);
-    mbar_init(&bars->eg0_done, 4);
+    mbar_init(&bars->cb_read, kMathWarps);
+    mbar_init(&bars->eg_done, kMathWarps);
     mbar_init(&bars->xs_ready, 4);
     mbar_init(&bars->yd_full, 1);
     mbar_init(&bars->yd_empty, 4);
@@ -210,7 +225,6 @@ __global__ void __launch_bounds__(kThreadsFused, 1)
     tma_prefetch_desc(&tm_x);
     tma_prefetch_desc(&tm_b);
     tma_prefetch_desc(&tm_c);
-    tma_prefetch_desc(&tm_da);
   }
   if (warp == 1) {
     tmem_alloc(&s_tmem, kTmemCols);
@@ -222,8 +236,8 @@ __global__ void __launch_bounds__(kThreadsFused, 1)
   const uint32_t tmem = s_tmem;
 
   if (warp == 0) {
-    // ------------------------------------------------------------------ TMA producer (warp)
-    const uint32_t tx = kXBytes + 2 * kBCBytes + 16u * steps;
+    // ------------------------------------------------------------------ TMA producer
+    const uint32_t tx = kXBytes + 2 * kBCBytes;
     for (int t = 0; t < nt; ++t) {
       const int s = t & 1;
       if (t >= 2 && !wait_bar(&bars->empty[s], ((t - 2) >> 1) & 1, abort, a.hdr, 1)) break;
@@ -236,11 +250,9 @@ __global__ void __launch_bounds__(kThreadsFused, 1)
       tma_load_3d_elect(smem + kOffC + s * kBCBytes, &tm_c, &bars->full[s], 0, g, row);
       tma_load_3d_elect(smem + kOffC + s * kBCBytes + kBCBytes / 2, &tm_c, &bars->full[s], 64, g,
                         row);
-      tma_load_2d_elect(smem + kOffDA + s * kDABytes, &tm_da, &bars->full[s], h & ~3,
-                        b * a.T + t * steps);
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------------ MMA issuer (warp)
+    // ------------------------------------------------------------------ MMA issuer
     // Per tile t the issue order is  Yd_t, CB_{t+1}, Yo_t, K3_t.  CB_{t+1} overwrites the TMEM
     // columns that Yd_t reads as its A operand; MMAs issued by one thread execute in order.
     const uint32_t id_cb = idesc_bf16(128, 128, 0, 0);
@@ -270,7 +282,7 @@ __global__ void __launch_bounds__(kThreadsFused, 1)
       const uint32_t sC = smem_u32(smem + kOffC + s * kBCBytes);
       const uint32_t sX = smem_u32(smem + kOffX + s * kXBytes);
       // Yd = (L o CB)_hi x + (L o CB)_lo x   (A from TMEM; K = 2 x 128)
-      if (!wait_bar(&bars->eg0_done, t & 1, abort, a.hdr, 3)) break;
+      if (!wait_bar(&bars->eg_done, t & 1, abort, a.hdr, 3)) break;
       if (t >= 1 && !wait_bar(&bars->yd_empty, (t - 1) & 1, abort, a.hdr, 4)) break;
       tc_fence_after();
 #pragma unroll
@@ -280,12 +292,13 @@ __global__ void __launch_bounds__(kThreadsFused, 1)
                           id_yd, ks > 0);
       }
       mma_commit_elect(&bars->yd_full);
-      // CB of the next tile
+      // CB of the next tile, before Yo_t if its operands have already landed
+      bool cb_done = true;
       if (t + 1 < nt) {
-        if (!wait_bar(&bars->full[(t + 1) & 1], ((t + 1) >> 1) & 1, abort, a.hdr, 5)) break;
-        issue_cb(t + 1);
+        cb_done = mbar_test_wait(&bars->full[(t + 1) & 1], ((t + 1) >> 1) & 1);
+        if (cb_done) issue_cb(t + 1);
       }
-      // Yo = C [h_hi | h_lo]   (N = 128: the two halves are summed by the state group)
+      // Yo = C [h_hi | h_lo]   (N = 128; the two halves are summed in the output step)
       if (!wait_bar(&bars->hb_full, t & 1, abort, a.hdr, 7)) break;
       if (t >= 1 && !wait_bar(&bars->yo_empty, (t - 1) & 1, abort, a.hdr, 8)) break;
       tc_fence_after();
@@ -296,6 +309,10 @@ __global__ void __launch_bounds__(kThreadsFused, 1)
                        sdesc_sw128(sHhi + ks * 2048, kOffHlo - kOffHhi, 1024), id_yo, ks > 0);
       }
       mma_commit_elect(&bars->yo_full);
+      if (!cb_done) {
+        if (!wait_bar(&bars->full[(t + 1) & 1], ((t + 1) >> 1) & 1, abort, a.hdr, 5)) break;
+        issue_cb(t + 1);
+      }
       // K3: S^T = B^T [(dec o x)_hi | (dec o x)_lo]   (A = B as MN-major: M = state index)
       if (!wait_bar(&bars->xs_ready, t & 1, abort, a.hdr, 10)) break;
       if (t >= 1 && !wait_bar(&bars->s_empty, (t - 1) & 1, abort, a.hdr, 6)) break;
@@ -309,208 +326,281 @@ __global__ void __launch_bounds__(kThreadsFused, 1)
       mma_commit_elect(&bars->s_full);
       if (t + 2 < nt) mma_commit_elect(&bars->empty[s]);
     }
-  } else if (warp < 6) {
-    // ------------------------------------------------------------------ mask group (warps 2-5)
-    const int q = warp & 3;                 // TMEM lane quarter
-    const int i = q * 32 + lane;            // tile row owned by this thread
-    const uint32_t lane_addr = static_cast<uint32_t>(q * 32) << 16;
+  } else if (warp == 2) {
+    // ------------------------------------------------------------------ K1 (one warp)
+    // Reads dA straight from global memory (one tile ahead, into registers) and publishes the
+    // tile's prefix sums and decay factors into a ring of kInfoSlots slots.
+    const int per = (steps + 31) / 32;                 // steps per lane (<= 4)
+    const int beg = min(steps, lane * per), end = min(steps, beg + per);
+    const float* dsrc = a.dA + (size_t)b * a.T * a.H + h;
+    float dnext[4];
+    auto load_tile = [&](int t) {
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        dnext[k] = (beg + k < end) ? __ldg(dsrc + (size_t)(t * steps + beg + k) * a.H) : 0.f;
+    };
+    load_tile(0);
     for (int t = 0; t < nt; ++t) {
-      const int s = t & 1;
-      if (!wait_bar(&bars->full[s], (t >> 1) & 1, abort, a.hdr, 11)) break;
-      TileInfo& ti = info[s];
-      // K1: tile-local inclusive cumsum of dA over `steps` time steps (warp 2 only), in
-      // double-float, stored per fused row (expanded over the R ranks of each step)
-      if (warp == 2) {
-        const float* dA = reinterpret_cast<const float*>(smem + kOffDA + s * kDABytes);
-        const int per = (steps + 31) / 32;
-        const int beg = min(steps, lane * per), end = min(steps, beg + per);
-        DF sum = {0.f, 0.f};
-        for (int k = beg; k < end; ++k) sum = df_add(sum, DF{dA[k * 4 + (h & 3)], 0.f});
-        DF incl = sum;
+      float dcur[4];
 #pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-          const DF v = df_shfl_up(incl, off);
-          if (lane >= off) incl = df_add(incl, v);
-        }
-        const DF last = {__shfl_sync(0xffffffffu, incl.hi, 31), __shfl_sync(0xffffffffu, incl.lo, 31)};
-        DF acc = df_shfl_up(incl, 1);   // exclusive prefix of this lane's first step
-        if (lane == 0) acc = DF{0.f, 0.f};
-        for (int k = beg; k < end; ++k) {
-          acc = df_add(acc, DF{dA[k * 4 + (h & 3)], 0.f});
-          const float c = acc.hi + acc.lo;
-          const float d = (last.hi - acc.hi) + (last.lo - acc.lo);
-          // log2-scaled copy for the mask: (hi, lo) * log2(e) as a double-float
-          const float l2e = 1.4426950408889634f;
-          const float chi = acc.hi * l2e;
-          const float clo = fmaf(acc.hi, l2e, -chi) + acc.lo * l2e;
-          const float ec = exp2f(c * l2e), ed = exp2f(d * l2e);
-          for (int r = 0; r < R; ++r) {
-            const int j = k * R + r;
-            ti.cum_hi[j] = chi;
-            ti.cum_lo[j] = clo;
-            ti.expcum[j] = ec;
-            ti.dec[j] = ed;
-          }
-        }
-        if (lane == 0) ti.etile = exp2f((last.hi + last.lo) * 1.4426950408889634f);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars->info_ready[s]);
-      } else if (!wait_bar(&bars->info_ready[s], (t >> 1) & 1, abort, a.hdr, 12)) {
-        break;
+      for (int k = 0; k < 4; ++k) dcur[k] = dnext[k];
+      if (t + 1 < nt) load_tile(t + 1);
+      DF sum = {0.f, 0.f};
+      int pos = 0;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        pos |= (dcur[k] > 0.f);
+        sum = df_add(sum, DF{dcur[k], 0.f});
       }
-      // mask: (L o CB)[i][j] = exp(cum[i/R] - cum[j/R]) CB[i][j] for j/R <= i/R, else 0,
-      // split into bf16 hi + lo and written back to TMEM as the A operand of Yd
-      if (!wait_bar(&bars->cb_full, t & 1, abort, a.hdr, 13)) break;
-      tc_fence_after();
-      // row i may see columns j < jlim (steps up to its own); the warp needs columns < ncols
-      const int jlim = (i / R + 1) * R;
-      const int ncols = min(kTileRows, ((q * 32 + 31) / R + 1) * R);
-      const float chi = ti.cum_hi[i], clo = ti.cum_lo[i];
-#pragma unroll 1
-      for (int h0 = 0; h0 < kTileRows; h0 += 32) {
-        float v[32];
-        if (h0 < ncols) {
-          tmem_ld32(tmem + lane_addr + kColCB + h0, v);
-          tmem_ld_wait();
-        }
+      DF incl = sum;
 #pragma unroll
-        for (int c = 0; c < 32; c += 16) {
-          const int c0 = h0 + c;
-          uint32_t hi[8], lo[8];
-          if (c0 >= ncols) {
+      for (int off = 1; off < 32; off <<= 1) {
+        const DF v = df_shfl_up(incl, off);
+        if (lane >= off) incl = df_add(incl, v);
+      }
+      const DF last = df_shfl(incl, 31);
+      DF acc = df_shfl_up(incl, 1);   // exclusive prefix of this lane's first step
+      if (lane == 0) acc = DF{0.f, 0.f};
+      const int monotone = __all_sync(0xffffffffu, pos == 0);
+      const int slot = t % kInfoSlots;
+      if (t >= kInfoSlots &&
+          !wait_bar(&bars->info_empty[slot], ((t - kInfoSlots) / kInfoSlots) & 1, abort, a.hdr, 11))
+        break;
+      TileInfo& ti = info[slot];
 #pragma unroll
-            for (int k = 0; k < 8; ++k) hi[k] = lo[k] = 0u;
-          } else {
-#pragma unroll
-            for (int k = 0; k < 16; k += 2) {
-              const int j = c0 + k;
-              const float2 ch = *reinterpret_cast<const float2*>(&ti.cum_hi[j]);
-              const float2 cl = *reinterpret_cast<const float2*>(&ti.cum_lo[j]);
-              // mask before the exponential: future columns get exponent -inf (-> 0)
-              const float e0 = (j < jlim) ? (chi - ch.x) + (clo - cl.x) : -INFINITY;
-              const float e1 = (j + 1 < jlim) ? (chi - ch.y) + (clo - cl.y) : -INFINITY;
-              split_pack(ex2_approx(e0) * v[c + k], ex2_approx(e1) * v[c + k + 1], hi[k / 2],
-                         lo[k / 2]);
-            }
+      for (int k = 0; k < 4; ++k) {
+        if (beg + k < end) {
+          acc = df_add(acc, DF{dcur[k], 0.f});
+          const float chi = acc.hi * kLog2e;
+          const float clo = fmaf(acc.hi, kLog2e, -chi) + acc.lo * kLog2e;
+          for (int r = 0; r < R; ++r) {
+            ti.cum_hi[(beg + k) * R + r] = chi;
+            ti.cum_lo[(beg + k) * R + r] = clo;
           }
-          // columns [c0/2, c0/2+8) were read in this or an earlier step: safe to overwrite
-          tmem_st8(tmem + lane_addr + kColCB + c0 / 2, hi);
-          tmem_st8(tmem + lane_addr + kColMlo + c0 / 2, lo);
         }
+      }
+      if (lane == 0) {
+        const float lhi = last.hi * kLog2e;
+        ti.last_hi = lhi;
+        ti.last_lo = fmaf(last.hi, kLog2e, -lhi) + last.lo * kLog2e;
+        ti.etile = ex2_approx(lhi + ti.last_lo);
+        ti.monotone = monotone;
+      }
+      __syncwarp();
+      // qf of the rank-one blocks: the reference of column block c is its last fused row
+#pragma unroll
+      for (int e = lane; e < kTileRows; e += 32) {
+        const int ref = (e >> 5) * 32 + 31;
+        ti.qf[e] = ex2_approx((ti.cum_hi[ref] - ti.cum_hi[e]) + (ti.cum_lo[ref] - ti.cum_lo[e]));
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->info_ready[slot]);
+    }
+  } else {
+    // ------------------------------------------------------------------ math warps (3-10)
+    // Two groups of four warps; each group covers all 128 TMEM lanes (warp w owns lanes of
+    // quarter w % 4, thread row i).  The mask of a tile is split between the groups by columns
+    // (group g takes the g-th 16 columns of every 32-column block).  Besides its half of the
+    // mask, group A splits dec o x; group B writes the output, updates the state and writes
+    // h_in.  Per tile t:  A: (dec o x)_t, mask_{t+1};  B: mask_{t+1}, output_t, K4_t, h_in(t+1).
+    const int q = warp & 3;                 // TMEM lane quarter
+    const int grp = (warp - 3) >> 2;        // 0: group A (warps 3-6), 1: group B (warps 7-10)
+    const int i = q * 32 + lane;            // tile row (and state row) owned by this thread
+    const uint32_t lane_addr = static_cast<uint32_t>(q * 32) << 16;
+    // this group's half of the mask of tile t for row i
+    auto do_mask = [&](int t) -> bool {
+      const int slot = t % kInfoSlots;
+      TileInfo& ti = info[slot];
+      if (!wait_bar(&bars->info_ready[slot], (t / kInfoSlots) & 1, abort, a.hdr, 12)) return false;
+      if (!wait_bar(&bars->cb_full, t & 1, abort, a.hdr, 13)) return false;
+      tc_fence_after();
+      const int jlim = (i / R + 1) * R;       // columns j < jlim are at or before row i's step
+      const bool fact = ti.monotone != 0;
+      const float chi = ti.cum_hi[i], clo = ti.cum_lo[i];
+      uint32_t hi[4][8], lo[4][8];
+      float v[2][16];
+      tmem_ld16(tmem + lane_addr + kColCB + grp * 16, v[0]);
+      tmem_ld_wait();
+      reg_tie(v[0]);
+#pragma unroll
+      for (int cb = 0; cb < 4; ++cb) {
+        const int c0 = cb * 32 + grp * 16;    // this thread's 16 columns of block cb
+        // prefetch the next block's columns while this one is processed
+        if (cb + 1 <= q) tmem_ld16(tmem + lane_addr + kColCB + c0 + 32, v[(cb + 1) & 1]);
+        const float* w = v[cb & 1];
+        if (cb > q) {                          // entirely above the diagonal (warp-uniform)
+#pragma unroll
+          for (int k = 0; k < 8; ++k) hi[cb][k] = lo[cb][k] = 0u;
+        } else if (cb < q && fact) {           // rank-one block strictly below the diagonal
+          const int ref = cb * 32 + 31;
+          const float r = ex2_approx((chi - ti.cum_hi[ref]) + (clo - ti.cum_lo[ref]));
+#pragma unroll
+          for (int k = 0; k < 16; k += 4) {
+            const float4 qq = *reinterpret_cast<const float4*>(&ti.qf[c0 + k]);
+            split_pack(w[k] * (qq.x * r), w[k + 1] * (qq.y * r), hi[cb][k / 2], lo[cb][k / 2]);
+            split_pack(w[k + 2] * (qq.z * r), w[k + 3] * (qq.w * r), hi[cb][k / 2 + 1],
+                       lo[cb][k / 2 + 1]);
+          }
+        } else {                               // diagonal block (or a non-monotone tile)
+#pragma unroll
+          for (int k = 0; k < 16; k += 2) {
+            const int j = c0 + k;
+            const float2 ch = *reinterpret_cast<const float2*>(&ti.cum_hi[j]);
+            const float2 cl = *reinterpret_cast<const float2*>(&ti.cum_lo[j]);
+            // mask before the exponential: future columns get exponent -inf (-> 0)
+            const float e0 = (j < jlim) ? (chi - ch.x) + (clo - cl.x) : -INFINITY;
+            const float e1 = (j + 1 < jlim) ? (chi - ch.y) + (clo - cl.y) : -INFINITY;
+            split_pack(ex2_approx(e0) * w[k], ex2_approx(e1) * w[k + 1], hi[cb][k / 2],
+                       lo[cb][k / 2]);
+          }
+        }
+        if (cb + 1 <= q) {
+          tmem_ld_wait();
+          reg_tie(v[(cb + 1) & 1]);
+        }
+      }
+      // all CB reads of both groups precede the in-place writes of the hi part
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->cb_read);
+      if (!wait_bar(&bars->cb_read, t & 1, abort, a.hdr, 15)) return false;
+      tc_fence_after();
+#pragma unroll
+      for (int cb = 0; cb < 4; ++cb) {
+        const int c0 = cb * 32 + grp * 16;
+        tmem_st8(tmem + lane_addr + kColCB + c0 / 2, hi[cb]);
+        tmem_st8(tmem + lane_addr + kColMlo + c0 / 2, lo[cb]);
       }
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->eg0_done);
-      // dec o x, split: hi in place of x (after Yd_t has read x), lo in its own buffer
-      if (!wait_bar(&bars->yd_full, t & 1, abort, a.hdr, 14)) break;
-      {
-        const float w = ti.dec[i];
-        uint8_t* xrow = smem + kOffX + s * kXBytes;
-        uint8_t* xlo = smem + kOffXlo;
+      if (lane == 0) mbar_arrive(&bars->eg_done);
+      return true;
+    };
+    if (grp == 0) {
+      // ---------------------------------------------------------------- group A
+      bool ok = do_mask(0);
+      for (int t = 0; ok && t < nt; ++t) {
+        const int s = t & 1;
+        TileInfo& ti = info[t % kInfoSlots];
+        // dec o x, split: hi in place of x (after Yd_t has read x), lo in its own buffer
+        if (!wait_bar(&bars->yd_full, t & 1, abort, a.hdr, 14)) break;
+        {
+          const float w = ex2_approx((ti.last_hi - ti.cum_hi[i]) + (ti.last_lo - ti.cum_lo[i]));
+          uint8_t* xrow = smem + kOffX + s * kXBytes;
+          uint8_t* xlo = smem + kOffXlo;
+          uint4 u[8];
+#pragma unroll
+          for (int ch = 0; ch < 8; ++ch) u[ch] = *reinterpret_cast<const uint4*>(xrow + sw128_off16(i, ch * 8));
+#pragma unroll
+          for (int ch = 0; ch < 8; ++ch) {
+            const uint32_t off = sw128_off16(i, ch * 8);
+            const float2 f0 = unpack_bf16(u[ch].x), f1 = unpack_bf16(u[ch].y),
+                         f2 = unpack_bf16(u[ch].z), f3 = unpack_bf16(u[ch].w);
+            uint4 uh, ul;
+            split_pack(f0.x * w, f0.y * w, uh.x, ul.x);
+            split_pack(f1.x * w, f1.y * w, uh.y, ul.y);
+            split_pack(f2.x * w, f2.y * w, uh.z, ul.z);
+            split_pack(f3.x * w, f3.y * w, uh.w, ul.w);
+            *reinterpret_cast<uint4*>(xrow + off) = uh;
+            *reinterpret_cast<uint4*>(xlo + off) = ul;
+          }
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->xs_ready);
+        if (t + 1 < nt && !do_mask(t + 1)) break;
+      }
+    } else {
+      // ---------------------------------------------------------------- group B
+      float hst[kP];                        // state row i
+      const size_t st_base = (size_t)seq * kP * kN;
+#pragma unroll
+      for (int p = 0; p < kP; ++p) hst[p] = a.init ? a.init[st_base + (size_t)p * kN + i] : 0.f;
+      uint8_t* hbhi = smem + kOffHhi;
+      uint8_t* hblo = smem + kOffHlo;
+      auto write_hb = [&]() {
 #pragma unroll
         for (int ch = 0; ch < 8; ++ch) {
-          const uint32_t off = sw128_off16(i, ch * 8);
-          uint4* p = reinterpret_cast<uint4*>(xrow + off);
-          const uint4 u = *p;
-          const float2 f0 = unpack_bf16(u.x), f1 = unpack_bf16(u.y), f2 = unpack_bf16(u.z),
-                       f3 = unpack_bf16(u.w);
           uint4 uh, ul;
-          split_pack(f0.x * w, f0.y * w, uh.x, ul.x);
-          split_pack(f1.x * w, f1.y * w, uh.y, ul.y);
-          split_pack(f2.x * w, f2.y * w, uh.z, ul.z);
-          split_pack(f3.x * w, f3.y * w, uh.w, ul.w);
-          *p = uh;
-          *reinterpret_cast<uint4*>(xlo + off) = ul;
+          split_pack(hst[ch * 8 + 0], hst[ch * 8 + 1], uh.x, ul.x);
+          split_pack(hst[ch * 8 + 2], hst[ch * 8 + 3], uh.y, ul.y);
+          split_pack(hst[ch * 8 + 4], hst[ch * 8 + 5], uh.z, ul.z);
+          split_pack(hst[ch * 8 + 6], hst[ch * 8 + 7], uh.w, ul.w);
+          const uint32_t off = sw128_off16(i, ch * 8);
+          *reinterpret_cast<uint4*>(hbhi + off) = uh;
+          *reinterpret_cast<uint4*>(hblo + off) = ul;
         }
-      }
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->xs_ready);
-    }
-  } else {
-    // ------------------------------------------------------------------ state group (warps 6-9)
-    const int q = warp & 3;
-    const int n = q * 32 + lane;            // state row (and output row) owned by this thread
-    const uint32_t lane_addr = static_cast<uint32_t>(q * 32) << 16;
-    float hst[kP];
-    const size_t st_base = (size_t)seq * kP * kN;
-#pragma unroll
-    for (int p = 0; p < kP; ++p) hst[p] = a.init ? a.init[st_base + (size_t)p * kN + n] : 0.f;
-    uint8_t* hbhi = smem + kOffHhi;
-    uint8_t* hblo = smem + kOffHlo;
-    auto write_hb = [&]() {
-#pragma unroll
-      for (int ch = 0; ch < 8; ++ch) {
-        uint4 uh, ul;
-        split_pack(hst[ch * 8 + 0], hst[ch * 8 + 1], uh.x, ul.x);
-        split_pack(hst[ch * 8 + 2], hst[ch * 8 + 3], uh.y, ul.y);
-        split_pack(hst[ch * 8 + 4], hst[ch * 8 + 5], uh.z, ul.z);
-        split_pack(hst[ch * 8 + 6], hst[ch * 8 + 7], uh.w, ul.w);
-        const uint32_t off = sw128_off16(n, ch * 8);
-        *reinterpret_cast<uint4*>(hbhi + off) = uh;
-        *reinterpret_cast<uint4*>(hblo + off) = ul;
-      }
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->hb_full);
-    };
-    write_hb();
-    for (int t = 0; t < nt; ++t) {
-      const int s = t & 1;
-      TileInfo& ti = info[s];
-      // output: y = Yd + exp(cum[i/R]) (Yo_hi + Yo_lo)
-      if (!wait_bar(&bars->yo_full, t & 1, abort, a.hdr, 21)) break;
-      if (!wait_bar(&bars->yd_full, t & 1, abort, a.hdr, 22)) break;
-      tc_fence_after();
-      const float sc = ti.expcum[n];
-      __nv_bfloat16* yrow = a.y + ((size_t)(row_base + t * kTileRows + n) * a.H + h) * kP;
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->hb_full);
+      };
+      write_hb();
+      bool ok = do_mask(0);
+      for (int t = 0; ok && t < nt; ++t) {
+        const int slot = t % kInfoSlots;
+        TileInfo& ti = info[slot];
+        if (t + 1 < nt && !do_mask(t + 1)) break;
+        // output: y = Yd + exp(cum[i/R]) (Yo_hi + Yo_lo)
+        if (!wait_bar(&bars->yo_full, t & 1, abort, a.hdr, 21)) break;
+        if (!wait_bar(&bars->yd_full, t & 1, abort, a.hdr, 22)) break;
+        tc_fence_after();
+        {
+          const float sc = ex2_approx(ti.cum_hi[i] + ti.cum_lo[i]);   // exp(cum_i)
+          __nv_bfloat16* yrow = a.y + ((size_t)(row_base + t * kTileRows + i) * a.H + h) * kP;
 #pragma unroll 1
-      for (int c = 0; c < kP; c += 16) {
-        float vd[16], vh[16], vl[16];
-        tmem_ld16(tmem + lane_addr + kColYd + c, vd);
-        tmem_ld16(tmem + lane_addr + kColYo + c, vh);
-        tmem_ld16(tmem + lane_addr + kColYo + 64 + c, vl);
-        tmem_ld_wait();
-        uint32_t pk[8];
+          for (int c = 0; c < kP; c += 16) {
+            float vd[16], vh[16], vl[16];
+            tmem_ld16(tmem + lane_addr + kColYd + c, vd);
+            tmem_ld16(tmem + lane_addr + kColYo + c, vh);
+            tmem_ld16(tmem + lane_addr + kColYo + 64 + c, vl);
+            tmem_ld_wait();
+            reg_tie(vd);
+            reg_tie(vh);
+            reg_tie(vl);
+            uint32_t pk[8];
 #pragma unroll
-        for (int k = 0; k < 8; ++k)
-          pk[k] = pack_bf16(fmaf(sc, vh[2 * k] + vl[2 * k], vd[2 * k]),
-                            fmaf(sc, vh[2 * k + 1] + vl[2 * k + 1], vd[2 * k + 1]));
-        uint4* dst = reinterpret_cast<uint4*>(yrow + c);
-        dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-        dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(&bars->yd_empty);
-        mbar_arrive(&bars->yo_empty);
-      }
-      // K4: h <- exp(cum_last) h + S_hi + S_lo
-      if (!wait_bar(&bars->s_full, t & 1, abort, a.hdr, 20)) break;
-      tc_fence_after();
-      const float e = ti.etile;
+            for (int k = 0; k < 8; ++k)
+              pk[k] = pack_bf16(fmaf(sc, vh[2 * k] + vl[2 * k], vd[2 * k]),
+                                fmaf(sc, vh[2 * k + 1] + vl[2 * k + 1], vd[2 * k + 1]));
+            uint4* dst = reinterpret_cast<uint4*>(yrow + c);
+            dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&bars->yd_empty);
+          mbar_arrive(&bars->yo_empty);
+        }
+        // K4: h <- exp(cum_last) h + S_hi + S_lo
+        if (!wait_bar(&bars->s_full, t & 1, abort, a.hdr, 20)) break;
+        tc_fence_after();
+        const float e = ti.etile;
 #pragma unroll
-      for (int c = 0; c < kP; c += 16) {
-        float sh[16], sl[16];
-        tmem_ld16(tmem + lane_addr + kColS + c, sh);
-        tmem_ld16(tmem + lane_addr + kColS + 64 + c, sl);
-        tmem_ld_wait();
+        for (int c = 0; c < kP; c += 16) {
+          float sh[16], sl[16];
+          tmem_ld16(tmem + lane_addr + kColS + c, sh);
+          tmem_ld16(tmem + lane_addr + kColS + 64 + c, sl);
+          tmem_ld_wait();
+          reg_tie(sh);
+          reg_tie(sl);
 #pragma unroll
-        for (int k = 0; k < 16; ++k) hst[c + k] = fmaf(e, hst[c + k], sh[k] + sl[k]);
+          for (int k = 0; k < 16; ++k) hst[c + k] = fmaf(e, hst[c + k], sh[k] + sl[k]);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&bars->s_empty);
+          mbar_arrive(&bars->info_empty[slot]);   // every use of this tile's info is done
+        }
+        if (t + 1 < nt) write_hb();   // Yo_t has already consumed h_in(t) (yo_full waited)
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(&bars->s_empty);
-        if (t + 2 < nt) mbar_arrive(&bars->empty[s]);
-      }
-      if (t + 1 < nt) write_hb();   // Yo_t has already consumed h_in(t) (yo_full waited above)
-    }
-    if (a.final_state && !*abort) {
+      if (a.final_state && !*abort) {
 #pragma unroll
-      for (int p = 0; p < kP; ++p) a.final_state[st_base + (size_t)p * kN + n] = hst[p];
+        for (int p = 0; p < kP; ++p) a.final_state[st_base + (size_t)p * kN + i] = hst[p];
+      }
     }
   }
 
@@ -562,7 +652,7 @@ bool fused_bf16_supported(int64_t T, int64_t H, int64_t P, int64_t N, int64_t R,
 
 cudaError_t fused_bf16_forward(const GenericParams& p, cudaStream_t st) {
   const int64_t rows = p.batch * p.T * p.R;
-  CUtensorMap mx, mb, mc, mda;
+  CUtensorMap mx, mb, mc;
   {
     cuuint64_t dims[3] = {(cuuint64_t)p.P, (cuuint64_t)p.H, (cuuint64_t)rows};
     cuuint64_t str[2] = {(cuuint64_t)p.P * 2, (cuuint64_t)p.H * p.P * 2};
@@ -583,15 +673,8 @@ cudaError_t fused_bf16_forward(const GenericParams& p, cudaStream_t st) {
       return cudaErrorInvalidValue;
   }
   const int steps = (int)(kTileRows / p.R);
-  {
-    cuuint64_t dims[2] = {(cuuint64_t)p.H, (cuuint64_t)(p.batch * p.T)};
-    cuuint64_t str[1] = {(cuuint64_t)p.H * 4};
-    cuuint32_t box[2] = {4, (cuuint32_t)steps};
-    if (!make_map(&mda, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, p.dA, dims, str, box,
-                  CU_TENSOR_MAP_SWIZZLE_NONE))
-      return cudaErrorInvalidValue;
-  }
   FusedArgs a;
+  a.dA = p.dA;
   a.init = p.init;
   a.final_state = p.final_state;
   a.y = static_cast<__nv_bfloat16*>(p.y);
@@ -606,7 +689,7 @@ cudaError_t fused_bf16_forward(const GenericParams& p, cudaStream_t st) {
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
   if (e != cudaSuccess) return e;
   ssd_fused_bf16_kernel<<<(unsigned)(p.batch * p.H), kThreadsFused, kSmemAlloc, st>>>(a, mx, mb,
-                                                                                     mc, mda);
+                                                                                     mc);
   return cudaGetLastError();
 }
 
