@@ -9,7 +9,8 @@
 //       hi + lo and written back to TMEM;  Yd = (L o CB) x     tcgen05.mma (A from TMEM)
 //   K3  S^T = B^T (dec o x), dec_i = exp(cum_last - cum[i/R]), (dec o x) split hi + lo
 //   K5b Yo = C h_in, h_in split hi + lo;  y = Yd + exp(cum[i/R]) Yo -> bf16 -> global
-//   K4  h_out = exp(cum_last) h_in + S               (fp32, in registers)
+//   K4  h_out = exp(cum_last) h_in + S^T: the K3 accumulator is preloaded with
+//       exp(cum_last) h_in, so the tensor core adds S^T onto the decayed state.
 // The serial.rs page runs K1..K5 per chunk with the K4 loop across chunks; a 128-row tile is a
 // sub-block of a chunk, and the part of a chunk's 1-semiseparable mask below a tile's diagonal
 // block has rank one (exp(cum_i - cum_j) = exp(cum_i) exp(-cum_j)), which is exactly what the
@@ -23,15 +24,19 @@
 // 2e-2 (1 + |y|) bound when decay is slow and y cancels.  Products of two bf16 inputs are exact
 // in the fp32 accumulators.
 //
-// Warp roles (352 threads):
-//   warp 0      TMA producer (x, B, C, dA tiles; two stages)
+// Warp roles (352 threads; TMEM lane quarter q = warp % 4 is the SM sub-partition):
+//   warp 0      TMA producer (x, B, C tiles; two stages)
 //   warp 1      MMA issuer and TMEM owner; per tile: Yd_t, CB_{t+1}, Yo_t, K3_t
 //   warp 2      K1 for each tile as soon as its dA lands (runs ahead of the math warps)
-//   warps 3-10  math: two groups of four warps, each group covering all 128 TMEM lanes; the
-//               groups split every element-wise phase in halves (columns or P).  Per tile
-//               they run  dec o x (t), mask (t+1), output (t), state update (t).
-// Every wait is bounded; a wait that gives up latches SSD_ERR_TIMEOUT in the workspace header
-// and the CTA stops issuing work.
+//   warps 3-6   "mask" warps, one per lane quarter q: (dec o x)_t for a share of the rows
+//               (larger shares on the quarters with less mask work), then the diagonal
+//               block q and the block q-1 of the mask of tile t+1
+//   warps 7-10  "state" warps, one per quarter: the mask blocks 0..q-2 of tile t+1, the output
+//               rows of quarter q of tile t, and state rows of quarter q (h_in split for Yo,
+//               decayed state preloaded into the K3 accumulator)
+// Each warp rewrites only TMEM columns that it has read itself, so the masked operand is
+// formed in place without a barrier between warps.  Every wait is bounded; a wait that gives
+// up latches SSD_ERR_TIMEOUT in the workspace header and the CTA stops issuing work.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <math.h>
@@ -53,7 +58,6 @@ constexpr int kTileRows = 128;
 constexpr int kP = 64;
 constexpr int kN = 128;
 constexpr int kThreadsFused = 352;
-constexpr int kMathWarps = 8;
 constexpr uint64_t kWaitNs = 2000000000ull;   // 2 s per wait before giving up
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -84,17 +88,24 @@ static_assert(kSmemAlloc <= 232448, "exceeds the 227 KB shared-memory limit per 
 
 // TMEM columns (128 lanes x 512 columns of 32 bit).
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColCB = 0;      // CB fp32 [0,128); after masking, (L o CB) hi packed two
-                                    // bf16 per column in [0,64)
-constexpr uint32_t kColMlo = 128;   // (L o CB) lo, packed, [128,192)
-constexpr uint32_t kColYd = 192;    // Yd [192,256)
-constexpr uint32_t kColYo = 256;    // Yo from h_hi [256,320) and from h_lo [320,384)
-constexpr uint32_t kColS = 384;     // S^T from (dec o x)_hi [384,448) and _lo [448,512)
+constexpr uint32_t kColM = 0;     // CB fp32 [0,128); each 32-column block cb is rewritten in
+                                  // place as 16 columns of (L o CB) hi then 16 columns of lo,
+                                  // two bf16 per column
+constexpr uint32_t kColYd = 128;  // Yd, two buffers: [128,192) and [192,256)
+constexpr uint32_t kColYo = 256;  // Yo from h_hi [256,320) and from h_lo [320,384)
+constexpr uint32_t kColS = 384;   // exp(cum_last) h_in + B^T (dec o x)_hi [384,448),
+                                  // B^T (dec o x)_lo [448,512)
+
+// (dec o x) work units (32 rows x 16 columns) per lane quarter: the quarters with fewer mask
+// blocks (and no other role on their sub-partition) take more.
+__device__ __forceinline__ int xs_unit_begin(int q) {
+  return q == 0 ? 0 : (q == 1 ? 7 : (q == 2 ? 12 : 13));
+}
+__device__ __forceinline__ int xs_unit_end(int q) { return q == 3 ? 16 : xs_unit_begin(q + 1); }
 
 struct Bars {
   uint64_t full[2], empty[2], info_ready[kInfoSlots], info_empty[kInfoSlots];
-  uint64_t cb_full, cb_read, eg_done, xs_ready, yd_full, yd_empty, yo_full, yo_empty, s_full,
-      s_empty, hb_full;
+  uint64_t cb_full, m_ready, yd_full, xs_ready, yo_full, s_full, hb_full;
 };
 static_assert(sizeof(Bars) + 8 <= 256, "barrier block");
 
@@ -141,12 +152,44 @@ __device__ __forceinline__ float2 unpack_bf16(uint32_t u) {
   return make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xffff0000u));
 }
 
+// Paired fp32 arithmetic (one instruction for two lanes of a float2, round to nearest).
+__device__ __forceinline__ uint64_t f2_bits(float2 v) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(v.x), "f"(v.y));
+  return r;
+}
+__device__ __forceinline__ float2 bits_f2(uint64_t r) {
+  float2 v;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(v.x), "=f"(v.y) : "l"(r));
+  return v;
+}
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(f2_bits(a)), "l"(f2_bits(b)));
+  return bits_f2(r);
+}
+__device__ __forceinline__ float2 add2(float2 a, float2 b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(f2_bits(a)), "l"(f2_bits(b)));
+  return bits_f2(r);
+}
+__device__ __forceinline__ float2 sub2(float2 a, float2 b) {
+  uint64_t r;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(f2_bits(a)), "l"(f2_bits(b)));
+  return bits_f2(r);
+}
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(f2_bits(a)), "l"(f2_bits(b)), "l"(f2_bits(c)));
+  return bits_f2(r);
+}
+
 // v = hi + lo with hi = bf16(v) and lo = bf16(v - hi): two bf16 terms carry ~16 mantissa bits.
-// Packs the pair (a, b) of each into one 32-bit word (a in the low half).
-__device__ __forceinline__ void split_pack(float a, float b, uint32_t& hi, uint32_t& lo) {
-  hi = pack_bf16(a, b);
-  const float2 hf = unpack_bf16(hi);
-  lo = pack_bf16(a - hf.x, b - hf.y);
+// Packs the pair (v.x, v.y) of each into one 32-bit word (v.x in the low half).
+__device__ __forceinline__ void split2(float2 v, uint32_t& hi, uint32_t& lo) {
+  hi = pack_bf16(v.x, v.y);
+  const float2 r = sub2(v, unpack_bf16(hi));
+  lo = pack_bf16(r.x, r.y);
 }
 
 // Double-float arithmetic (unevaluated sum hi + lo of two floats), from Knuth's TwoSum: the
@@ -174,6 +217,44 @@ __device__ __forceinline__ DF df_shfl(DF v, int src) {
   return {__shfl_sync(0xffffffffu, v.hi, src), __shfl_sync(0xffffffffu, v.lo, src)};
 }
 
+// One 32-column block cb of the masked operand for the calling thread's row (w = its CB
+// values): below the diagonal block and with a monotone tile the factorized form
+// exp(cum_i - cum_ref) * qf_j, else one exponential per element with the causal cut at jlim.
+__device__ __forceinline__ void mask_block(const TileInfo& ti, int cb, bool exact, float chi,
+                                           float clo, int jlim, const float (&w)[32],
+                                           uint32_t (&hi)[16], uint32_t (&lo)[16]) {
+  if (!exact) {
+    const int ref = cb * 32 + 31;
+    const float r = ex2_approx((chi - ti.cum_hi[ref]) + (clo - ti.cum_lo[ref]));
+    const float2 rr = make_float2(r, r);
+#pragma unroll
+    for (int k = 0; k < 32; k += 4) {
+      const float4 qq = *reinterpret_cast<const float4*>(&ti.qf[cb * 32 + k]);
+      split2(mul2(make_float2(w[k], w[k + 1]), mul2(make_float2(qq.x, qq.y), rr)), hi[k / 2],
+             lo[k / 2]);
+      split2(mul2(make_float2(w[k + 2], w[k + 3]), mul2(make_float2(qq.z, qq.w), rr)),
+             hi[k / 2 + 1], lo[k / 2 + 1]);
+    }
+  } else {
+    const float2 ch2 = make_float2(chi, chi), cl2 = make_float2(clo, clo);
+#pragma unroll
+    for (int k = 0; k < 32; k += 4) {
+      const int j = cb * 32 + k;
+      const float4 ch = *reinterpret_cast<const float4*>(&ti.cum_hi[j]);
+      const float4 cl = *reinterpret_cast<const float4*>(&ti.cum_lo[j]);
+      const float2 e0 = add2(sub2(ch2, make_float2(ch.x, ch.y)), sub2(cl2, make_float2(cl.x, cl.y)));
+      const float2 e1 = add2(sub2(ch2, make_float2(ch.z, ch.w)), sub2(cl2, make_float2(cl.z, cl.w)));
+      // future columns (j >= jlim) are cut after the exponential, which may overflow there
+      const float2 l0 = make_float2(j < jlim ? ex2_approx(e0.x) : 0.f,
+                                    j + 1 < jlim ? ex2_approx(e0.y) : 0.f);
+      const float2 l1 = make_float2(j + 2 < jlim ? ex2_approx(e1.x) : 0.f,
+                                    j + 3 < jlim ? ex2_approx(e1.y) : 0.f);
+      split2(mul2(make_float2(w[k], w[k + 1]), l0), hi[k / 2], lo[k / 2]);
+      split2(mul2(make_float2(w[k + 2], w[k + 3]), l1), hi[k / 2 + 1], lo[k / 2 + 1]);
+    }
+  }
+}
+
 __global__ void __launch_bounds__(kThreadsFused, 1)
     ssd_fused_bf16_kernel(FusedArgs a, const __grid_constant__ CUtensorMap tm_x,
                           const __grid_constant__ CUtensorMap tm_b,
@@ -190,7 +271,9 @@ __global__ void __launch_bounds__(kThreadsFused, 1)
     return;
   }
 
-  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  // warp index broadcast from lane 0: provably uniform, so role branches stay convergent
+  const int warp = __shfl_sync(0xffffffffu, static_cast<int>(threadIdx.x / 32), 0);
+  const int lane = threadIdx.x % 32;
   const int seq = blockIdx.x;                 // (b, h)
   const int b = seq / a.H, h = seq % a.H;
   const int g = h / (a.H / a.G);
@@ -206,18 +289,14 @@ __global__ void __launch_bounds__(kThreadsFused, 1)
     }
     for (int k = 0; k < kInfoSlots; ++k) {
       mbar_init(&bars->info_ready[k], 1);
-      mbar_init(&bars->info_empty[k], 4);   // group B, after the tile's last use of its info
+      mbar_init(&bars->info_empty[k], 4);   // state warps, after the tile's last use of its info
     }
     mbar_init(&bars->cb_full, 1);
-    mbar_init(&bars->cb_read, kMathWarps);
-    mbar_init(&bars->eg_done, kMathWarps);
-    mbar_init(&bars->xs_ready, 4);
+    mbar_init(&bars->m_ready, 6);            // 4 mask warps + the state warps of quarters 2, 3
     mbar_init(&bars->yd_full, 1);
-    mbar_init(&bars->yd_empty, 4);
+    mbar_init(&bars->xs_ready, 4);
     mbar_init(&bars->yo_full, 1);
-    mbar_init(&bars->yo_empty, 4);
     mbar_init(&bars->s_full, 1);
-    mbar_init(&bars->s_empty, 4);
     mbar_init(&bars->hb_full, 4);
     fence_mbar_init();
   }
@@ -255,6 +334,7 @@ __global__ void __launch_bounds__(kThreadsFused, 1)
     // ------------------------------------------------------------------ MMA issuer
     // Per tile t the issue order is  Yd_t, CB_{t+1}, Yo_t, K3_t.  CB_{t+1} overwrites the TMEM
     // columns that Yd_t reads as its A operand; MMAs issued by one thread execute in order.
+    // Every MMA loop is straight-line code (no branch between two MMAs).
     const uint32_t id_cb = idesc_bf16(128, 128, 0, 0);
     const uint32_t id_yd = idesc_bf16(128, 64, 0, 1);
     const uint32_t id_k3 = idesc_bf16(128, 128, 1, 1);
@@ -269,7 +349,7 @@ __global__ void __launch_bounds__(kThreadsFused, 1)
 #pragma unroll
       for (int ks = 0; ks < 8; ++ks) {
         const uint32_t off = (ks >> 2) * (kBCBytes / 2) + (ks & 3) * 32;
-        mma_bf16_elect(tmem + kColCB, sdesc_sw128(sC + off, 0, 1024),
+        mma_bf16_elect(tmem + kColM, sdesc_sw128(sC + off, 0, 1024),
                        sdesc_sw128(sB + off, 0, 1024), id_cb, ks > 0);
       }
       mma_commit_elect(&bars->cb_full);
@@ -281,26 +361,25 @@ __global__ void __launch_bounds__(kThreadsFused, 1)
       const uint32_t sB = smem_u32(smem + kOffB + s * kBCBytes);
       const uint32_t sC = smem_u32(smem + kOffC + s * kBCBytes);
       const uint32_t sX = smem_u32(smem + kOffX + s * kXBytes);
-      // Yd = (L o CB)_hi x + (L o CB)_lo x   (A from TMEM; K = 2 x 128)
-      if (!wait_bar(&bars->eg_done, t & 1, abort, a.hdr, 3)) break;
-      if (t >= 1 && !wait_bar(&bars->yd_empty, (t - 1) & 1, abort, a.hdr, 4)) break;
+      // Yd = (L o CB)_hi x + (L o CB)_lo x   (A from TMEM; K = 2 x 128).  Block cb of the
+      // operand holds hi in columns [32cb, 32cb+16) and lo in [32cb+16, 32cb+32).
+      if (!wait_bar(&bars->m_ready, t & 1, abort, a.hdr, 3)) break;
       tc_fence_after();
+      const uint32_t yd = tmem + kColYd + (t & 1) * 64;
 #pragma unroll
       for (int ks = 0; ks < 16; ++ks) {
-        const uint32_t acol = (ks < 8 ? kColCB : kColMlo) + (ks & 7) * 8;
-        mma_bf16_ts_elect(tmem + kColYd, tmem + acol, sdesc_sw128(sX + (ks & 7) * 2048, 0, 1024),
-                          id_yd, ks > 0);
+        const int kk = ks & 7;
+        const uint32_t acol = kColM + (kk >> 1) * 32 + (kk & 1) * 8 + (ks < 8 ? 0 : 16);
+        mma_bf16_ts_elect(yd, tmem + acol, sdesc_sw128(sX + kk * 2048, 0, 1024), id_yd, ks > 0);
       }
       mma_commit_elect(&bars->yd_full);
-      // CB of the next tile, before Yo_t if its operands have already landed
-      bool cb_done = true;
+      // CB of the next tile
       if (t + 1 < nt) {
-        cb_done = mbar_test_wait(&bars->full[(t + 1) & 1], ((t + 1) >> 1) & 1);
-        if (cb_done) issue_cb(t + 1);
+        if (!wait_bar(&bars->full[(t + 1) & 1], ((t + 1) >> 1) & 1, abort, a.hdr, 5)) break;
+        issue_cb(t + 1);
       }
       // Yo = C [h_hi | h_lo]   (N = 128; the two halves are summed in the output step)
       if (!wait_bar(&bars->hb_full, t & 1, abort, a.hdr, 7)) break;
-      if (t >= 1 && !wait_bar(&bars->yo_empty, (t - 1) & 1, abort, a.hdr, 8)) break;
       tc_fence_after();
 #pragma unroll
       for (int ks = 0; ks < 8; ++ks) {
@@ -309,19 +388,15 @@ __global__ void __launch_bounds__(kThreadsFused, 1)
                        sdesc_sw128(sHhi + ks * 2048, kOffHlo - kOffHhi, 1024), id_yo, ks > 0);
       }
       mma_commit_elect(&bars->yo_full);
-      if (!cb_done) {
-        if (!wait_bar(&bars->full[(t + 1) & 1], ((t + 1) >> 1) & 1, abort, a.hdr, 5)) break;
-        issue_cb(t + 1);
-      }
-      // K3: S^T = B^T [(dec o x)_hi | (dec o x)_lo]   (A = B as MN-major: M = state index)
+      // K3: S^T += B^T [(dec o x)_hi | (dec o x)_lo]   (A = B as MN-major: M = state index);
+      // the accumulator holds [exp(cum_last) h_in | 0] written by the state warps
       if (!wait_bar(&bars->xs_ready, t & 1, abort, a.hdr, 10)) break;
-      if (t >= 1 && !wait_bar(&bars->s_empty, (t - 1) & 1, abort, a.hdr, 6)) break;
       tc_fence_after();
       const uint32_t lbo_x = sXlo - sX;   // distance from the hi block (in place of x) to lo
 #pragma unroll
       for (int ks = 0; ks < 8; ++ks) {
         mma_bf16_elect(tmem + kColS, sdesc_sw128(sB + ks * 2048, kBCBytes / 2, 1024),
-                       sdesc_sw128(sX + ks * 2048, lbo_x, 1024), id_k3, ks > 0);
+                       sdesc_sw128(sX + ks * 2048, lbo_x, 1024), id_k3, 1);
       }
       mma_commit_elect(&bars->s_full);
       if (t + 2 < nt) mma_commit_elect(&bars->empty[s]);
@@ -398,208 +473,231 @@ __global__ void __launch_bounds__(kThreadsFused, 1)
     }
   } else {
     // ------------------------------------------------------------------ math warps (3-10)
-    // Two groups of four warps; each group covers all 128 TMEM lanes (warp w owns lanes of
-    // quarter w % 4, thread row i).  The mask of a tile is split between the groups by columns
-    // (group g takes the g-th 16 columns of every 32-column block).  Besides its half of the
-    // mask, group A splits dec o x; group B writes the output, updates the state and writes
-    // h_in.  Per tile t:  A: (dec o x)_t, mask_{t+1};  B: mask_{t+1}, output_t, K4_t, h_in(t+1).
-    const int q = warp & 3;                 // TMEM lane quarter
-    const int grp = (warp - 3) >> 2;        // 0: group A (warps 3-6), 1: group B (warps 7-10)
+    const int q = warp & 3;                 // TMEM lane quarter == SM sub-partition
+    const bool mask_role = warp < 7;        // warps 3-6: mask warps; 7-10: state warps
     const int i = q * 32 + lane;            // tile row (and state row) owned by this thread
     const uint32_t lane_addr = static_cast<uint32_t>(q * 32) << 16;
-    // this group's half of the mask of tile t for row i
-    auto do_mask = [&](int t) -> bool {
+    const int jlim = (i / R + 1) * R;       // columns j < jlim are at or before row i's step
+    // Mask blocks [cb0, cb1) of tile t for this thread's row, in place; blocks [cb1, zero_end)
+    // are above the diagonal and set to zero.  Waits for the tile's info and CB.
+    auto mask_part = [&](int t, int cb0, int cb1, int zero_end) -> bool {
       const int slot = t % kInfoSlots;
-      TileInfo& ti = info[slot];
+      const TileInfo& ti = info[slot];
       if (!wait_bar(&bars->info_ready[slot], (t / kInfoSlots) & 1, abort, a.hdr, 12)) return false;
       if (!wait_bar(&bars->cb_full, t & 1, abort, a.hdr, 13)) return false;
       tc_fence_after();
-      const int jlim = (i / R + 1) * R;       // columns j < jlim are at or before row i's step
-      const bool fact = ti.monotone != 0;
+      const bool fact_ok = ti.monotone != 0;
       const float chi = ti.cum_hi[i], clo = ti.cum_lo[i];
-      uint32_t hi[4][8], lo[4][8];
-      float v[2][16];
-      tmem_ld16(tmem + lane_addr + kColCB + grp * 16, v[0]);
-      tmem_ld_wait();
-      reg_tie(v[0]);
-#pragma unroll
-      for (int cb = 0; cb < 4; ++cb) {
-        const int c0 = cb * 32 + grp * 16;    // this thread's 16 columns of block cb
-        // prefetch the next block's columns while this one is processed
-        if (cb + 1 <= q) tmem_ld16(tmem + lane_addr + kColCB + c0 + 32, v[(cb + 1) & 1]);
-        const float* w = v[cb & 1];
-        if (cb > q) {                          // entirely above the diagonal (warp-uniform)
-#pragma unroll
-          for (int k = 0; k < 8; ++k) hi[cb][k] = lo[cb][k] = 0u;
-        } else if (cb < q && fact) {           // rank-one block strictly below the diagonal
-          const int ref = cb * 32 + 31;
-          const float r = ex2_approx((chi - ti.cum_hi[ref]) + (clo - ti.cum_lo[ref]));
-#pragma unroll
-          for (int k = 0; k < 16; k += 4) {
-            const float4 qq = *reinterpret_cast<const float4*>(&ti.qf[c0 + k]);
-            split_pack(w[k] * (qq.x * r), w[k + 1] * (qq.y * r), hi[cb][k / 2], lo[cb][k / 2]);
-            split_pack(w[k + 2] * (qq.z * r), w[k + 3] * (qq.w * r), hi[cb][k / 2 + 1],
-                       lo[cb][k / 2 + 1]);
-          }
-        } else {                               // diagonal block (or a non-monotone tile)
-#pragma unroll
-          for (int k = 0; k < 16; k += 2) {
-            const int j = c0 + k;
-            const float2 ch = *reinterpret_cast<const float2*>(&ti.cum_hi[j]);
-            const float2 cl = *reinterpret_cast<const float2*>(&ti.cum_lo[j]);
-            // mask before the exponential: future columns get exponent -inf (-> 0)
-            const float e0 = (j < jlim) ? (chi - ch.x) + (clo - cl.x) : -INFINITY;
-            const float e1 = (j + 1 < jlim) ? (chi - ch.y) + (clo - cl.y) : -INFINITY;
-            split_pack(ex2_approx(e0) * w[k], ex2_approx(e1) * w[k + 1], hi[cb][k / 2],
-                       lo[cb][k / 2]);
-          }
-        }
-        if (cb + 1 <= q) {
-          tmem_ld_wait();
-          reg_tie(v[(cb + 1) & 1]);
-        }
+#pragma unroll 1
+      for (int cb = cb0; cb < cb1; ++cb) {
+        float w[32];
+        tmem_ld32(tmem + lane_addr + kColM + cb * 32, w);
+        tmem_ld_wait();
+        reg_tie(w);
+        uint32_t hi[16], lo[16];
+        mask_block(ti, cb, cb == q || !fact_ok, chi, clo, jlim, w, hi, lo);
+        tmem_st16u(tmem + lane_addr + kColM + cb * 32, hi);
+        tmem_st16u(tmem + lane_addr + kColM + cb * 32 + 16, lo);
       }
-      // all CB reads of both groups precede the in-place writes of the hi part
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->cb_read);
-      if (!wait_bar(&bars->cb_read, t & 1, abort, a.hdr, 15)) return false;
-      tc_fence_after();
+      if (cb1 < zero_end) {
+        uint32_t z[16];
 #pragma unroll
-      for (int cb = 0; cb < 4; ++cb) {
-        const int c0 = cb * 32 + grp * 16;
-        tmem_st8(tmem + lane_addr + kColCB + c0 / 2, hi[cb]);
-        tmem_st8(tmem + lane_addr + kColMlo + c0 / 2, lo[cb]);
+        for (int k = 0; k < 16; ++k) z[k] = 0u;
+#pragma unroll 1
+        for (int cb = cb1; cb < zero_end; ++cb) {
+          tmem_st16u(tmem + lane_addr + kColM + cb * 32, z);
+          tmem_st16u(tmem + lane_addr + kColM + cb * 32 + 16, z);
+        }
       }
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->eg_done);
+      if (lane == 0) mbar_arrive(&bars->m_ready);
       return true;
     };
-    if (grp == 0) {
-      // ---------------------------------------------------------------- group A
-      bool ok = do_mask(0);
-      for (int t = 0; ok && t < nt; ++t) {
-        const int s = t & 1;
-        TileInfo& ti = info[t % kInfoSlots];
-        // dec o x, split: hi in place of x (after Yd_t has read x), lo in its own buffer
-        if (!wait_bar(&bars->yd_full, t & 1, abort, a.hdr, 14)) break;
-        {
-          const float w = ex2_approx((ti.last_hi - ti.cum_hi[i]) + (ti.last_lo - ti.cum_lo[i]));
-          uint8_t* xrow = smem + kOffX + s * kXBytes;
-          uint8_t* xlo = smem + kOffXlo;
-          uint4 u[8];
-#pragma unroll
-          for (int ch = 0; ch < 8; ++ch) u[ch] = *reinterpret_cast<const uint4*>(xrow + sw128_off16(i, ch * 8));
-#pragma unroll
-          for (int ch = 0; ch < 8; ++ch) {
-            const uint32_t off = sw128_off16(i, ch * 8);
-            const float2 f0 = unpack_bf16(u[ch].x), f1 = unpack_bf16(u[ch].y),
-                         f2 = unpack_bf16(u[ch].z), f3 = unpack_bf16(u[ch].w);
-            uint4 uh, ul;
-            split_pack(f0.x * w, f0.y * w, uh.x, ul.x);
-            split_pack(f1.x * w, f1.y * w, uh.y, ul.y);
-            split_pack(f2.x * w, f2.y * w, uh.z, ul.z);
-            split_pack(f3.x * w, f3.y * w, uh.w, ul.w);
-            *reinterpret_cast<uint4*>(xrow + off) = uh;
-            *reinterpret_cast<uint4*>(xlo + off) = ul;
-          }
+    if (mask_role) {
+      // ---------------------------------------------------------------- mask warps
+      // mask blocks max(q-1, 0) .. q (the diagonal block is exact), zero blocks q+1 .. 3
+      const int cb0 = q >= 1 ? q - 1 : 0;
+      const int ub = xs_unit_begin(q), ue = xs_unit_end(q);
+      uint8_t* xlo = smem + kOffXlo;
+      // (dec o x) of tile t, split: hi in place of x (after Yd_t has read x), lo in its own
+      // buffer; this warp's units of 32 rows x 16 columns
+      auto scale_x = [&](int t) -> bool {
+        const TileInfo& ti = info[t % kInfoSlots];
+        if (!wait_bar(&bars->yd_full, t & 1, abort, a.hdr, 14)) return false;
+        uint8_t* xs = smem + kOffX + (t & 1) * kXBytes;
+#pragma unroll 1
+        for (int u = ub; u < ue; ++u) {
+          const int row = (u >> 2) * 32 + lane, c0 = (u & 3) * 16;
+          const float wd =
+              ex2_approx((ti.last_hi - ti.cum_hi[row]) + (ti.last_lo - ti.cum_lo[row]));
+          const float2 w2 = make_float2(wd, wd);
+          const uint32_t o0 = sw128_off16(row, c0), o1 = sw128_off16(row, c0 + 8);
+          const uint4 v0 = *reinterpret_cast<const uint4*>(xs + o0);
+          const uint4 v1 = *reinterpret_cast<const uint4*>(xs + o1);
+          uint4 h0, l0, h1, l1;
+          split2(mul2(unpack_bf16(v0.x), w2), h0.x, l0.x);
+          split2(mul2(unpack_bf16(v0.y), w2), h0.y, l0.y);
+          split2(mul2(unpack_bf16(v0.z), w2), h0.z, l0.z);
+          split2(mul2(unpack_bf16(v0.w), w2), h0.w, l0.w);
+          split2(mul2(unpack_bf16(v1.x), w2), h1.x, l1.x);
+          split2(mul2(unpack_bf16(v1.y), w2), h1.y, l1.y);
+          split2(mul2(unpack_bf16(v1.z), w2), h1.z, l1.z);
+          split2(mul2(unpack_bf16(v1.w), w2), h1.w, l1.w);
+          *reinterpret_cast<uint4*>(xs + o0) = h0;
+          *reinterpret_cast<uint4*>(xs + o1) = h1;
+          *reinterpret_cast<uint4*>(xlo + o0) = l0;
+          *reinterpret_cast<uint4*>(xlo + o1) = l1;
         }
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars->xs_ready);
-        if (t + 1 < nt && !do_mask(t + 1)) break;
+        return true;
+      };
+      // one loop with one call site per phase (t = -1 only masks tile 0)
+      for (int t = -1; t < nt; ++t) {
+        if (t >= 0 && !scale_x(t)) break;
+        if (t + 1 < nt && !mask_part(t + 1, cb0, q + 1, 4)) break;
       }
     } else {
-      // ---------------------------------------------------------------- group B
-      float hst[kP];                        // state row i
+      // ---------------------------------------------------------------- state warps
+      // state row n = i: h_in split into [h_hi | h_lo] for Yo, exp(cum_last) h_in preloaded
+      // into the K3 accumulator (lo half zeroed); output rows i of every tile.
       const size_t st_base = (size_t)seq * kP * kN;
-#pragma unroll
-      for (int p = 0; p < kP; ++p) hst[p] = a.init ? a.init[st_base + (size_t)p * kN + i] : 0.f;
       uint8_t* hbhi = smem + kOffHhi;
       uint8_t* hblo = smem + kOffHlo;
-      auto write_hb = [&]() {
+      // writes h (32 values of columns [c0, c0+32) of state row i) to the Yo operand and the
+      // decayed copy e*h into the K3 accumulator
+      auto put_state = [&](int c0, const float (&hv)[32], float e) {
+        float eh[32];
 #pragma unroll
-        for (int ch = 0; ch < 8; ++ch) {
+        for (int k = 0; k < 32; k += 8) {
           uint4 uh, ul;
-          split_pack(hst[ch * 8 + 0], hst[ch * 8 + 1], uh.x, ul.x);
-          split_pack(hst[ch * 8 + 2], hst[ch * 8 + 3], uh.y, ul.y);
-          split_pack(hst[ch * 8 + 4], hst[ch * 8 + 5], uh.z, ul.z);
-          split_pack(hst[ch * 8 + 6], hst[ch * 8 + 7], uh.w, ul.w);
-          const uint32_t off = sw128_off16(i, ch * 8);
+          split2(make_float2(hv[k], hv[k + 1]), uh.x, ul.x);
+          split2(make_float2(hv[k + 2], hv[k + 3]), uh.y, ul.y);
+          split2(make_float2(hv[k + 4], hv[k + 5]), uh.z, ul.z);
+          split2(make_float2(hv[k + 6], hv[k + 7]), uh.w, ul.w);
+          const uint32_t off = sw128_off16(i, c0 + k);
           *reinterpret_cast<uint4*>(hbhi + off) = uh;
           *reinterpret_cast<uint4*>(hblo + off) = ul;
         }
+        const float2 e2 = make_float2(e, e);
+#pragma unroll
+        for (int k = 0; k < 32; k += 2) {
+          const float2 v = mul2(make_float2(hv[k], hv[k + 1]), e2);
+          eh[k] = v.x;
+          eh[k + 1] = v.y;
+        }
+        float z[16];
+#pragma unroll
+        for (int k = 0; k < 16; ++k) z[k] = 0.f;
+        float e0[16], e1[16];
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+          e0[k] = eh[k];
+          e1[k] = eh[16 + k];
+        }
+        tmem_st16(tmem + lane_addr + kColS + c0, e0);
+        tmem_st16(tmem + lane_addr + kColS + c0 + 16, e1);
+        tmem_st16(tmem + lane_addr + kColS + 64 + c0, z);
+        tmem_st16(tmem + lane_addr + kColS + 64 + c0 + 16, z);
+      };
+      auto publish_state = [&]() {
+        tmem_st_wait();
         fence_proxy_async_smem();
+        tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars->hb_full);
       };
-      write_hb();
-      bool ok = do_mask(0);
-      for (int t = 0; ok && t < nt; ++t) {
+      bool ok = wait_bar(&bars->info_ready[0], 0, abort, a.hdr, 16);
+      if (ok) {
+        const float e0 = info[0].etile;
+#pragma unroll 1
+        for (int c0 = 0; c0 < kP; c0 += 32) {
+          float hv[32];
+#pragma unroll
+          for (int k = 0; k < 32; ++k)
+            hv[k] = a.init ? a.init[st_base + (size_t)(c0 + k) * kN + i] : 0.f;
+          put_state(c0, hv, e0);
+        }
+        publish_state();
+      }
+      for (int t = -1; ok && t < nt; ++t) {
+        if (q >= 2 && t + 1 < nt && !mask_part(t + 1, 0, q - 1, q - 1)) break;
+        if (t < 0) continue;
         const int slot = t % kInfoSlots;
-        TileInfo& ti = info[slot];
-        if (t + 1 < nt && !do_mask(t + 1)) break;
+        const TileInfo& ti = info[slot];
+        const bool next = t + 1 < nt;
         // output: y = Yd + exp(cum[i/R]) (Yo_hi + Yo_lo)
         if (!wait_bar(&bars->yo_full, t & 1, abort, a.hdr, 21)) break;
-        if (!wait_bar(&bars->yd_full, t & 1, abort, a.hdr, 22)) break;
         tc_fence_after();
         {
           const float sc = ex2_approx(ti.cum_hi[i] + ti.cum_lo[i]);   // exp(cum_i)
+          const float2 sc2 = make_float2(sc, sc);
           __nv_bfloat16* yrow = a.y + ((size_t)(row_base + t * kTileRows + i) * a.H + h) * kP;
+          const uint32_t yd = tmem + lane_addr + kColYd + (t & 1) * 64;
 #pragma unroll 1
-          for (int c = 0; c < kP; c += 16) {
-            float vd[16], vh[16], vl[16];
-            tmem_ld16(tmem + lane_addr + kColYd + c, vd);
-            tmem_ld16(tmem + lane_addr + kColYo + c, vh);
-            tmem_ld16(tmem + lane_addr + kColYo + 64 + c, vl);
+          for (int c = 0; c < kP; c += 32) {
+            float vd[32], vh[32], vl[32];
+            tmem_ld32(yd + c, vd);
+            tmem_ld32(tmem + lane_addr + kColYo + c, vh);
+            tmem_ld32(tmem + lane_addr + kColYo + 64 + c, vl);
             tmem_ld_wait();
             reg_tie(vd);
             reg_tie(vh);
             reg_tie(vl);
-            uint32_t pk[8];
+            uint32_t pk[16];
 #pragma unroll
-            for (int k = 0; k < 8; ++k)
-              pk[k] = pack_bf16(fmaf(sc, vh[2 * k] + vl[2 * k], vd[2 * k]),
-                                fmaf(sc, vh[2 * k + 1] + vl[2 * k + 1], vd[2 * k + 1]));
+            for (int k = 0; k < 16; ++k) {
+              const float2 o = fma2(sc2, add2(make_float2(vh[2 * k], vh[2 * k + 1]),
+                                              make_float2(vl[2 * k], vl[2 * k + 1])),
+                                    make_float2(vd[2 * k], vd[2 * k + 1]));
+              pk[k] = pack_bf16(o.x, o.y);
+            }
             uint4* dst = reinterpret_cast<uint4*>(yrow + c);
             dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
             dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+            dst[2] = make_uint4(pk[8], pk[9], pk[10], pk[11]);
+            dst[3] = make_uint4(pk[12], pk[13], pk[14], pk[15]);
           }
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(&bars->yd_empty);
-          mbar_arrive(&bars->yo_empty);
-        }
-        // K4: h <- exp(cum_last) h + S_hi + S_lo
+        // K4: h_in(t+1) = S_hi + S_lo (the accumulator already holds the decayed h_in(t))
         if (!wait_bar(&bars->s_full, t & 1, abort, a.hdr, 20)) break;
+        float enext = 0.f;
+        if (next) {
+          const int ns = (t + 1) % kInfoSlots;
+          if (!wait_bar(&bars->info_ready[ns], ((t + 1) / kInfoSlots) & 1, abort, a.hdr, 17))
+            break;
+          enext = info[ns].etile;
+        }
         tc_fence_after();
-        const float e = ti.etile;
-#pragma unroll
-        for (int c = 0; c < kP; c += 16) {
-          float sh[16], sl[16];
-          tmem_ld16(tmem + lane_addr + kColS + c, sh);
-          tmem_ld16(tmem + lane_addr + kColS + 64 + c, sl);
+#pragma unroll 1
+        for (int c0 = 0; c0 < kP; c0 += 32) {
+          float sh[32], sl[32];
+          tmem_ld32(tmem + lane_addr + kColS + c0, sh);
+          tmem_ld32(tmem + lane_addr + kColS + 64 + c0, sl);
           tmem_ld_wait();
           reg_tie(sh);
           reg_tie(sl);
+          float hv[32];
 #pragma unroll
-          for (int k = 0; k < 16; ++k) hst[c + k] = fmaf(e, hst[c + k], sh[k] + sl[k]);
+          for (int k = 0; k < 32; k += 2) {
+            const float2 v = add2(make_float2(sh[k], sh[k + 1]), make_float2(sl[k], sl[k + 1]));
+            hv[k] = v.x;
+            hv[k + 1] = v.y;
+          }
+          if (next) {
+            put_state(c0, hv, enext);
+          } else if (a.final_state) {
+#pragma unroll
+            for (int k = 0; k < 32; ++k) a.final_state[st_base + (size_t)(c0 + k) * kN + i] = hv[k];
+          }
         }
+        if (next) publish_state();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(&bars->s_empty);
-          mbar_arrive(&bars->info_empty[slot]);   // every use of this tile's info is done
-        }
-        if (t + 1 < nt) write_hb();   // Yo_t has already consumed h_in(t) (yo_full waited)
-      }
-      if (a.final_state && !*abort) {
-#pragma unroll
-        for (int p = 0; p < kP; ++p) a.final_state[st_base + (size_t)p * kN + i] = hst[p];
+        if (lane == 0) mbar_arrive(&bars->info_empty[slot]);   // last use of this tile's info
       }
     }
   }
