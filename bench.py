@@ -175,8 +175,9 @@ def run_ours(args, rank, world, local):
         ws = torch.empty(pkg.selective_scan_workspace_bytes(cfg.batch, cfg.seqlen, cfg.d_model,
                                                             cfg.d_state), dtype=torch.uint8,
                          device=dev)
-        fn = lambda: pkg.selective_scan_forward(d["u"], d["delta"], d["A"], d["B"], d["C"],
-                                                d["skip"], y=y, workspace=ws)
+        # validated once; each step is only the C-ABI call
+        fn = pkg.SelectiveScanPlan(d["u"], d["delta"], d["A"], d["B"], d["C"], d["skip"], y=y,
+                                   workspace=ws, stream=stream)
         launches_per_call = 3
         variant = "selective_scan"
         dtype = "f32"
@@ -190,10 +191,10 @@ def run_ours(args, rank, world, local):
                           device=dev)
         shape = pkg.shape_of(d["x"], d["B"], cfg.chunk_len, cfg.theta)
         ws = torch.empty(pkg.ssd_chunked_workspace_bytes(shape), dtype=torch.uint8, device=dev)
-        fn = lambda: pkg.ssd_chunked_forward(d["x"], d["dA"], d["B"], d["C"],
-                                             chunk_len=cfg.chunk_len, theta=d["theta"],
-                                             init_state=d["init_state"], y=y, final_state=fin,
-                                             workspace=ws)
+        # validated once; each step is only the C-ABI call
+        fn = pkg.SSDForwardPlan(d["x"], d["dA"], d["B"], d["C"], chunk_len=cfg.chunk_len,
+                                theta=d["theta"], init_state=d["init_state"], y=y,
+                                final_state=fin, workspace=ws, stream=stream)
         variant = pkg.ssd_chunked_variant(shape)
         launches_per_call = {"generic": 3 + (2 if cfg.theta else 0)}.get(variant, 1)
         dtype = cfg.dtype

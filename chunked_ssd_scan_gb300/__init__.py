@@ -17,7 +17,7 @@ from . import workloads  # noqa: F401  (seeded synthetic inputs; no scan arithme
 
 __all__ = [
     "SSDError", "load_library", "ssd_shape", "ssd_chunked_workspace_bytes", "ssd_chunked_variant",
-    "ssd_chunked_forward", "selective_scan_workspace_bytes", "selective_scan_forward",
+    "ssd_chunked_forward", "SSDForwardPlan", "SelectiveScanPlan", "selective_scan_workspace_bytes", "selective_scan_forward",
     "workspace_status", "STATUS", "VARIANTS",
 ]
 
@@ -125,6 +125,61 @@ def shape_of(x: torch.Tensor, B: torch.Tensor, chunk_len: int, has_theta: bool) 
     return make_shape(b, T, H, P, N, G, R, chunk_len, x.dtype, has_theta)
 
 
+class SSDForwardPlan:
+    """Arguments of ``ssd_chunked_forward`` validated once, for repeated calls on the same
+    buffers.  Calling the plan makes only the C call (on the stream given here, or the stream
+    that is current at construction).  Shapes and dtypes are those of ``ssd_chunked_forward``.
+    """
+
+    def __init__(self, x: torch.Tensor, dA: torch.Tensor, B: torch.Tensor, C: torch.Tensor, *,
+                 chunk_len: int, theta: Optional[torch.Tensor] = None,
+                 init_state: Optional[torch.Tensor] = None, y: Optional[torch.Tensor] = None,
+                 final_state: Optional[torch.Tensor] = None, return_final_state: bool = True,
+                 workspace: Optional[torch.Tensor] = None, stream=None):
+        if x.dim() != 5 or B.dim() != 5:
+            raise ValueError("x must be [b,T,R,H,P] and B/C [b,T,R,G,N]")
+        b, T, R, H, P = x.shape
+        G, N = B.shape[3], B.shape[4]
+        _check_cuda("x", x)
+        if x.dtype not in (torch.float32, torch.bfloat16):
+            raise ValueError("x/B/C must be float32 or bfloat16")
+        _check_cuda("B", B, x.dtype, (b, T, R, G, N))
+        _check_cuda("C", C, x.dtype, (b, T, R, G, N))
+        _check_cuda("dA", dA, torch.float32, (b, T, H))
+        if theta is not None:
+            _check_cuda("theta", theta, torch.float32, (b, T, H, N // 2))
+        if init_state is not None:
+            _check_cuda("init_state", init_state, torch.float32, (b, H, P, N))
+        self.shape = shape_of(x, B, chunk_len, theta is not None)
+        self._lib = load_library()
+        if y is None:
+            y = torch.empty_like(x)
+        _check_cuda("y", y, x.dtype, x.shape)
+        if final_state is None and return_final_state:
+            final_state = torch.empty((b, H, P, N), dtype=torch.float32, device=x.device)
+        if final_state is not None:
+            _check_cuda("final_state", final_state, torch.float32, (b, H, P, N))
+        need = int(self._lib.ssd_chunked_workspace_bytes(ctypes.byref(self.shape)))
+        if need == 0:
+            raise SSDError(2, "ssd_chunked_workspace_bytes (shape not supported)")
+        if workspace is None:
+            workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
+        _check_cuda("workspace", workspace, torch.uint8)
+        # keep every buffer alive as long as the plan
+        self.inputs = (x, dA, B, C, theta, init_state)
+        self.y, self.final_state, self.workspace = y, final_state, workspace
+        self._args = (ctypes.byref(self.shape), _ptr(x), _ptr(dA), _ptr(B), _ptr(C), _ptr(theta),
+                      _ptr(init_state), _ptr(y), _ptr(final_state), _ptr(workspace),
+                      ctypes.c_size_t(workspace.numel()), _stream_handle(stream))
+        self._fn = self._lib.ssd_chunked_forward
+
+    def __call__(self):
+        st = self._fn(*self._args)
+        if st != 0:
+            raise SSDError(st, "ssd_chunked_forward")
+        return self.y, self.final_state
+
+
 def ssd_chunked_forward(x: torch.Tensor, dA: torch.Tensor, B: torch.Tensor, C: torch.Tensor, *,
                         chunk_len: int, theta: Optional[torch.Tensor] = None,
                         init_state: Optional[torch.Tensor] = None,
@@ -137,76 +192,57 @@ def ssd_chunked_forward(x: torch.Tensor, dA: torch.Tensor, B: torch.Tensor, C: t
     x [b,T,R,H,P], B/C [b,T,R,G,N] (all f32 or all bf16), dA [b,T,H] f32, theta [b,T,H,N/2] f32,
     init_state [b,H,P,N] f32.  Returns (y, final_state) (final_state None if not requested).
     """
-    if x.dim() != 5 or B.dim() != 5:
-        raise ValueError("x must be [b,T,R,H,P] and B/C [b,T,R,G,N]")
-    b, T, R, H, P = x.shape
-    G, N = B.shape[3], B.shape[4]
-    _check_cuda("x", x)
-    if x.dtype not in (torch.float32, torch.bfloat16):
-        raise ValueError("x/B/C must be float32 or bfloat16")
-    _check_cuda("B", B, x.dtype, (b, T, R, G, N))
-    _check_cuda("C", C, x.dtype, (b, T, R, G, N))
-    _check_cuda("dA", dA, torch.float32, (b, T, H))
-    if theta is not None:
-        _check_cuda("theta", theta, torch.float32, (b, T, H, N // 2))
-    if init_state is not None:
-        _check_cuda("init_state", init_state, torch.float32, (b, H, P, N))
-    shape = shape_of(x, B, chunk_len, theta is not None)
-    lib = load_library()
-    if y is None:
-        y = torch.empty_like(x)
-    _check_cuda("y", y, x.dtype, x.shape)
-    if final_state is None and return_final_state:
-        final_state = torch.empty((b, H, P, N), dtype=torch.float32, device=x.device)
-    if final_state is not None:
-        _check_cuda("final_state", final_state, torch.float32, (b, H, P, N))
-    need = int(lib.ssd_chunked_workspace_bytes(ctypes.byref(shape)))
-    if need == 0:
-        raise SSDError(2, "ssd_chunked_workspace_bytes (shape not supported)")
-    if workspace is None:
-        workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
-    _check_cuda("workspace", workspace, torch.uint8)
-    st = lib.ssd_chunked_forward(ctypes.byref(shape), _ptr(x), _ptr(dA), _ptr(B), _ptr(C),
-                                 _ptr(theta), _ptr(init_state), _ptr(y), _ptr(final_state),
-                                 _ptr(workspace), ctypes.c_size_t(workspace.numel()),
-                                 _stream_handle(stream))
-    if st != 0:
-        raise SSDError(st, "ssd_chunked_forward")
-    return y, final_state
+    return SSDForwardPlan(x, dA, B, C, chunk_len=chunk_len, theta=theta, init_state=init_state,
+                          y=y, final_state=final_state, return_final_state=return_final_state,
+                          workspace=workspace, stream=stream)()
 
 
 def selective_scan_workspace_bytes(batch, seqlen, d_model, d_state) -> int:
     return int(load_library().selective_scan_workspace_bytes(batch, seqlen, d_model, d_state))
 
 
+class SelectiveScanPlan:
+    """Arguments of ``selective_scan_forward`` validated once, for repeated calls on the same
+    buffers; calling the plan makes only the C call (stream fixed at construction)."""
+
+    def __init__(self, u, delta, A, B, C, skip=None, *, y=None, workspace=None, stream=None):
+        b, T, D = u.shape
+        N = A.shape[1]
+        f32 = torch.float32
+        _check_cuda("u", u, f32)
+        _check_cuda("delta", delta, f32, (b, T, D))
+        _check_cuda("A", A, f32, (D, N))
+        _check_cuda("B", B, f32, (b, T, N))
+        _check_cuda("C", C, f32, (b, T, N))
+        if skip is not None:
+            _check_cuda("skip", skip, f32, (D,))
+        self._lib = load_library()
+        if y is None:
+            y = torch.empty_like(u)
+        _check_cuda("y", y, f32, (b, T, D))
+        need = int(self._lib.selective_scan_workspace_bytes(b, T, D, N))
+        if need == 0:
+            raise SSDError(2, "selective_scan_workspace_bytes (sizes not supported)")
+        if workspace is None:
+            workspace = torch.empty(need, dtype=torch.uint8, device=u.device)
+        _check_cuda("workspace", workspace, torch.uint8)
+        self.inputs = (u, delta, A, B, C, skip)
+        self.y, self.workspace = y, workspace
+        self._args = (_ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(skip), _ptr(y), b, T,
+                      D, N, _ptr(workspace), ctypes.c_size_t(workspace.numel()),
+                      _stream_handle(stream))
+        self._fn = self._lib.selective_scan_forward
+
+    def __call__(self):
+        st = self._fn(*self._args)
+        if st != 0:
+            raise SSDError(st, "selective_scan_forward")
+        return self.y
+
+
 def selective_scan_forward(u, delta, A, B, C, skip=None, *, y=None, workspace=None, stream=None):
     """Diagonal-A selective scan through ``selective_scan_forward`` (all f32).  Returns y."""
-    b, T, D = u.shape
-    N = A.shape[1]
-    f32 = torch.float32
-    _check_cuda("u", u, f32)
-    _check_cuda("delta", delta, f32, (b, T, D))
-    _check_cuda("A", A, f32, (D, N))
-    _check_cuda("B", B, f32, (b, T, N))
-    _check_cuda("C", C, f32, (b, T, N))
-    if skip is not None:
-        _check_cuda("skip", skip, f32, (D,))
-    lib = load_library()
-    if y is None:
-        y = torch.empty_like(u)
-    _check_cuda("y", y, f32, (b, T, D))
-    need = int(lib.selective_scan_workspace_bytes(b, T, D, N))
-    if need == 0:
-        raise SSDError(2, "selective_scan_workspace_bytes (sizes not supported)")
-    if workspace is None:
-        workspace = torch.empty(need, dtype=torch.uint8, device=u.device)
-    _check_cuda("workspace", workspace, torch.uint8)
-    st = lib.selective_scan_forward(_ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(skip),
-                                    _ptr(y), b, T, D, N, _ptr(workspace),
-                                    ctypes.c_size_t(workspace.numel()), _stream_handle(stream))
-    if st != 0:
-        raise SSDError(st, "selective_scan_forward")
-    return y
+    return SelectiveScanPlan(u, delta, A, B, C, skip, y=y, workspace=workspace, stream=stream)()
 
 
 def workspace_status(workspace: torch.Tensor, stream=None):

@@ -42,6 +42,7 @@
 #include <math.h>
 #include <string.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "common.cuh"
@@ -735,6 +736,71 @@ bool make_map(CUtensorMap* m, CUtensorMapDataType dt, uint32_t rank, const void*
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Encoded tensor maps of the last few distinct (pointers, shape) keys per host thread: a call
+// with the same buffers skips the three encodes.
+struct MapKey {
+  const void *x, *B, *C;
+  int64_t batch, T, H, G, R, P, N;
+  bool operator==(const MapKey& o) const {
+    return x == o.x && B == o.B && C == o.C && batch == o.batch && T == o.T && H == o.H &&
+           G == o.G && R == o.R && P == o.P && N == o.N;
+  }
+};
+struct MapEntry {
+  MapKey key;
+  CUtensorMap mx, mb, mc;
+  bool valid = false;
+};
+constexpr int kMapCacheSize = 4;
+
+bool encode_maps(const GenericParams& p, MapEntry& m) {
+  const int64_t rows = p.batch * p.T * p.R;
+  {
+    cuuint64_t dims[3] = {(cuuint64_t)p.P, (cuuint64_t)p.H, (cuuint64_t)rows};
+    cuuint64_t str[2] = {(cuuint64_t)p.P * 2, (cuuint64_t)p.H * p.P * 2};
+    cuuint32_t box[3] = {64, 1, kTileRows};
+    if (!make_map(&m.mx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, p.x, dims, str, box,
+                  CU_TENSOR_MAP_SWIZZLE_128B))
+      return false;
+  }
+  cuuint64_t dims[3] = {(cuuint64_t)p.N, (cuuint64_t)p.G, (cuuint64_t)rows};
+  cuuint64_t str[2] = {(cuuint64_t)p.N * 2, (cuuint64_t)p.G * p.N * 2};
+  cuuint32_t box[3] = {64, 1, kTileRows};
+  return make_map(&m.mb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, p.B, dims, str, box,
+                  CU_TENSOR_MAP_SWIZZLE_128B) &&
+         make_map(&m.mc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, p.C, dims, str, box,
+                  CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+const MapEntry* cached_maps(const GenericParams& p) {
+  thread_local MapEntry cache[kMapCacheSize];
+  thread_local int next = 0;
+  const MapKey key{p.x, p.B, p.C, p.batch, p.T, p.H, p.G, p.R, p.P, p.N};
+  for (auto& m : cache)
+    if (m.valid && m.key == key) return &m;
+  MapEntry& m = cache[next];
+  next = (next + 1) % kMapCacheSize;
+  m.valid = false;
+  if (!encode_maps(p, m)) return nullptr;
+  m.key = key;
+  m.valid = true;
+  return &m;
+}
+
+// The kernel's dynamic shared-memory limit is raised once per device.
+cudaError_t ensure_smem_attribute() {
+  static std::atomic<uint64_t> done{0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = dev < 64 ? (1ull << dev) : 0ull;
+  if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+  e = cudaFuncSetAttribute(ssd_fused_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           kSmemAlloc);
+  if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_acq_rel);
+  return e;
+}
+
 }  // namespace
 
 bool fused_bf16_supported(int64_t T, int64_t H, int64_t P, int64_t N, int64_t R, int64_t l,
@@ -749,27 +815,8 @@ bool fused_bf16_supported(int64_t T, int64_t H, int64_t P, int64_t N, int64_t R,
 }
 
 cudaError_t fused_bf16_forward(const GenericParams& p, cudaStream_t st) {
-  const int64_t rows = p.batch * p.T * p.R;
-  CUtensorMap mx, mb, mc;
-  {
-    cuuint64_t dims[3] = {(cuuint64_t)p.P, (cuuint64_t)p.H, (cuuint64_t)rows};
-    cuuint64_t str[2] = {(cuuint64_t)p.P * 2, (cuuint64_t)p.H * p.P * 2};
-    cuuint32_t box[3] = {64, 1, kTileRows};
-    if (!make_map(&mx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, p.x, dims, str, box,
-                  CU_TENSOR_MAP_SWIZZLE_128B))
-      return cudaErrorInvalidValue;
-  }
-  {
-    cuuint64_t dims[3] = {(cuuint64_t)p.N, (cuuint64_t)p.G, (cuuint64_t)rows};
-    cuuint64_t str[2] = {(cuuint64_t)p.N * 2, (cuuint64_t)p.G * p.N * 2};
-    cuuint32_t box[3] = {64, 1, kTileRows};
-    if (!make_map(&mb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, p.B, dims, str, box,
-                  CU_TENSOR_MAP_SWIZZLE_128B))
-      return cudaErrorInvalidValue;
-    if (!make_map(&mc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, p.C, dims, str, box,
-                  CU_TENSOR_MAP_SWIZZLE_128B))
-      return cudaErrorInvalidValue;
-  }
+  const MapEntry* m = cached_maps(p);
+  if (!m) return cudaErrorInvalidValue;
   const int steps = (int)(kTileRows / p.R);
   FusedArgs a;
   a.dA = p.dA;
@@ -783,11 +830,10 @@ cudaError_t fused_bf16_forward(const GenericParams& p, cudaStream_t st) {
   a.G = (int32_t)p.G;
   a.ntiles = (int32_t)(p.T * p.R / kTileRows);
   a.steps = steps;
-  cudaError_t e = cudaFuncSetAttribute(ssd_fused_bf16_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
+  cudaError_t e = ensure_smem_attribute();
   if (e != cudaSuccess) return e;
-  ssd_fused_bf16_kernel<<<(unsigned)(p.batch * p.H), kThreadsFused, kSmemAlloc, st>>>(a, mx, mb,
-                                                                                     mc);
+  ssd_fused_bf16_kernel<<<(unsigned)(p.batch * p.H), kThreadsFused, kSmemAlloc, st>>>(
+      a, m->mx, m->mb, m->mc);
   return cudaGetLastError();
 }
 
