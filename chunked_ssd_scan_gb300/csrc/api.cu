@@ -195,7 +195,9 @@ ssd_status selective_scan_forward(const float* u, const float* delta, const floa
   off = align_up(off + sizeof(float) * (size_t)(batch * p.nseg * d_state * d_model), kWsAlign);
   p.agg_dt = reinterpret_cast<float*>(ws + off);
   p.hdr = reinterpret_cast<WsHeader*>(ws);
-  const cudaError_t e = selective_scan_launch(p, static_cast<cudaStream_t>(stream));
+  const cudaError_t e = selective_scan_onepass_supported(batch, d_model, d_state)
+                            ? selective_scan_onepass_launch(p, static_cast<cudaStream_t>(stream))
+                            : selective_scan_launch(p, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
 }
 

@@ -112,9 +112,206 @@ cudaError_t launch_nb(const SelectiveScanParams& p, cudaStream_t st) {
   return cudaGetLastError();
 }
 
+// ------------------------------------------------------------------------------------------------
+// One-pass selective scan for d_state N = 2 * LPC in {8, 16, 32, 64} and d_model % 4 == 0.
+// A warp owns 32 / LPC channels d of one batch row; the LPC lanes of a channel each carry two
+// of its N states through the whole sequence, so every exp(delta * A) is evaluated exactly
+// once (2^x on the special-function unit with A pre-scaled by log2 e) and no segment state
+// goes to memory.  Every LPC steps the lanes of a channel sum their C . h partials with a
+// transpose-reduce (log2 LPC shuffle levels), after which lane l holds y of step t0 + l.
+// The block's delta, u, B and C rows are staged through shared memory in a ring of
+// kSsStages stages of kSsSteps steps (16-byte cp.async, zero-filled past T and D), so loads
+// run several stages ahead of the serial recurrence.
+// ------------------------------------------------------------------------------------------------
+constexpr int kSsWarps = 4;
+constexpr int kSsSteps = 64;
+constexpr int kSsStages = 4;
+
+__device__ __forceinline__ float ss_ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Paired fp32 arithmetic (one instruction for both lanes of a float2, round to nearest).
+__device__ __forceinline__ uint64_t ss_bits(float2 v) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(v.x), "f"(v.y));
+  return r;
+}
+__device__ __forceinline__ float2 ss_f2(uint64_t r) {
+  float2 v;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(v.x), "=f"(v.y) : "l"(r));
+  return v;
+}
+__device__ __forceinline__ float2 ss_mul2(float2 a, float2 b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(ss_bits(a)), "l"(ss_bits(b)));
+  return ss_f2(r);
+}
+__device__ __forceinline__ float2 ss_fma2(float2 a, float2 b, float2 c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(ss_bits(a)), "l"(ss_bits(b)), "l"(ss_bits(c)));
+  return ss_f2(r);
+}
+
+// 16-byte global->shared copy; src_bytes 0 writes zeros without reading.
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, int src_bytes) {
+  const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(dst));
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(d), "l"(src), "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+template <int LPC>
+struct SsLayout {
+  static constexpr int kN = 2 * LPC;
+  static constexpr int kCpw = 32 / LPC;                  // channels per warp
+  static constexpr int kCpb = kCpw * kSsWarps;           // channels per block
+  static constexpr int kDtFloats = kSsSteps * kCpb;
+  static constexpr int kBFloats = kSsSteps * kN;
+  static constexpr int kStageFloats = 2 * kDtFloats + 2 * kBFloats;
+  static constexpr size_t kSmemBytes = sizeof(float) * kStageFloats * kSsStages;
+};
+
+template <int LPC>
+__global__ void __launch_bounds__(32 * kSsWarps) ss_onepass_kernel(SelectiveScanParams p) {
+  using Lay = SsLayout<LPC>;
+  constexpr int kN = Lay::kN, kCpb = Lay::kCpb;
+  extern __shared__ __align__(16) float ss_sm[];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int64_t groups = (p.D + kCpb - 1) / kCpb;
+  const int64_t b = blockIdx.x / groups;
+  const int64_t d0 = (blockIdx.x % groups) * kCpb;
+  const int cl = warp * Lay::kCpw + lane / LPC;         // channel within the block
+  const int64_t d = d0 + cl;
+  const int l = lane % LPC;                              // this lane carries states 2l, 2l+1
+  const bool dv = d < p.D;
+  const int64_t dd = dv ? d : 0;
+  const float kLog2e = 1.4426950408889634f;
+  const float a0 = dv ? p.A[dd * kN + 2 * l] * kLog2e : 0.f;
+  const float a1 = dv ? p.A[dd * kN + 2 * l + 1] * kLog2e : 0.f;
+  const float sk = (dv && l == 0 && p.skip) ? p.skip[dd] : 0.f;   // skip term added once
+  const int64_t T = p.T, D = p.D;
+  const int64_t nst = (T + kSsSteps - 1) / kSsSteps;
+
+  auto issue = [&](int64_t st) {
+    float* sm = ss_sm + (st % kSsStages) * Lay::kStageFloats;
+    const int64_t t0 = st * kSsSteps;
+    constexpr int kDtChunks = kSsSteps * kCpb / 4, kBChunks = kSsSteps * kN / 4;
+    for (int c = threadIdx.x; c < kDtChunks; c += 32 * kSsWarps) {
+      const int k = c / (kCpb / 4), q = c % (kCpb / 4);
+      const int64_t t = t0 + k, dc = d0 + 4 * q;
+      const bool ok = t < T && dc < D;
+      const int64_t off = ok ? (b * T + t) * D + dc : 0;
+      cp_async16(sm + k * kCpb + 4 * q, p.delta + off, ok ? 16 : 0);
+      cp_async16(sm + Lay::kDtFloats + k * kCpb + 4 * q, p.u + off, ok ? 16 : 0);
+    }
+    for (int c = threadIdx.x; c < kBChunks; c += 32 * kSsWarps) {
+      const int k = c / (kN / 4), q = c % (kN / 4);
+      const int64_t t = t0 + k;
+      const bool ok = t < T;
+      const int64_t off = ok ? (b * T + t) * kN + 4 * q : 0;
+      cp_async16(sm + 2 * Lay::kDtFloats + k * kN + 4 * q, p.B + off, ok ? 16 : 0);
+      cp_async16(sm + 2 * Lay::kDtFloats + Lay::kBFloats + k * kN + 4 * q, p.C + off,
+                 ok ? 16 : 0);
+    }
+  };
+
+#pragma unroll 1
+  for (int s = 0; s < kSsStages - 1; ++s) {
+    if (s < nst) issue(s);
+    cp_async_commit();
+  }
+  float* yp = p.y + b * T * D + dd;
+  float h0 = 0.f, h1 = 0.f;
+#pragma unroll 1
+  for (int64_t st = 0; st < nst; ++st) {
+    if (st + kSsStages - 1 < nst) issue(st + kSsStages - 1);
+    cp_async_commit();
+    cp_async_wait<kSsStages - 1>();
+    __syncthreads();
+    const float* sm = ss_sm + (st % kSsStages) * Lay::kStageFloats;
+    const float* sdt = sm + cl;
+    const float* su = sm + Lay::kDtFloats + cl;
+    const float* sB = sm + 2 * Lay::kDtFloats + 2 * l;
+    const float* sC = sm + 2 * Lay::kDtFloats + Lay::kBFloats + 2 * l;
+    const int64_t t0 = st * kSsSteps;
+    // unrolled over the whole stage so one group's reduction overlaps the next group's steps
+#pragma unroll
+    for (int k0 = 0; k0 < kSsSteps; k0 += LPC) {
+      float v[LPC];
+#pragma unroll
+      for (int k = 0; k < LPC; ++k) {
+        const int kk = k0 + k;
+        const float dt = sdt[kk * kCpb], uu = su[kk * kCpb];
+        const float2 bb = *reinterpret_cast<const float2*>(sB + kk * kN);
+        const float2 cc = *reinterpret_cast<const float2*>(sC + kk * kN);
+        const float du = dt * uu;   // zero-filled steps past T: dt = 0 keeps h
+        const float2 e = make_float2(ss_ex2(a0 * dt), ss_ex2(a1 * dt));
+        const float2 h = ss_fma2(e, make_float2(h0, h1), ss_mul2(make_float2(du, du), bb));
+        h0 = h.x;
+        h1 = h.y;
+        v[k] = fmaf(cc.x, h0, fmaf(cc.y, h1, sk * uu));
+      }
+      // transpose-reduce over the LPC lanes of the channel: at the level with lane bit m the
+      // lanes with that bit keep the upper half of their values, the others the lower half,
+      // and each adds its partner's copy of the half it keeps
+#pragma unroll
+      for (int m = LPC / 2, cnt = LPC; m >= 1; m >>= 1, cnt >>= 1) {
+        const bool up_half = (l & m) != 0;
+#pragma unroll
+        for (int i = 0; i < cnt / 2; ++i) {
+          const float send = up_half ? v[i] : v[i + cnt / 2];
+          const float keep = up_half ? v[i + cnt / 2] : v[i];
+          v[i] = keep + __shfl_xor_sync(0xffffffffu, send, m);
+        }
+      }
+      const int64_t t = t0 + k0 + l;
+      if (dv && t < T) yp[t * D] = v[0];
+    }
+    __syncthreads();   // the stage's buffer is refilled by a later issue
+  }
+}
+
+template <int LPC>
+cudaError_t launch_onepass(const SelectiveScanParams& p, cudaStream_t st) {
+  using Lay = SsLayout<LPC>;
+  const int64_t blocks = p.batch * ((p.D + Lay::kCpb - 1) / Lay::kCpb);
+  if (Lay::kSmemBytes > 48 * 1024) {
+    const cudaError_t e = cudaFuncSetAttribute(
+        ss_onepass_kernel<LPC>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Lay::kSmemBytes);
+    if (e != cudaSuccess) return e;
+  }
+  ss_onepass_kernel<LPC><<<(unsigned)blocks, 32 * kSsWarps, Lay::kSmemBytes, st>>>(p);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 int64_t ss_segment_length(int64_t) { return kSegLen; }
+
+bool selective_scan_onepass_supported(int64_t batch, int64_t D, int64_t N) {
+  if (N != 8 && N != 16 && N != 32 && N != 64) return false;
+  if (D % 4 != 0) return false;                      // 16-byte staging of delta / u rows
+  const int64_t cpb = 64 / N * kSsWarps;             // channels per block
+  const int64_t blocks = batch * ((D + cpb - 1) / cpb);
+  return blocks <= 0x7fffffffLL;
+}
+
+cudaError_t selective_scan_onepass_launch(const SelectiveScanParams& p, cudaStream_t st) {
+  switch (p.N) {
+    case 8: return launch_onepass<4>(p, st);
+    case 16: return launch_onepass<8>(p, st);
+    case 32: return launch_onepass<16>(p, st);
+    case 64: return launch_onepass<32>(p, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
 
 cudaError_t selective_scan_launch(const SelectiveScanParams& p, cudaStream_t st) {
   if (p.N <= 16) return launch_nb<16>(p, st);

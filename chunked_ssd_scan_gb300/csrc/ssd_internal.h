@@ -55,5 +55,8 @@ bool fused_bf16_supported(int64_t T, int64_t H, int64_t P, int64_t N, int64_t R,
                           bool bf16, bool theta);
 cudaError_t fused_bf16_forward(const GenericParams& p, cudaStream_t st);
 cudaError_t selective_scan_launch(const SelectiveScanParams& p, cudaStream_t st);
+// Single-kernel path for d_state in {8, 16, 32, 64} (no workspace use beyond the header).
+bool selective_scan_onepass_supported(int64_t batch, int64_t D, int64_t N);
+cudaError_t selective_scan_onepass_launch(const SelectiveScanParams& p, cudaStream_t st);
 
 }  // namespace ssd

@@ -36,6 +36,14 @@ def test_full_workload():
     wl.SelectiveScanConfig("ragged_T", 1, 1000, 130, 16),
     wl.SelectiveScanConfig("N1", 1, 300, 64, 1),
     wl.SelectiveScanConfig("N64", 2, 257, 96, 64),
+    wl.SelectiveScanConfig("N32_ragged_D", 1, 333, 50, 32),
+    wl.SelectiveScanConfig("N8_ragged_D", 2, 77, 13, 8),
+    # one-pass staged kernel (d_model % 4 == 0): ragged channel blocks and ragged stages
+    wl.SelectiveScanConfig("onepass_N16_D20", 2, 1000, 20, 16),
+    wl.SelectiveScanConfig("onepass_N8_D36", 1, 130, 36, 8),
+    wl.SelectiveScanConfig("onepass_N32_D12", 1, 65, 12, 32),
+    wl.SelectiveScanConfig("onepass_N64_D8", 1, 200, 8, 64),
+    wl.SelectiveScanConfig("onepass_T1", 3, 1, 4, 16),
     wl.SelectiveScanConfig("N17", 1, 129, 40, 17),
     wl.SelectiveScanConfig("D1", 3, 70, 1, 8),
 ], ids=lambda c: c.name)
