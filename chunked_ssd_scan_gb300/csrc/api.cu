@@ -51,6 +51,9 @@ int32_t pick_variant(const ssd_shape* s) {
   if (fused_bf16_supported(s->seqlen, s->nheads, s->headdim, s->dstate, s->mimo_rank,
                            s->chunk_len, s->io_dtype == SSD_BF16, s->has_theta != 0))
     return SSD_VARIANT_TC_BF16;
+  if (simt32_supported(s->headdim, s->dstate, s->mimo_rank, s->chunk_len, s->io_dtype == SSD_BF16,
+                       s->has_theta != 0))
+    return SSD_VARIANT_TILED_F32;
   return SSD_VARIANT_GENERIC;
 }
 
@@ -137,8 +140,11 @@ ssd_status ssd_chunked_forward(const ssd_shape* shape, const void* x, const floa
   p.phisum = theta ? reinterpret_cast<double*>(ws + lay.phisum) : nullptr;
   p.hdr = reinterpret_cast<WsHeader*>(ws);
   cudaError_t e;
-  if (pick_variant(shape) == SSD_VARIANT_TC_BF16) {
+  const int32_t variant = pick_variant(shape);
+  if (variant == SSD_VARIANT_TC_BF16) {
     e = fused_bf16_forward(p, static_cast<cudaStream_t>(stream));
+  } else if (variant == SSD_VARIANT_TILED_F32) {
+    e = simt32_forward(p, static_cast<cudaStream_t>(stream));
   } else {
     e = generic_forward(p, shape->io_dtype == SSD_BF16, static_cast<cudaStream_t>(stream));
   }

@@ -1,0 +1,78 @@
+// Small floating-point helpers shared by the CUDA kernels: 2^x on the special-function unit,
+// paired fp32 instructions, and double-float (hi + lo) sums.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace ssd {
+namespace fp {
+
+// 2^x on the special-function unit (relative error about 2^-22; 2^-inf = 0).
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Paired fp32 arithmetic: one instruction for both lanes of a float2, round to nearest.
+__device__ __forceinline__ uint64_t f2_bits(float2 v) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(v.x), "f"(v.y));
+  return r;
+}
+__device__ __forceinline__ float2 bits_f2(uint64_t r) {
+  float2 v;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(v.x), "=f"(v.y) : "l"(r));
+  return v;
+}
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(f2_bits(a)), "l"(f2_bits(b)));
+  return bits_f2(r);
+}
+__device__ __forceinline__ float2 add2(float2 a, float2 b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(f2_bits(a)), "l"(f2_bits(b)));
+  return bits_f2(r);
+}
+__device__ __forceinline__ float2 sub2(float2 a, float2 b) {
+  uint64_t r;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(f2_bits(a)), "l"(f2_bits(b)));
+  return bits_f2(r);
+}
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;"
+      : "=l"(r)
+      : "l"(f2_bits(a)), "l"(f2_bits(b)), "l"(f2_bits(c)));
+  return bits_f2(r);
+}
+
+// Double-float arithmetic (unevaluated sum hi + lo of two floats), from Knuth's TwoSum: prefix
+// sums of dA reach |cum| ~ 10^3 within a tile or chunk, and the decay mask needs cum_i - cum_j
+// to a few float ulps of the difference, not of |cum|.  fp64 is avoided on purpose (slow here).
+struct DF {
+  float hi, lo;
+};
+__device__ __forceinline__ DF two_sum(float a, float b) {
+  const float s = a + b;
+  const float bb = s - a;
+  const float err = (a - (s - bb)) + (b - bb);
+  return {s, err};
+}
+__device__ __forceinline__ DF df_add(DF x, DF y) {
+  DF s = two_sum(x.hi, y.hi);
+  const float e = s.lo + x.lo + y.lo;
+  const float hi = s.hi + e;
+  return {hi, e - (hi - s.hi)};
+}
+__device__ __forceinline__ DF df_shfl_up(DF v, int off) {
+  return {__shfl_up_sync(0xffffffffu, v.hi, off), __shfl_up_sync(0xffffffffu, v.lo, off)};
+}
+__device__ __forceinline__ DF df_shfl(DF v, int src) {
+  return {__shfl_sync(0xffffffffu, v.hi, src), __shfl_sync(0xffffffffu, v.lo, src)};
+}
+
+}  // namespace fp
+}  // namespace ssd

@@ -13,6 +13,7 @@
 #include <mutex>
 
 #include "common.cuh"
+#include "fp_helpers.cuh"
 #include "ssd_internal.h"
 
 namespace ssd {
@@ -127,34 +128,6 @@ constexpr int kSsWarps = 4;
 constexpr int kSsSteps = 64;
 constexpr int kSsStages = 4;
 
-__device__ __forceinline__ float ss_ex2(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-
-// Paired fp32 arithmetic (one instruction for both lanes of a float2, round to nearest).
-__device__ __forceinline__ uint64_t ss_bits(float2 v) {
-  uint64_t r;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(v.x), "f"(v.y));
-  return r;
-}
-__device__ __forceinline__ float2 ss_f2(uint64_t r) {
-  float2 v;
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(v.x), "=f"(v.y) : "l"(r));
-  return v;
-}
-__device__ __forceinline__ float2 ss_mul2(float2 a, float2 b) {
-  uint64_t r;
-  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(ss_bits(a)), "l"(ss_bits(b)));
-  return ss_f2(r);
-}
-__device__ __forceinline__ float2 ss_fma2(float2 a, float2 b, float2 c) {
-  uint64_t r;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(ss_bits(a)), "l"(ss_bits(b)), "l"(ss_bits(c)));
-  return ss_f2(r);
-}
-
 // 16-byte global->shared copy; src_bytes 0 writes zeros without reading.
 __device__ __forceinline__ void cp_async16(void* dst, const void* src, int src_bytes) {
   const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(dst));
@@ -252,8 +225,8 @@ __global__ void __launch_bounds__(32 * kSsWarps) ss_onepass_kernel(SelectiveScan
         const float2 bb = *reinterpret_cast<const float2*>(sB + kk * kN);
         const float2 cc = *reinterpret_cast<const float2*>(sC + kk * kN);
         const float du = dt * uu;   // zero-filled steps past T: dt = 0 keeps h
-        const float2 e = make_float2(ss_ex2(a0 * dt), ss_ex2(a1 * dt));
-        const float2 h = ss_fma2(e, make_float2(h0, h1), ss_mul2(make_float2(du, du), bb));
+        const float2 e = make_float2(fp::ex2_approx(a0 * dt), fp::ex2_approx(a1 * dt));
+        const float2 h = fp::fma2(e, make_float2(h0, h1), fp::mul2(make_float2(du, du), bb));
         h0 = h.x;
         h1 = h.y;
         v[k] = fmaf(cc.x, h0, fmaf(cc.y, h1, sk * uu));

@@ -46,6 +46,7 @@
 #include <mutex>
 
 #include "common.cuh"
+#include "fp_helpers.cuh"
 #include "ssd_internal.h"
 #include "tc_ptx.cuh"
 
@@ -54,6 +55,7 @@ namespace ssd {
 namespace {
 
 using namespace tc;
+using namespace fp;
 
 constexpr int kTileRows = 128;
 constexpr int kP = 64;
@@ -137,13 +139,6 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatil
   }
 }
 
-// 2^x on the special-function unit (relative error about 2^-22; 2^-inf = 0).
-__device__ __forceinline__ float ex2_approx(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
   return *reinterpret_cast<uint32_t*>(&v);
@@ -153,69 +148,12 @@ __device__ __forceinline__ float2 unpack_bf16(uint32_t u) {
   return make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xffff0000u));
 }
 
-// Paired fp32 arithmetic (one instruction for two lanes of a float2, round to nearest).
-__device__ __forceinline__ uint64_t f2_bits(float2 v) {
-  uint64_t r;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(v.x), "f"(v.y));
-  return r;
-}
-__device__ __forceinline__ float2 bits_f2(uint64_t r) {
-  float2 v;
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(v.x), "=f"(v.y) : "l"(r));
-  return v;
-}
-__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
-  uint64_t r;
-  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(f2_bits(a)), "l"(f2_bits(b)));
-  return bits_f2(r);
-}
-__device__ __forceinline__ float2 add2(float2 a, float2 b) {
-  uint64_t r;
-  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(f2_bits(a)), "l"(f2_bits(b)));
-  return bits_f2(r);
-}
-__device__ __forceinline__ float2 sub2(float2 a, float2 b) {
-  uint64_t r;
-  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(f2_bits(a)), "l"(f2_bits(b)));
-  return bits_f2(r);
-}
-__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
-  uint64_t r;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(f2_bits(a)), "l"(f2_bits(b)), "l"(f2_bits(c)));
-  return bits_f2(r);
-}
-
 // v = hi + lo with hi = bf16(v) and lo = bf16(v - hi): two bf16 terms carry ~16 mantissa bits.
 // Packs the pair (v.x, v.y) of each into one 32-bit word (v.x in the low half).
 __device__ __forceinline__ void split2(float2 v, uint32_t& hi, uint32_t& lo) {
   hi = pack_bf16(v.x, v.y);
   const float2 r = sub2(v, unpack_bf16(hi));
   lo = pack_bf16(r.x, r.y);
-}
-
-// Double-float arithmetic (unevaluated sum hi + lo of two floats), from Knuth's TwoSum: the
-// prefix sums of dA reach |cum| ~ 10^3 within a tile, and the mask needs cum_i - cum_j to a
-// few float ulps of the difference, not of |cum|.  fp64 is avoided on purpose (very slow here).
-struct DF {
-  float hi, lo;
-};
-__device__ __forceinline__ DF two_sum(float a, float b) {
-  const float s = a + b;
-  const float bb = s - a;
-  const float err = (a - (s - bb)) + (b - bb);
-  return {s, err};
-}
-__device__ __forceinline__ DF df_add(DF x, DF y) {
-  DF s = two_sum(x.hi, y.hi);
-  const float e = s.lo + x.lo + y.lo;
-  const float hi = s.hi + e;
-  return {hi, e - (hi - s.hi)};
-}
-__device__ __forceinline__ DF df_shfl_up(DF v, int off) {
-  return {__shfl_up_sync(0xffffffffu, v.hi, off), __shfl_up_sync(0xffffffffu, v.lo, off)};
-}
-__device__ __forceinline__ DF df_shfl(DF v, int src) {
-  return {__shfl_sync(0xffffffffu, v.hi, src), __shfl_sync(0xffffffffu, v.lo, src)};
 }
 
 // One 32-column block cb of the masked operand for the calling thread's row (w = its CB

@@ -126,29 +126,54 @@ __device__ void stage_bc_rows(const GenericParams& p, const T* __restrict__ src,
   }
 }
 
-__global__ void phi_chunk_sum_kernel(GenericParams p) {
+// Per-chunk theta sums in fp64: every thread of the block takes one pair and a slice of the
+// chunk's steps (loads coalesced over pairs); the slices are combined in shared memory.
+constexpr int kPhiThreads = 256;
+
+__global__ void __launch_bounds__(kPhiThreads) phi_chunk_sum_kernel(GenericParams p) {
+  __shared__ double part[kPhiThreads];
   const int64_t c = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
-  const int64_t K = p.N / 2;
-  for (int64_t k = threadIdx.x; k < K; k += blockDim.x) {
+  const int K = (int)(p.N / 2);
+  const int groups = kPhiThreads / K;             // K <= 128 (N <= 256)
+  const int k = threadIdx.x % K, grp = threadIdx.x / K;
+  double s = 0.0;
+  if (grp < groups) {
     const float* th = p.theta + ((b * p.T + c * p.l) * p.H + h) * K + k;
-    double s = 0.0;
-    for (int64_t t = 0; t < p.l; ++t) s += (double)__ldg(th + t * p.H * K);
-    p.phisum[((b * p.nch + c) * p.H + h) * K + k] = s;
+    for (int64_t t = grp; t < p.l; t += groups) s += (double)__ldg(th + t * p.H * K);
+  }
+  part[threadIdx.x] = s;
+  __syncthreads();
+  if (threadIdx.x < K) {
+    double tot = 0.0;
+    for (int g = 0; g < groups; ++g) tot += part[g * K + threadIdx.x];
+    p.phisum[((b * p.nch + c) * p.H + h) * K + threadIdx.x] = tot;
   }
 }
 
+// Chunk-start angles: an exclusive fp64 prefix of the chunk sums per (batch, head, pair),
+// reduced to [-pi, pi]; the chunk sums are loaded several chunks ahead.
 __global__ void phi_prefix_kernel(GenericParams p) {
   const int64_t K = p.N / 2;
   const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (idx >= p.batch * p.H * K) return;
   const int64_t k = idx % K, h = (idx / K) % p.H, b = idx / (K * p.H);
+  const double* src = p.phisum + (b * p.nch * p.H + h) * K + k;   // + c * H * K
+  double* dst = p.phi + (b * (p.nch + 1) * p.H + h) * K + k;
+  const int64_t cs = p.H * K;
   double acc = 0.0;
-  for (int64_t c = 0; c < p.nch; ++c) {
-    p.phi[((b * (p.nch + 1) + c) * p.H + h) * K + k] = acc - kTwoPi * rint(acc * (1.0 / kTwoPi));
-    acc += p.phisum[((b * p.nch + c) * p.H + h) * K + k];
+  for (int64_t c0 = 0; c0 < p.nch; c0 += 8) {
+    double v[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) v[j] = (c0 + j < p.nch) ? src[(c0 + j) * cs] : 0.0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (c0 + j < p.nch) {
+        dst[(c0 + j) * cs] = acc - kTwoPi * rint(acc * (1.0 / kTwoPi));
+        acc += v[j];
+      }
+    }
   }
-  p.phi[((b * (p.nch + 1) + p.nch) * p.H + h) * K + k] =
-      acc - kTwoPi * rint(acc * (1.0 / kTwoPi));
+  dst[p.nch * cs] = acc - kTwoPi * rint(acc * (1.0 / kTwoPi));
 }
 
 template <typename T, int OPT>
@@ -204,43 +229,62 @@ __global__ void __launch_bounds__(kThreads) chunk_state_kernel(GenericParams p) 
   if (threadIdx.x == 0) p.cend[(b * p.nch + c) * p.H + h] = cum_end;
 }
 
-// One thread carries one state element (or, with rotation, one interleaved pair) through all
-// chunks of one (batch, head).
+// One thread carries one state element (or, with rotation, one interleaved pair) of one
+// (batch, head) through all chunks; the grid covers every element of every (batch, head), and
+// the chunk states are loaded kStatePrefetch chunks ahead of the serial update.
+constexpr int kStatePrefetch = 8;
+
 template <bool kPairs>
 __global__ void __launch_bounds__(kThreads) state_pass_kernel(GenericParams p) {
-  const int64_t bh = blockIdx.x;
-  const int64_t b = bh / p.H, h = bh % p.H;
   const int64_t PN = p.P * p.N, K = p.N / 2;
   constexpr int W = kPairs ? 2 : 1;
-  for (int64_t q = threadIdx.x; q < PN / W; q += blockDim.x) {
-    const int64_t off = W * q;
-    float hv[W];
+  const int64_t per_bh = PN / W;
+  const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= p.batch * p.H * per_bh) return;
+  const int64_t bh = idx / per_bh, q = idx % per_bh;
+  const int64_t b = bh / p.H, h = bh % p.H;
+  const int64_t off = W * q;
+  const int64_t cstride = p.H * PN;              // from chunk c to c + 1 in states
+  float* sp = p.states + ((b * p.nch) * p.H + h) * PN + off;
+  const float* ce = p.cend + (b * p.nch) * p.H + h;
+  float hv[W];
 #pragma unroll
-    for (int w = 0; w < W; ++w) hv[w] = p.init ? p.init[(b * p.H + h) * PN + off + w] : 0.f;
-    for (int64_t c = 0; c < p.nch; ++c) {
-      float* sp = p.states + ((b * p.nch + c) * p.H + h) * PN + off;
-      const float a = expf(p.cend[(b * p.nch + c) * p.H + h]);
+  for (int w = 0; w < W; ++w) hv[w] = p.init ? p.init[(b * p.H + h) * PN + off + w] : 0.f;
+  for (int64_t c0 = 0; c0 < p.nch; c0 += kStatePrefetch) {
+    float sv[kStatePrefetch][W], av[kStatePrefetch];
 #pragma unroll
-      for (int w = 0; w < W; ++w) {
-        const float s = sp[w];
-        sp[w] = hv[w];
-        hv[w] = a * hv[w] + s;
+    for (int k = 0; k < kStatePrefetch; ++k) {
+      if (c0 + k < p.nch) {
+        av[k] = ce[(c0 + k) * p.H];
+#pragma unroll
+        for (int w = 0; w < W; ++w) sv[k][w] = sp[(c0 + k) * cstride + w];
       }
     }
-    if (kPairs) {
-      // back to the physical frame: turn the pair by +Phi_{T-1}
-      const float ang =
-          reduce_two_pi(p.phi[((b * (p.nch + 1) + p.nch) * p.H + h) * K + (off % p.N) / 2]);
-      float s, co;
-      sincosf(ang, &s, &co);
-      const float e = co * hv[0] - s * hv[W - 1], o = s * hv[0] + co * hv[W - 1];
-      hv[0] = e;
-      hv[W - 1] = o;
-    }
-    if (p.final_state) {
 #pragma unroll
-      for (int w = 0; w < W; ++w) p.final_state[(b * p.H + h) * PN + off + w] = hv[w];
+    for (int k = 0; k < kStatePrefetch; ++k) {
+      if (c0 + k < p.nch) {
+        const float a = expf(av[k]);
+#pragma unroll
+        for (int w = 0; w < W; ++w) {
+          sp[(c0 + k) * cstride + w] = hv[w];
+          hv[w] = a * hv[w] + sv[k][w];
+        }
+      }
     }
+  }
+  if (kPairs) {
+    // back to the physical frame: turn the pair by +Phi_{T-1}
+    const float ang =
+        reduce_two_pi(p.phi[((b * (p.nch + 1) + p.nch) * p.H + h) * K + (off % p.N) / 2]);
+    float s, co;
+    sincosf(ang, &s, &co);
+    const float e = co * hv[0] - s * hv[W - 1], o = s * hv[0] + co * hv[W - 1];
+    hv[0] = e;
+    hv[W - 1] = o;
+  }
+  if (p.final_state) {
+#pragma unroll
+    for (int w = 0; w < W; ++w) p.final_state[(b * p.H + h) * PN + off + w] = hv[w];
   }
 }
 
@@ -399,25 +443,35 @@ bool generic_supported(int64_t l, int64_t R, int64_t P, int64_t N, bool theta) {
   return generic_state_smem(l, P, N, theta) <= lim && generic_scan_smem(l, P, N, theta) <= lim;
 }
 
+cudaError_t generic_phi(const GenericParams& p, cudaStream_t st) {
+  phi_chunk_sum_kernel<<<dim3((unsigned)p.nch, (unsigned)p.H, (unsigned)p.batch), kPhiThreads, 0,
+                         st>>>(p);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const int64_t n = p.batch * p.H * (p.N / 2);
+  phi_prefix_kernel<<<(unsigned)((n + 127) / 128), 128, 0, st>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t generic_state_pass(const GenericParams& p, cudaStream_t st) {
+  const int64_t n = p.batch * p.H * p.P * p.N / (p.theta ? 2 : 1);
+  const unsigned blocks = (unsigned)((n + kThreads - 1) / kThreads);
+  if (p.theta) {
+    state_pass_kernel<true><<<blocks, kThreads, 0, st>>>(p);
+  } else {
+    state_pass_kernel<false><<<blocks, kThreads, 0, st>>>(p);
+  }
+  return cudaGetLastError();
+}
+
 cudaError_t generic_forward(const GenericParams& p, bool bf16, cudaStream_t st) {
   cudaError_t e;
-  if (p.theta) {
-    phi_chunk_sum_kernel<<<dim3((unsigned)p.nch, (unsigned)p.H, (unsigned)p.batch), 128, 0, st>>>(p);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    const int64_t n = p.batch * p.H * (p.N / 2);
-    phi_prefix_kernel<<<(unsigned)((n + 127) / 128), 128, 0, st>>>(p);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  }
+  if (p.theta && (e = generic_phi(p, st)) != cudaSuccess) return e;
   const bool th = p.theta != nullptr;
   const size_t s1 = generic_state_smem(p.l, p.P, p.N, th);
   e = bf16 ? launch_state_dispatch<__nv_bfloat16>(p, s1, st) : launch_state_dispatch<float>(p, s1, st);
   if (e != cudaSuccess) return e;
-  if (p.theta) {
-    state_pass_kernel<true><<<(unsigned)(p.batch * p.H), kThreads, 0, st>>>(p);
-  } else {
-    state_pass_kernel<false><<<(unsigned)(p.batch * p.H), kThreads, 0, st>>>(p);
-  }
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if ((e = generic_state_pass(p, st)) != cudaSuccess) return e;
   const size_t s2 = generic_scan_smem(p.l, p.P, p.N, th);
   return bf16 ? launch_scan_dispatch<__nv_bfloat16>(p, s2, st) : launch_scan_dispatch<float>(p, s2, st);
 }

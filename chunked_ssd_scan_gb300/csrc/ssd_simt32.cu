@@ -1,0 +1,332 @@
+// Register-tiled CUDA-core chunked SSD forward for fp32 I/O with P = N = 64 and mimo_rank 1.
+//
+// Same chunk decomposition as the generic path (the serial.rs page's K1..K5, with the rotation
+// absorbed into B and C as on the scan.py page):
+//   phi kernels         : chunk-start angles (shared with the generic path)
+//   simt_state_kernel   : K1 and K3 for one chunk, S_c[p][n] = sum_j exp(cum_end - cum_j) x_j[p] B~_j[n]
+//   state_pass          : K4 across chunks (shared with the generic path)
+//   simt_scan_kernel    : K2 and K5 for one chunk, in 64-row tiles:
+//                         y_i = sum_{j <= i} exp(cum_i - cum_j) (C~_i . B~_j) x_j + exp(cum_i) C~_i . h_in
+// Every contraction is a 64 x 64 x 64 block product from shared memory: each of the 256 threads
+// owns a 4 x 4 output block and reads two float4 per k (16 FMAs per 32 bytes of shared memory).
+// The tensor core is not used here on purpose: its fp32 accumulation truncates toward zero at
+// every MMA, and with slowly decaying states the partial sums are large enough that the bias
+// exceeds the fp32 tolerance (1e-4 (1 + |y|)) where y cancels; these kernels accumulate with
+// round-to-nearest fp32 FMAs.  Exponentials use exp2f on double-float prefix sums, and the
+// rotation uses sincosf on double-float angles.
+#include <math.h>
+
+#include "common.cuh"
+#include "fp_helpers.cuh"
+#include "ssd_internal.h"
+
+namespace ssd {
+
+namespace {
+
+using namespace fp;
+
+constexpr int kT64 = 64;                     // tile edge (rows, sources, P and N)
+constexpr int kSimtThreads = 256;
+constexpr int kPairs64 = 32;
+constexpr int kMaxChunk64 = 512;
+constexpr float kLog2e64 = 1.4426950408889634f;
+constexpr float kTwoPiHi64 = 6.28318548202514648f;        // float(2 pi)
+constexpr float kTwoPiLo64 = -1.7484556000744487e-07f;    // 2 pi - kTwoPiHi64
+constexpr int kTileFloats = kT64 * kT64;
+
+// log2-scaled double-float prefix sums of dA over steps [0, n) of a chunk, by warp 0:
+// cum_hi/cum_lo[t] is the inclusive sum up to step t; *total (natural units) if non-null.
+__device__ void chunk_prefix64(const float* __restrict__ src, int64_t stride, int n, float* cum_hi,
+                               float* cum_lo, float* total) {
+  if (threadIdx.x >= 32) return;
+  const int lane = threadIdx.x;
+  const int per = (n + 31) / 32;
+  const int beg = min(n, lane * per), end = min(n, beg + per);
+  DF s = {0.f, 0.f};
+  for (int t = beg; t < end; ++t) s = df_add(s, DF{__ldg(src + (int64_t)t * stride), 0.f});
+  DF incl = s;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const DF v = df_shfl_up(incl, off);
+    if (lane >= off) incl = df_add(incl, v);
+  }
+  const DF last = df_shfl(incl, 31);
+  DF acc = df_shfl_up(incl, 1);
+  if (lane == 0) acc = DF{0.f, 0.f};
+  for (int t = beg; t < end; ++t) {
+    acc = df_add(acc, DF{__ldg(src + (int64_t)t * stride), 0.f});
+    const float chi = acc.hi * kLog2e64;
+    cum_hi[t] = chi;
+    cum_lo[t] = fmaf(acc.hi, kLog2e64, -chi) + acc.lo * kLog2e64;
+  }
+  if (lane == 0 && total) *total = last.hi + last.lo;
+}
+
+// Rotation angles Phi_t (inclusive cumulative theta from the chunk-start angle) for steps
+// [0, n) and all 32 pairs, reduced to [-pi, pi], into ang[t * 32 + k]: theta is staged into
+// `ang` (coalesced), then each warp runs a double-float prefix per pair in place.
+__device__ void chunk_angles64(const GenericParams& p, int64_t b, int64_t c, int64_t h, int n,
+                               float* ang) {
+  const float* th = p.theta + ((b * p.T + c * p.l) * p.H + h) * kPairs64;
+  for (int e = threadIdx.x; e < n * (kPairs64 / 4); e += blockDim.x) {
+    const int t = e / (kPairs64 / 4), q = e % (kPairs64 / 4);
+    *reinterpret_cast<float4*>(ang + t * kPairs64 + 4 * q) =
+        __ldg(reinterpret_cast<const float4*>(th + (int64_t)t * p.H * kPairs64) + q);
+  }
+  __syncthreads();
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int per = (n + 31) / 32;
+  const int beg = min(n, lane * per), end = min(n, beg + per);
+  for (int k = warp; k < kPairs64; k += blockDim.x / 32) {
+    const double a0 = p.phi[((b * (p.nch + 1) + c) * p.H + h) * kPairs64 + k];   // in [-pi, pi]
+    const float s_hi = (float)a0;
+    const DF start = {s_hi, (float)(a0 - (double)s_hi)};
+    DF s = {0.f, 0.f};
+    for (int t = beg; t < end; ++t) s = df_add(s, DF{ang[t * kPairs64 + k], 0.f});
+    DF incl = s;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const DF v = df_shfl_up(incl, off);
+      if (lane >= off) incl = df_add(incl, v);
+    }
+    DF acc = df_shfl_up(incl, 1);
+    if (lane == 0) acc = DF{0.f, 0.f};
+    acc = df_add(acc, start);
+    for (int t = beg; t < end; ++t) {
+      acc = df_add(acc, DF{ang[t * kPairs64 + k], 0.f});
+      const float q = rintf(acc.hi * 0.15915494309189535f);
+      ang[t * kPairs64 + k] = (fmaf(-q, kTwoPiHi64, acc.hi) - q * kTwoPiLo64) + acc.lo;
+    }
+  }
+  __syncthreads();
+}
+
+// acc[r][c] += sum_k At[k][4 ty + r] * Bt[k][4 tx + c] over k < 64 (both operands k-major,
+// 64 floats per k row).
+__device__ __forceinline__ void block_product(const float* __restrict__ At,
+                                              const float* __restrict__ Bt, int ty, int tx,
+                                              float (&acc)[4][4]) {
+#pragma unroll 8
+  for (int k = 0; k < kT64; ++k) {
+    const float4 a = *reinterpret_cast<const float4*>(At + k * kT64 + 4 * ty);
+    const float4 bq = *reinterpret_cast<const float4*>(Bt + k * kT64 + 4 * tx);
+    const float av[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const float2 lo = fma2(make_float2(av[r], av[r]), make_float2(bq.x, bq.y),
+                             make_float2(acc[r][0], acc[r][1]));
+      const float2 hi = fma2(make_float2(av[r], av[r]), make_float2(bq.z, bq.w),
+                             make_float2(acc[r][2], acc[r][3]));
+      acc[r][0] = lo.x;
+      acc[r][1] = lo.y;
+      acc[r][2] = hi.x;
+      acc[r][3] = hi.y;
+    }
+  }
+}
+
+// Stages 64 rows (chunk steps s0 ..) of a B/C tensor turned by -Phi (if theta) into dst, either
+// row-major dst[row][n] (transpose = false) or transposed dst[n][row].
+__device__ void stage_bc64(const GenericParams& p, const float* __restrict__ src, int64_t b,
+                           int64_t c, int64_t g, int s0, const float* ang, float* dst,
+                           bool transpose) {
+  const int tid = threadIdx.x;
+  const int row = tid >> 2, q0 = (tid & 3) * 16;   // 4 threads per row, 16 values each
+  const float4* s4 = reinterpret_cast<const float4*>(
+      src + ((b * p.T + c * p.l + s0 + row) * p.G + g) * kT64 + q0);
+  float v[16];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const float4 f = __ldg(s4 + q);
+    v[4 * q] = f.x;
+    v[4 * q + 1] = f.y;
+    v[4 * q + 2] = f.z;
+    v[4 * q + 3] = f.w;
+  }
+  if (p.theta) {
+    const float* ar = ang + (s0 + row) * kPairs64 + q0 / 2;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      float s, co;
+      sincosf(ar[k], &s, &co);
+      const float a = v[2 * k], bb = v[2 * k + 1];
+      v[2 * k] = co * a + s * bb;
+      v[2 * k + 1] = -s * a + co * bb;
+    }
+  }
+  if (transpose) {
+#pragma unroll
+    for (int k = 0; k < 16; ++k) dst[(q0 + k) * kT64 + row] = v[k];
+  } else {
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      *reinterpret_cast<float4*>(dst + row * kT64 + q0 + 4 * q) =
+          make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+  }
+}
+
+// Stages x rows (chunk steps s0 ..) into dst[row][p], each row scaled by scale[row] if given.
+__device__ void stage_x64(const GenericParams& p, int64_t b, int64_t c, int64_t h, int s0,
+                          const float* scale, float* dst) {
+  const int tid = threadIdx.x;
+  const int row = tid >> 2, q0 = (tid & 3) * 16;
+  const float4* s4 = reinterpret_cast<const float4*>(
+      static_cast<const float*>(p.x) + ((b * p.T + c * p.l + s0 + row) * p.H + h) * kT64 + q0);
+  const float w = scale ? scale[row] : 1.f;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const float4 f = __ldg(s4 + q);
+    *reinterpret_cast<float4*>(dst + row * kT64 + q0 + 4 * q) =
+        make_float4(f.x * w, f.y * w, f.z * w, f.w * w);
+  }
+}
+
+// ---------------------------------------------------------------------------------- K1 + K3
+size_t simt_state_smem(int64_t l, bool theta) {
+  return sizeof(float) * (2 * kTileFloats + 3 * l + (theta ? l * kPairs64 : 0) + 4);
+}
+
+__global__ void __launch_bounds__(kSimtThreads) simt_state_kernel(GenericParams p) {
+  extern __shared__ __align__(16) float sm64[];
+  const int64_t c = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int64_t g = h / (p.H / p.G);
+  const int l = (int)p.l;
+  float* xs = sm64;                        // X~ [j][p] of one 64-step block
+  float* bs = xs + kTileFloats;            // B~ [j][n]
+  float* cum_hi = bs + kTileFloats;
+  float* cum_lo = cum_hi + l;
+  float* dec = cum_lo + l;
+  float* ang = dec + l;
+  float* total = ang + (p.theta ? l * kPairs64 : 0);
+  chunk_prefix64(p.dA + (b * p.T + c * p.l) * p.H + h, p.H, l, cum_hi, cum_lo, total);
+  if (p.theta) {
+    chunk_angles64(p, b, c, h, l, ang);
+  } else {
+    __syncthreads();
+  }
+  for (int t = threadIdx.x; t < l; t += kSimtThreads)
+    dec[t] = exp2f((cum_hi[l - 1] - cum_hi[t]) + (cum_lo[l - 1] - cum_lo[t]));
+  __syncthreads();
+  const int tx = threadIdx.x % 16, ty = threadIdx.x / 16;   // output rows p = 4 ty.., cols n = 4 tx..
+  float acc[4][4] = {};
+  for (int j0 = 0; j0 < l; j0 += kT64) {
+    stage_x64(p, b, c, h, j0, dec + j0, xs);
+    stage_bc64(p, static_cast<const float*>(p.B), b, c, g, j0, ang, bs, false);
+    __syncthreads();
+    block_product(xs, bs, ty, tx, acc);   // S[p][n] += sum_j X~[j][p] B~[j][n]
+    __syncthreads();
+  }
+  float* dst = p.states + ((b * p.nch + c) * p.H + h) * kTileFloats;
+#pragma unroll
+  for (int r = 0; r < 4; ++r)
+    *reinterpret_cast<float4*>(dst + (4 * ty + r) * kT64 + 4 * tx) =
+        make_float4(acc[r][0], acc[r][1], acc[r][2], acc[r][3]);
+  if (threadIdx.x == 0) p.cend[(b * p.nch + c) * p.H + h] = *total;
+}
+
+// ---------------------------------------------------------------------------------- K2 + K5
+// smem: C~^T [n][i] of the row tile, h_in^T [n][p], B~^T [n][j] (rewritten as (L o CB)^T [j][i]
+// once CB is in registers), x [j][p], prefix sums, angles.
+size_t simt_scan_smem(int64_t l, bool theta) {
+  return sizeof(float) * (4 * kTileFloats + 2 * l + (theta ? l * kPairs64 : 0));
+}
+
+__global__ void __launch_bounds__(kSimtThreads) simt_scan_kernel(GenericParams p) {
+  extern __shared__ __align__(16) float sm64[];
+  const int64_t c = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int64_t g = h / (p.H / p.G);
+  const int l = (int)p.l;
+  float* ct = sm64;                        // C~^T [n][i]
+  float* ht = ct + kTileFloats;            // h_in^T [n][p]
+  float* bt = ht + kTileFloats;            // B~^T [n][j], then M^T [j][i]
+  float* xs = bt + kTileFloats;            // x [j][p]
+  float* cum_hi = xs + kTileFloats;
+  float* cum_lo = cum_hi + l;
+  float* ang = cum_lo + l;
+  chunk_prefix64(p.dA + (b * p.T + c * p.l) * p.H + h, p.H, l, cum_hi, cum_lo, nullptr);
+  {
+    // h_in [p][n] (written over S by the state pass) -> h^T [n][p]
+    const float* hin = p.states + ((b * p.nch + c) * p.H + h) * kTileFloats;
+    for (int e = threadIdx.x; e < kTileFloats; e += kSimtThreads)
+      ht[(e % kT64) * kT64 + e / kT64] = hin[e];
+  }
+  if (p.theta) {
+    chunk_angles64(p, b, c, h, l, ang);
+  } else {
+    __syncthreads();
+  }
+  const int tx = threadIdx.x % 16, ty = threadIdx.x / 16;   // rows i = 4 ty.., cols 4 tx..
+  const float* Csrc = static_cast<const float*>(p.C);
+  const float* Bsrc = static_cast<const float*>(p.B);
+  for (int i0 = 0; i0 < l; i0 += kT64) {
+    stage_bc64(p, Csrc, b, c, g, i0, ang, ct, true);
+    __syncthreads();
+    float yo[4][4] = {};
+    block_product(ct, ht, ty, tx, yo);   // Yo[i][p] = sum_n C~[i][n] h[p][n]
+    float yd[4][4] = {};
+    for (int j0 = 0; j0 <= i0; j0 += kT64) {
+      stage_bc64(p, Bsrc, b, c, g, j0, ang, bt, true);
+      stage_x64(p, b, c, h, j0, nullptr, xs);
+      __syncthreads();
+      float cb[4][4] = {};
+      block_product(ct, bt, ty, tx, cb);   // CB[i][j] = sum_n C~[i][n] B~[j][n]
+      __syncthreads();                     // every read of B~^T done before M^T overwrites it
+      // (L o CB)^T: causal cut before the exponential
+#pragma unroll
+      for (int jj = 0; jj < 4; ++jj) {
+        const int sj = j0 + 4 * tx + jj;
+        float m[4];
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          const int si = i0 + 4 * ty + r;
+          m[r] = sj <= si ? exp2f((cum_hi[si] - cum_hi[sj]) + (cum_lo[si] - cum_lo[sj])) * cb[r][jj]
+                          : 0.f;
+        }
+        *reinterpret_cast<float4*>(bt + (4 * tx + jj) * kT64 + 4 * ty) =
+            make_float4(m[0], m[1], m[2], m[3]);
+      }
+      __syncthreads();
+      block_product(bt, xs, ty, tx, yd);   // Yd[i][p] += sum_j M[i][j] x[j][p]
+      __syncthreads();
+    }
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const int si = i0 + 4 * ty + r;
+      const float sc = exp2f(cum_hi[si] + cum_lo[si]);   // exp(cum_i)
+      float* yrow = static_cast<float*>(p.y) + ((b * p.T + c * p.l + si) * p.H + h) * kT64;
+      *reinterpret_cast<float4*>(yrow + 4 * tx) =
+          make_float4(fmaf(sc, yo[r][0], yd[r][0]), fmaf(sc, yo[r][1], yd[r][1]),
+                      fmaf(sc, yo[r][2], yd[r][2]), fmaf(sc, yo[r][3], yd[r][3]));
+    }
+  }
+}
+
+}  // namespace
+
+bool simt32_supported(int64_t P, int64_t N, int64_t R, int64_t l, bool bf16, bool theta) {
+  if (bf16 || P != kT64 || N != kT64 || R != 1) return false;
+  if (l < kT64 || l > kMaxChunk64 || (l % kT64) != 0) return false;
+  return simt_state_smem(l, theta) <= 227 * 1024 && simt_scan_smem(l, theta) <= 227 * 1024;
+}
+
+cudaError_t simt32_forward(const GenericParams& p, cudaStream_t st) {
+  cudaError_t e;
+  const bool th = p.theta != nullptr;
+  if (th && (e = generic_phi(p, st)) != cudaSuccess) return e;
+  const size_t s1 = simt_state_smem(p.l, th), s2 = simt_scan_smem(p.l, th);
+  if ((e = cudaFuncSetAttribute(simt_state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)s1)) != cudaSuccess)
+    return e;
+  if ((e = cudaFuncSetAttribute(simt_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)s2)) != cudaSuccess)
+    return e;
+  const dim3 grid((unsigned)p.nch, (unsigned)p.H, (unsigned)p.batch);
+  simt_state_kernel<<<grid, kSimtThreads, s1, st>>>(p);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if ((e = generic_state_pass(p, st)) != cudaSuccess) return e;
+  simt_scan_kernel<<<grid, kSimtThreads, s2, st>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace ssd

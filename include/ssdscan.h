@@ -64,7 +64,7 @@ typedef enum ssd_kernel_variant {
   SSD_VARIANT_NONE = 0,    /* shape not supported                                    */
   SSD_VARIANT_GENERIC = 1, /* CUDA-core fp32 chunk pipeline (any supported shape)    */
   SSD_VARIANT_TC_BF16 = 2, /* fused tcgen05/TMEM kernel, bf16 operands, fp32 accum.  */
-  SSD_VARIANT_TC_TF32 = 3  /* fused tcgen05/TMEM kernel, split-tf32 operands (f32 io) */
+  SSD_VARIANT_TILED_F32 = 3 /* register-tiled CUDA-core fp32 kernels, P = N = 64, R = 1  */
 } ssd_kernel_variant;
 
 /*

@@ -68,11 +68,22 @@ EDGE = [
     wl.SSDConfig("fused_one_tile", 1, 128, 4, 64, 128, 128, 1, 1, "bf16"),
     wl.SSDConfig("fused_r2_g2", 2, 320, 8, 64, 128, 64, 2, 2, "bf16"),
     wl.SSDConfig("fused_r8_g4", 1, 256, 4, 64, 128, 16, 8, 4, "bf16"),
+    # register-tiled fp32 path: one 64-row tile per chunk without rotation, two groups; six
+    # tiles per chunk with rotation and one group shared by three heads
+    wl.SSDConfig("tiled_f32_l64_g2", 2, 512, 4, 64, 64, 64, 1, 2, "f32"),
+    wl.SSDConfig("tiled_f32_l384_theta_shared", 1, 768, 3, 64, 64, 384, 1, 1, "f32", theta=True),
 ]
 
 
+def test_f32_workloads_use_the_tiled_kernels():
+    for cfg in (wl.LONG_ROT_F32, EDGE[-1], EDGE[-2]):
+        shape = pkg.make_shape(cfg.batch, cfg.seqlen, cfg.nheads, cfg.headdim, cfg.dstate,
+                               cfg.ngroups, cfg.mimo_rank, cfg.chunk_len, cfg.dtype, cfg.theta)
+        assert pkg.ssd_chunked_variant(shape) == "tiled_f32", cfg.name
+
+
 def test_bf16_workloads_use_the_fused_kernel():
-    for cfg in (wl.MAMBA2_SISO_BF16, wl.MAMBA3_MIMO_BF16, EDGE[-1], EDGE[-2], EDGE[-3]):
+    for cfg in (wl.MAMBA2_SISO_BF16, wl.MAMBA3_MIMO_BF16, EDGE[-3], EDGE[-4], EDGE[-5]):
         shape = pkg.make_shape(cfg.batch, cfg.seqlen, cfg.nheads, cfg.headdim, cfg.dstate,
                                cfg.ngroups, cfg.mimo_rank, cfg.chunk_len, cfg.dtype, cfg.theta)
         assert pkg.ssd_chunked_variant(shape) == "tc_bf16", cfg.name
