@@ -172,7 +172,7 @@ def run_ours(args, rank, world, local):
         host = wl.make_selective_scan_inputs(cfg, seed=0)
         d = {k: v.to(dev) for k, v in host.items()}
         y = torch.empty_like(d["u"])
-        ws = torch.empty(pkg.selective_scan_workspace_bytes(cfg.batch, cfg.seqlen, cfg.d_model,
+        ws = torch.zeros(pkg.selective_scan_workspace_bytes(cfg.batch, cfg.seqlen, cfg.d_model,
                                                             cfg.d_state), dtype=torch.uint8,
                          device=dev)
         # validated once; each step is only the C-ABI call
@@ -190,13 +190,14 @@ def run_ours(args, rank, world, local):
         fin = torch.empty((cfg.batch, cfg.nheads, cfg.headdim, cfg.dstate), dtype=torch.float32,
                           device=dev)
         shape = pkg.shape_of(d["x"], d["B"], cfg.chunk_len, cfg.theta)
-        ws = torch.empty(pkg.ssd_chunked_workspace_bytes(shape), dtype=torch.uint8, device=dev)
+        ws = torch.zeros(pkg.ssd_chunked_workspace_bytes(shape), dtype=torch.uint8, device=dev)
         # validated once; each step is only the C-ABI call
         fn = pkg.SSDForwardPlan(d["x"], d["dA"], d["B"], d["C"], chunk_len=cfg.chunk_len,
                                 theta=d["theta"], init_state=d["init_state"], y=y,
                                 final_state=fin, workspace=ws, stream=stream)
         variant = pkg.ssd_chunked_variant(shape)
-        launches_per_call = {"generic": 3 + (2 if cfg.theta else 0)}.get(variant, 1)
+        launches_per_call = {"generic": 3 + (2 if cfg.theta else 0),
+                             "tiled_f32": 3 + (2 if cfg.theta else 0)}.get(variant, 1)
         dtype = cfg.dtype
         io_bytes = cfg.io_bytes()
         flops = cfg.causal_flops()
@@ -304,7 +305,7 @@ def e2e_measure(args, cfg, is_ss, host, dev, stream):
         outs = [(y, torch.empty(y.shape, dtype=y.dtype).pin_memory()),
                 (fin, torch.empty(fin.shape, dtype=fin.dtype).pin_memory())]
         shape = pkg.shape_of(dbuf["x"], dbuf["B"], cfg.chunk_len, cfg.theta)
-        ws = torch.empty(pkg.ssd_chunked_workspace_bytes(shape), dtype=torch.uint8, device=dev)
+        ws = torch.zeros(pkg.ssd_chunked_workspace_bytes(shape), dtype=torch.uint8, device=dev)
 
         def call():
             pkg.ssd_chunked_forward(dbuf["x"], dbuf["dA"], dbuf["B"], dbuf["C"],

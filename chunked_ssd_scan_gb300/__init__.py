@@ -18,7 +18,7 @@ from . import workloads  # noqa: F401  (seeded synthetic inputs; no scan arithme
 __all__ = [
     "SSDError", "load_library", "ssd_shape", "ssd_chunked_workspace_bytes", "ssd_chunked_variant",
     "ssd_chunked_forward", "SSDForwardPlan", "SelectiveScanPlan", "selective_scan_workspace_bytes", "selective_scan_forward",
-    "workspace_status", "STATUS", "VARIANTS",
+    "workspace_status", "wait_selftest", "STATUS", "VARIANTS",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -74,6 +74,8 @@ def load_library(path: Optional[str] = None):
     lib.ssd_workspace_status.argtypes = [_VP, _VP, ctypes.POINTER(ctypes.c_int64)]
     lib.ssd_status_string.restype = ctypes.c_char_p
     lib.ssd_status_string.argtypes = [ctypes.c_int]
+    lib.ssd_wait_selftest.restype = ctypes.c_int
+    lib.ssd_wait_selftest.argtypes = [_VP, ctypes.c_size_t, ctypes.c_uint64, _VP]
     lib.ssd_abi_version.restype = ctypes.c_int32
     lib.ssd_abi_version.argtypes = []
     if path is None:
@@ -163,7 +165,7 @@ class SSDForwardPlan:
         if need == 0:
             raise SSDError(2, "ssd_chunked_workspace_bytes (shape not supported)")
         if workspace is None:
-            workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
+            workspace = torch.zeros(need, dtype=torch.uint8, device=x.device)   # zero header
         _check_cuda("workspace", workspace, torch.uint8)
         # keep every buffer alive as long as the plan
         self.inputs = (x, dA, B, C, theta, init_state)
@@ -224,7 +226,7 @@ class SelectiveScanPlan:
         if need == 0:
             raise SSDError(2, "selective_scan_workspace_bytes (sizes not supported)")
         if workspace is None:
-            workspace = torch.empty(need, dtype=torch.uint8, device=u.device)
+            workspace = torch.zeros(need, dtype=torch.uint8, device=u.device)   # zero header
         _check_cuda("workspace", workspace, torch.uint8)
         self.inputs = (u, delta, A, B, C, skip)
         self.y, self.workspace = y, workspace
@@ -243,6 +245,16 @@ class SelectiveScanPlan:
 def selective_scan_forward(u, delta, A, B, C, skip=None, *, y=None, workspace=None, stream=None):
     """Diagonal-A selective scan through ``selective_scan_forward`` (all f32).  Returns y."""
     return SelectiveScanPlan(u, delta, A, B, C, skip, y=y, workspace=workspace, stream=stream)()
+
+
+def wait_selftest(workspace: torch.Tensor, wait_ns: int, stream=None) -> None:
+    """Runs the bounded-wait self-test (``ssd_wait_selftest``): a device wait that nothing
+    satisfies gives up after ``wait_ns`` and latches SSD_ERR_TIMEOUT in ``workspace``."""
+    _check_cuda("workspace", workspace, torch.uint8)
+    st = load_library().ssd_wait_selftest(_ptr(workspace), ctypes.c_size_t(workspace.numel()),
+                                          ctypes.c_uint64(int(wait_ns)), _stream_handle(stream))
+    if st != 0:
+        raise SSDError(st, "ssd_wait_selftest")
 
 
 def workspace_status(workspace: torch.Tensor, stream=None):

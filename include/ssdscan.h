@@ -94,7 +94,9 @@ int32_t ssd_chunked_variant(const ssd_shape* shape);
  * Arguments: x, B, C, y are device pointers of io_dtype; dA, theta, init_state, final_state are
  * device f32.  theta may be NULL only if shape->has_theta == 0 (and must be non-NULL otherwise);
  * init_state and final_state may be NULL.  x, B, C, y, dA, final_state must be 16-byte aligned.
- * workspace: device memory of at least ssd_chunked_workspace_bytes(shape), 256-byte aligned.
+ * workspace: device memory of at least ssd_chunked_workspace_bytes(shape), 256-byte aligned; its
+ * first 256 bytes (the error header) must be zero before the first call (ssd_workspace_status
+ * clears them again after reporting an error; the rest is scratch).
  * stream: cudaStream_t as void*.
  * Errors: INVALID_ARG / UNSUPPORTED / WORKSPACE are detected on the host before any launch and
  * leave every output untouched; CUDA reports a failed launch.  Device-side waits that give up
@@ -157,6 +159,18 @@ ssd_status selective_scan_forward_noalloc(const float* u, const float* delta, co
  * device-recorded detail word (0 when none).
  */
 ssd_status ssd_workspace_status(void* workspace, void* stream, int64_t* detail);
+
+/*
+ * Failure-path self-test (the pages have no counterpart).  Launches one thread on `stream` that
+ * waits on a device barrier nothing arrives on, for at most wait_ns nanoseconds (1 .. 1e8), and
+ * then latches SSD_ERR_TIMEOUT with detail 900 in the workspace header, exactly as a pipeline
+ * wait of the forward kernels does when it gives up.  ssd_workspace_status then reports it.
+ * workspace: device memory of at least 256 bytes, 256-byte aligned, header zeroed (as for every
+ * workspace before its first use).  Returns SSD_ERR_WORKSPACE / SSD_ERR_INVALID_ARG for bad
+ * arguments (nothing launched), SSD_ERR_CUDA if the launch failed, else SSD_OK.
+ */
+ssd_status ssd_wait_selftest(void* workspace, size_t workspace_bytes, uint64_t wait_ns,
+                             void* stream);
 
 /* Human-readable name of a status code (static storage). */
 const char* ssd_status_string(ssd_status status);

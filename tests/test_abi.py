@@ -147,3 +147,16 @@ def test_selective_scan_rejections(lib):
     bad[0] = _VP(None)
     assert f(*bad, 1, 16, 8, 16, _VP(A16), ctypes.c_size_t(1 << 20), _VP(None)) == 1
     assert f(*args, 1, 16, 8, 16, _VP(A16), ctypes.c_size_t(8), _VP(None)) == 4
+
+
+@no_gpu_only
+def test_wait_selftest_argument_checks(lib):
+    """Rejected on the host before any launch (no GPU needed)."""
+    f = lib.ssd_wait_selftest
+    f.restype = ctypes.c_int
+    f.argtypes = [_VP, ctypes.c_size_t, ctypes.c_uint64, _VP]
+    assert f(None, 256, 1000, None) == 4                      # no workspace
+    assert f(_VP(A16 + 16), 256, 1000, None) == 4             # not 256-byte aligned
+    assert f(_VP(A16), 128, 1000, None) == 4                  # smaller than the header
+    assert f(_VP(A16), 256, 0, None) == 1                     # no wait
+    assert f(_VP(A16), 256, 200_000_000, None) == 1           # above the 100 ms cap
