@@ -10,6 +10,8 @@
 // d_state states in registers; loads of u/delta/y are coalesced over d.
 #include <math.h>
 
+#include <algorithm>
+
 #include <mutex>
 
 #include "common.cuh"
@@ -126,7 +128,8 @@ cudaError_t launch_nb(const SelectiveScanParams& p, cudaStream_t st) {
 // ------------------------------------------------------------------------------------------------
 constexpr int kSsWarps = 4;
 constexpr int kSsSteps = 64;
-constexpr int kSsStages = 4;
+constexpr int kSsStages = 3;
+constexpr int kSsTargetWarpsPerSM = 16;   // segments are added until about this many warps exist
 
 // 16-byte global->shared copy; src_bytes 0 writes zeros without reading.
 __device__ __forceinline__ void cp_async16(void* dst, const void* src, int src_bytes) {
@@ -151,15 +154,21 @@ struct SsLayout {
   static constexpr size_t kSmemBytes = sizeof(float) * kStageFloats * kSsStages;
 };
 
-template <int LPC>
+// kOut = false: the segment's end state from a zero start and its summed delta (segments
+// 0 .. nseg-2; no C, no output).  kOut = true: the segment from its true input state (left in
+// agg_h by the carry pass) with y.
+template <int LPC, bool kOut>
 __global__ void __launch_bounds__(32 * kSsWarps) ss_onepass_kernel(SelectiveScanParams p) {
   using Lay = SsLayout<LPC>;
   constexpr int kN = Lay::kN, kCpb = Lay::kCpb;
   extern __shared__ __align__(16) float ss_sm[];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t groups = (p.D + kCpb - 1) / kCpb;
-  const int64_t b = blockIdx.x / groups;
-  const int64_t d0 = (blockIdx.x % groups) * kCpb;
+  const int64_t nrun = kOut ? p.nseg : p.nseg - 1;      // segments this pass covers
+  const int64_t seg = blockIdx.x % nrun;
+  const int64_t bgrp = blockIdx.x / nrun;
+  const int64_t b = bgrp / groups;
+  const int64_t d0 = (bgrp % groups) * kCpb;
   const int cl = warp * Lay::kCpw + lane / LPC;         // channel within the block
   const int64_t d = d0 + cl;
   const int l = lane % LPC;                              // this lane carries states 2l, 2l+1
@@ -168,18 +177,19 @@ __global__ void __launch_bounds__(32 * kSsWarps) ss_onepass_kernel(SelectiveScan
   const float kLog2e = 1.4426950408889634f;
   const float a0 = dv ? p.A[dd * kN + 2 * l] * kLog2e : 0.f;
   const float a1 = dv ? p.A[dd * kN + 2 * l + 1] * kLog2e : 0.f;
-  const float sk = (dv && l == 0 && p.skip) ? p.skip[dd] : 0.f;   // skip term added once
+  const float sk = (dv && p.skip) ? p.skip[dd] : 0.f;
   const int64_t T = p.T, D = p.D;
-  const int64_t nst = (T + kSsSteps - 1) / kSsSteps;
+  const int64_t t_beg = seg * p.seg_len, t_end = min(T, t_beg + p.seg_len);
+  const int64_t nst = (t_end - t_beg + kSsSteps - 1) / kSsSteps;
 
   auto issue = [&](int64_t st) {
     float* sm = ss_sm + (st % kSsStages) * Lay::kStageFloats;
-    const int64_t t0 = st * kSsSteps;
+    const int64_t t0 = t_beg + st * kSsSteps;
     constexpr int kDtChunks = kSsSteps * kCpb / 4, kBChunks = kSsSteps * kN / 4;
     for (int c = threadIdx.x; c < kDtChunks; c += 32 * kSsWarps) {
       const int k = c / (kCpb / 4), q = c % (kCpb / 4);
       const int64_t t = t0 + k, dc = d0 + 4 * q;
-      const bool ok = t < T && dc < D;
+      const bool ok = t < t_end && dc < D;
       const int64_t off = ok ? (b * T + t) * D + dc : 0;
       cp_async16(sm + k * kCpb + 4 * q, p.delta + off, ok ? 16 : 0);
       cp_async16(sm + Lay::kDtFloats + k * kCpb + 4 * q, p.u + off, ok ? 16 : 0);
@@ -187,11 +197,12 @@ __global__ void __launch_bounds__(32 * kSsWarps) ss_onepass_kernel(SelectiveScan
     for (int c = threadIdx.x; c < kBChunks; c += 32 * kSsWarps) {
       const int k = c / (kN / 4), q = c % (kN / 4);
       const int64_t t = t0 + k;
-      const bool ok = t < T;
+      const bool ok = t < t_end;
       const int64_t off = ok ? (b * T + t) * kN + 4 * q : 0;
       cp_async16(sm + 2 * Lay::kDtFloats + k * kN + 4 * q, p.B + off, ok ? 16 : 0);
-      cp_async16(sm + 2 * Lay::kDtFloats + Lay::kBFloats + k * kN + 4 * q, p.C + off,
-                 ok ? 16 : 0);
+      if (kOut)
+        cp_async16(sm + 2 * Lay::kDtFloats + Lay::kBFloats + k * kN + 4 * q, p.C + off,
+                   ok ? 16 : 0);
     }
   };
 
@@ -201,7 +212,12 @@ __global__ void __launch_bounds__(32 * kSsWarps) ss_onepass_kernel(SelectiveScan
     cp_async_commit();
   }
   float* yp = p.y + b * T * D + dd;
-  float h0 = 0.f, h1 = 0.f;
+  float* agg = p.agg_h + ((b * p.nseg + seg) * kN + 2 * l) * D + dd;   // [b, seg, n, d]
+  float h0 = 0.f, h1 = 0.f, sdt_sum = 0.f;
+  if (kOut && seg > 0 && dv) {   // segment-input state from the carry pass
+    h0 = agg[0];
+    h1 = agg[D];
+  }
 #pragma unroll 1
   for (int64_t st = 0; st < nst; ++st) {
     if (st + kSsStages - 1 < nst) issue(st + kSsStages - 1);
@@ -213,8 +229,21 @@ __global__ void __launch_bounds__(32 * kSsWarps) ss_onepass_kernel(SelectiveScan
     const float* su = sm + Lay::kDtFloats + cl;
     const float* sB = sm + 2 * Lay::kDtFloats + 2 * l;
     const float* sC = sm + 2 * Lay::kDtFloats + Lay::kBFloats + 2 * l;
-    const int64_t t0 = st * kSsSteps;
-    // unrolled over the whole stage so one group's reduction overlaps the next group's steps
+    const int64_t t0 = t_beg + st * kSsSteps;
+    if constexpr (!kOut) {
+#pragma unroll 16
+      for (int kk = 0; kk < kSsSteps; ++kk) {
+        const float dt = sdt[kk * kCpb], uu = su[kk * kCpb];
+        const float2 bb = *reinterpret_cast<const float2*>(sB + kk * kN);
+        const float du = dt * uu;   // zero-filled steps past the segment: dt = 0 keeps h
+        const float2 e = make_float2(fp::ex2_approx(a0 * dt), fp::ex2_approx(a1 * dt));
+        const float2 h = fp::fma2(e, make_float2(h0, h1), fp::mul2(make_float2(du, du), bb));
+        h0 = h.x;
+        h1 = h.y;
+        sdt_sum += dt;
+      }
+    } else {
+      // unrolled over the whole stage so one group's reduction overlaps the next group's steps
 #pragma unroll
     for (int k0 = 0; k0 < kSsSteps; k0 += LPC) {
       float v[LPC];
@@ -229,7 +258,7 @@ __global__ void __launch_bounds__(32 * kSsWarps) ss_onepass_kernel(SelectiveScan
         const float2 h = fp::fma2(e, make_float2(h0, h1), fp::mul2(make_float2(du, du), bb));
         h0 = h.x;
         h1 = h.y;
-        v[k] = fmaf(cc.x, h0, fmaf(cc.y, h1, sk * uu));
+        v[k] = fmaf(cc.x, h0, cc.y * h1);
       }
       // transpose-reduce over the LPC lanes of the channel: at the level with lane bit m the
       // lanes with that bit keep the upper half of their values, the others the lower half,
@@ -245,22 +274,75 @@ __global__ void __launch_bounds__(32 * kSsWarps) ss_onepass_kernel(SelectiveScan
         }
       }
       const int64_t t = t0 + k0 + l;
-      if (dv && t < T) yp[t * D] = v[0];
+      if (dv && t < t_end) yp[t * D] = fmaf(sk, su[(k0 + l) * kCpb], v[0]);   // + skip * u
+    }
     }
     __syncthreads();   // the stage's buffer is refilled by a later issue
   }
+  if (!kOut && dv) {
+    agg[0] = h0;
+    agg[D] = h1;
+    if (l == 0) p.agg_dt[(b * p.nseg + seg) * D + dd] = sdt_sum;
+  }
+}
+
+// Segment-input states for the one-pass path, one thread per (b, state n, d): h_in(0) = 0,
+// h_in(s+1) = exp(A[d,n] * sum delta_s) h_in(s) + end_s, written over end_s in place.
+__global__ void __launch_bounds__(kSsThreads) ss_carry_states_kernel(SelectiveScanParams p) {
+  const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= p.batch * p.N * p.D) return;
+  const int64_t d = idx % p.D, n = (idx / p.D) % p.N, b = idx / (p.D * p.N);
+  const float a = p.A[d * p.N + n];
+  float h = 0.f;
+  for (int64_t s = 0; s + 1 < p.nseg; ++s) {
+    float* q = p.agg_h + ((b * p.nseg + s) * p.N + n) * p.D + d;
+    const float end = *q;
+    *q = h;
+    h = expf(a * p.agg_dt[(b * p.nseg + s) * p.D + d]) * h + end;
+  }
+  p.agg_h[((b * p.nseg + p.nseg - 1) * p.N + n) * p.D + d] = h;
 }
 
 template <int LPC>
 cudaError_t launch_onepass(const SelectiveScanParams& p, cudaStream_t st) {
   using Lay = SsLayout<LPC>;
-  const int64_t blocks = p.batch * ((p.D + Lay::kCpb - 1) / Lay::kCpb);
+  const int64_t groups = p.batch * ((p.D + Lay::kCpb - 1) / Lay::kCpb);
+  // Segments of T (each at least 256 steps, a multiple of the staging step) until about
+  // kSsTargetWarpsPerSM warps per SM exist: one warp per scheduler cannot hide the latency of
+  // its serial recurrence.  The extra cost is one more exponential per step of every segment
+  // but the last (the state-only pass).
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  const int64_t warps = groups * kSsWarps;
+  int64_t nseg = ((int64_t)sms * kSsTargetWarpsPerSM + warps - 1) / warps;
+  nseg = std::max<int64_t>(1, std::min<int64_t>(nseg, p.T / 256));
+  int64_t seg_len = (p.T + nseg - 1) / nseg;
+  seg_len = (seg_len + kSsSteps - 1) / kSsSteps * kSsSteps;
+  SelectiveScanParams q = p;
+  q.seg_len = seg_len;
+  q.nseg = (p.T + seg_len - 1) / seg_len;   // <= ceil(T / 64): fits the workspace's segment arrays
   if (Lay::kSmemBytes > 48 * 1024) {
-    const cudaError_t e = cudaFuncSetAttribute(
-        ss_onepass_kernel<LPC>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Lay::kSmemBytes);
-    if (e != cudaSuccess) return e;
+    if ((e = cudaFuncSetAttribute(ss_onepass_kernel<LPC, false>,
+                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  (int)Lay::kSmemBytes)) != cudaSuccess)
+      return e;
+    if ((e = cudaFuncSetAttribute(ss_onepass_kernel<LPC, true>,
+                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  (int)Lay::kSmemBytes)) != cudaSuccess)
+      return e;
   }
-  ss_onepass_kernel<LPC><<<(unsigned)blocks, 32 * kSsWarps, Lay::kSmemBytes, st>>>(p);
+  if (q.nseg > 1) {
+    ss_onepass_kernel<LPC, false>
+        <<<(unsigned)(groups * (q.nseg - 1)), 32 * kSsWarps, Lay::kSmemBytes, st>>>(q);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    ss_carry_states_kernel<<<(unsigned)((q.batch * q.N * q.D + kSsThreads - 1) / kSsThreads),
+                             kSsThreads, 0, st>>>(q);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  ss_onepass_kernel<LPC, true>
+      <<<(unsigned)(groups * q.nseg), 32 * kSsWarps, Lay::kSmemBytes, st>>>(q);
   return cudaGetLastError();
 }
 
