@@ -116,20 +116,20 @@ cudaError_t launch_nb(const SelectiveScanParams& p, cudaStream_t st) {
 }
 
 // ------------------------------------------------------------------------------------------------
-// One-pass selective scan for d_state N = 2 * LPC in {8, 16, 32, 64} and d_model % 4 == 0.
-// A warp owns 32 / LPC channels d of one batch row; the LPC lanes of a channel each carry two
-// of its N states through the whole sequence, so every exp(delta * A) is evaluated exactly
-// once (2^x on the special-function unit with A pre-scaled by log2 e) and no segment state
-// goes to memory.  Every LPC steps the lanes of a channel sum their C . h partials with a
-// transpose-reduce (log2 LPC shuffle levels), after which lane l holds y of step t0 + l.
-// The block's delta, u, B and C rows are staged through shared memory in a ring of
-// kSsStages stages of kSsSteps steps (16-byte cp.async, zero-filled past T and D), so loads
-// run several stages ahead of the serial recurrence.
+// One-pass selective scan for d_state N = 4 * LPC in {8, 16, 32, 64} and d_model % 4 == 0.
+// A warp owns 32 / LPC channels d of one batch row; the LPC lanes of a channel each carry four
+// of its N states, so every exp(delta * A) is evaluated on the special-function unit (2^x with
+// A pre-scaled by log2 e) and only segment boundary states go to memory.  T is cut into
+// segments (at least 256 steps) so that enough warps exist: a state-only pass gives each
+// segment's end state from zero, a carry pass chains them, and the output pass runs each
+// segment from its true input state.  Every LPC steps the lanes of a channel sum their C . h
+// partials with a transpose-reduce (log2 LPC shuffle levels), after which lane l holds y of
+// step t0 + l.  The block's delta, u, B and C rows are staged through shared memory in a ring
+// of kSsStages stages of kSsSteps steps (16-byte cp.async, zero-filled past the segment and D).
 // ------------------------------------------------------------------------------------------------
 constexpr int kSsWarps = 4;
 constexpr int kSsSteps = 64;
-constexpr int kSsStages = 3;
-constexpr int kSsTargetWarpsPerSM = 16;   // segments are added until about this many warps exist
+constexpr int kSsStages = 2;
 
 // 16-byte global->shared copy; src_bytes 0 writes zeros without reading.
 __device__ __forceinline__ void cp_async16(void* dst, const void* src, int src_bytes) {
@@ -143,9 +143,9 @@ __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
-template <int LPC>
+template <int SPL, int LPC>
 struct SsLayout {
-  static constexpr int kN = 2 * LPC;
+  static constexpr int kN = SPL * LPC;                   // d_state
   static constexpr int kCpw = 32 / LPC;                  // channels per warp
   static constexpr int kCpb = kCpw * kSsWarps;           // channels per block
   static constexpr int kDtFloats = kSsSteps * kCpb;
@@ -154,12 +154,38 @@ struct SsLayout {
   static constexpr size_t kSmemBytes = sizeof(float) * kStageFloats * kSsStages;
 };
 
+// SPL consecutive floats (8 or 16 bytes) from shared memory.
+template <int SPL>
+__device__ __forceinline__ void ld_states(const float* src, float (&v)[SPL]) {
+  if constexpr (SPL == 4) {
+    const float4 f = *reinterpret_cast<const float4*>(src);
+    v[0] = f.x; v[1] = f.y; v[2] = f.z; v[3] = f.w;
+  } else {
+    const float2 f = *reinterpret_cast<const float2*>(src);
+    v[0] = f.x; v[1] = f.y;
+  }
+}
+
+// One step of SPL states: h <- exp(A dt) h + (dt u) B, exponentials as 2^(A log2e dt).
+template <int SPL>
+__device__ __forceinline__ void ss_step(const float (&a)[SPL], float dt, float du,
+                                        const float (&bb)[SPL], float (&h)[SPL]) {
+#pragma unroll
+  for (int j = 0; j < SPL; j += 2) {
+    const float2 e = make_float2(fp::ex2_approx(a[j] * dt), fp::ex2_approx(a[j + 1] * dt));
+    const float2 r =
+        fp::fma2(e, make_float2(h[j], h[j + 1]), fp::mul2(make_float2(du, du), make_float2(bb[j], bb[j + 1])));
+    h[j] = r.x;
+    h[j + 1] = r.y;
+  }
+}
+
 // kOut = false: the segment's end state from a zero start and its summed delta (segments
 // 0 .. nseg-2; no C, no output).  kOut = true: the segment from its true input state (left in
-// agg_h by the carry pass) with y.
-template <int LPC, bool kOut>
+// agg_h by the carry pass) with y.  Lane l of a channel carries states SPL*l .. SPL*l+SPL-1.
+template <int SPL, int LPC, bool kOut>
 __global__ void __launch_bounds__(32 * kSsWarps) ss_onepass_kernel(SelectiveScanParams p) {
-  using Lay = SsLayout<LPC>;
+  using Lay = SsLayout<SPL, LPC>;
   constexpr int kN = Lay::kN, kCpb = Lay::kCpb;
   extern __shared__ __align__(16) float ss_sm[];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -171,12 +197,16 @@ __global__ void __launch_bounds__(32 * kSsWarps) ss_onepass_kernel(SelectiveScan
   const int64_t d0 = (bgrp % groups) * kCpb;
   const int cl = warp * Lay::kCpw + lane / LPC;         // channel within the block
   const int64_t d = d0 + cl;
-  const int l = lane % LPC;                              // this lane carries states 2l, 2l+1
+  const int l = lane % LPC;
   const bool dv = d < p.D;
   const int64_t dd = dv ? d : 0;
   const float kLog2e = 1.4426950408889634f;
-  const float a0 = dv ? p.A[dd * kN + 2 * l] * kLog2e : 0.f;
-  const float a1 = dv ? p.A[dd * kN + 2 * l + 1] * kLog2e : 0.f;
+  float a[SPL], h[SPL];
+#pragma unroll
+  for (int j = 0; j < SPL; ++j) {
+    a[j] = dv ? p.A[dd * kN + SPL * l + j] * kLog2e : 0.f;
+    h[j] = 0.f;
+  }
   const float sk = (dv && p.skip) ? p.skip[dd] : 0.f;
   const int64_t T = p.T, D = p.D;
   const int64_t t_beg = seg * p.seg_len, t_end = min(T, t_beg + p.seg_len);
@@ -212,11 +242,11 @@ __global__ void __launch_bounds__(32 * kSsWarps) ss_onepass_kernel(SelectiveScan
     cp_async_commit();
   }
   float* yp = p.y + b * T * D + dd;
-  float* agg = p.agg_h + ((b * p.nseg + seg) * kN + 2 * l) * D + dd;   // [b, seg, n, d]
-  float h0 = 0.f, h1 = 0.f, sdt_sum = 0.f;
+  float* agg = p.agg_h + ((b * p.nseg + seg) * kN + SPL * l) * D + dd;   // [b, seg, n, d]
+  float sdt_sum = 0.f;
   if (kOut && seg > 0 && dv) {   // segment-input state from the carry pass
-    h0 = agg[0];
-    h1 = agg[D];
+#pragma unroll
+    for (int j = 0; j < SPL; ++j) h[j] = agg[j * D];
   }
 #pragma unroll 1
   for (int64_t st = 0; st < nst; ++st) {
@@ -227,61 +257,58 @@ __global__ void __launch_bounds__(32 * kSsWarps) ss_onepass_kernel(SelectiveScan
     const float* sm = ss_sm + (st % kSsStages) * Lay::kStageFloats;
     const float* sdt = sm + cl;
     const float* su = sm + Lay::kDtFloats + cl;
-    const float* sB = sm + 2 * Lay::kDtFloats + 2 * l;
-    const float* sC = sm + 2 * Lay::kDtFloats + Lay::kBFloats + 2 * l;
+    const float* sB = sm + 2 * Lay::kDtFloats + SPL * l;
+    const float* sC = sm + 2 * Lay::kDtFloats + Lay::kBFloats + SPL * l;
     const int64_t t0 = t_beg + st * kSsSteps;
     if constexpr (!kOut) {
 #pragma unroll 16
       for (int kk = 0; kk < kSsSteps; ++kk) {
         const float dt = sdt[kk * kCpb], uu = su[kk * kCpb];
-        const float2 bb = *reinterpret_cast<const float2*>(sB + kk * kN);
-        const float du = dt * uu;   // zero-filled steps past the segment: dt = 0 keeps h
-        const float2 e = make_float2(fp::ex2_approx(a0 * dt), fp::ex2_approx(a1 * dt));
-        const float2 h = fp::fma2(e, make_float2(h0, h1), fp::mul2(make_float2(du, du), bb));
-        h0 = h.x;
-        h1 = h.y;
+        float bb[SPL];
+        ld_states<SPL>(sB + kk * kN, bb);
+        ss_step<SPL>(a, dt, dt * uu, bb, h);   // zero-filled steps past the segment keep h
         sdt_sum += dt;
       }
     } else {
       // unrolled over the whole stage so one group's reduction overlaps the next group's steps
 #pragma unroll
-    for (int k0 = 0; k0 < kSsSteps; k0 += LPC) {
-      float v[LPC];
+      for (int k0 = 0; k0 < kSsSteps; k0 += LPC) {
+        float v[LPC];
 #pragma unroll
-      for (int k = 0; k < LPC; ++k) {
-        const int kk = k0 + k;
-        const float dt = sdt[kk * kCpb], uu = su[kk * kCpb];
-        const float2 bb = *reinterpret_cast<const float2*>(sB + kk * kN);
-        const float2 cc = *reinterpret_cast<const float2*>(sC + kk * kN);
-        const float du = dt * uu;   // zero-filled steps past T: dt = 0 keeps h
-        const float2 e = make_float2(fp::ex2_approx(a0 * dt), fp::ex2_approx(a1 * dt));
-        const float2 h = fp::fma2(e, make_float2(h0, h1), fp::mul2(make_float2(du, du), bb));
-        h0 = h.x;
-        h1 = h.y;
-        v[k] = fmaf(cc.x, h0, cc.y * h1);
-      }
-      // transpose-reduce over the LPC lanes of the channel: at the level with lane bit m the
-      // lanes with that bit keep the upper half of their values, the others the lower half,
-      // and each adds its partner's copy of the half it keeps
+        for (int k = 0; k < LPC; ++k) {
+          const int kk = k0 + k;
+          const float dt = sdt[kk * kCpb], uu = su[kk * kCpb];
+          float bb[SPL], cc[SPL];
+          ld_states<SPL>(sB + kk * kN, bb);
+          ld_states<SPL>(sC + kk * kN, cc);
+          ss_step<SPL>(a, dt, dt * uu, bb, h);
+          float acc = cc[0] * h[0];
 #pragma unroll
-      for (int m = LPC / 2, cnt = LPC; m >= 1; m >>= 1, cnt >>= 1) {
-        const bool up_half = (l & m) != 0;
-#pragma unroll
-        for (int i = 0; i < cnt / 2; ++i) {
-          const float send = up_half ? v[i] : v[i + cnt / 2];
-          const float keep = up_half ? v[i + cnt / 2] : v[i];
-          v[i] = keep + __shfl_xor_sync(0xffffffffu, send, m);
+          for (int j = 1; j < SPL; ++j) acc = fmaf(cc[j], h[j], acc);
+          v[k] = acc;
         }
+        // transpose-reduce over the LPC lanes of the channel: at the level with lane bit m
+        // the lanes with that bit keep the upper half of their values, the others the lower
+        // half, and each adds its partner's copy of the half it keeps
+#pragma unroll
+        for (int m = LPC / 2, cnt = LPC; m >= 1; m >>= 1, cnt >>= 1) {
+          const bool up_half = (l & m) != 0;
+#pragma unroll
+          for (int i = 0; i < cnt / 2; ++i) {
+            const float send = up_half ? v[i] : v[i + cnt / 2];
+            const float keep = up_half ? v[i + cnt / 2] : v[i];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, m);
+          }
+        }
+        const int64_t t = t0 + k0 + l;
+        if (dv && t < t_end) yp[t * D] = fmaf(sk, su[(k0 + l) * kCpb], v[0]);   // + skip * u
       }
-      const int64_t t = t0 + k0 + l;
-      if (dv && t < t_end) yp[t * D] = fmaf(sk, su[(k0 + l) * kCpb], v[0]);   // + skip * u
-    }
     }
     __syncthreads();   // the stage's buffer is refilled by a later issue
   }
   if (!kOut && dv) {
-    agg[0] = h0;
-    agg[D] = h1;
+#pragma unroll
+    for (int j = 0; j < SPL; ++j) agg[j * D] = h[j];
     if (l == 0) p.agg_dt[(b * p.nseg + seg) * D + dd] = sdt_sum;
   }
 }
@@ -293,55 +320,72 @@ __global__ void __launch_bounds__(kSsThreads) ss_carry_states_kernel(SelectiveSc
   if (idx >= p.batch * p.N * p.D) return;
   const int64_t d = idx % p.D, n = (idx / p.D) % p.N, b = idx / (p.D * p.N);
   const float a = p.A[d * p.N + n];
+  const int64_t sstride = p.N * p.D;            // from segment s to s + 1 in agg_h
+  float* q = p.agg_h + ((b * p.nseg) * p.N + n) * p.D + d;
+  const float* sd = p.agg_dt + (b * p.nseg) * p.D + d;
   float h = 0.f;
-  for (int64_t s = 0; s + 1 < p.nseg; ++s) {
-    float* q = p.agg_h + ((b * p.nseg + s) * p.N + n) * p.D + d;
-    const float end = *q;
-    *q = h;
-    h = expf(a * p.agg_dt[(b * p.nseg + s) * p.D + d]) * h + end;
+  for (int64_t s0 = 0; s0 + 1 < p.nseg; s0 += 8) {   // loads eight segments ahead of the chain
+    float ev[8], dv[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const bool in = s0 + k + 1 < p.nseg;
+      ev[k] = in ? q[(s0 + k) * sstride] : 0.f;
+      dv[k] = in ? sd[(s0 + k) * p.D] : 0.f;
+    }
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      if (s0 + k + 1 < p.nseg) {
+        q[(s0 + k) * sstride] = h;
+        h = expf(a * dv[k]) * h + ev[k];
+      }
+    }
   }
-  p.agg_h[((b * p.nseg + p.nseg - 1) * p.N + n) * p.D + d] = h;
+  q[(p.nseg - 1) * sstride] = h;
 }
 
-template <int LPC>
+template <int SPL, int LPC>
 cudaError_t launch_onepass(const SelectiveScanParams& p, cudaStream_t st) {
-  using Lay = SsLayout<LPC>;
+  using Lay = SsLayout<SPL, LPC>;
   const int64_t groups = p.batch * ((p.D + Lay::kCpb - 1) / Lay::kCpb);
-  // Segments of T (each at least 256 steps, a multiple of the staging step) until about
-  // kSsTargetWarpsPerSM warps per SM exist: one warp per scheduler cannot hide the latency of
-  // its serial recurrence.  The extra cost is one more exponential per step of every segment
-  // but the last (the state-only pass).
+  // Segments of T (each at least 256 steps, a multiple of the staging step) until the output
+  // pass fills one wave of resident blocks: one warp per scheduler cannot hide the latency of
+  // its serial recurrence, and a second partial wave would idle most SMs.  The extra cost is
+  // one more exponential per step of every segment but the last (the state-only pass).
   int dev = 0, sms = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
-  const int64_t warps = groups * kSsWarps;
-  int64_t nseg = ((int64_t)sms * kSsTargetWarpsPerSM + warps - 1) / warps;
+  if (Lay::kSmemBytes > 48 * 1024) {
+    if ((e = cudaFuncSetAttribute(ss_onepass_kernel<SPL, LPC, false>,
+                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  (int)Lay::kSmemBytes)) != cudaSuccess)
+      return e;
+    if ((e = cudaFuncSetAttribute(ss_onepass_kernel<SPL, LPC, true>,
+                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  (int)Lay::kSmemBytes)) != cudaSuccess)
+      return e;
+  }
+  int per_sm = 0;
+  if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, ss_onepass_kernel<SPL, LPC, true>,
+                                                          32 * kSsWarps, Lay::kSmemBytes)) !=
+      cudaSuccess)
+    return e;
+  int64_t nseg = std::max<int64_t>(1, (int64_t)sms * std::max(per_sm, 1) / groups);
   nseg = std::max<int64_t>(1, std::min<int64_t>(nseg, p.T / 256));
   int64_t seg_len = (p.T + nseg - 1) / nseg;
   seg_len = (seg_len + kSsSteps - 1) / kSsSteps * kSsSteps;
   SelectiveScanParams q = p;
   q.seg_len = seg_len;
   q.nseg = (p.T + seg_len - 1) / seg_len;   // <= ceil(T / 64): fits the workspace's segment arrays
-  if (Lay::kSmemBytes > 48 * 1024) {
-    if ((e = cudaFuncSetAttribute(ss_onepass_kernel<LPC, false>,
-                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  (int)Lay::kSmemBytes)) != cudaSuccess)
-      return e;
-    if ((e = cudaFuncSetAttribute(ss_onepass_kernel<LPC, true>,
-                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  (int)Lay::kSmemBytes)) != cudaSuccess)
-      return e;
-  }
   if (q.nseg > 1) {
-    ss_onepass_kernel<LPC, false>
+    ss_onepass_kernel<SPL, LPC, false>
         <<<(unsigned)(groups * (q.nseg - 1)), 32 * kSsWarps, Lay::kSmemBytes, st>>>(q);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     ss_carry_states_kernel<<<(unsigned)((q.batch * q.N * q.D + kSsThreads - 1) / kSsThreads),
                              kSsThreads, 0, st>>>(q);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
-  ss_onepass_kernel<LPC, true>
+  ss_onepass_kernel<SPL, LPC, true>
       <<<(unsigned)(groups * q.nseg), 32 * kSsWarps, Lay::kSmemBytes, st>>>(q);
   return cudaGetLastError();
 }
@@ -353,17 +397,17 @@ int64_t ss_segment_length(int64_t) { return kSegLen; }
 bool selective_scan_onepass_supported(int64_t batch, int64_t D, int64_t N) {
   if (N != 8 && N != 16 && N != 32 && N != 64) return false;
   if (D % 4 != 0) return false;                      // 16-byte staging of delta / u rows
-  const int64_t cpb = 64 / N * kSsWarps;             // channels per block
+  const int64_t cpb = 128 / N * kSsWarps;            // channels per block (4 states per lane)
   const int64_t blocks = batch * ((D + cpb - 1) / cpb);
   return blocks <= 0x7fffffffLL;
 }
 
 cudaError_t selective_scan_onepass_launch(const SelectiveScanParams& p, cudaStream_t st) {
   switch (p.N) {
-    case 8: return launch_onepass<4>(p, st);
-    case 16: return launch_onepass<8>(p, st);
-    case 32: return launch_onepass<16>(p, st);
-    case 64: return launch_onepass<32>(p, st);
+    case 8: return launch_onepass<4, 2>(p, st);
+    case 16: return launch_onepass<4, 4>(p, st);
+    case 32: return launch_onepass<4, 8>(p, st);
+    case 64: return launch_onepass<4, 16>(p, st);
     default: return cudaErrorInvalidValue;
   }
 }
