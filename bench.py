@@ -199,8 +199,7 @@ def run_ours(args, rank, world, local):
                                 theta=d["theta"], init_state=d["init_state"], y=y,
                                 final_state=fin, workspace=ws, stream=stream)
         variant = pkg.ssd_chunked_variant(shape)
-        launches_per_call = {"generic": 3 + (2 if cfg.theta else 0),
-                             "tiled_f32": 3 + (2 if cfg.theta else 0)}.get(variant, 1)
+        launches_per_call = pkg.ssd_chunked_launches(shape)
         dtype = cfg.dtype
         io_bytes = cfg.io_bytes()
         flops = cfg.causal_flops()

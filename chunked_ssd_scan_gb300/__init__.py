@@ -17,7 +17,7 @@ from . import workloads  # noqa: F401  (seeded synthetic inputs; no scan arithme
 
 __all__ = [
     "SSDError", "load_library", "ssd_shape", "ssd_chunked_workspace_bytes", "ssd_chunked_variant",
-    "ssd_chunked_forward", "SSDForwardPlan", "SelectiveScanPlan", "selective_scan_workspace_bytes", "selective_scan_forward",
+    "ssd_chunked_launches", "ssd_chunked_forward", "SSDForwardPlan", "SelectiveScanPlan", "selective_scan_workspace_bytes", "selective_scan_forward",
     "workspace_status", "wait_selftest", "STATUS", "VARIANTS",
 ]
 
@@ -64,6 +64,8 @@ def load_library(path: Optional[str] = None):
     lib.ssd_chunked_workspace_bytes.argtypes = [SP]
     lib.ssd_chunked_variant.restype = ctypes.c_int32
     lib.ssd_chunked_variant.argtypes = [SP]
+    lib.ssd_chunked_launches.restype = ctypes.c_int32
+    lib.ssd_chunked_launches.argtypes = [SP]
     lib.ssd_chunked_forward.restype = ctypes.c_int
     lib.ssd_chunked_forward.argtypes = [SP] + [_VP] * 9 + [ctypes.c_size_t, _VP]
     lib.selective_scan_workspace_bytes.restype = ctypes.c_size_t
@@ -119,6 +121,11 @@ def ssd_chunked_workspace_bytes(shape: ssd_shape) -> int:
 
 def ssd_chunked_variant(shape: ssd_shape) -> str:
     return VARIANTS.get(int(load_library().ssd_chunked_variant(ctypes.byref(shape))), "none")
+
+
+def ssd_chunked_launches(shape: ssd_shape) -> int:
+    """Kernel launches per ``ssd_chunked_forward`` call for ``shape`` on the current device."""
+    return int(load_library().ssd_chunked_launches(ctypes.byref(shape)))
 
 
 def shape_of(x: torch.Tensor, B: torch.Tensor, chunk_len: int, has_theta: bool) -> ssd_shape:

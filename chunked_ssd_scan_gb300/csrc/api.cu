@@ -60,7 +60,7 @@ int32_t pick_variant(const ssd_shape* s) {
 SsdLayout ssd_layout(const ssd_shape* s) {
   SsdLayout L;
   if (pick_variant(s) == SSD_VARIANT_TC_BF16) {   // the fused kernel keeps its state on chip
-    L.total = sizeof(WsHeader);
+    L.total = fused_bf16_workspace_bytes(s->batch, s->seqlen, s->nheads, s->mimo_rank);
     return L;
   }
   const int64_t nch = s->seqlen / s->chunk_len;
@@ -91,6 +91,14 @@ extern "C" {
 size_t ssd_chunked_workspace_bytes(const ssd_shape* shape) {
   if (check_shape(shape) != SSD_OK) return 0;
   return ssd_layout(shape).total;
+}
+
+int32_t ssd_chunked_launches(const ssd_shape* shape) {
+  if (check_shape(shape) != SSD_OK) return 0;
+  const int32_t v = pick_variant(shape);
+  if (v == SSD_VARIANT_TC_BF16)
+    return fused_bf16_launches(shape->batch, shape->seqlen, shape->nheads, shape->mimo_rank);
+  return 3 + (shape->has_theta ? 2 : 0);
 }
 
 int32_t ssd_chunked_variant(const ssd_shape* shape) {

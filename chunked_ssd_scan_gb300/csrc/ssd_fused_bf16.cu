@@ -42,6 +42,7 @@
 #include <math.h>
 #include <string.h>
 
+#include <algorithm>
 #include <atomic>
 #include <mutex>
 
@@ -119,6 +120,15 @@ struct FusedArgs {
   __nv_bfloat16* y;
   WsHeader* hdr;
   int32_t T, R, H, G, ntiles, steps;   // steps = time steps per tile (128 / R)
+  // Time segments: each (batch, head) sequence is cut into nseg segments of seg_tiles tiles
+  // (the last may be shorter), each run by its own CTA.  The state-only pre-pass writes the
+  // end state of every segment but the last (from the true initial state for segment 0, from
+  // zero otherwise) to seg_end and the segment's decay exp(sum dA) to seg_decay; a carry pass
+  // turns them into the true initial state of every segment (seg_init).
+  int32_t nseg, seg_tiles;
+  const float* seg_init;   // [b*H*nseg][P][N] (segment 0 unused: it starts from init)
+  float* seg_end;          // [b*H*nseg][P][N]
+  float* seg_decay;        // [b*H*nseg]
 };
 
 __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatile int* abort,
@@ -194,6 +204,9 @@ __device__ __forceinline__ void mask_block(const TileInfo& ti, int cb, bool exac
   }
 }
 
+// kPre = true: the state-only pre-pass of a segment (K1, (dec o x), K3, K4; no CB, mask, Yd, Yo
+// or output).  kPre = false: the full forward of a segment.
+template <bool kPre>
 __global__ void __launch_bounds__(kThreadsFused, 1)
     ssd_fused_bf16_kernel(FusedArgs a, const __grid_constant__ CUtensorMap tm_x,
                           const __grid_constant__ CUtensorMap tm_b,
@@ -213,11 +226,15 @@ __global__ void __launch_bounds__(kThreadsFused, 1)
   // warp index broadcast from lane 0: provably uniform, so role branches stay convergent
   const int warp = __shfl_sync(0xffffffffu, static_cast<int>(threadIdx.x / 32), 0);
   const int lane = threadIdx.x % 32;
-  const int seq = blockIdx.x;                 // (b, h)
+  const int nrun = kPre ? a.nseg - 1 : a.nseg;   // segments this launch runs per sequence
+  const int seq = blockIdx.x / nrun;             // (b, h)
+  const int seg = blockIdx.x % nrun;
   const int b = seq / a.H, h = seq % a.H;
   const int g = h / (a.H / a.G);
-  const int R = a.R, steps = a.steps, nt = a.ntiles;
-  const int row_base = b * a.T * R;           // fused row of (b, t=0, r=0)
+  const int R = a.R, steps = a.steps;
+  const int tbase = seg * a.seg_tiles;           // first tile of this segment
+  const int nt = min(a.ntiles - tbase, a.seg_tiles);
+  const int row_base = b * a.T * R + tbase * kTileRows;   // fused row of the segment's start
   volatile int* abort = &s_abort;
 
   if (threadIdx.x == 0) {
@@ -255,7 +272,7 @@ __global__ void __launch_bounds__(kThreadsFused, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------------ TMA producer
-    const uint32_t tx = kXBytes + 2 * kBCBytes;
+    const uint32_t tx = kPre ? kXBytes + kBCBytes : kXBytes + 2 * kBCBytes;
     for (int t = 0; t < nt; ++t) {
       const int s = t & 1;
       if (t >= 2 && !wait_bar(&bars->empty[s], ((t - 2) >> 1) & 1, abort, a.hdr, 1)) break;
@@ -265,9 +282,11 @@ __global__ void __launch_bounds__(kThreadsFused, 1)
       tma_load_3d_elect(smem + kOffB + s * kBCBytes, &tm_b, &bars->full[s], 0, g, row);
       tma_load_3d_elect(smem + kOffB + s * kBCBytes + kBCBytes / 2, &tm_b, &bars->full[s], 64, g,
                         row);
-      tma_load_3d_elect(smem + kOffC + s * kBCBytes, &tm_c, &bars->full[s], 0, g, row);
-      tma_load_3d_elect(smem + kOffC + s * kBCBytes + kBCBytes / 2, &tm_c, &bars->full[s], 64, g,
-                        row);
+      if (!kPre) {   // the pre-pass needs no C
+        tma_load_3d_elect(smem + kOffC + s * kBCBytes, &tm_c, &bars->full[s], 0, g, row);
+        tma_load_3d_elect(smem + kOffC + s * kBCBytes + kBCBytes / 2, &tm_c, &bars->full[s], 64,
+                          g, row);
+      }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
@@ -293,6 +312,25 @@ __global__ void __launch_bounds__(kThreadsFused, 1)
       }
       mma_commit_elect(&bars->cb_full);
     };
+    if constexpr (kPre) {
+      // K3 only; (dec o x)_lo of tile t sits in the (unused) C stage t & 1
+      for (int t = 0; t < nt; ++t) {
+        const int s = t & 1;
+        const uint32_t sB = smem_u32(smem + kOffB + s * kBCBytes);
+        const uint32_t sX = smem_u32(smem + kOffX + s * kXBytes);
+        const uint32_t lbo_x = smem_u32(smem + kOffC + s * kXBytes) - sX;
+        if (!wait_bar(&bars->hb_full, t & 1, abort, a.hdr, 7)) break;
+        if (!wait_bar(&bars->xs_ready, t & 1, abort, a.hdr, 10)) break;
+        tc_fence_after();
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+          mma_bf16_elect(tmem + kColS, sdesc_sw128(sB + ks * 2048, kBCBytes / 2, 1024),
+                         sdesc_sw128(sX + ks * 2048, lbo_x, 1024), id_k3, 1);
+        }
+        mma_commit_elect(&bars->s_full);
+        if (t + 2 < nt) mma_commit_elect(&bars->empty[s]);
+      }
+    } else {
     bool ok = wait_bar(&bars->full[0], 0, abort, a.hdr, 2);
     if (ok) issue_cb(0);
     for (int t = 0; ok && t < nt; ++t) {
@@ -340,13 +378,14 @@ __global__ void __launch_bounds__(kThreadsFused, 1)
       mma_commit_elect(&bars->s_full);
       if (t + 2 < nt) mma_commit_elect(&bars->empty[s]);
     }
+    }
   } else if (warp == 2) {
     // ------------------------------------------------------------------ K1 (one warp)
     // Reads dA straight from global memory (one tile ahead, into registers) and publishes the
     // tile's prefix sums and decay factors into a ring of kInfoSlots slots.
     const int per = (steps + 31) / 32;                 // steps per lane (<= 4)
     const int beg = min(steps, lane * per), end = min(steps, beg + per);
-    const float* dsrc = a.dA + (size_t)b * a.T * a.H + h;
+    const float* dsrc = a.dA + ((size_t)b * a.T + (size_t)tbase * steps) * a.H + h;
     float dnext[4];
     auto load_tile = [&](int t) {
 #pragma unroll
@@ -459,13 +498,20 @@ __global__ void __launch_bounds__(kThreadsFused, 1)
       // mask blocks max(q-1, 0) .. q (the diagonal block is exact), zero blocks q+1 .. 3
       const int cb0 = q >= 1 ? q - 1 : 0;
       const int ub = xs_unit_begin(q), ue = xs_unit_end(q);
-      uint8_t* xlo = smem + kOffXlo;
       // (dec o x) of tile t, split: hi in place of x (after Yd_t has read x), lo in its own
-      // buffer; this warp's units of 32 rows x 16 columns
+      // buffer (in the pre-pass, the unused C stage of the tile); this warp's units of 32 rows
+      // x 16 columns
       auto scale_x = [&](int t) -> bool {
         const TileInfo& ti = info[t % kInfoSlots];
-        if (!wait_bar(&bars->yd_full, t & 1, abort, a.hdr, 14)) return false;
+        if (kPre) {
+          if (!wait_bar(&bars->info_ready[t % kInfoSlots], (t / kInfoSlots) & 1, abort, a.hdr, 18))
+            return false;
+          if (!wait_bar(&bars->full[t & 1], (t >> 1) & 1, abort, a.hdr, 19)) return false;
+        } else if (!wait_bar(&bars->yd_full, t & 1, abort, a.hdr, 14)) {
+          return false;
+        }
         uint8_t* xs = smem + kOffX + (t & 1) * kXBytes;
+        uint8_t* xlo = kPre ? smem + kOffC + (t & 1) * kXBytes : smem + kOffXlo;
 #pragma unroll 1
         for (int u = ub; u < ue; ++u) {
           const int row = (u >> 2) * 32 + lane, c0 = (u & 3) * 16;
@@ -495,15 +541,21 @@ __global__ void __launch_bounds__(kThreadsFused, 1)
         return true;
       };
       // one loop with one call site per phase (t = -1 only masks tile 0)
-      for (int t = -1; t < nt; ++t) {
+      for (int t = kPre ? 0 : -1; t < nt; ++t) {
         if (t >= 0 && !scale_x(t)) break;
-        if (t + 1 < nt && !mask_part(t + 1, cb0, q + 1, 4)) break;
+        if (!kPre && t + 1 < nt && !mask_part(t + 1, cb0, q + 1, 4)) break;
       }
     } else {
       // ---------------------------------------------------------------- state warps
       // state row n = i: h_in split into [h_hi | h_lo] for Yo, exp(cum_last) h_in preloaded
       // into the K3 accumulator (lo half zeroed); output rows i of every tile.
       const size_t st_base = (size_t)seq * kP * kN;
+      const size_t seg_base = ((size_t)seq * a.nseg + seg) * kP * kN;
+      // initial state: the call's for segment 0; the carried one for later segments of the
+      // full pass; zero for later segments of the pre-pass
+      const float* init0 = seg == 0 ? (a.init ? a.init + st_base : nullptr)
+                                    : (kPre ? nullptr : a.seg_init + seg_base);
+      float seg_decay = 1.f;   // pre-pass: product of the tiles' exp(cum_last)
       uint8_t* hbhi = smem + kOffHhi;
       uint8_t* hblo = smem + kOffHlo;
       // writes h (32 values of columns [c0, c0+32) of state row i) to the Yo operand and the
@@ -512,6 +564,7 @@ __global__ void __launch_bounds__(kThreadsFused, 1)
         float eh[32];
 #pragma unroll
         for (int k = 0; k < 32; k += 8) {
+          if (kPre) break;   // the pre-pass has no Yo
           uint4 uh, ul;
           split2(make_float2(hv[k], hv[k + 1]), uh.x, ul.x);
           split2(make_float2(hv[k + 2], hv[k + 3]), uh.y, ul.y);
@@ -557,18 +610,20 @@ __global__ void __launch_bounds__(kThreadsFused, 1)
           float hv[32];
 #pragma unroll
           for (int k = 0; k < 32; ++k)
-            hv[k] = a.init ? a.init[st_base + (size_t)(c0 + k) * kN + i] : 0.f;
+            hv[k] = init0 ? init0[(size_t)(c0 + k) * kN + i] : 0.f;
           put_state(c0, hv, e0);
         }
         publish_state();
       }
       for (int t = -1; ok && t < nt; ++t) {
-        if (q >= 2 && t + 1 < nt && !mask_part(t + 1, 0, q - 1, q - 1)) break;
+        if (!kPre && q >= 2 && t + 1 < nt && !mask_part(t + 1, 0, q - 1, q - 1)) break;
         if (t < 0) continue;
         const int slot = t % kInfoSlots;
         const TileInfo& ti = info[slot];
         const bool next = t + 1 < nt;
+        if (kPre) seg_decay *= ti.etile;
         // output: y = Yd + exp(cum[i/R]) (Yo_hi + Yo_lo)
+        if (!kPre) {
         if (!wait_bar(&bars->yo_full, t & 1, abort, a.hdr, 21)) break;
         tc_fence_after();
         {
@@ -601,6 +656,7 @@ __global__ void __launch_bounds__(kThreadsFused, 1)
             dst[3] = make_uint4(pk[12], pk[13], pk[14], pk[15]);
           }
         }
+        }
         // K4: h_in(t+1) = S_hi + S_lo (the accumulator already holds the decayed h_in(t))
         if (!wait_bar(&bars->s_full, t & 1, abort, a.hdr, 20)) break;
         float enext = 0.f;
@@ -628,12 +684,16 @@ __global__ void __launch_bounds__(kThreadsFused, 1)
           }
           if (next) {
             put_state(c0, hv, enext);
-          } else if (a.final_state) {
+          } else if (kPre) {   // the segment's end state for the carry pass
+#pragma unroll
+            for (int k = 0; k < 32; ++k) a.seg_end[seg_base + (size_t)(c0 + k) * kN + i] = hv[k];
+          } else if (a.final_state && seg == a.nseg - 1) {
 #pragma unroll
             for (int k = 0; k < 32; ++k) a.final_state[st_base + (size_t)(c0 + k) * kN + i] = hv[k];
           }
         }
         if (next) publish_state();
+        if (kPre && !next && warp == 7 && lane == 0) a.seg_decay[(size_t)seq * a.nseg + seg] = seg_decay;
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars->info_empty[slot]);   // last use of this tile's info
@@ -733,13 +793,58 @@ cudaError_t ensure_smem_attribute() {
   if (e != cudaSuccess) return e;
   const uint64_t bit = dev < 64 ? (1ull << dev) : 0ull;
   if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
-  e = cudaFuncSetAttribute(ssd_fused_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           kSmemAlloc);
+  e = cudaFuncSetAttribute(ssd_fused_bf16_kernel<false>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(ssd_fused_bf16_kernel<true>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
   if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_acq_rel);
   return e;
 }
 
+// True initial state of every segment after the first, one thread per (sequence, state element):
+// segment 0's pre-pass started from the true state, later ones from zero, so
+// h(1) = end_0 and h(s+1) = decay_s h(s) + end_s.
+__global__ void fused_seg_carry_kernel(FusedArgs a, int64_t elems) {
+  const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= elems) return;
+  constexpr int64_t kPN = (int64_t)kP * kN;
+  const int64_t seq = idx / kPN, e = idx % kPN;
+  float* init = const_cast<float*>(a.seg_init);
+  float hcur = 0.f;
+  for (int s = 0; s + 1 < a.nseg; ++s) {
+    const float end = a.seg_end[(seq * a.nseg + s) * kPN + e];
+    hcur = s == 0 ? end : fmaf(a.seg_decay[seq * a.nseg + s], hcur, end);
+    init[(seq * a.nseg + s + 1) * kPN + e] = hcur;
+  }
+}
+
+// Segments per sequence: enough CTAs to cover the SMs when there are fewer sequences than SMs
+// (each segment keeps at least four tiles).
+int fused_segments(int64_t batch, int64_t H, int64_t ntiles) {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return 1;
+  const int64_t seqs = batch * H;
+  int64_t n = sms / std::max<int64_t>(seqs, 1);
+  n = std::min<int64_t>(n, ntiles / 4);
+  n = std::min<int64_t>(n, 16);
+  return (int)std::max<int64_t>(n, 1);
+}
+
 }  // namespace
+
+size_t fused_bf16_workspace_bytes(int64_t batch, int64_t T, int64_t H, int64_t R) {
+  const int64_t ntiles = T * R / kTileRows;
+  const int nseg = fused_segments(batch, H, ntiles);
+  size_t bytes = sizeof(WsHeader);
+  if (nseg > 1) {
+    const size_t seg_states = (size_t)batch * H * nseg * kP * kN;
+    bytes += 2 * seg_states * sizeof(float) + align_up((size_t)batch * H * nseg * sizeof(float), 256);
+  }
+  return bytes;
+}
 
 bool fused_bf16_supported(int64_t T, int64_t H, int64_t P, int64_t N, int64_t R, int64_t l,
                           bool bf16, bool theta) {
@@ -768,11 +873,33 @@ cudaError_t fused_bf16_forward(const GenericParams& p, cudaStream_t st) {
   a.G = (int32_t)p.G;
   a.ntiles = (int32_t)(p.T * p.R / kTileRows);
   a.steps = steps;
+  a.nseg = fused_segments(p.batch, p.H, a.ntiles);
+  a.seg_tiles = (a.ntiles + a.nseg - 1) / a.nseg;
+  a.nseg = (a.ntiles + a.seg_tiles - 1) / a.seg_tiles;   // no empty segment
+  // workspace after the header: segment initial states, end states, decays
+  char* ws = reinterpret_cast<char*>(p.hdr);
+  const size_t seg_states = (size_t)p.batch * p.H * a.nseg * kP * kN;
+  a.seg_init = reinterpret_cast<const float*>(ws + sizeof(WsHeader));
+  a.seg_end = reinterpret_cast<float*>(ws + sizeof(WsHeader) + seg_states * sizeof(float));
+  a.seg_decay = reinterpret_cast<float*>(ws + sizeof(WsHeader) + 2 * seg_states * sizeof(float));
   cudaError_t e = ensure_smem_attribute();
   if (e != cudaSuccess) return e;
-  ssd_fused_bf16_kernel<<<(unsigned)(p.batch * p.H), kThreadsFused, kSmemAlloc, st>>>(
-      a, m->mx, m->mb, m->mc);
+  const unsigned seqs = (unsigned)(p.batch * p.H);
+  if (a.nseg > 1) {
+    ssd_fused_bf16_kernel<true><<<seqs * (a.nseg - 1), kThreadsFused, kSmemAlloc, st>>>(
+        a, m->mx, m->mb, m->mc);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    const int64_t elems = (int64_t)seqs * kP * kN;
+    fused_seg_carry_kernel<<<(unsigned)((elems + 255) / 256), 256, 0, st>>>(a, elems);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  ssd_fused_bf16_kernel<false><<<seqs * a.nseg, kThreadsFused, kSmemAlloc, st>>>(a, m->mx, m->mb,
+                                                                                 m->mc);
   return cudaGetLastError();
+}
+
+int fused_bf16_launches(int64_t batch, int64_t T, int64_t H, int64_t R) {
+  return fused_segments(batch, H, T * R / kTileRows) > 1 ? 3 : 1;
 }
 
 }  // namespace ssd

@@ -61,6 +61,10 @@ int64_t ss_segment_length(int64_t T);
 bool fused_bf16_supported(int64_t T, int64_t H, int64_t P, int64_t N, int64_t R, int64_t l,
                           bool bf16, bool theta);
 cudaError_t fused_bf16_forward(const GenericParams& p, cudaStream_t st);
+// Workspace bytes of the fused kernel (header plus, when sequences are cut into time segments,
+// the segment states) and its launches per call.
+size_t fused_bf16_workspace_bytes(int64_t batch, int64_t T, int64_t H, int64_t R);
+int fused_bf16_launches(int64_t batch, int64_t T, int64_t H, int64_t R);
 cudaError_t selective_scan_launch(const SelectiveScanParams& p, cudaStream_t st);
 // Single-kernel path for d_state in {8, 16, 32, 64} (no workspace use beyond the header).
 bool selective_scan_onepass_supported(int64_t batch, int64_t D, int64_t N);

@@ -79,6 +79,14 @@ size_t ssd_chunked_workspace_bytes(const ssd_shape* shape);
 int32_t ssd_chunked_variant(const ssd_shape* shape);
 
 /*
+ * Kernel launches one ssd_chunked_forward call makes for `shape` on the current device (0 if
+ * the shape is not supported); for profiling and launch accounting.  The fused kernel cuts
+ * sequences into time segments when there are fewer (batch, head) sequences than SMs, which
+ * adds a state-only pre-pass and a carry launch.
+ */
+int32_t ssd_chunked_launches(const ssd_shape* shape);
+
+/*
  * Chunked SSD forward scan (serial.rs: ssd_serial and K1..K5; scan.py: rotation absorption).
  *
  * Per (batch b, head h), with g = h / (H/G), Phi_t = sum_{s<=t} theta[b,s,h,:]:
