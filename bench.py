@@ -38,7 +38,7 @@ FALLBACK_BF16_TFLOPS = 1900.0
 # dram__bytes_read.sum + dram__bytes_write.sum of one launch of the dominant kernel, from one
 # ncu capture of the same workload (the profiles/ summaries); writes still held in L2 when the
 # kernel ends are not counted.  Variants without a capture report null.
-NCU_TRAFFIC_BYTES = {"tc_bf16": 100_496_128, "selective_scan": 78_705_408}
+NCU_TRAFFIC_BYTES = {"selective_scan": 72_165_888}
 
 
 def parse_args():
