@@ -57,13 +57,21 @@ int32_t pick_variant(const ssd_shape* s) {
   return SSD_VARIANT_GENERIC;
 }
 
+// Chunk length the kernels tile time by.  The decomposition is exact for any chunk length, so
+// this is a tiling choice: the register-tiled fp32 kernels use 64 (their quadratic work per row
+// grows with the chunk, the chunk-state traffic shrinks with it; 64 is the faster trade on
+// GB300), every other path the caller's chunk_len.
+int64_t kernel_chunk_len(const ssd_shape* s) {
+  return pick_variant(s) == SSD_VARIANT_TILED_F32 ? 64 : s->chunk_len;
+}
+
 SsdLayout ssd_layout(const ssd_shape* s) {
   SsdLayout L;
   if (pick_variant(s) == SSD_VARIANT_TC_BF16) {   // the fused kernel keeps its state on chip
     L.total = fused_bf16_workspace_bytes(s->batch, s->seqlen, s->nheads, s->mimo_rank);
     return L;
   }
-  const int64_t nch = s->seqlen / s->chunk_len;
+  const int64_t nch = s->seqlen / kernel_chunk_len(s);
   size_t off = sizeof(WsHeader);
   L.states = off;
   off = align_up(off + sizeof(float) * (size_t)(s->batch * nch * s->nheads * s->headdim * s->dstate),
@@ -140,8 +148,8 @@ ssd_status ssd_chunked_forward(const ssd_shape* shape, const void* x, const floa
   p.N = shape->dstate;
   p.G = shape->ngroups;
   p.R = shape->mimo_rank;
-  p.l = shape->chunk_len;
-  p.nch = shape->seqlen / shape->chunk_len;
+  p.l = kernel_chunk_len(shape);
+  p.nch = shape->seqlen / p.l;
   p.states = reinterpret_cast<float*>(ws + lay.states);
   p.cend = reinterpret_cast<float*>(ws + lay.cend);
   p.phi = theta ? reinterpret_cast<double*>(ws + lay.phi) : nullptr;

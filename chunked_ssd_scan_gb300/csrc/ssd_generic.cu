@@ -21,6 +21,7 @@
 #include <math.h>
 
 #include "common.cuh"
+#include "fp_helpers.cuh"
 #include "ssd_internal.h"
 
 namespace ssd {
@@ -126,54 +127,53 @@ __device__ void stage_bc_rows(const GenericParams& p, const T* __restrict__ src,
   }
 }
 
-// Per-chunk theta sums in fp64: every thread of the block takes one pair and a slice of the
-// chunk's steps (loads coalesced over pairs); the slices are combined in shared memory.
+// Per-chunk theta sums: one warp per chunk, lanes over pairs (loads coalesced over the pairs of
+// one step), kPhiChunksPerBlock chunks per block; the sum is carried as a double-float (TwoSum)
+// pair, which is exact enough for the fp64 chunk sums and avoids a chain of slow fp64 adds.
 constexpr int kPhiThreads = 256;
+constexpr int kPhiChunksPerBlock = kPhiThreads / 32;
 
 __global__ void __launch_bounds__(kPhiThreads) phi_chunk_sum_kernel(GenericParams p) {
-  __shared__ double part[kPhiThreads];
-  const int64_t c = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
-  const int K = (int)(p.N / 2);
-  const int groups = kPhiThreads / K;             // K <= 128 (N <= 256)
-  const int k = threadIdx.x % K, grp = threadIdx.x / K;
-  double s = 0.0;
-  if (grp < groups) {
+  const int64_t c = (int64_t)blockIdx.x * kPhiChunksPerBlock + threadIdx.x / 32;
+  const int64_t h = blockIdx.y, b = blockIdx.z;
+  if (c >= p.nch) return;
+  const int64_t K = p.N / 2;
+  for (int64_t k = threadIdx.x % 32; k < K; k += 32) {
     const float* th = p.theta + ((b * p.T + c * p.l) * p.H + h) * K + k;
-    for (int64_t t = grp; t < p.l; t += groups) s += (double)__ldg(th + t * p.H * K);
-  }
-  part[threadIdx.x] = s;
-  __syncthreads();
-  if (threadIdx.x < K) {
-    double tot = 0.0;
-    for (int g = 0; g < groups; ++g) tot += part[g * K + threadIdx.x];
-    p.phisum[((b * p.nch + c) * p.H + h) * K + threadIdx.x] = tot;
+    fp::DF s = {0.f, 0.f};
+    for (int64_t t = 0; t < p.l; ++t) s = fp::df_add(s, fp::DF{__ldg(th + t * p.H * K), 0.f});
+    p.phisum[((b * p.nch + c) * p.H + h) * K + k] = (double)s.hi + (double)s.lo;
   }
 }
 
 // Chunk-start angles: an exclusive fp64 prefix of the chunk sums per (batch, head, pair),
-// reduced to [-pi, pi]; the chunk sums are loaded several chunks ahead.
+// reduced to [-pi, pi].  One warp per (batch, head, pair): each lane sums a contiguous run of
+// chunks, the lane totals are scanned with shuffles, and each lane then writes its run.
 __global__ void phi_prefix_kernel(GenericParams p) {
   const int64_t K = p.N / 2;
-  const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (idx >= p.batch * p.H * K) return;
-  const int64_t k = idx % K, h = (idx / K) % p.H, b = idx / (K * p.H);
+  const int64_t wid = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) / 32;
+  const int lane = threadIdx.x % 32;
+  if (wid >= p.batch * p.H * K) return;   // uniform over the warp
+  const int64_t k = wid % K, h = (wid / K) % p.H, b = wid / (K * p.H);
   const double* src = p.phisum + (b * p.nch * p.H + h) * K + k;   // + c * H * K
   double* dst = p.phi + (b * (p.nch + 1) * p.H + h) * K + k;
   const int64_t cs = p.H * K;
-  double acc = 0.0;
-  for (int64_t c0 = 0; c0 < p.nch; c0 += 8) {
-    double v[8];
+  const int64_t per = (p.nch + 31) / 32;
+  const int64_t c0 = min((int64_t)lane * per, p.nch), c1 = min(c0 + per, p.nch);
+  double run = 0.0;
+  for (int64_t c = c0; c < c1; ++c) run += src[c * cs];
+  double incl = run;
 #pragma unroll
-    for (int j = 0; j < 8; ++j) v[j] = (c0 + j < p.nch) ? src[(c0 + j) * cs] : 0.0;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      if (c0 + j < p.nch) {
-        dst[(c0 + j) * cs] = acc - kTwoPi * rint(acc * (1.0 / kTwoPi));
-        acc += v[j];
-      }
-    }
+  for (int off = 1; off < 32; off <<= 1) {
+    const double v = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += v;
   }
-  dst[p.nch * cs] = acc - kTwoPi * rint(acc * (1.0 / kTwoPi));
+  double acc = incl - run;   // exclusive prefix of this lane's first chunk
+  for (int64_t c = c0; c < c1; ++c) {
+    dst[c * cs] = acc - kTwoPi * rint(acc * (1.0 / kTwoPi));
+    acc += src[c * cs];
+  }
+  if (lane == 31) dst[p.nch * cs] = incl - kTwoPi * rint(incl * (1.0 / kTwoPi));
 }
 
 template <typename T, int OPT>
@@ -232,7 +232,7 @@ __global__ void __launch_bounds__(kThreads) chunk_state_kernel(GenericParams p) 
 // One thread carries one state element (or, with rotation, one interleaved pair) of one
 // (batch, head) through all chunks; the grid covers every element of every (batch, head), and
 // the chunk states are loaded kStatePrefetch chunks ahead of the serial update.
-constexpr int kStatePrefetch = 8;
+constexpr int kStatePrefetch = 16;
 
 template <bool kPairs>
 __global__ void __launch_bounds__(kThreads) state_pass_kernel(GenericParams p) {
@@ -444,12 +444,13 @@ bool generic_supported(int64_t l, int64_t R, int64_t P, int64_t N, bool theta) {
 }
 
 cudaError_t generic_phi(const GenericParams& p, cudaStream_t st) {
-  phi_chunk_sum_kernel<<<dim3((unsigned)p.nch, (unsigned)p.H, (unsigned)p.batch), kPhiThreads, 0,
-                         st>>>(p);
+  phi_chunk_sum_kernel<<<dim3((unsigned)((p.nch + kPhiChunksPerBlock - 1) / kPhiChunksPerBlock),
+                              (unsigned)p.H, (unsigned)p.batch),
+                         kPhiThreads, 0, st>>>(p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  const int64_t n = p.batch * p.H * (p.N / 2);
-  phi_prefix_kernel<<<(unsigned)((n + 127) / 128), 128, 0, st>>>(p);
+  const int64_t warps = p.batch * p.H * (p.N / 2);
+  phi_prefix_kernel<<<(unsigned)((warps * 32 + 127) / 128), 128, 0, st>>>(p);
   return cudaGetLastError();
 }
 

@@ -64,10 +64,13 @@ __device__ void chunk_prefix64(const float* __restrict__ src, int64_t stride, in
 }
 
 // Rotation angles Phi_t (inclusive cumulative theta from the chunk-start angle) for steps
-// [0, n) and all 32 pairs, reduced to [-pi, pi], into ang[t * 32 + k]: theta is staged into
-// `ang` (coalesced), then each warp runs a double-float prefix per pair in place.
+// [0, n) and all 32 pairs, reduced to [-pi, pi], into ang[t * 32 + k].  theta is staged into
+// `ang` (coalesced); thread (pair k, group gr) then sums its run of consecutive steps as a
+// double-float, the group totals of each pair are prefix-summed through shared memory, and
+// each thread rewrites its run in place.
 __device__ void chunk_angles64(const GenericParams& p, int64_t b, int64_t c, int64_t h, int n,
                                float* ang) {
+  __shared__ float part_hi[kSimtThreads], part_lo[kSimtThreads];
   const float* th = p.theta + ((b * p.T + c * p.l) * p.H + h) * kPairs64;
   for (int e = threadIdx.x; e < n * (kPairs64 / 4); e += blockDim.x) {
     const int t = e / (kPairs64 / 4), q = e % (kPairs64 / 4);
@@ -75,29 +78,24 @@ __device__ void chunk_angles64(const GenericParams& p, int64_t b, int64_t c, int
         __ldg(reinterpret_cast<const float4*>(th + (int64_t)t * p.H * kPairs64) + q);
   }
   __syncthreads();
-  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int per = (n + 31) / 32;
-  const int beg = min(n, lane * per), end = min(n, beg + per);
-  for (int k = warp; k < kPairs64; k += blockDim.x / 32) {
-    const double a0 = p.phi[((b * (p.nch + 1) + c) * p.H + h) * kPairs64 + k];   // in [-pi, pi]
-    const float s_hi = (float)a0;
-    const DF start = {s_hi, (float)(a0 - (double)s_hi)};
-    DF s = {0.f, 0.f};
-    for (int t = beg; t < end; ++t) s = df_add(s, DF{ang[t * kPairs64 + k], 0.f});
-    DF incl = s;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const DF v = df_shfl_up(incl, off);
-      if (lane >= off) incl = df_add(incl, v);
-    }
-    DF acc = df_shfl_up(incl, 1);
-    if (lane == 0) acc = DF{0.f, 0.f};
-    acc = df_add(acc, start);
-    for (int t = beg; t < end; ++t) {
-      acc = df_add(acc, DF{ang[t * kPairs64 + k], 0.f});
-      const float q = rintf(acc.hi * 0.15915494309189535f);
-      ang[t * kPairs64 + k] = (fmaf(-q, kTwoPiHi64, acc.hi) - q * kTwoPiLo64) + acc.lo;
-    }
+  constexpr int kGroups = kSimtThreads / kPairs64;        // 8 step groups per pair
+  const int k = threadIdx.x % kPairs64, gr = threadIdx.x / kPairs64;
+  const int per = (n + kGroups - 1) / kGroups;
+  const int beg = min(n, gr * per), end = min(n, beg + per);
+  DF run = {0.f, 0.f};
+  for (int t = beg; t < end; ++t) run = df_add(run, DF{ang[t * kPairs64 + k], 0.f});
+  part_hi[threadIdx.x] = run.hi;
+  part_lo[threadIdx.x] = run.lo;
+  __syncthreads();
+  const double a0 = p.phi[((b * (p.nch + 1) + c) * p.H + h) * kPairs64 + k];   // in [-pi, pi]
+  const float s_hi = (float)a0;
+  DF acc = {s_hi, (float)(a0 - (double)s_hi)};
+  for (int g = 0; g < gr; ++g)
+    acc = df_add(acc, DF{part_hi[g * kPairs64 + k], part_lo[g * kPairs64 + k]});
+  for (int t = beg; t < end; ++t) {
+    acc = df_add(acc, DF{ang[t * kPairs64 + k], 0.f});
+    const float q = rintf(acc.hi * 0.15915494309189535f);
+    ang[t * kPairs64 + k] = (fmaf(-q, kTwoPiHi64, acc.hi) - q * kTwoPiLo64) + acc.lo;
   }
   __syncthreads();
 }
