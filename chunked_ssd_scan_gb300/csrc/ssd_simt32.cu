@@ -130,6 +130,28 @@ __device__ void stage_bc64(const GenericParams& p, const float* __restrict__ src
                            int64_t c, int64_t g, int s0, const float* ang, float* dst,
                            bool transpose) {
   const int tid = threadIdx.x;
+  if (!transpose) {
+    // row-major: the 16 lanes of a half-warp read and write one row (coalesced loads,
+    // conflict-free shared stores)
+    const int ch = tid & 15;
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const int row = (tid >> 4) + 16 * r;
+      float4 f = __ldg(reinterpret_cast<const float4*>(
+                           src + ((b * p.T + c * p.l + s0 + row) * p.G + g) * kT64) + ch);
+      if (p.theta) {
+        const float* ar = ang + (s0 + row) * kPairs64 + 2 * ch;
+        float s, co;
+        sincosf(ar[0], &s, &co);
+        const float e0 = co * f.x + s * f.y, o0 = -s * f.x + co * f.y;
+        sincosf(ar[1], &s, &co);
+        const float e1 = co * f.z + s * f.w, o1 = -s * f.z + co * f.w;
+        f = make_float4(e0, o0, e1, o1);
+      }
+      *reinterpret_cast<float4*>(dst + row * kT64 + 4 * ch) = f;
+    }
+    return;
+  }
   const int row = tid >> 2, q0 = (tid & 3) * 16;   // 4 threads per row, 16 values each
   const float4* s4 = reinterpret_cast<const float4*>(
       src + ((b * p.T + c * p.l + s0 + row) * p.G + g) * kT64 + q0);
@@ -153,29 +175,23 @@ __device__ void stage_bc64(const GenericParams& p, const float* __restrict__ src
       v[2 * k + 1] = -s * a + co * bb;
     }
   }
-  if (transpose) {
 #pragma unroll
-    for (int k = 0; k < 16; ++k) dst[(q0 + k) * kT64 + row] = v[k];
-  } else {
-#pragma unroll
-    for (int q = 0; q < 4; ++q)
-      *reinterpret_cast<float4*>(dst + row * kT64 + q0 + 4 * q) =
-          make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-  }
+  for (int k = 0; k < 16; ++k) dst[(q0 + k) * kT64 + row] = v[k];
 }
 
 // Stages x rows (chunk steps s0 ..) into dst[row][p], each row scaled by scale[row] if given.
 __device__ void stage_x64(const GenericParams& p, int64_t b, int64_t c, int64_t h, int s0,
                           const float* scale, float* dst) {
   const int tid = threadIdx.x;
-  const int row = tid >> 2, q0 = (tid & 3) * 16;
-  const float4* s4 = reinterpret_cast<const float4*>(
-      static_cast<const float*>(p.x) + ((b * p.T + c * p.l + s0 + row) * p.H + h) * kT64 + q0);
-  const float w = scale ? scale[row] : 1.f;
+  const int ch = tid & 15;   // half-warps read and write whole rows
 #pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    const float4 f = __ldg(s4 + q);
-    *reinterpret_cast<float4*>(dst + row * kT64 + q0 + 4 * q) =
+  for (int r = 0; r < 4; ++r) {
+    const int row = (tid >> 4) + 16 * r;
+    const float4 f = __ldg(reinterpret_cast<const float4*>(
+                               static_cast<const float*>(p.x) +
+                               ((b * p.T + c * p.l + s0 + row) * p.H + h) * kT64) + ch);
+    const float w = scale ? scale[row] : 1.f;
+    *reinterpret_cast<float4*>(dst + row * kT64 + 4 * ch) =
         make_float4(f.x * w, f.y * w, f.z * w, f.w * w);
   }
 }
@@ -246,8 +262,9 @@ __global__ void __launch_bounds__(kSimtThreads) simt_scan_kernel(GenericParams p
   {
     // h_in [p][n] (written over S by the state pass) -> h^T [n][p]
     const float* hin = p.states + ((b * p.nch + c) * p.H + h) * kTileFloats;
+    // lanes over consecutive p: conflict-free shared stores of h^T[n][p]
     for (int e = threadIdx.x; e < kTileFloats; e += kSimtThreads)
-      ht[(e % kT64) * kT64 + e / kT64] = hin[e];
+      ht[(e / kT64) * kT64 + e % kT64] = hin[(e % kT64) * kT64 + e / kT64];
   }
   if (p.theta) {
     chunk_angles64(p, b, c, h, l, ang);
