@@ -101,13 +101,16 @@ __device__ void chunk_angles64(const GenericParams& p, int64_t b, int64_t c, int
 }
 
 // acc[r][c] += sum_k At[k][4 ty + r] * Bt[k][4 tx + c] over k < 64 (both operands k-major,
-// 64 floats per k row).
+// 64 floats per k row).  With kSwzA the 16-byte chunks of At's row k are stored permuted
+// (chunk c at c ^ ((k >> 2) & 15)), the layout the masked operand is written in.
+template <bool kSwzA = false>
 __device__ __forceinline__ void block_product(const float* __restrict__ At,
                                               const float* __restrict__ Bt, int ty, int tx,
                                               float (&acc)[4][4]) {
 #pragma unroll 8
   for (int k = 0; k < kT64; ++k) {
-    const float4 a = *reinterpret_cast<const float4*>(At + k * kT64 + 4 * ty);
+    const int ca = kSwzA ? (ty ^ ((k >> 2) & 15)) : ty;
+    const float4 a = *reinterpret_cast<const float4*>(At + k * kT64 + 4 * ca);
     const float4 bq = *reinterpret_cast<const float4*>(Bt + k * kT64 + 4 * tx);
     const float av[4] = {a.x, a.y, a.z, a.w};
 #pragma unroll
@@ -298,11 +301,13 @@ __global__ void __launch_bounds__(kSimtThreads) simt_scan_kernel(GenericParams p
           m[r] = sj <= si ? exp2f((cum_hi[si] - cum_hi[sj]) + (cum_lo[si] - cum_lo[sj])) * cb[r][jj]
                           : 0.f;
         }
-        *reinterpret_cast<float4*>(bt + (4 * tx + jj) * kT64 + 4 * ty) =
+        // row 4 tx + jj, chunk ty permuted by the row: the 16 lanes of a half-warp write 16
+        // different chunks (conflict-free)
+        *reinterpret_cast<float4*>(bt + (4 * tx + jj) * kT64 + 4 * (ty ^ tx)) =
             make_float4(m[0], m[1], m[2], m[3]);
       }
       __syncthreads();
-      block_product(bt, xs, ty, tx, yd);   // Yd[i][p] += sum_j M[i][j] x[j][p]
+      block_product<true>(bt, xs, ty, tx, yd);   // Yd[i][p] += sum_j M[i][j] x[j][p]
       __syncthreads();
     }
 #pragma unroll
