@@ -68,6 +68,8 @@ EDGE = [
     wl.SSDConfig("fused_one_tile", 1, 128, 4, 64, 128, 128, 1, 1, "bf16"),
     wl.SSDConfig("fused_r2_g2", 2, 320, 8, 64, 128, 64, 2, 2, "bf16"),
     wl.SSDConfig("fused_r8_g4", 1, 256, 4, 64, 128, 16, 8, 4, "bf16"),
+    # fused kernel with time segments of unequal length (9 tiles on 8 sequences: 5 + 4)
+    wl.SSDConfig("fused_uneven_segments", 1, 1152, 8, 64, 128, 128, 1, 1, "bf16"),
     # register-tiled fp32 path: one 64-row tile per chunk without rotation, two groups; six
     # tiles per chunk with rotation and one group shared by three heads
     wl.SSDConfig("tiled_f32_l64_g2", 2, 512, 4, 64, 64, 64, 1, 2, "f32"),
@@ -82,8 +84,19 @@ def test_f32_workloads_use_the_tiled_kernels():
         assert pkg.ssd_chunked_variant(shape) == "tiled_f32", cfg.name
 
 
+def test_fused_launches_follow_the_segmentation():
+    """Fewer sequences than SMs: pre-pass + carry + full pass; otherwise one launch."""
+    def launches(cfg):
+        return pkg.ssd_chunked_launches(pkg.make_shape(
+            cfg.batch, cfg.seqlen, cfg.nheads, cfg.headdim, cfg.dstate, cfg.ngroups,
+            cfg.mimo_rank, cfg.chunk_len, cfg.dtype, cfg.theta))
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert launches(wl.MAMBA3_MIMO_BF16) == (3 if 64 * 2 <= sms else 1)
+    assert launches(wl.MAMBA2_SISO_BF16) == (3 if 128 * 2 <= sms else 1)
+
+
 def test_bf16_workloads_use_the_fused_kernel():
-    for cfg in (wl.MAMBA2_SISO_BF16, wl.MAMBA3_MIMO_BF16, EDGE[-3], EDGE[-4], EDGE[-5]):
+    for cfg in (wl.MAMBA2_SISO_BF16, wl.MAMBA3_MIMO_BF16, EDGE[-3], EDGE[-4], EDGE[-5], EDGE[-6]):
         shape = pkg.make_shape(cfg.batch, cfg.seqlen, cfg.nheads, cfg.headdim, cfg.dstate,
                                cfg.ngroups, cfg.mimo_rank, cfg.chunk_len, cfg.dtype, cfg.theta)
         assert pkg.ssd_chunked_variant(shape) == "tc_bf16", cfg.name
