@@ -37,6 +37,12 @@
 // Each warp rewrites only TMEM columns that it has read itself, so the masked operand is
 // formed in place without a barrier between warps.  Every wait is bounded; a wait that gives
 // up latches SSD_ERR_TIMEOUT in the workspace header and the CTA stops issuing work.
+//
+// Time segments: with fewer sequences than SMs, each sequence is cut into segments run by
+// separate CTAs.  The same kernel in its state-only form (kPre: K1, dec o x, K3 and K4; no C,
+// CB, mask, Yd, Yo or output) gives each earlier segment's end state, fused_seg_carry_kernel
+// turns them into every segment's true initial state, and the full form then runs all segments
+// in parallel, writing every y once.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <math.h>
