@@ -68,15 +68,23 @@ __device__ void chunk_prefix64(const float* __restrict__ src, int64_t stride, in
 // `ang` (coalesced); thread (pair k, group gr) then sums its run of consecutive steps as a
 // double-float, the group totals of each pair are prefix-summed through shared memory, and
 // each thread rewrites its run in place.
-__device__ void chunk_angles64(const GenericParams& p, int64_t b, int64_t c, int64_t h, int n,
-                               float* ang) {
-  __shared__ float part_hi[kSimtThreads], part_lo[kSimtThreads];
+// theta rows of steps [0, n) into ang[t * 32 + k] with 16-byte cp.async (not waited for).
+__device__ void issue_theta64(const GenericParams& p, int64_t b, int64_t c, int64_t h, int n,
+                              float* ang) {
   const float* th = p.theta + ((b * p.T + c * p.l) * p.H + h) * kPairs64;
   for (int e = threadIdx.x; e < n * (kPairs64 / 4); e += blockDim.x) {
     const int t = e / (kPairs64 / 4), q = e % (kPairs64 / 4);
-    *reinterpret_cast<float4*>(ang + t * kPairs64 + 4 * q) =
-        __ldg(reinterpret_cast<const float4*>(th + (int64_t)t * p.H * kPairs64) + q);
+    cp_async16(ang + t * kPairs64 + 4 * q, th + (int64_t)t * p.H * kPairs64 + 4 * q, 16);
   }
+}
+
+// With staged = true the theta rows were issued earlier by issue_theta64 (and are waited for
+// here).
+__device__ void chunk_angles64(const GenericParams& p, int64_t b, int64_t c, int64_t h, int n,
+                               float* ang, bool staged = false) {
+  __shared__ float part_hi[kSimtThreads], part_lo[kSimtThreads];
+  if (!staged) issue_theta64(p, b, c, h, n, ang);
+  cp_async_wait_all();
   __syncthreads();
   constexpr int kGroups = kSimtThreads / kPairs64;        // 8 step groups per pair
   const int k = threadIdx.x % kPairs64, gr = threadIdx.x / kPairs64;
@@ -261,6 +269,16 @@ __global__ void __launch_bounds__(kSimtThreads) simt_scan_kernel(GenericParams p
   float* cum_hi = xs + kTileFloats;
   float* cum_lo = cum_hi + l;
   float* ang = cum_lo + l;
+  // theta and the first x tile are in flight while the prefix sums and h_in are staged
+  if (p.theta) issue_theta64(p, b, c, h, l, ang);
+  {
+    const float* xsrc = static_cast<const float*>(p.x);
+    for (int e = threadIdx.x; e < kTileFloats / 4; e += kSimtThreads) {
+      const int row = e / (kT64 / 4), q = e % (kT64 / 4);
+      cp_async16(xs + row * kT64 + 4 * q,
+                 xsrc + ((b * p.T + c * p.l + row) * p.H + h) * kT64 + 4 * q, 16);
+    }
+  }
   chunk_prefix64(p.dA + (b * p.T + c * p.l) * p.H + h, p.H, l, cum_hi, cum_lo, nullptr);
   {
     // h_in [p][n] (written over S by the state pass) -> h^T [n][p]
@@ -270,8 +288,9 @@ __global__ void __launch_bounds__(kSimtThreads) simt_scan_kernel(GenericParams p
       ht[(e / kT64) * kT64 + e % kT64] = hin[(e % kT64) * kT64 + e / kT64];
   }
   if (p.theta) {
-    chunk_angles64(p, b, c, h, l, ang);
+    chunk_angles64(p, b, c, h, l, ang, true);
   } else {
+    cp_async_wait_all();
     __syncthreads();
   }
   const int tx = threadIdx.x % 16, ty = threadIdx.x / 16;   // rows i = 4 ty.., cols 4 tx..
@@ -285,7 +304,7 @@ __global__ void __launch_bounds__(kSimtThreads) simt_scan_kernel(GenericParams p
     float yd[4][4] = {};
     for (int j0 = 0; j0 <= i0; j0 += kT64) {
       stage_bc64(p, Bsrc, b, c, g, j0, ang, bt, true);
-      stage_x64(p, b, c, h, j0, nullptr, xs);
+      if (j0 > 0 || i0 > 0) stage_x64(p, b, c, h, j0, nullptr, xs);   // tile 0 was prefetched
       __syncthreads();
       float cb[4][4] = {};
       block_product(ct, bt, ty, tx, cb);   // CB[i][j] = sum_n C~[i][n] B~[j][n]
