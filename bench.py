@@ -228,6 +228,9 @@ def run_ours(args, rank, world, local):
     if world > 1:
         torch.distributed.barrier()
     step_ms = timed_steps(fn, args.steps, args.warmup, stream, flush)
+    status = pkg.workspace_status(ws, stream)   # a bounded device wait that gave up shows here
+    if status != ("SSD_OK", 0):
+        raise RuntimeError(f"device-side error word after the timed steps: {status}")
     if world > 1:
         torch.distributed.barrier()
     clk = clocks.stop() if clocks else None
@@ -348,6 +351,10 @@ def e2e_measure(args, cfg, is_ss, host, dev, stream):
     e.record(stream)
     torch.cuda.synchronize()
     ms = s.elapsed_time(e) / n
+    if not is_ss:
+        status = pkg.workspace_status(ws, stream)
+        if status != ("SSD_OK", 0):
+            raise RuntimeError(f"device-side error word after the end-to-end steps: {status}")
     return {"value": round(cfg.tokens / (ms * 1e-3), 1), "unit": "tokens/s",
             "ms_per_step": round(ms, 4), "h2d_bytes_per_step": int(h2d),
             "d2h_bytes_per_step": int(d2h), "steps": n}

@@ -40,7 +40,6 @@ ssd_status check_shape(const ssd_shape* s) {
     return SSD_ERR_INVALID_ARG;
   if (!mul_ok(s->batch, s->nheads, &t) || !mul_ok(t, s->headdim, &t) || !mul_ok(t, s->dstate, &t))
     return SSD_ERR_INVALID_ARG;
-  if (s->seqlen % s->chunk_len != 0) return SSD_ERR_UNSUPPORTED;
   if (s->batch > 65535 || s->nheads > 65535) return SSD_ERR_UNSUPPORTED;   // grid limits
   if (!generic_supported(s->chunk_len, s->mimo_rank, s->headdim, s->dstate, s->has_theta != 0))
     return SSD_ERR_UNSUPPORTED;
@@ -71,7 +70,8 @@ SsdLayout ssd_layout(const ssd_shape* s) {
     L.total = fused_bf16_workspace_bytes(s->batch, s->seqlen, s->nheads, s->mimo_rank);
     return L;
   }
-  const int64_t nch = s->seqlen / kernel_chunk_len(s);
+  const int64_t l = kernel_chunk_len(s);
+  const int64_t nch = (s->seqlen + l - 1) / l;   // the last chunk may be short
   size_t off = sizeof(WsHeader);
   L.states = off;
   off = align_up(off + sizeof(float) * (size_t)(s->batch * nch * s->nheads * s->headdim * s->dstate),
@@ -149,7 +149,7 @@ ssd_status ssd_chunked_forward(const ssd_shape* shape, const void* x, const floa
   p.G = shape->ngroups;
   p.R = shape->mimo_rank;
   p.l = kernel_chunk_len(shape);
-  p.nch = shape->seqlen / p.l;
+  p.nch = (shape->seqlen + p.l - 1) / p.l;   // the last chunk may be short
   p.states = reinterpret_cast<float*>(ws + lay.states);
   p.cend = reinterpret_cast<float*>(ws + lay.cend);
   p.phi = theta ? reinterpret_cast<double*>(ws + lay.phi) : nullptr;

@@ -38,6 +38,11 @@
 // formed in place without a barrier between warps.  Every wait is bounded; a wait that gives
 // up latches SSD_ERR_TIMEOUT in the workspace header and the CTA stops issuing work.
 //
+// Ragged sequences: when seqlen * R is not a multiple of 128 the last tile is partial.  The
+// tensor maps carry the batch as their own dimension, so TMA fills the rows past the end of a
+// sequence with zeros (x = B = C = 0), K1 reads dA = 0 there, and no y is written for them:
+// zero padding, which leaves y of the real steps and the final state unchanged.
+//
 // Time segments: with fewer sequences than SMs, each sequence is cut into segments run by
 // separate CTAs.  The same kernel in its state-only form (kPre: K1, dec o x, K3 and K4; no C,
 // CB, mask, Yd, Yo or output) gives each earlier segment's end state, fused_seg_carry_kernel
@@ -68,7 +73,7 @@ constexpr int kTileRows = 128;
 constexpr int kP = 64;
 constexpr int kN = 128;
 constexpr int kThreadsFused = 352;
-constexpr uint64_t kWaitNs = 2000000000ull;   // 2 s per wait before giving up
+constexpr long long kWaitCycles = 4000000000ll;   // per wait before giving up (~2 s at 2 GHz)
 constexpr float kLog2e = 1.4426950408889634f;
 
 // Shared-memory map (offsets from the 1024-aligned dynamic shared window).
@@ -140,14 +145,12 @@ struct FusedArgs {
 __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatile int* abort,
                                          WsHeader* hdr, int site) {
   if (mbar_try_wait(bar, parity)) return true;
-  uint64_t t0;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
+  // bounded in cycles of this SM's clock, which only moves forward
+  const long long t0 = clock64();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
     if (*abort) return false;
-    uint64_t t1;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t1));
-    if (t1 - t0 > kWaitNs) {
+    if (clock64() - t0 > kWaitCycles) {
       *abort = 1;
       if (hdr) latch_error(hdr, SSD_ERR_TIMEOUT, site);
       return false;
@@ -240,7 +243,9 @@ __global__ void __launch_bounds__(kThreadsFused, 1)
   const int R = a.R, steps = a.steps;
   const int tbase = seg * a.seg_tiles;           // first tile of this segment
   const int nt = min(a.ntiles - tbase, a.seg_tiles);
-  const int row_base = b * a.T * R + tbase * kTileRows;   // fused row of the segment's start
+  const int seg_row = tbase * kTileRows;                  // fused row (within the sequence)
+                                                         // of the segment's start
+  const int64_t row_base = (int64_t)b * a.T * R + seg_row;   // ... in the whole tensor
   volatile int* abort = &s_abort;
 
   if (threadIdx.x == 0) {
@@ -283,15 +288,15 @@ __global__ void __launch_bounds__(kThreadsFused, 1)
       const int s = t & 1;
       if (t >= 2 && !wait_bar(&bars->empty[s], ((t - 2) >> 1) & 1, abort, a.hdr, 1)) break;
       mbar_arrive_expect_tx_elect(&bars->full[s], tx);
-      const int row = row_base + t * kTileRows;
-      tma_load_3d_elect(smem + kOffX + s * kXBytes, &tm_x, &bars->full[s], 0, h, row);
-      tma_load_3d_elect(smem + kOffB + s * kBCBytes, &tm_b, &bars->full[s], 0, g, row);
-      tma_load_3d_elect(smem + kOffB + s * kBCBytes + kBCBytes / 2, &tm_b, &bars->full[s], 64, g,
-                        row);
+      const int row = seg_row + t * kTileRows;   // rows past the sequence's end read as zeros
+      tma_load_4d_elect(smem + kOffX + s * kXBytes, &tm_x, &bars->full[s], 0, h, row, b);
+      tma_load_4d_elect(smem + kOffB + s * kBCBytes, &tm_b, &bars->full[s], 0, g, row, b);
+      tma_load_4d_elect(smem + kOffB + s * kBCBytes + kBCBytes / 2, &tm_b, &bars->full[s], 64, g,
+                        row, b);
       if (!kPre) {   // the pre-pass needs no C
-        tma_load_3d_elect(smem + kOffC + s * kBCBytes, &tm_c, &bars->full[s], 0, g, row);
-        tma_load_3d_elect(smem + kOffC + s * kBCBytes + kBCBytes / 2, &tm_c, &bars->full[s], 64,
-                          g, row);
+        tma_load_4d_elect(smem + kOffC + s * kBCBytes, &tm_c, &bars->full[s], 0, g, row, b);
+        tma_load_4d_elect(smem + kOffC + s * kBCBytes + kBCBytes / 2, &tm_c, &bars->full[s], 64,
+                          g, row, b);
       }
     }
   } else if (warp == 1) {
@@ -396,7 +401,9 @@ __global__ void __launch_bounds__(kThreadsFused, 1)
     auto load_tile = [&](int t) {
 #pragma unroll
       for (int k = 0; k < 4; ++k)
-        dnext[k] = (beg + k < end) ? __ldg(dsrc + (size_t)(t * steps + beg + k) * a.H) : 0.f;
+        dnext[k] = (beg + k < end && (tbase + t) * steps + beg + k < a.T)
+                       ? __ldg(dsrc + (size_t)(t * steps + beg + k) * a.H)
+                       : 0.f;
     };
     load_tile(0);
     for (int t = 0; t < nt; ++t) {
@@ -513,6 +520,10 @@ __global__ void __launch_bounds__(kThreadsFused, 1)
           if (!wait_bar(&bars->info_ready[t % kInfoSlots], (t / kInfoSlots) & 1, abort, a.hdr, 18))
             return false;
           if (!wait_bar(&bars->full[t & 1], (t >> 1) & 1, abort, a.hdr, 19)) return false;
+          // K3 of the previous tile first: without it these warps could complete two phases of
+          // xs_ready (tiles t-1 and t, both of whose loads are issued up front) before the MMA
+          // warp tests the first, and a parity wait cannot tell those phases apart
+          if (t >= 1 && !wait_bar(&bars->s_full, (t - 1) & 1, abort, a.hdr, 22)) return false;
         } else if (!wait_bar(&bars->yd_full, t & 1, abort, a.hdr, 14)) {
           return false;
         }
@@ -636,6 +647,7 @@ __global__ void __launch_bounds__(kThreadsFused, 1)
           const float sc = ex2_approx(ti.cum_hi[i] + ti.cum_lo[i]);   // exp(cum_i)
           const float2 sc2 = make_float2(sc, sc);
           __nv_bfloat16* yrow = a.y + ((size_t)(row_base + t * kTileRows + i) * a.H + h) * kP;
+          const bool real = seg_row + t * kTileRows + i < a.T * R;   // else a padding row
           const uint32_t yd = tmem + lane_addr + kColYd + (t & 1) * 64;
 #pragma unroll 1
           for (int c = 0; c < kP; c += 32) {
@@ -655,6 +667,7 @@ __global__ void __launch_bounds__(kThreadsFused, 1)
                                     make_float2(vd[2 * k], vd[2 * k + 1]));
               pk[k] = pack_bf16(o.x, o.y);
             }
+            if (!real) continue;
             uint4* dst = reinterpret_cast<uint4*>(yrow + c);
             dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
             dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
@@ -734,7 +747,7 @@ bool make_map(CUtensorMap* m, CUtensorMapDataType dt, uint32_t rank, const void*
               CUtensorMapSwizzle sw) {
   auto enc = get_encode();
   if (!enc) return false;
-  cuuint32_t es[3] = {1, 1, 1};
+  cuuint32_t es[4] = {1, 1, 1, 1};
   return enc(m, dt, rank, const_cast<void*>(base), dims, strides, box, es,
              CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
@@ -757,22 +770,26 @@ struct MapEntry {
 };
 constexpr int kMapCacheSize = 4;
 
+// Maps over [batch][T * R fused rows][heads or groups][P or N]: the batch is a dimension of
+// its own so that a tile running past the end of a sequence reads zeros, not the next one.
 bool encode_maps(const GenericParams& p, MapEntry& m) {
-  const int64_t rows = p.batch * p.T * p.R;
+  const int64_t rows = p.T * p.R;
   {
-    cuuint64_t dims[3] = {(cuuint64_t)p.P, (cuuint64_t)p.H, (cuuint64_t)rows};
-    cuuint64_t str[2] = {(cuuint64_t)p.P * 2, (cuuint64_t)p.H * p.P * 2};
-    cuuint32_t box[3] = {64, 1, kTileRows};
-    if (!make_map(&m.mx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, p.x, dims, str, box,
+    cuuint64_t dims[4] = {(cuuint64_t)p.P, (cuuint64_t)p.H, (cuuint64_t)rows, (cuuint64_t)p.batch};
+    cuuint64_t str[3] = {(cuuint64_t)p.P * 2, (cuuint64_t)p.H * p.P * 2,
+                         (cuuint64_t)rows * p.H * p.P * 2};
+    cuuint32_t box[4] = {64, 1, kTileRows, 1};
+    if (!make_map(&m.mx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, p.x, dims, str, box,
                   CU_TENSOR_MAP_SWIZZLE_128B))
       return false;
   }
-  cuuint64_t dims[3] = {(cuuint64_t)p.N, (cuuint64_t)p.G, (cuuint64_t)rows};
-  cuuint64_t str[2] = {(cuuint64_t)p.N * 2, (cuuint64_t)p.G * p.N * 2};
-  cuuint32_t box[3] = {64, 1, kTileRows};
-  return make_map(&m.mb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, p.B, dims, str, box,
+  cuuint64_t dims[4] = {(cuuint64_t)p.N, (cuuint64_t)p.G, (cuuint64_t)rows, (cuuint64_t)p.batch};
+  cuuint64_t str[3] = {(cuuint64_t)p.N * 2, (cuuint64_t)p.G * p.N * 2,
+                       (cuuint64_t)rows * p.G * p.N * 2};
+  cuuint32_t box[4] = {64, 1, kTileRows, 1};
+  return make_map(&m.mb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, p.B, dims, str, box,
                   CU_TENSOR_MAP_SWIZZLE_128B) &&
-         make_map(&m.mc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, p.C, dims, str, box,
+         make_map(&m.mc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, p.C, dims, str, box,
                   CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
@@ -841,8 +858,11 @@ int fused_segments(int64_t batch, int64_t H, int64_t ntiles) {
 
 }  // namespace
 
+// Tiles of 128 fused rows per sequence (the last may be partial).
+int64_t fused_tiles(int64_t T, int64_t R) { return (T * R + kTileRows - 1) / kTileRows; }
+
 size_t fused_bf16_workspace_bytes(int64_t batch, int64_t T, int64_t H, int64_t R) {
-  const int64_t ntiles = T * R / kTileRows;
+  const int64_t ntiles = fused_tiles(T, R);
   const int nseg = fused_segments(batch, H, ntiles);
   size_t bytes = sizeof(WsHeader);
   if (nseg > 1) {
@@ -858,7 +878,7 @@ bool fused_bf16_supported(int64_t T, int64_t H, int64_t P, int64_t N, int64_t R,
   if (P != kP || N != kN) return false;
   if (R < 1 || R > 32 || (kTileRows % R) != 0) return false;
   if (H % 4 != 0) return false;                      // dA tile loads use 16-byte boxes
-  if ((T * R) % kTileRows != 0) return false;
+  (void)T;
   (void)l;
   return true;
 }
@@ -877,7 +897,7 @@ cudaError_t fused_bf16_forward(const GenericParams& p, cudaStream_t st) {
   a.R = (int32_t)p.R;
   a.H = (int32_t)p.H;
   a.G = (int32_t)p.G;
-  a.ntiles = (int32_t)(p.T * p.R / kTileRows);
+  a.ntiles = (int32_t)fused_tiles(p.T, p.R);
   a.steps = steps;
   a.nseg = fused_segments(p.batch, p.H, a.ntiles);
   a.seg_tiles = (a.ntiles + a.nseg - 1) / a.nseg;
@@ -905,7 +925,7 @@ cudaError_t fused_bf16_forward(const GenericParams& p, cudaStream_t st) {
 }
 
 int fused_bf16_launches(int64_t batch, int64_t T, int64_t H, int64_t R) {
-  return fused_segments(batch, H, T * R / kTileRows) > 1 ? 3 : 1;
+  return fused_segments(batch, H, fused_tiles(T, R)) > 1 ? 3 : 1;
 }
 
 }  // namespace ssd

@@ -17,7 +17,9 @@
 // are never exponentiated).
 //
 // This path handles every supported shape; the fused tensor-core kernels take over the shapes
-// they implement.
+// they implement.  When seqlen is not a multiple of the chunk length the last chunk is short:
+// its missing steps read as dA = 0, x = 0 and B = C = theta = 0 (zero padding, which leaves y of
+// the real steps and the final state unchanged) and their y is not written.
 #include <math.h>
 
 #include "common.cuh"
@@ -34,21 +36,22 @@ constexpr int kScanRows = 64;    // output rows per chunk_scan block
 constexpr int kScanCols = 32;    // source rows per chunk_scan step
 constexpr double kTwoPi = 6.283185307179586476925286766559;
 
-// Block-cooperative inclusive cumsum of l values read with stride `stride` (warp 0 does it).
+// Block-cooperative inclusive cumsum of l values read with stride `stride` (warp 0 does it);
+// values at or after nv read as zero.
 // The prefix sums are accumulated in fp64 and kept as an unevaluated float pair hi + lo, so that
 // the segment sums cum[i] - cum[j] of the decay mask are exact to about one float ulp of the
 // difference itself (not of |cum|, which reaches hundreds within a chunk); this is the
 // segsum.rs page's difference-of-prefix-sums form with the rounding of the large prefix
 // removed.
-__device__ void chunk_cumsum(const float* __restrict__ src, int64_t stride, int l, float* s_hi,
-                             float* s_lo) {
+__device__ void chunk_cumsum(const float* __restrict__ src, int64_t stride, int l, int nv,
+                             float* s_hi, float* s_lo) {
   if (threadIdx.x < 32) {
     const int lane = threadIdx.x;
     const int per = (l + 31) / 32;
     const int beg = min(l, lane * per);
     const int end = min(l, beg + per);
     double s = 0.0;
-    for (int t = beg; t < end; ++t) s += (double)__ldg(src + (int64_t)t * stride);
+    for (int t = beg; t < min(end, nv); ++t) s += (double)__ldg(src + (int64_t)t * stride);
     double incl = s;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
@@ -57,7 +60,7 @@ __device__ void chunk_cumsum(const float* __restrict__ src, int64_t stride, int 
     }
     double acc = incl - s;
     for (int t = beg; t < end; ++t) {
-      acc += (double)__ldg(src + (int64_t)t * stride);
+      if (t < nv) acc += (double)__ldg(src + (int64_t)t * stride);
       const float hi = (float)acc;
       s_hi[t] = hi;
       s_lo[t] = (float)(acc - (double)hi);
@@ -68,6 +71,11 @@ __device__ void chunk_cumsum(const float* __restrict__ src, int64_t stride, int 
 // exp(cum[i] - cum[j]) from the hi/lo prefix pairs.
 __device__ __forceinline__ float seg_exp(const float* hi, const float* lo, int i, int j) {
   return expf((hi[i] - hi[j]) + (lo[i] - lo[j]));
+}
+
+// Real steps of chunk c (the last chunk may be short).
+__device__ __forceinline__ int chunk_steps(const GenericParams& p, int64_t c) {
+  return (int)min(p.l, p.T - c * p.l);
 }
 
 // x reduced to [-pi, pi] (fp64 in, fp32 out).
@@ -81,11 +89,12 @@ __device__ inline float reduce_two_pi(double a) {
 __device__ void chunk_angles(const GenericParams& p, int64_t b, int64_t c, int64_t h,
                              float* s_ang) {
   const int64_t K = p.N / 2;
+  const int nv = chunk_steps(p, c);
   for (int64_t k = threadIdx.x; k < K; k += blockDim.x) {
     double acc = p.phi[((b * (p.nch + 1) + c) * p.H + h) * K + k];
     const float* th = p.theta + ((b * p.T + c * p.l) * p.H + h) * K + k;
     for (int64_t t = 0; t < p.l; ++t) {
-      acc += (double)__ldg(th + t * p.H * K);
+      if (t < nv) acc += (double)__ldg(th + t * p.H * K);
       s_ang[t * K + k] = reduce_two_pi(acc);
     }
   }
@@ -96,7 +105,7 @@ template <typename T>
 __device__ void stage_bc_rows(const GenericParams& p, const T* __restrict__ src, int64_t b,
                               int64_t c, int64_t g, int64_t row0, int rows, const float* s_ang,
                               float* dst, int ld) {
-  const int64_t L = p.l * p.R;
+  const int64_t L = (int64_t)chunk_steps(p, c) * p.R;   // real rows of the chunk
   const int64_t N = p.N;
   const int64_t base = ((b * p.T + c * p.l) * p.R) * p.G + g;   // fused row 0, group g
   if (p.theta == nullptr) {
@@ -141,7 +150,8 @@ __global__ void __launch_bounds__(kPhiThreads) phi_chunk_sum_kernel(GenericParam
   for (int64_t k = threadIdx.x % 32; k < K; k += 32) {
     const float* th = p.theta + ((b * p.T + c * p.l) * p.H + h) * K + k;
     fp::DF s = {0.f, 0.f};
-    for (int64_t t = 0; t < p.l; ++t) s = fp::df_add(s, fp::DF{__ldg(th + t * p.H * K), 0.f});
+    const int nv = chunk_steps(p, c);
+    for (int64_t t = 0; t < nv; ++t) s = fp::df_add(s, fp::DF{__ldg(th + t * p.H * K), 0.f});
     p.phisum[((b * p.nch + c) * p.H + h) * K + k] = (double)s.hi + (double)s.lo;
   }
 }
@@ -190,7 +200,8 @@ __global__ void __launch_bounds__(kThreads) chunk_state_kernel(GenericParams p) 
   float* s_B = s_x + kStateRows * P;         // [kStateRows][N]
   float* s_ang = s_B + kStateRows * N;       // [l][N/2] when theta
 
-  chunk_cumsum(p.dA + (b * p.T + c * p.l) * p.H + h, p.H, l, s_cum, s_lo);
+  const int Lv = chunk_steps(p, c) * R;     // real rows of the chunk
+  chunk_cumsum(p.dA + (b * p.T + c * p.l) * p.H + h, p.H, l, Lv / R, s_cum, s_lo);
   if (p.theta) chunk_angles(p, b, c, h, s_ang);
   __syncthreads();
   const float cum_end = s_cum[l - 1] + s_lo[l - 1];
@@ -207,7 +218,9 @@ __global__ void __launch_bounds__(kThreads) chunk_state_kernel(GenericParams p) 
     const int rows = min(kStateRows, L - i0);
     for (int e = threadIdx.x; e < kStateRows * P; e += blockDim.x) {
       const int r = e / P, pp = e % P;
-      s_x[e] = (r < rows) ? ld_f32(xs + xbase + (int64_t)(i0 + r) * p.H * p.P + pp) : 0.f;
+      s_x[e] = (r < rows && i0 + r < Lv)
+                   ? ld_f32(xs + xbase + (int64_t)(i0 + r) * p.H * p.P + pp)
+                   : 0.f;
     }
     stage_bc_rows(p, static_cast<const T*>(p.B), b, c, g, i0, kStateRows, s_ang, s_B, N);
     __syncthreads();
@@ -308,7 +321,8 @@ __global__ void __launch_bounds__(kThreads) chunk_scan_kernel(GenericParams p) {
   float* s_M = s_x + kScanCols * P;                  // [kScanRows][kScanCols+1]
   float* s_ang = s_M + kScanRows * (kScanCols + 1);  // [l][N/2] when theta
 
-  chunk_cumsum(p.dA + (b * p.T + c * p.l) * p.H + h, p.H, l, s_cum, s_lo);
+  const int Lv = chunk_steps(p, c) * R;     // real rows of the chunk
+  chunk_cumsum(p.dA + (b * p.T + c * p.l) * p.H + h, p.H, l, Lv / R, s_cum, s_lo);
   if (p.theta) chunk_angles(p, b, c, h, s_ang);
   __syncthreads();
 
@@ -342,7 +356,7 @@ __global__ void __launch_bounds__(kThreads) chunk_scan_kernel(GenericParams p) {
     stage_bc_rows(p, static_cast<const T*>(p.B), b, c, g, j0, kScanCols, s_ang, s_B, ldn);
     for (int e = threadIdx.x; e < kScanCols * P; e += blockDim.x) {
       const int r = e / P, pp = e % P;
-      s_x[e] = (j0 + r < L) ? ld_f32(xs + xbase + (int64_t)(j0 + r) * p.H * p.P + pp) : 0.f;
+      s_x[e] = (j0 + r < Lv) ? ld_f32(xs + xbase + (int64_t)(j0 + r) * p.H * p.P + pp) : 0.f;
     }
     __syncthreads();
     for (int e = threadIdx.x; e < kScanRows * kScanCols; e += blockDim.x) {
@@ -369,7 +383,7 @@ __global__ void __launch_bounds__(kThreads) chunk_scan_kernel(GenericParams p) {
     }
   }
 
-  if (i < L) {
+  if (i < Lv) {
     T* ys = static_cast<T*>(p.y);
     T* yrow = ys + xbase + (int64_t)i * p.H * p.P;
 #pragma unroll

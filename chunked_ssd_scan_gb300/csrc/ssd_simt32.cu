@@ -13,7 +13,8 @@
 // every MMA, and with slowly decaying states the partial sums are large enough that the bias
 // exceeds the fp32 tolerance (1e-4 (1 + |y|)) where y cancels; these kernels accumulate with
 // round-to-nearest fp32 FMAs.  Exponentials use exp2f on double-float prefix sums, and the
-// rotation uses sincosf on double-float angles.
+// rotation uses sincosf on double-float angles.  A short last chunk (seqlen not a multiple of
+// 64) reads its missing steps as zeros (dA = x = B = C = theta = 0) and writes no y for them.
 #include <math.h>
 
 #include "common.cuh"
@@ -35,16 +36,22 @@ constexpr float kTwoPiHi64 = 6.28318548202514648f;        // float(2 pi)
 constexpr float kTwoPiLo64 = -1.7484556000744487e-07f;    // 2 pi - kTwoPiHi64
 constexpr int kTileFloats = kT64 * kT64;
 
-// log2-scaled double-float prefix sums of dA over steps [0, n) of a chunk, by warp 0:
-// cum_hi/cum_lo[t] is the inclusive sum up to step t; *total (natural units) if non-null.
-__device__ void chunk_prefix64(const float* __restrict__ src, int64_t stride, int n, float* cum_hi,
-                               float* cum_lo, float* total) {
+// Real steps of chunk c (the last chunk may be short).
+__device__ __forceinline__ int steps64(const GenericParams& p, int64_t c) {
+  return (int)min(p.l, p.T - c * p.l);
+}
+
+// log2-scaled double-float prefix sums of dA over steps [0, n) of a chunk, by warp 0 (steps at
+// or after nv read as zero): cum_hi/cum_lo[t] is the inclusive sum up to step t; *total
+// (natural units) if non-null.
+__device__ void chunk_prefix64(const float* __restrict__ src, int64_t stride, int n, int nv,
+                               float* cum_hi, float* cum_lo, float* total) {
   if (threadIdx.x >= 32) return;
   const int lane = threadIdx.x;
   const int per = (n + 31) / 32;
   const int beg = min(n, lane * per), end = min(n, beg + per);
   DF s = {0.f, 0.f};
-  for (int t = beg; t < end; ++t) s = df_add(s, DF{__ldg(src + (int64_t)t * stride), 0.f});
+  for (int t = beg; t < min(end, nv); ++t) s = df_add(s, DF{__ldg(src + (int64_t)t * stride), 0.f});
   DF incl = s;
 #pragma unroll
   for (int off = 1; off < 32; off <<= 1) {
@@ -55,7 +62,7 @@ __device__ void chunk_prefix64(const float* __restrict__ src, int64_t stride, in
   DF acc = df_shfl_up(incl, 1);
   if (lane == 0) acc = DF{0.f, 0.f};
   for (int t = beg; t < end; ++t) {
-    acc = df_add(acc, DF{__ldg(src + (int64_t)t * stride), 0.f});
+    if (t < nv) acc = df_add(acc, DF{__ldg(src + (int64_t)t * stride), 0.f});
     const float chi = acc.hi * kLog2e64;
     cum_hi[t] = chi;
     cum_lo[t] = fmaf(acc.hi, kLog2e64, -chi) + acc.lo * kLog2e64;
@@ -68,13 +75,17 @@ __device__ void chunk_prefix64(const float* __restrict__ src, int64_t stride, in
 // `ang` (coalesced); thread (pair k, group gr) then sums its run of consecutive steps as a
 // double-float, the group totals of each pair are prefix-summed through shared memory, and
 // each thread rewrites its run in place.
-// theta rows of steps [0, n) into ang[t * 32 + k] with 16-byte cp.async (not waited for).
+// theta rows of steps [0, n) into ang[t * 32 + k] with 16-byte cp.async (not waited for);
+// steps after the chunk's real ones are zero-filled (no global read).
 __device__ void issue_theta64(const GenericParams& p, int64_t b, int64_t c, int64_t h, int n,
                               float* ang) {
   const float* th = p.theta + ((b * p.T + c * p.l) * p.H + h) * kPairs64;
+  const int nv = steps64(p, c);
   for (int e = threadIdx.x; e < n * (kPairs64 / 4); e += blockDim.x) {
     const int t = e / (kPairs64 / 4), q = e % (kPairs64 / 4);
-    cp_async16(ang + t * kPairs64 + 4 * q, th + (int64_t)t * p.H * kPairs64 + 4 * q, 16);
+    const bool real = t < nv;
+    cp_async16(ang + t * kPairs64 + 4 * q, th + (int64_t)(real ? t : 0) * p.H * kPairs64 + 4 * q,
+               real ? 16 : 0);
   }
 }
 
@@ -145,11 +156,14 @@ __device__ void stage_bc64(const GenericParams& p, const float* __restrict__ src
     // row-major: the 16 lanes of a half-warp read and write one row (coalesced loads,
     // conflict-free shared stores)
     const int ch = tid & 15;
+    const int nv = steps64(p, c);
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
       const int row = (tid >> 4) + 16 * r;
-      float4 f = __ldg(reinterpret_cast<const float4*>(
-                           src + ((b * p.T + c * p.l + s0 + row) * p.G + g) * kT64) + ch);
+      float4 f = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (s0 + row < nv)
+        f = __ldg(reinterpret_cast<const float4*>(
+                      src + ((b * p.T + c * p.l + s0 + row) * p.G + g) * kT64) + ch);
       if (p.theta) {
         const float* ar = ang + (s0 + row) * kPairs64 + 2 * ch;
         float s, co;
@@ -167,9 +181,10 @@ __device__ void stage_bc64(const GenericParams& p, const float* __restrict__ src
   const float4* s4 = reinterpret_cast<const float4*>(
       src + ((b * p.T + c * p.l + s0 + row) * p.G + g) * kT64 + q0);
   float v[16];
+  const bool real = s0 + row < steps64(p, c);
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
-    const float4 f = __ldg(s4 + q);
+    const float4 f = real ? __ldg(s4 + q) : make_float4(0.f, 0.f, 0.f, 0.f);
     v[4 * q] = f.x;
     v[4 * q + 1] = f.y;
     v[4 * q + 2] = f.z;
@@ -195,12 +210,15 @@ __device__ void stage_x64(const GenericParams& p, int64_t b, int64_t c, int64_t 
                           const float* scale, float* dst) {
   const int tid = threadIdx.x;
   const int ch = tid & 15;   // half-warps read and write whole rows
+  const int nv = steps64(p, c);
 #pragma unroll
   for (int r = 0; r < 4; ++r) {
     const int row = (tid >> 4) + 16 * r;
-    const float4 f = __ldg(reinterpret_cast<const float4*>(
-                               static_cast<const float*>(p.x) +
-                               ((b * p.T + c * p.l + s0 + row) * p.H + h) * kT64) + ch);
+    float4 f = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (s0 + row < nv)
+      f = __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(p.x) +
+                                                ((b * p.T + c * p.l + s0 + row) * p.H + h) * kT64) +
+                ch);
     const float w = scale ? scale[row] : 1.f;
     *reinterpret_cast<float4*>(dst + row * kT64 + 4 * ch) =
         make_float4(f.x * w, f.y * w, f.z * w, f.w * w);
@@ -224,7 +242,8 @@ __global__ void __launch_bounds__(kSimtThreads) simt_state_kernel(GenericParams 
   float* dec = cum_lo + l;
   float* ang = dec + l;
   float* total = ang + (p.theta ? l * kPairs64 : 0);
-  chunk_prefix64(p.dA + (b * p.T + c * p.l) * p.H + h, p.H, l, cum_hi, cum_lo, total);
+  chunk_prefix64(p.dA + (b * p.T + c * p.l) * p.H + h, p.H, l, steps64(p, c), cum_hi, cum_lo,
+                 total);
   if (p.theta) {
     chunk_angles64(p, b, c, h, l, ang);
   } else {
@@ -273,13 +292,17 @@ __global__ void __launch_bounds__(kSimtThreads) simt_scan_kernel(GenericParams p
   if (p.theta) issue_theta64(p, b, c, h, l, ang);
   {
     const float* xsrc = static_cast<const float*>(p.x);
+    const int nv = steps64(p, c);
     for (int e = threadIdx.x; e < kTileFloats / 4; e += kSimtThreads) {
       const int row = e / (kT64 / 4), q = e % (kT64 / 4);
+      const bool real = row < nv;   // steps after the real ones are zero-filled
       cp_async16(xs + row * kT64 + 4 * q,
-                 xsrc + ((b * p.T + c * p.l + row) * p.H + h) * kT64 + 4 * q, 16);
+                 xsrc + ((b * p.T + c * p.l + (real ? row : 0)) * p.H + h) * kT64 + 4 * q,
+                 real ? 16 : 0);
     }
   }
-  chunk_prefix64(p.dA + (b * p.T + c * p.l) * p.H + h, p.H, l, cum_hi, cum_lo, nullptr);
+  chunk_prefix64(p.dA + (b * p.T + c * p.l) * p.H + h, p.H, l, steps64(p, c), cum_hi, cum_lo,
+                 nullptr);
   {
     // h_in [p][n] (written over S by the state pass) -> h^T [n][p]
     const float* hin = p.states + ((b * p.nch + c) * p.H + h) * kTileFloats;
@@ -329,9 +352,11 @@ __global__ void __launch_bounds__(kSimtThreads) simt_scan_kernel(GenericParams p
       block_product<true>(bt, xs, ty, tx, yd);   // Yd[i][p] += sum_j M[i][j] x[j][p]
       __syncthreads();
     }
+    const int nv = steps64(p, c);
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
       const int si = i0 + 4 * ty + r;
+      if (si >= nv) continue;   // padding step of a short last chunk
       const float sc = exp2f(cum_hi[si] + cum_lo[si]);   // exp(cum_i)
       float* yrow = static_cast<float*>(p.y) + ((b * p.T + c * p.l + si) * p.H + h) * kT64;
       *reinterpret_cast<float4*>(yrow + 4 * tx) =

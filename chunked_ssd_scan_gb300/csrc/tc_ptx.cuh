@@ -320,6 +320,17 @@ __device__ __forceinline__ void tma_load_3d_elect(void* dst, const CUtensorMap* 
       : "memory");
 }
 
+__device__ __forceinline__ void tma_load_4d_elect(void* dst, const CUtensorMap* map,
+                                                  uint64_t* bar, int32_t x, int32_t y,
+                                                  int32_t z, int32_t w) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5, %6}], [%2];\n\t}" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z), "r"(w)
+      : "memory");
+}
+
 // 32 lanes x 32 bits, 32 consecutive columns per thread (no wait).
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
   uint32_t r[32];

@@ -54,7 +54,7 @@ typedef struct ssd_shape {
   int64_t dstate;    /* N (even when theta is given)                             */
   int64_t ngroups;   /* G, divides H                                             */
   int64_t mimo_rank; /* R >= 1; the fused chunk length is L = chunk_len * R      */
-  int64_t chunk_len; /* l; T must be a multiple of l                             */
+  int64_t chunk_len; /* l >= 1; need not divide T (the last chunk is then short) */
   int32_t io_dtype;  /* ssd_dtype of x, B, C and y                               */
   int32_t has_theta; /* 1 when theta will be passed (changes the workspace size) */
 } ssd_shape;
@@ -97,7 +97,11 @@ int32_t ssd_chunked_launches(const ssd_shape* shape);
  * Rot(theta) turns each interleaved pair (2k, 2k+1) of the dstate axis by +theta[...,k].
  * x is the pre-scaled value (no dt factor) and no skip term is added, as in K3/K5.
  * The result equals the sequential recurrence above for any chunk_len; chunk_len sets how the
- * kernels tile time (K1..K5 granularity) and must divide seqlen.
+ * kernels tile time (K1..K5 granularity).  When it does not divide seqlen the last chunk is short
+ * (scan.py page, chunked_scan): the kernels treat its missing steps as zero padding (dA = 0,
+ * x = 0; moments.rs page: a pad step is an identity decay with a zero write, so the state passes
+ * through unchanged), which leaves y of the real steps and the final state exactly those of the
+ * unpadded recurrence, and write no y there.
  *
  * Arguments: x, B, C, y are device pointers of io_dtype; dA, theta, init_state, final_state are
  * device f32.  theta may be NULL only if shape->has_theta == 0 (and must be non-NULL otherwise);

@@ -17,10 +17,14 @@ def to_np(t):
 
 
 def gpu_ssd(inp: dict, chunk_len: int, dev: str = "cuda", final: bool = True):
+    """One forward through the C ABI; the device-side error word of its workspace must be clean
+    (a bounded wait that gave up would otherwise only show as wrong numbers)."""
     d = {k: (v.to(dev) if v is not None else None) for k, v in inp.items()}
-    y, fin = pkg.ssd_chunked_forward(d["x"], d["dA"], d["B"], d["C"], chunk_len=chunk_len,
-                                     theta=d["theta"], init_state=d["init_state"],
-                                     return_final_state=final)
+    plan = pkg.SSDForwardPlan(d["x"], d["dA"], d["B"], d["C"], chunk_len=chunk_len,
+                              theta=d["theta"], init_state=d["init_state"],
+                              return_final_state=final)
+    y, fin = plan()
+    assert pkg.workspace_status(plan.workspace) == ("SSD_OK", 0)
     torch.cuda.synchronize()
     return to_np(y), to_np(fin)
 

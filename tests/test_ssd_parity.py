@@ -77,6 +77,58 @@ EDGE = [
 ]
 
 
+# seqlen not a multiple of chunk_len (and, for the fused kernel, of the 128-row tile): the last
+# chunk or tile is short and runs as zero padding; every path, with groups, MIMO, rotation and
+# time segments.
+RAGGED = [
+    wl.SSDConfig("ragged_generic_f32", 2, 250, 3, 16, 16, 64, 1, 3, "f32"),
+    wl.SSDConfig("ragged_generic_mimo_theta_f32", 2, 77, 2, 8, 12, 16, 3, 2, "f32", theta=True),
+    wl.SSDConfig("ragged_generic_bf16", 1, 100, 4, 24, 40, 32, 2, 2, "bf16"),
+    wl.SSDConfig("ragged_fused_bf16", 2, 300, 4, 64, 128, 256, 1, 1, "bf16"),
+    wl.SSDConfig("ragged_fused_mimo_bf16", 1, 90, 4, 64, 128, 32, 4, 2, "bf16"),
+    wl.SSDConfig("ragged_fused_segments_bf16", 1, 1000, 8, 64, 128, 128, 1, 1, "bf16"),
+    wl.SSDConfig("ragged_tiled_f32", 1, 200, 2, 64, 64, 64, 1, 1, "f32"),
+    wl.SSDConfig("ragged_tiled_theta_f32", 2, 130, 3, 64, 64, 128, 1, 1, "f32", theta=True),
+]
+
+
+@pytest.mark.parametrize("cfg", RAGGED, ids=lambda c: c.name)
+def test_ragged_sequence_lengths(cfg):
+    assert cfg.seqlen % cfg.chunk_len != 0
+    expect = {"generic": "generic", "fused": "tc_bf16", "tiled": "tiled_f32"}[cfg.name.split("_")[1]]
+    shape = pkg.make_shape(cfg.batch, cfg.seqlen, cfg.nheads, cfg.headdim, cfg.dstate,
+                           cfg.ngroups, cfg.mimo_rank, cfg.chunk_len, cfg.dtype, cfg.theta)
+    assert pkg.ssd_chunked_variant(shape) == expect, cfg.name
+    for kw in ({}, dict(slow_decay=True, init_state=True)):
+        inp = wl.make_ssd_inputs(cfg, seed=8, **kw)
+        y, fin = gpu_ssd(inp, cfg.chunk_len)
+        yr, fr = oracle_ssd(inp)
+        check_close(y, yr, TOL[cfg.dtype], f"{cfg.name} y")
+        check_close(fin, fr, TOL[cfg.dtype], f"{cfg.name} final_state")
+
+
+@pytest.mark.parametrize("cfg", [wl.SSDConfig("vlen_fused", 3, 512, 4, 64, 128, 128, 1, 1, "bf16"),
+                                 wl.SSDConfig("vlen_generic", 3, 200, 2, 16, 16, 64, 2, 2, "f32")],
+                         ids=lambda c: c.name)
+def test_per_sequence_valid_length_by_zero_padding(cfg):
+    """Sequences of different lengths in one batch: steps past a sequence's valid length carry
+    dA = 0 and x = 0 (the moments.rs page's pad semantics), so its final state is the state at
+    its last real step and its y on real steps is that of the truncated sequence."""
+    inp = wl.make_ssd_inputs(cfg, seed=10, init_state=True)
+    lens = [cfg.seqlen, cfg.seqlen - 77, 1]
+    for b, n in enumerate(lens):
+        inp["x"][b, n:] = 0
+        inp["dA"][b, n:] = 0
+    y, fin = gpu_ssd(inp, cfg.chunk_len)
+    for b, n in enumerate(lens):
+        sub = {k: (v[b:b + 1, :n].contiguous() if k != "init_state" else v[b:b + 1])
+               for k, v in inp.items() if v is not None}
+        sub.setdefault("theta", None)
+        yr, fr = oracle_ssd(sub)
+        check_close(y[b:b + 1, :n], yr, TOL[cfg.dtype], f"{cfg.name} y[b={b}, :{n}]")
+        check_close(fin[b:b + 1], fr, TOL[cfg.dtype], f"{cfg.name} final[b={b}]")
+
+
 def test_f32_workloads_use_the_tiled_kernels():
     for cfg in (wl.LONG_ROT_F32, EDGE[-1], EDGE[-2]):
         shape = pkg.make_shape(cfg.batch, cfg.seqlen, cfg.nheads, cfg.headdim, cfg.dstate,
@@ -145,6 +197,29 @@ def test_continuation_through_final_state():
     check_close(f2, ff, 1e-5, "continuation final")
 
 
+@pytest.mark.parametrize("split", [200, 77])
+def test_streaming_continuation_ragged_with_rotation(split):
+    """A stream cut at arbitrary steps (short last chunks on both sides) continues exactly through
+    final_state -> init_state; with rotation no angle carry is needed because the state crosses
+    the boundary in the physical frame."""
+    cfg = wl.SSDConfig("stream", 1, 512, 4, 16, 32, 64, 1, 2, "f32", theta=True)
+    inp = wl.make_ssd_inputs(cfg, seed=9, slow_decay=True, init_state=True)
+    yf, _ = gpu_ssd(inp, 64)
+    first = {k: (v[:, :split].contiguous() if (v is not None and k != "init_state") else v)
+             for k, v in inp.items()}
+    y1, f1 = gpu_ssd(first, 64)
+    second = {k: (v[:, split:].contiguous() if (v is not None and k != "init_state") else v)
+              for k, v in inp.items()}
+    second["init_state"] = torch.from_numpy(f1).float()
+    y2, f2 = gpu_ssd(second, 64)
+    # the two halves accumulate their angles from different origins, so they match the unsplit
+    # call to the fp32 bound, not bitwise: both are checked against the oracle of the whole
+    yr, fr = oracle_ssd(inp)
+    check_close(np.concatenate([y1, y2], axis=1), yr, TOL["f32"], "stream y")
+    check_close(f2, fr, TOL["f32"], "stream final")
+    check_close(yf, yr, TOL["f32"], "unsplit y")
+
+
 def test_deterministic_bitwise():
     cfg = wl.MAMBA2_SISO_BF16.with_(batch=1, seqlen=1024, nheads=8)
     inp = wl.make_ssd_inputs(cfg, seed=7, init_state=True)
@@ -156,8 +231,8 @@ def test_deterministic_bitwise():
 def test_host_rejections_with_real_buffers():
     cfg = wl.TINY_SISO_F32
     d = wl.make_ssd_inputs(cfg, seed=0, device="cuda")
-    with pytest.raises(pkg.SSDError) as e:
-        pkg.ssd_chunked_forward(d["x"], d["dA"], d["B"], d["C"], chunk_len=48)
+    with pytest.raises(pkg.SSDError) as e:   # fused chunk beyond the generic path's limit
+        pkg.ssd_chunked_forward(d["x"], d["dA"], d["B"], d["C"], chunk_len=8192)
     assert e.value.status == 2
     with pytest.raises(ValueError):
         pkg.ssd_chunked_forward(d["x"].cpu(), d["dA"], d["B"], d["C"], chunk_len=64)
