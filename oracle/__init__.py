@@ -3,8 +3,8 @@
 TEST INFRASTRUCTURE ONLY: imported by the test suite, by the smoke check and by the benchmark's
 CPU-baseline leg, never by the library.  It shares no code with the CUDA path.
 
-- ``ssd`` / ``selective_scan`` call the plain sequential recurrences in ``ssd_oracle.c``
-  (C, fp64, threads over independent problems).  These are the oracle proper.
+- ``ssd`` / ``ssd_trapezoidal`` / ``selective_scan`` call the plain sequential recurrences in
+  ``ssd_oracle.c`` (C, fp64, threads over independent problems).  These are the oracle proper.
 - ``chunked_ref`` (numpy, fp64) restates the serial.rs page's K1..K5 chunk decomposition, the
   segsum.rs page's stable segment sum, and the scan.py page's cumulative-angle rotation.  It is
   not an oracle for the GPU; the pin tests use it to check the sequential oracle against the
@@ -13,6 +13,7 @@ CPU-baseline leg, never by the library.  It shares no code with the CUDA path.
 Inputs are numpy arrays (any float dtype; they are upcast to float64) in the library's layouts:
     x  [b,T,R,H,P]   dA [b,T,H]   B, C [b,T,R,G,N]   theta [b,T,H,N/2]   init [b,H,P,N]
     u, delta [b,T,D] A [D,N]      B, C [b,T,N]       skip [D]
+    gamma, beta [b,T,H]   prev_x [b,R,H,P]   prev_B [b,R,G,N]        (trapezoidal form)
 """
 from __future__ import annotations
 
@@ -48,6 +49,8 @@ def _lib():
         lib = ctypes.CDLL(build())
         lib.oracle_ssd_ex.restype = ctypes.c_int
         lib.oracle_ssd_ex.argtypes = [_D] * 8 + [_I64] * 8 + [ctypes.c_int]
+        lib.oracle_ssd_trap_ex.restype = ctypes.c_int
+        lib.oracle_ssd_trap_ex.argtypes = [_D] * 12 + [_I64] * 8 + [ctypes.c_int]
         lib.oracle_selective_scan_ex.restype = ctypes.c_int
         lib.oracle_selective_scan_ex.argtypes = [_D] * 7 + [_I64] * 5 + [ctypes.c_int]
         _LIB = lib
@@ -92,6 +95,32 @@ def ssd(x, dA, B, C, theta=None, init_state=None, nthreads=None, mutation: int =
     return y, fin
 
 
+def ssd_trapezoidal(x, dA, B, C, gamma, beta, theta=None, init_state=None, prev_x=None,
+                    prev_B=None, nthreads=None, mutation: int = 0):
+    """Sequential fp64 trapezoidal SSD recurrence (see ssd_oracle.c).  Returns (y, final_state)."""
+    x, dA, B, C, gamma, beta = (_f64(v) for v in (x, dA, B, C, gamma, beta))
+    theta, init_state, prev_x, prev_B = (_f64(v) for v in (theta, init_state, prev_x, prev_B))
+    b, T, R, H, P = x.shape
+    G, N = B.shape[3], B.shape[4]
+    assert dA.shape == (b, T, H) and gamma.shape == (b, T, H) and beta.shape == (b, T, H)
+    assert B.shape == (b, T, R, G, N) and C.shape == B.shape
+    if theta is not None:
+        assert theta.shape == (b, T, H, N // 2)
+    if init_state is not None:
+        assert init_state.shape == (b, H, P, N)
+    if prev_x is not None or prev_B is not None:
+        assert prev_x.shape == (b, R, H, P) and prev_B.shape == (b, R, G, N)
+    y = np.zeros((b, T, R, H, P), np.float64)
+    fin = np.zeros((b, H, P, N), np.float64)
+    rc = _lib().oracle_ssd_trap_ex(_ptr(x), _ptr(dA), _ptr(B), _ptr(C), _ptr(gamma), _ptr(beta),
+                                   _ptr(theta), _ptr(init_state), _ptr(prev_x), _ptr(prev_B),
+                                   _ptr(y), _ptr(fin), b, T, R, H, G, P, N,
+                                   nthreads or default_threads(), int(mutation))
+    if rc != 0:
+        raise ValueError(f"oracle_ssd_trap rejected its arguments (code {rc})")
+    return y, fin
+
+
 def selective_scan(u, delta, A, B, C, skip=None, nthreads=None, mutation: int = 0):
     """Sequential fp64 selective scan.  Returns y [b,T,D]."""
     u, delta, A, B, C, skip = (_f64(v) for v in (u, delta, A, B, C, skip))
@@ -118,6 +147,11 @@ MUTATIONS_SSD = {
     "rank_local_output": 4,
     "rotation_sign": 5,
     "group_index": 6,
+}
+MUTATIONS_TRAP = {
+    "no_beta": 9,
+    "beta_turned_late": 10,
+    "beta_on_current_write": 11,
 }
 MUTATIONS_SS = {
     "no_skip": 7,

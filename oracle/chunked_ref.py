@@ -133,3 +133,39 @@ def chunked_forward(x, dA, B, C, theta=None, init_state=None, chunk_len=64):
     if phi is not None:
         final = rotate_pairs(final, phi[:, T - 1][:, :, None, :])
     return y, final
+
+
+def trapezoidal_absorbed(x, dA, B, C, gamma, beta, theta=None, init_state=None, prev_x=None,
+                         prev_B=None):
+    """The scan.py page's trapezoidal forward in its absorbed frame: per step the write
+    S_t = sum_r x_{t,r} (outer) B_{t,r}; the beta stream is S shifted one step (S_{-1} from
+    prev_x/prev_B); w_t = gamma_t R(-Phi_t) S_t + beta_t R(-Phi_{t-1}) S_{t-1} with Phi_{-1} = 0;
+    g_t = exp(dA_t) g_{t-1} + w_t from g_{-1} = h_{-1}; h_t = R(Phi_t) g_t; y_t = C_t . h_t.
+    Returns (y [b,T,R,H,P], final [b,H,P,N])."""
+    x, dA, B, C, gamma, beta = (np.asarray(v, np.float64) for v in (x, dA, B, C, gamma, beta))
+    b, T, R, H, P = x.shape
+    G, N = B.shape[3], B.shape[4]
+    Bh = np.repeat(B, H // G, axis=3)                        # [b,T,R,H,N]
+    Ch = np.repeat(C, H // G, axis=3)
+    S = np.einsum("btrhp,btrhn->bthpn", x, Bh)               # [b,T,H,P,N]
+    if prev_x is not None:
+        s0 = np.einsum("brhp,brhn->bhpn", np.asarray(prev_x, np.float64),
+                       np.repeat(np.asarray(prev_B, np.float64), H // G, axis=2))
+    else:
+        s0 = np.zeros((b, H, P, N))
+    Sprev = np.concatenate([s0[:, None], S[:, :-1]], axis=1)
+    if theta is not None:
+        phi = np.cumsum(np.asarray(theta, np.float64), axis=1)   # [b,T,H,N/2]
+    else:
+        phi = np.zeros((b, T, H, N // 2))
+    phi_prev = np.concatenate([np.zeros_like(phi[:, :1]), phi[:, :-1]], axis=1)
+    w = (gamma[..., None, None] * rotate_pairs(S, -phi[:, :, :, None, :])
+         + beta[..., None, None] * rotate_pairs(Sprev, -phi_prev[:, :, :, None, :]))
+    g = np.zeros((b, H, P, N)) if init_state is None else np.asarray(init_state, np.float64).copy()
+    y = np.zeros((b, T, R, H, P))
+    for t in range(T):
+        g = np.exp(dA[:, t])[:, :, None, None] * g + w[:, t]
+        h = rotate_pairs(g, phi[:, t][:, :, None, :])
+        y[:, t] = np.einsum("brhn,bhpn->brhp", Ch[:, t], h)
+    final = rotate_pairs(g, phi[:, T - 1][:, :, None, :]) if T else g
+    return y, final

@@ -27,6 +27,16 @@
  *     The oracle applies this rotation to the state directly at every step (the rotated
  *     recurrence itself), never the absorbed cumulative-angle form the GPU uses.
  *
+ *   Trapezoidal SSD (Mamba-3; scan.py page, the trapezoidal forward: the beta term carries the
+ *   PREVIOUS step's write and is turned by one step less of rotation), per (b, h):
+ *     S_t         = sum_r x[b,t,r,h,:] (outer) B[b,t,r,g,:]      (S_{-1} from prev_x, prev_B)
+ *     h_t         = R(theta_t) (exp(dA_t) h_{t-1} + beta_t S_{t-1}) + gamma_t S_t
+ *     y, final    as above.
+ *   In the scan.py page's absorbed frame this is g_t = alpha_t g_{t-1} + gamma_t R(-Phi_t) S_t
+ *   + beta_t R(-Phi_{t-1}) S_{t-1} with h_t = R(Phi_t) g_t; the oracle runs the physical-frame
+ *   form above, state first decayed and fed the previous write, then turned, then fed the
+ *   current write.
+ *
  *   Selective scan (SSM Selective Scan page, problem statement), one problem per (b, d):
  *     h_{-1}[n] = 0
  *     h_t[n]    = exp(delta[b,t,d] * A[d,n]) * h_{t-1}[n] + delta[b,t,d] * B[b,t,n] * u[b,t,d]
@@ -53,6 +63,8 @@ typedef struct {
   int mutation;
   int64_t nthreads;
   int64_t tid;
+  /* trapezoidal form only (NULL gamma = the plain recurrence above) */
+  const double *gamma, *beta, *prev_x, *prev_B;
 } ssd_job;
 
 /* Planted-mistake codes, used only by the oracle's own pin tests. */
@@ -66,7 +78,76 @@ enum {
   MUT_GROUP_INDEX = 6,     /* maps head h to group h % G instead of h / (H/G)  */
   MUT_SS_NO_SKIP = 7,      /* selective scan: drops the skip term              */
   MUT_SS_DELTA_B = 8,      /* selective scan: forgets the delta factor on B    */
+  MUT_TRAP_NO_BETA = 9,    /* trapezoidal: drops the beta (previous-write) term */
+  MUT_TRAP_BETA_TURNED_LATE = 10, /* trapezoidal: feeds beta*S_{t-1} after the turn */
+  MUT_TRAP_BETA_CURRENT = 11,     /* trapezoidal: beta multiplies S_t, not S_{t-1} */
 };
+
+/* The trapezoidal recurrence for one (b, h); h and the two write buffers hold P*N doubles. */
+static void trap_one(const ssd_job* j, int64_t b, int64_t hh, double* h, double* sprev,
+                     double* scur) {
+  const int64_t T = j->T, R = j->R, H = j->H, G = j->G, P = j->P, N = j->N;
+  const int64_t g = hh / (H / G);
+  if (j->init) {
+    memcpy(h, j->init + ((b * H + hh) * P) * N, sizeof(double) * P * N);
+  } else {
+    memset(h, 0, sizeof(double) * P * N);
+  }
+  /* S_{-1}: the write of the step before the first (the previous call's last step) */
+  for (int64_t p = 0; p < P; ++p) {
+    for (int64_t n = 0; n < N; ++n) {
+      double w = 0.0;
+      if (j->prev_x && j->prev_B) {
+        for (int64_t r = 0; r < R; ++r)
+          w += j->prev_x[((b * R + r) * H + hh) * P + p] * j->prev_B[((b * R + r) * G + g) * N + n];
+      }
+      sprev[p * N + n] = w;
+    }
+  }
+  for (int64_t t = 0; t < T; ++t) {
+    const double a = exp(j->dA[(b * T + t) * H + hh]);
+    const double gm = j->gamma[(b * T + t) * H + hh];
+    const double bt = j->beta[(b * T + t) * H + hh];
+    for (int64_t p = 0; p < P; ++p) {
+      for (int64_t n = 0; n < N; ++n) {
+        double w = 0.0;
+        for (int64_t r = 0; r < R; ++r)
+          w += j->x[(((b * T + t) * R + r) * H + hh) * P + p] *
+               j->B[(((b * T + t) * R + r) * G + g) * N + n];
+        scur[p * N + n] = w;
+      }
+    }
+    const double* fed = (j->mutation == MUT_TRAP_BETA_CURRENT) ? scur : sprev;
+    const int late = j->mutation == MUT_TRAP_BETA_TURNED_LATE;
+    const double bw = (j->mutation == MUT_TRAP_NO_BETA) ? 0.0 : bt;
+    for (int64_t e = 0; e < P * N; ++e) h[e] = a * h[e] + (late ? 0.0 : bw * fed[e]);
+    if (j->theta) {
+      const double* th = j->theta + ((b * T + t) * H + hh) * (N / 2);
+      for (int64_t k = 0; k < N / 2; ++k) {
+        const double c = cos(th[k]), s = sin(th[k]);
+        for (int64_t p = 0; p < P; ++p) {
+          double* hp = h + p * N;
+          const double e0 = hp[2 * k], o0 = hp[2 * k + 1];
+          hp[2 * k] = c * e0 - s * o0;
+          hp[2 * k + 1] = s * e0 + c * o0;
+        }
+      }
+    }
+    for (int64_t e = 0; e < P * N; ++e) h[e] += gm * scur[e] + (late ? bw * fed[e] : 0.0);
+    for (int64_t r = 0; r < R; ++r) {
+      const double* cv = j->C + (((b * T + t) * R + r) * G + g) * N;
+      for (int64_t p = 0; p < P; ++p) {
+        double acc = 0.0;
+        for (int64_t n = 0; n < N; ++n) acc += cv[n] * h[p * N + n];
+        j->y[(((b * T + t) * R + r) * H + hh) * P + p] = acc;
+      }
+    }
+    memcpy(sprev, scur, sizeof(double) * P * N);
+  }
+  if (j->final_state) {
+    memcpy(j->final_state + ((b * H + hh) * P) * N, h, sizeof(double) * P * N);
+  }
+}
 
 static void ssd_one(const ssd_job* j, int64_t b, int64_t hh, double* h) {
   const int64_t T = j->T, R = j->R, H = j->H, G = j->G, P = j->P, N = j->N;
@@ -138,10 +219,14 @@ static void ssd_one(const ssd_job* j, int64_t b, int64_t hh, double* h) {
 
 static void* ssd_worker(void* arg) {
   const ssd_job* j = (const ssd_job*)arg;
-  double* h = (double*)malloc(sizeof(double) * j->P * j->N);
+  double* h = (double*)malloc(sizeof(double) * j->P * j->N * 3);
   if (!h) return (void*)1;
   for (int64_t idx = j->tid; idx < j->batch * j->H; idx += j->nthreads) {
-    ssd_one(j, idx / j->H, idx % j->H, h);
+    if (j->gamma) {
+      trap_one(j, idx / j->H, idx % j->H, h, h + j->P * j->N, h + 2 * j->P * j->N);
+    } else {
+      ssd_one(j, idx / j->H, idx % j->H, h);
+    }
   }
   free(h);
   return NULL;
@@ -154,11 +239,11 @@ static int64_t clamp_threads(int64_t nthreads, int64_t work) {
   return nthreads < 1 ? 1 : nthreads;
 }
 
-/* Returns 0 on success, a negative value on invalid arguments or allocation failure. */
-int oracle_ssd_ex(const double* x, const double* dA, const double* B, const double* C,
-                  const double* theta, const double* init_state, double* y, double* final_state,
-                  int64_t batch, int64_t T, int64_t R, int64_t H, int64_t G, int64_t P, int64_t N,
-                  int64_t nthreads, int mutation) {
+static int run_ssd(const double* x, const double* dA, const double* B, const double* C,
+                   const double* theta, const double* init_state, double* y, double* final_state,
+                   int64_t batch, int64_t T, int64_t R, int64_t H, int64_t G, int64_t P, int64_t N,
+                   int64_t nthreads, int mutation, const double* gamma, const double* beta,
+                   const double* prev_x, const double* prev_B) {
   if (!x || !dA || !B || !C || !y) return -1;
   if (batch < 0 || T < 0 || R < 1 || H < 1 || G < 1 || P < 1 || N < 1) return -2;
   if (H % G != 0) return -3;
@@ -180,8 +265,9 @@ int oracle_ssd_ex(const double* x, const double* dA, const double* B, const doub
   }
   int rc = 0;
   for (int64_t i = 0; i < nt; ++i) {
-    ssd_job j = {x, dA, B, C, theta, init_state, y, final_state, batch, T, R, H, G, P, N,
-                 mutation, nt, i};
+    ssd_job j = {x,  dA, B,    C,     theta,  init_state, y,      final_state, batch, T,
+                 R,  H,  G,    P,     N,      mutation,   nt,     i,           gamma, beta,
+                 prev_x, prev_B};
     jobs[i] = j;
   }
   for (int64_t i = 1; i < nt; ++i) pthread_create(&th[i], NULL, ssd_worker, &jobs[i]);
@@ -194,6 +280,27 @@ int oracle_ssd_ex(const double* x, const double* dA, const double* B, const doub
   free(jobs);
   free(th);
   return rc;
+}
+
+/* Returns 0 on success, a negative value on invalid arguments or allocation failure. */
+int oracle_ssd_ex(const double* x, const double* dA, const double* B, const double* C,
+                  const double* theta, const double* init_state, double* y, double* final_state,
+                  int64_t batch, int64_t T, int64_t R, int64_t H, int64_t G, int64_t P, int64_t N,
+                  int64_t nthreads, int mutation) {
+  return run_ssd(x, dA, B, C, theta, init_state, y, final_state, batch, T, R, H, G, P, N,
+                 nthreads, mutation, NULL, NULL, NULL, NULL);
+}
+
+/* Trapezoidal form: gamma, beta [b,T,H]; prev_x [b,R,H,P] and prev_B [b,R,G,N] may be NULL
+ * (no previous write). */
+int oracle_ssd_trap_ex(const double* x, const double* dA, const double* B, const double* C,
+                       const double* gamma, const double* beta, const double* theta,
+                       const double* init_state, const double* prev_x, const double* prev_B,
+                       double* y, double* final_state, int64_t batch, int64_t T, int64_t R,
+                       int64_t H, int64_t G, int64_t P, int64_t N, int64_t nthreads, int mutation) {
+  if (!gamma || !beta) return -1;
+  return run_ssd(x, dA, B, C, theta, init_state, y, final_state, batch, T, R, H, G, P, N,
+                 nthreads, mutation, gamma, beta, prev_x, prev_B);
 }
 
 int oracle_ssd(const double* x, const double* dA, const double* B, const double* C,

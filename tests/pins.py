@@ -252,3 +252,88 @@ def pin_causality_and_continuation(mutation=0):
 SSD_PINS = [pin_closed_form, pin_special_cases, pin_chunk_invariance, pin_rotation,
             pin_mimo_superposition, pin_causality_and_continuation]
 SS_PINS = [pin_worked_example, pin_selective_scan_superposition]
+
+
+# ------------------------------------------------------------------------------ trapezoidal
+def _trap_problem(seed, b, T, R, H, G, P, N, *, theta=False, prev=True):
+    x, dA, B, C, th, h0 = _problem(seed, b, T, R, H, G, P, N, theta=theta, init=True)
+    r = _rng(seed + 1000)
+    gamma = r.uniform(0.2, 1.0, (b, T, H))
+    beta = r.uniform(0.2, 1.0, (b, T, H))
+    px = r.standard_normal((b, R, H, P)) if prev else None
+    pb = r.standard_normal((b, R, G, N)) if prev else None
+    return x, dA, B, C, gamma, beta, th, h0, px, pb
+
+
+def pin_trapezoidal_rule(mutation=0):
+    """With no decay (dA = 0) and gamma = beta = 1/2 the state is the trapezoidal-rule sum of the
+    writes; for a write that is linear in time, s_t = t, with s_{-1} = -1 from the previous
+    step, that sum is exact: h_t = integral of s from -1 to t = (t^2 - 1)/2."""
+    T = 12
+    t = np.arange(T, dtype=np.float64)
+    x = t.reshape(1, T, 1, 1, 1)
+    one = np.ones((1, T, 1, 1, 1))
+    half = np.full((1, T, 1), 0.5)
+    y, f = oracle.ssd_trapezoidal(x, np.zeros((1, T, 1)), one, one, half, half,
+                                  prev_x=np.full((1, 1, 1, 1), -1.0),
+                                  prev_B=np.ones((1, 1, 1, 1)), mutation=mutation)
+    ref = (t * t - 1.0) / 2.0
+    return [("trapezoid_of_linear_write", _maxerr(y.reshape(T), ref), 1e-12),
+            ("trapezoid_final", _maxerr(f.reshape(1), ref[-1:]), 1e-12)]
+
+
+def pin_trapezoidal_absorbed_frame(mutation=0):
+    """The scan.py page's own trapezoidal algebra (absorbed frame: the gamma write turned by
+    -Phi_t, the beta write by -Phi_{t-1}, one step less; chunked_ref.trapezoidal_absorbed)
+    against the oracle's physical-frame recurrence, with MIMO ranks, groups, an initial state
+    and a previous write."""
+    res = []
+    x, dA, B, C, gm, bt, th, h0, px, pb = _trap_problem(41, 2, 23, 2, 4, 2, 3, 6, theta=True)
+    y, f = oracle.ssd_trapezoidal(x, dA, B, C, gm, bt, th, h0, px, pb, mutation=mutation)
+    y2, f2 = chunked_ref.trapezoidal_absorbed(x, dA, B, C, gm, bt, th, h0, px, pb)
+    res.append(("trap_absorbed_y", _maxerr(y, y2), 1e-10))
+    res.append(("trap_absorbed_final", _maxerr(f, f2), 1e-10))
+    return res
+
+
+def pin_trapezoidal_combined_injection(mutation=0):
+    """The moments.rs page's combined injections: the trapezoid is one scalar-decay system with
+    2R write channels, x^ = [gamma_t x_t, beta_t x_{t-1}] and b^ = [B_t, R(theta_t) B_{t-1}]
+    (the previous write turned by this step's angle), read by the R output channels -- checked
+    against the plain oracle with zero C on the extra channels.  Also: beta = 0 and gamma = 1
+    is the plain recurrence, and a stream cut in two continues exactly through final_state and
+    the last step's (x, B) as the next call's previous write."""
+    res = []
+    b, T, R, H, G, P, N = 2, 19, 2, 2, 2, 3, 4
+    x, dA, B, C, gm, bt, th, h0, px, pb = _trap_problem(43, b, T, R, H, G, P, N, theta=True)
+    y, f = oracle.ssd_trapezoidal(x, dA, B, C, gm, bt, th, h0, px, pb, mutation=mutation)
+    xp = np.concatenate([px[:, None], x[:, :-1]], axis=1)          # x_{t-1}
+    bp = np.concatenate([pb[:, None], B[:, :-1]], axis=1)          # B_{t-1}
+    xh = np.concatenate([gm[:, :, None, :, None] * x, bt[:, :, None, :, None] * xp], axis=2)
+    # b^ turned by theta_t of each head: expand the groups to heads first
+    bph = np.repeat(bp, H // G, axis=3)
+    bh = np.concatenate([np.repeat(B, H // G, axis=3),
+                         chunked_ref.rotate_pairs(bph, th[:, :, None, :, :])], axis=2)
+    ch = np.concatenate([np.repeat(C, H // G, axis=3), np.zeros((b, T, R, H, N))], axis=2)
+    y2, f2 = oracle.ssd(xh, dA, bh, ch, th, h0)
+    res.append(("combined_injection_y", _maxerr(y, y2[:, :, :R]), 1e-10))
+    res.append(("combined_injection_final", _maxerr(f, f2), 1e-10))
+    ones, zeros = np.ones_like(gm), np.zeros_like(bt)
+    y3, f3 = oracle.ssd_trapezoidal(x, dA, B, C, ones, zeros, th, h0, px, pb, mutation=mutation)
+    y4, f4 = oracle.ssd(x, dA, B, C, th, h0)
+    res.append(("beta0_gamma1_is_plain", max(_maxerr(y3, y4), _maxerr(f3, f4)), 1e-12))
+    k = 8
+    sl = lambda a, lo, hi: None if a is None else a[:, lo:hi]
+    ya, fa = oracle.ssd_trapezoidal(sl(x, 0, k), sl(dA, 0, k), sl(B, 0, k), sl(C, 0, k),
+                                    sl(gm, 0, k), sl(bt, 0, k), sl(th, 0, k), h0, px, pb,
+                                    mutation=mutation)
+    yb, fb = oracle.ssd_trapezoidal(sl(x, k, T), sl(dA, k, T), sl(B, k, T), sl(C, k, T),
+                                    sl(gm, k, T), sl(bt, k, T), sl(th, k, T), fa,
+                                    x[:, k - 1], B[:, k - 1], mutation=mutation)
+    res.append(("stream_continuation",
+                max(_maxerr(np.concatenate([ya, yb], axis=1), y), _maxerr(fb, f)), 1e-12))
+    return res
+
+
+TRAP_PINS = [pin_trapezoidal_rule, pin_trapezoidal_absorbed_frame,
+             pin_trapezoidal_combined_injection]

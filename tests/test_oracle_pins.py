@@ -7,7 +7,8 @@ from oracle import chunked_ref
 from tests import pins
 
 
-@pytest.mark.parametrize("pin", pins.SSD_PINS + pins.SS_PINS, ids=lambda f: f.__name__)
+@pytest.mark.parametrize("pin", pins.SSD_PINS + pins.SS_PINS + pins.TRAP_PINS,
+                         ids=lambda f: f.__name__)
 def test_pin_holds(pin):
     for name, err, tol in pin(0):
         assert err <= tol, f"{name}: error {err:.3e} > {tol:.1e}"
@@ -17,6 +18,12 @@ def test_pin_holds(pin):
 def test_planted_ssd_mistake_is_caught(name, code):
     failed = [n for pin in pins.SSD_PINS for (n, err, tol) in pin(code) if not err <= tol]
     assert failed, f"planted mistake '{name}' passed every SSD pin"
+
+
+@pytest.mark.parametrize("name,code", sorted(oracle.MUTATIONS_TRAP.items()))
+def test_planted_trapezoidal_mistake_is_caught(name, code):
+    failed = [n for pin in pins.TRAP_PINS for (n, err, tol) in pin(code) if not err <= tol]
+    assert failed, f"planted mistake '{name}' passed every trapezoidal pin"
 
 
 @pytest.mark.parametrize("name,code", sorted(oracle.MUTATIONS_SS.items()))
