@@ -78,6 +78,8 @@ def workload(name):
             return c
     if name == wl.SELECTIVE_SCAN_F32.name:
         return wl.SELECTIVE_SCAN_F32
+    if name == wl.TRAP_MIMO_ROT_F32.name:
+        return wl.TRAP_MIMO_ROT_F32
     raise SystemExit(f"unknown workload {name}")
 
 
@@ -201,6 +203,26 @@ def run_ours(args, rank, world, local):
         dtype = "f32"
         io_bytes = cfg.io_bytes()
         flops = 0
+    elif cfg.trapezoidal:
+        host = wl.make_trap_inputs(cfg, seed=0)
+        d = {k: (v.to(dev) if v is not None else None) for k, v in host.items()}
+        y = torch.empty_like(d["x"])
+        fin = torch.empty((cfg.batch, cfg.nheads, cfg.headdim, cfg.dstate), dtype=torch.float32,
+                          device=dev)
+        shape = pkg.shape_of(d["x"], d["B"], cfg.chunk_len, cfg.theta)
+        ws = torch.zeros(pkg.ssd_trapezoidal_workspace_bytes(shape), dtype=torch.uint8,
+                         device=dev)
+        fn = pkg.SSDTrapezoidalPlan(d["x"], d["dA"], d["B"], d["C"], d["gamma"], d["beta"],
+                                    chunk_len=cfg.chunk_len, theta=d["theta"],
+                                    prev_x=d["prev_x"], prev_B=d["prev_B"],
+                                    init_state=d["init_state"], y=y, final_state=fin,
+                                    workspace=ws, stream=stream)
+        variant = "trapezoidal"
+        # two expansion kernels, the chunk pipeline on 2R write channels, the output compaction
+        launches_per_call = 2 + 3 + (2 if cfg.theta else 0) + 1
+        dtype = cfg.dtype
+        io_bytes = cfg.io_bytes()
+        flops = cfg.with_(mimo_rank=2 * cfg.mimo_rank).causal_flops()
     else:
         host = wl.make_ssd_inputs(cfg, seed=0)
         d = {k: (v.to(dev) if v is not None else None) for k, v in host.items()}
@@ -292,6 +314,8 @@ def config_dict(cfg, is_ss):
              "nheads": cfg.nheads, "headdim": cfg.headdim, "dstate": cfg.dstate,
              "chunk_len": cfg.chunk_len, "mimo_rank": cfg.mimo_rank, "ngroups": cfg.ngroups,
              "io_dtype": cfg.dtype, "theta": cfg.theta}
+        if cfg.trapezoidal:
+            c["trapezoidal"] = True
     c["l2"] = "flushed between timed steps (256 MiB write, outside the timed events)"
     c["cuda_graph"] = False
     return c
@@ -320,13 +344,25 @@ def e2e_measure(args, cfg, is_ss, host, dev, stream):
         outs = [(y, torch.empty(y.shape, dtype=y.dtype).pin_memory()),
                 (fin, torch.empty(fin.shape, dtype=fin.dtype).pin_memory())]
         shape = pkg.shape_of(dbuf["x"], dbuf["B"], cfg.chunk_len, cfg.theta)
-        ws = torch.zeros(pkg.ssd_chunked_workspace_bytes(shape), dtype=torch.uint8, device=dev)
+        if cfg.trapezoidal:
+            ws = torch.zeros(pkg.ssd_trapezoidal_workspace_bytes(shape), dtype=torch.uint8,
+                             device=dev)
 
-        def call():
-            pkg.ssd_chunked_forward(dbuf["x"], dbuf["dA"], dbuf["B"], dbuf["C"],
-                                    chunk_len=cfg.chunk_len, theta=dbuf["theta"],
-                                    init_state=dbuf["init_state"], y=y, final_state=fin,
-                                    workspace=ws)
+            def call():
+                pkg.ssd_trapezoidal_forward(dbuf["x"], dbuf["dA"], dbuf["B"], dbuf["C"],
+                                            dbuf["gamma"], dbuf["beta"], chunk_len=cfg.chunk_len,
+                                            theta=dbuf["theta"], prev_x=dbuf["prev_x"],
+                                            prev_B=dbuf["prev_B"], init_state=dbuf["init_state"],
+                                            y=y, final_state=fin, workspace=ws)
+        else:
+            ws = torch.zeros(pkg.ssd_chunked_workspace_bytes(shape), dtype=torch.uint8,
+                             device=dev)
+
+            def call():
+                pkg.ssd_chunked_forward(dbuf["x"], dbuf["dA"], dbuf["B"], dbuf["C"],
+                                        chunk_len=cfg.chunk_len, theta=dbuf["theta"],
+                                        init_state=dbuf["init_state"], y=y, final_state=fin,
+                                        workspace=ws)
 
     h2d = sum(v.numel() * v.element_size() for v in pin.values() if v is not None)
     d2h = sum(o.numel() * o.element_size() for o, _ in outs)
@@ -378,6 +414,10 @@ def _ssd_sample(cfg, host, heads, batches=1):
         "theta": None if a["theta"] is None else a["theta"][:nb, :, :heads],
         "init_state": None if a["init_state"] is None else a["init_state"][:nb, :heads],
     }
+    if "gamma" in a:   # trapezoidal form
+        sub["gamma"], sub["beta"] = a["gamma"][:nb, :, :heads], a["beta"][:nb, :, :heads]
+        sub["prev_x"] = None if a["prev_x"] is None else a["prev_x"][:nb, :, :heads]
+        sub["prev_B"] = None if a["prev_B"] is None else a["prev_B"][:nb, :, :groups]
     sub = {k: (None if v is None else np.ascontiguousarray(v)) for k, v in sub.items()}
     return sub, heads
 
@@ -386,8 +426,13 @@ def _time_oracle_ssd(sub, nthr):
     import oracle
 
     t0 = time.perf_counter()
-    oracle.ssd(sub["x"], sub["dA"], sub["B"], sub["C"], sub["theta"], sub["init_state"],
-               nthreads=nthr)
+    if "gamma" in sub:
+        oracle.ssd_trapezoidal(sub["x"], sub["dA"], sub["B"], sub["C"], sub["gamma"],
+                               sub["beta"], sub["theta"], sub["init_state"], sub["prev_x"],
+                               sub["prev_B"], nthreads=nthr)
+    else:
+        oracle.ssd(sub["x"], sub["dA"], sub["B"], sub["C"], sub["theta"], sub["init_state"],
+                   nthreads=nthr)
     return time.perf_counter() - t0
 
 
@@ -455,7 +500,8 @@ def run_reference(args, rank, world):
     cfg = workload(args.workload)
     from chunked_ssd_scan_gb300 import workloads as wl
     is_ss = isinstance(cfg, wl.SelectiveScanConfig)
-    host = (wl.make_selective_scan_inputs(cfg, seed=0) if is_ss else wl.make_ssd_inputs(cfg, 0))
+    host = (wl.make_selective_scan_inputs(cfg, seed=0) if is_ss
+            else wl.make_trap_inputs(cfg, 0) if cfg.trapezoidal else wl.make_ssd_inputs(cfg, 0))
     per_step = max(0.5, min(20.0, 150.0 / max(1, args.steps + args.warmup)))
     step, frac, cores, desc = oracle_sampler(cfg, is_ss, host, per_step)
     for _ in range(args.warmup):

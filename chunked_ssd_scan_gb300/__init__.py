@@ -17,7 +17,9 @@ from . import workloads  # noqa: F401  (seeded synthetic inputs; no scan arithme
 
 __all__ = [
     "SSDError", "load_library", "ssd_shape", "ssd_chunked_workspace_bytes", "ssd_chunked_variant",
-    "ssd_chunked_launches", "ssd_chunked_forward", "SSDForwardPlan", "SelectiveScanPlan", "selective_scan_workspace_bytes", "selective_scan_forward",
+    "ssd_chunked_launches", "ssd_chunked_forward", "SSDForwardPlan", "SelectiveScanPlan",
+    "selective_scan_workspace_bytes", "selective_scan_forward", "ssd_trapezoidal_workspace_bytes",
+    "ssd_trapezoidal_forward", "SSDTrapezoidalPlan",
     "workspace_status", "wait_selftest", "STATUS", "VARIANTS",
 ]
 
@@ -68,6 +70,10 @@ def load_library(path: Optional[str] = None):
     lib.ssd_chunked_launches.argtypes = [SP]
     lib.ssd_chunked_forward.restype = ctypes.c_int
     lib.ssd_chunked_forward.argtypes = [SP] + [_VP] * 9 + [ctypes.c_size_t, _VP]
+    lib.ssd_trapezoidal_workspace_bytes.restype = ctypes.c_size_t
+    lib.ssd_trapezoidal_workspace_bytes.argtypes = [SP]
+    lib.ssd_trapezoidal_forward.restype = ctypes.c_int
+    lib.ssd_trapezoidal_forward.argtypes = [SP] + [_VP] * 13 + [ctypes.c_size_t, _VP]
     lib.selective_scan_workspace_bytes.restype = ctypes.c_size_t
     lib.selective_scan_workspace_bytes.argtypes = [_I64] * 4
     lib.selective_scan_forward.restype = ctypes.c_int
@@ -204,6 +210,81 @@ def ssd_chunked_forward(x: torch.Tensor, dA: torch.Tensor, B: torch.Tensor, C: t
     return SSDForwardPlan(x, dA, B, C, chunk_len=chunk_len, theta=theta, init_state=init_state,
                           y=y, final_state=final_state, return_final_state=return_final_state,
                           workspace=workspace, stream=stream)()
+
+
+def ssd_trapezoidal_workspace_bytes(shape: ssd_shape) -> int:
+    return int(load_library().ssd_trapezoidal_workspace_bytes(ctypes.byref(shape)))
+
+
+class SSDTrapezoidalPlan:
+    """Validated buffers for repeated ``ssd_trapezoidal_forward`` calls (C-ABI call only).
+
+    x [b,T,R,H,P], B/C [b,T,R,G,N] (f32 or bf16), dA, gamma, beta [b,T,H] f32,
+    theta [b,T,H,N/2] f32, prev_x [b,R,H,P] and prev_B [b,R,G,N] (x's dtype; the previous call's
+    last step, both or neither), init_state [b,H,P,N] f32.
+    """
+
+    def __init__(self, x, dA, B, C, gamma, beta, *, chunk_len: int, theta=None, prev_x=None,
+                 prev_B=None, init_state=None, y=None, final_state=None,
+                 return_final_state: bool = True, workspace=None, stream=None):
+        if x.dim() != 5 or B.dim() != 5:
+            raise ValueError("x must be [b,T,R,H,P] and B/C [b,T,R,G,N]")
+        b, T, R, H, P = x.shape
+        G, N = B.shape[3], B.shape[4]
+        _check_cuda("x", x)
+        if x.dtype not in (torch.float32, torch.bfloat16):
+            raise ValueError("x/B/C must be float32 or bfloat16")
+        _check_cuda("B", B, x.dtype, (b, T, R, G, N))
+        _check_cuda("C", C, x.dtype, (b, T, R, G, N))
+        for name, t in (("dA", dA), ("gamma", gamma), ("beta", beta)):
+            _check_cuda(name, t, torch.float32, (b, T, H))
+        if theta is not None:
+            _check_cuda("theta", theta, torch.float32, (b, T, H, N // 2))
+        if (prev_x is None) != (prev_B is None):
+            raise ValueError("prev_x and prev_B go together")
+        if prev_x is not None:
+            _check_cuda("prev_x", prev_x, x.dtype, (b, R, H, P))
+            _check_cuda("prev_B", prev_B, x.dtype, (b, R, G, N))
+        if init_state is not None:
+            _check_cuda("init_state", init_state, torch.float32, (b, H, P, N))
+        self.shape = shape_of(x, B, chunk_len, theta is not None)
+        self._lib = load_library()
+        if y is None:
+            y = torch.empty_like(x)
+        _check_cuda("y", y, x.dtype, x.shape)
+        if final_state is None and return_final_state:
+            final_state = torch.empty((b, H, P, N), dtype=torch.float32, device=x.device)
+        if final_state is not None:
+            _check_cuda("final_state", final_state, torch.float32, (b, H, P, N))
+        need = int(self._lib.ssd_trapezoidal_workspace_bytes(ctypes.byref(self.shape)))
+        if need == 0:
+            raise SSDError(2, "ssd_trapezoidal_workspace_bytes (shape not supported)")
+        if workspace is None:
+            workspace = torch.zeros(need, dtype=torch.uint8, device=x.device)   # zero header
+        _check_cuda("workspace", workspace, torch.uint8)
+        self.inputs = (x, dA, B, C, gamma, beta, theta, prev_x, prev_B, init_state)
+        self.y, self.final_state, self.workspace = y, final_state, workspace
+        self._args = (ctypes.byref(self.shape), _ptr(x), _ptr(dA), _ptr(B), _ptr(C), _ptr(gamma),
+                      _ptr(beta), _ptr(theta), _ptr(prev_x), _ptr(prev_B), _ptr(init_state),
+                      _ptr(y), _ptr(final_state), _ptr(workspace),
+                      ctypes.c_size_t(workspace.numel()), _stream_handle(stream))
+        self._fn = self._lib.ssd_trapezoidal_forward
+
+    def __call__(self):
+        st = self._fn(*self._args)
+        if st != 0:
+            raise SSDError(st, "ssd_trapezoidal_forward")
+        return self.y, self.final_state
+
+
+def ssd_trapezoidal_forward(x, dA, B, C, gamma, beta, *, chunk_len: int, theta=None,
+                            prev_x=None, prev_B=None, init_state=None, y=None, final_state=None,
+                            return_final_state: bool = True, workspace=None, stream=None):
+    """Trapezoidal Mamba-3 forward through ``ssd_trapezoidal_forward``; returns (y, final)."""
+    return SSDTrapezoidalPlan(x, dA, B, C, gamma, beta, chunk_len=chunk_len, theta=theta,
+                              prev_x=prev_x, prev_B=prev_B, init_state=init_state, y=y,
+                              final_state=final_state, return_final_state=return_final_state,
+                              workspace=workspace, stream=stream)()
 
 
 def selective_scan_workspace_bytes(batch, seqlen, d_model, d_state) -> int:

@@ -92,6 +92,49 @@ SsdLayout ssd_layout(const ssd_shape* s) {
 
 bool al16(const void* p) { return p == nullptr || aligned16(p); }
 
+// The trapezoidal form runs as this expanded problem: 2R fp32 write channels, B/C per head when
+// theta is given (the shifted channel is turned by each head's own angle).
+ssd_shape trap_expanded(const ssd_shape* s) {
+  ssd_shape e = *s;
+  e.mimo_rank = 2 * s->mimo_rank;
+  e.io_dtype = SSD_F32;
+  if (s->has_theta) e.ngroups = s->nheads;
+  return e;
+}
+
+struct TrapLayout {
+  SsdLayout inner;   // the generic pipeline's buffers (offsets from the workspace start)
+  size_t xh = 0, bh = 0, ch = 0, yh = 0, total = 0;
+};
+
+ssd_status check_trap_shape(const ssd_shape* s) {
+  ssd_status st = check_shape(s);
+  if (st != SSD_OK) return st;
+  if (s->mimo_rank > (int64_t(1) << 30)) return SSD_ERR_UNSUPPORTED;
+  const ssd_shape e = trap_expanded(s);
+  if ((st = check_shape(&e)) != SSD_OK) return st;
+  return pick_variant(&e) == SSD_VARIANT_GENERIC ? SSD_OK : SSD_ERR_UNSUPPORTED;
+}
+
+TrapLayout trap_layout(const ssd_shape* s) {
+  const ssd_shape e = trap_expanded(s);
+  TrapLayout L;
+  L.inner = ssd_layout(&e);
+  const size_t xs = sizeof(float) * (size_t)(e.batch * e.seqlen * e.mimo_rank * e.nheads * e.headdim);
+  const size_t bs = sizeof(float) * (size_t)(e.batch * e.seqlen * e.mimo_rank * e.ngroups * e.dstate);
+  size_t off = align_up(L.inner.total, kWsAlign);
+  L.xh = off;
+  off = align_up(off + xs, kWsAlign);
+  L.bh = off;
+  off = align_up(off + bs, kWsAlign);
+  L.ch = off;
+  off = align_up(off + bs, kWsAlign);
+  L.yh = off;
+  off = align_up(off + xs, kWsAlign);
+  L.total = off;
+  return L;
+}
+
 }  // namespace
 
 extern "C" {
@@ -165,6 +208,87 @@ ssd_status ssd_chunked_forward(const ssd_shape* shape, const void* x, const floa
     e = generic_forward(p, shape->io_dtype == SSD_BF16, static_cast<cudaStream_t>(stream));
   }
   return e == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
+}
+
+size_t ssd_trapezoidal_workspace_bytes(const ssd_shape* shape) {
+  if (check_trap_shape(shape) != SSD_OK) return 0;
+  return trap_layout(shape).total;
+}
+
+ssd_status ssd_trapezoidal_forward(const ssd_shape* shape, const void* x, const float* dA,
+                                   const void* B, const void* C, const float* gamma,
+                                   const float* beta, const float* theta, const void* prev_x,
+                                   const void* prev_B, const float* init_state, void* y,
+                                   float* final_state, void* workspace, size_t workspace_bytes,
+                                   void* stream) {
+  const ssd_status sc = check_trap_shape(shape);
+  if (sc != SSD_OK) return sc;
+  if (!x || !dA || !B || !C || !gamma || !beta || !y) return SSD_ERR_INVALID_ARG;
+  if ((shape->has_theta != 0) != (theta != nullptr)) return SSD_ERR_INVALID_ARG;
+  if ((prev_x == nullptr) != (prev_B == nullptr)) return SSD_ERR_INVALID_ARG;
+  if (!al16(x) || !al16(dA) || !al16(B) || !al16(C) || !al16(y) || !al16(theta) ||
+      !al16(gamma) || !al16(beta) || !al16(init_state) || !al16(final_state))
+    return SSD_ERR_INVALID_ARG;
+  const TrapLayout lay = trap_layout(shape);
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) % kWsAlign) != 0 ||
+      workspace_bytes < lay.total)
+    return SSD_ERR_WORKSPACE;
+  const ssd_shape e = trap_expanded(shape);
+  char* ws = static_cast<char*>(workspace);
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const bool bf16 = shape->io_dtype == SSD_BF16;
+
+  TrapArgs t;
+  memset(&t, 0, sizeof(t));
+  t.x = x;
+  t.B = B;
+  t.C = C;
+  t.prev_x = prev_x;
+  t.prev_B = prev_B;
+  t.gamma = gamma;
+  t.beta = beta;
+  t.theta = theta;
+  t.y = y;
+  t.xh = reinterpret_cast<float*>(ws + lay.xh);
+  t.bh = reinterpret_cast<float*>(ws + lay.bh);
+  t.ch = reinterpret_cast<float*>(ws + lay.ch);
+  t.yh = reinterpret_cast<float*>(ws + lay.yh);
+  t.batch = shape->batch;
+  t.T = shape->seqlen;
+  t.R = shape->mimo_rank;
+  t.H = shape->nheads;
+  t.G = shape->ngroups;
+  t.G2 = e.ngroups;
+  t.P = shape->headdim;
+  t.N = shape->dstate;
+  if (trap_expand(t, bf16, st) != cudaSuccess) return SSD_ERR_CUDA;
+
+  GenericParams p;
+  memset(&p, 0, sizeof(p));
+  p.x = t.xh;
+  p.dA = dA;
+  p.B = t.bh;
+  p.C = t.ch;
+  p.theta = theta;
+  p.init = init_state;
+  p.y = t.yh;
+  p.final_state = final_state;
+  p.batch = e.batch;
+  p.T = e.seqlen;
+  p.H = e.nheads;
+  p.P = e.headdim;
+  p.N = e.dstate;
+  p.G = e.ngroups;
+  p.R = e.mimo_rank;
+  p.l = e.chunk_len;
+  p.nch = (e.seqlen + p.l - 1) / p.l;
+  p.states = reinterpret_cast<float*>(ws + lay.inner.states);
+  p.cend = reinterpret_cast<float*>(ws + lay.inner.cend);
+  p.phi = theta ? reinterpret_cast<double*>(ws + lay.inner.phi) : nullptr;
+  p.phisum = theta ? reinterpret_cast<double*>(ws + lay.inner.phisum) : nullptr;
+  p.hdr = reinterpret_cast<WsHeader*>(ws);
+  if (generic_forward(p, false, st) != cudaSuccess) return SSD_ERR_CUDA;
+  return trap_compact(t, bf16, st) == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
 }
 
 size_t selective_scan_workspace_bytes(int64_t batch, int64_t seqlen, int64_t d_model,

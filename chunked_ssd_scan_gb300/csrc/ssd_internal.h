@@ -39,6 +39,17 @@ cudaError_t generic_state_pass(const GenericParams& p, cudaStream_t st);
 bool simt32_supported(int64_t P, int64_t N, int64_t R, int64_t l, bool bf16, bool theta);
 cudaError_t simt32_forward(const GenericParams& p, cudaStream_t st);
 
+// Trapezoidal form: the 2R-channel expansion around the generic pipeline.
+struct TrapArgs {
+  const void *x, *B, *C, *prev_x, *prev_B;   // I/O dtype
+  const float *gamma, *beta, *theta;
+  void* y;                                    // I/O dtype, R channels
+  float *xh, *bh, *ch, *yh;                   // workspace: the expanded problem (fp32, 2R channels)
+  int64_t batch, T, R, H, G, G2, P, N;        // G2: groups of the expanded B/C (H when theta)
+};
+cudaError_t trap_expand(const TrapArgs& a, bool bf16, cudaStream_t st);
+cudaError_t trap_compact(const TrapArgs& a, bool bf16, cudaStream_t st);
+
 // Selective scan.
 struct SelectiveScanParams {
   const float* u;

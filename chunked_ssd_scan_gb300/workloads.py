@@ -11,6 +11,11 @@ Recipe (one torch CPU ``Generator`` per call, seeded):
     dt = softplus(N(0,1) - 2)  [b,T,H];  A_h = -exp(U(0, ln 16))  [H];  dA = dt * A_h
     "slow decay" variant: dA = -U(0, 0.01)  (so the chunk-to-chunk state carry stays visible)
     theta ~ U(-0.1, 0.1)  [b,T,H,N/2];  init_state ~ N(0,1)  [b,H,P,N] when requested
+- Trapezoidal form (make_trap_inputs): the SSD draws above, then from a second generator
+  (seed + 104729) lam, s, prev_x, prev_B:
+    lam = sigmoid(N(0,1)), s = softplus(N(0,1) - 2)  [b,T,H];
+    gamma = lam * s;  beta = (1 - lam) * s * exp(dA)   (the generalised trapezoid's weights);
+    prev_x ~ N(0,1) * x_scale [b,R,H,P], prev_B ~ N(0,1) * bc_scale [b,R,G,N] when requested
 - Selective scan draw order u, delta, A, B, C, skip:
     u ~ N(0,1);  delta = softplus(N(0,1));  A = -U(0.5, 2)  [D,N];  B, C ~ N(0,1)  [b,T,N];
     skip ~ N(0,1)  [D]
@@ -39,6 +44,7 @@ class SSDConfig:
     theta: bool = False
     x_scale: float = 1.0
     bc_scale: float = 1.0
+    trapezoidal: bool = False   # the trapezoidal form (gamma, beta and the previous write)
 
     @property
     def torch_dtype(self) -> torch.dtype:
@@ -63,6 +69,9 @@ class SSDConfig:
         nbytes += b * H * P * N * 4                 # final state written
         if self.theta:
             nbytes += b * T * H * (N // 2) * 4      # theta read
+        if self.trapezoidal:
+            nbytes += 2 * b * T * H * 4             # gamma, beta read
+            nbytes += b * R * (H * P + G * N) * e   # previous write read
         return nbytes
 
     def causal_flops(self) -> int:
@@ -107,6 +116,9 @@ MAMBA3_MIMO_BF16 = SSDConfig("mamba3_mimo_bf16", 2, 8192, 32, 64, 128, 64, 4, 32
 LONG_ROT_F32 = SSDConfig("long_rotation_f32", 1, 131072, 24, 64, 64, 256, 1, 24, "f32",
                          theta=True)
 SELECTIVE_SCAN_F32 = SelectiveScanConfig("selective_scan_f32", 4, 4096, 512, 16)
+# Trapezoidal Mamba-3 (a measured shape of the trapezoidal row; not one of the five workloads).
+TRAP_MIMO_ROT_F32 = SSDConfig("mamba3_trapezoidal_f32", 1, 16384, 16, 64, 64, 64, 2, 16, "f32",
+                              theta=True, trapezoidal=True)
 
 SSD_CONFIGS = [TINY_SISO_F32, MAMBA2_SISO_BF16, MAMBA3_MIMO_BF16, LONG_ROT_F32]
 
@@ -145,6 +157,31 @@ def make_ssd_inputs(cfg: SSDConfig, seed: int = 0, *, slow_decay: bool = False,
         "theta": theta,
         "init_state": init,
     }
+    if device is not None:
+        out = {k: (v.to(device) if v is not None else None) for k, v in out.items()}
+    return out
+
+
+def make_trap_inputs(cfg: SSDConfig, seed: int = 0, *, slow_decay: bool = False,
+                     init_state: bool = False, prev: bool = True,
+                     device: Optional[str] = None) -> dict:
+    """make_ssd_inputs plus gamma, beta and (optionally) the previous step's x and B."""
+    out = make_ssd_inputs(cfg, seed, slow_decay=slow_decay, init_state=init_state)
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed + 104729)
+    b, T, R, H, P, N, G = (cfg.batch, cfg.seqlen, cfg.mimo_rank, cfg.nheads, cfg.headdim,
+                           cfg.dstate, cfg.ngroups)
+    f32 = torch.float32
+    lam = torch.sigmoid(torch.randn((b, T, H), generator=g, dtype=f32))
+    sc = torch.nn.functional.softplus(torch.randn((b, T, H), generator=g, dtype=f32) - 2.0)
+    out["gamma"] = (lam * sc).contiguous()
+    out["beta"] = ((1.0 - lam) * sc * torch.exp(out["dA"])).contiguous()
+    out["prev_x"] = out["prev_B"] = None
+    if prev:
+        out["prev_x"] = (torch.randn((b, R, H, P), generator=g, dtype=f32) * cfg.x_scale
+                         ).to(cfg.torch_dtype)
+        out["prev_B"] = (torch.randn((b, R, G, N), generator=g, dtype=f32) * cfg.bc_scale
+                         ).to(cfg.torch_dtype)
     if device is not None:
         out = {k: (v.to(device) if v is not None else None) for k, v in out.items()}
     return out

@@ -119,6 +119,34 @@ ssd_status ssd_chunked_forward(const ssd_shape* shape, const void* x, const floa
                                const float* init_state, void* y, float* final_state,
                                void* workspace, size_t workspace_bytes, void* stream);
 
+/* Bytes of device workspace ssd_trapezoidal_forward needs for `shape` (0 if unsupported). */
+size_t ssd_trapezoidal_workspace_bytes(const ssd_shape* shape);
+
+/*
+ * Trapezoidal Mamba-3 SSD forward (scan.py page, the trapezoidal forward; moments.rs page,
+ * combined injections).  Per (batch b, head h), g = h / (H/G), with the step write
+ * S_t = sum_r x[b,t,r,h,:] (outer) B[b,t,r,g,:]:
+ *   h_t = Rot(theta_t) (exp(dA[b,t,h]) h_{t-1} + beta[b,t,h] S_{t-1}) + gamma[b,t,h] S_t
+ *   y[b,t,r,h,:] = h_t . C[b,t,r,g,:];   final_state[b,h] = h_{T-1}
+ * i.e. the beta term carries the previous step's write, turned by one step less of the
+ * cumulative rotation than the gamma term.  S_{-1} = sum_r prev_x[b,r,h,:] (outer) prev_B[b,r,g,:]
+ * (the last step of the previous call, for streaming) or zero when prev_x and prev_B are NULL.
+ * h_{-1} = init_state (zeros if NULL); final_state may be NULL.
+ * Arguments: as ssd_chunked_forward, plus gamma and beta (device f32 [batch, seqlen, nheads]) and
+ * prev_x [batch, mimo_rank, nheads, headdim], prev_B [batch, mimo_rank, ngroups, dstate] (device,
+ * io_dtype; both or neither).  The shape is the caller's (R = mimo_rank output and write
+ * channels); the library runs it as one scalar-decay scan with 2R write channels
+ * (x^ = [gamma x_t, beta x_{t-1}], B^ = [B_t, Rot(theta_t) B_{t-1}]) built in fp32 in the
+ * workspace, on the CUDA-core chunk pipeline.  Errors, asynchrony and the workspace header as
+ * for ssd_chunked_forward; UNSUPPORTED when the expanded shape exceeds that pipeline's limits.
+ */
+ssd_status ssd_trapezoidal_forward(const ssd_shape* shape, const void* x, const float* dA,
+                                   const void* B, const void* C, const float* gamma,
+                                   const float* beta, const float* theta, const void* prev_x,
+                                   const void* prev_B, const float* init_state, void* y,
+                                   float* final_state, void* workspace, size_t workspace_bytes,
+                                   void* stream);
+
 /* Bytes of device workspace selective_scan_forward needs (0 if the sizes are invalid). */
 size_t selective_scan_workspace_bytes(int64_t batch, int64_t seqlen, int64_t d_model,
                                       int64_t d_state);

@@ -63,3 +63,22 @@ def slice_heads(inp: dict, cfg: wl.SSDConfig, b: int, h: int) -> dict:
         "init_state": (None if inp["init_state"] is None
                        else inp["init_state"][b:b + 1, h:h + 1].contiguous()),
     }
+
+
+def gpu_trap(inp: dict, chunk_len: int, dev: str = "cuda"):
+    """One trapezoidal forward through the C ABI, workspace error word checked."""
+    d = {k: (v.to(dev) if v is not None else None) for k, v in inp.items()}
+    plan = pkg.SSDTrapezoidalPlan(d["x"], d["dA"], d["B"], d["C"], d["gamma"], d["beta"],
+                                  chunk_len=chunk_len, theta=d["theta"], prev_x=d["prev_x"],
+                                  prev_B=d["prev_B"], init_state=d["init_state"])
+    y, fin = plan()
+    assert pkg.workspace_status(plan.workspace) == ("SSD_OK", 0)
+    torch.cuda.synchronize()
+    return to_np(y), to_np(fin)
+
+
+def oracle_trap(inp: dict):
+    return oracle.ssd_trapezoidal(to_np(inp["x"]), to_np(inp["dA"]), to_np(inp["B"]),
+                                  to_np(inp["C"]), to_np(inp["gamma"]), to_np(inp["beta"]),
+                                  to_np(inp["theta"]), to_np(inp["init_state"]),
+                                  to_np(inp["prev_x"]), to_np(inp["prev_B"]))
