@@ -298,6 +298,18 @@ __global__ void __launch_bounds__(kThreadsFused, 1)
         tma_load_4d_elect(smem + kOffC + s * kBCBytes + kBCBytes / 2, &tm_c, &bars->full[s], 64,
                           g, row, b);
       }
+      // Tile t+2 reuses this stage only after K3_t; pulling it into L2 now takes the DRAM
+      // latency out of that later load.
+      if (t + 2 < nt) {
+        const int r2 = row + 2 * kTileRows;
+        tma_prefetch_l2_4d_elect(&tm_x, 0, h, r2, b);
+        tma_prefetch_l2_4d_elect(&tm_b, 0, g, r2, b);
+        tma_prefetch_l2_4d_elect(&tm_b, 64, g, r2, b);
+        if (!kPre) {
+          tma_prefetch_l2_4d_elect(&tm_c, 0, g, r2, b);
+          tma_prefetch_l2_4d_elect(&tm_c, 64, g, r2, b);
+        }
+      }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer

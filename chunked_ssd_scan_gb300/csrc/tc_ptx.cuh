@@ -331,6 +331,17 @@ __device__ __forceinline__ void tma_load_4d_elect(void* dst, const CUtensorMap* 
       : "memory");
 }
 
+// Prefetch of a 4-D box into L2 (no shared memory, no barrier), by one elected lane.
+__device__ __forceinline__ void tma_prefetch_l2_4d_elect(const CUtensorMap* map, int32_t x,
+                                                         int32_t y, int32_t z, int32_t w) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];\n\t}" ::"l"(
+          reinterpret_cast<uint64_t>(map)),
+      "r"(x), "r"(y), "r"(z), "r"(w)
+      : "memory");
+}
+
 // 32 lanes x 32 bits, 32 consecutive columns per thread (no wait).
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
   uint32_t r[32];
