@@ -119,6 +119,17 @@ __device__ void chunk_angles64(const GenericParams& p, int64_t b, int64_t c, int
   __syncthreads();
 }
 
+// Owner of the 4 x 4 output block (rows 4 ty.., cols 4 tx..) of a 64 x 64 product: each warp
+// covers 4 consecutive ty by 8 consecutive tx, so per k its A reads are 64 contiguous bytes and
+// its B reads 128 contiguous bytes -- one shared-memory wavefront each (a 2 x 16 warp shape
+// needs three).
+__device__ __forceinline__ int tile_tx() {
+  return (threadIdx.x & 7) + 8 * ((threadIdx.x >> 5) & 1);
+}
+__device__ __forceinline__ int tile_ty() {
+  return ((threadIdx.x >> 3) & 3) + 4 * (threadIdx.x >> 6);
+}
+
 // acc[r][c] += sum_k At[k][4 ty + r] * Bt[k][4 tx + c] over k < 64 (both operands k-major,
 // 64 floats per k row).  With kSwzA the 16-byte chunks of At's row k are stored permuted
 // (chunk c at c ^ ((k >> 2) & 15)), the layout the masked operand is written in.
@@ -252,7 +263,7 @@ __global__ void __launch_bounds__(kSimtThreads) simt_state_kernel(GenericParams 
   for (int t = threadIdx.x; t < l; t += kSimtThreads)
     dec[t] = exp2f((cum_hi[l - 1] - cum_hi[t]) + (cum_lo[l - 1] - cum_lo[t]));
   __syncthreads();
-  const int tx = threadIdx.x % 16, ty = threadIdx.x / 16;   // output rows p = 4 ty.., cols n = 4 tx..
+  const int tx = tile_tx(), ty = tile_ty();   // output rows p = 4 ty.., cols n = 4 tx..
   float acc[4][4] = {};
   for (int j0 = 0; j0 < l; j0 += kT64) {
     stage_x64(p, b, c, h, j0, dec + j0, xs);
@@ -316,7 +327,7 @@ __global__ void __launch_bounds__(kSimtThreads) simt_scan_kernel(GenericParams p
     cp_async_wait_all();
     __syncthreads();
   }
-  const int tx = threadIdx.x % 16, ty = threadIdx.x / 16;   // rows i = 4 ty.., cols 4 tx..
+  const int tx = tile_tx(), ty = tile_ty();   // rows i = 4 ty.., cols 4 tx..
   const float* Csrc = static_cast<const float*>(p.C);
   const float* Bsrc = static_cast<const float*>(p.B);
   for (int i0 = 0; i0 < l; i0 += kT64) {
@@ -343,8 +354,9 @@ __global__ void __launch_bounds__(kSimtThreads) simt_scan_kernel(GenericParams p
           m[r] = sj <= si ? exp2f((cum_hi[si] - cum_hi[sj]) + (cum_lo[si] - cum_lo[sj])) * cb[r][jj]
                           : 0.f;
         }
-        // row 4 tx + jj, chunk ty permuted by the row: the 16 lanes of a half-warp write 16
-        // different chunks (conflict-free)
+        // row 4 tx + jj, chunk ty permuted by the row: per instruction the warp writes 8 rows
+        // (consecutive tx) and, in each, the chunks ty ^ tx of 4 consecutive ty, which hit every
+        // bank group once per four lanes (conflict-free)
         *reinterpret_cast<float4*>(bt + (4 * tx + jj) * kT64 + 4 * (ty ^ tx)) =
             make_float4(m[0], m[1], m[2], m[3]);
       }
