@@ -128,7 +128,7 @@ cudaError_t launch_nb(const SelectiveScanParams& p, cudaStream_t st) {
 // of kSsStages stages of kSsSteps steps (16-byte cp.async, zero-filled past the segment and D).
 // ------------------------------------------------------------------------------------------------
 constexpr int kSsWarps = 4;
-constexpr int kSsSteps = 64;
+constexpr int kSsSteps = 16;
 constexpr int kSsStages = 2;
 
 
