@@ -33,12 +33,16 @@ L2_FLUSH_BYTES = 256 << 20
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 
-# dram__bytes_read.sum + dram__bytes_write.sum per launch of the dominant kernel, from the ncu
-# capture summarised under profiles/ (None until captured for the current kernel).
 # dram__bytes_read.sum + dram__bytes_write.sum of one launch of the dominant kernel, from one
-# ncu capture of the same workload (the profiles/ summaries); writes still held in L2 when the
-# kernel ends are not counted.  Variants without a capture report null.
-NCU_TRAFFIC_BYTES = {"selective_scan": 72_165_888}
+# ncu capture of the same workload and the current kernel (profiles/dram_traffic.md); writes
+# still held in L2 when the kernel ends are not counted.  Workloads without a capture report
+# null.
+NCU_TRAFFIC_BYTES = {
+    "mamba2_siso_bf16": 77_707_008 + 21_843_200,           # ssd_fused_bf16_kernel<false>
+    "mamba3_mimo_bf16": 1_353_165_824 + 253_219_328,       # ssd_fused_bf16_kernel<false>
+    "long_rotation_f32": 3_937_626_368 + 788_668_672,      # simt_scan_kernel
+    "selective_scan_f32": 71_228_672 + 6_168_320,          # ss_onepass_kernel (output pass)
+}
 
 
 def parse_args():
@@ -261,8 +265,11 @@ def run_ours(args, rank, world, local):
     hbm, tf, peak_src = measured_peaks()
     achieved = io_bytes / (ms * 1e-3) / 1e9
     roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
-            "frac": round(achieved / hbm, 4), "traffic": NCU_TRAFFIC_BYTES.get(variant),
-            "peak_source": peak_src, "kernel": f"ssd_chunked_forward[{variant}]",
+            "frac": round(achieved / hbm, 4), "traffic": NCU_TRAFFIC_BYTES.get(cfg.name),
+            "peak_source": peak_src,
+            "kernel": ("selective_scan_forward" if is_ss
+                       else "ssd_trapezoidal_forward" if variant == "trapezoidal"
+                       else f"ssd_chunked_forward[{variant}]"),
             "algorithmic_bytes_per_launch": io_bytes}
     if flops:
         roof["tensor_tflops"] = round(flops / (ms * 1e-3) / 1e12, 2)
