@@ -116,8 +116,10 @@ cudaError_t launch_nb(const SelectiveScanParams& p, cudaStream_t st) {
 }
 
 // ------------------------------------------------------------------------------------------------
-// One-pass selective scan for d_state N = 4 * LPC in {8, 16, 32, 64} and d_model % 4 == 0.
-// A warp owns 32 / LPC channels d of one batch row; the LPC lanes of a channel each carry four
+// One-pass selective scan for d_state N = SPL * LPC in {8, 16, 32, 64} and d_model % 4 == 0
+// (SPL = 4 states per lane, 8 for N = 16, where fewer lanes per channel means fewer shared-
+// memory reads per channel-step: the output pass is bound by them).
+// A warp owns 32 / LPC channels d of one batch row; the LPC lanes of a channel each carry SPL
 // of its N states, so every exp(delta * A) is evaluated on the special-function unit (2^x with
 // A pre-scaled by log2 e) and only segment boundary states go to memory.  T is cut into
 // segments (at least 256 steps) so that enough warps exist: a state-only pass gives each
@@ -146,9 +148,12 @@ struct SsLayout {
 // SPL consecutive floats (8 or 16 bytes) from shared memory.
 template <int SPL>
 __device__ __forceinline__ void ld_states(const float* src, float (&v)[SPL]) {
-  if constexpr (SPL == 4) {
-    const float4 f = *reinterpret_cast<const float4*>(src);
-    v[0] = f.x; v[1] = f.y; v[2] = f.z; v[3] = f.w;
+  if constexpr (SPL % 4 == 0) {
+#pragma unroll
+    for (int q = 0; q < SPL / 4; ++q) {
+      const float4 f = *reinterpret_cast<const float4*>(src + 4 * q);
+      v[4 * q] = f.x; v[4 * q + 1] = f.y; v[4 * q + 2] = f.z; v[4 * q + 3] = f.w;
+    }
   } else {
     const float2 f = *reinterpret_cast<const float2*>(src);
     v[0] = f.x; v[1] = f.y;
@@ -386,7 +391,8 @@ int64_t ss_segment_length(int64_t) { return kSegLen; }
 bool selective_scan_onepass_supported(int64_t batch, int64_t D, int64_t N) {
   if (N != 8 && N != 16 && N != 32 && N != 64) return false;
   if (D % 4 != 0) return false;                      // 16-byte staging of delta / u rows
-  const int64_t cpb = 128 / N * kSsWarps;            // channels per block (4 states per lane)
+  const int64_t cpb = 128 / N * kSsWarps;   // channels per block at 4 states per lane (a lower
+                                            // bound: more blocks than any SPL launches)
   const int64_t blocks = batch * ((D + cpb - 1) / cpb);
   return blocks <= 0x7fffffffLL;
 }
@@ -394,7 +400,7 @@ bool selective_scan_onepass_supported(int64_t batch, int64_t D, int64_t N) {
 cudaError_t selective_scan_onepass_launch(const SelectiveScanParams& p, cudaStream_t st) {
   switch (p.N) {
     case 8: return launch_onepass<4, 2>(p, st);
-    case 16: return launch_onepass<4, 4>(p, st);
+    case 16: return launch_onepass<8, 2>(p, st);
     case 32: return launch_onepass<4, 8>(p, st);
     case 64: return launch_onepass<4, 16>(p, st);
     default: return cudaErrorInvalidValue;
