@@ -57,11 +57,11 @@ int32_t pick_variant(const ssd_shape* s) {
 }
 
 // Chunk length the kernels tile time by.  The decomposition is exact for any chunk length, so
-// this is a tiling choice: the register-tiled fp32 kernels use 64 (their quadratic work per row
-// grows with the chunk, the chunk-state traffic shrinks with it; 64 is the faster trade on
-// GB300), every other path the caller's chunk_len.
+// this is a tiling choice: the register-tiled fp32 kernels use 64 rank-fused rows, i.e. 64 / R
+// steps (their quadratic work per row grows with the chunk, the chunk-state traffic shrinks
+// with it; 64 rows is the faster trade on GB300), every other path the caller's chunk_len.
 int64_t kernel_chunk_len(const ssd_shape* s) {
-  return pick_variant(s) == SSD_VARIANT_TILED_F32 ? 64 : s->chunk_len;
+  return pick_variant(s) == SSD_VARIANT_TILED_F32 ? 64 / s->mimo_rank : s->chunk_len;
 }
 
 SsdLayout ssd_layout(const ssd_shape* s) {
@@ -113,7 +113,8 @@ ssd_status check_trap_shape(const ssd_shape* s) {
   if (s->mimo_rank > (int64_t(1) << 30)) return SSD_ERR_UNSUPPORTED;
   const ssd_shape e = trap_expanded(s);
   if ((st = check_shape(&e)) != SSD_OK) return st;
-  return pick_variant(&e) == SSD_VARIANT_GENERIC ? SSD_OK : SSD_ERR_UNSUPPORTED;
+  const int32_t v = pick_variant(&e);
+  return (v == SSD_VARIANT_GENERIC || v == SSD_VARIANT_TILED_F32) ? SSD_OK : SSD_ERR_UNSUPPORTED;
 }
 
 TrapLayout trap_layout(const ssd_shape* s) {
@@ -280,14 +281,16 @@ ssd_status ssd_trapezoidal_forward(const ssd_shape* shape, const void* x, const 
   p.N = e.dstate;
   p.G = e.ngroups;
   p.R = e.mimo_rank;
-  p.l = e.chunk_len;
+  p.l = kernel_chunk_len(&e);
   p.nch = (e.seqlen + p.l - 1) / p.l;
   p.states = reinterpret_cast<float*>(ws + lay.inner.states);
   p.cend = reinterpret_cast<float*>(ws + lay.inner.cend);
   p.phi = theta ? reinterpret_cast<double*>(ws + lay.inner.phi) : nullptr;
   p.phisum = theta ? reinterpret_cast<double*>(ws + lay.inner.phisum) : nullptr;
   p.hdr = reinterpret_cast<WsHeader*>(ws);
-  if (generic_forward(p, false, st) != cudaSuccess) return SSD_ERR_CUDA;
+  const cudaError_t ce = pick_variant(&e) == SSD_VARIANT_TILED_F32 ? simt32_forward(p, st)
+                                                                    : generic_forward(p, false, st);
+  if (ce != cudaSuccess) return SSD_ERR_CUDA;
   return trap_compact(t, bf16, st) == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
 }
 

@@ -1,4 +1,4 @@
-// Register-tiled CUDA-core chunked SSD forward for fp32 I/O with P = N = 64 and mimo_rank 1.
+// Register-tiled CUDA-core chunked SSD forward for fp32 I/O with P = N = 64 and R | 64.
 //
 // Same chunk decomposition as the generic path (the serial.rs page's K1..K5, with the rotation
 // absorbed into B and C as on the scan.py page):
@@ -7,6 +7,9 @@
 //   state_pass          : K4 across chunks (shared with the generic path)
 //   simt_scan_kernel    : K2 and K5 for one chunk, in 64-row tiles:
 //                         y_i = sum_{j <= i} exp(cum_i - cum_j) (C~_i . B~_j) x_j + exp(cum_i) C~_i . h_in
+// With MIMO rank R the rows are the rank-fused rows i = t R + r (the serial.rs page's K2
+// reshape), contiguous in memory, and a chunk is 64 / R steps = 64 rows; decays, angles and
+// the causal cut use the step i / R of a row.
 // Every contraction is a 64 x 64 x 64 block product from shared memory: each of the 256 threads
 // owns a 4 x 4 output block and reads two float4 per k (16 FMAs per 32 bytes of shared memory).
 // The tensor core is not used here on purpose: its fp32 accumulation truncates toward zero at
@@ -35,6 +38,9 @@ constexpr float kLog2e64 = 1.4426950408889634f;
 constexpr float kTwoPiHi64 = 6.28318548202514648f;        // float(2 pi)
 constexpr float kTwoPiLo64 = -1.7484556000744487e-07f;    // 2 pi - kTwoPiHi64
 constexpr int kTileFloats = kT64 * kT64;
+
+// log2 of the rank (a power of two dividing 64): row i belongs to step i >> rank_shift.
+__device__ __forceinline__ int rank_shift(const GenericParams& p) { return __ffs((int)p.R) - 1; }
 
 // Real steps of chunk c (the last chunk may be short).
 __device__ __forceinline__ int steps64(const GenericParams& p, int64_t c) {
@@ -163,20 +169,22 @@ __device__ void stage_bc64(const GenericParams& p, const float* __restrict__ src
                            int64_t c, int64_t g, int s0, const float* ang, float* dst,
                            bool transpose) {
   const int tid = threadIdx.x;
+  const int R = (int)p.R;
+  const int64_t row0 = (b * p.T + c * p.l) * R;   // fused row of the chunk's first step
+  const int nvr = steps64(p, c) * R;              // real rows of the chunk
   if (!transpose) {
     // row-major: the 16 lanes of a half-warp read and write one row (coalesced loads,
     // conflict-free shared stores)
     const int ch = tid & 15;
-    const int nv = steps64(p, c);
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
       const int row = (tid >> 4) + 16 * r;
       float4 f = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (s0 + row < nv)
-        f = __ldg(reinterpret_cast<const float4*>(
-                      src + ((b * p.T + c * p.l + s0 + row) * p.G + g) * kT64) + ch);
+      if (s0 + row < nvr)
+        f = __ldg(reinterpret_cast<const float4*>(src + ((row0 + s0 + row) * p.G + g) * kT64) +
+                  ch);
       if (p.theta) {
-        const float* ar = ang + (s0 + row) * kPairs64 + 2 * ch;
+        const float* ar = ang + ((s0 + row) >> rank_shift(p)) * kPairs64 + 2 * ch;
         float s, co;
         sincosf(ar[0], &s, &co);
         const float e0 = co * f.x + s * f.y, o0 = -s * f.x + co * f.y;
@@ -189,10 +197,10 @@ __device__ void stage_bc64(const GenericParams& p, const float* __restrict__ src
     return;
   }
   const int row = tid >> 2, q0 = (tid & 3) * 16;   // 4 threads per row, 16 values each
+  const bool real = s0 + row < nvr;
   const float4* s4 = reinterpret_cast<const float4*>(
-      src + ((b * p.T + c * p.l + s0 + row) * p.G + g) * kT64 + q0);
+      src + ((row0 + (real ? s0 + row : 0)) * p.G + g) * kT64 + q0);
   float v[16];
-  const bool real = s0 + row < steps64(p, c);
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
     const float4 f = real ? __ldg(s4 + q) : make_float4(0.f, 0.f, 0.f, 0.f);
@@ -202,7 +210,7 @@ __device__ void stage_bc64(const GenericParams& p, const float* __restrict__ src
     v[4 * q + 3] = f.w;
   }
   if (p.theta) {
-    const float* ar = ang + (s0 + row) * kPairs64 + q0 / 2;
+    const float* ar = ang + ((s0 + row) >> rank_shift(p)) * kPairs64 + q0 / 2;
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
       float s, co;
@@ -216,21 +224,24 @@ __device__ void stage_bc64(const GenericParams& p, const float* __restrict__ src
   for (int k = 0; k < 16; ++k) dst[(q0 + k) * kT64 + row] = v[k];
 }
 
-// Stages x rows (chunk steps s0 ..) into dst[row][p], each row scaled by scale[row] if given.
+// Stages 64 x rows (fused rows s0 .. of the chunk) into dst[row][p], each row scaled by
+// scale[step of the row] if given.
 __device__ void stage_x64(const GenericParams& p, int64_t b, int64_t c, int64_t h, int s0,
                           const float* scale, float* dst) {
   const int tid = threadIdx.x;
   const int ch = tid & 15;   // half-warps read and write whole rows
-  const int nv = steps64(p, c);
+  const int R = (int)p.R;
+  const int64_t row0 = (b * p.T + c * p.l) * R;
+  const int nvr = steps64(p, c) * R;
 #pragma unroll
   for (int r = 0; r < 4; ++r) {
     const int row = (tid >> 4) + 16 * r;
     float4 f = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (s0 + row < nv)
+    if (s0 + row < nvr)
       f = __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(p.x) +
-                                                ((b * p.T + c * p.l + s0 + row) * p.H + h) * kT64) +
+                                                ((row0 + s0 + row) * p.H + h) * kT64) +
                 ch);
-    const float w = scale ? scale[row] : 1.f;
+    const float w = scale ? scale[(s0 + row) >> rank_shift(p)] : 1.f;
     *reinterpret_cast<float4*>(dst + row * kT64 + 4 * ch) =
         make_float4(f.x * w, f.y * w, f.z * w, f.w * w);
   }
@@ -265,8 +276,8 @@ __global__ void __launch_bounds__(kSimtThreads) simt_state_kernel(GenericParams 
   __syncthreads();
   const int tx = tile_tx(), ty = tile_ty();   // output rows p = 4 ty.., cols n = 4 tx..
   float acc[4][4] = {};
-  for (int j0 = 0; j0 < l; j0 += kT64) {
-    stage_x64(p, b, c, h, j0, dec + j0, xs);
+  for (int j0 = 0; j0 < l * (int)p.R; j0 += kT64) {   // fused rows
+    stage_x64(p, b, c, h, j0, dec, xs);
     stage_bc64(p, static_cast<const float*>(p.B), b, c, g, j0, ang, bs, false);
     __syncthreads();
     block_product(xs, bs, ty, tx, acc);   // S[p][n] += sum_j X~[j][p] B~[j][n]
@@ -287,7 +298,7 @@ size_t simt_scan_smem(int64_t l, bool theta) {
   return sizeof(float) * (4 * kTileFloats + 2 * l + (theta ? l * kPairs64 : 0));
 }
 
-__global__ void __launch_bounds__(kSimtThreads) simt_scan_kernel(GenericParams p) {
+__global__ void __launch_bounds__(kSimtThreads, 3) simt_scan_kernel(GenericParams p) {
   extern __shared__ __align__(16) float sm64[];
   const int64_t c = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int64_t g = h / (p.H / p.G);
@@ -303,13 +314,13 @@ __global__ void __launch_bounds__(kSimtThreads) simt_scan_kernel(GenericParams p
   if (p.theta) issue_theta64(p, b, c, h, l, ang);
   {
     const float* xsrc = static_cast<const float*>(p.x);
-    const int nv = steps64(p, c);
+    const int nvr = steps64(p, c) * (int)p.R;
+    const int64_t row0 = (b * p.T + c * p.l) * p.R;
     for (int e = threadIdx.x; e < kTileFloats / 4; e += kSimtThreads) {
       const int row = e / (kT64 / 4), q = e % (kT64 / 4);
-      const bool real = row < nv;   // steps after the real ones are zero-filled
+      const bool real = row < nvr;   // rows after the real ones are zero-filled
       cp_async16(xs + row * kT64 + 4 * q,
-                 xsrc + ((b * p.T + c * p.l + (real ? row : 0)) * p.H + h) * kT64 + 4 * q,
-                 real ? 16 : 0);
+                 xsrc + ((row0 + (real ? row : 0)) * p.H + h) * kT64 + 4 * q, real ? 16 : 0);
     }
   }
   chunk_prefix64(p.dA + (b * p.T + c * p.l) * p.H + h, p.H, l, steps64(p, c), cum_hi, cum_lo,
@@ -330,7 +341,8 @@ __global__ void __launch_bounds__(kSimtThreads) simt_scan_kernel(GenericParams p
   const int tx = tile_tx(), ty = tile_ty();   // rows i = 4 ty.., cols 4 tx..
   const float* Csrc = static_cast<const float*>(p.C);
   const float* Bsrc = static_cast<const float*>(p.B);
-  for (int i0 = 0; i0 < l; i0 += kT64) {
+  const int R = (int)p.R, rs = rank_shift(p);
+  for (int i0 = 0; i0 < l * R; i0 += kT64) {   // fused rows
     stage_bc64(p, Csrc, b, c, g, i0, ang, ct, true);
     __syncthreads();
     float yo[4][4] = {};
@@ -346,12 +358,12 @@ __global__ void __launch_bounds__(kSimtThreads) simt_scan_kernel(GenericParams p
       // (L o CB)^T: causal cut before the exponential
 #pragma unroll
       for (int jj = 0; jj < 4; ++jj) {
-        const int sj = j0 + 4 * tx + jj;
+        const int tj = (j0 + 4 * tx + jj) >> rs;   // step of source row j
         float m[4];
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
-          const int si = i0 + 4 * ty + r;
-          m[r] = sj <= si ? exp2f((cum_hi[si] - cum_hi[sj]) + (cum_lo[si] - cum_lo[sj])) * cb[r][jj]
+          const int ti = (i0 + 4 * ty + r) >> rs;
+          m[r] = tj <= ti ? exp2f((cum_hi[ti] - cum_hi[tj]) + (cum_lo[ti] - cum_lo[tj])) * cb[r][jj]
                           : 0.f;
         }
         // row 4 tx + jj, chunk ty permuted by the row: per instruction the warp writes 8 rows
@@ -364,13 +376,15 @@ __global__ void __launch_bounds__(kSimtThreads) simt_scan_kernel(GenericParams p
       block_product<true>(bt, xs, ty, tx, yd);   // Yd[i][p] += sum_j M[i][j] x[j][p]
       __syncthreads();
     }
-    const int nv = steps64(p, c);
+    const int nvr = steps64(p, c) * R;
+    const int64_t row0 = (b * p.T + c * p.l) * R;
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
       const int si = i0 + 4 * ty + r;
-      if (si >= nv) continue;   // padding step of a short last chunk
-      const float sc = exp2f(cum_hi[si] + cum_lo[si]);   // exp(cum_i)
-      float* yrow = static_cast<float*>(p.y) + ((b * p.T + c * p.l + si) * p.H + h) * kT64;
+      if (si >= nvr) continue;   // padding row of a short last chunk
+      const int ti = si >> rs;
+      const float sc = exp2f(cum_hi[ti] + cum_lo[ti]);   // exp(cum of row i's step)
+      float* yrow = static_cast<float*>(p.y) + ((row0 + si) * p.H + h) * kT64;
       *reinterpret_cast<float4*>(yrow + 4 * tx) =
           make_float4(fmaf(sc, yo[r][0], yd[r][0]), fmaf(sc, yo[r][1], yd[r][1]),
                       fmaf(sc, yo[r][2], yd[r][2]), fmaf(sc, yo[r][3], yd[r][3]));
@@ -381,7 +395,7 @@ __global__ void __launch_bounds__(kSimtThreads) simt_scan_kernel(GenericParams p
 }  // namespace
 
 bool simt32_supported(int64_t P, int64_t N, int64_t R, int64_t l, bool bf16, bool theta) {
-  if (bf16 || P != kT64 || N != kT64 || R != 1) return false;
+  if (bf16 || P != kT64 || N != kT64 || R < 1 || R > kT64 || (kT64 % R) != 0) return false;
   if (l < kT64 || l > kMaxChunk64 || (l % kT64) != 0) return false;
   return simt_state_smem(l, theta) <= 227 * 1024 && simt_scan_smem(l, theta) <= 227 * 1024;
 }

@@ -74,6 +74,10 @@ EDGE = [
     # tiles per chunk with rotation and one group shared by three heads
     wl.SSDConfig("tiled_f32_l64_g2", 2, 512, 4, 64, 64, 64, 1, 2, "f32"),
     wl.SSDConfig("tiled_f32_l384_theta_shared", 1, 768, 3, 64, 64, 384, 1, 1, "f32", theta=True),
+    # register-tiled fp32 path with MIMO rank-fused rows (64 / R steps per chunk): rank 2 with
+    # rotation and a ragged tail; rank 4 with two groups
+    wl.SSDConfig("tiled_f32_mimo_r2_theta", 1, 200, 2, 64, 64, 64, 2, 1, "f32", theta=True),
+    wl.SSDConfig("tiled_f32_mimo_r4_groups", 2, 96, 4, 64, 64, 128, 4, 2, "f32"),
 ]
 
 
@@ -130,7 +134,7 @@ def test_per_sequence_valid_length_by_zero_padding(cfg):
 
 
 def test_f32_workloads_use_the_tiled_kernels():
-    for cfg in (wl.LONG_ROT_F32, EDGE[-1], EDGE[-2]):
+    for cfg in (wl.LONG_ROT_F32, EDGE[-1], EDGE[-2], EDGE[-3], EDGE[-4]):
         shape = pkg.make_shape(cfg.batch, cfg.seqlen, cfg.nheads, cfg.headdim, cfg.dstate,
                                cfg.ngroups, cfg.mimo_rank, cfg.chunk_len, cfg.dtype, cfg.theta)
         assert pkg.ssd_chunked_variant(shape) == "tiled_f32", cfg.name
@@ -148,7 +152,7 @@ def test_fused_launches_follow_the_segmentation():
 
 
 def test_bf16_workloads_use_the_fused_kernel():
-    for cfg in (wl.MAMBA2_SISO_BF16, wl.MAMBA3_MIMO_BF16, EDGE[-3], EDGE[-4], EDGE[-5], EDGE[-6]):
+    for cfg in (wl.MAMBA2_SISO_BF16, wl.MAMBA3_MIMO_BF16, EDGE[-5], EDGE[-6], EDGE[-7], EDGE[-8]):
         shape = pkg.make_shape(cfg.batch, cfg.seqlen, cfg.nheads, cfg.headdim, cfg.dstate,
                                cfg.ngroups, cfg.mimo_rank, cfg.chunk_len, cfg.dtype, cfg.theta)
         assert pkg.ssd_chunked_variant(shape) == "tc_bf16", cfg.name
