@@ -49,6 +49,8 @@ def _lib():
         lib = ctypes.CDLL(build())
         lib.oracle_ssd_ex.restype = ctypes.c_int
         lib.oracle_ssd_ex.argtypes = [_D] * 8 + [_I64] * 8 + [ctypes.c_int]
+        lib.oracle_ssd_rot_ex.restype = ctypes.c_int
+        lib.oracle_ssd_rot_ex.argtypes = [_D] * 8 + [_I64] * 8 + [ctypes.c_int, _I64, ctypes.c_int]
         lib.oracle_ssd_trap_ex.restype = ctypes.c_int
         lib.oracle_ssd_trap_ex.argtypes = [_D] * 12 + [_I64] * 8 + [ctypes.c_int]
         lib.oracle_selective_scan_ex.restype = ctypes.c_int
@@ -92,6 +94,27 @@ def ssd(x, dA, B, C, theta=None, init_state=None, nthreads=None, mutation: int =
                               nthreads or default_threads(), int(mutation))
     if rc != 0:
         raise ValueError(f"oracle_ssd rejected its arguments (code {rc})")
+    return y, fin
+
+
+def ssd_rotation_variant(x, dA, B, C, theta, init_state=None, rope_dim: int = 0,
+                         halves: bool = False, nthreads=None, mutation: int = 0):
+    """Sequential fp64 SSD recurrence whose rotation turns only the first rope_dim state dims
+    (0 = all), pairing (2k, 2k+1) or, with halves, (k, k + rope_dim/2); theta [b,T,H,rope_dim/2].
+    Returns (y, final_state)."""
+    x, dA, B, C, theta, init_state = (_f64(v) for v in (x, dA, B, C, theta, init_state))
+    b, T, R, H, P = x.shape
+    G, N = B.shape[3], B.shape[4]
+    rd = rope_dim or N
+    assert theta.shape == (b, T, H, rd // 2)
+    y = np.zeros((b, T, R, H, P), np.float64)
+    fin = np.zeros((b, H, P, N), np.float64)
+    rc = _lib().oracle_ssd_rot_ex(_ptr(x), _ptr(dA), _ptr(B), _ptr(C), _ptr(theta),
+                                  _ptr(init_state), _ptr(y), _ptr(fin), b, T, R, H, G, P, N,
+                                  int(rope_dim), int(bool(halves)), nthreads or default_threads(),
+                                  int(mutation))
+    if rc != 0:
+        raise ValueError(f"oracle_ssd_rot rejected its arguments (code {rc})")
     return y, fin
 
 
@@ -152,6 +175,10 @@ MUTATIONS_TRAP = {
     "no_beta": 9,
     "beta_turned_late": 10,
     "beta_on_current_write": 11,
+}
+MUTATIONS_ROT = {
+    "interleaved_instead_of_halves": 12,
+    "rope_on_last_dims": 13,
 }
 MUTATIONS_SS = {
     "no_skip": 7,

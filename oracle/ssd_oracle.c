@@ -26,6 +26,11 @@
  *         (a, b) -> (cos*a - sin*b, sin*a + cos*b).
  *     The oracle applies this rotation to the state directly at every step (the rotated
  *     recurrence itself), never the absorbed cumulative-angle form the GPU uses.
+ *   - Rotation variants (moments.rs page, RotationSeq::Angle { rope_dim, rotate_pairwise }; the
+ *     page names them without defining them, read plainly): only the first rope_dim state
+ *     dimensions turn, theta then has rope_dim/2 angles per step, and the pair k is either the
+ *     interleaved (2k, 2k+1) (rotate_pairwise, the default) or the split halves
+ *     (k, k + rope_dim/2).
  *
  *   Trapezoidal SSD (Mamba-3; scan.py page, the trapezoidal forward: the beta term carries the
  *   PREVIOUS step's write and is turned by one step less of rotation), per (b, h):
@@ -65,6 +70,9 @@ typedef struct {
   int64_t tid;
   /* trapezoidal form only (NULL gamma = the plain recurrence above) */
   const double *gamma, *beta, *prev_x, *prev_B;
+  /* rotation variant: rope_dim (0 = N) and halves (0 = interleaved pairs) */
+  int64_t rope_dim;
+  int halves;
 } ssd_job;
 
 /* Planted-mistake codes, used only by the oracle's own pin tests. */
@@ -81,7 +89,22 @@ enum {
   MUT_TRAP_NO_BETA = 9,    /* trapezoidal: drops the beta (previous-write) term */
   MUT_TRAP_BETA_TURNED_LATE = 10, /* trapezoidal: feeds beta*S_{t-1} after the turn */
   MUT_TRAP_BETA_CURRENT = 11,     /* trapezoidal: beta multiplies S_t, not S_{t-1} */
+  MUT_ROT_INTERLEAVED = 12,       /* rotation variant: ignores the split-halves pairing */
+  MUT_ROPE_LAST_DIMS = 13,        /* rotation variant: turns the last rope_dim dims */
 };
+
+/* The pair of state dimensions that angle k of the rotation variant turns. */
+static void rot_pair(const ssd_job* j, int64_t k, int64_t* d0, int64_t* d1) {
+  const int64_t rd = j->rope_dim > 0 ? j->rope_dim : j->N;
+  const int64_t off = (j->mutation == MUT_ROPE_LAST_DIMS) ? j->N - rd : 0;
+  if (j->halves && j->mutation != MUT_ROT_INTERLEAVED) {
+    *d0 = off + k;
+    *d1 = off + k + rd / 2;
+  } else {
+    *d0 = off + 2 * k;
+    *d1 = off + 2 * k + 1;
+  }
+}
 
 /* The trapezoidal recurrence for one (b, h); h and the two write buffers hold P*N doubles. */
 static void trap_one(const ssd_job* j, int64_t b, int64_t hh, double* h, double* sprev,
@@ -164,15 +187,18 @@ static void ssd_one(const ssd_job* j, int64_t b, int64_t hh, double* h) {
   for (int64_t t = 0; t < T; ++t) {
     const double a = (j->mutation == MUT_NO_DECAY) ? 1.0 : exp(j->dA[(b * T + t) * H + hh]);
     if (j->theta) {
-      const double* th = j->theta + ((b * T + t) * H + hh) * (N / 2);
-      for (int64_t k = 0; k < N / 2; ++k) {
+      const int64_t K = (j->rope_dim > 0 ? j->rope_dim : N) / 2;
+      const double* th = j->theta + ((b * T + t) * H + hh) * K;
+      for (int64_t k = 0; k < K; ++k) {
         const double ang = (j->mutation == MUT_ROT_SIGN) ? -th[k] : th[k];
         const double c = cos(ang), s = sin(ang);
+        int64_t d0, d1;
+        rot_pair(j, k, &d0, &d1);
         for (int64_t p = 0; p < P; ++p) {
           double* hp = h + p * N;
-          const double e = hp[2 * k], o = hp[2 * k + 1];
-          hp[2 * k] = c * e - s * o;
-          hp[2 * k + 1] = s * e + c * o;
+          const double e = hp[d0], o = hp[d1];
+          hp[d0] = c * e - s * o;
+          hp[d1] = s * e + c * o;
         }
       }
     }
@@ -243,11 +269,12 @@ static int run_ssd(const double* x, const double* dA, const double* B, const dou
                    const double* theta, const double* init_state, double* y, double* final_state,
                    int64_t batch, int64_t T, int64_t R, int64_t H, int64_t G, int64_t P, int64_t N,
                    int64_t nthreads, int mutation, const double* gamma, const double* beta,
-                   const double* prev_x, const double* prev_B) {
+                   const double* prev_x, const double* prev_B, int64_t rope_dim, int halves) {
   if (!x || !dA || !B || !C || !y) return -1;
   if (batch < 0 || T < 0 || R < 1 || H < 1 || G < 1 || P < 1 || N < 1) return -2;
   if (H % G != 0) return -3;
   if (theta && (N % 2 != 0)) return -4;
+  if (rope_dim < 0 || rope_dim > N || (rope_dim % 2) != 0) return -6;
   if (batch == 0 || T == 0) {
     if (final_state) {
       for (int64_t i = 0; i < batch * H * P * N; ++i)
@@ -267,7 +294,7 @@ static int run_ssd(const double* x, const double* dA, const double* B, const dou
   for (int64_t i = 0; i < nt; ++i) {
     ssd_job j = {x,  dA, B,    C,     theta,  init_state, y,      final_state, batch, T,
                  R,  H,  G,    P,     N,      mutation,   nt,     i,           gamma, beta,
-                 prev_x, prev_B};
+                 prev_x, prev_B, rope_dim, halves};
     jobs[i] = j;
   }
   for (int64_t i = 1; i < nt; ++i) pthread_create(&th[i], NULL, ssd_worker, &jobs[i]);
@@ -288,7 +315,18 @@ int oracle_ssd_ex(const double* x, const double* dA, const double* B, const doub
                   int64_t batch, int64_t T, int64_t R, int64_t H, int64_t G, int64_t P, int64_t N,
                   int64_t nthreads, int mutation) {
   return run_ssd(x, dA, B, C, theta, init_state, y, final_state, batch, T, R, H, G, P, N,
-                 nthreads, mutation, NULL, NULL, NULL, NULL);
+                 nthreads, mutation, NULL, NULL, NULL, NULL, 0, 0);
+}
+
+/* Rotation variants: theta [b,T,H,rope_dim/2] (rope_dim 0 = dstate); halves = 1 pairs the
+ * dimensions (k, k + rope_dim/2) instead of (2k, 2k+1). */
+int oracle_ssd_rot_ex(const double* x, const double* dA, const double* B, const double* C,
+                      const double* theta, const double* init_state, double* y,
+                      double* final_state, int64_t batch, int64_t T, int64_t R, int64_t H,
+                      int64_t G, int64_t P, int64_t N, int64_t rope_dim, int halves,
+                      int64_t nthreads, int mutation) {
+  return run_ssd(x, dA, B, C, theta, init_state, y, final_state, batch, T, R, H, G, P, N,
+                 nthreads, mutation, NULL, NULL, NULL, NULL, rope_dim, halves);
 }
 
 /* Trapezoidal form: gamma, beta [b,T,H]; prev_x [b,R,H,P] and prev_B [b,R,G,N] may be NULL
@@ -300,7 +338,7 @@ int oracle_ssd_trap_ex(const double* x, const double* dA, const double* B, const
                        int64_t H, int64_t G, int64_t P, int64_t N, int64_t nthreads, int mutation) {
   if (!gamma || !beta) return -1;
   return run_ssd(x, dA, B, C, theta, init_state, y, final_state, batch, T, R, H, G, P, N,
-                 nthreads, mutation, gamma, beta, prev_x, prev_B);
+                 nthreads, mutation, gamma, beta, prev_x, prev_B, 0, 0);
 }
 
 int oracle_ssd(const double* x, const double* dA, const double* B, const double* C,

@@ -337,3 +337,52 @@ def pin_trapezoidal_combined_injection(mutation=0):
 
 TRAP_PINS = [pin_trapezoidal_rule, pin_trapezoidal_absorbed_frame,
              pin_trapezoidal_combined_injection]
+
+
+# ------------------------------------------------------------------------- rotation variants
+def pin_rotation_variant_reductions(mutation=0):
+    """rope_dim = N with interleaved pairs is the plain rotated recurrence (exactly), and the
+    split-halves pairing is the interleaved one on a permuted state axis: with the state
+    dimensions reordered so that k -> 2k and k + N/2 -> 2k+1, B, C and the initial state
+    reordered alike, y is unchanged and the final state is the reordered one."""
+    res = []
+    x, dA, B, C, th, h0 = _problem(51, 2, 29, 2, 2, 1, 3, 8, theta=True, init=True)
+    y, f = oracle.ssd_rotation_variant(x, dA, B, C, th, h0, rope_dim=8, halves=False,
+                                       mutation=mutation)
+    y0, f0 = oracle.ssd(x, dA, B, C, th, h0)
+    res.append(("full_interleaved_is_plain", max(_maxerr(y, y0), _maxerr(f, f0)), 0.0))
+    N = 8
+    perm = np.empty(N, dtype=int)        # new position of old dimension d
+    perm[:N // 2] = 2 * np.arange(N // 2)
+    perm[N // 2:] = 2 * np.arange(N // 2) + 1
+    inv = np.argsort(perm)               # old dimension at new position
+    yh, fh = oracle.ssd_rotation_variant(x, dA, B, C, th, h0, rope_dim=8, halves=True,
+                                         mutation=mutation)
+    yp, fp = oracle.ssd(x, dA, B[..., inv], C[..., inv], th, h0[..., inv])
+    res.append(("halves_is_permuted_interleaved_y", _maxerr(yh, yp), 1e-12))
+    res.append(("halves_is_permuted_interleaved_final", _maxerr(fh[..., inv], fp), 1e-12))
+    return res
+
+
+def pin_rope_dim_superposition(mutation=0):
+    """With rope_dim < N the state splits into two independent blocks: the first rope_dim
+    dimensions turn, the rest follow the unrotated recurrence; y is the sum of the two blocks'
+    outputs (C . h splits over the state axis) -- for both pairings."""
+    res = []
+    Dr = 4
+    x, dA, B, C, th, h0 = _problem(53, 1, 31, 2, 2, 2, 3, 10, theta=False, init=True)
+    th = _rng(54).uniform(-0.4, 0.4, (1, 31, 2, Dr // 2))
+    for halves in (False, True):
+        y, f = oracle.ssd_rotation_variant(x, dA, B, C, th, h0, rope_dim=Dr, halves=halves,
+                                           mutation=mutation)
+        ya, fa = oracle.ssd_rotation_variant(x, dA, B[..., :Dr], C[..., :Dr], th,
+                                             h0[..., :Dr], rope_dim=Dr, halves=halves)
+        yb, fb = oracle.ssd(x, dA, B[..., Dr:], C[..., Dr:], None, h0[..., Dr:])
+        tag = "halves" if halves else "interleaved"
+        res.append((f"rope_{tag}_y", _maxerr(y, ya + yb), 1e-12))
+        res.append((f"rope_{tag}_final",
+                    _maxerr(f, np.concatenate([fa, fb], axis=-1)), 1e-12))
+    return res
+
+
+ROT_PINS = [pin_rotation_variant_reductions, pin_rope_dim_superposition]

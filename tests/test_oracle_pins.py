@@ -7,7 +7,7 @@ from oracle import chunked_ref
 from tests import pins
 
 
-@pytest.mark.parametrize("pin", pins.SSD_PINS + pins.SS_PINS + pins.TRAP_PINS,
+@pytest.mark.parametrize("pin", pins.SSD_PINS + pins.SS_PINS + pins.TRAP_PINS + pins.ROT_PINS,
                          ids=lambda f: f.__name__)
 def test_pin_holds(pin):
     for name, err, tol in pin(0):
@@ -24,6 +24,12 @@ def test_planted_ssd_mistake_is_caught(name, code):
 def test_planted_trapezoidal_mistake_is_caught(name, code):
     failed = [n for pin in pins.TRAP_PINS for (n, err, tol) in pin(code) if not err <= tol]
     assert failed, f"planted mistake '{name}' passed every trapezoidal pin"
+
+
+@pytest.mark.parametrize("name,code", sorted(oracle.MUTATIONS_ROT.items()))
+def test_planted_rotation_variant_mistake_is_caught(name, code):
+    failed = [n for pin in pins.ROT_PINS for (n, err, tol) in pin(code) if not err <= tol]
+    assert failed, f"planted mistake '{name}' passed every rotation-variant pin"
 
 
 @pytest.mark.parametrize("name,code", sorted(oracle.MUTATIONS_SS.items()))
