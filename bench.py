@@ -84,6 +84,8 @@ def workload(name):
         return wl.SELECTIVE_SCAN_F32
     if name == wl.TRAP_MIMO_ROT_F32.name:
         return wl.TRAP_MIMO_ROT_F32
+    if name == wl.ROT_VARIANT_F32.name:
+        return wl.ROT_VARIANT_F32
     raise SystemExit(f"unknown workload {name}")
 
 
@@ -227,6 +229,29 @@ def run_ours(args, rank, world, local):
         dtype = cfg.dtype
         io_bytes = cfg.io_bytes()
         flops = cfg.with_(mimo_rank=2 * cfg.mimo_rank).causal_flops()
+    elif cfg.rope_dim or cfg.halves:
+        import ctypes
+        host = wl.make_ssd_inputs(cfg, seed=0)
+        d = {k: (v.to(dev) if v is not None else None) for k, v in host.items()}
+        y = torch.empty_like(d["x"])
+        fin = torch.empty((cfg.batch, cfg.nheads, cfg.headdim, cfg.dstate), dtype=torch.float32,
+                          device=dev)
+        shape = pkg.shape_of(d["x"], d["B"], cfg.chunk_len, True)
+        ws = torch.zeros(pkg.load_library().ssd_rotation_variant_workspace_bytes(
+            ctypes.byref(shape), cfg.rope_dim, int(cfg.halves)), dtype=torch.uint8, device=dev)
+
+        def fn():
+            pkg.ssd_rotation_variant_forward(d["x"], d["dA"], d["B"], d["C"], d["theta"],
+                                             chunk_len=cfg.chunk_len, rope_dim=cfg.rope_dim,
+                                             halves=cfg.halves, init_state=d["init_state"], y=y,
+                                             final_state=fin, workspace=ws, stream=stream)
+        variant = "rotation_variant"
+        # B/C reorder (+ final-state reorder) for split halves, theta padding, the chunked call
+        launches_per_call = (pkg.ssd_chunked_launches(shape) + (2 if cfg.halves else 0)
+                             + (1 if cfg.rope_dim and cfg.rope_dim < cfg.dstate else 0))
+        dtype = cfg.dtype
+        io_bytes = cfg.io_bytes()
+        flops = cfg.causal_flops()
     else:
         host = wl.make_ssd_inputs(cfg, seed=0)
         d = {k: (v.to(dev) if v is not None else None) for k, v in host.items()}
@@ -269,6 +294,7 @@ def run_ours(args, rank, world, local):
             "peak_source": peak_src,
             "kernel": ("selective_scan_forward" if is_ss
                        else "ssd_trapezoidal_forward" if variant == "trapezoidal"
+                       else "ssd_rotation_variant_forward" if variant == "rotation_variant"
                        else f"ssd_chunked_forward[{variant}]"),
             "algorithmic_bytes_per_launch": io_bytes}
     if flops:
@@ -323,6 +349,8 @@ def config_dict(cfg, is_ss):
              "io_dtype": cfg.dtype, "theta": cfg.theta}
         if cfg.trapezoidal:
             c["trapezoidal"] = True
+        if cfg.rope_dim or cfg.halves:
+            c["rope_dim"], c["halves"] = cfg.rope_dim, cfg.halves
     c["l2"] = "flushed between timed steps (256 MiB write, outside the timed events)"
     c["cuda_graph"] = False
     return c
@@ -351,7 +379,20 @@ def e2e_measure(args, cfg, is_ss, host, dev, stream):
         outs = [(y, torch.empty(y.shape, dtype=y.dtype).pin_memory()),
                 (fin, torch.empty(fin.shape, dtype=fin.dtype).pin_memory())]
         shape = pkg.shape_of(dbuf["x"], dbuf["B"], cfg.chunk_len, cfg.theta)
-        if cfg.trapezoidal:
+        if cfg.rope_dim or cfg.halves:
+            import ctypes
+            shape = pkg.shape_of(dbuf["x"], dbuf["B"], cfg.chunk_len, True)
+            ws = torch.zeros(pkg.load_library().ssd_rotation_variant_workspace_bytes(
+                ctypes.byref(shape), cfg.rope_dim, int(cfg.halves)), dtype=torch.uint8,
+                device=dev)
+
+            def call():
+                pkg.ssd_rotation_variant_forward(dbuf["x"], dbuf["dA"], dbuf["B"], dbuf["C"],
+                                                 dbuf["theta"], chunk_len=cfg.chunk_len,
+                                                 rope_dim=cfg.rope_dim, halves=cfg.halves,
+                                                 init_state=dbuf["init_state"], y=y,
+                                                 final_state=fin, workspace=ws)
+        elif cfg.trapezoidal:
             ws = torch.zeros(pkg.ssd_trapezoidal_workspace_bytes(shape), dtype=torch.uint8,
                              device=dev)
 
@@ -421,11 +462,14 @@ def _ssd_sample(cfg, host, heads, batches=1):
         "theta": None if a["theta"] is None else a["theta"][:nb, :, :heads],
         "init_state": None if a["init_state"] is None else a["init_state"][:nb, :heads],
     }
+    if cfg.rope_dim or cfg.halves:
+        sub["rope_dim"], sub["halves"] = cfg.rope_dim, cfg.halves
     if "gamma" in a:   # trapezoidal form
         sub["gamma"], sub["beta"] = a["gamma"][:nb, :, :heads], a["beta"][:nb, :, :heads]
         sub["prev_x"] = None if a["prev_x"] is None else a["prev_x"][:nb, :, :heads]
         sub["prev_B"] = None if a["prev_B"] is None else a["prev_B"][:nb, :, :groups]
-    sub = {k: (None if v is None else np.ascontiguousarray(v)) for k, v in sub.items()}
+    sub = {k: (np.ascontiguousarray(v) if isinstance(v, np.ndarray) else v)
+           for k, v in sub.items()}
     return sub, heads
 
 
@@ -433,7 +477,11 @@ def _time_oracle_ssd(sub, nthr):
     import oracle
 
     t0 = time.perf_counter()
-    if "gamma" in sub:
+    if "rope_dim" in sub:
+        oracle.ssd_rotation_variant(sub["x"], sub["dA"], sub["B"], sub["C"], sub["theta"],
+                                    sub["init_state"], rope_dim=sub["rope_dim"],
+                                    halves=sub["halves"], nthreads=nthr)
+    elif "gamma" in sub:
         oracle.ssd_trapezoidal(sub["x"], sub["dA"], sub["B"], sub["C"], sub["gamma"],
                                sub["beta"], sub["theta"], sub["init_state"], sub["prev_x"],
                                sub["prev_B"], nthreads=nthr)

@@ -19,7 +19,7 @@ __all__ = [
     "SSDError", "load_library", "ssd_shape", "ssd_chunked_workspace_bytes", "ssd_chunked_variant",
     "ssd_chunked_launches", "ssd_chunked_forward", "SSDForwardPlan", "SelectiveScanPlan",
     "selective_scan_workspace_bytes", "selective_scan_forward", "ssd_trapezoidal_workspace_bytes",
-    "ssd_trapezoidal_forward", "SSDTrapezoidalPlan",
+    "ssd_trapezoidal_forward", "SSDTrapezoidalPlan", "ssd_rotation_variant_forward",
     "workspace_status", "wait_selftest", "STATUS", "VARIANTS",
 ]
 
@@ -74,6 +74,11 @@ def load_library(path: Optional[str] = None):
     lib.ssd_trapezoidal_workspace_bytes.argtypes = [SP]
     lib.ssd_trapezoidal_forward.restype = ctypes.c_int
     lib.ssd_trapezoidal_forward.argtypes = [SP] + [_VP] * 13 + [ctypes.c_size_t, _VP]
+    lib.ssd_rotation_variant_workspace_bytes.restype = ctypes.c_size_t
+    lib.ssd_rotation_variant_workspace_bytes.argtypes = [SP, _I64, ctypes.c_int32]
+    lib.ssd_rotation_variant_forward.restype = ctypes.c_int
+    lib.ssd_rotation_variant_forward.argtypes = ([SP, _I64, ctypes.c_int32] + [_VP] * 9
+                                                 + [ctypes.c_size_t, _VP])
     lib.selective_scan_workspace_bytes.restype = ctypes.c_size_t
     lib.selective_scan_workspace_bytes.argtypes = [_I64] * 4
     lib.selective_scan_forward.restype = ctypes.c_int
@@ -285,6 +290,47 @@ def ssd_trapezoidal_forward(x, dA, B, C, gamma, beta, *, chunk_len: int, theta=N
                               prev_x=prev_x, prev_B=prev_B, init_state=init_state, y=y,
                               final_state=final_state, return_final_state=return_final_state,
                               workspace=workspace, stream=stream)()
+
+
+def ssd_rotation_variant_forward(x, dA, B, C, theta, *, chunk_len: int, rope_dim: int = 0,
+                                 halves: bool = False, init_state=None, y=None,
+                                 final_state=None, return_final_state: bool = True,
+                                 workspace=None, stream=None):
+    """Rotated SSD forward with a partial rotation (the first rope_dim state dims, 0 = all) and
+    the interleaved (2k, 2k+1) or split-halves (k, k + rope_dim/2) pairing, through
+    ``ssd_rotation_variant_forward``.  theta [b,T,H,rope_dim/2] f32.  Returns (y, final)."""
+    if x.dim() != 5 or B.dim() != 5:
+        raise ValueError("x must be [b,T,R,H,P] and B/C [b,T,R,G,N]")
+    b, T, R, H, P = x.shape
+    G, N = B.shape[3], B.shape[4]
+    rd = rope_dim or N
+    _check_cuda("x", x)
+    _check_cuda("B", B, x.dtype, (b, T, R, G, N))
+    _check_cuda("C", C, x.dtype, (b, T, R, G, N))
+    _check_cuda("dA", dA, torch.float32, (b, T, H))
+    _check_cuda("theta", theta, torch.float32, (b, T, H, rd // 2))
+    if init_state is not None:
+        _check_cuda("init_state", init_state, torch.float32, (b, H, P, N))
+    shape = shape_of(x, B, chunk_len, True)
+    lib = load_library()
+    if y is None:
+        y = torch.empty_like(x)
+    if final_state is None and return_final_state:
+        final_state = torch.empty((b, H, P, N), dtype=torch.float32, device=x.device)
+    need = int(lib.ssd_rotation_variant_workspace_bytes(ctypes.byref(shape), int(rope_dim),
+                                                        int(bool(halves))))
+    if need == 0:
+        raise SSDError(2, "ssd_rotation_variant_workspace_bytes (shape not supported)")
+    if workspace is None:
+        workspace = torch.zeros(need, dtype=torch.uint8, device=x.device)
+    st = lib.ssd_rotation_variant_forward(ctypes.byref(shape), int(rope_dim), int(bool(halves)),
+                                          _ptr(x), _ptr(dA), _ptr(B), _ptr(C), _ptr(theta),
+                                          _ptr(init_state), _ptr(y), _ptr(final_state),
+                                          _ptr(workspace), ctypes.c_size_t(workspace.numel()),
+                                          _stream_handle(stream))
+    if st != 0:
+        raise SSDError(st, "ssd_rotation_variant_forward")
+    return y, final_state
 
 
 def selective_scan_workspace_bytes(batch, seqlen, d_model, d_state) -> int:

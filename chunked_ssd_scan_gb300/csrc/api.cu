@@ -138,6 +138,10 @@ TrapLayout trap_layout(const ssd_shape* s) {
 
 }  // namespace
 
+namespace ssd {
+ssd_status shape_status(const ssd_shape* s) { return check_shape(s); }
+}  // namespace ssd
+
 extern "C" {
 
 size_t ssd_chunked_workspace_bytes(const ssd_shape* shape) {

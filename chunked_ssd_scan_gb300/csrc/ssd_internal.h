@@ -5,6 +5,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include "../../include/ssdscan.h"
+
 namespace ssd {
 
 struct WsHeader;
@@ -38,6 +40,9 @@ cudaError_t generic_state_pass(const GenericParams& p, cudaStream_t st);
 // fp32 I/O with P = N = 64, mimo_rank 1, 64 | chunk_len <= 512: register-tiled CUDA-core kernels.
 bool simt32_supported(int64_t P, int64_t N, int64_t R, int64_t l, bool bf16, bool theta);
 cudaError_t simt32_forward(const GenericParams& p, cudaStream_t st);
+
+// Host-side validation of an SSD shape (the ssd_chunked_* rules).
+ssd_status shape_status(const ssd_shape* s);
 
 // Trapezoidal form: the 2R-channel expansion around the generic pipeline.
 struct TrapArgs {

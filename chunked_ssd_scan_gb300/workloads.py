@@ -45,6 +45,8 @@ class SSDConfig:
     x_scale: float = 1.0
     bc_scale: float = 1.0
     trapezoidal: bool = False   # the trapezoidal form (gamma, beta and the previous write)
+    rope_dim: int = 0           # rotation variant: rotated state dims (0 = all of dstate)
+    halves: bool = False        # rotation variant: split-halves pairing
 
     @property
     def torch_dtype(self) -> torch.dtype:
@@ -68,7 +70,7 @@ class SSDConfig:
         nbytes += b * T * H * 4                     # dA read
         nbytes += b * H * P * N * 4                 # final state written
         if self.theta:
-            nbytes += b * T * H * (N // 2) * 4      # theta read
+            nbytes += b * T * H * ((self.rope_dim or N) // 2) * 4   # theta read
         if self.trapezoidal:
             nbytes += 2 * b * T * H * 4             # gamma, beta read
             nbytes += b * R * (H * P + G * N) * e   # previous write read
@@ -116,6 +118,10 @@ MAMBA3_MIMO_BF16 = SSDConfig("mamba3_mimo_bf16", 2, 8192, 32, 64, 128, 64, 4, 32
 LONG_ROT_F32 = SSDConfig("long_rotation_f32", 1, 131072, 24, 64, 64, 256, 1, 24, "f32",
                          theta=True)
 SELECTIVE_SCAN_F32 = SelectiveScanConfig("selective_scan_f32", 4, 4096, 512, 16)
+# Rotation variant: config 3's shape at T = 32768 with half of the state rotated, split-halves
+# pairing (a measured shape of the rotation-variant row; not one of the five workloads).
+ROT_VARIANT_F32 = SSDConfig("rotation_halves_rope32_f32", 1, 32768, 24, 64, 64, 256, 1, 24,
+                            "f32", theta=True, rope_dim=32, halves=True)
 # Trapezoidal Mamba-3 (a measured shape of the trapezoidal row; not one of the five workloads).
 TRAP_MIMO_ROT_F32 = SSDConfig("mamba3_trapezoidal_f32", 1, 16384, 16, 64, 64, 64, 2, 16, "f32",
                               theta=True, trapezoidal=True)
@@ -147,7 +153,8 @@ def make_ssd_inputs(cfg: SSDConfig, seed: int = 0, *, slow_decay: bool = False,
         dA = dt * A_h
     theta = None
     if cfg.theta:
-        theta = (torch.rand((b, T, H, N // 2), generator=g, dtype=f32) * 0.2 - 0.1)
+        theta = (torch.rand((b, T, H, (cfg.rope_dim or N) // 2), generator=g, dtype=f32) * 0.2
+                 - 0.1)
     init = torch.randn((b, H, P, N), generator=g, dtype=f32) if init_state else None
     out = {
         "x": x.to(cfg.torch_dtype),

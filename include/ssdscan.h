@@ -147,6 +147,28 @@ ssd_status ssd_trapezoidal_forward(const ssd_shape* shape, const void* x, const 
                                    float* final_state, void* workspace, size_t workspace_bytes,
                                    void* stream);
 
+/* Bytes of device workspace ssd_rotation_variant_forward needs (0 if unsupported/invalid). */
+size_t ssd_rotation_variant_workspace_bytes(const ssd_shape* shape, int64_t rope_dim,
+                                            int32_t halves);
+
+/*
+ * Rotation variants of the rotated SSD forward (moments.rs page, RotationSeq::Angle with
+ * rope_dim and rotate_pairwise; the page names them without defining them, so the plain
+ * reading): the rotation turns only the first rope_dim state dimensions (0 = all of dstate;
+ * even, <= dstate), with theta [batch, seqlen, nheads, rope_dim/2], and angle k turns the pair
+ * (2k, 2k+1) when halves == 0 (rotate_pairwise, the ssd_chunked_forward convention) or
+ * (k, k + rope_dim/2) when halves == 1.  Dimensions past rope_dim follow the unrotated
+ * recurrence.  shape->has_theta must be 1.  Everything else (layouts, asynchrony, errors, the
+ * workspace header) as ssd_chunked_forward, which it runs after reordering the state axis of
+ * B, C and init_state in the workspace (halves only) and padding theta with zero angles
+ * (rope_dim < dstate only); final_state is reordered back.
+ */
+ssd_status ssd_rotation_variant_forward(const ssd_shape* shape, int64_t rope_dim,
+                                        int32_t halves, const void* x, const float* dA,
+                                        const void* B, const void* C, const float* theta,
+                                        const float* init_state, void* y, float* final_state,
+                                        void* workspace, size_t workspace_bytes, void* stream);
+
 /* Bytes of device workspace selective_scan_forward needs (0 if the sizes are invalid). */
 size_t selective_scan_workspace_bytes(int64_t batch, int64_t seqlen, int64_t d_model,
                                       int64_t d_state);
