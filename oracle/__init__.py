@@ -49,6 +49,8 @@ def _lib():
         lib = ctypes.CDLL(build())
         lib.oracle_ssd_ex.restype = ctypes.c_int
         lib.oracle_ssd_ex.argtypes = [_D] * 8 + [_I64] * 8 + [ctypes.c_int]
+        lib.oracle_ssd_backward_ex.restype = ctypes.c_int
+        lib.oracle_ssd_backward_ex.argtypes = [_D] * 12 + [_I64] * 8 + [ctypes.c_int]
         lib.oracle_ssd_rot_ex.restype = ctypes.c_int
         lib.oracle_ssd_rot_ex.argtypes = [_D] * 8 + [_I64] * 8 + [ctypes.c_int, _I64, ctypes.c_int]
         lib.oracle_ssd_trap_ex.restype = ctypes.c_int
@@ -95,6 +97,27 @@ def ssd(x, dA, B, C, theta=None, init_state=None, nthreads=None, mutation: int =
     if rc != 0:
         raise ValueError(f"oracle_ssd rejected its arguments (code {rc})")
     return y, fin
+
+
+def ssd_backward(x, dA, B, C, dy, init_state=None, dfinal=None, nthreads=None,
+                 mutation: int = 0):
+    """Reverse mode of the unrotated SSD recurrence for the loss <dy, y> + <dfinal, final>.
+    Returns dict dx [b,T,R,H,P], ddA [b,T,H], dB, dC [b,T,R,G,N], dinit [b,H,P,N]."""
+    x, dA, B, C, dy = (_f64(v) for v in (x, dA, B, C, dy))
+    init_state, dfinal = _f64(init_state), _f64(dfinal)
+    b, T, R, H, P = x.shape
+    G, N = B.shape[3], B.shape[4]
+    assert dy.shape == x.shape
+    out = {"dx": np.zeros_like(x), "ddA": np.zeros_like(dA), "dB": np.zeros_like(B),
+           "dC": np.zeros_like(C), "dinit": np.zeros((b, H, P, N))}
+    rc = _lib().oracle_ssd_backward_ex(_ptr(x), _ptr(dA), _ptr(B), _ptr(C), _ptr(init_state),
+                                       _ptr(dy), _ptr(dfinal), _ptr(out["dx"]), _ptr(out["ddA"]),
+                                       _ptr(out["dB"]), _ptr(out["dC"]), _ptr(out["dinit"]),
+                                       b, T, R, H, G, P, N, nthreads or default_threads(),
+                                       int(mutation))
+    if rc != 0:
+        raise ValueError(f"oracle_ssd_backward rejected its arguments (code {rc})")
+    return out
 
 
 def ssd_rotation_variant(x, dA, B, C, theta, init_state=None, rope_dim: int = 0,
@@ -179,6 +202,10 @@ MUTATIONS_TRAP = {
 MUTATIONS_ROT = {
     "interleaved_instead_of_halves": 12,
     "rope_on_last_dims": 13,
+}
+MUTATIONS_BWD = {
+    "dy_added_after_decay": 14,
+    "ddA_without_decay_factor": 15,
 }
 MUTATIONS_SS = {
     "no_skip": 7,

@@ -350,6 +350,199 @@ int oracle_ssd(const double* x, const double* dA, const double* B, const double*
 }
 
 /* ---------------------------------------------------------------------------------------- */
+/* Backward of the (unrotated) SSD recurrence                                                */
+/* ---------------------------------------------------------------------------------------- */
+/*
+ * Reverse mode of h_t = exp(dA_t) h_{t-1} + sum_r x_{t,r} (outer) B_{t,r}, y_{t,r} = C_{t,r} . h_t
+ * for the loss <dy, y> + <dfinal, h_{T-1}> (the backward the scan.py page asks a trainable scan
+ * to have), per (b, h), walking t from T-1 down with g = dL/dh_t:
+ *   g   += sum_r dy_{t,r} (outer) C_{t,r}            dC_{t,r} += h_t^T dy_{t,r}
+ *   dx_{t,r} = g B_{t,r}     dB_{t,r} += g^T x_{t,r}   ddA_t = exp(dA_t) <g, h_{t-1}>
+ *   g   <- exp(dA_t) g                                 dinit = g after t = 0.
+ * dB and dC sum over the heads of a group.  States are recomputed forward from checkpoints every
+ * kCkpt steps, so memory stays O((T / kCkpt + kCkpt) P N) per problem.
+ */
+enum { MUT_BWD_DY_AFTER_DECAY = 14, MUT_BWD_NO_DECAY_IN_DDA = 15 };
+
+typedef struct {
+  const double *x, *dA, *B, *C, *init, *dy, *dfinal;
+  double *dx, *ddA, *dB, *dC, *dinit;
+  int64_t batch, T, R, H, G, P, N;
+  int mutation;
+  int64_t nthreads, tid;
+  pthread_mutex_t* lock;   /* dB/dC are shared by the heads of a group */
+} bwd_job;
+
+#define ORACLE_CKPT 64
+
+static void bwd_one(const bwd_job* j, int64_t b, int64_t hh, double* ck, double* seg, double* g,
+                    double* dBl, double* dCl) {
+  const int64_t T = j->T, R = j->R, H = j->H, G = j->G, P = j->P, N = j->N, PN = P * N;
+  const int64_t g_ = hh / (H / G);
+  const int64_t nck = (T + ORACLE_CKPT - 1) / ORACLE_CKPT;
+  /* forward pass keeping the state entering every checkpoint segment */
+  double* h = seg;   /* scratch row 0 of seg as the running state */
+  if (j->init) {
+    memcpy(h, j->init + ((b * H + hh) * P) * N, sizeof(double) * PN);
+  } else {
+    memset(h, 0, sizeof(double) * PN);
+  }
+  for (int64_t t = 0; t < T; ++t) {
+    if (t % ORACLE_CKPT == 0) memcpy(ck + (t / ORACLE_CKPT) * PN, h, sizeof(double) * PN);
+    const double a = exp(j->dA[(b * T + t) * H + hh]);
+    for (int64_t p = 0; p < P; ++p)
+      for (int64_t n = 0; n < N; ++n) {
+        double w = 0.0;
+        for (int64_t r = 0; r < R; ++r)
+          w += j->x[(((b * T + t) * R + r) * H + hh) * P + p] *
+               j->B[(((b * T + t) * R + r) * G + g_) * N + n];
+        h[p * N + n] = a * h[p * N + n] + w;
+      }
+  }
+  if (j->dfinal) {
+    memcpy(g, j->dfinal + ((b * H + hh) * P) * N, sizeof(double) * PN);
+  } else {
+    memset(g, 0, sizeof(double) * PN);
+  }
+  memset(dBl, 0, sizeof(double) * T * R * N);
+  memset(dCl, 0, sizeof(double) * T * R * N);
+  for (int64_t c = nck - 1; c >= 0; --c) {
+    const int64_t t0 = c * ORACLE_CKPT, t1 = (t0 + ORACLE_CKPT < T) ? t0 + ORACLE_CKPT : T;
+    /* recompute the states h_{t0-1} .. h_{t1-1} into seg rows 0 .. (t1 - t0) */
+    memcpy(seg, ck + c * PN, sizeof(double) * PN);
+    for (int64_t t = t0; t < t1; ++t) {
+      const double a = exp(j->dA[(b * T + t) * H + hh]);
+      const double* hp = seg + (t - t0) * PN;
+      double* hn = seg + (t - t0 + 1) * PN;
+      for (int64_t p = 0; p < P; ++p)
+        for (int64_t n = 0; n < N; ++n) {
+          double w = 0.0;
+          for (int64_t r = 0; r < R; ++r)
+            w += j->x[(((b * T + t) * R + r) * H + hh) * P + p] *
+                 j->B[(((b * T + t) * R + r) * G + g_) * N + n];
+          hn[p * N + n] = a * hp[p * N + n] + w;
+        }
+    }
+    for (int64_t t = t1 - 1; t >= t0; --t) {
+      const double a = exp(j->dA[(b * T + t) * H + hh]);
+      const double* ht = seg + (t - t0 + 1) * PN;   /* h_t */
+      const double* hprev = seg + (t - t0) * PN;    /* h_{t-1} */
+      for (int64_t r = 0; r < R; ++r) {
+        const double* dyv = j->dy + (((b * T + t) * R + r) * H + hh) * P;
+        const double* cv = j->C + (((b * T + t) * R + r) * G + g_) * N;
+        for (int64_t n = 0; n < N; ++n) {
+          double s = 0.0;
+          for (int64_t p = 0; p < P; ++p) s += dyv[p] * ht[p * N + n];
+          dCl[(t * R + r) * N + n] += s;
+        }
+        if (j->mutation != MUT_BWD_DY_AFTER_DECAY)
+          for (int64_t p = 0; p < P; ++p)
+            for (int64_t n = 0; n < N; ++n) g[p * N + n] += dyv[p] * cv[n];
+      }
+      for (int64_t r = 0; r < R; ++r) {
+        const double* xv = j->x + (((b * T + t) * R + r) * H + hh) * P;
+        const double* bv = j->B + (((b * T + t) * R + r) * G + g_) * N;
+        for (int64_t p = 0; p < P; ++p) {
+          double s = 0.0;
+          for (int64_t n = 0; n < N; ++n) s += g[p * N + n] * bv[n];
+          j->dx[(((b * T + t) * R + r) * H + hh) * P + p] = s;
+        }
+        for (int64_t n = 0; n < N; ++n) {
+          double s = 0.0;
+          for (int64_t p = 0; p < P; ++p) s += g[p * N + n] * xv[p];
+          dBl[(t * R + r) * N + n] += s;
+        }
+      }
+      double da = 0.0;
+      for (int64_t e = 0; e < PN; ++e) da += g[e] * hprev[e];
+      j->ddA[(b * T + t) * H + hh] = (j->mutation == MUT_BWD_NO_DECAY_IN_DDA) ? da : a * da;
+      for (int64_t e = 0; e < PN; ++e) g[e] *= a;
+      if (j->mutation == MUT_BWD_DY_AFTER_DECAY) {   /* the planted mistake: dy lands late */
+        for (int64_t r = 0; r < R; ++r) {
+          const double* dyv = j->dy + (((b * T + t) * R + r) * H + hh) * P;
+          const double* cv = j->C + (((b * T + t) * R + r) * G + g_) * N;
+          for (int64_t p = 0; p < P; ++p)
+            for (int64_t n = 0; n < N; ++n) g[p * N + n] += dyv[p] * cv[n];
+        }
+      }
+    }
+  }
+  if (j->dinit) memcpy(j->dinit + ((b * H + hh) * P) * N, g, sizeof(double) * PN);
+  pthread_mutex_lock(j->lock);
+  for (int64_t t = 0; t < T; ++t)
+    for (int64_t r = 0; r < R; ++r)
+      for (int64_t n = 0; n < N; ++n) {
+        const int64_t o = (((b * T + t) * R + r) * G + g_) * N + n;
+        j->dB[o] += dBl[(t * R + r) * N + n];
+        j->dC[o] += dCl[(t * R + r) * N + n];
+      }
+  pthread_mutex_unlock(j->lock);
+}
+
+static void* bwd_worker(void* arg) {
+  const bwd_job* j = (const bwd_job*)arg;
+  const int64_t PN = j->P * j->N, nck = (j->T + ORACLE_CKPT - 1) / ORACLE_CKPT;
+  double* ck = (double*)malloc(sizeof(double) * PN * (size_t)nck);
+  double* seg = (double*)malloc(sizeof(double) * PN * (ORACLE_CKPT + 1));
+  double* g = (double*)malloc(sizeof(double) * PN);
+  double* dBl = (double*)malloc(sizeof(double) * j->T * j->R * j->N);
+  double* dCl = (double*)malloc(sizeof(double) * j->T * j->R * j->N);
+  void* rc = NULL;
+  if (!ck || !seg || !g || !dBl || !dCl) {
+    rc = (void*)1;
+  } else {
+    for (int64_t idx = j->tid; idx < j->batch * j->H; idx += j->nthreads)
+      bwd_one(j, idx / j->H, idx % j->H, ck, seg, g, dBl, dCl);
+  }
+  free(ck);
+  free(seg);
+  free(g);
+  free(dBl);
+  free(dCl);
+  return rc;
+}
+
+/* Backward of the unrotated SSD: dy [b,T,R,H,P] and dfinal [b,H,P,N] (nullable) in; dx, ddA,
+ * dB, dC (zeroed here) and dinit (nullable) out.  Returns 0 or a negative error. */
+int oracle_ssd_backward_ex(const double* x, const double* dA, const double* B, const double* C,
+                           const double* init_state, const double* dy, const double* dfinal,
+                           double* dx, double* ddA, double* dB, double* dC, double* dinit,
+                           int64_t batch, int64_t T, int64_t R, int64_t H, int64_t G, int64_t P,
+                           int64_t N, int64_t nthreads, int mutation) {
+  if (!x || !dA || !B || !C || !dy || !dx || !ddA || !dB || !dC) return -1;
+  if (batch < 1 || T < 1 || R < 1 || H < 1 || G < 1 || P < 1 || N < 1) return -2;
+  if (H % G != 0) return -3;
+  memset(dB, 0, sizeof(double) * (size_t)(batch * T * R * G * N));
+  memset(dC, 0, sizeof(double) * (size_t)(batch * T * R * G * N));
+  const int64_t nt = clamp_threads(nthreads, batch * H);
+  bwd_job* jobs = (bwd_job*)calloc((size_t)nt, sizeof(bwd_job));
+  pthread_t* th = (pthread_t*)calloc((size_t)nt, sizeof(pthread_t));
+  pthread_mutex_t lock;
+  if (!jobs || !th || pthread_mutex_init(&lock, NULL) != 0) {
+    free(jobs);
+    free(th);
+    return -5;
+  }
+  for (int64_t i = 0; i < nt; ++i) {
+    bwd_job jb = {x,  dA, B, C, init_state, dy, dfinal, dx,       ddA, dB, dC, dinit,
+                  batch, T, R, H, G, P, N, mutation, nt, i, &lock};
+    jobs[i] = jb;
+  }
+  int rc = 0;
+  for (int64_t i = 1; i < nt; ++i) pthread_create(&th[i], NULL, bwd_worker, &jobs[i]);
+  if (bwd_worker(&jobs[0]) != NULL) rc = -5;
+  for (int64_t i = 1; i < nt; ++i) {
+    void* ret = NULL;
+    pthread_join(th[i], &ret);
+    if (ret != NULL) rc = -5;
+  }
+  pthread_mutex_destroy(&lock);
+  free(jobs);
+  free(th);
+  return rc;
+}
+
+/* ---------------------------------------------------------------------------------------- */
 /* Selective scan                                                                            */
 /* ---------------------------------------------------------------------------------------- */
 
