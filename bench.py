@@ -32,6 +32,8 @@ METRIC = "SSD forward tokens/s and % of roofline (HBM GB/s / tensor-pipe) at 1 G
 L2_FLUSH_BYTES = 256 << 20
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
+# fp32 FMA peak of the CUDA cores: 152 SMs x 128 lanes x 2 FLOP x 2.07 GHz (maximum SM clock).
+ALU_FP32_TFLOPS = round(152 * 128 * 2 * 2.07e9 / 1e12, 1)
 
 # dram__bytes_read.sum + dram__bytes_write.sum of one launch of the dominant kernel, from one
 # ncu capture of the same workload and the current kernel (profiles/dram_traffic.md); writes
@@ -43,6 +45,14 @@ NCU_TRAFFIC_BYTES = {
     "long_rotation_f32": 3_937_626_368 + 788_668_672,      # simt_scan_kernel
     "selective_scan_f32": 71_228_672 + 6_168_320,          # ss_onepass_kernel (output pass)
 }
+
+
+def metric_name(cfg, is_ss):
+    if is_ss:
+        return "selective scan tokens/s at 1 GB300"
+    if getattr(cfg, "backward", False):
+        return "SSD backward tokens/s and % of roofline (fp32 CUDA-core FLOP/s) at 1 GB300"
+    return METRIC
 
 
 def parse_args():
@@ -86,6 +96,8 @@ def workload(name):
         return wl.TRAP_MIMO_ROT_F32
     if name == wl.ROT_VARIANT_F32.name:
         return wl.ROT_VARIANT_F32
+    if name == wl.MAMBA2_BWD_BF16.name:
+        return wl.MAMBA2_BWD_BF16
     raise SystemExit(f"unknown workload {name}")
 
 
@@ -209,6 +221,18 @@ def run_ours(args, rank, world, local):
         dtype = "f32"
         io_bytes = cfg.io_bytes()
         flops = 0
+    elif cfg.backward:
+        host = wl.make_bwd_inputs(cfg, seed=0)
+        d = {k: (v.to(dev) if v is not None else None) for k, v in host.items()}
+        fn = pkg.SSDBackwardPlan(d["x"], d["dA"], d["B"], d["C"], d["dy"],
+                                 init_state=d["init_state"], dfinal=d["dfinal"], stream=stream)
+        ws = fn.workspace
+        variant = "backward"
+        # chunk-state recompute (2), dL/dh_in per chunk, the reverse carry, the chunk gradients
+        launches_per_call = 5
+        dtype = cfg.dtype
+        io_bytes = cfg.io_bytes()
+        flops = cfg.backward_flops()
     elif cfg.trapezoidal:
         host = wl.make_trap_inputs(cfg, seed=0)
         d = {k: (v.to(dev) if v is not None else None) for k, v in host.items()}
@@ -293,18 +317,30 @@ def run_ours(args, rank, world, local):
             "frac": round(achieved / hbm, 4), "traffic": NCU_TRAFFIC_BYTES.get(cfg.name),
             "peak_source": peak_src,
             "kernel": ("selective_scan_forward" if is_ss
+                       else "ssd_chunked_backward" if variant == "backward"
                        else "ssd_trapezoidal_forward" if variant == "trapezoidal"
                        else "ssd_rotation_variant_forward" if variant == "rotation_variant"
                        else f"ssd_chunked_forward[{variant}]"),
             "algorithmic_bytes_per_launch": io_bytes}
-    if flops:
+    if variant == "backward":
+        # fp32 FMA work on CUDA cores: the bound is the SMs' fp32 lanes at the maximum clock
+        alu = ALU_FP32_TFLOPS
+        a_tf = flops / (ms * 1e-3) / 1e12
+        roof = {"bound": "alu", "achieved": round(a_tf, 2), "peak": alu, "unit": "TFLOP/s",
+                "frac": round(a_tf / alu, 4), "traffic": NCU_TRAFFIC_BYTES.get(cfg.name),
+                "peak_source": "derived: 152 SMs x 128 fp32 lanes x 2 FLOP x 2.07 GHz",
+                "kernel": "ssd_chunked_backward", "algorithmic_flops_per_launch": flops,
+                "algorithmic_bytes_per_launch": io_bytes,
+                "hbm_gbs": round(io_bytes / (ms * 1e-3) / 1e9, 1),
+                "hbm_frac": round(io_bytes / (ms * 1e-3) / 1e9 / hbm, 4)}
+    elif flops:
         roof["tensor_tflops"] = round(flops / (ms * 1e-3) / 1e12, 2)
         roof["tensor_frac_of_bf16_peak"] = round(flops / (ms * 1e-3) / 1e12 / tf, 4)
         t_roof = max(io_bytes / (hbm * 1e9), flops / (tf * 1e12))
         roof["roofline_frac"] = round(t_roof / (ms * 1e-3), 4)
 
     out = {
-        "metric": METRIC if not is_ss else "selective scan tokens/s at 1 GB300",
+        "metric": metric_name(cfg, is_ss),
         "value": round(tokens / (ms * 1e-3), 1),
         "unit": "tokens/s",
         "n_gpus": world,
@@ -351,6 +387,9 @@ def config_dict(cfg, is_ss):
             c["trapezoidal"] = True
         if cfg.rope_dim or cfg.halves:
             c["rope_dim"], c["halves"] = cfg.rope_dim, cfg.halves
+        if cfg.backward:
+            c["backward"] = True
+            c["chunk_len"] = max(1, 64 // cfg.mimo_rank)   # the backward tiles by 64 fused rows
     c["l2"] = "flushed between timed steps (256 MiB write, outside the timed events)"
     c["cuda_graph"] = False
     return c
@@ -372,6 +411,15 @@ def e2e_measure(args, cfg, is_ss, host, dev, stream):
         def call():
             pkg.selective_scan_forward(dbuf["u"], dbuf["delta"], dbuf["A"], dbuf["B"],
                                        dbuf["C"], dbuf["skip"], y=y)
+    elif cfg.backward:
+        plan = pkg.SSDBackwardPlan(dbuf["x"], dbuf["dA"], dbuf["B"], dbuf["C"], dbuf["dy"],
+                                   init_state=dbuf["init_state"], dfinal=dbuf["dfinal"])
+        ws = plan.workspace
+        outs = [(v, torch.empty(v.shape, dtype=v.dtype).pin_memory())
+                for v in plan.grads.values() if v is not None]
+
+        def call():
+            plan()
     else:
         y = torch.empty_like(dbuf["x"])
         fin = torch.empty((cfg.batch, cfg.nheads, cfg.headdim, cfg.dstate),
@@ -464,6 +512,8 @@ def _ssd_sample(cfg, host, heads, batches=1):
     }
     if cfg.rope_dim or cfg.halves:
         sub["rope_dim"], sub["halves"] = cfg.rope_dim, cfg.halves
+    if "dy" in a:   # backward
+        sub["dy"], sub["dfinal"] = a["dy"][:nb, :, :, :heads], a["dfinal"][:nb, :heads]
     if "gamma" in a:   # trapezoidal form
         sub["gamma"], sub["beta"] = a["gamma"][:nb, :, :heads], a["beta"][:nb, :, :heads]
         sub["prev_x"] = None if a["prev_x"] is None else a["prev_x"][:nb, :, :heads]
@@ -477,7 +527,10 @@ def _time_oracle_ssd(sub, nthr):
     import oracle
 
     t0 = time.perf_counter()
-    if "rope_dim" in sub:
+    if "dy" in sub:
+        oracle.ssd_backward(sub["x"], sub["dA"], sub["B"], sub["C"], sub["dy"],
+                            init_state=sub["init_state"], dfinal=sub["dfinal"], nthreads=nthr)
+    elif "rope_dim" in sub:
         oracle.ssd_rotation_variant(sub["x"], sub["dA"], sub["B"], sub["C"], sub["theta"],
                                     sub["init_state"], rope_dim=sub["rope_dim"],
                                     halves=sub["halves"], nthreads=nthr)
@@ -556,7 +609,8 @@ def run_reference(args, rank, world):
     from chunked_ssd_scan_gb300 import workloads as wl
     is_ss = isinstance(cfg, wl.SelectiveScanConfig)
     host = (wl.make_selective_scan_inputs(cfg, seed=0) if is_ss
-            else wl.make_trap_inputs(cfg, 0) if cfg.trapezoidal else wl.make_ssd_inputs(cfg, 0))
+            else wl.make_trap_inputs(cfg, 0) if cfg.trapezoidal
+            else wl.make_bwd_inputs(cfg, 0) if cfg.backward else wl.make_ssd_inputs(cfg, 0))
     per_step = max(0.5, min(20.0, 150.0 / max(1, args.steps + args.warmup)))
     step, frac, cores, desc = oracle_sampler(cfg, is_ss, host, per_step)
     for _ in range(args.warmup):
@@ -566,7 +620,7 @@ def run_reference(args, rank, world):
     val = round(cfg.tokens * frac / sec, 1)
     return {
         "impl": "reference",
-        "metric": METRIC if not is_ss else "selective scan tokens/s at 1 GB300",
+        "metric": metric_name(cfg, is_ss),
         "value": val, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(cfg.tokens / val * 1e3, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",

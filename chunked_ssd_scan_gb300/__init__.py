@@ -20,6 +20,7 @@ __all__ = [
     "ssd_chunked_launches", "ssd_chunked_forward", "SSDForwardPlan", "SelectiveScanPlan",
     "selective_scan_workspace_bytes", "selective_scan_forward", "ssd_trapezoidal_workspace_bytes",
     "ssd_trapezoidal_forward", "SSDTrapezoidalPlan", "ssd_rotation_variant_forward",
+    "ssd_backward_workspace_bytes", "ssd_chunked_backward", "SSDBackwardPlan",
     "workspace_status", "wait_selftest", "STATUS", "VARIANTS",
 ]
 
@@ -80,6 +81,10 @@ def load_library(path: Optional[str] = None):
     lib.ssd_rotation_variant_forward.argtypes = ([SP, _I64, ctypes.c_int32] + [_VP] * 9
                                                  + [ctypes.c_size_t, _VP])
     lib.selective_scan_workspace_bytes.restype = ctypes.c_size_t
+    lib.ssd_backward_workspace_bytes.restype = ctypes.c_size_t
+    lib.ssd_backward_workspace_bytes.argtypes = [SP]
+    lib.ssd_chunked_backward.restype = ctypes.c_int
+    lib.ssd_chunked_backward.argtypes = [SP] + [_VP] * 13 + [ctypes.c_size_t, _VP]
     lib.selective_scan_workspace_bytes.argtypes = [_I64] * 4
     lib.selective_scan_forward.restype = ctypes.c_int
     lib.selective_scan_forward.argtypes = [_VP] * 7 + [_I64] * 4 + [_VP, ctypes.c_size_t, _VP]
@@ -331,6 +336,78 @@ def ssd_rotation_variant_forward(x, dA, B, C, theta, *, chunk_len: int, rope_dim
     if st != 0:
         raise SSDError(st, "ssd_rotation_variant_forward")
     return y, final_state
+
+
+def ssd_backward_workspace_bytes(shape: ssd_shape) -> int:
+    return int(load_library().ssd_backward_workspace_bytes(ctypes.byref(shape)))
+
+
+class SSDBackwardPlan:
+    """Arguments of ``ssd_chunked_backward`` validated once, for repeated calls on the same
+    buffers (the gradients are allocated here unless given).  dy [b,T,R,H,P] and dfinal
+    [b,H,P,N] are f32; every gradient is f32.  Calling the plan makes only the C call and
+    returns the dict dx, ddA, dB, dC, dinit (None unless return_dinit)."""
+
+    def __init__(self, x: torch.Tensor, dA: torch.Tensor, B: torch.Tensor, C: torch.Tensor,
+                 dy: torch.Tensor, *, init_state: Optional[torch.Tensor] = None,
+                 dfinal: Optional[torch.Tensor] = None, return_dinit: bool = True,
+                 grads: Optional[dict] = None, workspace: Optional[torch.Tensor] = None,
+                 stream=None):
+        if x.dim() != 5 or B.dim() != 5:
+            raise ValueError("x must be [b,T,R,H,P] and B/C [b,T,R,G,N]")
+        b, T, R, H, P = x.shape
+        G, N = B.shape[3], B.shape[4]
+        _check_cuda("x", x)
+        if x.dtype not in (torch.float32, torch.bfloat16):
+            raise ValueError("x/B/C must be float32 or bfloat16")
+        _check_cuda("B", B, x.dtype, (b, T, R, G, N))
+        _check_cuda("C", C, x.dtype, (b, T, R, G, N))
+        _check_cuda("dA", dA, torch.float32, (b, T, H))
+        _check_cuda("dy", dy, torch.float32, (b, T, R, H, P))
+        if init_state is not None:
+            _check_cuda("init_state", init_state, torch.float32, (b, H, P, N))
+        if dfinal is not None:
+            _check_cuda("dfinal", dfinal, torch.float32, (b, H, P, N))
+        self.shape = shape_of(x, B, 64, False)
+        self._lib = load_library()
+        need = int(self._lib.ssd_backward_workspace_bytes(ctypes.byref(self.shape)))
+        if need == 0:
+            raise SSDError(2, "ssd_backward_workspace_bytes (shape not supported)")
+        if workspace is None:
+            workspace = torch.zeros(need, dtype=torch.uint8, device=x.device)   # zero header
+        _check_cuda("workspace", workspace, torch.uint8)
+        shapes = {"dx": (b, T, R, H, P), "ddA": (b, T, H), "dB": (b, T, R, G, N),
+                  "dC": (b, T, R, G, N), "dinit": (b, H, P, N)}
+        g = dict(grads or {})
+        for k, shp in shapes.items():
+            if k == "dinit" and not return_dinit:
+                g[k] = None
+                continue
+            if g.get(k) is None:
+                g[k] = torch.empty(shp, dtype=torch.float32, device=x.device)
+            _check_cuda(k, g[k], torch.float32, shp)
+        self.inputs = (x, dA, B, C, dy, init_state, dfinal)
+        self.grads, self.workspace = g, workspace
+        self._args = (ctypes.byref(self.shape), _ptr(x), _ptr(dA), _ptr(B), _ptr(C),
+                      _ptr(init_state), _ptr(dy), _ptr(dfinal), _ptr(g["dx"]), _ptr(g["ddA"]),
+                      _ptr(g["dB"]), _ptr(g["dC"]), _ptr(g["dinit"]), _ptr(workspace),
+                      ctypes.c_size_t(workspace.numel()), _stream_handle(stream))
+        self._fn = self._lib.ssd_chunked_backward
+
+    def __call__(self):
+        st = self._fn(*self._args)
+        if st != 0:
+            raise SSDError(st, "ssd_chunked_backward")
+        return self.grads
+
+
+def ssd_chunked_backward(x, dA, B, C, dy, *, init_state=None, dfinal=None,
+                         return_dinit: bool = True, grads=None, workspace=None, stream=None):
+    """Gradients of <dy, y> + <dfinal, final_state> for the unrotated SSD forward, through
+    ``ssd_chunked_backward``.  Returns a dict of f32 tensors dx, ddA, dB, dC and dinit."""
+    return SSDBackwardPlan(x, dA, B, C, dy, init_state=init_state, dfinal=dfinal,
+                           return_dinit=return_dinit, grads=grads, workspace=workspace,
+                           stream=stream)()
 
 
 def selective_scan_workspace_bytes(batch, seqlen, d_model, d_state) -> int:

@@ -47,6 +47,7 @@ class SSDConfig:
     trapezoidal: bool = False   # the trapezoidal form (gamma, beta and the previous write)
     rope_dim: int = 0           # rotation variant: rotated state dims (0 = all of dstate)
     halves: bool = False        # rotation variant: split-halves pairing
+    backward: bool = False      # the reverse mode (dy, dfinal in; dx, ddA, dB, dC, dinit out)
 
     @property
     def torch_dtype(self) -> torch.dtype:
@@ -65,6 +66,12 @@ class SSDConfig:
         e = 4 if self.dtype == "f32" else 2
         b, T, R, H, P, N, G = (self.batch, self.seqlen, self.mimo_rank, self.nheads, self.headdim,
                                self.dstate, self.ngroups)
+        if self.backward:   # inputs x, B, C, dA, dy, init, dfinal; f32 gradients out
+            nbytes = b * T * R * H * P * (e + 4 + 4)     # x, dy read, dx written
+            nbytes += b * T * R * G * N * (e + 4) * 2    # B, C read, dB, dC written
+            nbytes += b * T * H * 4 * 2                  # dA read, ddA written
+            nbytes += b * H * P * N * 4 * 3              # init, dfinal read, dinit written
+            return nbytes
         nbytes = b * T * R * H * P * e * 2          # x read, y written
         nbytes += b * T * R * G * N * e * 2         # B, C read
         nbytes += b * T * H * 4                     # dA read
@@ -88,6 +95,24 @@ class SSDConfig:
         state = 2 * P * N * L * b * nch * H                  # K3
         off = 2 * L * N * P * b * nch * H                    # K5 inter-chunk
         return cb + diag + state + off
+
+    def backward_flops(self) -> int:
+        """FLOPs of the chunked backward at 64 fused rows per chunk (64 / R steps), causal part
+        only: the chunk-state recompute and dL/dh_in contribution (2 P N L each), the pairwise
+        C.B (per group) and dy.x products, and dx, dB, dC (each a causal pairwise sum plus a
+        P x N state product per row)."""
+        b, T, R, H, P, N, G = (self.batch, self.seqlen, self.mimo_rank, self.nheads,
+                               self.headdim, self.dstate, self.ngroups)
+        l = max(1, 64 // R)
+        nch = -(-T // l)
+        L = l * R
+        pairs = R * R * l * (l + 1) // 2
+        per_head = (2 * 2 * P * N * L            # state recompute, D_c
+                    + 2 * pairs * P              # dy_i . x_j
+                    + 2 * pairs * P + 2 * L * N * P    # dx
+                    + 2 * pairs * N + 2 * L * P * N    # dB
+                    + 2 * pairs * N + 2 * L * P * N)   # dC
+        return b * nch * (H * per_head + G * 2 * pairs * N)
 
 
 @dataclasses.dataclass(frozen=True)
@@ -125,6 +150,10 @@ ROT_VARIANT_F32 = SSDConfig("rotation_halves_rope32_f32", 1, 32768, 24, 64, 64, 
 # Trapezoidal Mamba-3 (a measured shape of the trapezoidal row; not one of the five workloads).
 TRAP_MIMO_ROT_F32 = SSDConfig("mamba3_trapezoidal_f32", 1, 16384, 16, 64, 64, 64, 2, 16, "f32",
                               theta=True, trapezoidal=True)
+
+# Backward of the unrotated SSD on config 1's shape (a measured shape of the backward row).
+MAMBA2_BWD_BF16 = SSDConfig("mamba2_backward_bf16", 4, 4096, 32, 64, 128, 64, 1, 1, "bf16",
+                            backward=True)
 
 SSD_CONFIGS = [TINY_SISO_F32, MAMBA2_SISO_BF16, MAMBA3_MIMO_BF16, LONG_ROT_F32]
 
@@ -189,6 +218,20 @@ def make_trap_inputs(cfg: SSDConfig, seed: int = 0, *, slow_decay: bool = False,
                          ).to(cfg.torch_dtype)
         out["prev_B"] = (torch.randn((b, R, G, N), generator=g, dtype=f32) * cfg.bc_scale
                          ).to(cfg.torch_dtype)
+    if device is not None:
+        out = {k: (v.to(device) if v is not None else None) for k, v in out.items()}
+    return out
+
+
+def make_bwd_inputs(cfg: SSDConfig, seed: int = 0, *, device: Optional[str] = None) -> dict:
+    """A forward problem (with an initial state) plus the cotangents dy [b,T,R,H,P] and dfinal
+    [b,H,P,N] (standard normal f32, from a second generator) for the backward."""
+    out = make_ssd_inputs(cfg, seed, init_state=True)
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed + 7919)
+    b, T, R, H, P, N = cfg.batch, cfg.seqlen, cfg.mimo_rank, cfg.nheads, cfg.headdim, cfg.dstate
+    out["dy"] = torch.randn((b, T, R, H, P), generator=g, dtype=torch.float32)
+    out["dfinal"] = torch.randn((b, H, P, N), generator=g, dtype=torch.float32)
     if device is not None:
         out = {k: (v.to(device) if v is not None else None) for k, v in out.items()}
     return out

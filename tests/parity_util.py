@@ -51,6 +51,28 @@ def check_close(got, ref, tol, what):
     return float(err.max()), nrel
 
 
+def check_close_inner(got, ref, tol, what, axis=1):
+    """Gate for a gradient that is an inner product of two state-sized matrices per element
+    (ddA_t = exp(dA_t) <dL/dh_t, h_{t-1}>): its fp32 rounding scales with the size of the
+    summed terms, which is the size of the values along the time axis, not with |ref| of one
+    element (the inner product crosses zero).  |got - ref| <= tol (1 + |ref|) + tol / 10 * the
+    RMS of ref along `axis` (the same (batch, head) sequence)."""
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    assert got.shape == ref.shape, f"{what}: shape {got.shape} != {ref.shape}"
+    assert np.all(np.isfinite(got)), f"{what}: non-finite output"
+    rms = np.sqrt(np.mean(ref * ref, axis=axis, keepdims=True))
+    err = np.abs(got - ref)
+    bound = tol * (1.0 + np.abs(ref)) + 0.1 * tol * rms
+    bad = err > bound
+    if np.any(bad):
+        idx = np.unravel_index(np.argmax(err - bound), err.shape)
+        raise AssertionError(
+            f"{what}: {int(bad.sum())} of {bad.size} elements outside the gate: worst at {idx} "
+            f"got {got[idx]:.6g} ref {ref[idx]:.6g} bound {bound[idx]:.3g}")
+    return float(err.max())
+
+
 def slice_heads(inp: dict, cfg: wl.SSDConfig, b: int, h: int) -> dict:
     """The independent (batch b, head h) sub-problem, as a batch-1, one-head, one-group problem."""
     g = h // (cfg.nheads // cfg.ngroups)

@@ -38,7 +38,9 @@ def test_header_declares_the_abi():
     for expected in ("ssd_chunked_forward", "ssd_chunked_workspace_bytes", "ssd_chunked_variant",
                      "selective_scan_forward", "selective_scan_workspace_bytes",
                      "ssd_workspace_status", "ssd_status_string", "ssd_abi_version",
-                     "ssd_trapezoidal_forward", "ssd_trapezoidal_workspace_bytes"):
+                     "ssd_trapezoidal_forward", "ssd_trapezoidal_workspace_bytes",
+                     "ssd_rotation_variant_forward", "ssd_rotation_variant_workspace_bytes",
+                     "ssd_chunked_backward", "ssd_backward_workspace_bytes"):
         assert expected in names
 
 
