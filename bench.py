@@ -228,8 +228,8 @@ def run_ours(args, rank, world, local):
                                  init_state=d["init_state"], dfinal=d["dfinal"], stream=stream)
         ws = fn.workspace
         variant = "backward"
-        # chunk-state recompute (2), dL/dh_in per chunk, the reverse carry, the chunk gradients
-        launches_per_call = 5
+        # chunk products (S_c, D_c), the two-way carry across chunks, the chunk gradients
+        launches_per_call = 3
         dtype = cfg.dtype
         io_bytes = cfg.io_bytes()
         flops = cfg.backward_flops()

@@ -1,21 +1,22 @@
 // Backward of the chunked SSD forward (unrotated; CUDA-core fp32), recompute per chunk.
 //
 // The scan.py page asks for a scan that can train; the moments.rs page's memory model keeps only
-// the chunk-boundary states and recomputes inside a chunk.  Here:
-//   1. generic_states: the forward chunk-input states h_in(c) (K1, K3, K4; no y), 64 fused rows
-//      per chunk;
-//   2. bwd_dstate_kernel: per chunk D_c = sum_i exp(cum_i) dy_i (outer) C_i, the part of
-//      dL/dh_in(c) that the chunk's own outputs contribute;
-//   3. bwd_state_pass_kernel: the reverse of K4 across chunks, G_c = dL/dh_out(c) = dL/dh_in(c+1),
-//      G_{nch-1} = dfinal, dL/dh_in(c) = exp(cum_end(c)) G_c + D_c, dinit = dL/dh_in(0);
-//   4. bwd_chunk_grad_kernel: per chunk, with L_ij = exp(cum_i - cum_j) below the step diagonal,
+// the chunk-boundary states and recomputes inside a chunk.  Three launches:
+//   1. bwd_chunk_state_kernel: per chunk both rank-Lr products, the chunk's own end state
+//      S_c = sum_i exp(cum_end - cum_i) x_i (outer) B_i and D_c = sum_i exp(cum_i) dy_i (outer) C_i,
+//      the part of dL/dh_in(c) that the chunk's own outputs contribute;
+//   2. bwd_carry_kernel: the carry across chunks both ways, h_in(c) forward (K4) and
+//      G_c = dL/dh_out(c) backward (G_{nch-1} = dfinal, dL/dh_in(c) = exp(cum_end(c)) G_c + D_c,
+//      dinit = dL/dh_in(0));
+//   3. bwd_chunk_grad_kernel: per chunk, with L_ij = exp(cum_i - cum_j) below the step diagonal,
 //      CB_ij = C_i . B_j and DX_ij = dy_i . x_j:
 //        dx_j = sum_i L_ij CB_ij dy_i + exp(cum_end - cum_j) G B_j
 //        dB_j = sum_i L_ij DX_ij C_i + exp(cum_end - cum_j) G^T x_j
 //        dC_i = sum_j L_ij DX_ij B_j + exp(cum_i) h_in^T dy_i
 //      and the gradient of every prefix sum cum_s (from L, exp(cum_i), exp(cum_end - cum_j) and
 //      exp(cum_end) h_in), whose suffix sums over the chunk's steps are ddA.
-// Rows are rank-fused (i = t R + r, step i / R); dB and dC add over the heads of a group.
+// Rows are rank-fused (i = t R + r, step i / R), 64 per chunk; dB and dC add over the heads of a
+// group.
 #include <math.h>
 #include <string.h>
 
@@ -56,66 +57,157 @@ __device__ __forceinline__ int bwd_steps(const GenericParams& p, int64_t c) {
   return (int)min(p.l, p.T - c * p.l);
 }
 
-// Dynamic shared memory of bwd_dstate_kernel: prefix sums, dy rows [Lr][P], C rows [Lr][N].
-size_t bwd_dstate_smem(int64_t Lr, int64_t P, int64_t N) {
-  return kBwdRows * sizeof(double) + sizeof(float) * (size_t)(Lr * P + Lr * N);
+// Register tiles: thread t owns rows t / 16 + 16 a (a < 4) and columns t % 16 + 16 q (q < NQ)
+// of a 64 x (16 NQ) output, so one k step loads 4 + NQ values for 4 NQ FMAs and the 16 lanes of
+// a half-warp read 16 consecutive floats.
+template <int NQ>
+constexpr int nq_cols() { return 16 * NQ; }
+
+// Dynamic shared memory of bwd_chunk_state_kernel: the prefix sums, then the scaled x and dy rows
+// [Lr][P] and the B and C rows [Lr][N].
+size_t bwd_state_smem(int64_t Lr, int64_t P, int64_t N) {
+  return kBwdRows * sizeof(double) + sizeof(float) * (size_t)(2 * Lr * P + 2 * Lr * N);
 }
 
-// D_c[p][n] = sum_i exp(cum_{i/R}) dy_i[p] C_i[n], written to dst (one CTA per (c, h, b)).
-template <typename T>
+// Per chunk (one CTA per (c, h, b)), both rank-Lr products of the chunk:
+//   S_c[p][n] = sum_i exp(cum_end - cum_i) x_i[p] B_i[n]   (the chunk's own end state, K3)
+//   D_c[p][n] = sum_i exp(cum_i) dy_i[p] C_i[n]             (its outputs' part of dL/dh_in(c))
+// and the chunk's total log-decay cum_end.
+template <typename T, int NQ>
 __global__ void __launch_bounds__(kBwdThreads)
-    bwd_dstate_kernel(GenericParams p, const float* __restrict__ dy, float* __restrict__ dst) {
-  extern __shared__ double bwd_dsm[];
-  double* cum = bwd_dsm;                                       // [kBwdRows]
+    bwd_chunk_state_kernel(GenericParams p, const float* __restrict__ dy,
+                           float* __restrict__ dst) {
+  extern __shared__ double bwd_ssm[];
+  double* cum = bwd_ssm;                                        // [kBwdRows]
   const int l = (int)p.l, R = (int)p.R, P = (int)p.P, N = (int)p.N, Lr = l * R;
-  float* sdy = reinterpret_cast<float*>(cum + kBwdRows);      // [Lr][P]
-  float* sc = sdy + Lr * P;                                    // [Lr][N]
+  float* sx = reinterpret_cast<float*>(cum + kBwdRows);        // [Lr][P]
+  float* sdy = sx + Lr * P;                                     // [Lr][P]
+  float* sB = sdy + Lr * P;                                     // [Lr][N]
+  float* sC = sB + Lr * N;                                      // [Lr][N]
   const int64_t c = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int64_t g = h / (p.H / p.G);
   const int nv = bwd_steps(p, c), nvr = nv * R;
-  bwd_cumsum(p.dA + (b * p.T + c * p.l) * p.H + h, p.H, l, nv, cum);
-  const int64_t row0 = (b * p.T + c * p.l) * R;
-  const T* C = static_cast<const T*>(p.C);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  bwd_cumsum(p.dA + (b * p.T + c * p.l) * p.H + h, p.H, l, nv, cum);
+  __syncthreads();
+  const double cum_end = cum[l - 1];
+  const int64_t row0 = (b * p.T + c * p.l) * R;
+  const T* xs = static_cast<const T*>(p.x);
+  const T* Bs = static_cast<const T*>(p.B);
+  const T* Cs = static_cast<const T*>(p.C);
   for (int i = warp; i < Lr; i += kBwdWarps) {
-    const float* src = dy + ((row0 + i) * p.H + h) * P;
-    for (int pp = lane; pp < P; pp += 32) sdy[i * P + pp] = i < nvr ? src[pp] : 0.f;
-    const T* cs = C + ((row0 + i) * p.G + g) * N;
-    for (int n = lane; n < N; n += 32) sc[i * N + n] = i < nvr ? ld_f32(cs + n) : 0.f;
+    const bool real = i < nvr;
+    const float wl = expf((float)(cum_end - cum[i / R])), we = expf((float)cum[i / R]);
+    const int64_t xo = ((row0 + i) * p.H + h) * P, bo = ((row0 + i) * p.G + g) * N;
+    for (int pp = lane; pp < P; pp += 32) {
+      sx[i * P + pp] = real ? wl * ld_f32(xs + xo + pp) : 0.f;
+      sdy[i * P + pp] = real ? we * __ldg(dy + xo + pp) : 0.f;
+    }
+    for (int n = lane; n < N; n += 32) {
+      sB[i * N + n] = real ? ld_f32(Bs + bo + n) : 0.f;
+      sC[i * N + n] = real ? ld_f32(Cs + bo + n) : 0.f;
+    }
   }
   __syncthreads();
-  for (int i = warp; i < Lr; i += kBwdWarps) {   // fold exp(cum) into the dy rows
-    const float w = expf((float)cum[i / R]);
-    for (int pp = lane; pp < P; pp += 32) sdy[i * P + pp] *= w;
+  const int t16 = threadIdx.x >> 4, l16 = threadIdx.x & 15;
+  int pc[4], nc[NQ];
+#pragma unroll
+  for (int a = 0; a < 4; ++a) pc[a] = min(t16 + 16 * a, P - 1);
+#pragma unroll
+  for (int q = 0; q < NQ; ++q) nc[q] = min(l16 + 16 * q, N - 1);
+  float as[4][NQ], ad[4][NQ];
+#pragma unroll
+  for (int a = 0; a < 4; ++a)
+#pragma unroll
+    for (int q = 0; q < NQ; ++q) as[a][q] = ad[a][q] = 0.f;
+  for (int i = 0; i < Lr; ++i) {
+    float xv[4], dv[4], bv[NQ], cv[NQ];
+#pragma unroll
+    for (int a = 0; a < 4; ++a) {
+      xv[a] = sx[i * P + pc[a]];
+      dv[a] = sdy[i * P + pc[a]];
+    }
+#pragma unroll
+    for (int q = 0; q < NQ; ++q) {
+      bv[q] = sB[i * N + nc[q]];
+      cv[q] = sC[i * N + nc[q]];
+    }
+#pragma unroll
+    for (int a = 0; a < 4; ++a)
+#pragma unroll
+      for (int q = 0; q < NQ; ++q) {
+        as[a][q] = fmaf(xv[a], bv[q], as[a][q]);
+        ad[a][q] = fmaf(dv[a], cv[q], ad[a][q]);
+      }
   }
-  __syncthreads();
-  float* out = dst + ((b * p.nch + c) * p.H + h) * (int64_t)P * N;
-  for (int o = threadIdx.x; o < P * N; o += kBwdThreads) {
-    const int pp = o / N, n = o % N;
-    float s = 0.f;
-    for (int i = 0; i < Lr; ++i) s = fmaf(sdy[i * P + pp], sc[i * N + n], s);
-    out[o] = s;
+  const int64_t so = ((b * p.nch + c) * p.H + h) * (int64_t)P * N;
+#pragma unroll
+  for (int a = 0; a < 4; ++a) {
+    const int pp = t16 + 16 * a;
+#pragma unroll
+    for (int q = 0; q < NQ; ++q) {
+      const int n = l16 + 16 * q;
+      if (pp < P && n < N) {
+        p.states[so + pp * N + n] = as[a][q];
+        dst[so + pp * N + n] = ad[a][q];
+      }
+    }
   }
+  if (threadIdx.x == 0) p.cend[(b * p.nch + c) * p.H + h] = (float)cum_end;
 }
 
-// Reverse K4, one thread per state element of one (b, h): G_c = dL/dh_out(c) replaces D_c in
-// place; dinit = dL/dh_in(0).
-__global__ void __launch_bounds__(kBwdThreads)
-    bwd_state_pass_kernel(GenericParams p, const float* __restrict__ dfinal,
-                          float* __restrict__ dg, float* __restrict__ dinit) {
+// Both carries across chunks, one thread per state element of one (b, h), loads kCarryAhead
+// chunks ahead of the serial update:
+//   forward  (K4): states[c] <- h_in(c),  h_in(c+1) = exp(cend_c) h_in(c) + S_c,  h_in(0) = init
+//   backward:      dg[c] <- G_c = dL/dh_in(c+1),  dL/dh_in(c) = exp(cend_c) G_c + D_c,
+//                  G_{nch-1} = dfinal, dinit = dL/dh_in(0).
+constexpr int kCarryAhead = 16;
+
+__global__ void __launch_bounds__(kBwdThreads, 2)
+    bwd_carry_kernel(GenericParams p, const float* __restrict__ dfinal, float* __restrict__ dg,
+                     float* __restrict__ dinit) {
   const int64_t PN = p.P * p.N;
   const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (idx >= p.batch * p.H * PN) return;
   const int64_t bh = idx / PN, e = idx % PN;
   const int64_t b = bh / p.H, h = bh % p.H;
-  float g = dfinal ? dfinal[idx] : 0.f;
-  for (int64_t c = p.nch - 1; c >= 0; --c) {
-    float* slot = dg + ((b * p.nch + c) * p.H + h) * PN + e;
-    const float d = *slot;
-    *slot = g;                                              // G_c
-    g = fmaf(expf(p.cend[(b * p.nch + c) * p.H + h]), g, d);   // dL/dh_in(c)
+  const int64_t cs = p.H * PN;                        // chunk stride
+  float* sp = p.states + (b * p.nch * p.H + h) * PN + e;
+  float* gp = dg + (b * p.nch * p.H + h) * PN + e;
+  const float* ce = p.cend + b * p.nch * p.H + h;
+  float hv = p.init ? p.init[idx] : 0.f;
+  for (int64_t c0 = 0; c0 < p.nch; c0 += kCarryAhead) {
+    float sv[kCarryAhead], av[kCarryAhead];
+#pragma unroll
+    for (int k = 0; k < kCarryAhead; ++k)
+      if (c0 + k < p.nch) {
+        sv[k] = sp[(c0 + k) * cs];
+        av[k] = ce[(c0 + k) * p.H];
+      }
+#pragma unroll
+    for (int k = 0; k < kCarryAhead; ++k)
+      if (c0 + k < p.nch) {
+        sp[(c0 + k) * cs] = hv;
+        hv = fmaf(expf(av[k]), hv, sv[k]);
+      }
   }
-  if (dinit) dinit[idx] = g;
+  float gv = dfinal ? dfinal[idx] : 0.f;
+  for (int64_t c1 = p.nch - 1; c1 >= 0; c1 -= kCarryAhead) {
+    float dv[kCarryAhead], av[kCarryAhead];
+#pragma unroll
+    for (int k = 0; k < kCarryAhead; ++k)
+      if (c1 - k >= 0) {
+        dv[k] = gp[(c1 - k) * cs];
+        av[k] = ce[(c1 - k) * p.H];
+      }
+#pragma unroll
+    for (int k = 0; k < kCarryAhead; ++k)
+      if (c1 - k >= 0) {
+        gp[(c1 - k) * cs] = gv;
+        gv = fmaf(expf(av[k]), gv, dv[k]);
+      }
+  }
+  if (dinit) dinit[idx] = gv;
 }
 
 // Dynamic shared memory of bwd_chunk_grad_kernel: per-step prefix sums and four per-row double
@@ -127,16 +219,20 @@ size_t bwd_grad_smem(int64_t Lr, int64_t P, int64_t N) {
   return (5 * kBwdRows + kBwdWarps) * sizeof(double) + f * sizeof(float);
 }
 
-__device__ __forceinline__ float warp_sum(float v) {
+// Sum over the 16 lanes of a half-warp (every lane of the warp takes part).
+__device__ __forceinline__ float half_warp_sum(float v) {
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+  for (int off = 8; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
   return v;
 }
 
 // Every gradient of one chunk (one CTA per (c, h, b)); dB and dC are added atomically (the heads
 // of a group share them and were zeroed by the caller); dx and ddA are written for real steps.
-template <typename T>
-__global__ void __launch_bounds__(kBwdThreads)
+// The per-row gradients are register-tiled products over the chunk's rows or the state:
+//   dx = M^T dy + diag(el) B G^T,  dB = A^T C + diag(el) x G,  dC = A B + diag(e) dy h_in
+// with M = L o CB, A = L o DX, el_j = exp(cum_end - cum_j), e_i = exp(cum_i).
+template <typename T, int NQ>
+__global__ void __launch_bounds__(kBwdThreads, 1)
     bwd_chunk_grad_kernel(GenericParams p, const float* __restrict__ dy,
                           const float* __restrict__ dg, float* __restrict__ dx,
                           float* __restrict__ ddA, float* __restrict__ dB,
@@ -183,16 +279,17 @@ __global__ void __launch_bounds__(kBwdThreads)
     }
   }
   const int64_t so = ((b * p.nch + c) * p.H + h) * (int64_t)P * N;
-  for (int e = threadIdx.x; e < P * N; e += kBwdThreads) {
-    const int pp = e / N, n = e % N;
-    sH[pp * NS + n] = p.states[so + e];
-    sG[pp * NS + n] = dg[so + e];
+  for (int pp = warp; pp < P; pp += kBwdWarps) {
+    for (int n = lane; n < N; n += 32) {
+      sH[pp * NS + n] = p.states[so + pp * N + n];
+      sG[pp * NS + n] = dg[so + pp * N + n];
+    }
   }
   __syncthreads();
 
-  // Pairwise products: thread (ty, tx) owns rows i = ty + 16a and columns j = tx + 16b.
+  const int t16 = threadIdx.x >> 4, l16 = threadIdx.x & 15;
+  // Pairwise products: thread owns rows i = t16 + 16a and columns j = l16 + 16q of the chunk.
   {
-    const int ty = threadIdx.x >> 4, tx = threadIdx.x & 15;
     float cb[4][4], dx4[4][4];
 #pragma unroll
     for (int a = 0; a < 4; ++a)
@@ -201,8 +298,8 @@ __global__ void __launch_bounds__(kBwdThreads)
     int ri[4], cj[4];
 #pragma unroll
     for (int a = 0; a < 4; ++a) {
-      ri[a] = min(ty + 16 * a, Lr - 1);
-      cj[a] = min(tx + 16 * a, Lr - 1);
+      ri[a] = min(t16 + 16 * a, Lr - 1);
+      cj[a] = min(l16 + 16 * a, Lr - 1);
     }
     for (int n = 0; n < N; ++n) {
       float cv[4], bv[4];
@@ -230,10 +327,10 @@ __global__ void __launch_bounds__(kBwdThreads)
     }
 #pragma unroll
     for (int a = 0; a < 4; ++a) {
-      const int i = ty + 16 * a;
+      const int i = t16 + 16 * a;
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
-        const int j = tx + 16 * q;
+        const int j = l16 + 16 * q;
         if (i < Lr && j < Lr) {
           const int si = i / R, sj = j / R;
           const float L = sj <= si ? expf((float)(cum[si] - cum[sj])) : 0.f;
@@ -248,135 +345,192 @@ __global__ void __launch_bounds__(kBwdThreads)
   __syncthreads();
 
   const double cum_end = cum[l - 1];
-  if (threadIdx.x < Lr) {   // W row sums
-    double s = 0.0;
-    for (int j = 0; j < Lr; ++j) s += (double)sW[threadIdx.x * LS + j];
-    roww[threadIdx.x] = s;
+  if (threadIdx.x < Lr) {   // W row sums (four fp32 partials, then fp64)
+    float s4[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int j = 0; j < Lr; ++j) s4[j & 3] += sW[threadIdx.x * LS + j];
+    roww[threadIdx.x] = ((double)s4[0] + s4[1]) + ((double)s4[2] + s4[3]);
   } else if (threadIdx.x >= 128 && threadIdx.x < 128 + Lr) {   // W column sums
     const int j = threadIdx.x - 128;
-    double s = 0.0;
-    for (int i = 0; i < Lr; ++i) s += (double)sW[i * LS + j];
-    colw[j] = s;
+    float s4[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int i = 0; i < Lr; ++i) s4[i & 3] += sW[i * LS + j];
+    colw[j] = ((double)s4[0] + s4[1]) + ((double)s4[2] + s4[3]);
   }
 
-  // dx_j = sum_i M_ij dy_i + u_j with u_j = exp(cum_end - cum_j) G B_j; Q_j = x_j . u_j.
-  for (int j = warp; j < Lr; j += kBwdWarps) {
-    const int sj = j / R;
-    const float el = expf((float)(cum_end - cum[sj]));
-    float acc[2] = {0.f, 0.f}, u[2] = {0.f, 0.f};
-    for (int i = sj * R; i < Lr; ++i) {
-      const float m = sM[i * LS + j];
+  int rc[4];   // this thread's rows (clamped for loads)
 #pragma unroll
-      for (int k = 0; k < 2; ++k) {
-        const int pp = lane + 32 * k;
-        if (pp < P) acc[k] = fmaf(m, sdy[i * PS + pp], acc[k]);
-      }
-    }
+  for (int a = 0; a < 4; ++a) rc[a] = min(t16 + 16 * a, Lr - 1);
+  float el[4];
+#pragma unroll
+  for (int a = 0; a < 4; ++a) el[a] = expf((float)(cum_end - cum[rc[a] / R]));
+
+  // dx [Lr x P]: u = el_j (B G^T)_jp first (Q_j = x_j . u_j), then + (M^T dy)_jp.
+  {
+    int pc[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) pc[q] = min(l16 + 16 * q, P - 1);
+    float acc[4][4];
+#pragma unroll
+    for (int a = 0; a < 4; ++a)
+#pragma unroll
+      for (int q = 0; q < 4; ++q) acc[a][q] = 0.f;
     for (int n = 0; n < N; ++n) {
-      const float bv = sB[j * NS + n];
+      float bv[4], gv[4];
 #pragma unroll
-      for (int k = 0; k < 2; ++k) {
-        const int pp = lane + 32 * k;
-        if (pp < P) u[k] = fmaf(sG[pp * NS + n], bv, u[k]);
+      for (int a = 0; a < 4; ++a) bv[a] = sB[rc[a] * NS + n];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) gv[q] = sG[pc[q] * NS + n];
+#pragma unroll
+      for (int a = 0; a < 4; ++a)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) acc[a][q] = fmaf(bv[a], gv[q], acc[a][q]);
+    }
+#pragma unroll
+    for (int a = 0; a < 4; ++a) {
+      float qs = 0.f;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        acc[a][q] *= el[a];
+        if (l16 + 16 * q < P) qs = fmaf(sx[rc[a] * PS + pc[q]], acc[a][q], qs);
+      }
+      qs = half_warp_sum(qs);
+      if (l16 == 0 && t16 + 16 * a < Lr) qj[t16 + 16 * a] = (double)qs;
+    }
+    for (int i = (t16 / R) * R; i < Lr; ++i) {   // M_ij = 0 before row j's step
+      float mv[4], dv[4];
+#pragma unroll
+      for (int a = 0; a < 4; ++a) mv[a] = sM[i * LS + rc[a]];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) dv[q] = sdy[i * PS + pc[q]];
+#pragma unroll
+      for (int a = 0; a < 4; ++a)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) acc[a][q] = fmaf(mv[a], dv[q], acc[a][q]);
+    }
+#pragma unroll
+    for (int a = 0; a < 4; ++a) {
+      const int j = t16 + 16 * a;
+      if (j < nvr) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int pp = l16 + 16 * q;
+          if (pp < P) dx[((row0 + j) * p.H + h) * P + pp] = acc[a][q];
+        }
       }
     }
-    float q = 0.f;
-#pragma unroll
-    for (int k = 0; k < 2; ++k) {
-      const int pp = lane + 32 * k;
-      if (pp < P) {
-        u[k] *= el;
-        q = fmaf(sx[j * PS + pp], u[k], q);
-        if (j < nvr) dx[((row0 + j) * p.H + h) * P + pp] = acc[k] + u[k];
-      }
-    }
-    q = warp_sum(q);
-    if (lane == 0) qj[j] = (double)q;
   }
 
-  // dB_j = sum_i A_ij C_i + exp(cum_end - cum_j) G^T x_j.
-  for (int j = warp; j < Lr; j += kBwdWarps) {
-    const int sj = j / R;
-    const float el = expf((float)(cum_end - cum[sj]));
-    float acc[4] = {0.f, 0.f, 0.f, 0.f}, v[4] = {0.f, 0.f, 0.f, 0.f};
-    for (int i = sj * R; i < Lr; ++i) {
-      const float a = sA[i * LS + j];
+  int nc[NQ];
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const int n = lane + 32 * k;
-        if (n < N) acc[k] = fmaf(a, sC[i * NS + n], acc[k]);
-      }
-    }
+  for (int q = 0; q < NQ; ++q) nc[q] = min(l16 + 16 * q, N - 1);
+
+  // dB [Lr x N]: el_j (x G)_jn, then + (A^T C)_jn.
+  {
+    float acc[4][NQ];
+#pragma unroll
+    for (int a = 0; a < 4; ++a)
+#pragma unroll
+      for (int q = 0; q < NQ; ++q) acc[a][q] = 0.f;
     for (int pp = 0; pp < P; ++pp) {
-      const float xv = sx[j * PS + pp];
+      float xv[4], gv[NQ];
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const int n = lane + 32 * k;
-        if (n < N) v[k] = fmaf(sG[pp * NS + n], xv, v[k]);
-      }
+      for (int a = 0; a < 4; ++a) xv[a] = sx[rc[a] * PS + pp];
+#pragma unroll
+      for (int q = 0; q < NQ; ++q) gv[q] = sG[pp * NS + nc[q]];
+#pragma unroll
+      for (int a = 0; a < 4; ++a)
+#pragma unroll
+        for (int q = 0; q < NQ; ++q) acc[a][q] = fmaf(xv[a], gv[q], acc[a][q]);
     }
-    if (j < nvr) {
-      float* dst = dB + ((row0 + j) * p.G + g) * N;
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const int n = lane + 32 * k;
-        if (n < N) atomicAdd(dst + n, fmaf(el, v[k], acc[k]));
+    for (int a = 0; a < 4; ++a)
+#pragma unroll
+      for (int q = 0; q < NQ; ++q) acc[a][q] *= el[a];
+    for (int i = (t16 / R) * R; i < Lr; ++i) {   // A_ij = 0 before row j's step
+      float av[4], cv[NQ];
+#pragma unroll
+      for (int a = 0; a < 4; ++a) av[a] = sA[i * LS + rc[a]];
+#pragma unroll
+      for (int q = 0; q < NQ; ++q) cv[q] = sC[i * NS + nc[q]];
+#pragma unroll
+      for (int a = 0; a < 4; ++a)
+#pragma unroll
+        for (int q = 0; q < NQ; ++q) acc[a][q] = fmaf(av[a], cv[q], acc[a][q]);
+    }
+#pragma unroll
+    for (int a = 0; a < 4; ++a) {
+      const int j = t16 + 16 * a;
+      if (j < nvr) {
+        float* dst = dB + ((row0 + j) * p.G + g) * N;
+#pragma unroll
+        for (int q = 0; q < NQ; ++q)
+          if (l16 + 16 * q < N) atomicAdd(dst + l16 + 16 * q, acc[a][q]);
       }
     }
   }
 
-  // dC_i = sum_j A_ij B_j + exp(cum_i) h_in^T dy_i; E_i = exp(cum_i) C_i . (h_in^T dy_i).
-  for (int i = warp; i < Lr; i += kBwdWarps) {
-    const int si = i / R, jend = (si + 1) * R;
-    const float ei = expf((float)cum[si]);
-    float acc[4] = {0.f, 0.f, 0.f, 0.f}, v[4] = {0.f, 0.f, 0.f, 0.f};
+  // dC [Lr x N]: e_i (dy h_in)_in first (E_i = C_i . that row), then + (A B)_in.
+  {
+    float acc[4][NQ];
+#pragma unroll
+    for (int a = 0; a < 4; ++a)
+#pragma unroll
+      for (int q = 0; q < NQ; ++q) acc[a][q] = 0.f;
+    for (int pp = 0; pp < P; ++pp) {
+      float dv[4], hv[NQ];
+#pragma unroll
+      for (int a = 0; a < 4; ++a) dv[a] = sdy[rc[a] * PS + pp];
+#pragma unroll
+      for (int q = 0; q < NQ; ++q) hv[q] = sH[pp * NS + nc[q]];
+#pragma unroll
+      for (int a = 0; a < 4; ++a)
+#pragma unroll
+        for (int q = 0; q < NQ; ++q) acc[a][q] = fmaf(dv[a], hv[q], acc[a][q]);
+    }
+#pragma unroll
+    for (int a = 0; a < 4; ++a) {
+      const float ei = expf((float)cum[rc[a] / R]);
+      float es = 0.f;
+#pragma unroll
+      for (int q = 0; q < NQ; ++q) {
+        acc[a][q] *= ei;
+        if (l16 + 16 * q < N) es = fmaf(sC[rc[a] * NS + nc[q]], acc[a][q], es);
+      }
+      es = half_warp_sum(es);
+      if (l16 == 0 && t16 + 16 * a < Lr) ein[t16 + 16 * a] = (double)es;
+    }
+    const int jend = min(Lr, (rc[3] / R + 1) * R);   // A_ij = 0 after row i's step
     for (int j = 0; j < jend; ++j) {
-      const float a = sA[i * LS + j];
+      float av[4], bv[NQ];
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const int n = lane + 32 * k;
-        if (n < N) acc[k] = fmaf(a, sB[j * NS + n], acc[k]);
+      for (int a = 0; a < 4; ++a) av[a] = sA[rc[a] * LS + j];
+#pragma unroll
+      for (int q = 0; q < NQ; ++q) bv[q] = sB[j * NS + nc[q]];
+#pragma unroll
+      for (int a = 0; a < 4; ++a)
+#pragma unroll
+        for (int q = 0; q < NQ; ++q) acc[a][q] = fmaf(av[a], bv[q], acc[a][q]);
+    }
+#pragma unroll
+    for (int a = 0; a < 4; ++a) {
+      const int i = t16 + 16 * a;
+      if (i < nvr) {
+        float* dst = dC + ((row0 + i) * p.G + g) * N;
+#pragma unroll
+        for (int q = 0; q < NQ; ++q)
+          if (l16 + 16 * q < N) atomicAdd(dst + l16 + 16 * q, acc[a][q]);
       }
     }
-    for (int pp = 0; pp < P; ++pp) {
-      const float dv = sdy[i * PS + pp];
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const int n = lane + 32 * k;
-        if (n < N) v[k] = fmaf(sH[pp * NS + n], dv, v[k]);
-      }
-    }
-    float e = 0.f;
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const int n = lane + 32 * k;
-      if (n < N) {
-        v[k] *= ei;
-        e = fmaf(sC[i * NS + n], v[k], e);
-      }
-    }
-    if (i < nvr) {
-      float* dst = dC + ((row0 + i) * p.G + g) * N;
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const int n = lane + 32 * k;
-        if (n < N) atomicAdd(dst + n, acc[k] + v[k]);
-      }
-    }
-    e = warp_sum(e);
-    if (lane == 0) ein[i] = (double)e;
   }
 
   // <G, h_in>, for the chunk-end gradient of exp(cum_end) h_in.
   {
-    double s = 0.0;
-    for (int e = threadIdx.x; e < P * N; e += kBwdThreads) {
-      const int pp = e / N, n = e % N;
-      s += (double)sG[pp * NS + n] * (double)sH[pp * NS + n];
-    }
+    float s = 0.f;
+    for (int pp = warp; pp < P; pp += kBwdWarps)
+      for (int n = lane; n < N; n += 32) s = fmaf(sG[pp * NS + n], sH[pp * NS + n], s);
+    double d = (double)s;
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-    if (lane == 0) red[warp] = s;
+    for (int off = 16; off > 0; off >>= 1) d += __shfl_xor_sync(0xffffffffu, d, off);
+    if (lane == 0) red[warp] = d;
   }
   __syncthreads();
 
@@ -412,8 +566,7 @@ ssd_status bwd_shape_status(const ssd_shape* s) {
   const int64_t l = bwd_chunk_steps(s->mimo_rank), Lr = l * s->mimo_rank;
   const size_t lim = 227 * 1024;
   if (bwd_grad_smem(Lr, s->headdim, s->dstate) > lim ||
-      bwd_dstate_smem(Lr, s->headdim, s->dstate) > lim ||
-      !generic_supported(l, s->mimo_rank, s->headdim, s->dstate, false))
+      bwd_state_smem(Lr, s->headdim, s->dstate) > lim)
     return SSD_ERR_UNSUPPORTED;
   return SSD_OK;
 }
@@ -436,28 +589,39 @@ BwdLayout bwd_layout(const ssd_shape* s) {
 
 bool al16_or_null(const void* q) { return q == nullptr || aligned16(q); }
 
+template <typename T, int NQ>
+cudaError_t bwd_launch_nq(const GenericParams& p, const float* dy, const float* dfinal,
+                          float* dx, float* ddA, float* dB, float* dC, float* dinit, float* dg,
+                          cudaStream_t st) {
+  const int64_t Lr = p.l * p.R;
+  const dim3 grid((unsigned)p.nch, (unsigned)p.H, (unsigned)p.batch);
+  const size_t s1 = bwd_state_smem(Lr, p.P, p.N);
+  cudaError_t e = cudaFuncSetAttribute(bwd_chunk_state_kernel<T, NQ>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s1);
+  if (e != cudaSuccess) return e;
+  bwd_chunk_state_kernel<T, NQ><<<grid, kBwdThreads, s1, st>>>(p, dy, dg);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  const int64_t n = p.batch * p.H * p.P * p.N;
+  bwd_carry_kernel<<<(unsigned)((n + kBwdThreads - 1) / kBwdThreads), kBwdThreads, 0, st>>>(
+      p, dfinal, dg, dinit);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  const size_t s2 = bwd_grad_smem(Lr, p.P, p.N);
+  e = cudaFuncSetAttribute(bwd_chunk_grad_kernel<T, NQ>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s2);
+  if (e != cudaSuccess) return e;
+  bwd_chunk_grad_kernel<T, NQ><<<grid, kBwdThreads, s2, st>>>(p, dy, dg, dx, ddA, dB, dC);
+  return cudaGetLastError();
+}
+
+// Column tiles of 16 state dims: N <= 16, 32, 64 or 128.
 template <typename T>
 cudaError_t bwd_launch(const GenericParams& p, const float* dy, const float* dfinal, float* dx,
                        float* ddA, float* dB, float* dC, float* dinit, float* dg,
                        cudaStream_t st) {
-  const int64_t Lr = p.l * p.R;
-  const dim3 grid((unsigned)p.nch, (unsigned)p.H, (unsigned)p.batch);
-  const size_t s1 = bwd_dstate_smem(Lr, p.P, p.N);
-  cudaError_t e = cudaFuncSetAttribute(bwd_dstate_kernel<T>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s1);
-  if (e != cudaSuccess) return e;
-  bwd_dstate_kernel<T><<<grid, kBwdThreads, s1, st>>>(p, dy, dg);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  const int64_t n = p.batch * p.H * p.P * p.N;
-  bwd_state_pass_kernel<<<(unsigned)((n + kBwdThreads - 1) / kBwdThreads), kBwdThreads, 0, st>>>(
-      p, dfinal, dg, dinit);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  const size_t s2 = bwd_grad_smem(Lr, p.P, p.N);
-  e = cudaFuncSetAttribute(bwd_chunk_grad_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)s2);
-  if (e != cudaSuccess) return e;
-  bwd_chunk_grad_kernel<T><<<grid, kBwdThreads, s2, st>>>(p, dy, dg, dx, ddA, dB, dC);
-  return cudaGetLastError();
+  if (p.N <= 16) return bwd_launch_nq<T, 1>(p, dy, dfinal, dx, ddA, dB, dC, dinit, dg, st);
+  if (p.N <= 32) return bwd_launch_nq<T, 2>(p, dy, dfinal, dx, ddA, dB, dC, dinit, dg, st);
+  if (p.N <= 64) return bwd_launch_nq<T, 4>(p, dy, dfinal, dx, ddA, dB, dC, dinit, dg, st);
+  return bwd_launch_nq<T, 8>(p, dy, dfinal, dx, ddA, dB, dC, dinit, dg, st);
 }
 
 }  // namespace
@@ -515,7 +679,6 @@ ssd_status ssd_chunked_backward(const ssd_shape* shape, const void* x, const flo
   const size_t bc = sizeof(float) * (size_t)(p.batch * p.T * p.R * p.G * p.N);
   if (cudaMemsetAsync(dB, 0, bc, st) != cudaSuccess || cudaMemsetAsync(dC, 0, bc, st) != cudaSuccess)
     return SSD_ERR_CUDA;
-  if (generic_states(p, bf16, st) != cudaSuccess) return SSD_ERR_CUDA;
   const cudaError_t e =
       bf16 ? bwd_launch<__nv_bfloat16>(p, dy, dfinal, dx, ddA, dB, dC, dinit, dg, st)
            : bwd_launch<float>(p, dy, dfinal, dx, ddA, dB, dC, dinit, dg, st);
