@@ -65,6 +65,9 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
+    # smaller cases of a workload's shape, for profiler captures (not bench lines)
+    ap.add_argument("--batch", type=int, default=0, help="override the workload's batch")
+    ap.add_argument("--seqlen", type=int, default=0, help="override the workload's seqlen")
     return ap.parse_args()
 
 
@@ -85,7 +88,17 @@ def measured_peaks():
         return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
 
 
-def workload(name):
+def workload(name, batch=0, seqlen=0):
+    cfg = _named_workload(name)
+    kw = {}
+    if batch:
+        kw["batch"] = batch
+    if seqlen:
+        kw["seqlen"] = seqlen
+    return cfg.with_(**kw) if kw else cfg
+
+
+def _named_workload(name):
     from chunked_ssd_scan_gb300 import workloads as wl
     for c in wl.SSD_CONFIGS:
         if c.name == name:
@@ -201,7 +214,7 @@ def run_ours(args, rank, world, local):
 
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    cfg = workload(args.workload)
+    cfg = workload(args.workload, args.batch, args.seqlen)
     stream = torch.cuda.current_stream()
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     is_ss = isinstance(cfg, wl.SelectiveScanConfig)
@@ -312,9 +325,11 @@ def run_ours(args, rank, world, local):
     ms = slowest_replica_ms(sum(step_ms) / len(step_ms), world, dev)
     tokens = job_tokens(cfg.tokens, world)
     hbm, tf, peak_src = measured_peaks()
+    # the capture's bytes belong to the workload's own shape, not to an overridden one
+    traffic = None if (args.batch or args.seqlen) else NCU_TRAFFIC_BYTES.get(cfg.name)
     achieved = io_bytes / (ms * 1e-3) / 1e9
     roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
-            "frac": round(achieved / hbm, 4), "traffic": NCU_TRAFFIC_BYTES.get(cfg.name),
+            "frac": round(achieved / hbm, 4), "traffic": traffic,
             "peak_source": peak_src,
             "kernel": ("selective_scan_forward" if is_ss
                        else "ssd_chunked_backward" if variant == "backward"
@@ -327,7 +342,7 @@ def run_ours(args, rank, world, local):
         alu = ALU_FP32_TFLOPS
         a_tf = flops / (ms * 1e-3) / 1e12
         roof = {"bound": "alu", "achieved": round(a_tf, 2), "peak": alu, "unit": "TFLOP/s",
-                "frac": round(a_tf / alu, 4), "traffic": NCU_TRAFFIC_BYTES.get(cfg.name),
+                "frac": round(a_tf / alu, 4), "traffic": traffic,
                 "peak_source": "derived: 152 SMs x 128 fp32 lanes x 2 FLOP x 2.07 GHz",
                 "kernel": "ssd_chunked_backward", "algorithmic_flops_per_launch": flops,
                 "algorithmic_bytes_per_launch": io_bytes,
@@ -605,7 +620,7 @@ def cpu_baseline(cfg, is_ss, host, target_s: float = 12.0):
 def run_reference(args, rank, world):
     """Reference arm: the fp64 oracle on the host cores, W untimed and K timed steps, each step a
     bounded sample of the same workload; same metric and unit as our arm."""
-    cfg = workload(args.workload)
+    cfg = workload(args.workload, args.batch, args.seqlen)
     from chunked_ssd_scan_gb300 import workloads as wl
     is_ss = isinstance(cfg, wl.SelectiveScanConfig)
     host = (wl.make_selective_scan_inputs(cfg, seed=0) if is_ss

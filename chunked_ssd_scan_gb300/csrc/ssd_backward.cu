@@ -29,6 +29,7 @@ namespace {
 constexpr int kBwdThreads = 256, kBwdWarps = kBwdThreads / 32;
 constexpr int kBwdRows = 64;   // fused rows per chunk
 constexpr int kBwdMaxP = 64, kBwdMaxN = 128;
+constexpr int kRowsPerWarp = kBwdRows / kBwdWarps;
 
 // fp64 inclusive prefix sums of dA over the chunk's steps (warp 0); steps at or after nv are 0.
 __device__ void bwd_cumsum(const float* __restrict__ src, int64_t stride, int l, int nv,
@@ -57,33 +58,89 @@ __device__ __forceinline__ int bwd_steps(const GenericParams& p, int64_t c) {
   return (int)min(p.l, p.T - c * p.l);
 }
 
-// Register tiles: thread t owns rows t / 16 + 16 a (a < 4) and columns t % 16 + 16 q (q < NQ)
-// of a 64 x (16 NQ) output, so one k step loads 4 + NQ values for 4 NQ FMAs and the 16 lanes of
-// a half-warp read 16 consecutive floats.
+// Column tiles of the state axis: NQ values per thread, as HH runs of VW consecutive columns
+// (n = VW l16 + r + 16 VW hh for lane l16 of a half-warp), so one shared-memory load moves VW
+// floats and a half-warp reads 16 VW consecutive floats of a row.
 template <int NQ>
-constexpr int nq_cols() { return 16 * NQ; }
+struct ColTile {
+  static constexpr int VW = NQ < 4 ? NQ : 4;
+  static constexpr int HH = NQ / VW;
+};
+
+template <int V>
+__device__ __forceinline__ void lds_vec(const float* src, float* out) {
+  if constexpr (V == 4) {
+    const float4 v = *reinterpret_cast<const float4*>(src);
+    out[0] = v.x;
+    out[1] = v.y;
+    out[2] = v.z;
+    out[3] = v.w;
+  } else if constexpr (V == 2) {
+    const float2 v = *reinterpret_cast<const float2*>(src);
+    out[0] = v.x;
+    out[1] = v.y;
+  } else {
+    out[0] = *src;
+  }
+}
+
+template <int V>
+__device__ __forceinline__ void atomic_add_vec(float* dst, const float* v) {
+  if constexpr (V == 4) {
+    atomicAdd(reinterpret_cast<float4*>(dst), make_float4(v[0], v[1], v[2], v[3]));
+  } else if constexpr (V == 2) {
+    atomicAdd(reinterpret_cast<float2*>(dst), make_float2(v[0], v[1]));
+  } else {
+    atomicAdd(dst, v[0]);
+  }
+}
+
+template <int V>
+__device__ __forceinline__ void st_vec(float* dst, const float* v) {
+  if constexpr (V == 4) {
+    *reinterpret_cast<float4*>(dst) = make_float4(v[0], v[1], v[2], v[3]);
+  } else if constexpr (V == 2) {
+    *reinterpret_cast<float2*>(dst) = make_float2(v[0], v[1]);
+  } else {
+    *dst = v[0];
+  }
+}
+
+// First column of run hh of lane l16, clamped so the loaded run stays inside the row (columns
+// past N are masked by the caller).
+template <int NQ>
+__device__ __forceinline__ int col0(int l16, int hh, int NR) {
+  constexpr int VW = ColTile<NQ>::VW;
+  return min(VW * l16 + 16 * VW * hh, NR - VW);
+}
+
+__host__ __device__ inline int round4(int v) { return (v + 3) & ~3; }
 
 // Dynamic shared memory of bwd_chunk_state_kernel: the prefix sums, then the scaled x and dy rows
-// [Lr][P] and the B and C rows [Lr][N].
+// [Lr][P4] and the B and C rows [Lr][N4] (P4, N4: P, N rounded up to 4, zero-padded).
 size_t bwd_state_smem(int64_t Lr, int64_t P, int64_t N) {
-  return kBwdRows * sizeof(double) + sizeof(float) * (size_t)(2 * Lr * P + 2 * Lr * N);
+  return kBwdRows * sizeof(double) +
+         sizeof(float) * (size_t)(2 * Lr * round4((int)P) + 2 * Lr * round4((int)N));
 }
 
 // Per chunk (one CTA per (c, h, b)), both rank-Lr products of the chunk:
 //   S_c[p][n] = sum_i exp(cum_end - cum_i) x_i[p] B_i[n]   (the chunk's own end state, K3)
 //   D_c[p][n] = sum_i exp(cum_i) dy_i[p] C_i[n]             (its outputs' part of dL/dh_in(c))
-// and the chunk's total log-decay cum_end.
+// and the chunk's total log-decay cum_end.  Thread (t16, l16) owns rows p = 4 t16 + a and the
+// column tile of l16.
 template <typename T, int NQ>
-__global__ void __launch_bounds__(kBwdThreads)
+__global__ void __launch_bounds__(kBwdThreads, 2)
     bwd_chunk_state_kernel(GenericParams p, const float* __restrict__ dy,
                            float* __restrict__ dst) {
+  constexpr int VW = ColTile<NQ>::VW, HH = ColTile<NQ>::HH;
   extern __shared__ double bwd_ssm[];
   double* cum = bwd_ssm;                                        // [kBwdRows]
   const int l = (int)p.l, R = (int)p.R, P = (int)p.P, N = (int)p.N, Lr = l * R;
-  float* sx = reinterpret_cast<float*>(cum + kBwdRows);        // [Lr][P]
-  float* sdy = sx + Lr * P;                                     // [Lr][P]
-  float* sB = sdy + Lr * P;                                     // [Lr][N]
-  float* sC = sB + Lr * N;                                      // [Lr][N]
+  const int P4 = round4(P), N4 = round4(N);
+  float* sx = reinterpret_cast<float*>(cum + kBwdRows);        // [Lr][P4]
+  float* sdy = sx + Lr * P4;                                    // [Lr][P4]
+  float* sB = sdy + Lr * P4;                                    // [Lr][N4]
+  float* sC = sB + Lr * N4;                                     // [Lr][N4]
   const int64_t c = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int64_t g = h / (p.H / p.G);
   const int nv = bwd_steps(p, c), nvr = nv * R;
@@ -95,26 +152,58 @@ __global__ void __launch_bounds__(kBwdThreads)
   const T* xs = static_cast<const T*>(p.x);
   const T* Bs = static_cast<const T*>(p.B);
   const T* Cs = static_cast<const T*>(p.C);
-  for (int i = warp; i < Lr; i += kBwdWarps) {
-    const bool real = i < nvr;
-    const float wl = expf((float)(cum_end - cum[i / R])), we = expf((float)cum[i / R]);
-    const int64_t xo = ((row0 + i) * p.H + h) * P, bo = ((row0 + i) * p.G + g) * N;
-    for (int pp = lane; pp < P; pp += 32) {
-      sx[i * P + pp] = real ? wl * ld_f32(xs + xo + pp) : 0.f;
-      sdy[i * P + pp] = real ? we * __ldg(dy + xo + pp) : 0.f;
+  {
+    // each warp stages its 8 rows i = warp + 8 k: every global load first, then the stores
+    float xr[kRowsPerWarp][2], dr[kRowsPerWarp][2], br[kRowsPerWarp][4], cr[kRowsPerWarp][4];
+#pragma unroll
+    for (int k = 0; k < kRowsPerWarp; ++k) {
+      const int i = warp + kBwdWarps * k;
+      const bool real = i < nvr;
+      const int64_t xo = ((row0 + i) * p.H + h) * P, bo = ((row0 + i) * p.G + g) * N;
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int pp = lane + 32 * u;
+        const bool v = real && pp < P;
+        xr[k][u] = v ? ld_f32(xs + xo + pp) : 0.f;
+        dr[k][u] = v ? __ldg(dy + xo + pp) : 0.f;
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int n = lane + 32 * u;
+        const bool v = real && n < N;
+        br[k][u] = v ? ld_f32(Bs + bo + n) : 0.f;
+        cr[k][u] = v ? ld_f32(Cs + bo + n) : 0.f;
+      }
     }
-    for (int n = lane; n < N; n += 32) {
-      sB[i * N + n] = real ? ld_f32(Bs + bo + n) : 0.f;
-      sC[i * N + n] = real ? ld_f32(Cs + bo + n) : 0.f;
+#pragma unroll
+    for (int k = 0; k < kRowsPerWarp; ++k) {
+      const int i = warp + kBwdWarps * k;
+      if (i >= Lr) continue;
+      const float wl = expf((float)(cum_end - cum[i / R])), we = expf((float)cum[i / R]);
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int pp = lane + 32 * u;
+        if (pp < P4) {
+          sx[i * P4 + pp] = wl * xr[k][u];
+          sdy[i * P4 + pp] = we * dr[k][u];
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int n = lane + 32 * u;
+        if (n < N4) {
+          sB[i * N4 + n] = br[k][u];
+          sC[i * N4 + n] = cr[k][u];
+        }
+      }
     }
   }
   __syncthreads();
   const int t16 = threadIdx.x >> 4, l16 = threadIdx.x & 15;
-  int pc[4], nc[NQ];
+  const int p0 = min(4 * t16, P4 - 4);
+  int n0[HH];
 #pragma unroll
-  for (int a = 0; a < 4; ++a) pc[a] = min(t16 + 16 * a, P - 1);
-#pragma unroll
-  for (int q = 0; q < NQ; ++q) nc[q] = min(l16 + 16 * q, N - 1);
+  for (int hh = 0; hh < HH; ++hh) n0[hh] = col0<NQ>(l16, hh, N4);
   float as[4][NQ], ad[4][NQ];
 #pragma unroll
   for (int a = 0; a < 4; ++a)
@@ -122,15 +211,12 @@ __global__ void __launch_bounds__(kBwdThreads)
     for (int q = 0; q < NQ; ++q) as[a][q] = ad[a][q] = 0.f;
   for (int i = 0; i < Lr; ++i) {
     float xv[4], dv[4], bv[NQ], cv[NQ];
+    lds_vec<4>(sx + i * P4 + p0, xv);
+    lds_vec<4>(sdy + i * P4 + p0, dv);
 #pragma unroll
-    for (int a = 0; a < 4; ++a) {
-      xv[a] = sx[i * P + pc[a]];
-      dv[a] = sdy[i * P + pc[a]];
-    }
-#pragma unroll
-    for (int q = 0; q < NQ; ++q) {
-      bv[q] = sB[i * N + nc[q]];
-      cv[q] = sC[i * N + nc[q]];
+    for (int hh = 0; hh < HH; ++hh) {
+      lds_vec<VW>(sB + i * N4 + n0[hh], bv + hh * VW);
+      lds_vec<VW>(sC + i * N4 + n0[hh], cv + hh * VW);
     }
 #pragma unroll
     for (int a = 0; a < 4; ++a)
@@ -143,79 +229,73 @@ __global__ void __launch_bounds__(kBwdThreads)
   const int64_t so = ((b * p.nch + c) * p.H + h) * (int64_t)P * N;
 #pragma unroll
   for (int a = 0; a < 4; ++a) {
-    const int pp = t16 + 16 * a;
+    const int pp = p0 + a;
+    if (pp >= P || p0 != 4 * t16) continue;
 #pragma unroll
-    for (int q = 0; q < NQ; ++q) {
-      const int n = l16 + 16 * q;
-      if (pp < P && n < N) {
-        p.states[so + pp * N + n] = as[a][q];
-        dst[so + pp * N + n] = ad[a][q];
-      }
+    for (int hh = 0; hh < HH; ++hh) {
+      const int n = n0[hh];
+      if (n != VW * l16 + 16 * VW * hh || n >= N) continue;   // a clamped (duplicate) run
+      st_vec<VW>(p.states + so + pp * N + n, as[a] + hh * VW);
+      st_vec<VW>(dst + so + pp * N + n, ad[a] + hh * VW);
     }
   }
   if (threadIdx.x == 0) p.cend[(b * p.nch + c) * p.H + h] = (float)cum_end;
 }
 
-// Both carries across chunks, one thread per state element of one (b, h), loads kCarryAhead
-// chunks ahead of the serial update:
+// The carries across chunks, one thread per state element of one (b, h) and direction (the
+// first b H P N threads forward, the rest backward), loading kCarryAhead chunks ahead of the
+// serial update:
 //   forward  (K4): states[c] <- h_in(c),  h_in(c+1) = exp(cend_c) h_in(c) + S_c,  h_in(0) = init
 //   backward:      dg[c] <- G_c = dL/dh_in(c+1),  dL/dh_in(c) = exp(cend_c) G_c + D_c,
 //                  G_{nch-1} = dfinal, dinit = dL/dh_in(0).
 constexpr int kCarryAhead = 16;
 
-__global__ void __launch_bounds__(kBwdThreads, 2)
+__global__ void __launch_bounds__(kBwdThreads)
     bwd_carry_kernel(GenericParams p, const float* __restrict__ dfinal, float* __restrict__ dg,
                      float* __restrict__ dinit) {
-  const int64_t PN = p.P * p.N;
-  const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (idx >= p.batch * p.H * PN) return;
+  const int64_t PN = p.P * p.N, n_el = p.batch * p.H * PN;
+  int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= 2 * n_el) return;
+  const bool back = idx >= n_el;
+  if (back) idx -= n_el;
   const int64_t bh = idx / PN, e = idx % PN;
   const int64_t b = bh / p.H, h = bh % p.H;
   const int64_t cs = p.H * PN;                        // chunk stride
-  float* sp = p.states + (b * p.nch * p.H + h) * PN + e;
-  float* gp = dg + (b * p.nch * p.H + h) * PN + e;
+  float* vp = (back ? dg : p.states) + (b * p.nch * p.H + h) * PN + e;
   const float* ce = p.cend + b * p.nch * p.H + h;
-  float hv = p.init ? p.init[idx] : 0.f;
-  for (int64_t c0 = 0; c0 < p.nch; c0 += kCarryAhead) {
+  float v = back ? (dfinal ? dfinal[idx] : 0.f) : (p.init ? p.init[idx] : 0.f);
+  for (int64_t k0 = 0; k0 < p.nch; k0 += kCarryAhead) {
     float sv[kCarryAhead], av[kCarryAhead];
 #pragma unroll
     for (int k = 0; k < kCarryAhead; ++k)
-      if (c0 + k < p.nch) {
-        sv[k] = sp[(c0 + k) * cs];
-        av[k] = ce[(c0 + k) * p.H];
+      if (k0 + k < p.nch) {
+        const int64_t c = back ? p.nch - 1 - (k0 + k) : k0 + k;
+        sv[k] = vp[c * cs];
+        av[k] = ce[c * p.H];
       }
 #pragma unroll
     for (int k = 0; k < kCarryAhead; ++k)
-      if (c0 + k < p.nch) {
-        sp[(c0 + k) * cs] = hv;
-        hv = fmaf(expf(av[k]), hv, sv[k]);
+      if (k0 + k < p.nch) {
+        const int64_t c = back ? p.nch - 1 - (k0 + k) : k0 + k;
+        vp[c * cs] = v;
+        v = fmaf(expf(av[k]), v, sv[k]);
       }
   }
-  float gv = dfinal ? dfinal[idx] : 0.f;
-  for (int64_t c1 = p.nch - 1; c1 >= 0; c1 -= kCarryAhead) {
-    float dv[kCarryAhead], av[kCarryAhead];
-#pragma unroll
-    for (int k = 0; k < kCarryAhead; ++k)
-      if (c1 - k >= 0) {
-        dv[k] = gp[(c1 - k) * cs];
-        av[k] = ce[(c1 - k) * p.H];
-      }
-#pragma unroll
-    for (int k = 0; k < kCarryAhead; ++k)
-      if (c1 - k >= 0) {
-        gp[(c1 - k) * cs] = gv;
-        gv = fmaf(expf(av[k]), gv, dv[k]);
-      }
-  }
-  if (dinit) dinit[idx] = gv;
+  if (back && dinit) dinit[idx] = v;
 }
 
-// Dynamic shared memory of bwd_chunk_grad_kernel: per-step prefix sums and four per-row double
-// vectors, then x, dy [Lr][P+1], B, C [Lr][N+1], h_in, G [P][N+1] and M, A, W [Lr][Lr+1] (one
-// float of padding per row keeps the column walks free of bank conflicts).
+// Shared-memory row strides of bwd_chunk_grad_kernel: the row length rounded up to 4 plus 4, so
+// rows start 16-byte aligned and the 8 lanes of a 16-byte load phase that read 8 different rows
+// hit 8 different bank groups.
+__host__ __device__ inline int bwd_stride(int len) { return round4(len) + 4; }
+
+// Dynamic shared memory of bwd_chunk_grad_kernel: per-step prefix sums, four per-row double
+// vectors and the warp partials of <G, h_in>, the warps' partial column sums of W, then x, dy
+// [Lr][P], B, C [Lr][N], h_in, G [P][N] and M, A [Lr][Lr] at the strides above.
 size_t bwd_grad_smem(int64_t Lr, int64_t P, int64_t N) {
-  const size_t f = 2 * (size_t)(Lr * (P + 1)) + 2 * (size_t)(Lr * (N + 1)) +
-                   2 * (size_t)(P * (N + 1)) + 3 * (size_t)(Lr * (Lr + 1));
+  const size_t PS = bwd_stride((int)P), NS = bwd_stride((int)N), LS = bwd_stride((int)Lr);
+  const size_t f = kBwdWarps * kBwdRows + 2 * (size_t)Lr * PS + 2 * (size_t)Lr * NS +
+                   2 * (size_t)P * NS + 2 * (size_t)Lr * LS;
   return (5 * kBwdRows + kBwdWarps) * sizeof(double) + f * sizeof(float);
 }
 
@@ -230,23 +310,28 @@ __device__ __forceinline__ float half_warp_sum(float v) {
 // of a group share them and were zeroed by the caller); dx and ddA are written for real steps.
 // The per-row gradients are register-tiled products over the chunk's rows or the state:
 //   dx = M^T dy + diag(el) B G^T,  dB = A^T C + diag(el) x G,  dC = A B + diag(e) dy h_in
-// with M = L o CB, A = L o DX, el_j = exp(cum_end - cum_j), e_i = exp(cum_i).
+// with M = L o CB, A = L o DX, el_j = exp(cum_end - cum_j), e_i = exp(cum_i).  Thread
+// (t16, l16) owns output rows 4 t16 + a (a < 4) and, along P, columns l16 + 16 q, along N the
+// column tile of l16 (ColTile); products whose reduction runs along a row load 4 k at a time.
 template <typename T, int NQ>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     bwd_chunk_grad_kernel(GenericParams p, const float* __restrict__ dy,
                           const float* __restrict__ dg, float* __restrict__ dx,
                           float* __restrict__ ddA, float* __restrict__ dB,
                           float* __restrict__ dC) {
+  constexpr int VW = ColTile<NQ>::VW, HH = ColTile<NQ>::HH;
   extern __shared__ double bwd_gsm[];
   const int l = (int)p.l, R = (int)p.R, P = (int)p.P, N = (int)p.N, Lr = l * R;
-  const int PS = P + 1, NS = N + 1, LS = Lr + 1;
+  const int P4 = round4(P), N4 = round4(N);
+  const int PS = bwd_stride(P), NS = bwd_stride(N), LS = bwd_stride(Lr);
   double* cum = bwd_gsm;               // [l] inclusive prefix sums of dA
-  double* roww = cum + kBwdRows;       // [Lr] sum_j W_ij
+  double* roww = cum + kBwdRows;       // [Lr] sum_j W_ij, W = M o DX
   double* colw = roww + kBwdRows;      // [Lr] sum_i W_ij
   double* ein = colw + kBwdRows;       // [Lr] exp(cum_i) C_i . (h_in^T dy_i)
   double* qj = ein + kBwdRows;         // [Lr] exp(cum_end - cum_j) x_j . (G B_j)
   double* red = qj + kBwdRows;         // [kBwdWarps] partial sums of <G, h_in>
-  float* sx = reinterpret_cast<float*>(red + kBwdWarps);
+  float* colp = reinterpret_cast<float*>(red + kBwdWarps);   // [kBwdWarps][kBwdRows]
+  float* sx = colp + kBwdWarps * kBwdRows;
   float* sdy = sx + Lr * PS;
   float* sB = sdy + Lr * PS;
   float* sC = sB + Lr * NS;
@@ -254,7 +339,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   float* sG = sH + P * NS;
   float* sM = sG + P * NS;             // L_ij CB_ij
   float* sA = sM + Lr * LS;            // L_ij DX_ij
-  float* sW = sA + Lr * LS;            // L_ij CB_ij DX_ij
 
   const int64_t c = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int64_t g = h / (p.H / p.G);
@@ -266,29 +350,78 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const T* Cs = static_cast<const T*>(p.C);
 
   bwd_cumsum(p.dA + (b * p.T + c * p.l) * p.H + h, p.H, l, nv, cum);
-  for (int i = warp; i < Lr; i += kBwdWarps) {
-    const bool real = i < nvr;
-    const int64_t xo = ((row0 + i) * p.H + h) * P, bo = ((row0 + i) * p.G + g) * N;
-    for (int pp = lane; pp < P; pp += 32) {
-      sx[i * PS + pp] = real ? ld_f32(xs + xo + pp) : 0.f;
-      sdy[i * PS + pp] = real ? __ldg(dy + xo + pp) : 0.f;
+  // Rows first (group 0: dy by async copy), then h_in and G (group 1), which are needed only
+  // after the pairwise products and land while those are computed.  Pads are zeroed.
+  {
+    // each warp stages its 8 rows i = warp + 8 k: every global load first, then the stores
+    float xr[kRowsPerWarp][2], br[kRowsPerWarp][4], cr[kRowsPerWarp][4];
+#pragma unroll
+    for (int k = 0; k < kRowsPerWarp; ++k) {
+      const int i = warp + kBwdWarps * k;
+      const bool real = i < nvr;
+      const int64_t xo = ((row0 + i) * p.H + h) * P, bo = ((row0 + i) * p.G + g) * N;
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int pp = lane + 32 * u;
+        const bool v = real && pp < P;
+        xr[k][u] = v ? ld_f32(xs + xo + pp) : 0.f;
+        if (v) cp_async4(sdy + i * PS + pp, dy + xo + pp);
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int n = lane + 32 * u;
+        const bool v = real && n < N;
+        br[k][u] = v ? ld_f32(Bs + bo + n) : 0.f;
+        cr[k][u] = v ? ld_f32(Cs + bo + n) : 0.f;
+      }
     }
-    for (int n = lane; n < N; n += 32) {
-      sB[i * NS + n] = real ? ld_f32(Bs + bo + n) : 0.f;
-      sC[i * NS + n] = real ? ld_f32(Cs + bo + n) : 0.f;
+#pragma unroll
+    for (int k = 0; k < kRowsPerWarp; ++k) {
+      const int i = warp + kBwdWarps * k;
+      if (i >= Lr) continue;
+      const bool real = i < nvr;
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int pp = lane + 32 * u;
+        if (pp < P4) {
+          sx[i * PS + pp] = xr[k][u];
+          if (!(real && pp < P)) sdy[i * PS + pp] = 0.f;
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int n = lane + 32 * u;
+        if (n < N4) {
+          sB[i * NS + n] = br[k][u];
+          sC[i * NS + n] = cr[k][u];
+        }
+      }
+      for (int j = Lr + lane; j < LS; j += 32) {   // M and A past the chunk's rows read as zero
+        sM[i * LS + j] = 0.f;
+        sA[i * LS + j] = 0.f;
+      }
     }
   }
+  cp_async_commit();
   const int64_t so = ((b * p.nch + c) * p.H + h) * (int64_t)P * N;
   for (int pp = warp; pp < P; pp += kBwdWarps) {
-    for (int n = lane; n < N; n += 32) {
-      sH[pp * NS + n] = p.states[so + pp * N + n];
-      sG[pp * NS + n] = dg[so + pp * N + n];
+    for (int n = lane; n < N4; n += 32) {
+      if (n < N) {
+        cp_async4(sH + pp * NS + n, p.states + so + pp * N + n);
+        cp_async4(sG + pp * NS + n, dg + so + pp * N + n);
+      } else {
+        sH[pp * NS + n] = 0.f;
+        sG[pp * NS + n] = 0.f;
+      }
     }
   }
+  cp_async_commit();
+  cp_async_wait<1>();
   __syncthreads();
 
   const int t16 = threadIdx.x >> 4, l16 = threadIdx.x & 15;
-  // Pairwise products: thread owns rows i = t16 + 16a and columns j = l16 + 16q of the chunk.
+  // Pairwise products: rows i = t16 + 16a, columns j = l16 + 16q of the chunk; M, A and the
+  // row and column sums of W.
   {
     float cb[4][4], dx4[4][4];
 #pragma unroll
@@ -301,30 +434,35 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       ri[a] = min(t16 + 16 * a, Lr - 1);
       cj[a] = min(l16 + 16 * a, Lr - 1);
     }
-    for (int n = 0; n < N; ++n) {
-      float cv[4], bv[4];
+    for (int n = 0; n < N4; n += 4) {
+      float cv[4][4], bv[4][4];
 #pragma unroll
       for (int a = 0; a < 4; ++a) {
-        cv[a] = sC[ri[a] * NS + n];
-        bv[a] = sB[cj[a] * NS + n];
+        lds_vec<4>(sC + ri[a] * NS + n, cv[a]);
+        lds_vec<4>(sB + cj[a] * NS + n, bv[a]);
       }
 #pragma unroll
-      for (int a = 0; a < 4; ++a)
+      for (int k = 0; k < 4; ++k)
 #pragma unroll
-        for (int q = 0; q < 4; ++q) cb[a][q] = fmaf(cv[a], bv[q], cb[a][q]);
+        for (int a = 0; a < 4; ++a)
+#pragma unroll
+          for (int q = 0; q < 4; ++q) cb[a][q] = fmaf(cv[a][k], bv[q][k], cb[a][q]);
     }
-    for (int pp = 0; pp < P; ++pp) {
-      float dv[4], xv[4];
+    for (int pp = 0; pp < P4; pp += 4) {
+      float dv[4][4], xv[4][4];
 #pragma unroll
       for (int a = 0; a < 4; ++a) {
-        dv[a] = sdy[ri[a] * PS + pp];
-        xv[a] = sx[cj[a] * PS + pp];
+        lds_vec<4>(sdy + ri[a] * PS + pp, dv[a]);
+        lds_vec<4>(sx + cj[a] * PS + pp, xv[a]);
       }
 #pragma unroll
-      for (int a = 0; a < 4; ++a)
+      for (int k = 0; k < 4; ++k)
 #pragma unroll
-        for (int q = 0; q < 4; ++q) dx4[a][q] = fmaf(dv[a], xv[q], dx4[a][q]);
+        for (int a = 0; a < 4; ++a)
+#pragma unroll
+          for (int q = 0; q < 4; ++q) dx4[a][q] = fmaf(dv[a][k], xv[q][k], dx4[a][q]);
     }
+    float rs[4] = {0.f, 0.f, 0.f, 0.f}, cs[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int a = 0; a < 4; ++a) {
       const int i = t16 + 16 * a;
@@ -337,28 +475,40 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           const float m = L * cb[a][q];
           sM[i * LS + j] = m;
           sA[i * LS + j] = L * dx4[a][q];
-          sW[i * LS + j] = m * dx4[a][q];
+          const float w = m * dx4[a][q];
+          rs[a] += w;
+          cs[q] += w;
         }
       }
     }
+#pragma unroll
+    for (int a = 0; a < 4; ++a) {
+      const float r = half_warp_sum(rs[a]);
+      if (l16 == 0 && t16 + 16 * a < Lr) roww[t16 + 16 * a] = (double)r;
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float v = cs[q] + __shfl_xor_sync(0xffffffffu, cs[q], 16);   // both half-warps
+      if (lane < 16 && l16 + 16 * q < Lr) colp[warp * kBwdRows + l16 + 16 * q] = v;
+    }
   }
+  cp_async_wait<0>();
   __syncthreads();
 
   const double cum_end = cum[l - 1];
-  if (threadIdx.x < Lr) {   // W row sums (four fp32 partials, then fp64)
-    float s4[4] = {0.f, 0.f, 0.f, 0.f};
-    for (int j = 0; j < Lr; ++j) s4[j & 3] += sW[threadIdx.x * LS + j];
-    roww[threadIdx.x] = ((double)s4[0] + s4[1]) + ((double)s4[2] + s4[3]);
-  } else if (threadIdx.x >= 128 && threadIdx.x < 128 + Lr) {   // W column sums
-    const int j = threadIdx.x - 128;
-    float s4[4] = {0.f, 0.f, 0.f, 0.f};
-    for (int i = 0; i < Lr; ++i) s4[i & 3] += sW[i * LS + j];
-    colw[j] = ((double)s4[0] + s4[1]) + ((double)s4[2] + s4[3]);
+  if (threadIdx.x < Lr) {   // W column sums over the warps' partials
+    double sacc = 0.0;
+    for (int w = 0; w < kBwdWarps; ++w) sacc += (double)colp[w * kBwdRows + threadIdx.x];
+    colw[threadIdx.x] = sacc;
   }
 
-  int rc[4];   // this thread's rows (clamped for loads)
+  const int r0 = 4 * t16;   // this thread's output rows r0 + a (clamped for loads)
+  int rc[4];
 #pragma unroll
-  for (int a = 0; a < 4; ++a) rc[a] = min(t16 + 16 * a, Lr - 1);
+  for (int a = 0; a < 4; ++a) rc[a] = min(r0 + a, Lr - 1);
+  // 16-byte aligned start of the 4 rows' columns of M and A; only a thread whose rows all lie
+  // past the chunk (outputs discarded) is moved back inside the row
+  const int ra = min(r0, LS - 4);
   float el[4];
 #pragma unroll
   for (int a = 0; a < 4; ++a) el[a] = expf((float)(cum_end - cum[rc[a] / R]));
@@ -373,16 +523,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     for (int a = 0; a < 4; ++a)
 #pragma unroll
       for (int q = 0; q < 4; ++q) acc[a][q] = 0.f;
-    for (int n = 0; n < N; ++n) {
-      float bv[4], gv[4];
+    for (int n = 0; n < N4; n += 4) {
+      float bv[4][4], gv[4][4];
 #pragma unroll
-      for (int a = 0; a < 4; ++a) bv[a] = sB[rc[a] * NS + n];
+      for (int a = 0; a < 4; ++a) lds_vec<4>(sB + rc[a] * NS + n, bv[a]);
 #pragma unroll
-      for (int q = 0; q < 4; ++q) gv[q] = sG[pc[q] * NS + n];
+      for (int q = 0; q < 4; ++q) lds_vec<4>(sG + pc[q] * NS + n, gv[q]);
 #pragma unroll
-      for (int a = 0; a < 4; ++a)
+      for (int k = 0; k < 4; ++k)
 #pragma unroll
-        for (int q = 0; q < 4; ++q) acc[a][q] = fmaf(bv[a], gv[q], acc[a][q]);
+        for (int a = 0; a < 4; ++a)
+#pragma unroll
+          for (int q = 0; q < 4; ++q) acc[a][q] = fmaf(bv[a][k], gv[q][k], acc[a][q]);
     }
 #pragma unroll
     for (int a = 0; a < 4; ++a) {
@@ -393,12 +545,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (l16 + 16 * q < P) qs = fmaf(sx[rc[a] * PS + pc[q]], acc[a][q], qs);
       }
       qs = half_warp_sum(qs);
-      if (l16 == 0 && t16 + 16 * a < Lr) qj[t16 + 16 * a] = (double)qs;
+      if (l16 == 0 && r0 + a < Lr) qj[r0 + a] = (double)qs;
     }
-    for (int i = (t16 / R) * R; i < Lr; ++i) {   // M_ij = 0 before row j's step
+    for (int i = (r0 / R) * R; i < Lr; ++i) {   // M_ij = 0 before row j's step
       float mv[4], dv[4];
-#pragma unroll
-      for (int a = 0; a < 4; ++a) mv[a] = sM[i * LS + rc[a]];
+      lds_vec<4>(sM + i * LS + ra, mv);
 #pragma unroll
       for (int q = 0; q < 4; ++q) dv[q] = sdy[i * PS + pc[q]];
 #pragma unroll
@@ -408,7 +559,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
 #pragma unroll
     for (int a = 0; a < 4; ++a) {
-      const int j = t16 + 16 * a;
+      const int j = r0 + a;
       if (j < nvr) {
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
@@ -419,9 +570,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
   }
 
-  int nc[NQ];
+  int n0[HH];
+  bool nown[HH];   // the run is this lane's own (not a clamped duplicate) and inside N
 #pragma unroll
-  for (int q = 0; q < NQ; ++q) nc[q] = min(l16 + 16 * q, N - 1);
+  for (int hh = 0; hh < HH; ++hh) {
+    n0[hh] = col0<NQ>(l16, hh, N4);
+    nown[hh] = n0[hh] == VW * l16 + 16 * VW * hh && n0[hh] < N;
+  }
 
   // dB [Lr x N]: el_j (x G)_jn, then + (A^T C)_jn.
   {
@@ -430,27 +585,31 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     for (int a = 0; a < 4; ++a)
 #pragma unroll
       for (int q = 0; q < NQ; ++q) acc[a][q] = 0.f;
-    for (int pp = 0; pp < P; ++pp) {
-      float xv[4], gv[NQ];
+    for (int pp = 0; pp < P4; pp += 4) {
+      float xv[4][4];
 #pragma unroll
-      for (int a = 0; a < 4; ++a) xv[a] = sx[rc[a] * PS + pp];
+      for (int a = 0; a < 4; ++a) lds_vec<4>(sx + rc[a] * PS + pp, xv[a]);
 #pragma unroll
-      for (int q = 0; q < NQ; ++q) gv[q] = sG[pp * NS + nc[q]];
+      for (int k = 0; k < 4; ++k) {
+        if (pp + k >= P) break;
+        float gv[NQ];
 #pragma unroll
-      for (int a = 0; a < 4; ++a)
+        for (int hh = 0; hh < HH; ++hh) lds_vec<VW>(sG + (pp + k) * NS + n0[hh], gv + hh * VW);
 #pragma unroll
-        for (int q = 0; q < NQ; ++q) acc[a][q] = fmaf(xv[a], gv[q], acc[a][q]);
+        for (int a = 0; a < 4; ++a)
+#pragma unroll
+          for (int q = 0; q < NQ; ++q) acc[a][q] = fmaf(xv[a][k], gv[q], acc[a][q]);
+      }
     }
 #pragma unroll
     for (int a = 0; a < 4; ++a)
 #pragma unroll
       for (int q = 0; q < NQ; ++q) acc[a][q] *= el[a];
-    for (int i = (t16 / R) * R; i < Lr; ++i) {   // A_ij = 0 before row j's step
+    for (int i = (r0 / R) * R; i < Lr; ++i) {   // A_ij = 0 before row j's step
       float av[4], cv[NQ];
+      lds_vec<4>(sA + i * LS + ra, av);
 #pragma unroll
-      for (int a = 0; a < 4; ++a) av[a] = sA[i * LS + rc[a]];
-#pragma unroll
-      for (int q = 0; q < NQ; ++q) cv[q] = sC[i * NS + nc[q]];
+      for (int hh = 0; hh < HH; ++hh) lds_vec<VW>(sC + i * NS + n0[hh], cv + hh * VW);
 #pragma unroll
       for (int a = 0; a < 4; ++a)
 #pragma unroll
@@ -458,12 +617,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
 #pragma unroll
     for (int a = 0; a < 4; ++a) {
-      const int j = t16 + 16 * a;
+      const int j = r0 + a;
       if (j < nvr) {
         float* dst = dB + ((row0 + j) * p.G + g) * N;
 #pragma unroll
-        for (int q = 0; q < NQ; ++q)
-          if (l16 + 16 * q < N) atomicAdd(dst + l16 + 16 * q, acc[a][q]);
+        for (int hh = 0; hh < HH; ++hh)
+          if (nown[hh]) atomic_add_vec<VW>(dst + n0[hh], acc[a] + hh * VW);
       }
     }
   }
@@ -475,78 +634,113 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     for (int a = 0; a < 4; ++a)
 #pragma unroll
       for (int q = 0; q < NQ; ++q) acc[a][q] = 0.f;
-    for (int pp = 0; pp < P; ++pp) {
-      float dv[4], hv[NQ];
+    for (int pp = 0; pp < P4; pp += 4) {
+      float dv[4][4];
 #pragma unroll
-      for (int a = 0; a < 4; ++a) dv[a] = sdy[rc[a] * PS + pp];
+      for (int a = 0; a < 4; ++a) lds_vec<4>(sdy + rc[a] * PS + pp, dv[a]);
 #pragma unroll
-      for (int q = 0; q < NQ; ++q) hv[q] = sH[pp * NS + nc[q]];
+      for (int k = 0; k < 4; ++k) {
+        if (pp + k >= P) break;
+        float hv[NQ];
 #pragma unroll
-      for (int a = 0; a < 4; ++a)
+        for (int hh = 0; hh < HH; ++hh) lds_vec<VW>(sH + (pp + k) * NS + n0[hh], hv + hh * VW);
 #pragma unroll
-        for (int q = 0; q < NQ; ++q) acc[a][q] = fmaf(dv[a], hv[q], acc[a][q]);
+        for (int a = 0; a < 4; ++a)
+#pragma unroll
+          for (int q = 0; q < NQ; ++q) acc[a][q] = fmaf(dv[a][k], hv[q], acc[a][q]);
+      }
     }
 #pragma unroll
     for (int a = 0; a < 4; ++a) {
       const float ei = expf((float)cum[rc[a] / R]);
+      float cv[NQ];
+#pragma unroll
+      for (int hh = 0; hh < HH; ++hh) lds_vec<VW>(sC + rc[a] * NS + n0[hh], cv + hh * VW);
       float es = 0.f;
 #pragma unroll
       for (int q = 0; q < NQ; ++q) {
         acc[a][q] *= ei;
-        if (l16 + 16 * q < N) es = fmaf(sC[rc[a] * NS + nc[q]], acc[a][q], es);
+        if (nown[q / VW]) es = fmaf(cv[q], acc[a][q], es);
       }
       es = half_warp_sum(es);
-      if (l16 == 0 && t16 + 16 * a < Lr) ein[t16 + 16 * a] = (double)es;
+      if (l16 == 0 && r0 + a < Lr) ein[r0 + a] = (double)es;
     }
     const int jend = min(Lr, (rc[3] / R + 1) * R);   // A_ij = 0 after row i's step
-    for (int j = 0; j < jend; ++j) {
-      float av[4], bv[NQ];
+    for (int j0 = 0; j0 < jend; j0 += 4) {
+      float av[4][4];
 #pragma unroll
-      for (int a = 0; a < 4; ++a) av[a] = sA[rc[a] * LS + j];
+      for (int a = 0; a < 4; ++a) lds_vec<4>(sA + rc[a] * LS + j0, av[a]);
 #pragma unroll
-      for (int q = 0; q < NQ; ++q) bv[q] = sB[j * NS + nc[q]];
+      for (int k = 0; k < 4; ++k) {
+        if (j0 + k >= jend) break;
+        float bv[NQ];
 #pragma unroll
-      for (int a = 0; a < 4; ++a)
+        for (int hh = 0; hh < HH; ++hh) lds_vec<VW>(sB + (j0 + k) * NS + n0[hh], bv + hh * VW);
 #pragma unroll
-        for (int q = 0; q < NQ; ++q) acc[a][q] = fmaf(av[a], bv[q], acc[a][q]);
+        for (int a = 0; a < 4; ++a)
+#pragma unroll
+          for (int q = 0; q < NQ; ++q) acc[a][q] = fmaf(av[a][k], bv[q], acc[a][q]);
+      }
     }
 #pragma unroll
     for (int a = 0; a < 4; ++a) {
-      const int i = t16 + 16 * a;
+      const int i = r0 + a;
       if (i < nvr) {
         float* dst = dC + ((row0 + i) * p.G + g) * N;
 #pragma unroll
-        for (int q = 0; q < NQ; ++q)
-          if (l16 + 16 * q < N) atomicAdd(dst + l16 + 16 * q, acc[a][q]);
+        for (int hh = 0; hh < HH; ++hh)
+          if (nown[hh]) atomic_add_vec<VW>(dst + n0[hh], acc[a] + hh * VW);
       }
     }
   }
 
   // <G, h_in>, for the chunk-end gradient of exp(cum_end) h_in.
   {
-    float s = 0.f;
+    float sacc = 0.f;
     for (int pp = warp; pp < P; pp += kBwdWarps)
-      for (int n = lane; n < N; n += 32) s = fmaf(sG[pp * NS + n], sH[pp * NS + n], s);
-    double d = (double)s;
+      for (int n = lane; n < N; n += 32) sacc = fmaf(sG[pp * NS + n], sH[pp * NS + n], sacc);
+    double d = (double)sacc;
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) d += __shfl_xor_sync(0xffffffffu, d, off);
     if (lane == 0) red[warp] = d;
   }
   __syncthreads();
 
-  // dL/dcum_s, then ddA_t = sum_{s >= t} dL/dcum_s over the chunk's steps.
-  if (threadIdx.x == 0) {
+  // dL/dcum_s, then ddA_t = sum_{s >= t} dL/dcum_s over the chunk's steps: warp 0, lane k
+  // holds steps 2k and 2k + 1 (l <= 64), and a shuffle scan forms the suffix sums.
+  if (warp == 0) {
     double gh = 0.0, qsum = 0.0;
+#pragma unroll
     for (int w = 0; w < kBwdWarps; ++w) gh += red[w];
-    for (int j = 0; j < Lr; ++j) qsum += qj[j];
-    double suffix = qsum + exp(cum_end) * gh;   // the chunk-end terms, on the last step
-    for (int s = l - 1; s >= 0; --s) {
-      for (int r = 0; r < R; ++r) {
-        const int i = s * R + r;
-        suffix += roww[i] - colw[i] + ein[i] - qj[i];
+    for (int j = lane; j < Lr; j += 32) qsum += qj[j];
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) qsum += __shfl_xor_sync(0xffffffffu, qsum, off);
+    double d2[2];
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const int st = 2 * lane + k;
+      double v = 0.0;
+      if (st < l) {
+        for (int r = 0; r < R; ++r) {
+          const int i = st * R + r;
+          v += roww[i] - colw[i] + ein[i] - qj[i];
+        }
+        if (st == l - 1) v += qsum + exp(cum_end) * gh;   // the chunk-end terms
       }
-      if (s < nv) ddA[(b * p.T + c * p.l + s) * p.H + h] = (float)suffix;
+      d2[k] = v;
     }
+    // suffix sums: first over the lanes above (inclusive scan from the top), then within a lane
+    double tot = d2[0] + d2[1], incl = tot;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const double v = __shfl_down_sync(0xffffffffu, incl, off);
+      if (lane + off < 32) incl += v;
+    }
+    const double above = incl - tot;   // steps 2 lane + 2 and later
+    const double s1 = above + d2[1], s0 = s1 + d2[0];
+    const int64_t base = (b * p.T + c * p.l) * p.H + h;
+    if (2 * lane < nv) ddA[base + (int64_t)(2 * lane) * p.H] = (float)s0;
+    if (2 * lane + 1 < nv) ddA[base + (int64_t)(2 * lane + 1) * p.H] = (float)s1;
   }
 }
 
@@ -561,7 +755,8 @@ ssd_status bwd_shape_status(const ssd_shape* s) {
   const ssd_status st = shape_status(s);
   if (st != SSD_OK) return st;
   if (s->has_theta != 0) return SSD_ERR_UNSUPPORTED;
-  if (s->mimo_rank > kBwdRows || s->headdim > kBwdMaxP || s->dstate > kBwdMaxN)
+  if (s->mimo_rank > kBwdRows || s->headdim > kBwdMaxP || s->dstate > kBwdMaxN ||
+      (s->dstate % 4) != 0)
     return SSD_ERR_UNSUPPORTED;
   const int64_t l = bwd_chunk_steps(s->mimo_rank), Lr = l * s->mimo_rank;
   const size_t lim = 227 * 1024;
@@ -601,7 +796,7 @@ cudaError_t bwd_launch_nq(const GenericParams& p, const float* dy, const float* 
   if (e != cudaSuccess) return e;
   bwd_chunk_state_kernel<T, NQ><<<grid, kBwdThreads, s1, st>>>(p, dy, dg);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  const int64_t n = p.batch * p.H * p.P * p.N;
+  const int64_t n = 2 * p.batch * p.H * p.P * p.N;
   bwd_carry_kernel<<<(unsigned)((n + kBwdThreads - 1) / kBwdThreads), kBwdThreads, 0, st>>>(
       p, dfinal, dg, dinit);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;

@@ -25,6 +25,10 @@ CASES = [
     wl.SSDConfig("bwd_mimo3_f32", 1, 50, 2, 16, 32, 64, 3, 2, "f32"),
     # one step
     wl.SSDConfig("bwd_one_step_f32", 1, 1, 2, 16, 16, 64, 2, 1, "f32"),
+    # R = 5 (12 steps = 60 rows per chunk), P = 48, N = 96: partial row and column tiles
+    wl.SSDConfig("bwd_mimo5_p48_n96_f32", 1, 40, 2, 48, 96, 64, 5, 1, "f32"),
+    # P = N = 20: two-wide column runs, odd tile edges, bf16
+    wl.SSDConfig("bwd_p20_n20_bf16", 1, 70, 4, 20, 20, 64, 1, 2, "bf16"),
 ]
 
 KEYS = ("dx", "ddA", "dB", "dC", "dinit")
@@ -109,7 +113,8 @@ def test_backward_rejections():
     for bad in (pkg.make_shape(1, 64, 2, 16, 16, 1, 1, 64, "f32", True),     # rotation
                 pkg.make_shape(1, 64, 2, 128, 16, 1, 1, 64, "f32", False),   # headdim > 64
                 pkg.make_shape(1, 64, 2, 16, 256, 1, 1, 64, "f32", False),   # dstate > 128
-                pkg.make_shape(1, 64, 2, 16, 16, 1, 128, 64, "f32", False)):  # rank > 64
+                pkg.make_shape(1, 64, 2, 16, 16, 1, 128, 64, "f32", False),  # rank > 64
+                pkg.make_shape(1, 64, 2, 16, 18, 1, 1, 64, "f32", False)):   # dstate % 4
         assert lib.ssd_backward_workspace_bytes(ctypes.byref(bad)) == 0
         st = lib.ssd_chunked_backward(ctypes.byref(bad), *([None] * 13), ctypes.c_size_t(0),
                                       None)
