@@ -145,15 +145,13 @@ __global__ void __launch_bounds__(kBwdThreads, 2)
   const int64_t g = h / (p.H / p.G);
   const int nv = bwd_steps(p, c), nvr = nv * R;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  bwd_cumsum(p.dA + (b * p.T + c * p.l) * p.H + h, p.H, l, nv, cum);
-  __syncthreads();
-  const double cum_end = cum[l - 1];
   const int64_t row0 = (b * p.T + c * p.l) * R;
   const T* xs = static_cast<const T*>(p.x);
   const T* Bs = static_cast<const T*>(p.B);
   const T* Cs = static_cast<const T*>(p.C);
   {
-    // each warp stages its 8 rows i = warp + 8 k: every global load first, then the stores
+    // each warp stages its 8 rows i = warp + 8 k: every global load first (before the prefix
+    // sums are waited for), then the scaled stores
     float xr[kRowsPerWarp][2], dr[kRowsPerWarp][2], br[kRowsPerWarp][4], cr[kRowsPerWarp][4];
 #pragma unroll
     for (int k = 0; k < kRowsPerWarp; ++k) {
@@ -175,6 +173,9 @@ __global__ void __launch_bounds__(kBwdThreads, 2)
         cr[k][u] = v ? ld_f32(Cs + bo + n) : 0.f;
       }
     }
+    bwd_cumsum(p.dA + (b * p.T + c * p.l) * p.H + h, p.H, l, nv, cum);
+    __syncthreads();
+    const double cum_end = cum[l - 1];
 #pragma unroll
     for (int k = 0; k < kRowsPerWarp; ++k) {
       const int i = warp + kBwdWarps * k;
@@ -239,7 +240,7 @@ __global__ void __launch_bounds__(kBwdThreads, 2)
       st_vec<VW>(dst + so + pp * N + n, ad[a] + hh * VW);
     }
   }
-  if (threadIdx.x == 0) p.cend[(b * p.nch + c) * p.H + h] = (float)cum_end;
+  if (threadIdx.x == 0) p.cend[(b * p.nch + c) * p.H + h] = (float)cum[l - 1];
 }
 
 // The carries across chunks, one thread per state element of one (b, h) and direction (the
