@@ -44,6 +44,8 @@ NCU_TRAFFIC_BYTES = {
     "mamba3_mimo_bf16": 1_353_165_824 + 253_219_328,       # ssd_fused_bf16_kernel<false>
     "long_rotation_f32": 3_937_626_368 + 788_668_672,      # simt_scan_kernel
     "selective_scan_f32": 71_228_672 + 6_168_320,          # ss_onepass_kernel (output pass)
+    # bwd_chunk_grad_kernel, captured at batch 1 and scaled by 4 (traffic grows with the batch)
+    "mamba2_backward_bf16": (191_535_616 + 23_637_248) * 4,
 }
 
 
