@@ -50,7 +50,7 @@ def _lib():
         lib.oracle_ssd_ex.restype = ctypes.c_int
         lib.oracle_ssd_ex.argtypes = [_D] * 8 + [_I64] * 8 + [ctypes.c_int]
         lib.oracle_ssd_backward_ex.restype = ctypes.c_int
-        lib.oracle_ssd_backward_ex.argtypes = [_D] * 12 + [_I64] * 8 + [ctypes.c_int]
+        lib.oracle_ssd_backward_ex.argtypes = [_D] * 14 + [_I64] * 8 + [ctypes.c_int]
         lib.oracle_ssd_rot_ex.restype = ctypes.c_int
         lib.oracle_ssd_rot_ex.argtypes = [_D] * 8 + [_I64] * 8 + [ctypes.c_int, _I64, ctypes.c_int]
         lib.oracle_ssd_trap_ex.restype = ctypes.c_int
@@ -99,20 +99,26 @@ def ssd(x, dA, B, C, theta=None, init_state=None, nthreads=None, mutation: int =
     return y, fin
 
 
-def ssd_backward(x, dA, B, C, dy, init_state=None, dfinal=None, nthreads=None,
+def ssd_backward(x, dA, B, C, dy, init_state=None, dfinal=None, theta=None, nthreads=None,
                  mutation: int = 0):
-    """Reverse mode of the unrotated SSD recurrence for the loss <dy, y> + <dfinal, final>.
-    Returns dict dx [b,T,R,H,P], ddA [b,T,H], dB, dC [b,T,R,G,N], dinit [b,H,P,N]."""
+    """Reverse mode of the SSD recurrence (rotated when theta [b,T,H,N/2] is given, interleaved
+    pairs) for the loss <dy, y> + <dfinal, final>.  Returns dict dx [b,T,R,H,P], ddA [b,T,H],
+    dB, dC [b,T,R,G,N], dinit [b,H,P,N] and, with theta, dtheta [b,T,H,N/2]."""
     x, dA, B, C, dy = (_f64(v) for v in (x, dA, B, C, dy))
-    init_state, dfinal = _f64(init_state), _f64(dfinal)
+    init_state, dfinal, theta = _f64(init_state), _f64(dfinal), _f64(theta)
     b, T, R, H, P = x.shape
     G, N = B.shape[3], B.shape[4]
     assert dy.shape == x.shape
+    if theta is not None:
+        assert theta.shape == (b, T, H, N // 2)
     out = {"dx": np.zeros_like(x), "ddA": np.zeros_like(dA), "dB": np.zeros_like(B),
            "dC": np.zeros_like(C), "dinit": np.zeros((b, H, P, N))}
-    rc = _lib().oracle_ssd_backward_ex(_ptr(x), _ptr(dA), _ptr(B), _ptr(C), _ptr(init_state),
-                                       _ptr(dy), _ptr(dfinal), _ptr(out["dx"]), _ptr(out["ddA"]),
-                                       _ptr(out["dB"]), _ptr(out["dC"]), _ptr(out["dinit"]),
+    if theta is not None:
+        out["dtheta"] = np.zeros_like(theta)
+    rc = _lib().oracle_ssd_backward_ex(_ptr(x), _ptr(dA), _ptr(B), _ptr(C), _ptr(theta),
+                                       _ptr(init_state), _ptr(dy), _ptr(dfinal), _ptr(out["dx"]),
+                                       _ptr(out["ddA"]), _ptr(out["dB"]), _ptr(out["dC"]),
+                                       _ptr(out.get("dtheta")), _ptr(out["dinit"]),
                                        b, T, R, H, G, P, N, nthreads or default_threads(),
                                        int(mutation))
     if rc != 0:
@@ -206,6 +212,7 @@ MUTATIONS_ROT = {
 MUTATIONS_BWD = {
     "dy_added_after_decay": 14,
     "ddA_without_decay_factor": 15,
+    "state_gradient_turned_forward": 16,
 }
 MUTATIONS_SS = {
     "no_skip": 7,

@@ -353,20 +353,23 @@ int oracle_ssd(const double* x, const double* dA, const double* B, const double*
 /* Backward of the (unrotated) SSD recurrence                                                */
 /* ---------------------------------------------------------------------------------------- */
 /*
- * Reverse mode of h_t = exp(dA_t) h_{t-1} + sum_r x_{t,r} (outer) B_{t,r}, y_{t,r} = C_{t,r} . h_t
+ * Reverse mode of h_t = exp(dA_t) R(theta_t) h_{t-1} + sum_r x_{t,r} (outer) B_{t,r},
+ * y_{t,r} = C_{t,r} . h_t (R(theta) = I when theta is NULL; interleaved pairs, all of dstate)
  * for the loss <dy, y> + <dfinal, h_{T-1}> (the backward the scan.py page asks a trainable scan
- * to have), per (b, h), walking t from T-1 down with g = dL/dh_t:
+ * to have), per (b, h), walking t from T-1 down with g = dL/dh_t and u_t = R(theta_t) h_{t-1}:
  *   g   += sum_r dy_{t,r} (outer) C_{t,r}            dC_{t,r} += h_t^T dy_{t,r}
- *   dx_{t,r} = g B_{t,r}     dB_{t,r} += g^T x_{t,r}   ddA_t = exp(dA_t) <g, h_{t-1}>
- *   g   <- exp(dA_t) g                                 dinit = g after t = 0.
+ *   dx_{t,r} = g B_{t,r}     dB_{t,r} += g^T x_{t,r}   ddA_t = exp(dA_t) <g, u_t>
+ *   dtheta_{t,k} = exp(dA_t) sum_p (g[p,2k+1] u_t[p,2k] - g[p,2k] u_t[p,2k+1])
+ *                  (the derivative of the turn of pair k is the quarter turn J u)
+ *   g   <- exp(dA_t) R(theta_t)^T g = exp(dA_t) R(-theta_t) g;   dinit = g after t = 0.
  * dB and dC sum over the heads of a group.  States are recomputed forward from checkpoints every
  * kCkpt steps, so memory stays O((T / kCkpt + kCkpt) P N) per problem.
  */
-enum { MUT_BWD_DY_AFTER_DECAY = 14, MUT_BWD_NO_DECAY_IN_DDA = 15 };
+enum { MUT_BWD_DY_AFTER_DECAY = 14, MUT_BWD_NO_DECAY_IN_DDA = 15, MUT_BWD_TURN_FORWARD = 16 };
 
 typedef struct {
-  const double *x, *dA, *B, *C, *init, *dy, *dfinal;
-  double *dx, *ddA, *dB, *dC, *dinit;
+  const double *x, *dA, *B, *C, *theta, *init, *dy, *dfinal;
+  double *dx, *ddA, *dB, *dC, *dtheta, *dinit;
   int64_t batch, T, R, H, G, P, N;
   int mutation;
   int64_t nthreads, tid;
@@ -375,13 +378,43 @@ typedef struct {
 
 #define ORACLE_CKPT 64
 
+/* Turns every interleaved pair (2k, 2k+1) of each of the P rows of v (P x N) by sign * th[k]. */
+static void bwd_turn(const double* th, int64_t P, int64_t N, double sign, double* v) {
+  for (int64_t k = 0; k < N / 2; ++k) {
+    const double c = cos(sign * th[k]), s = sin(sign * th[k]);
+    for (int64_t p = 0; p < P; ++p) {
+      double* vp = v + p * N;
+      const double e = vp[2 * k], o = vp[2 * k + 1];
+      vp[2 * k] = c * e - s * o;
+      vp[2 * k + 1] = s * e + c * o;
+    }
+  }
+}
+
+/* One step of the forward recurrence: hn = exp(dA_t) R(theta_t) hp + sum_r x_{t,r} B_{t,r}. */
+static void bwd_forward_step(const bwd_job* j, int64_t b, int64_t hh, int64_t g_, int64_t t,
+                             const double* hp, double* hn) {
+  const int64_t T = j->T, R = j->R, H = j->H, G = j->G, P = j->P, N = j->N;
+  const double a = exp(j->dA[(b * T + t) * H + hh]);
+  memcpy(hn, hp, sizeof(double) * P * N);
+  if (j->theta) bwd_turn(j->theta + ((b * T + t) * H + hh) * (N / 2), P, N, 1.0, hn);
+  for (int64_t p = 0; p < P; ++p)
+    for (int64_t n = 0; n < N; ++n) {
+      double w = 0.0;
+      for (int64_t r = 0; r < R; ++r)
+        w += j->x[(((b * T + t) * R + r) * H + hh) * P + p] *
+             j->B[(((b * T + t) * R + r) * G + g_) * N + n];
+      hn[p * N + n] = a * hn[p * N + n] + w;
+    }
+}
+
 static void bwd_one(const bwd_job* j, int64_t b, int64_t hh, double* ck, double* seg, double* g,
-                    double* dBl, double* dCl) {
+                    double* u, double* dBl, double* dCl) {
   const int64_t T = j->T, R = j->R, H = j->H, G = j->G, P = j->P, N = j->N, PN = P * N;
   const int64_t g_ = hh / (H / G);
   const int64_t nck = (T + ORACLE_CKPT - 1) / ORACLE_CKPT;
   /* forward pass keeping the state entering every checkpoint segment */
-  double* h = seg;   /* scratch row 0 of seg as the running state */
+  double* h = seg;   /* rows 0 and 1 of seg as the running state */
   if (j->init) {
     memcpy(h, j->init + ((b * H + hh) * P) * N, sizeof(double) * PN);
   } else {
@@ -389,15 +422,8 @@ static void bwd_one(const bwd_job* j, int64_t b, int64_t hh, double* ck, double*
   }
   for (int64_t t = 0; t < T; ++t) {
     if (t % ORACLE_CKPT == 0) memcpy(ck + (t / ORACLE_CKPT) * PN, h, sizeof(double) * PN);
-    const double a = exp(j->dA[(b * T + t) * H + hh]);
-    for (int64_t p = 0; p < P; ++p)
-      for (int64_t n = 0; n < N; ++n) {
-        double w = 0.0;
-        for (int64_t r = 0; r < R; ++r)
-          w += j->x[(((b * T + t) * R + r) * H + hh) * P + p] *
-               j->B[(((b * T + t) * R + r) * G + g_) * N + n];
-        h[p * N + n] = a * h[p * N + n] + w;
-      }
+    bwd_forward_step(j, b, hh, g_, t, h, seg + PN);
+    memcpy(h, seg + PN, sizeof(double) * PN);
   }
   if (j->dfinal) {
     memcpy(g, j->dfinal + ((b * H + hh) * P) * N, sizeof(double) * PN);
@@ -410,21 +436,11 @@ static void bwd_one(const bwd_job* j, int64_t b, int64_t hh, double* ck, double*
     const int64_t t0 = c * ORACLE_CKPT, t1 = (t0 + ORACLE_CKPT < T) ? t0 + ORACLE_CKPT : T;
     /* recompute the states h_{t0-1} .. h_{t1-1} into seg rows 0 .. (t1 - t0) */
     memcpy(seg, ck + c * PN, sizeof(double) * PN);
-    for (int64_t t = t0; t < t1; ++t) {
-      const double a = exp(j->dA[(b * T + t) * H + hh]);
-      const double* hp = seg + (t - t0) * PN;
-      double* hn = seg + (t - t0 + 1) * PN;
-      for (int64_t p = 0; p < P; ++p)
-        for (int64_t n = 0; n < N; ++n) {
-          double w = 0.0;
-          for (int64_t r = 0; r < R; ++r)
-            w += j->x[(((b * T + t) * R + r) * H + hh) * P + p] *
-                 j->B[(((b * T + t) * R + r) * G + g_) * N + n];
-          hn[p * N + n] = a * hp[p * N + n] + w;
-        }
-    }
+    for (int64_t t = t0; t < t1; ++t)
+      bwd_forward_step(j, b, hh, g_, t, seg + (t - t0) * PN, seg + (t - t0 + 1) * PN);
     for (int64_t t = t1 - 1; t >= t0; --t) {
       const double a = exp(j->dA[(b * T + t) * H + hh]);
+      const double* th = j->theta ? j->theta + ((b * T + t) * H + hh) * (N / 2) : NULL;
       const double* ht = seg + (t - t0 + 1) * PN;   /* h_t */
       const double* hprev = seg + (t - t0) * PN;    /* h_{t-1} */
       for (int64_t r = 0; r < R; ++r) {
@@ -453,10 +469,23 @@ static void bwd_one(const bwd_job* j, int64_t b, int64_t hh, double* ck, double*
           dBl[(t * R + r) * N + n] += s;
         }
       }
+      /* u_t = R(theta_t) h_{t-1}, the state the decay multiplies */
+      memcpy(u, hprev, sizeof(double) * PN);
+      if (th) bwd_turn(th, P, N, 1.0, u);
       double da = 0.0;
-      for (int64_t e = 0; e < PN; ++e) da += g[e] * hprev[e];
+      for (int64_t e = 0; e < PN; ++e) da += g[e] * u[e];
       j->ddA[(b * T + t) * H + hh] = (j->mutation == MUT_BWD_NO_DECAY_IN_DDA) ? da : a * da;
+      if (th && j->dtheta) {
+        double* dth = j->dtheta + ((b * T + t) * H + hh) * (N / 2);
+        for (int64_t k = 0; k < N / 2; ++k) {
+          double s = 0.0;
+          for (int64_t p = 0; p < P; ++p)
+            s += g[p * N + 2 * k + 1] * u[p * N + 2 * k] - g[p * N + 2 * k] * u[p * N + 2 * k + 1];
+          dth[k] = a * s;
+        }
+      }
       for (int64_t e = 0; e < PN; ++e) g[e] *= a;
+      if (th) bwd_turn(th, P, N, (j->mutation == MUT_BWD_TURN_FORWARD) ? 1.0 : -1.0, g);
       if (j->mutation == MUT_BWD_DY_AFTER_DECAY) {   /* the planted mistake: dy lands late */
         for (int64_t r = 0; r < R; ++r) {
           const double* dyv = j->dy + (((b * T + t) * R + r) * H + hh) * P;
@@ -485,33 +514,38 @@ static void* bwd_worker(void* arg) {
   double* ck = (double*)malloc(sizeof(double) * PN * (size_t)nck);
   double* seg = (double*)malloc(sizeof(double) * PN * (ORACLE_CKPT + 1));
   double* g = (double*)malloc(sizeof(double) * PN);
+  double* u = (double*)malloc(sizeof(double) * PN);
   double* dBl = (double*)malloc(sizeof(double) * j->T * j->R * j->N);
   double* dCl = (double*)malloc(sizeof(double) * j->T * j->R * j->N);
   void* rc = NULL;
-  if (!ck || !seg || !g || !dBl || !dCl) {
+  if (!ck || !seg || !g || !u || !dBl || !dCl) {
     rc = (void*)1;
   } else {
     for (int64_t idx = j->tid; idx < j->batch * j->H; idx += j->nthreads)
-      bwd_one(j, idx / j->H, idx % j->H, ck, seg, g, dBl, dCl);
+      bwd_one(j, idx / j->H, idx % j->H, ck, seg, g, u, dBl, dCl);
   }
   free(ck);
   free(seg);
   free(g);
+  free(u);
   free(dBl);
   free(dCl);
   return rc;
 }
 
-/* Backward of the unrotated SSD: dy [b,T,R,H,P] and dfinal [b,H,P,N] (nullable) in; dx, ddA,
- * dB, dC (zeroed here) and dinit (nullable) out.  Returns 0 or a negative error. */
+/* Backward of the SSD (rotated when theta [b,T,H,N/2] is given): dy [b,T,R,H,P] and dfinal
+ * [b,H,P,N] (nullable) in; dx, ddA, dB, dC (zeroed here), dtheta (nullable; needs theta) and
+ * dinit (nullable) out.  Returns 0 or a negative error. */
 int oracle_ssd_backward_ex(const double* x, const double* dA, const double* B, const double* C,
-                           const double* init_state, const double* dy, const double* dfinal,
-                           double* dx, double* ddA, double* dB, double* dC, double* dinit,
-                           int64_t batch, int64_t T, int64_t R, int64_t H, int64_t G, int64_t P,
-                           int64_t N, int64_t nthreads, int mutation) {
+                           const double* theta, const double* init_state, const double* dy,
+                           const double* dfinal, double* dx, double* ddA, double* dB, double* dC,
+                           double* dtheta, double* dinit, int64_t batch, int64_t T, int64_t R,
+                           int64_t H, int64_t G, int64_t P, int64_t N, int64_t nthreads,
+                           int mutation) {
   if (!x || !dA || !B || !C || !dy || !dx || !ddA || !dB || !dC) return -1;
   if (batch < 1 || T < 1 || R < 1 || H < 1 || G < 1 || P < 1 || N < 1) return -2;
   if (H % G != 0) return -3;
+  if (theta && (N % 2) != 0) return -4;
   memset(dB, 0, sizeof(double) * (size_t)(batch * T * R * G * N));
   memset(dC, 0, sizeof(double) * (size_t)(batch * T * R * G * N));
   const int64_t nt = clamp_threads(nthreads, batch * H);
@@ -524,8 +558,8 @@ int oracle_ssd_backward_ex(const double* x, const double* dA, const double* B, c
     return -5;
   }
   for (int64_t i = 0; i < nt; ++i) {
-    bwd_job jb = {x,  dA, B, C, init_state, dy, dfinal, dx,       ddA, dB, dC, dinit,
-                  batch, T, R, H, G, P, N, mutation, nt, i, &lock};
+    bwd_job jb = {x,   dA,  B,  C,  theta,  init_state, dy,    dfinal, dx, ddA, dB, dC,
+                  dtheta, dinit, batch, T, R, H, G, P, N, mutation, nt, i, &lock};
     jobs[i] = jb;
   }
   int rc = 0;

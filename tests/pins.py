@@ -394,29 +394,35 @@ def pin_backward_finite_differences(mutation=0):
     L = <dy, y> + <dfinal, final> and a random direction v of each input, (L(X + eps v) -
     L(X - eps v)) / (2 eps) must equal <dL/dX, v>.  MIMO ranks, a group shared by two heads
     (dB, dC summed over them), an initial state and a length that crosses the oracle's
-    64-step recompute checkpoint."""
+    64-step recompute checkpoint; once without and once with the rotation (dtheta too)."""
     res = []
-    x, dA, B, C, _, h0 = _problem(61, 2, 70, 2, 2, 1, 3, 4, init=True)
-    r = _rng(62)
-    dy = r.standard_normal(x.shape)
-    dfin = r.standard_normal(h0.shape)
-    g = oracle.ssd_backward(x, dA, B, C, dy, h0, dfin, mutation=mutation)
+    for rot in (False, True):
+        x, dA, B, C, th, h0 = _problem(61 + rot, 2, 70, 2, 2, 1, 3, 4, theta=rot, init=True)
+        r = _rng(62 + rot)
+        dy = r.standard_normal(x.shape)
+        dfin = r.standard_normal(h0.shape)
+        g = oracle.ssd_backward(x, dA, B, C, dy, h0, dfin, theta=th, mutation=mutation)
 
-    def loss(xx, aa, bb, cc, hh):
-        y, f = oracle.ssd(xx, aa, bb, cc, None, hh)
-        return float((dy * y).sum() + (dfin * f).sum())
+        def loss(xx, aa, bb, cc, hh, tt):
+            y, f = oracle.ssd(xx, aa, bb, cc, tt, hh)
+            return float((dy * y).sum() + (dfin * f).sum())
 
-    args = {"x": x, "ddA": dA, "dB": B, "dC": C, "dinit": h0}
-    order = ["x", "ddA", "dB", "dC", "dinit"]
-    eps = 1e-5
-    for name in order:
-        v = r.standard_normal(args[name].shape)
-        plus = [args[k] + (eps * v if k == name else 0) for k in order]
-        minus = [args[k] - (eps * v if k == name else 0) for k in order]
-        fd = (loss(*plus) - loss(*minus)) / (2 * eps)
-        gk = "dx" if name == "x" else name
-        an = float((g[gk] * v).sum())
-        res.append((f"fd_{gk}", abs(fd - an) / (1.0 + abs(fd)), 1e-7))
+        args = {"x": x, "ddA": dA, "dB": B, "dC": C, "dinit": h0, "dtheta": th}
+        order = ["x", "ddA", "dB", "dC", "dinit", "dtheta"]
+        eps = 1e-5
+        for name in order:
+            if args[name] is None:
+                continue
+            v = r.standard_normal(args[name].shape)
+            plus = [None if args[k] is None else args[k] + (eps * v if k == name else 0)
+                    for k in order]
+            minus = [None if args[k] is None else args[k] - (eps * v if k == name else 0)
+                     for k in order]
+            fd = (loss(*plus) - loss(*minus)) / (2 * eps)
+            gk = "dx" if name == "x" else name
+            an = float((g[gk] * v).sum())
+            tag = "rot_" if rot else ""
+            res.append((f"fd_{tag}{gk}", abs(fd - an) / (1.0 + abs(fd)), 1e-7))
     return res
 
 
