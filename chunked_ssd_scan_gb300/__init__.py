@@ -84,7 +84,7 @@ def load_library(path: Optional[str] = None):
     lib.ssd_backward_workspace_bytes.restype = ctypes.c_size_t
     lib.ssd_backward_workspace_bytes.argtypes = [SP]
     lib.ssd_chunked_backward.restype = ctypes.c_int
-    lib.ssd_chunked_backward.argtypes = [SP] + [_VP] * 13 + [ctypes.c_size_t, _VP]
+    lib.ssd_chunked_backward.argtypes = [SP] + [_VP] * 15 + [ctypes.c_size_t, _VP]
     lib.selective_scan_workspace_bytes.argtypes = [_I64] * 4
     lib.selective_scan_forward.restype = ctypes.c_int
     lib.selective_scan_forward.argtypes = [_VP] * 7 + [_I64] * 4 + [_VP, ctypes.c_size_t, _VP]
@@ -345,11 +345,13 @@ def ssd_backward_workspace_bytes(shape: ssd_shape) -> int:
 class SSDBackwardPlan:
     """Arguments of ``ssd_chunked_backward`` validated once, for repeated calls on the same
     buffers (the gradients are allocated here unless given).  dy [b,T,R,H,P] and dfinal
-    [b,H,P,N] are f32; every gradient is f32.  Calling the plan makes only the C call and
-    returns the dict dx, ddA, dB, dC, dinit (None unless return_dinit)."""
+    [b,H,P,N] are f32; theta [b,T,H,N/2] f32 selects the rotated form (and dtheta); every
+    gradient is f32.  Calling the plan makes only the C call and returns the dict dx, ddA, dB,
+    dC, dtheta (None without theta) and dinit (None unless return_dinit)."""
 
     def __init__(self, x: torch.Tensor, dA: torch.Tensor, B: torch.Tensor, C: torch.Tensor,
-                 dy: torch.Tensor, *, init_state: Optional[torch.Tensor] = None,
+                 dy: torch.Tensor, *, theta: Optional[torch.Tensor] = None,
+                 init_state: Optional[torch.Tensor] = None,
                  dfinal: Optional[torch.Tensor] = None, return_dinit: bool = True,
                  grads: Optional[dict] = None, workspace: Optional[torch.Tensor] = None,
                  stream=None):
@@ -364,11 +366,13 @@ class SSDBackwardPlan:
         _check_cuda("C", C, x.dtype, (b, T, R, G, N))
         _check_cuda("dA", dA, torch.float32, (b, T, H))
         _check_cuda("dy", dy, torch.float32, (b, T, R, H, P))
+        if theta is not None:
+            _check_cuda("theta", theta, torch.float32, (b, T, H, N // 2))
         if init_state is not None:
             _check_cuda("init_state", init_state, torch.float32, (b, H, P, N))
         if dfinal is not None:
             _check_cuda("dfinal", dfinal, torch.float32, (b, H, P, N))
-        self.shape = shape_of(x, B, 64, False)
+        self.shape = shape_of(x, B, 64, theta is not None)
         self._lib = load_library()
         need = int(self._lib.ssd_backward_workspace_bytes(ctypes.byref(self.shape)))
         if need == 0:
@@ -377,21 +381,22 @@ class SSDBackwardPlan:
             workspace = torch.zeros(need, dtype=torch.uint8, device=x.device)   # zero header
         _check_cuda("workspace", workspace, torch.uint8)
         shapes = {"dx": (b, T, R, H, P), "ddA": (b, T, H), "dB": (b, T, R, G, N),
-                  "dC": (b, T, R, G, N), "dinit": (b, H, P, N)}
+                  "dC": (b, T, R, G, N), "dtheta": (b, T, H, N // 2), "dinit": (b, H, P, N)}
         g = dict(grads or {})
         for k, shp in shapes.items():
-            if k == "dinit" and not return_dinit:
+            if (k == "dinit" and not return_dinit) or (k == "dtheta" and theta is None):
                 g[k] = None
                 continue
             if g.get(k) is None:
                 g[k] = torch.empty(shp, dtype=torch.float32, device=x.device)
             _check_cuda(k, g[k], torch.float32, shp)
-        self.inputs = (x, dA, B, C, dy, init_state, dfinal)
+        self.inputs = (x, dA, B, C, theta, dy, init_state, dfinal)
         self.grads, self.workspace = g, workspace
-        self._args = (ctypes.byref(self.shape), _ptr(x), _ptr(dA), _ptr(B), _ptr(C),
+        self._args = (ctypes.byref(self.shape), _ptr(x), _ptr(dA), _ptr(B), _ptr(C), _ptr(theta),
                       _ptr(init_state), _ptr(dy), _ptr(dfinal), _ptr(g["dx"]), _ptr(g["ddA"]),
-                      _ptr(g["dB"]), _ptr(g["dC"]), _ptr(g["dinit"]), _ptr(workspace),
-                      ctypes.c_size_t(workspace.numel()), _stream_handle(stream))
+                      _ptr(g["dB"]), _ptr(g["dC"]), _ptr(g["dtheta"]), _ptr(g["dinit"]),
+                      _ptr(workspace), ctypes.c_size_t(workspace.numel()),
+                      _stream_handle(stream))
         self._fn = self._lib.ssd_chunked_backward
 
     def __call__(self):
@@ -401,11 +406,12 @@ class SSDBackwardPlan:
         return self.grads
 
 
-def ssd_chunked_backward(x, dA, B, C, dy, *, init_state=None, dfinal=None,
+def ssd_chunked_backward(x, dA, B, C, dy, *, theta=None, init_state=None, dfinal=None,
                          return_dinit: bool = True, grads=None, workspace=None, stream=None):
-    """Gradients of <dy, y> + <dfinal, final_state> for the unrotated SSD forward, through
-    ``ssd_chunked_backward``.  Returns a dict of f32 tensors dx, ddA, dB, dC and dinit."""
-    return SSDBackwardPlan(x, dA, B, C, dy, init_state=init_state, dfinal=dfinal,
+    """Gradients of <dy, y> + <dfinal, final_state> for the SSD forward (rotated when theta is
+    given), through ``ssd_chunked_backward``.  Returns a dict of f32 tensors dx, ddA, dB, dC,
+    dtheta and dinit."""
+    return SSDBackwardPlan(x, dA, B, C, dy, theta=theta, init_state=init_state, dfinal=dfinal,
                            return_dinit=return_dinit, grads=grads, workspace=workspace,
                            stream=stream)()
 

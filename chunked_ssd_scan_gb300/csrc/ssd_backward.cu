@@ -128,7 +128,7 @@ size_t bwd_state_smem(int64_t Lr, int64_t P, int64_t N) {
 //   D_c[p][n] = sum_i exp(cum_i) dy_i[p] C_i[n]             (its outputs' part of dL/dh_in(c))
 // and the chunk's total log-decay cum_end.  Thread (t16, l16) owns rows p = 4 t16 + a and the
 // column tile of l16.
-template <typename T, int NQ>
+template <typename TX, typename TBC, int NQ>
 __global__ void __launch_bounds__(kBwdThreads, 2)
     bwd_chunk_state_kernel(GenericParams p, const float* __restrict__ dy,
                            float* __restrict__ dst) {
@@ -146,9 +146,9 @@ __global__ void __launch_bounds__(kBwdThreads, 2)
   const int nv = bwd_steps(p, c), nvr = nv * R;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t row0 = (b * p.T + c * p.l) * R;
-  const T* xs = static_cast<const T*>(p.x);
-  const T* Bs = static_cast<const T*>(p.B);
-  const T* Cs = static_cast<const T*>(p.C);
+  const TX* xs = static_cast<const TX*>(p.x);
+  const TBC* Bs = static_cast<const TBC*>(p.B);
+  const TBC* Cs = static_cast<const TBC*>(p.C);
   {
     // each warp stages its 8 rows i = warp + 8 k: every global load first (before the prefix
     // sums are waited for), then the scaled stores
@@ -246,14 +246,15 @@ __global__ void __launch_bounds__(kBwdThreads, 2)
 // The carries across chunks, one thread per state element of one (b, h) and direction (the
 // first b H P N threads forward, the rest backward), loading kCarryAhead chunks ahead of the
 // serial update:
-//   forward  (K4): states[c] <- h_in(c),  h_in(c+1) = exp(cend_c) h_in(c) + S_c,  h_in(0) = init
+//   forward  (K4): states[c] <- h_in(c),  h_in(c+1) = exp(cend_c) h_in(c) + S_c,  h_in(0) = init,
+//                  gfin <- the final state (when asked for)
 //   backward:      dg[c] <- G_c = dL/dh_in(c+1),  dL/dh_in(c) = exp(cend_c) G_c + D_c,
 //                  G_{nch-1} = dfinal, dinit = dL/dh_in(0).
 constexpr int kCarryAhead = 16;
 
 __global__ void __launch_bounds__(kBwdThreads)
     bwd_carry_kernel(GenericParams p, const float* __restrict__ dfinal, float* __restrict__ dg,
-                     float* __restrict__ dinit) {
+                     float* __restrict__ dinit, float* __restrict__ gfin) {
   const int64_t PN = p.P * p.N, n_el = p.batch * p.H * PN;
   int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (idx >= 2 * n_el) return;
@@ -283,6 +284,7 @@ __global__ void __launch_bounds__(kBwdThreads)
       }
   }
   if (back && dinit) dinit[idx] = v;
+  if (!back && gfin) gfin[idx] = v;   // the state after the last chunk
 }
 
 // Shared-memory row strides of bwd_chunk_grad_kernel: the row length rounded up to 4 plus 4, so
@@ -314,7 +316,7 @@ __device__ __forceinline__ float half_warp_sum(float v) {
 // with M = L o CB, A = L o DX, el_j = exp(cum_end - cum_j), e_i = exp(cum_i).  Thread
 // (t16, l16) owns output rows 4 t16 + a (a < 4) and, along P, columns l16 + 16 q, along N the
 // column tile of l16 (ColTile); products whose reduction runs along a row load 4 k at a time.
-template <typename T, int NQ>
+template <typename TX, typename TBC, int NQ>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     bwd_chunk_grad_kernel(GenericParams p, const float* __restrict__ dy,
                           const float* __restrict__ dg, float* __restrict__ dx,
@@ -346,9 +348,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const int nv = bwd_steps(p, c), nvr = nv * R;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t row0 = (b * p.T + c * p.l) * R;
-  const T* xs = static_cast<const T*>(p.x);
-  const T* Bs = static_cast<const T*>(p.B);
-  const T* Cs = static_cast<const T*>(p.C);
+  const TX* xs = static_cast<const TX*>(p.x);
+  const TBC* Bs = static_cast<const TBC*>(p.B);
+  const TBC* Cs = static_cast<const TBC*>(p.C);
 
   bwd_cumsum(p.dA + (b * p.T + c * p.l) * p.H + h, p.H, l, nv, cum);
   // Rows first (group 0: dy by async copy), then h_in and G (group 1), which are needed only
@@ -745,17 +747,199 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   }
 }
 
+// ---------------------------------------------------------------------------------------------
+// Rotation.  With Phi_t = sum_{u <= t} theta_u (per head and pair) the rotated recurrence is the
+// plain one on B~ = R(-Phi_t) B, C~ = R(-Phi_t) C (per head) in the absorbed frame
+// g_t = R(-Phi_t) h_t (scan.py page, THE TRICK), with h_{T-1} = R(Phi_{T-1}) g_{T-1}.  The plain
+// backward runs on (x, dA, B~, C~, init) with dL/dg_{T-1} = R(-Phi_{T-1}) dfinal, and the chain
+// rule takes its dB~, dC~ back:
+//   dB = R(Phi) dB~, dC = R(Phi) dC~ (summed over the heads of a group);
+//   dL/dPhi_t[k] = sum over the step's rows of (dB~_0 B~_1 - dB~_1 B~_0 + dC~_0 C~_1 - dC~_1 C~_0)
+//                  (+ sum_p (dfinal_1 h_0 - dfinal_0 h_1) of the final state at t = T-1),
+// since d R(-phi) v / d phi = -J R(-phi) v and d R(phi) v / d phi = J R(phi) v with J the quarter
+// turn; dtheta_t = sum_{t' >= t} dL/dPhi_{t'}.
+constexpr double kBwdTwoPi = 6.283185307179586476925286766559;
+constexpr int kRotLanes = 32, kRotRows = 8;
+
+__device__ __forceinline__ float bwd_reduce_angle(double a) {
+  return (float)(a - kBwdTwoPi * rint(a * (1.0 / kBwdTwoPi)));
+}
+
+unsigned bwd_blocks(int64_t n) {
+  return (unsigned)(n < 1 ? 1 : (n > 0x7fffffff ? 0x7fffffff : n));
+}
+
+// Phi_t of every step, reduced to [-pi, pi], from the chunk-start angles: one thread per
+// (batch, chunk, head, pair), pairs fastest.
+__global__ void __launch_bounds__(kBwdThreads)
+    bwd_phi_steps_kernel(GenericParams p, float* __restrict__ phiT) {
+  const int64_t K = p.N / 2;
+  const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= p.batch * p.nch * p.H * K) return;
+  const int64_t k = idx % K, h = (idx / K) % p.H, c = (idx / (K * p.H)) % p.nch;
+  const int64_t b = idx / (K * p.H * p.nch);
+  double acc = p.phi[((b * (p.nch + 1) + c) * p.H + h) * K + k];
+  const int nv = bwd_steps(p, c);
+  const int64_t t0 = b * p.T + c * p.l;
+  for (int t = 0; t < nv; ++t) {
+    const int64_t o = ((t0 + t) * p.H + h) * K + k;
+    acc += (double)__ldg(p.theta + o);
+    phiT[o] = bwd_reduce_angle(acc);
+  }
+}
+
+// B~ = R(-Phi_t) B and C~ = R(-Phi_t) C per head, fp32: one block per step.
+template <typename T>
+__global__ void __launch_bounds__(kRotLanes * kRotRows)
+    bwd_rot_bc_kernel(const T* __restrict__ B, const T* __restrict__ C,
+                      const float* __restrict__ phiT, float* __restrict__ Bt,
+                      float* __restrict__ Ct, int64_t steps, int64_t R, int64_t H, int64_t G,
+                      int64_t N) {
+  const int64_t K = N / 2, hpg = H / G;
+  for (int64_t bt = blockIdx.x; bt < steps; bt += gridDim.x) {
+    for (int64_t r = 0; r < R; ++r) {
+      for (int64_t h = threadIdx.y; h < H; h += kRotRows) {
+        const int64_t src = ((bt * R + r) * G + h / hpg) * N, dst = ((bt * R + r) * H + h) * N;
+        for (int64_t k = threadIdx.x; k < K; k += kRotLanes) {
+          float sn, cs;
+          sincosf(phiT[(bt * H + h) * K + k], &sn, &cs);
+          const float b0 = ld_f32(B + src + 2 * k), b1 = ld_f32(B + src + 2 * k + 1);
+          const float c0 = ld_f32(C + src + 2 * k), c1 = ld_f32(C + src + 2 * k + 1);
+          Bt[dst + 2 * k] = cs * b0 + sn * b1;
+          Bt[dst + 2 * k + 1] = cs * b1 - sn * b0;
+          Ct[dst + 2 * k] = cs * c0 + sn * c1;
+          Ct[dst + 2 * k + 1] = cs * c1 - sn * c0;
+        }
+      }
+    }
+  }
+}
+
+// dL/dg_{T-1} = R(-Phi_{T-1}) dfinal: one thread per (batch, head, p, pair).
+__global__ void __launch_bounds__(kBwdThreads)
+    bwd_rot_dfinal_kernel(GenericParams p, const float* __restrict__ dfinal,
+                          float* __restrict__ dfin_t) {
+  const int64_t K = p.N / 2;
+  const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= p.batch * p.H * p.P * K) return;
+  const int64_t k = idx % K, bh = idx / (K * p.P);
+  const int64_t b = bh / p.H, h = bh % p.H;
+  float sn, cs;
+  sincosf(bwd_reduce_angle(p.phi[((b * (p.nch + 1) + p.nch) * p.H + h) * K + k]), &sn, &cs);
+  const float d0 = dfinal[2 * idx], d1 = dfinal[2 * idx + 1];
+  dfin_t[2 * idx] = cs * d0 + sn * d1;
+  dfin_t[2 * idx + 1] = cs * d1 - sn * d0;
+}
+
+// Per step (one block): dB and dC per group from the heads' dB~, dC~ turned back by +Phi, and
+// dL/dPhi_t per (head, pair) into dphi.
+__global__ void __launch_bounds__(kRotLanes * kRotRows)
+    bwd_rot_grad_kernel(const float* __restrict__ Bt, const float* __restrict__ Ct,
+                        const float* __restrict__ dBt, const float* __restrict__ dCt,
+                        const float* __restrict__ phiT, float* __restrict__ dB,
+                        float* __restrict__ dC, float* __restrict__ dphi, int64_t steps,
+                        int64_t R, int64_t H, int64_t G, int64_t N) {
+  const int64_t K = N / 2, hpg = H / G;
+  for (int64_t bt = blockIdx.x; bt < steps; bt += gridDim.x) {
+    for (int64_t h = threadIdx.y; h < H; h += kRotRows) {
+      for (int64_t k = threadIdx.x; k < K; k += kRotLanes) {
+        float s = 0.f;
+        for (int64_t r = 0; r < R; ++r) {
+          const int64_t o = ((bt * R + r) * H + h) * N + 2 * k;
+          s += dBt[o] * Bt[o + 1] - dBt[o + 1] * Bt[o] + dCt[o] * Ct[o + 1] - dCt[o + 1] * Ct[o];
+        }
+        dphi[(bt * H + h) * K + k] = s;
+      }
+    }
+    for (int64_t r = 0; r < R; ++r) {
+      for (int64_t g = threadIdx.y; g < G; g += kRotRows) {
+        for (int64_t k = threadIdx.x; k < K; k += kRotLanes) {
+          float b0 = 0.f, b1 = 0.f, c0 = 0.f, c1 = 0.f;
+          for (int64_t h = g * hpg; h < (g + 1) * hpg; ++h) {
+            float sn, cs;
+            sincosf(phiT[(bt * H + h) * K + k], &sn, &cs);
+            const int64_t o = ((bt * R + r) * H + h) * N + 2 * k;
+            const float e0 = dBt[o], e1 = dBt[o + 1], f0 = dCt[o], f1 = dCt[o + 1];
+            b0 += cs * e0 - sn * e1;
+            b1 += sn * e0 + cs * e1;
+            c0 += cs * f0 - sn * f1;
+            c1 += sn * f0 + cs * f1;
+          }
+          const int64_t o = ((bt * R + r) * G + g) * N + 2 * k;
+          dB[o] = b0;
+          dB[o + 1] = b1;
+          dC[o] = c0;
+          dC[o + 1] = c1;
+        }
+      }
+    }
+  }
+}
+
+// Per (batch, chunk, head, pair): the chunk's sum of dL/dPhi (fp64).
+__global__ void __launch_bounds__(kBwdThreads)
+    bwd_dphi_chunk_sum_kernel(GenericParams p, const float* __restrict__ dphi,
+                              double* __restrict__ csum) {
+  const int64_t K = p.N / 2;
+  const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= p.batch * p.nch * p.H * K) return;
+  const int64_t k = idx % K, h = (idx / K) % p.H, c = (idx / (K * p.H)) % p.nch;
+  const int64_t b = idx / (K * p.H * p.nch);
+  const int nv = bwd_steps(p, c);
+  const int64_t t0 = b * p.T + c * p.l;
+  double s = 0.0;
+  for (int t = 0; t < nv; ++t) s += (double)dphi[((t0 + t) * p.H + h) * K + k];
+  csum[idx] = s;
+}
+
+// dtheta_t = sum_{t' >= t} dL/dPhi_{t'}: the later chunks' sums, the final-state term
+// sum_p (dfinal_1 h_0 - dfinal_0 h_1) with h = R(Phi_{T-1}) g_{T-1}, then the chunk backwards.
+__global__ void __launch_bounds__(kBwdThreads)
+    bwd_dtheta_kernel(GenericParams p, const float* __restrict__ dphi,
+                      const double* __restrict__ csum, const float* __restrict__ dfinal,
+                      const float* __restrict__ gfin, float* __restrict__ dtheta) {
+  const int64_t K = p.N / 2;
+  const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= p.batch * p.nch * p.H * K) return;
+  const int64_t k = idx % K, h = (idx / K) % p.H, c = (idx / (K * p.H)) % p.nch;
+  const int64_t b = idx / (K * p.H * p.nch);
+  double acc = 0.0;
+  for (int64_t c2 = c + 1; c2 < p.nch; ++c2) acc += csum[((b * p.nch + c2) * p.H + h) * K + k];
+  if (dfinal) {
+    float sn, cs;
+    sincosf(bwd_reduce_angle(p.phi[((b * (p.nch + 1) + p.nch) * p.H + h) * K + k]), &sn, &cs);
+    double f = 0.0;
+    for (int64_t pp = 0; pp < p.P; ++pp) {
+      const int64_t o = ((b * p.H + h) * p.P + pp) * p.N + 2 * k;
+      const float g0 = gfin[o], g1 = gfin[o + 1];
+      const float h0 = cs * g0 - sn * g1, h1 = sn * g0 + cs * g1;
+      f += (double)(dfinal[o + 1] * h0 - dfinal[o] * h1);
+    }
+    acc += f;
+  }
+  const int nv = bwd_steps(p, c);
+  const int64_t t0 = b * p.T + c * p.l;
+  for (int t = nv - 1; t >= 0; --t) {
+    const int64_t o = ((t0 + t) * p.H + h) * K + k;
+    acc += (double)dphi[o];
+    dtheta[o] = (float)acc;
+  }
+}
+
 // Fused rows per backward chunk: 64 / R steps of R rows.
 int64_t bwd_chunk_steps(int64_t R) { return R >= kBwdRows ? 1 : kBwdRows / R; }
 
 struct BwdLayout {
-  size_t states = 0, cend = 0, dg = 0, total = 0;
+  size_t states = 0, cend = 0, dg = 0;
+  // rotation only
+  size_t phi = 0, phisum = 0, phiT = 0, Bt = 0, Ct = 0, dBt = 0, dCt = 0, dfin = 0, gfin = 0,
+         dphi = 0, csum = 0;
+  size_t total = 0;
 };
 
 ssd_status bwd_shape_status(const ssd_shape* s) {
   const ssd_status st = shape_status(s);
   if (st != SSD_OK) return st;
-  if (s->has_theta != 0) return SSD_ERR_UNSUPPORTED;
   if (s->mimo_rank > kBwdRows || s->headdim > kBwdMaxP || s->dstate > kBwdMaxN ||
       (s->dstate % 4) != 0)
     return SSD_ERR_UNSUPPORTED;
@@ -770,54 +954,137 @@ ssd_status bwd_shape_status(const ssd_shape* s) {
 BwdLayout bwd_layout(const ssd_shape* s) {
   const int64_t l = bwd_chunk_steps(s->mimo_rank);
   const int64_t nch = (s->seqlen + l - 1) / l;
-  const size_t st = sizeof(float) * (size_t)(s->batch * nch * s->nheads * s->headdim * s->dstate);
+  const size_t b = (size_t)s->batch, T = (size_t)s->seqlen, R = (size_t)s->mimo_rank;
+  const size_t H = (size_t)s->nheads, P = (size_t)s->headdim, N = (size_t)s->dstate, K = N / 2;
+  const size_t st = sizeof(float) * b * (size_t)nch * H * P * N;
   BwdLayout L;
   size_t off = sizeof(WsHeader);
-  L.states = off;
-  off = align_up(off + st, kWsAlign);
-  L.cend = off;
-  off = align_up(off + sizeof(float) * (size_t)(s->batch * nch * s->nheads), kWsAlign);
-  L.dg = off;
-  off = align_up(off + st, kWsAlign);
+  auto take = [&](size_t bytes) {
+    const size_t at = off;
+    off = align_up(off + bytes, kWsAlign);
+    return at;
+  };
+  L.states = take(st);
+  L.cend = take(sizeof(float) * b * (size_t)nch * H);
+  L.dg = take(st);
+  if (s->has_theta) {
+    L.phi = take(sizeof(double) * b * (size_t)(nch + 1) * H * K);
+    L.phisum = take(sizeof(double) * b * (size_t)nch * H * K);
+    L.phiT = take(sizeof(float) * b * T * H * K);
+    const size_t bc = sizeof(float) * b * T * R * H * N;
+    L.Bt = take(bc);
+    L.Ct = take(bc);
+    L.dBt = take(bc);
+    L.dCt = take(bc);
+    L.dfin = take(sizeof(float) * b * H * P * N);
+    L.gfin = take(sizeof(float) * b * H * P * N);
+    L.dphi = take(sizeof(float) * b * T * H * K);
+    L.csum = take(sizeof(double) * b * (size_t)nch * H * K);
+  }
   L.total = off;
   return L;
 }
 
 bool al16_or_null(const void* q) { return q == nullptr || aligned16(q); }
 
-template <typename T, int NQ>
+template <typename TX, typename TBC, int NQ>
 cudaError_t bwd_launch_nq(const GenericParams& p, const float* dy, const float* dfinal,
                           float* dx, float* ddA, float* dB, float* dC, float* dinit, float* dg,
-                          cudaStream_t st) {
+                          float* gfin, cudaStream_t st) {
   const int64_t Lr = p.l * p.R;
   const dim3 grid((unsigned)p.nch, (unsigned)p.H, (unsigned)p.batch);
   const size_t s1 = bwd_state_smem(Lr, p.P, p.N);
-  cudaError_t e = cudaFuncSetAttribute(bwd_chunk_state_kernel<T, NQ>,
+  cudaError_t e = cudaFuncSetAttribute(bwd_chunk_state_kernel<TX, TBC, NQ>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s1);
   if (e != cudaSuccess) return e;
-  bwd_chunk_state_kernel<T, NQ><<<grid, kBwdThreads, s1, st>>>(p, dy, dg);
+  bwd_chunk_state_kernel<TX, TBC, NQ><<<grid, kBwdThreads, s1, st>>>(p, dy, dg);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   const int64_t n = 2 * p.batch * p.H * p.P * p.N;
   bwd_carry_kernel<<<(unsigned)((n + kBwdThreads - 1) / kBwdThreads), kBwdThreads, 0, st>>>(
-      p, dfinal, dg, dinit);
+      p, dfinal, dg, dinit, gfin);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   const size_t s2 = bwd_grad_smem(Lr, p.P, p.N);
-  e = cudaFuncSetAttribute(bwd_chunk_grad_kernel<T, NQ>,
+  e = cudaFuncSetAttribute(bwd_chunk_grad_kernel<TX, TBC, NQ>,
                            cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s2);
   if (e != cudaSuccess) return e;
-  bwd_chunk_grad_kernel<T, NQ><<<grid, kBwdThreads, s2, st>>>(p, dy, dg, dx, ddA, dB, dC);
+  bwd_chunk_grad_kernel<TX, TBC, NQ><<<grid, kBwdThreads, s2, st>>>(p, dy, dg, dx, ddA, dB, dC);
   return cudaGetLastError();
 }
 
 // Column tiles of 16 state dims: N <= 16, 32, 64 or 128.
-template <typename T>
+template <typename TX, typename TBC>
 cudaError_t bwd_launch(const GenericParams& p, const float* dy, const float* dfinal, float* dx,
-                       float* ddA, float* dB, float* dC, float* dinit, float* dg,
+                       float* ddA, float* dB, float* dC, float* dinit, float* dg, float* gfin,
                        cudaStream_t st) {
-  if (p.N <= 16) return bwd_launch_nq<T, 1>(p, dy, dfinal, dx, ddA, dB, dC, dinit, dg, st);
-  if (p.N <= 32) return bwd_launch_nq<T, 2>(p, dy, dfinal, dx, ddA, dB, dC, dinit, dg, st);
-  if (p.N <= 64) return bwd_launch_nq<T, 4>(p, dy, dfinal, dx, ddA, dB, dC, dinit, dg, st);
-  return bwd_launch_nq<T, 8>(p, dy, dfinal, dx, ddA, dB, dC, dinit, dg, st);
+  if (p.N <= 16)
+    return bwd_launch_nq<TX, TBC, 1>(p, dy, dfinal, dx, ddA, dB, dC, dinit, dg, gfin, st);
+  if (p.N <= 32)
+    return bwd_launch_nq<TX, TBC, 2>(p, dy, dfinal, dx, ddA, dB, dC, dinit, dg, gfin, st);
+  if (p.N <= 64)
+    return bwd_launch_nq<TX, TBC, 4>(p, dy, dfinal, dx, ddA, dB, dC, dinit, dg, gfin, st);
+  return bwd_launch_nq<TX, TBC, 8>(p, dy, dfinal, dx, ddA, dB, dC, dinit, dg, gfin, st);
+}
+
+// The rotated backward: angles, the absorbed-frame B~, C~ and dL/dg_{T-1}, the plain backward on
+// them (dB~, dC~ into the workspace), then dB, dC, dtheta by the chain rule.
+cudaError_t bwd_rotated(GenericParams p, const ssd_shape* s, const BwdLayout& lay, char* ws,
+                        const float* dy, const float* dfinal, float* dx, float* ddA, float* dB,
+                        float* dC, float* dtheta, float* dinit, float* dg, cudaStream_t st) {
+  const int64_t K = p.N / 2, steps = p.batch * p.T;
+  p.phi = reinterpret_cast<double*>(ws + lay.phi);
+  p.phisum = reinterpret_cast<double*>(ws + lay.phisum);
+  float* phiT = reinterpret_cast<float*>(ws + lay.phiT);
+  float* Bt = reinterpret_cast<float*>(ws + lay.Bt);
+  float* Ct = reinterpret_cast<float*>(ws + lay.Ct);
+  float* dBt = reinterpret_cast<float*>(ws + lay.dBt);
+  float* dCt = reinterpret_cast<float*>(ws + lay.dCt);
+  float* dfin_t = dfinal ? reinterpret_cast<float*>(ws + lay.dfin) : nullptr;
+  float* gfin = reinterpret_cast<float*>(ws + lay.gfin);
+  float* dphi = reinterpret_cast<float*>(ws + lay.dphi);
+  double* csum = reinterpret_cast<double*>(ws + lay.csum);
+  cudaError_t e = generic_phi(p, st);
+  if (e != cudaSuccess) return e;
+  const int64_t nk = p.batch * p.nch * p.H * K;
+  bwd_phi_steps_kernel<<<bwd_blocks((nk + kBwdThreads - 1) / kBwdThreads), kBwdThreads, 0, st>>>(
+      p, phiT);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  const dim3 blk(kRotLanes, kRotRows);
+  if (s->io_dtype == SSD_BF16) {
+    bwd_rot_bc_kernel<__nv_bfloat16><<<bwd_blocks(steps), blk, 0, st>>>(
+        static_cast<const __nv_bfloat16*>(p.B), static_cast<const __nv_bfloat16*>(p.C), phiT, Bt,
+        Ct, steps, p.R, p.H, p.G, p.N);
+  } else {
+    bwd_rot_bc_kernel<float><<<bwd_blocks(steps), blk, 0, st>>>(
+        static_cast<const float*>(p.B), static_cast<const float*>(p.C), phiT, Bt, Ct, steps, p.R,
+        p.H, p.G, p.N);
+  }
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if (dfinal) {
+    const int64_t nf = p.batch * p.H * p.P * K;
+    bwd_rot_dfinal_kernel<<<bwd_blocks((nf + kBwdThreads - 1) / kBwdThreads), kBwdThreads, 0,
+                            st>>>(p, dfinal, dfin_t);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  const size_t bc = sizeof(float) * (size_t)(steps * p.R * p.H * p.N);
+  if ((e = cudaMemsetAsync(dBt, 0, bc, st)) != cudaSuccess) return e;
+  if ((e = cudaMemsetAsync(dCt, 0, bc, st)) != cudaSuccess) return e;
+  GenericParams q = p;   // the plain problem in the absorbed frame: fp32 B~, C~, one group per head
+  q.B = Bt;
+  q.C = Ct;
+  q.G = p.H;
+  q.theta = nullptr;
+  e = s->io_dtype == SSD_BF16
+          ? bwd_launch<__nv_bfloat16, float>(q, dy, dfin_t, dx, ddA, dBt, dCt, dinit, dg, gfin, st)
+          : bwd_launch<float, float>(q, dy, dfin_t, dx, ddA, dBt, dCt, dinit, dg, gfin, st);
+  if (e != cudaSuccess) return e;
+  bwd_rot_grad_kernel<<<bwd_blocks(steps), blk, 0, st>>>(Bt, Ct, dBt, dCt, phiT, dB, dC, dphi,
+                                                          steps, p.R, p.H, p.G, p.N);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  const unsigned gk = bwd_blocks((nk + kBwdThreads - 1) / kBwdThreads);
+  bwd_dphi_chunk_sum_kernel<<<gk, kBwdThreads, 0, st>>>(p, dphi, csum);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  bwd_dtheta_kernel<<<gk, kBwdThreads, 0, st>>>(p, dphi, csum, dfinal, gfin, dtheta);
+  return cudaGetLastError();
 }
 
 }  // namespace
@@ -833,14 +1100,17 @@ size_t ssd_backward_workspace_bytes(const ssd_shape* shape) {
 }
 
 ssd_status ssd_chunked_backward(const ssd_shape* shape, const void* x, const float* dA,
-                                const void* B, const void* C, const float* init_state,
-                                const float* dy, const float* dfinal, float* dx, float* ddA,
-                                float* dB, float* dC, float* dinit, void* workspace,
-                                size_t workspace_bytes, void* stream) {
+                                const void* B, const void* C, const float* theta,
+                                const float* init_state, const float* dy, const float* dfinal,
+                                float* dx, float* ddA, float* dB, float* dC, float* dtheta,
+                                float* dinit, void* workspace, size_t workspace_bytes,
+                                void* stream) {
   const ssd_status vs = bwd_shape_status(shape);
   if (vs != SSD_OK) return vs;
   if (!x || !dA || !B || !C || !dy || !dx || !ddA || !dB || !dC) return SSD_ERR_INVALID_ARG;
-  const void* ptrs[] = {x, dA, B, C, init_state, dy, dfinal, dx, ddA, dB, dC, dinit};
+  const bool rot = shape->has_theta != 0;
+  if (rot != (theta != nullptr) || rot != (dtheta != nullptr)) return SSD_ERR_INVALID_ARG;
+  const void* ptrs[] = {x, dA, B, C, theta, init_state, dy, dfinal, dx, ddA, dB, dC, dtheta, dinit};
   for (const void* q : ptrs)
     if (!al16_or_null(q)) return SSD_ERR_INVALID_ARG;
   const BwdLayout lay = bwd_layout(shape);
@@ -857,6 +1127,7 @@ ssd_status ssd_chunked_backward(const ssd_shape* shape, const void* x, const flo
   p.dA = dA;
   p.B = B;
   p.C = C;
+  p.theta = theta;
   p.init = init_state;
   p.batch = shape->batch;
   p.T = shape->seqlen;
@@ -872,12 +1143,18 @@ ssd_status ssd_chunked_backward(const ssd_shape* shape, const void* x, const flo
   p.hdr = reinterpret_cast<WsHeader*>(ws);
   float* dg = reinterpret_cast<float*>(ws + lay.dg);
 
-  const size_t bc = sizeof(float) * (size_t)(p.batch * p.T * p.R * p.G * p.N);
-  if (cudaMemsetAsync(dB, 0, bc, st) != cudaSuccess || cudaMemsetAsync(dC, 0, bc, st) != cudaSuccess)
-    return SSD_ERR_CUDA;
-  const cudaError_t e =
-      bf16 ? bwd_launch<__nv_bfloat16>(p, dy, dfinal, dx, ddA, dB, dC, dinit, dg, st)
-           : bwd_launch<float>(p, dy, dfinal, dx, ddA, dB, dC, dinit, dg, st);
+  cudaError_t e;
+  if (rot) {
+    e = bwd_rotated(p, shape, lay, ws, dy, dfinal, dx, ddA, dB, dC, dtheta, dinit, dg, st);
+  } else {
+    const size_t bc = sizeof(float) * (size_t)(p.batch * p.T * p.R * p.G * p.N);
+    if (cudaMemsetAsync(dB, 0, bc, st) != cudaSuccess ||
+        cudaMemsetAsync(dC, 0, bc, st) != cudaSuccess)
+      return SSD_ERR_CUDA;
+    e = bf16 ? bwd_launch<__nv_bfloat16, __nv_bfloat16>(p, dy, dfinal, dx, ddA, dB, dC, dinit, dg,
+                                                        nullptr, st)
+             : bwd_launch<float, float>(p, dy, dfinal, dx, ddA, dB, dC, dinit, dg, nullptr, st);
+  }
   return e == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
 }
 

@@ -173,27 +173,33 @@ ssd_status ssd_rotation_variant_forward(const ssd_shape* shape, int64_t rope_dim
 size_t ssd_backward_workspace_bytes(const ssd_shape* shape);
 
 /*
- * Reverse mode of the unrotated SSD forward (scan.py page: a scan that can be trained; the
- * moments.rs page's memory model of keeping chunk-boundary states and recomputing inside a
- * chunk).  For the loss L = <dy, y> + <dfinal, final_state> of ssd_chunked_forward on the same
- * inputs (has_theta must be 0), it writes
+ * Reverse mode of the SSD forward (scan.py page: a scan that can be trained, its verify()
+ * differentiating the rotated Mamba-3 scan; the moments.rs page's memory model of keeping
+ * chunk-boundary states and recomputing inside a chunk).  For the loss
+ * L = <dy, y> + <dfinal, final_state> of ssd_chunked_forward on the same inputs it writes
  *   dx [b,T,R,H,P] = dL/dx,  ddA [b,T,H] = dL/ddA,  dB, dC [b,T,R,G,N] = dL/dB, dL/dC (summed over
- *   the heads of a group),  dinit [b,H,P,N] = dL/dinit_state (may be NULL: not written).
+ *   the heads of a group),  dtheta [b,T,H,N/2] = dL/dtheta (has_theta = 1 only; NULL otherwise),
+ *   dinit [b,H,P,N] = dL/dinit_state (may be NULL: not written).
  * dy [b,T,R,H,P] and dfinal [b,H,P,N] (NULL = zero) are device f32; x, B, C in io_dtype as for
- * the forward; dA, init_state (NULL = zeros) f32; every gradient is device f32.  All pointers
- * 16-byte aligned, outputs not aliasing inputs.  The call recomputes the chunk-input states
- * (64 fused rows per chunk, i.e. 64/R steps, whatever shape->chunk_len says; seqlen need not be a
- * multiple), carries dL/dstate backwards across chunks, and forms each chunk's gradients from
- * its 64 x 64 pairwise products, all in fp32 on CUDA cores with the in-chunk log-decay sums in
- * fp64.  Limits: mimo_rank <= 64, headdim <= 64, dstate <= 128 (else UNSUPPORTED).  dB and dC
- * are zeroed by the call and accumulated atomically, so their low bits can vary between runs
- * when H/G > 1.  Asynchrony, workspace and errors as ssd_chunked_forward.
+ * the forward; dA, theta, init_state (NULL = zeros) f32; every gradient is device f32.  All
+ * pointers 16-byte aligned, outputs not aliasing inputs.  theta and dtheta are given exactly when
+ * shape->has_theta is 1.  The call recomputes the chunk-input states (64 fused rows per chunk,
+ * i.e. 64/R steps, whatever shape->chunk_len says; seqlen need not be a multiple), carries
+ * dL/dstate backwards across chunks, and forms each chunk's gradients from its 64 x 64 pairwise
+ * products, all in fp32 on CUDA cores with the in-chunk log-decay sums in fp64.  With the
+ * rotation it runs that on B~ = R(-Phi)B, C~ = R(-Phi)C per head in the workspace (Phi the
+ * cumulative angles) and turns dB~, dC~ back, forming dtheta as fp64 suffix sums over time.
+ * Limits: mimo_rank <= 64, headdim <= 64, dstate <= 128 and a multiple of 4 (else UNSUPPORTED).
+ * dB and dC are zeroed by the call and, without the rotation, accumulated atomically, so their
+ * low bits can vary between runs when H/G > 1.  Asynchrony, workspace and errors as
+ * ssd_chunked_forward.
  */
 ssd_status ssd_chunked_backward(const ssd_shape* shape, const void* x, const float* dA,
-                                const void* B, const void* C, const float* init_state,
-                                const float* dy, const float* dfinal, float* dx, float* ddA,
-                                float* dB, float* dC, float* dinit, void* workspace,
-                                size_t workspace_bytes, void* stream);
+                                const void* B, const void* C, const float* theta,
+                                const float* init_state, const float* dy, const float* dfinal,
+                                float* dx, float* ddA, float* dB, float* dC, float* dtheta,
+                                float* dinit, void* workspace, size_t workspace_bytes,
+                                void* stream);
 
 /* Bytes of device workspace selective_scan_forward needs (0 if the sizes are invalid). */
 size_t selective_scan_workspace_bytes(int64_t batch, int64_t seqlen, int64_t d_model,

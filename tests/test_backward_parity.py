@@ -29,13 +29,23 @@ CASES = [
     wl.SSDConfig("bwd_mimo5_p48_n96_f32", 1, 40, 2, 48, 96, 64, 5, 1, "f32"),
     # P = N = 20: two-wide column runs, odd tile edges, bf16
     wl.SSDConfig("bwd_p20_n20_bf16", 1, 70, 4, 20, 20, 64, 1, 2, "bf16"),
+    # rotated: two heads per B/C group (dB, dC summed over differently turned heads), ragged T
+    wl.SSDConfig("bwd_rot_siso_f32", 2, 150, 4, 16, 16, 64, 1, 2, "f32", theta=True),
+    # rotated MIMO R = 2, bf16 inputs, one group
+    wl.SSDConfig("bwd_rot_mimo2_bf16", 1, 100, 4, 32, 32, 64, 2, 1, "bf16", theta=True),
+    # rotated P = N = 64 over four chunks
+    wl.SSDConfig("bwd_rot_p64n64_f32", 1, 256, 2, 64, 64, 64, 1, 1, "f32", theta=True),
 ]
 
 KEYS = ("dx", "ddA", "dB", "dC", "dinit")
 
 
+def _keys(inp):
+    return KEYS + (("dtheta",) if inp.get("theta") is not None else ())
+
+
 def _check(got, ref, k, what):
-    if k == "ddA":
+    if k in ("ddA", "dtheta"):   # inner products of two state-sized matrices per element
         check_close_inner(got, ref, TOL["f32"], what)
     else:
         check_close(got, ref, TOL["f32"], what)
@@ -52,19 +62,21 @@ def _draw(cfg, seed, with_state):
 
 def _gpu(inp):
     d = {k: (v.cuda() if v is not None else None) for k, v in inp.items()}
-    shape = pkg.shape_of(d["x"], d["B"], 64, False)
+    shape = pkg.shape_of(d["x"], d["B"], 64, d.get("theta") is not None)
     ws = torch.zeros(pkg.ssd_backward_workspace_bytes(shape), dtype=torch.uint8, device="cuda")
     out = pkg.ssd_chunked_backward(d["x"], d["dA"], d["B"], d["C"], d["dy"],
-                                   init_state=d["init_state"], dfinal=d["dfinal"], workspace=ws)
+                                   theta=d.get("theta"), init_state=d["init_state"],
+                                   dfinal=d["dfinal"], workspace=ws)
     assert pkg.workspace_status(ws) == ("SSD_OK", 0)
     torch.cuda.synchronize()
-    return {k: to_np(v) for k, v in out.items()}
+    return {k: to_np(v) for k, v in out.items() if v is not None}
 
 
 def _oracle(inp):
     return oracle.ssd_backward(to_np(inp["x"]), to_np(inp["dA"]), to_np(inp["B"]),
                                to_np(inp["C"]), to_np(inp["dy"]),
-                               init_state=to_np(inp["init_state"]), dfinal=to_np(inp["dfinal"]))
+                               init_state=to_np(inp["init_state"]), dfinal=to_np(inp["dfinal"]),
+                               theta=to_np(inp.get("theta")))
 
 
 @pytest.mark.parametrize("cfg", CASES, ids=lambda c: c.name)
@@ -72,7 +84,7 @@ def _oracle(inp):
 def test_backward_parity(cfg, with_state):
     inp = _draw(cfg, 41, with_state)
     got, ref = _gpu(inp), _oracle(inp)
-    for k in KEYS:
+    for k in _keys(inp):
         _check(got[k], ref[k], k, f"{cfg.name} {k}")
 
 
@@ -110,22 +122,32 @@ def test_backward_rejections():
     lib = pkg.load_library()
     ok = pkg.make_shape(1, 64, 2, 16, 16, 1, 1, 64, "f32", False)
     assert lib.ssd_backward_workspace_bytes(ctypes.byref(ok)) > 0
-    for bad in (pkg.make_shape(1, 64, 2, 16, 16, 1, 1, 64, "f32", True),     # rotation
-                pkg.make_shape(1, 64, 2, 128, 16, 1, 1, 64, "f32", False),   # headdim > 64
+    rot = pkg.make_shape(1, 64, 2, 16, 16, 1, 1, 64, "f32", True)
+    assert lib.ssd_backward_workspace_bytes(ctypes.byref(rot)) > \
+        lib.ssd_backward_workspace_bytes(ctypes.byref(ok))
+    for bad in (pkg.make_shape(1, 64, 2, 128, 16, 1, 1, 64, "f32", False),   # headdim > 64
                 pkg.make_shape(1, 64, 2, 16, 256, 1, 1, 64, "f32", False),   # dstate > 128
                 pkg.make_shape(1, 64, 2, 16, 16, 1, 128, 64, "f32", False),  # rank > 64
                 pkg.make_shape(1, 64, 2, 16, 18, 1, 1, 64, "f32", False)):   # dstate % 4
         assert lib.ssd_backward_workspace_bytes(ctypes.byref(bad)) == 0
-        st = lib.ssd_chunked_backward(ctypes.byref(bad), *([None] * 13), ctypes.c_size_t(0),
+        st = lib.ssd_chunked_backward(ctypes.byref(bad), *([None] * 15), ctypes.c_size_t(0),
                                       None)
         assert pkg.STATUS[st] == "SSD_ERR_UNSUPPORTED"
     x = torch.zeros((1, 64, 1, 2, 16), device="cuda")
     B = torch.zeros((1, 64, 1, 1, 16), device="cuda")
     dA = torch.zeros((1, 64, 2), device="cuda")
-    st = lib.ssd_chunked_backward(ctypes.byref(ok), pkg._ptr(x), pkg._ptr(dA), pkg._ptr(B),
-                                  pkg._ptr(B), None, pkg._ptr(x), None, pkg._ptr(x), None,
-                                  pkg._ptr(B), pkg._ptr(B), None, None, ctypes.c_size_t(0), None)
-    assert pkg.STATUS[st] == "SSD_ERR_INVALID_ARG"   # ddA missing
+    th = torch.zeros((1, 64, 2, 8), device="cuda")
+    P_ = pkg._ptr
+
+    def call(shape, theta, ddA, dtheta):
+        return pkg.STATUS[lib.ssd_chunked_backward(
+            ctypes.byref(shape), P_(x), P_(dA), P_(B), P_(B), theta, None, P_(x), None, P_(x),
+            ddA, P_(B), P_(B), dtheta, None, None, ctypes.c_size_t(0), None)]
+
+    assert call(ok, None, None, None) == "SSD_ERR_INVALID_ARG"            # ddA missing
+    assert call(rot, None, P_(dA), P_(th)) == "SSD_ERR_INVALID_ARG"       # theta missing
+    assert call(rot, P_(th), P_(dA), None) == "SSD_ERR_INVALID_ARG"       # dtheta missing
+    assert call(ok, P_(th), P_(dA), P_(th)) == "SSD_ERR_INVALID_ARG"      # theta, no has_theta
 
 
 def test_backward_full_size_sampled():
@@ -138,5 +160,5 @@ def test_backward_full_size_sampled():
     for b in (0, 3):
         sub = {k: (v[b:b + 1] if v is not None else None) for k, v in inp.items()}
         ref = _oracle(sub)
-        for k in KEYS:
+        for k in _keys(inp):
             _check(got[k][b:b + 1], ref[k], k, f"{k} batch {b}")
