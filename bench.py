@@ -113,6 +113,8 @@ def _named_workload(name):
         return wl.ROT_VARIANT_F32
     if name == wl.MAMBA2_BWD_BF16.name:
         return wl.MAMBA2_BWD_BF16
+    if name == wl.LONG_ROT_BWD_F32.name:
+        return wl.LONG_ROT_BWD_F32
     raise SystemExit(f"unknown workload {name}")
 
 
@@ -239,12 +241,14 @@ def run_ours(args, rank, world, local):
     elif cfg.backward:
         host = wl.make_bwd_inputs(cfg, seed=0)
         d = {k: (v.to(dev) if v is not None else None) for k, v in host.items()}
-        fn = pkg.SSDBackwardPlan(d["x"], d["dA"], d["B"], d["C"], d["dy"],
+        fn = pkg.SSDBackwardPlan(d["x"], d["dA"], d["B"], d["C"], d["dy"], theta=d["theta"],
                                  init_state=d["init_state"], dfinal=d["dfinal"], stream=stream)
         ws = fn.workspace
         variant = "backward"
-        # chunk products (S_c, D_c), the two-way carry across chunks, the chunk gradients
-        launches_per_call = 3
+        # chunk products (S_c, D_c), the two-way carry across chunks, the chunk gradients; with
+        # theta also the chunk and step angles, B~/C~, dL/dg_{T-1}, the turn back of dB~/dC~ and
+        # the two dtheta passes
+        launches_per_call = 3 + (8 if cfg.theta else 0)
         dtype = cfg.dtype
         io_bytes = cfg.io_bytes()
         flops = cfg.backward_flops()
@@ -430,7 +434,8 @@ def e2e_measure(args, cfg, is_ss, host, dev, stream):
                                        dbuf["C"], dbuf["skip"], y=y)
     elif cfg.backward:
         plan = pkg.SSDBackwardPlan(dbuf["x"], dbuf["dA"], dbuf["B"], dbuf["C"], dbuf["dy"],
-                                   init_state=dbuf["init_state"], dfinal=dbuf["dfinal"])
+                                   theta=dbuf["theta"], init_state=dbuf["init_state"],
+                                   dfinal=dbuf["dfinal"])
         ws = plan.workspace
         outs = [(v, torch.empty(v.shape, dtype=v.dtype).pin_memory())
                 for v in plan.grads.values() if v is not None]
@@ -546,7 +551,8 @@ def _time_oracle_ssd(sub, nthr):
     t0 = time.perf_counter()
     if "dy" in sub:
         oracle.ssd_backward(sub["x"], sub["dA"], sub["B"], sub["C"], sub["dy"],
-                            init_state=sub["init_state"], dfinal=sub["dfinal"], nthreads=nthr)
+                            init_state=sub["init_state"], dfinal=sub["dfinal"],
+                            theta=sub["theta"], nthreads=nthr)
     elif "rope_dim" in sub:
         oracle.ssd_rotation_variant(sub["x"], sub["dA"], sub["B"], sub["C"], sub["theta"],
                                     sub["init_state"], rope_dim=sub["rope_dim"],

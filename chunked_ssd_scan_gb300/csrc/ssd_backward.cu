@@ -748,51 +748,49 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 }
 
 // ---------------------------------------------------------------------------------------------
-// Rotation.  With Phi_t = sum_{u <= t} theta_u (per head and pair) the rotated recurrence is the
-// plain one on B~ = R(-Phi_t) B, C~ = R(-Phi_t) C (per head) in the absorbed frame
-// g_t = R(-Phi_t) h_t (scan.py page, THE TRICK), with h_{T-1} = R(Phi_{T-1}) g_{T-1}.  The plain
-// backward runs on (x, dA, B~, C~, init) with dL/dg_{T-1} = R(-Phi_{T-1}) dfinal, and the chain
-// rule takes its dB~, dC~ back:
-//   dB = R(Phi) dB~, dC = R(Phi) dC~ (summed over the heads of a group);
-//   dL/dPhi_t[k] = sum over the step's rows of (dB~_0 B~_1 - dB~_1 B~_0 + dC~_0 C~_1 - dC~_1 C~_0)
-//                  (+ sum_p (dfinal_1 h_0 - dfinal_0 h_1) of the final state at t = T-1),
-// since d R(-phi) v / d phi = -J R(-phi) v and d R(phi) v / d phi = J R(phi) v with J the quarter
-// turn; dtheta_t = sum_{t' >= t} dL/dPhi_{t'}.
-constexpr double kBwdTwoPi = 6.283185307179586476925286766559;
+// Rotation, in chunk-local frames.  Within chunk c let phi_t be the sum of theta over the chunk's
+// steps up to t (zero before the chunk).  The rotated recurrence is then, inside the chunk, the
+// plain one on B^ = R(-phi_t) B and C^ = R(-phi_t) C (per head) for the state g_t = R(-phi_t) h_t
+// (scan.py page, THE TRICK, restarted at every chunk), entered with the physical h_in(c) and left
+// by h_in(c+1) = R(phi_end) g_end.  The plain chunk kernels run on B^, C^; the carry turns by
+// phi_end at each chunk boundary (backward: G^_c = R(-phi_end) dL/dh_in(c+1), dfinal entering
+// physical).  The chain rule then gives
+//   dB = R(phi) dB^, dC = R(phi) dC^ (summed over the heads of a group);
+//   dL/dphi_t = sum over the step's rows of (dB^_0 B^_1 - dB^_1 B^_0 + dC^_0 C^_1 - dC^_1 C^_0),
+//               plus, at the chunk's last step, sum_p (G^_1 g_0 - G^_0 g_1) with g = g_end
+//   (d R(-phi) v / d phi = -J R(-phi) v and d R(phi) v / d phi = J R(phi) v, J the quarter turn);
+//   dtheta_t = sum of dL/dphi over the steps t .. chunk end.
+// Every dtheta is a sum over one chunk at most: angles never grow past a chunk's sum and no sum
+// runs over the whole sequence (whose terms cancel far below their size).
 constexpr int kRotLanes = 32, kRotRows = 8;
-
-__device__ __forceinline__ float bwd_reduce_angle(double a) {
-  return (float)(a - kBwdTwoPi * rint(a * (1.0 / kBwdTwoPi)));
-}
 
 unsigned bwd_blocks(int64_t n) {
   return (unsigned)(n < 1 ? 1 : (n > 0x7fffffff ? 0x7fffffff : n));
 }
 
-// Phi_t of every step, reduced to [-pi, pi], from the chunk-start angles: one thread per
-// (batch, chunk, head, pair), pairs fastest.
+// Chunk-local angles phi_t: one thread per (batch, chunk, head, pair), pairs fastest.
 __global__ void __launch_bounds__(kBwdThreads)
-    bwd_phi_steps_kernel(GenericParams p, float* __restrict__ phiT) {
+    bwd_phi_local_kernel(GenericParams p, float* __restrict__ phiL) {
   const int64_t K = p.N / 2;
   const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (idx >= p.batch * p.nch * p.H * K) return;
   const int64_t k = idx % K, h = (idx / K) % p.H, c = (idx / (K * p.H)) % p.nch;
   const int64_t b = idx / (K * p.H * p.nch);
-  double acc = p.phi[((b * (p.nch + 1) + c) * p.H + h) * K + k];
   const int nv = bwd_steps(p, c);
   const int64_t t0 = b * p.T + c * p.l;
+  double acc = 0.0;
   for (int t = 0; t < nv; ++t) {
     const int64_t o = ((t0 + t) * p.H + h) * K + k;
     acc += (double)__ldg(p.theta + o);
-    phiT[o] = bwd_reduce_angle(acc);
+    phiL[o] = (float)acc;
   }
 }
 
-// B~ = R(-Phi_t) B and C~ = R(-Phi_t) C per head, fp32: one block per step.
+// B^ = R(-phi_t) B and C^ = R(-phi_t) C per head, fp32: one block per step.
 template <typename T>
 __global__ void __launch_bounds__(kRotLanes * kRotRows)
     bwd_rot_bc_kernel(const T* __restrict__ B, const T* __restrict__ C,
-                      const float* __restrict__ phiT, float* __restrict__ Bt,
+                      const float* __restrict__ phiL, float* __restrict__ Bt,
                       float* __restrict__ Ct, int64_t steps, int64_t R, int64_t H, int64_t G,
                       int64_t N) {
   const int64_t K = N / 2, hpg = H / G;
@@ -802,7 +800,7 @@ __global__ void __launch_bounds__(kRotLanes * kRotRows)
         const int64_t src = ((bt * R + r) * G + h / hpg) * N, dst = ((bt * R + r) * H + h) * N;
         for (int64_t k = threadIdx.x; k < K; k += kRotLanes) {
           float sn, cs;
-          sincosf(phiT[(bt * H + h) * K + k], &sn, &cs);
+          sincosf(phiL[(bt * H + h) * K + k], &sn, &cs);
           const float b0 = ld_f32(B + src + 2 * k), b1 = ld_f32(B + src + 2 * k + 1);
           const float c0 = ld_f32(C + src + 2 * k), c1 = ld_f32(C + src + 2 * k + 1);
           Bt[dst + 2 * k] = cs * b0 + sn * b1;
@@ -815,28 +813,108 @@ __global__ void __launch_bounds__(kRotLanes * kRotRows)
   }
 }
 
-// dL/dg_{T-1} = R(-Phi_{T-1}) dfinal: one thread per (batch, head, p, pair).
+// The carries with the turn at each chunk boundary, one thread per state pair (b, h, p, k) and
+// direction (forward first), loading kCarryAhead chunks ahead:
+//   forward:  states[c] <- h_in(c),  h_in(c+1) = R(phi_end) (exp(cend_c) h_in(c) + S_c),
+//             gfin <- h_in(nch) (the final state)
+//   backward: dg[c] <- G^_c = R(-phi_end) v,  v <- exp(cend_c) G^_c + D_c  from v = dfinal,
+//             dinit <- v.
 __global__ void __launch_bounds__(kBwdThreads)
-    bwd_rot_dfinal_kernel(GenericParams p, const float* __restrict__ dfinal,
-                          float* __restrict__ dfin_t) {
-  const int64_t K = p.N / 2;
-  const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (idx >= p.batch * p.H * p.P * K) return;
-  const int64_t k = idx % K, bh = idx / (K * p.P);
+    bwd_carry_rot_kernel(GenericParams p, const float* __restrict__ phiL,
+                         const float* __restrict__ dfinal, float* __restrict__ dg,
+                         float* __restrict__ dinit, float* __restrict__ gfin) {
+  const int64_t K = p.N / 2, PK = p.P * K, n_pr = p.batch * p.H * PK;
+  int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= 2 * n_pr) return;
+  const bool back = idx >= n_pr;
+  if (back) idx -= n_pr;
+  const int64_t k = idx % K, pp = (idx / K) % p.P, bh = idx / PK;
   const int64_t b = bh / p.H, h = bh % p.H;
-  float sn, cs;
-  sincosf(bwd_reduce_angle(p.phi[((b * (p.nch + 1) + p.nch) * p.H + h) * K + k]), &sn, &cs);
-  const float d0 = dfinal[2 * idx], d1 = dfinal[2 * idx + 1];
-  dfin_t[2 * idx] = cs * d0 + sn * d1;
-  dfin_t[2 * idx + 1] = cs * d1 - sn * d0;
+  const int64_t PN = p.P * p.N, cs = p.H * PN;          // chunk stride of states / dg
+  const int64_t e0 = (bh * p.P + pp) * p.N + 2 * k;     // element of the pair in [b,H,P,N]
+  float* vp = (back ? dg : p.states) + (b * p.nch * p.H + h) * PN + pp * p.N + 2 * k;
+  const float* ce = p.cend + b * p.nch * p.H + h;
+  const float* init = back ? dfinal : p.init;
+  float v0 = init ? init[e0] : 0.f, v1 = init ? init[e0 + 1] : 0.f;
+  for (int64_t k0 = 0; k0 < p.nch; k0 += kCarryAhead) {
+    float s0[kCarryAhead], s1[kCarryAhead], av[kCarryAhead], ph[kCarryAhead];
+#pragma unroll
+    for (int q = 0; q < kCarryAhead; ++q)
+      if (k0 + q < p.nch) {
+        const int64_t c = back ? p.nch - 1 - (k0 + q) : k0 + q;
+        s0[q] = vp[c * cs];
+        s1[q] = vp[c * cs + 1];
+        av[q] = ce[c * p.H];
+        const int64_t tl = b * p.T + c * p.l + bwd_steps(p, c) - 1;   // the chunk's last step
+        ph[q] = phiL[(tl * p.H + h) * K + k];
+      }
+#pragma unroll
+    for (int q = 0; q < kCarryAhead; ++q)
+      if (k0 + q < p.nch) {
+        const int64_t c = back ? p.nch - 1 - (k0 + q) : k0 + q;
+        const float a = expf(av[q]);
+        float sn, co;
+        sincosf(ph[q], &sn, &co);
+        if (back) {
+          const float g0 = co * v0 + sn * v1, g1 = co * v1 - sn * v0;   // R(-phi_end) v
+          vp[c * cs] = g0;
+          vp[c * cs + 1] = g1;
+          v0 = fmaf(a, g0, s0[q]);
+          v1 = fmaf(a, g1, s1[q]);
+        } else {
+          vp[c * cs] = v0;
+          vp[c * cs + 1] = v1;
+          const float w0 = fmaf(a, v0, s0[q]), w1 = fmaf(a, v1, s1[q]);
+          v0 = co * w0 - sn * w1;                                        // R(phi_end) w
+          v1 = sn * w0 + co * w1;
+        }
+      }
+  }
+  if (back) {
+    if (dinit) {
+      dinit[e0] = v0;
+      dinit[e0 + 1] = v1;
+    }
+  } else {
+    gfin[e0] = v0;
+    gfin[e0 + 1] = v1;
+  }
 }
 
-// Per step (one block): dB and dC per group from the heads' dB~, dC~ turned back by +Phi, and
-// dL/dPhi_t per (head, pair) into dphi.
+// The chunk-end term of dL/dphi: sum_p (G^_1 g_0 - G^_0 g_1) with G^ = dg[c] and
+// g = g_end(c) = R(-phi_end) h_in(c+1) (the final state for the last chunk); one thread per
+// (batch, chunk, head, pair).
+__global__ void __launch_bounds__(kBwdThreads)
+    bwd_chunk_end_kernel(GenericParams p, const float* __restrict__ phiL,
+                         const float* __restrict__ dg, const float* __restrict__ gfin,
+                         float* __restrict__ eterm) {
+  const int64_t K = p.N / 2;
+  const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= p.batch * p.nch * p.H * K) return;
+  const int64_t k = idx % K, h = (idx / K) % p.H, c = (idx / (K * p.H)) % p.nch;
+  const int64_t b = idx / (K * p.H * p.nch);
+  const int64_t tl = b * p.T + c * p.l + bwd_steps(p, c) - 1;
+  float sn, co;
+  sincosf(phiL[(tl * p.H + h) * K + k], &sn, &co);
+  const int64_t PN = p.P * p.N;
+  const float* gh = dg + ((b * p.nch + c) * p.H + h) * PN + 2 * k;
+  const float* hn = (c + 1 < p.nch) ? p.states + ((b * p.nch + c + 1) * p.H + h) * PN + 2 * k
+                                    : gfin + (b * p.H + h) * PN + 2 * k;
+  double e = 0.0;
+  for (int64_t pp = 0; pp < p.P; ++pp) {
+    const float h0 = hn[pp * p.N], h1 = hn[pp * p.N + 1];
+    const float g0 = co * h0 + sn * h1, g1 = co * h1 - sn * h0;   // R(-phi_end) h_in(c+1)
+    e += (double)(gh[pp * p.N + 1] * g0 - gh[pp * p.N] * g1);
+  }
+  eterm[idx] = (float)e;
+}
+
+// Per step (one block): dB and dC per group from the heads' dB^, dC^ turned back by +phi, and
+// the step's dL/dphi per (head, pair) into dphi.
 __global__ void __launch_bounds__(kRotLanes * kRotRows)
     bwd_rot_grad_kernel(const float* __restrict__ Bt, const float* __restrict__ Ct,
                         const float* __restrict__ dBt, const float* __restrict__ dCt,
-                        const float* __restrict__ phiT, float* __restrict__ dB,
+                        const float* __restrict__ phiL, float* __restrict__ dB,
                         float* __restrict__ dC, float* __restrict__ dphi, int64_t steps,
                         int64_t R, int64_t H, int64_t G, int64_t N) {
   const int64_t K = N / 2, hpg = H / G;
@@ -857,7 +935,7 @@ __global__ void __launch_bounds__(kRotLanes * kRotRows)
           float b0 = 0.f, b1 = 0.f, c0 = 0.f, c1 = 0.f;
           for (int64_t h = g * hpg; h < (g + 1) * hpg; ++h) {
             float sn, cs;
-            sincosf(phiT[(bt * H + h) * K + k], &sn, &cs);
+            sincosf(phiL[(bt * H + h) * K + k], &sn, &cs);
             const int64_t o = ((bt * R + r) * H + h) * N + 2 * k;
             const float e0 = dBt[o], e1 = dBt[o + 1], f0 = dCt[o], f1 = dCt[o + 1];
             b0 += cs * e0 - sn * e1;
@@ -876,49 +954,19 @@ __global__ void __launch_bounds__(kRotLanes * kRotRows)
   }
 }
 
-// Per (batch, chunk, head, pair): the chunk's sum of dL/dPhi (fp64).
-__global__ void __launch_bounds__(kBwdThreads)
-    bwd_dphi_chunk_sum_kernel(GenericParams p, const float* __restrict__ dphi,
-                              double* __restrict__ csum) {
-  const int64_t K = p.N / 2;
-  const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (idx >= p.batch * p.nch * p.H * K) return;
-  const int64_t k = idx % K, h = (idx / K) % p.H, c = (idx / (K * p.H)) % p.nch;
-  const int64_t b = idx / (K * p.H * p.nch);
-  const int nv = bwd_steps(p, c);
-  const int64_t t0 = b * p.T + c * p.l;
-  double s = 0.0;
-  for (int t = 0; t < nv; ++t) s += (double)dphi[((t0 + t) * p.H + h) * K + k];
-  csum[idx] = s;
-}
-
-// dtheta_t = sum_{t' >= t} dL/dPhi_{t'}: the later chunks' sums, the final-state term
-// sum_p (dfinal_1 h_0 - dfinal_0 h_1) with h = R(Phi_{T-1}) g_{T-1}, then the chunk backwards.
+// dtheta_t = the chunk-end term plus dL/dphi over the steps t .. chunk end (fp64), one thread per
+// (batch, chunk, head, pair).
 __global__ void __launch_bounds__(kBwdThreads)
     bwd_dtheta_kernel(GenericParams p, const float* __restrict__ dphi,
-                      const double* __restrict__ csum, const float* __restrict__ dfinal,
-                      const float* __restrict__ gfin, float* __restrict__ dtheta) {
+                      const float* __restrict__ eterm, float* __restrict__ dtheta) {
   const int64_t K = p.N / 2;
   const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (idx >= p.batch * p.nch * p.H * K) return;
   const int64_t k = idx % K, h = (idx / K) % p.H, c = (idx / (K * p.H)) % p.nch;
   const int64_t b = idx / (K * p.H * p.nch);
-  double acc = 0.0;
-  for (int64_t c2 = c + 1; c2 < p.nch; ++c2) acc += csum[((b * p.nch + c2) * p.H + h) * K + k];
-  if (dfinal) {
-    float sn, cs;
-    sincosf(bwd_reduce_angle(p.phi[((b * (p.nch + 1) + p.nch) * p.H + h) * K + k]), &sn, &cs);
-    double f = 0.0;
-    for (int64_t pp = 0; pp < p.P; ++pp) {
-      const int64_t o = ((b * p.H + h) * p.P + pp) * p.N + 2 * k;
-      const float g0 = gfin[o], g1 = gfin[o + 1];
-      const float h0 = cs * g0 - sn * g1, h1 = sn * g0 + cs * g1;
-      f += (double)(dfinal[o + 1] * h0 - dfinal[o] * h1);
-    }
-    acc += f;
-  }
   const int nv = bwd_steps(p, c);
   const int64_t t0 = b * p.T + c * p.l;
+  double acc = (double)eterm[idx];
   for (int t = nv - 1; t >= 0; --t) {
     const int64_t o = ((t0 + t) * p.H + h) * K + k;
     acc += (double)dphi[o];
@@ -932,8 +980,7 @@ int64_t bwd_chunk_steps(int64_t R) { return R >= kBwdRows ? 1 : kBwdRows / R; }
 struct BwdLayout {
   size_t states = 0, cend = 0, dg = 0;
   // rotation only
-  size_t phi = 0, phisum = 0, phiT = 0, Bt = 0, Ct = 0, dBt = 0, dCt = 0, dfin = 0, gfin = 0,
-         dphi = 0, csum = 0;
+  size_t phiL = 0, Bt = 0, Ct = 0, dBt = 0, dCt = 0, gfin = 0, dphi = 0, eterm = 0;
   size_t total = 0;
 };
 
@@ -968,18 +1015,15 @@ BwdLayout bwd_layout(const ssd_shape* s) {
   L.cend = take(sizeof(float) * b * (size_t)nch * H);
   L.dg = take(st);
   if (s->has_theta) {
-    L.phi = take(sizeof(double) * b * (size_t)(nch + 1) * H * K);
-    L.phisum = take(sizeof(double) * b * (size_t)nch * H * K);
-    L.phiT = take(sizeof(float) * b * T * H * K);
+    L.phiL = take(sizeof(float) * b * T * H * K);
     const size_t bc = sizeof(float) * b * T * R * H * N;
     L.Bt = take(bc);
     L.Ct = take(bc);
     L.dBt = take(bc);
     L.dCt = take(bc);
-    L.dfin = take(sizeof(float) * b * H * P * N);
     L.gfin = take(sizeof(float) * b * H * P * N);
     L.dphi = take(sizeof(float) * b * T * H * K);
-    L.csum = take(sizeof(double) * b * (size_t)nch * H * K);
+    L.eterm = take(sizeof(float) * b * (size_t)nch * H * K);
   }
   L.total = off;
   return L;
@@ -987,10 +1031,11 @@ BwdLayout bwd_layout(const ssd_shape* s) {
 
 bool al16_or_null(const void* q) { return q == nullptr || aligned16(q); }
 
+// The three launches; with chunk-local angles phiL the carry turns at every chunk boundary.
 template <typename TX, typename TBC, int NQ>
 cudaError_t bwd_launch_nq(const GenericParams& p, const float* dy, const float* dfinal,
                           float* dx, float* ddA, float* dB, float* dC, float* dinit, float* dg,
-                          float* gfin, cudaStream_t st) {
+                          const float* phiL, float* gfin, cudaStream_t st) {
   const int64_t Lr = p.l * p.R;
   const dim3 grid((unsigned)p.nch, (unsigned)p.H, (unsigned)p.batch);
   const size_t s1 = bwd_state_smem(Lr, p.P, p.N);
@@ -999,9 +1044,15 @@ cudaError_t bwd_launch_nq(const GenericParams& p, const float* dy, const float* 
   if (e != cudaSuccess) return e;
   bwd_chunk_state_kernel<TX, TBC, NQ><<<grid, kBwdThreads, s1, st>>>(p, dy, dg);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  const int64_t n = 2 * p.batch * p.H * p.P * p.N;
-  bwd_carry_kernel<<<(unsigned)((n + kBwdThreads - 1) / kBwdThreads), kBwdThreads, 0, st>>>(
-      p, dfinal, dg, dinit, gfin);
+  if (phiL) {
+    const int64_t n = p.batch * p.H * p.P * p.N;   // two directions x N/2 pairs
+    bwd_carry_rot_kernel<<<(unsigned)((n + kBwdThreads - 1) / kBwdThreads), kBwdThreads, 0,
+                           st>>>(p, phiL, dfinal, dg, dinit, gfin);
+  } else {
+    const int64_t n = 2 * p.batch * p.H * p.P * p.N;
+    bwd_carry_kernel<<<(unsigned)((n + kBwdThreads - 1) / kBwdThreads), kBwdThreads, 0, st>>>(
+        p, dfinal, dg, dinit, gfin);
+  }
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   const size_t s2 = bwd_grad_smem(Lr, p.P, p.N);
   e = cudaFuncSetAttribute(bwd_chunk_grad_kernel<TX, TBC, NQ>,
@@ -1014,76 +1065,66 @@ cudaError_t bwd_launch_nq(const GenericParams& p, const float* dy, const float* 
 // Column tiles of 16 state dims: N <= 16, 32, 64 or 128.
 template <typename TX, typename TBC>
 cudaError_t bwd_launch(const GenericParams& p, const float* dy, const float* dfinal, float* dx,
-                       float* ddA, float* dB, float* dC, float* dinit, float* dg, float* gfin,
-                       cudaStream_t st) {
+                       float* ddA, float* dB, float* dC, float* dinit, float* dg,
+                       const float* phiL, float* gfin, cudaStream_t st) {
   if (p.N <= 16)
-    return bwd_launch_nq<TX, TBC, 1>(p, dy, dfinal, dx, ddA, dB, dC, dinit, dg, gfin, st);
+    return bwd_launch_nq<TX, TBC, 1>(p, dy, dfinal, dx, ddA, dB, dC, dinit, dg, phiL, gfin, st);
   if (p.N <= 32)
-    return bwd_launch_nq<TX, TBC, 2>(p, dy, dfinal, dx, ddA, dB, dC, dinit, dg, gfin, st);
+    return bwd_launch_nq<TX, TBC, 2>(p, dy, dfinal, dx, ddA, dB, dC, dinit, dg, phiL, gfin, st);
   if (p.N <= 64)
-    return bwd_launch_nq<TX, TBC, 4>(p, dy, dfinal, dx, ddA, dB, dC, dinit, dg, gfin, st);
-  return bwd_launch_nq<TX, TBC, 8>(p, dy, dfinal, dx, ddA, dB, dC, dinit, dg, gfin, st);
+    return bwd_launch_nq<TX, TBC, 4>(p, dy, dfinal, dx, ddA, dB, dC, dinit, dg, phiL, gfin, st);
+  return bwd_launch_nq<TX, TBC, 8>(p, dy, dfinal, dx, ddA, dB, dC, dinit, dg, phiL, gfin, st);
 }
 
-// The rotated backward: angles, the absorbed-frame B~, C~ and dL/dg_{T-1}, the plain backward on
-// them (dB~, dC~ into the workspace), then dB, dC, dtheta by the chain rule.
+// The rotated backward: chunk-local angles and B^, C^, the plain chunk kernels on them with the
+// turning carry, then dB, dC turned back and dtheta from per-chunk sums.
 cudaError_t bwd_rotated(GenericParams p, const ssd_shape* s, const BwdLayout& lay, char* ws,
                         const float* dy, const float* dfinal, float* dx, float* ddA, float* dB,
                         float* dC, float* dtheta, float* dinit, float* dg, cudaStream_t st) {
   const int64_t K = p.N / 2, steps = p.batch * p.T;
-  p.phi = reinterpret_cast<double*>(ws + lay.phi);
-  p.phisum = reinterpret_cast<double*>(ws + lay.phisum);
-  float* phiT = reinterpret_cast<float*>(ws + lay.phiT);
+  float* phiL = reinterpret_cast<float*>(ws + lay.phiL);
   float* Bt = reinterpret_cast<float*>(ws + lay.Bt);
   float* Ct = reinterpret_cast<float*>(ws + lay.Ct);
   float* dBt = reinterpret_cast<float*>(ws + lay.dBt);
   float* dCt = reinterpret_cast<float*>(ws + lay.dCt);
-  float* dfin_t = dfinal ? reinterpret_cast<float*>(ws + lay.dfin) : nullptr;
   float* gfin = reinterpret_cast<float*>(ws + lay.gfin);
   float* dphi = reinterpret_cast<float*>(ws + lay.dphi);
-  double* csum = reinterpret_cast<double*>(ws + lay.csum);
-  cudaError_t e = generic_phi(p, st);
-  if (e != cudaSuccess) return e;
+  float* eterm = reinterpret_cast<float*>(ws + lay.eterm);
   const int64_t nk = p.batch * p.nch * p.H * K;
-  bwd_phi_steps_kernel<<<bwd_blocks((nk + kBwdThreads - 1) / kBwdThreads), kBwdThreads, 0, st>>>(
-      p, phiT);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  const unsigned gk = bwd_blocks((nk + kBwdThreads - 1) / kBwdThreads);
+  bwd_phi_local_kernel<<<gk, kBwdThreads, 0, st>>>(p, phiL);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
   const dim3 blk(kRotLanes, kRotRows);
   if (s->io_dtype == SSD_BF16) {
     bwd_rot_bc_kernel<__nv_bfloat16><<<bwd_blocks(steps), blk, 0, st>>>(
-        static_cast<const __nv_bfloat16*>(p.B), static_cast<const __nv_bfloat16*>(p.C), phiT, Bt,
+        static_cast<const __nv_bfloat16*>(p.B), static_cast<const __nv_bfloat16*>(p.C), phiL, Bt,
         Ct, steps, p.R, p.H, p.G, p.N);
   } else {
     bwd_rot_bc_kernel<float><<<bwd_blocks(steps), blk, 0, st>>>(
-        static_cast<const float*>(p.B), static_cast<const float*>(p.C), phiT, Bt, Ct, steps, p.R,
+        static_cast<const float*>(p.B), static_cast<const float*>(p.C), phiL, Bt, Ct, steps, p.R,
         p.H, p.G, p.N);
   }
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  if (dfinal) {
-    const int64_t nf = p.batch * p.H * p.P * K;
-    bwd_rot_dfinal_kernel<<<bwd_blocks((nf + kBwdThreads - 1) / kBwdThreads), kBwdThreads, 0,
-                            st>>>(p, dfinal, dfin_t);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  }
   const size_t bc = sizeof(float) * (size_t)(steps * p.R * p.H * p.N);
   if ((e = cudaMemsetAsync(dBt, 0, bc, st)) != cudaSuccess) return e;
   if ((e = cudaMemsetAsync(dCt, 0, bc, st)) != cudaSuccess) return e;
-  GenericParams q = p;   // the plain problem in the absorbed frame: fp32 B~, C~, one group per head
+  GenericParams q = p;   // the chunk-local plain problem: fp32 B^, C^, one group per head
   q.B = Bt;
   q.C = Ct;
   q.G = p.H;
   q.theta = nullptr;
   e = s->io_dtype == SSD_BF16
-          ? bwd_launch<__nv_bfloat16, float>(q, dy, dfin_t, dx, ddA, dBt, dCt, dinit, dg, gfin, st)
-          : bwd_launch<float, float>(q, dy, dfin_t, dx, ddA, dBt, dCt, dinit, dg, gfin, st);
+          ? bwd_launch<__nv_bfloat16, float>(q, dy, dfinal, dx, ddA, dBt, dCt, dinit, dg, phiL,
+                                             gfin, st)
+          : bwd_launch<float, float>(q, dy, dfinal, dx, ddA, dBt, dCt, dinit, dg, phiL, gfin, st);
   if (e != cudaSuccess) return e;
-  bwd_rot_grad_kernel<<<bwd_blocks(steps), blk, 0, st>>>(Bt, Ct, dBt, dCt, phiT, dB, dC, dphi,
+  bwd_chunk_end_kernel<<<gk, kBwdThreads, 0, st>>>(p, phiL, dg, gfin, eterm);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  bwd_rot_grad_kernel<<<bwd_blocks(steps), blk, 0, st>>>(Bt, Ct, dBt, dCt, phiL, dB, dC, dphi,
                                                           steps, p.R, p.H, p.G, p.N);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  const unsigned gk = bwd_blocks((nk + kBwdThreads - 1) / kBwdThreads);
-  bwd_dphi_chunk_sum_kernel<<<gk, kBwdThreads, 0, st>>>(p, dphi, csum);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  bwd_dtheta_kernel<<<gk, kBwdThreads, 0, st>>>(p, dphi, csum, dfinal, gfin, dtheta);
+  bwd_dtheta_kernel<<<gk, kBwdThreads, 0, st>>>(p, dphi, eterm, dtheta);
   return cudaGetLastError();
 }
 
@@ -1152,8 +1193,9 @@ ssd_status ssd_chunked_backward(const ssd_shape* shape, const void* x, const flo
         cudaMemsetAsync(dC, 0, bc, st) != cudaSuccess)
       return SSD_ERR_CUDA;
     e = bf16 ? bwd_launch<__nv_bfloat16, __nv_bfloat16>(p, dy, dfinal, dx, ddA, dB, dC, dinit, dg,
-                                                        nullptr, st)
-             : bwd_launch<float, float>(p, dy, dfinal, dx, ddA, dB, dC, dinit, dg, nullptr, st);
+                                                        nullptr, nullptr, st)
+             : bwd_launch<float, float>(p, dy, dfinal, dx, ddA, dB, dC, dinit, dg, nullptr,
+                                        nullptr, st);
   }
   return e == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
 }

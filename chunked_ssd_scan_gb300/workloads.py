@@ -71,6 +71,8 @@ class SSDConfig:
             nbytes += b * T * R * G * N * (e + 4) * 2    # B, C read, dB, dC written
             nbytes += b * T * H * 4 * 2                  # dA read, ddA written
             nbytes += b * H * P * N * 4 * 3              # init, dfinal read, dinit written
+            if self.theta:
+                nbytes += b * T * H * (N // 2) * 4 * 2   # theta read, dtheta written
             return nbytes
         nbytes = b * T * R * H * P * e * 2          # x read, y written
         nbytes += b * T * R * G * N * e * 2         # B, C read
@@ -154,6 +156,9 @@ TRAP_MIMO_ROT_F32 = SSDConfig("mamba3_trapezoidal_f32", 1, 16384, 16, 64, 64, 64
 # Backward of the unrotated SSD on config 1's shape (a measured shape of the backward row).
 MAMBA2_BWD_BF16 = SSDConfig("mamba2_backward_bf16", 4, 4096, 32, 64, 128, 64, 1, 1, "bf16",
                             backward=True)
+# Rotated backward on config 3's shape (a measured shape of the backward row).
+LONG_ROT_BWD_F32 = SSDConfig("long_rotation_backward_f32", 1, 131072, 24, 64, 64, 256, 1, 24,
+                             "f32", theta=True, backward=True)
 
 SSD_CONFIGS = [TINY_SISO_F32, MAMBA2_SISO_BF16, MAMBA3_MIMO_BF16, LONG_ROT_F32]
 

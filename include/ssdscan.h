@@ -187,8 +187,9 @@ size_t ssd_backward_workspace_bytes(const ssd_shape* shape);
  * i.e. 64/R steps, whatever shape->chunk_len says; seqlen need not be a multiple), carries
  * dL/dstate backwards across chunks, and forms each chunk's gradients from its 64 x 64 pairwise
  * products, all in fp32 on CUDA cores with the in-chunk log-decay sums in fp64.  With the
- * rotation it runs that on B~ = R(-Phi)B, C~ = R(-Phi)C per head in the workspace (Phi the
- * cumulative angles) and turns dB~, dC~ back, forming dtheta as fp64 suffix sums over time.
+ * rotation it runs that per chunk on B^ = R(-phi)B, C^ = R(-phi)C per head in the workspace
+ * (phi the angle accumulated since the chunk's start), turns the state at each chunk boundary,
+ * turns dB^, dC^ back and forms dtheta from sums over one chunk plus a chunk-end term.
  * Limits: mimo_rank <= 64, headdim <= 64, dstate <= 128 and a multiple of 4 (else UNSUPPORTED).
  * dB and dC are zeroed by the call and, without the rotation, accumulated atomically, so their
  * low bits can vary between runs when H/G > 1.  Asynchrony, workspace and errors as

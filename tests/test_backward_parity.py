@@ -162,3 +162,23 @@ def test_backward_full_size_sampled():
         ref = _oracle(sub)
         for k in _keys(inp):
             _check(got[k][b:b + 1], ref[k], k, f"{k} batch {b}")
+
+
+def test_rotated_backward_full_size_sampled():
+    """The measured rotated backward shape (T = 131072, 24 heads, P = N = 64, one B/C group per
+    head, f32) through the launch the bench times; the oracle recomputes heads 0 and 23 (each
+    head its own group, so every gradient of those heads is checked)."""
+    cfg = wl.LONG_ROT_BWD_F32
+    inp = wl.make_bwd_inputs(cfg, seed=0)   # the bench's inputs
+    got = _gpu(inp)
+    for h in (0, 23):
+        sub = {"x": inp["x"][:, :, :, h:h + 1], "dA": inp["dA"][:, :, h:h + 1],
+               "B": inp["B"][:, :, :, h:h + 1], "C": inp["C"][:, :, :, h:h + 1],
+               "theta": inp["theta"][:, :, h:h + 1], "dy": inp["dy"][:, :, :, h:h + 1],
+               "init_state": inp["init_state"][:, h:h + 1], "dfinal": inp["dfinal"][:, h:h + 1]}
+        ref = _oracle(sub)
+        view = {"dx": got["dx"][:, :, :, h:h + 1], "ddA": got["ddA"][:, :, h:h + 1],
+                "dB": got["dB"][:, :, :, h:h + 1], "dC": got["dC"][:, :, :, h:h + 1],
+                "dtheta": got["dtheta"][:, :, h:h + 1], "dinit": got["dinit"][:, h:h + 1]}
+        for k in _keys(sub):
+            _check(view[k], ref[k], k, f"{k} head {h}")
