@@ -51,6 +51,8 @@ def _lib():
         lib.oracle_ssd_ex.argtypes = [_D] * 8 + [_I64] * 8 + [ctypes.c_int]
         lib.oracle_ssd_backward_ex.restype = ctypes.c_int
         lib.oracle_ssd_backward_ex.argtypes = [_D] * 14 + [_I64] * 8 + [ctypes.c_int]
+        lib.oracle_ssd_trap_backward_ex.restype = ctypes.c_int
+        lib.oracle_ssd_trap_backward_ex.argtypes = [_D] * 22 + [_I64] * 8 + [ctypes.c_int]
         lib.oracle_ssd_rot_ex.restype = ctypes.c_int
         lib.oracle_ssd_rot_ex.argtypes = [_D] * 8 + [_I64] * 8 + [ctypes.c_int, _I64, ctypes.c_int]
         lib.oracle_ssd_trap_ex.restype = ctypes.c_int
@@ -123,6 +125,38 @@ def ssd_backward(x, dA, B, C, dy, init_state=None, dfinal=None, theta=None, nthr
                                        int(mutation))
     if rc != 0:
         raise ValueError(f"oracle_ssd_backward rejected its arguments (code {rc})")
+    return out
+
+
+def ssd_trap_backward(x, dA, B, C, gamma, beta, dy, theta=None, init_state=None, prev_x=None,
+                      prev_B=None, dfinal=None, nthreads=None, mutation: int = 0):
+    """Reverse mode of the trapezoidal SSD recurrence (see ssd_oracle.c) for the loss
+    <dy, y> + <dfinal, final>.  Returns dict dx, ddA, dB, dC, dgamma, dbeta, dinit and, when
+    given theta / prev_x and prev_B, dtheta / dprev_x and dprev_B."""
+    x, dA, B, C, gamma, beta, dy = (_f64(v) for v in (x, dA, B, C, gamma, beta, dy))
+    theta, init_state, prev_x, prev_B, dfinal = (_f64(v) for v in
+                                                 (theta, init_state, prev_x, prev_B, dfinal))
+    b, T, R, H, P = x.shape
+    G, N = B.shape[3], B.shape[4]
+    assert dy.shape == x.shape and gamma.shape == (b, T, H) and beta.shape == (b, T, H)
+    out = {"dx": np.zeros_like(x), "ddA": np.zeros_like(dA), "dB": np.zeros_like(B),
+           "dC": np.zeros_like(C), "dgamma": np.zeros_like(gamma), "dbeta": np.zeros_like(beta),
+           "dinit": np.zeros((b, H, P, N))}
+    if theta is not None:
+        assert theta.shape == (b, T, H, N // 2)
+        out["dtheta"] = np.zeros_like(theta)
+    if prev_x is not None:
+        out["dprev_x"] = np.zeros_like(prev_x)
+        out["dprev_B"] = np.zeros_like(prev_B)
+    rc = _lib().oracle_ssd_trap_backward_ex(
+        _ptr(x), _ptr(dA), _ptr(B), _ptr(C), _ptr(gamma), _ptr(beta), _ptr(theta),
+        _ptr(init_state), _ptr(prev_x), _ptr(prev_B), _ptr(dy), _ptr(dfinal), _ptr(out["dx"]),
+        _ptr(out["ddA"]), _ptr(out["dB"]), _ptr(out["dC"]), _ptr(out["dgamma"]),
+        _ptr(out["dbeta"]), _ptr(out.get("dtheta")), _ptr(out["dinit"]), _ptr(out.get("dprev_x")),
+        _ptr(out.get("dprev_B")), b, T, R, H, G, P, N, nthreads or default_threads(),
+        int(mutation))
+    if rc != 0:
+        raise ValueError(f"oracle_ssd_trap_backward rejected its arguments (code {rc})")
     return out
 
 
@@ -213,6 +247,9 @@ MUTATIONS_BWD = {
     "dy_added_after_decay": 14,
     "ddA_without_decay_factor": 15,
     "state_gradient_turned_forward": 16,
+}
+MUTATIONS_TRAP_BWD = {
+    "beta_gradient_not_carried": 17,
 }
 MUTATIONS_SS = {
     "no_skip": 7,

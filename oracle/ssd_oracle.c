@@ -577,6 +577,279 @@ int oracle_ssd_backward_ex(const double* x, const double* dA, const double* B, c
 }
 
 /* ---------------------------------------------------------------------------------------- */
+/* Backward of the trapezoidal SSD recurrence                                                */
+/* ---------------------------------------------------------------------------------------- */
+/*
+ * Reverse mode of the trapezoidal recurrence (scan.py page, the trapezoidal forward; the forward
+ * is trap_one above), per (b, h), with S_t = sum_r x_{t,r} (outer) B_{t,r} (S_{-1} the previous
+ * write), u_t = exp(dA_t) h_{t-1} + beta_t S_{t-1}, v_t = R(theta_t) u_t, h_t = v_t + gamma_t S_t,
+ * for the loss <dy, y> + <dfinal, h_{T-1}>.  Walking t from T-1 down with g = dL/dh_t and
+ * dS = dL/dS_t (which already holds beta_{t+1} du_{t+1} from the step after):
+ *   g  += sum_r dy_{t,r} (outer) C_{t,r}            dC_{t,r} += h_t^T dy_{t,r}
+ *   dS += gamma_t g;  dgamma_t = <g, S_t>;  dx_{t,r} = dS B_{t,r};  dB_{t,r} += dS^T x_{t,r}
+ *   dtheta_{t,k} = sum_p (g[p,2k+1] v_t[p,2k] - g[p,2k] v_t[p,2k+1])
+ *   du = R(-theta_t) g;  ddA_t = exp(dA_t) <du, h_{t-1}>;  dbeta_t = <du, S_{t-1}>
+ *   dS <- beta_t du (for S_{t-1});  g <- exp(dA_t) du
+ * and after t = 0: dinit = g, dprev_x_r = dS prev_B_r, dprev_B_r = dS^T prev_x_r.  dB, dC and
+ * dprev_B sum over the heads of a group.  States are recomputed from checkpoints every kCkpt
+ * steps.
+ */
+enum { MUT_TBWD_NO_BETA_CARRY = 17 };
+
+typedef struct {
+  const double *x, *dA, *B, *C, *gamma, *beta, *theta, *init, *prev_x, *prev_B, *dy, *dfinal;
+  double *dx, *ddA, *dB, *dC, *dgamma, *dbeta, *dtheta, *dinit, *dprev_x, *dprev_B;
+  int64_t batch, T, R, H, G, P, N;
+  int mutation;
+  int64_t nthreads, tid;
+  pthread_mutex_t* lock;
+} tbwd_job;
+
+/* S = sum_r x_r (outer) B_r of step t (t = -1: the previous write, zero when absent). */
+static void tbwd_write(const tbwd_job* j, int64_t b, int64_t hh, int64_t g_, int64_t t,
+                       double* S) {
+  const int64_t T = j->T, R = j->R, H = j->H, G = j->G, P = j->P, N = j->N;
+  for (int64_t p = 0; p < P; ++p)
+    for (int64_t n = 0; n < N; ++n) {
+      double w = 0.0;
+      for (int64_t r = 0; r < R; ++r) {
+        if (t >= 0) {
+          w += j->x[(((b * T + t) * R + r) * H + hh) * P + p] *
+               j->B[(((b * T + t) * R + r) * G + g_) * N + n];
+        } else if (j->prev_x) {
+          w += j->prev_x[((b * R + r) * H + hh) * P + p] * j->prev_B[((b * R + r) * G + g_) * N + n];
+        }
+      }
+      S[p * N + n] = w;
+    }
+}
+
+/* One forward step: from h_{t-1} (hp) to u_t, v_t and h_t (hn); Sp = S_{t-1}, Sc = S_t. */
+static void tbwd_step(const tbwd_job* j, int64_t b, int64_t hh, int64_t t, const double* hp,
+                      const double* Sp, const double* Sc, double* u, double* v, double* hn) {
+  const int64_t T = j->T, H = j->H, P = j->P, N = j->N, PN = P * N;
+  const double a = exp(j->dA[(b * T + t) * H + hh]);
+  const double bt = j->beta[(b * T + t) * H + hh], gm = j->gamma[(b * T + t) * H + hh];
+  for (int64_t e = 0; e < PN; ++e) u[e] = a * hp[e] + bt * Sp[e];
+  memcpy(v, u, sizeof(double) * PN);
+  if (j->theta) bwd_turn(j->theta + ((b * T + t) * H + hh) * (N / 2), P, N, 1.0, v);
+  for (int64_t e = 0; e < PN; ++e) hn[e] = v[e] + gm * Sc[e];
+}
+
+static void tbwd_one(const tbwd_job* j, int64_t b, int64_t hh, double* ck, double* seg,
+                     double* g, double* dS, double* Sp, double* Sc, double* u, double* v,
+                     double* tmp, double* dBl, double* dCl, double* dpB) {
+  const int64_t T = j->T, R = j->R, H = j->H, G = j->G, P = j->P, N = j->N, PN = P * N;
+  const int64_t g_ = hh / (H / G);
+  const int64_t nck = (T + ORACLE_CKPT - 1) / ORACLE_CKPT;
+  double* h = seg;
+  if (j->init) {
+    memcpy(h, j->init + ((b * H + hh) * P) * N, sizeof(double) * PN);
+  } else {
+    memset(h, 0, sizeof(double) * PN);
+  }
+  for (int64_t t = 0; t < T; ++t) {
+    if (t % ORACLE_CKPT == 0) memcpy(ck + (t / ORACLE_CKPT) * PN, h, sizeof(double) * PN);
+    tbwd_write(j, b, hh, g_, t - 1, Sp);
+    tbwd_write(j, b, hh, g_, t, Sc);
+    tbwd_step(j, b, hh, t, h, Sp, Sc, u, v, tmp);
+    memcpy(h, tmp, sizeof(double) * PN);
+  }
+  if (j->dfinal) {
+    memcpy(g, j->dfinal + ((b * H + hh) * P) * N, sizeof(double) * PN);
+  } else {
+    memset(g, 0, sizeof(double) * PN);
+  }
+  memset(dS, 0, sizeof(double) * PN);
+  memset(dBl, 0, sizeof(double) * T * R * N);
+  memset(dCl, 0, sizeof(double) * T * R * N);
+  for (int64_t c = nck - 1; c >= 0; --c) {
+    const int64_t t0 = c * ORACLE_CKPT, t1 = (t0 + ORACLE_CKPT < T) ? t0 + ORACLE_CKPT : T;
+    memcpy(seg, ck + c * PN, sizeof(double) * PN);
+    for (int64_t t = t0; t < t1; ++t) {   /* h_{t0-1} .. h_{t1-1} into seg rows 0 .. t1-t0 */
+      tbwd_write(j, b, hh, g_, t - 1, Sp);
+      tbwd_write(j, b, hh, g_, t, Sc);
+      tbwd_step(j, b, hh, t, seg + (t - t0) * PN, Sp, Sc, u, v, seg + (t - t0 + 1) * PN);
+    }
+    for (int64_t t = t1 - 1; t >= t0; --t) {
+      const double a = exp(j->dA[(b * T + t) * H + hh]);
+      const double bt = j->beta[(b * T + t) * H + hh], gm = j->gamma[(b * T + t) * H + hh];
+      const double* ht = seg + (t - t0 + 1) * PN;
+      const double* hprev = seg + (t - t0) * PN;
+      tbwd_write(j, b, hh, g_, t - 1, Sp);
+      tbwd_write(j, b, hh, g_, t, Sc);
+      tbwd_step(j, b, hh, t, hprev, Sp, Sc, u, v, tmp);
+      for (int64_t r = 0; r < R; ++r) {
+        const double* dyv = j->dy + (((b * T + t) * R + r) * H + hh) * P;
+        const double* cv = j->C + (((b * T + t) * R + r) * G + g_) * N;
+        for (int64_t n = 0; n < N; ++n) {
+          double s = 0.0;
+          for (int64_t p = 0; p < P; ++p) s += dyv[p] * ht[p * N + n];
+          dCl[(t * R + r) * N + n] += s;
+        }
+        for (int64_t p = 0; p < P; ++p)
+          for (int64_t n = 0; n < N; ++n) g[p * N + n] += dyv[p] * cv[n];
+      }
+      double dgm = 0.0;
+      for (int64_t e = 0; e < PN; ++e) {
+        dS[e] += gm * g[e];
+        dgm += g[e] * Sc[e];
+      }
+      j->dgamma[(b * T + t) * H + hh] = dgm;
+      for (int64_t r = 0; r < R; ++r) {
+        const double* xv = j->x + (((b * T + t) * R + r) * H + hh) * P;
+        const double* bv = j->B + (((b * T + t) * R + r) * G + g_) * N;
+        for (int64_t p = 0; p < P; ++p) {
+          double s = 0.0;
+          for (int64_t n = 0; n < N; ++n) s += dS[p * N + n] * bv[n];
+          j->dx[(((b * T + t) * R + r) * H + hh) * P + p] = s;
+        }
+        for (int64_t n = 0; n < N; ++n) {
+          double s = 0.0;
+          for (int64_t p = 0; p < P; ++p) s += dS[p * N + n] * xv[p];
+          dBl[(t * R + r) * N + n] += s;
+        }
+      }
+      if (j->theta && j->dtheta) {
+        double* dth = j->dtheta + ((b * T + t) * H + hh) * (N / 2);
+        for (int64_t k = 0; k < N / 2; ++k) {
+          double s = 0.0;
+          for (int64_t p = 0; p < P; ++p)
+            s += g[p * N + 2 * k + 1] * v[p * N + 2 * k] - g[p * N + 2 * k] * v[p * N + 2 * k + 1];
+          dth[k] = s;
+        }
+      }
+      /* du = R(-theta_t) g, kept in g */
+      if (j->theta) bwd_turn(j->theta + ((b * T + t) * H + hh) * (N / 2), P, N, -1.0, g);
+      double da = 0.0, dbt = 0.0;
+      for (int64_t e = 0; e < PN; ++e) {
+        da += g[e] * hprev[e];
+        dbt += g[e] * Sp[e];
+      }
+      j->ddA[(b * T + t) * H + hh] = a * da;
+      j->dbeta[(b * T + t) * H + hh] = dbt;
+      if (j->mutation == MUT_TBWD_NO_BETA_CARRY) {
+        /* the planted mistake: the beta term's gradient is not carried to S_{t-1} */
+        for (int64_t e = 0; e < PN; ++e) dS[e] = 0.0;
+      } else {
+        for (int64_t e = 0; e < PN; ++e) dS[e] = bt * g[e];
+      }
+      for (int64_t e = 0; e < PN; ++e) g[e] *= a;
+    }
+  }
+  if (j->dinit) memcpy(j->dinit + ((b * H + hh) * P) * N, g, sizeof(double) * PN);
+  /* dS now holds dL/dS_{-1} */
+  memset(dpB, 0, sizeof(double) * R * N);
+  if (j->prev_x) {
+    for (int64_t r = 0; r < R; ++r) {
+      const double* pbv = j->prev_B + ((b * R + r) * G + g_) * N;
+      const double* pxv = j->prev_x + ((b * R + r) * H + hh) * P;
+      for (int64_t p = 0; p < P; ++p) {
+        double s = 0.0;
+        for (int64_t n = 0; n < N; ++n) s += dS[p * N + n] * pbv[n];
+        if (j->dprev_x) j->dprev_x[((b * R + r) * H + hh) * P + p] = s;
+      }
+      for (int64_t n = 0; n < N; ++n) {
+        double s = 0.0;
+        for (int64_t p = 0; p < P; ++p) s += dS[p * N + n] * pxv[p];
+        dpB[r * N + n] = s;
+      }
+    }
+  }
+  pthread_mutex_lock(j->lock);
+  for (int64_t t = 0; t < T; ++t)
+    for (int64_t r = 0; r < R; ++r)
+      for (int64_t n = 0; n < N; ++n) {
+        const int64_t o = (((b * T + t) * R + r) * G + g_) * N + n;
+        j->dB[o] += dBl[(t * R + r) * N + n];
+        j->dC[o] += dCl[(t * R + r) * N + n];
+      }
+  if (j->prev_x && j->dprev_B)
+    for (int64_t r = 0; r < R; ++r)
+      for (int64_t n = 0; n < N; ++n) j->dprev_B[((b * R + r) * G + g_) * N + n] += dpB[r * N + n];
+  pthread_mutex_unlock(j->lock);
+}
+
+static void* tbwd_worker(void* arg) {
+  const tbwd_job* j = (const tbwd_job*)arg;
+  const int64_t PN = j->P * j->N, nck = (j->T + ORACLE_CKPT - 1) / ORACLE_CKPT;
+  double* ck = (double*)malloc(sizeof(double) * PN * (size_t)nck);
+  double* seg = (double*)malloc(sizeof(double) * PN * (ORACLE_CKPT + 1));
+  double* buf = (double*)malloc(sizeof(double) * PN * 7);
+  double* dBl = (double*)malloc(sizeof(double) * j->T * j->R * j->N);
+  double* dCl = (double*)malloc(sizeof(double) * j->T * j->R * j->N);
+  double* dpB = (double*)malloc(sizeof(double) * j->R * j->N);
+  void* rc = NULL;
+  if (!ck || !seg || !buf || !dBl || !dCl || !dpB) {
+    rc = (void*)1;
+  } else {
+    for (int64_t idx = j->tid; idx < j->batch * j->H; idx += j->nthreads)
+      tbwd_one(j, idx / j->H, idx % j->H, ck, seg, buf, buf + PN, buf + 2 * PN, buf + 3 * PN,
+               buf + 4 * PN, buf + 5 * PN, buf + 6 * PN, dBl, dCl, dpB);
+  }
+  free(ck);
+  free(seg);
+  free(buf);
+  free(dBl);
+  free(dCl);
+  free(dpB);
+  return rc;
+}
+
+/* Backward of the trapezoidal SSD (theta, init_state, prev_x/prev_B, dfinal nullable; prev_x and
+ * prev_B both or neither).  dB, dC, dprev_B are zeroed here; dtheta (needs theta), dinit,
+ * dprev_x, dprev_B (need prev_x) nullable.  Returns 0 or a negative error. */
+int oracle_ssd_trap_backward_ex(const double* x, const double* dA, const double* B,
+                                const double* C, const double* gamma, const double* beta,
+                                const double* theta, const double* init_state,
+                                const double* prev_x, const double* prev_B, const double* dy,
+                                const double* dfinal, double* dx, double* ddA, double* dB,
+                                double* dC, double* dgamma, double* dbeta, double* dtheta,
+                                double* dinit, double* dprev_x, double* dprev_B, int64_t batch,
+                                int64_t T, int64_t R, int64_t H, int64_t G, int64_t P, int64_t N,
+                                int64_t nthreads, int mutation) {
+  if (!x || !dA || !B || !C || !gamma || !beta || !dy || !dx || !ddA || !dB || !dC || !dgamma ||
+      !dbeta)
+    return -1;
+  if (batch < 1 || T < 1 || R < 1 || H < 1 || G < 1 || P < 1 || N < 1) return -2;
+  if (H % G != 0) return -3;
+  if (theta && (N % 2) != 0) return -4;
+  if ((prev_x == NULL) != (prev_B == NULL)) return -6;
+  memset(dB, 0, sizeof(double) * (size_t)(batch * T * R * G * N));
+  memset(dC, 0, sizeof(double) * (size_t)(batch * T * R * G * N));
+  if (dprev_B) memset(dprev_B, 0, sizeof(double) * (size_t)(batch * R * G * N));
+  if (dprev_x) memset(dprev_x, 0, sizeof(double) * (size_t)(batch * R * H * P));
+  const int64_t nt = clamp_threads(nthreads, batch * H);
+  tbwd_job* jobs = (tbwd_job*)calloc((size_t)nt, sizeof(tbwd_job));
+  pthread_t* th = (pthread_t*)calloc((size_t)nt, sizeof(pthread_t));
+  pthread_mutex_t lock;
+  if (!jobs || !th || pthread_mutex_init(&lock, NULL) != 0) {
+    free(jobs);
+    free(th);
+    return -5;
+  }
+  for (int64_t i = 0; i < nt; ++i) {
+    tbwd_job jb = {x,      dA,     B,      C,     gamma, beta,  theta,   init_state, prev_x,
+                   prev_B, dy,     dfinal, dx,    ddA,   dB,    dC,      dgamma,     dbeta,
+                   dtheta, dinit,  dprev_x, dprev_B, batch, T,  R,       H,          G,
+                   P,      N,      mutation, nt,  i,     &lock};
+    jobs[i] = jb;
+  }
+  int rc = 0;
+  for (int64_t i = 1; i < nt; ++i) pthread_create(&th[i], NULL, tbwd_worker, &jobs[i]);
+  if (tbwd_worker(&jobs[0]) != NULL) rc = -5;
+  for (int64_t i = 1; i < nt; ++i) {
+    void* ret = NULL;
+    pthread_join(th[i], &ret);
+    if (ret != NULL) rc = -5;
+  }
+  pthread_mutex_destroy(&lock);
+  free(jobs);
+  free(th);
+  return rc;
+}
+
+/* ---------------------------------------------------------------------------------------- */
 /* Selective scan                                                                            */
 /* ---------------------------------------------------------------------------------------- */
 

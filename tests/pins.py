@@ -426,4 +426,35 @@ def pin_backward_finite_differences(mutation=0):
     return res
 
 
+def pin_trapezoidal_backward_finite_differences(mutation=0):
+    """The trapezoidal backward oracle against central differences of the trapezoidal forward
+    oracle along a random direction of each input (x, dA, B, C, gamma, beta, theta, init,
+    prev_x, prev_B): MIMO ranks, a group shared by two heads, the rotation, a previous write and
+    a length that crosses the 64-step recompute checkpoint."""
+    res = []
+    x, dA, B, C, gm, bt, th, h0, px, pb = _trap_problem(71, 2, 70, 2, 2, 1, 3, 4, theta=True)
+    r = _rng(72)
+    dy = r.standard_normal(x.shape)
+    dfin = r.standard_normal(h0.shape)
+    g = oracle.ssd_trap_backward(x, dA, B, C, gm, bt, dy, theta=th, init_state=h0, prev_x=px,
+                                 prev_B=pb, dfinal=dfin, mutation=mutation)
+
+    def loss(xx, aa, bb, cc, gg, be, tt, hh, pxx, pbb):
+        y, f = oracle.ssd_trapezoidal(xx, aa, bb, cc, gg, be, tt, hh, pxx, pbb)
+        return float((dy * y).sum() + (dfin * f).sum())
+
+    names = ["dx", "ddA", "dB", "dC", "dgamma", "dbeta", "dtheta", "dinit", "dprev_x", "dprev_B"]
+    vals = [x, dA, B, C, gm, bt, th, h0, px, pb]
+    eps = 1e-5
+    for i, name in enumerate(names):
+        v = r.standard_normal(vals[i].shape)
+        plus = [vals[k] + (eps * v if k == i else 0) for k in range(len(vals))]
+        minus = [vals[k] - (eps * v if k == i else 0) for k in range(len(vals))]
+        fd = (loss(*plus) - loss(*minus)) / (2 * eps)
+        an = float((g[name] * v).sum())
+        res.append((f"fd_trap_{name}", abs(fd - an) / (1.0 + abs(fd)), 1e-7))
+    return res
+
+
 BWD_PINS = [pin_backward_finite_differences]
+TRAP_BWD_PINS = [pin_trapezoidal_backward_finite_differences]

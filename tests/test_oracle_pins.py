@@ -8,7 +8,7 @@ from tests import pins
 
 
 @pytest.mark.parametrize("pin", pins.SSD_PINS + pins.SS_PINS + pins.TRAP_PINS + pins.ROT_PINS
-                         + pins.BWD_PINS,
+                         + pins.BWD_PINS + pins.TRAP_BWD_PINS,
                          ids=lambda f: f.__name__)
 def test_pin_holds(pin):
     for name, err, tol in pin(0):
@@ -86,3 +86,9 @@ def test_oracle_empty_inputs():
     y, f = oracle.ssd(np.zeros((2, 0, 1, 3, 4)), np.zeros((2, 0, 3)), np.zeros((2, 0, 1, 1, 5)),
                       np.zeros((2, 0, 1, 1, 5)), init_state=np.ones((2, 3, 4, 5)))
     assert y.shape == (2, 0, 1, 3, 4) and np.all(f == 1.0)
+
+
+@pytest.mark.parametrize("name,code", sorted(oracle.MUTATIONS_TRAP_BWD.items()))
+def test_planted_trapezoidal_backward_mistake_is_caught(name, code):
+    failed = [n for pin in pins.TRAP_BWD_PINS for (n, err, tol) in pin(code) if not err <= tol]
+    assert failed, f"planted mistake '{name}' passed every trapezoidal backward pin"
