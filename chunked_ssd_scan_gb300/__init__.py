@@ -21,6 +21,7 @@ __all__ = [
     "selective_scan_workspace_bytes", "selective_scan_forward", "ssd_trapezoidal_workspace_bytes",
     "ssd_trapezoidal_forward", "SSDTrapezoidalPlan", "ssd_rotation_variant_forward",
     "ssd_backward_workspace_bytes", "ssd_chunked_backward", "SSDBackwardPlan",
+    "ssd_trapezoidal_backward", "ssd_trapezoidal_backward_workspace_bytes",
     "workspace_status", "wait_selftest", "STATUS", "VARIANTS",
 ]
 
@@ -85,6 +86,10 @@ def load_library(path: Optional[str] = None):
     lib.ssd_backward_workspace_bytes.argtypes = [SP]
     lib.ssd_chunked_backward.restype = ctypes.c_int
     lib.ssd_chunked_backward.argtypes = [SP] + [_VP] * 15 + [ctypes.c_size_t, _VP]
+    lib.ssd_trapezoidal_backward_workspace_bytes.restype = ctypes.c_size_t
+    lib.ssd_trapezoidal_backward_workspace_bytes.argtypes = [SP]
+    lib.ssd_trapezoidal_backward.restype = ctypes.c_int
+    lib.ssd_trapezoidal_backward.argtypes = [SP] + [_VP] * 23 + [ctypes.c_size_t, _VP]
     lib.selective_scan_workspace_bytes.argtypes = [_I64] * 4
     lib.selective_scan_forward.restype = ctypes.c_int
     lib.selective_scan_forward.argtypes = [_VP] * 7 + [_I64] * 4 + [_VP, ctypes.c_size_t, _VP]
@@ -414,6 +419,64 @@ def ssd_chunked_backward(x, dA, B, C, dy, *, theta=None, init_state=None, dfinal
     return SSDBackwardPlan(x, dA, B, C, dy, theta=theta, init_state=init_state, dfinal=dfinal,
                            return_dinit=return_dinit, grads=grads, workspace=workspace,
                            stream=stream)()
+
+
+def ssd_trapezoidal_backward_workspace_bytes(shape: ssd_shape) -> int:
+    return int(load_library().ssd_trapezoidal_backward_workspace_bytes(ctypes.byref(shape)))
+
+
+def ssd_trapezoidal_backward(x, dA, B, C, gamma, beta, dy, *, theta=None, prev_x=None,
+                             prev_B=None, init_state=None, dfinal=None, workspace=None,
+                             stream=None):
+    """Gradients of <dy, y> + <dfinal, final_state> for the trapezoidal forward, through
+    ``ssd_trapezoidal_backward``.  Returns a dict of f32 tensors dx, ddA, dB, dC, dgamma, dbeta,
+    dtheta (None without theta), dinit, dprev_x and dprev_B (None without a previous write)."""
+    if x.dim() != 5 or B.dim() != 5:
+        raise ValueError("x must be [b,T,R,H,P] and B/C [b,T,R,G,N]")
+    b, T, R, H, P = x.shape
+    G, N = B.shape[3], B.shape[4]
+    _check_cuda("x", x)
+    _check_cuda("B", B, x.dtype, (b, T, R, G, N))
+    _check_cuda("C", C, x.dtype, (b, T, R, G, N))
+    for name, v in (("dA", dA), ("gamma", gamma), ("beta", beta)):
+        _check_cuda(name, v, torch.float32, (b, T, H))
+    _check_cuda("dy", dy, torch.float32, (b, T, R, H, P))
+    if theta is not None:
+        _check_cuda("theta", theta, torch.float32, (b, T, H, N // 2))
+    if (prev_x is None) != (prev_B is None):
+        raise ValueError("prev_x and prev_B go together")
+    if prev_x is not None:
+        _check_cuda("prev_x", prev_x, x.dtype, (b, R, H, P))
+        _check_cuda("prev_B", prev_B, x.dtype, (b, R, G, N))
+    for name, v in (("init_state", init_state), ("dfinal", dfinal)):
+        if v is not None:
+            _check_cuda(name, v, torch.float32, (b, H, P, N))
+    shape = shape_of(x, B, 64, theta is not None)
+    lib = load_library()
+    need = int(lib.ssd_trapezoidal_backward_workspace_bytes(ctypes.byref(shape)))
+    if need == 0:
+        raise SSDError(2, "ssd_trapezoidal_backward_workspace_bytes (shape not supported)")
+    if workspace is None:
+        workspace = torch.zeros(need, dtype=torch.uint8, device=x.device)
+    f32 = dict(dtype=torch.float32, device=x.device)
+    g = {"dx": torch.empty((b, T, R, H, P), **f32), "ddA": torch.empty((b, T, H), **f32),
+         "dB": torch.empty((b, T, R, G, N), **f32), "dC": torch.empty((b, T, R, G, N), **f32),
+         "dgamma": torch.empty((b, T, H), **f32), "dbeta": torch.empty((b, T, H), **f32),
+         "dtheta": torch.empty((b, T, H, N // 2), **f32) if theta is not None else None,
+         "dinit": torch.empty((b, H, P, N), **f32),
+         "dprev_x": torch.empty((b, R, H, P), **f32) if prev_x is not None else None,
+         "dprev_B": torch.empty((b, R, G, N), **f32) if prev_x is not None else None}
+    st = lib.ssd_trapezoidal_backward(
+        ctypes.byref(shape), _ptr(x), _ptr(dA), _ptr(B), _ptr(C), _ptr(gamma), _ptr(beta),
+        _ptr(theta), _ptr(prev_x), _ptr(prev_B), _ptr(init_state), _ptr(dy), _ptr(dfinal),
+        _ptr(g["dx"]), _ptr(g["ddA"]), _ptr(g["dB"]), _ptr(g["dC"]), _ptr(g["dgamma"]),
+        _ptr(g["dbeta"]), _ptr(g["dtheta"]), _ptr(g["dinit"]), _ptr(g["dprev_x"]),
+        _ptr(g["dprev_B"]), _ptr(workspace), ctypes.c_size_t(workspace.numel()),
+        _stream_handle(stream))
+    if st != 0:
+        raise SSDError(st, "ssd_trapezoidal_backward")
+    g["workspace"] = workspace
+    return g
 
 
 def selective_scan_workspace_bytes(batch, seqlen, d_model, d_state) -> int:

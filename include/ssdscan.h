@@ -202,6 +202,29 @@ ssd_status ssd_chunked_backward(const ssd_shape* shape, const void* x, const flo
                                 float* dinit, void* workspace, size_t workspace_bytes,
                                 void* stream);
 
+/* Bytes of device workspace ssd_trapezoidal_backward needs for `shape` (0 if unsupported). */
+size_t ssd_trapezoidal_backward_workspace_bytes(const ssd_shape* shape);
+
+/*
+ * Reverse mode of ssd_trapezoidal_forward (scan.py page: the trapezoidal forward, and a scan that
+ * can be trained).  For the loss L = <dy, y> + <dfinal, final_state> on the same inputs it writes
+ *   dx, ddA, dB, dC, dinit as ssd_chunked_backward; dgamma, dbeta [b,T,H] = dL/dgamma, dL/dbeta;
+ *   dtheta [b,T,H,N/2] (has_theta = 1 only; NULL otherwise); dprev_x [b,R,H,P], dprev_B [b,R,G,N]
+ *   = dL/dprev_x, dL/dprev_B (only when prev_x/prev_B are given; may be NULL).
+ * Arguments as ssd_trapezoidal_forward plus dy [b,T,R,H,P] and dfinal [b,H,P,N] (NULL = zero),
+ * device f32; every gradient is device f32 and 16-byte aligned; dinit may be NULL.  The call
+ * builds the forward's 2R-channel expansion in the workspace, runs ssd_chunked_backward on it
+ * (dy on the first R channels) and takes the gradients back through the expansion.  Limits: those
+ * of ssd_chunked_backward for 2R channels (2R <= 64, headdim <= 64, dstate <= 128 and a multiple
+ * of 4), else UNSUPPORTED.  Asynchrony, workspace and errors as ssd_chunked_forward.
+ */
+ssd_status ssd_trapezoidal_backward(
+    const ssd_shape* shape, const void* x, const float* dA, const void* B, const void* C,
+    const float* gamma, const float* beta, const float* theta, const void* prev_x,
+    const void* prev_B, const float* init_state, const float* dy, const float* dfinal, float* dx,
+    float* ddA, float* dB, float* dC, float* dgamma, float* dbeta, float* dtheta, float* dinit,
+    float* dprev_x, float* dprev_B, void* workspace, size_t workspace_bytes, void* stream);
+
 /* Bytes of device workspace selective_scan_forward needs (0 if the sizes are invalid). */
 size_t selective_scan_workspace_bytes(int64_t batch, int64_t seqlen, int64_t d_model,
                                       int64_t d_state);
