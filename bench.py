@@ -115,6 +115,8 @@ def _named_workload(name):
         return wl.MAMBA2_BWD_BF16
     if name == wl.LONG_ROT_BWD_F32.name:
         return wl.LONG_ROT_BWD_F32
+    if name == wl.TRAP_BWD_F32.name:
+        return wl.TRAP_BWD_F32
     raise SystemExit(f"unknown workload {name}")
 
 
@@ -238,6 +240,32 @@ def run_ours(args, rank, world, local):
         dtype = "f32"
         io_bytes = cfg.io_bytes()
         flops = 0
+    elif cfg.backward and cfg.trapezoidal:
+        host = wl.make_trap_bwd_inputs(cfg, seed=0)
+        d = {k: (v.to(dev) if v is not None else None) for k, v in host.items()}
+        wsb = torch.zeros(pkg.ssd_trapezoidal_backward_workspace_bytes(
+            pkg.shape_of(d["x"], d["B"], 64, cfg.theta)), dtype=torch.uint8, device=dev)
+
+        tgrads = pkg.ssd_trapezoidal_backward(
+            d["x"], d["dA"], d["B"], d["C"], d["gamma"], d["beta"], d["dy"], theta=d["theta"],
+            prev_x=d["prev_x"], prev_B=d["prev_B"], init_state=d["init_state"],
+            dfinal=d["dfinal"], workspace=wsb, stream=stream)
+
+        def fn():
+            pkg.ssd_trapezoidal_backward(d["x"], d["dA"], d["B"], d["C"], d["gamma"], d["beta"],
+                                         d["dy"], theta=d["theta"], prev_x=d["prev_x"],
+                                         prev_B=d["prev_B"], init_state=d["init_state"],
+                                         dfinal=d["dfinal"], grads=tgrads, workspace=wsb,
+                                         stream=stream)
+        ws = wsb
+        variant = "backward"
+        # the expansion (2), dy^, the rotated backward of the expanded problem (8), the two
+        # chain kernels
+        launches_per_call = 2 + 1 + (8 if cfg.theta else 3) + 2
+        dtype = cfg.dtype
+        io_bytes = cfg.io_bytes()
+        flops = cfg.with_(mimo_rank=2 * cfg.mimo_rank,
+                          ngroups=cfg.nheads if cfg.theta else cfg.ngroups).backward_flops()
     elif cfg.backward:
         host = wl.make_bwd_inputs(cfg, seed=0)
         d = {k: (v.to(dev) if v is not None else None) for k, v in host.items()}
@@ -350,7 +378,9 @@ def run_ours(args, rank, world, local):
         roof = {"bound": "alu", "achieved": round(a_tf, 2), "peak": alu, "unit": "TFLOP/s",
                 "frac": round(a_tf / alu, 4), "traffic": traffic,
                 "peak_source": "derived: 152 SMs x 128 fp32 lanes x 2 FLOP x 2.07 GHz",
-                "kernel": "ssd_chunked_backward", "algorithmic_flops_per_launch": flops,
+                "kernel": ("ssd_trapezoidal_backward" if cfg.trapezoidal
+                           else "ssd_chunked_backward"),
+                "algorithmic_flops_per_launch": flops,
                 "algorithmic_bytes_per_launch": io_bytes,
                 "hbm_gbs": round(io_bytes / (ms * 1e-3) / 1e9, 1),
                 "hbm_frac": round(io_bytes / (ms * 1e-3) / 1e9 / hbm, 4)}
@@ -432,6 +462,22 @@ def e2e_measure(args, cfg, is_ss, host, dev, stream):
         def call():
             pkg.selective_scan_forward(dbuf["u"], dbuf["delta"], dbuf["A"], dbuf["B"],
                                        dbuf["C"], dbuf["skip"], y=y)
+    elif cfg.backward and cfg.trapezoidal:
+        ws = torch.zeros(pkg.ssd_trapezoidal_backward_workspace_bytes(
+            pkg.shape_of(dbuf["x"], dbuf["B"], 64, cfg.theta)), dtype=torch.uint8, device=dev)
+        grads = pkg.ssd_trapezoidal_backward(
+            dbuf["x"], dbuf["dA"], dbuf["B"], dbuf["C"], dbuf["gamma"], dbuf["beta"], dbuf["dy"],
+            theta=dbuf["theta"], prev_x=dbuf["prev_x"], prev_B=dbuf["prev_B"],
+            init_state=dbuf["init_state"], dfinal=dbuf["dfinal"], workspace=ws)
+        grads.pop("workspace")
+        outs = [(v, torch.empty(v.shape, dtype=v.dtype).pin_memory())
+                for v in grads.values() if v is not None]
+
+        def call():
+            pkg.ssd_trapezoidal_backward(
+                dbuf["x"], dbuf["dA"], dbuf["B"], dbuf["C"], dbuf["gamma"], dbuf["beta"],
+                dbuf["dy"], theta=dbuf["theta"], prev_x=dbuf["prev_x"], prev_B=dbuf["prev_B"],
+                init_state=dbuf["init_state"], dfinal=dbuf["dfinal"], grads=grads, workspace=ws)
     elif cfg.backward:
         plan = pkg.SSDBackwardPlan(dbuf["x"], dbuf["dA"], dbuf["B"], dbuf["C"], dbuf["dy"],
                                    theta=dbuf["theta"], init_state=dbuf["init_state"],
@@ -549,7 +595,12 @@ def _time_oracle_ssd(sub, nthr):
     import oracle
 
     t0 = time.perf_counter()
-    if "dy" in sub:
+    if "dy" in sub and "gamma" in sub:
+        oracle.ssd_trap_backward(sub["x"], sub["dA"], sub["B"], sub["C"], sub["gamma"],
+                                 sub["beta"], sub["dy"], theta=sub["theta"],
+                                 init_state=sub["init_state"], prev_x=sub["prev_x"],
+                                 prev_B=sub["prev_B"], dfinal=sub["dfinal"], nthreads=nthr)
+    elif "dy" in sub:
         oracle.ssd_backward(sub["x"], sub["dA"], sub["B"], sub["C"], sub["dy"],
                             init_state=sub["init_state"], dfinal=sub["dfinal"],
                             theta=sub["theta"], nthreads=nthr)
@@ -632,6 +683,7 @@ def run_reference(args, rank, world):
     from chunked_ssd_scan_gb300 import workloads as wl
     is_ss = isinstance(cfg, wl.SelectiveScanConfig)
     host = (wl.make_selective_scan_inputs(cfg, seed=0) if is_ss
+            else wl.make_trap_bwd_inputs(cfg, 0) if cfg.trapezoidal and cfg.backward
             else wl.make_trap_inputs(cfg, 0) if cfg.trapezoidal
             else wl.make_bwd_inputs(cfg, 0) if cfg.backward else wl.make_ssd_inputs(cfg, 0))
     per_step = max(0.5, min(20.0, 150.0 / max(1, args.steps + args.warmup)))

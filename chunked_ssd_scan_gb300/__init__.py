@@ -426,11 +426,12 @@ def ssd_trapezoidal_backward_workspace_bytes(shape: ssd_shape) -> int:
 
 
 def ssd_trapezoidal_backward(x, dA, B, C, gamma, beta, dy, *, theta=None, prev_x=None,
-                             prev_B=None, init_state=None, dfinal=None, workspace=None,
-                             stream=None):
+                             prev_B=None, init_state=None, dfinal=None, grads=None,
+                             workspace=None, stream=None):
     """Gradients of <dy, y> + <dfinal, final_state> for the trapezoidal forward, through
     ``ssd_trapezoidal_backward``.  Returns a dict of f32 tensors dx, ddA, dB, dC, dgamma, dbeta,
-    dtheta (None without theta), dinit, dprev_x and dprev_B (None without a previous write)."""
+    dtheta (None without theta), dinit, dprev_x and dprev_B (None without a previous write),
+    plus the workspace used; `grads` (such a dict) supplies the output tensors."""
     if x.dim() != 5 or B.dim() != 5:
         raise ValueError("x must be [b,T,R,H,P] and B/C [b,T,R,G,N]")
     b, T, R, H, P = x.shape
@@ -458,14 +459,22 @@ def ssd_trapezoidal_backward(x, dA, B, C, gamma, beta, dy, *, theta=None, prev_x
         raise SSDError(2, "ssd_trapezoidal_backward_workspace_bytes (shape not supported)")
     if workspace is None:
         workspace = torch.zeros(need, dtype=torch.uint8, device=x.device)
-    f32 = dict(dtype=torch.float32, device=x.device)
-    g = {"dx": torch.empty((b, T, R, H, P), **f32), "ddA": torch.empty((b, T, H), **f32),
-         "dB": torch.empty((b, T, R, G, N), **f32), "dC": torch.empty((b, T, R, G, N), **f32),
-         "dgamma": torch.empty((b, T, H), **f32), "dbeta": torch.empty((b, T, H), **f32),
-         "dtheta": torch.empty((b, T, H, N // 2), **f32) if theta is not None else None,
-         "dinit": torch.empty((b, H, P, N), **f32),
-         "dprev_x": torch.empty((b, R, H, P), **f32) if prev_x is not None else None,
-         "dprev_B": torch.empty((b, R, G, N), **f32) if prev_x is not None else None}
+    shapes = {"dx": (b, T, R, H, P), "ddA": (b, T, H), "dB": (b, T, R, G, N),
+              "dC": (b, T, R, G, N), "dgamma": (b, T, H), "dbeta": (b, T, H),
+              "dtheta": (b, T, H, N // 2) if theta is not None else None,
+              "dinit": (b, H, P, N),
+              "dprev_x": (b, R, H, P) if prev_x is not None else None,
+              "dprev_B": (b, R, G, N) if prev_x is not None else None}
+    g = {}
+    for k, shp in shapes.items():
+        given = (grads or {}).get(k)
+        if shp is None:
+            g[k] = None
+        elif given is not None:
+            _check_cuda(k, given, torch.float32, shp)
+            g[k] = given
+        else:
+            g[k] = torch.empty(shp, dtype=torch.float32, device=x.device)
     st = lib.ssd_trapezoidal_backward(
         ctypes.byref(shape), _ptr(x), _ptr(dA), _ptr(B), _ptr(C), _ptr(gamma), _ptr(beta),
         _ptr(theta), _ptr(prev_x), _ptr(prev_B), _ptr(init_state), _ptr(dy), _ptr(dfinal),

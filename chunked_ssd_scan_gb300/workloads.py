@@ -73,6 +73,9 @@ class SSDConfig:
             nbytes += b * H * P * N * 4 * 3              # init, dfinal read, dinit written
             if self.theta:
                 nbytes += b * T * H * (N // 2) * 4 * 2   # theta read, dtheta written
+            if self.trapezoidal:
+                nbytes += b * T * H * 4 * 4              # gamma, beta read; dgamma, dbeta written
+                nbytes += b * R * (H * P + G * N) * (e + 4)   # previous write read, its grads
             return nbytes
         nbytes = b * T * R * H * P * e * 2          # x read, y written
         nbytes += b * T * R * G * N * e * 2         # B, C read
@@ -156,6 +159,9 @@ TRAP_MIMO_ROT_F32 = SSDConfig("mamba3_trapezoidal_f32", 1, 16384, 16, 64, 64, 64
 # Backward of the unrotated SSD on config 1's shape (a measured shape of the backward row).
 MAMBA2_BWD_BF16 = SSDConfig("mamba2_backward_bf16", 4, 4096, 32, 64, 128, 64, 1, 1, "bf16",
                             backward=True)
+# Trapezoidal backward on the trapezoidal forward's measured shape.
+TRAP_BWD_F32 = SSDConfig("mamba3_trapezoidal_backward_f32", 1, 16384, 16, 64, 64, 64, 2, 16,
+                         "f32", theta=True, trapezoidal=True, backward=True)
 # Rotated backward on config 3's shape (a measured shape of the backward row).
 LONG_ROT_BWD_F32 = SSDConfig("long_rotation_backward_f32", 1, 131072, 24, 64, 64, 256, 1, 24,
                              "f32", theta=True, backward=True)
@@ -223,6 +229,21 @@ def make_trap_inputs(cfg: SSDConfig, seed: int = 0, *, slow_decay: bool = False,
                          ).to(cfg.torch_dtype)
         out["prev_B"] = (torch.randn((b, R, G, N), generator=g, dtype=f32) * cfg.bc_scale
                          ).to(cfg.torch_dtype)
+    if device is not None:
+        out = {k: (v.to(device) if v is not None else None) for k, v in out.items()}
+    return out
+
+
+def make_trap_bwd_inputs(cfg: SSDConfig, seed: int = 0, *,
+                         device: Optional[str] = None) -> dict:
+    """A trapezoidal forward problem (initial state, previous write) plus the cotangents dy and
+    dfinal (standard normal f32, from a third generator) for its backward."""
+    out = make_trap_inputs(cfg, seed, init_state=True, prev=True)
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed + 7919)
+    b, T, R, H, P, N = cfg.batch, cfg.seqlen, cfg.mimo_rank, cfg.nheads, cfg.headdim, cfg.dstate
+    out["dy"] = torch.randn((b, T, R, H, P), generator=g, dtype=torch.float32)
+    out["dfinal"] = torch.randn((b, H, P, N), generator=g, dtype=torch.float32)
     if device is not None:
         out = {k: (v.to(device) if v is not None else None) for k, v in out.items()}
     return out

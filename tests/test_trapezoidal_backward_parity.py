@@ -76,3 +76,31 @@ def test_trapezoidal_backward_rejections():
     st = lib.ssd_trapezoidal_backward(ctypes.byref(too_wide), *([None] * 23), ctypes.c_size_t(0),
                                       None)
     assert pkg.STATUS[st] == "SSD_ERR_UNSUPPORTED"
+
+
+def test_trapezoidal_backward_full_size_sampled():
+    """The measured trapezoidal backward shape (T = 16384, 16 heads, P = N = 64, R = 2, one B/C
+    group per head, rotation, f32) through the launch the bench times; the oracle recomputes
+    heads 0 and 15 (each its own group, so every gradient of those heads is checked)."""
+    cfg = wl.TRAP_BWD_F32
+    inp = wl.make_trap_bwd_inputs(cfg, seed=0)   # the bench's inputs
+    got = _gpu(inp)
+    for h in (0, 15):
+        hs = slice(h, h + 1)
+        sub = {"x": inp["x"][:, :, :, hs], "dA": inp["dA"][:, :, hs],
+               "B": inp["B"][:, :, :, hs], "C": inp["C"][:, :, :, hs],
+               "gamma": inp["gamma"][:, :, hs], "beta": inp["beta"][:, :, hs],
+               "theta": inp["theta"][:, :, hs], "dy": inp["dy"][:, :, :, hs],
+               "init_state": inp["init_state"][:, hs], "dfinal": inp["dfinal"][:, hs],
+               "prev_x": inp["prev_x"][:, :, hs], "prev_B": inp["prev_B"][:, :, hs]}
+        ref = _oracle(sub)
+        view = {"dx": got["dx"][:, :, :, hs], "ddA": got["ddA"][:, :, hs],
+                "dB": got["dB"][:, :, :, hs], "dC": got["dC"][:, :, :, hs],
+                "dgamma": got["dgamma"][:, :, hs], "dbeta": got["dbeta"][:, :, hs],
+                "dtheta": got["dtheta"][:, :, hs], "dinit": got["dinit"][:, hs],
+                "dprev_x": got["dprev_x"][:, :, hs], "dprev_B": got["dprev_B"][:, :, hs]}
+        for k in sorted(ref):
+            if k in ("ddA", "dtheta", "dgamma", "dbeta"):
+                check_close_inner(view[k], ref[k], TOL["f32"], f"{k} head {h}")
+            else:
+                check_close(view[k], ref[k], TOL["f32"], f"{k} head {h}")
