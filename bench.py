@@ -214,6 +214,13 @@ def job_tokens(tokens_per_replica: int, world: int) -> int:
     return tokens_per_replica * world
 
 
+def kernel_chunk(pkg, shape, R, chunk_len):
+    """Steps per chunk the kernels actually tile by: the register-tiled fp32 path uses 64 fused
+    rows (64 / R steps) whatever chunk_len says; every other path tiles by chunk_len (the fused
+    bf16 kernel's FLOPs are not its bound, so its count keeps chunk_len)."""
+    return 64 // R if pkg.ssd_chunked_variant(shape) == "tiled_f32" else chunk_len
+
+
 def run_ours(args, rank, world, local):
     import chunked_ssd_scan_gb300 as pkg
     from chunked_ssd_scan_gb300 import workloads as wl
@@ -299,7 +306,12 @@ def run_ours(args, rank, world, local):
         launches_per_call = 2 + 3 + (2 if cfg.theta else 0) + 1
         dtype = cfg.dtype
         io_bytes = cfg.io_bytes()
-        flops = cfg.with_(mimo_rank=2 * cfg.mimo_rank).causal_flops()
+        exp = pkg.make_shape(cfg.batch, cfg.seqlen, cfg.nheads, cfg.headdim, cfg.dstate,
+                             cfg.nheads if cfg.theta else cfg.ngroups, 2 * cfg.mimo_rank,
+                             cfg.chunk_len, "f32", cfg.theta)
+        flops = cfg.with_(mimo_rank=2 * cfg.mimo_rank,
+                          chunk_len=kernel_chunk(pkg, exp, 2 * cfg.mimo_rank, cfg.chunk_len)
+                          ).causal_flops()
     elif cfg.rope_dim or cfg.halves:
         import ctypes
         host = wl.make_ssd_inputs(cfg, seed=0)
@@ -322,7 +334,8 @@ def run_ours(args, rank, world, local):
                              + (1 if cfg.rope_dim and cfg.rope_dim < cfg.dstate else 0))
         dtype = cfg.dtype
         io_bytes = cfg.io_bytes()
-        flops = cfg.causal_flops()
+        flops = cfg.with_(chunk_len=kernel_chunk(pkg, shape, cfg.mimo_rank,
+                                                 cfg.chunk_len)).causal_flops()
     else:
         host = wl.make_ssd_inputs(cfg, seed=0)
         d = {k: (v.to(dev) if v is not None else None) for k, v in host.items()}
@@ -339,7 +352,8 @@ def run_ours(args, rank, world, local):
         launches_per_call = pkg.ssd_chunked_launches(shape)
         dtype = cfg.dtype
         io_bytes = cfg.io_bytes()
-        flops = cfg.causal_flops()
+        flops = cfg.with_(chunk_len=kernel_chunk(pkg, shape, cfg.mimo_rank,
+                                                 cfg.chunk_len)).causal_flops()
 
     if world > 1:
         torch.distributed.barrier()
@@ -384,6 +398,22 @@ def run_ours(args, rank, world, local):
                 "algorithmic_bytes_per_launch": io_bytes,
                 "hbm_gbs": round(io_bytes / (ms * 1e-3) / 1e9, 1),
                 "hbm_frac": round(io_bytes / (ms * 1e-3) / 1e9 / hbm, 4)}
+    elif flops and variant != "tc_bf16":
+        # fp32 paths run their contractions as fp32 FMAs on the CUDA cores (no tensor cores:
+        # the fp32 accumulator of the tensor core truncates); the tighter of the HBM and the
+        # fp32-lane bound is the roofline
+        alu = ALU_FP32_TFLOPS
+        t_hbm, t_alu = io_bytes / (hbm * 1e9), flops / (alu * 1e12)
+        a_tf = flops / (ms * 1e-3) / 1e12
+        roof["alu_tflops"] = round(a_tf, 2)
+        roof["alu_frac"] = round(a_tf / alu, 4)
+        if t_alu > t_hbm:
+            roof.update({"bound": "alu", "achieved": round(a_tf, 2), "peak": alu,
+                         "unit": "TFLOP/s", "frac": round(a_tf / alu, 4),
+                         "peak_source": "derived: 152 SMs x 128 fp32 lanes x 2 FLOP x 2.07 GHz",
+                         "algorithmic_flops_per_launch": flops,
+                         "hbm_gbs": round(achieved, 1), "hbm_frac": round(achieved / hbm, 4)})
+        roof["roofline_frac"] = round(max(t_hbm, t_alu) / (ms * 1e-3), 4)
     elif flops:
         roof["tensor_tflops"] = round(flops / (ms * 1e-3) / 1e12, 2)
         roof["tensor_frac_of_bf16_peak"] = round(flops / (ms * 1e-3) / 1e12 / tf, 4)
