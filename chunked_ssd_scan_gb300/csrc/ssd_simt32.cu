@@ -137,17 +137,19 @@ __device__ __forceinline__ int tile_ty() {
 }
 
 // acc[r][c] += sum_k At[k][4 ty + r] * Bt[k][4 tx + c] over k < 64 (both operands k-major,
-// 64 floats per k row).  With kSwzA the 16-byte chunks of At's row k are stored permuted
-// (chunk c at c ^ ((k >> 2) & 15)), the layout the masked operand is written in.
-template <bool kSwzA = false>
+// 64 floats per k row).  With kSwzA (kSwzB) the 16-byte chunks of At's (Bt's) row k are stored
+// permuted, chunk c at c ^ ((k >> 2) & 15): the layouts the masked operand and the transposed
+// h_in are written in.
+template <bool kSwzA = false, bool kSwzB = false>
 __device__ __forceinline__ void block_product(const float* __restrict__ At,
                                               const float* __restrict__ Bt, int ty, int tx,
                                               float (&acc)[4][4]) {
 #pragma unroll 8
   for (int k = 0; k < kT64; ++k) {
     const int ca = kSwzA ? (ty ^ ((k >> 2) & 15)) : ty;
+    const int cb = kSwzB ? (tx ^ ((k >> 2) & 15)) : tx;
     const float4 a = *reinterpret_cast<const float4*>(At + k * kT64 + 4 * ca);
-    const float4 bq = *reinterpret_cast<const float4*>(Bt + k * kT64 + 4 * tx);
+    const float4 bq = *reinterpret_cast<const float4*>(Bt + k * kT64 + 4 * cb);
     const float av[4] = {a.x, a.y, a.z, a.w};
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
@@ -326,11 +328,19 @@ __global__ void __launch_bounds__(kSimtThreads, 3) simt_scan_kernel(GenericParam
   chunk_prefix64(p.dA + (b * p.T + c * p.l) * p.H + h, p.H, l, steps64(p, c), cum_hi, cum_lo,
                  nullptr);
   {
-    // h_in [p][n] (written over S by the state pass) -> h^T [n][p]
-    const float* hin = p.states + ((b * p.nch + c) * p.H + h) * kTileFloats;
-    // lanes over consecutive p: conflict-free shared stores of h^T[n][p]
-    for (int e = threadIdx.x; e < kTileFloats; e += kSimtThreads)
-      ht[(e / kT64) * kT64 + e % kT64] = hin[(e % kT64) * kT64 + e / kT64];
+    // h_in [p][n] (written over S by the state pass) -> h^T [n][p] with the 16-byte chunks of
+    // row n permuted (chunk c at c ^ ((n >> 2) & 15)): half-warps read whole rows p as float4
+    // (coalesced), and the transposed scalar stores of a warp then spread over the bank groups
+    const float4* hin = reinterpret_cast<const float4*>(
+        p.states + ((b * p.nch + c) * p.H + h) * kTileFloats);
+    for (int e = threadIdx.x; e < kTileFloats / 4; e += kSimtThreads) {
+      const int pp = e >> 4, q = e & 15;   // row p, n = 4 q .. 4 q + 3
+      const float4 v = __ldg(hin + e);
+      const float vv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        ht[(4 * q + i) * kT64 + 4 * ((pp >> 2) ^ q) + (pp & 3)] = vv[i];
+    }
   }
   if (p.theta) {
     chunk_angles64(p, b, c, h, l, ang, true);
@@ -346,7 +356,7 @@ __global__ void __launch_bounds__(kSimtThreads, 3) simt_scan_kernel(GenericParam
     stage_bc64(p, Csrc, b, c, g, i0, ang, ct, true);
     __syncthreads();
     float yo[4][4] = {};
-    block_product(ct, ht, ty, tx, yo);   // Yo[i][p] = sum_n C~[i][n] h[p][n]
+    block_product<false, true>(ct, ht, ty, tx, yo);   // Yo[i][p] = sum_n C~[i][n] h[p][n]
     float yd[4][4] = {};
     for (int j0 = 0; j0 <= i0; j0 += kT64) {
       stage_bc64(p, Bsrc, b, c, g, j0, ang, bt, true);
