@@ -1,4 +1,4 @@
-// Backward of the chunked SSD forward (unrotated; CUDA-core fp32), recompute per chunk.
+// Backward of the chunked SSD forward (CUDA-core fp32), recompute per chunk.
 //
 // The scan.py page asks for a scan that can train; the moments.rs page's memory model keeps only
 // the chunk-boundary states and recomputes inside a chunk.  Three launches:
@@ -16,7 +16,8 @@
 //      and the gradient of every prefix sum cum_s (from L, exp(cum_i), exp(cum_end - cum_j) and
 //      exp(cum_end) h_in), whose suffix sums over the chunk's steps are ddA.
 // Rows are rank-fused (i = t R + r, step i / R), 64 per chunk; dB and dC add over the heads of a
-// group.
+// group.  With the rotation the same three kernels run in chunk-local frames (the rotation
+// section below), around angle, staging and chain-rule kernels.
 #include <math.h>
 #include <string.h>
 

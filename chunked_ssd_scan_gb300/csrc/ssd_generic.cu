@@ -479,14 +479,6 @@ cudaError_t generic_state_pass(const GenericParams& p, cudaStream_t st) {
   return cudaGetLastError();
 }
 
-cudaError_t generic_states(const GenericParams& p, bool bf16, cudaStream_t st) {
-  const size_t s1 = generic_state_smem(p.l, p.P, p.N, p.theta != nullptr);
-  cudaError_t e = bf16 ? launch_state_dispatch<__nv_bfloat16>(p, s1, st)
-                       : launch_state_dispatch<float>(p, s1, st);
-  if (e != cudaSuccess) return e;
-  return generic_state_pass(p, st);
-}
-
 cudaError_t generic_forward(const GenericParams& p, bool bf16, cudaStream_t st) {
   cudaError_t e;
   if (p.theta && (e = generic_phi(p, st)) != cudaSuccess) return e;

@@ -37,8 +37,6 @@ cudaError_t generic_forward(const GenericParams& p, bool bf16, cudaStream_t st);
 // (phi, phisum) and the K4 pass over chunks (states -> h_in in place, final state).
 cudaError_t generic_phi(const GenericParams& p, cudaStream_t st);
 cudaError_t generic_state_pass(const GenericParams& p, cudaStream_t st);
-// K1 + K3 + K4 only: the chunk-input state h_in(c) of every chunk in p.states (no y).
-cudaError_t generic_states(const GenericParams& p, bool bf16, cudaStream_t st);
 // fp32 I/O with P = N = 64, mimo_rank 1, 64 | chunk_len <= 512: register-tiled CUDA-core kernels.
 bool simt32_supported(int64_t P, int64_t N, int64_t R, int64_t l, bool bf16, bool theta);
 cudaError_t simt32_forward(const GenericParams& p, cudaStream_t st);
