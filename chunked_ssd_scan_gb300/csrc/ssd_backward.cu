@@ -310,6 +310,29 @@ __device__ __forceinline__ float half_warp_sum(float v) {
   return v;
 }
 
+// acc[a][q] += sum_k U[ri[a]][k] V[cj[q]][k] over the row length K4 (rows at stride S, read 4 k at
+// a time).  With kTri the blocks q > a (entirely above the step diagonal) are skipped.
+template <bool kTri>
+__device__ __forceinline__ void pair_products(const float* U, const float* V, int S, int K4,
+                                              const int (&ri)[4], const int (&cj)[4],
+                                              float (&acc)[4][4]) {
+  for (int k0 = 0; k0 < K4; k0 += 4) {
+    float uv[4][4], vv[4][4];
+#pragma unroll
+    for (int a = 0; a < 4; ++a) {
+      lds_vec<4>(U + ri[a] * S + k0, uv[a]);
+      lds_vec<4>(V + cj[a] * S + k0, vv[a]);
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+#pragma unroll
+      for (int a = 0; a < 4; ++a)
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          if (!kTri || q <= a) acc[a][q] = fmaf(uv[a][k], vv[q][k], acc[a][q]);
+  }
+}
+
 // Every gradient of one chunk (one CTA per (c, h, b)); dB and dC are added atomically (the heads
 // of a group share them and were zeroed by the caller); dx and ddA are written for real steps.
 // The per-row gradients are register-tiled products over the chunk's rows or the state:
@@ -438,33 +461,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       ri[a] = min(t16 + 16 * a, Lr - 1);
       cj[a] = min(l16 + 16 * a, Lr - 1);
     }
-    for (int n = 0; n < N4; n += 4) {
-      float cv[4][4], bv[4][4];
-#pragma unroll
-      for (int a = 0; a < 4; ++a) {
-        lds_vec<4>(sC + ri[a] * NS + n, cv[a]);
-        lds_vec<4>(sB + cj[a] * NS + n, bv[a]);
-      }
-#pragma unroll
-      for (int k = 0; k < 4; ++k)
-#pragma unroll
-        for (int a = 0; a < 4; ++a)
-#pragma unroll
-          for (int q = 0; q < 4; ++q) cb[a][q] = fmaf(cv[a][k], bv[q][k], cb[a][q]);
-    }
-    for (int pp = 0; pp < P4; pp += 4) {
-      float dv[4][4], xv[4][4];
-#pragma unroll
-      for (int a = 0; a < 4; ++a) {
-        lds_vec<4>(sdy + ri[a] * PS + pp, dv[a]);
-        lds_vec<4>(sx + cj[a] * PS + pp, xv[a]);
-      }
-#pragma unroll
-      for (int k = 0; k < 4; ++k)
-#pragma unroll
-        for (int a = 0; a < 4; ++a)
-#pragma unroll
-          for (int q = 0; q < 4; ++q) dx4[a][q] = fmaf(dv[a][k], xv[q][k], dx4[a][q]);
+    // with R | 16 the 16-row blocks hold whole steps, so the blocks above the diagonal are zero
+    if ((16 % R) == 0) {
+      pair_products<true>(sC, sB, NS, N4, ri, cj, cb);
+      pair_products<true>(sdy, sx, PS, P4, ri, cj, dx4);
+    } else {
+      pair_products<false>(sC, sB, NS, N4, ri, cj, cb);
+      pair_products<false>(sdy, sx, PS, P4, ri, cj, dx4);
     }
     float rs[4] = {0.f, 0.f, 0.f, 0.f}, cs[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
