@@ -254,6 +254,23 @@ size_t simt_state_smem(int64_t l, bool theta) {
   return sizeof(float) * (2 * kTileFloats + 3 * l + (theta ? l * kPairs64 : 0) + 4);
 }
 
+// Raw x and B rows of the chunk's first 64 fused rows into xs[row][p] and bs[row][n] with
+// 16-byte cp.async (not waited for); rows past the chunk's real ones are zero-filled.
+__device__ void issue_rows64(const GenericParams& p, int64_t b, int64_t c, int64_t h, int64_t g,
+                             float* xs, float* bs) {
+  const float* xsrc = static_cast<const float*>(p.x);
+  const float* bsrc = static_cast<const float*>(p.B);
+  const int nvr = steps64(p, c) * (int)p.R;
+  const int64_t row0 = (b * p.T + c * p.l) * p.R;
+  for (int e = threadIdx.x; e < kTileFloats / 4; e += kSimtThreads) {
+    const int row = e / (kT64 / 4), q = e % (kT64 / 4);
+    const bool real = row < nvr;
+    const int64_t r = row0 + (real ? row : 0);
+    cp_async16(xs + row * kT64 + 4 * q, xsrc + (r * p.H + h) * kT64 + 4 * q, real ? 16 : 0);
+    cp_async16(bs + row * kT64 + 4 * q, bsrc + (r * p.G + g) * kT64 + 4 * q, real ? 16 : 0);
+  }
+}
+
 __global__ void __launch_bounds__(kSimtThreads) simt_state_kernel(GenericParams p) {
   extern __shared__ __align__(16) float sm64[];
   const int64_t c = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
@@ -266,21 +283,46 @@ __global__ void __launch_bounds__(kSimtThreads) simt_state_kernel(GenericParams 
   float* dec = cum_lo + l;
   float* ang = dec + l;
   float* total = ang + (p.theta ? l * kPairs64 : 0);
+  // the first block's raw rows are in flight while the prefix sums and the angles are formed
+  issue_rows64(p, b, c, h, g, xs, bs);
   chunk_prefix64(p.dA + (b * p.T + c * p.l) * p.H + h, p.H, l, steps64(p, c), cum_hi, cum_lo,
                  total);
   if (p.theta) {
-    chunk_angles64(p, b, c, h, l, ang);
+    chunk_angles64(p, b, c, h, l, ang);   // its wait covers the rows too
   } else {
     __syncthreads();
   }
   for (int t = threadIdx.x; t < l; t += kSimtThreads)
     dec[t] = exp2f((cum_hi[l - 1] - cum_hi[t]) + (cum_lo[l - 1] - cum_lo[t]));
+  cp_async_wait_all();
   __syncthreads();
   const int tx = tile_tx(), ty = tile_ty();   // output rows p = 4 ty.., cols n = 4 tx..
+  const int rs = rank_shift(p);
   float acc[4][4] = {};
   for (int j0 = 0; j0 < l * (int)p.R; j0 += kT64) {   // fused rows
-    stage_x64(p, b, c, h, j0, dec, xs);
-    stage_bc64(p, static_cast<const float*>(p.B), b, c, g, j0, ang, bs, false);
+    if (j0 == 0) {
+      // in place: x rows scaled by the decay to the chunk end, B rows turned by -Phi
+      for (int e = threadIdx.x; e < kTileFloats / 4; e += kSimtThreads) {
+        const int row = e / (kT64 / 4);
+        float4* x4 = reinterpret_cast<float4*>(xs) + e;
+        const float w = dec[row >> rs];
+        const float4 v = *x4;
+        *x4 = make_float4(v.x * w, v.y * w, v.z * w, v.w * w);
+      }
+      if (p.theta) {
+        for (int e = threadIdx.x; e < kTileFloats / 2; e += kSimtThreads) {
+          const int row = e / kPairs64, k = e % kPairs64;
+          float2* b2 = reinterpret_cast<float2*>(bs) + e;
+          float sn, co;
+          sincosf(ang[(row >> rs) * kPairs64 + k], &sn, &co);
+          const float2 v = *b2;
+          *b2 = make_float2(co * v.x + sn * v.y, -sn * v.x + co * v.y);
+        }
+      }
+    } else {
+      stage_x64(p, b, c, h, j0, dec, xs);
+      stage_bc64(p, static_cast<const float*>(p.B), b, c, g, j0, ang, bs, false);
+    }
     __syncthreads();
     block_product(xs, bs, ty, tx, acc);   // S[p][n] += sum_j X~[j][p] B~[j][n]
     __syncthreads();
