@@ -140,12 +140,14 @@ __device__ __forceinline__ int tile_ty() {
 // 64 floats per k row).  With kSwzA (kSwzB) the 16-byte chunks of At's (Bt's) row k are stored
 // permuted, chunk c at c ^ ((k >> 2) & 15): the layouts the masked operand and the transposed
 // h_in are written in.
+// kmax (a multiple of 8, uniform over the warp) ends the reduction early where the rest of A's
+// k rows are known to be zero.
 template <bool kSwzA = false, bool kSwzB = false>
 __device__ __forceinline__ void block_product(const float* __restrict__ At,
                                               const float* __restrict__ Bt, int ty, int tx,
-                                              float (&acc)[4][4]) {
+                                              float (&acc)[4][4], int kmax = kT64) {
 #pragma unroll 8
-  for (int k = 0; k < kT64; ++k) {
+  for (int k = 0; k < kmax; ++k) {
     const int ca = kSwzA ? (ty ^ ((k >> 2) & 15)) : ty;
     const int cb = kSwzB ? (tx ^ ((k >> 2) & 15)) : tx;
     const float4 a = *reinterpret_cast<const float4*>(At + k * kT64 + 4 * ca);
@@ -404,8 +406,15 @@ __global__ void __launch_bounds__(kSimtThreads, 3) simt_scan_kernel(GenericParam
       stage_bc64(p, Bsrc, b, c, g, j0, ang, bt, true);
       if (j0 > 0 || i0 > 0) stage_x64(p, b, c, h, j0, nullptr, xs);   // tile 0 was prefetched
       __syncthreads();
+      // On the diagonal tile this warp's rows i0 + 16 (w >> 1) .. + 15 see no source row of a
+      // later step: its C~B~ block is skipped when every column is such a row (the mask below
+      // then writes zeros), and its (L o CB) x product stops at the first such row.
+      const bool diag = j0 == i0;
+      const int wrow = i0 + 16 * (threadIdx.x >> 6) + 15, wcol = j0 + 32 * ((threadIdx.x >> 5) & 1);
+      const bool cb_zero = diag && (wcol >> rs) > (wrow >> rs);
+      const int kmax = diag ? min(kT64, (((wrow >> rs) + 1) << rs) - j0) : kT64;
       float cb[4][4] = {};
-      block_product(ct, bt, ty, tx, cb);   // CB[i][j] = sum_n C~[i][n] B~[j][n]
+      if (!cb_zero) block_product(ct, bt, ty, tx, cb);   // CB[i][j] = sum_n C~[i][n] B~[j][n]
       __syncthreads();                     // every read of B~^T done before M^T overwrites it
       // (L o CB)^T: causal cut before the exponential
 #pragma unroll
@@ -425,7 +434,7 @@ __global__ void __launch_bounds__(kSimtThreads, 3) simt_scan_kernel(GenericParam
             make_float4(m[0], m[1], m[2], m[3]);
       }
       __syncthreads();
-      block_product<true>(bt, xs, ty, tx, yd);   // Yd[i][p] += sum_j M[i][j] x[j][p]
+      block_product<true>(bt, xs, ty, tx, yd, kmax);   // Yd[i][p] += sum_j M[i][j] x[j][p]
       __syncthreads();
     }
     const int nvr = steps64(p, c) * R;
