@@ -163,3 +163,60 @@ def test_wait_selftest_argument_checks(lib):
     assert f(_VP(A16), 128, 1000, None) == 4                  # smaller than the header
     assert f(_VP(A16), 256, 0, None) == 1                     # no wait
     assert f(_VP(A16), 256, 200_000_000, None) == 1           # above the 100 ms cap
+
+
+def _bwd(lib, shape, theta=None, dtheta=None, dx=A16, ddA=A16, x=A16, ws=A16, ws_bytes=None):
+    if ws_bytes is None:
+        ws_bytes = lib.ssd_backward_workspace_bytes(ctypes.byref(shape))
+    return lib.ssd_chunked_backward(ctypes.byref(shape), _VP(x), _VP(A16), _VP(A16), _VP(A16),
+                                    _VP(theta), _VP(None), _VP(A16), _VP(None), _VP(dx),
+                                    _VP(ddA), _VP(A16), _VP(A16), _VP(dtheta), _VP(None),
+                                    _VP(ws), ctypes.c_size_t(ws_bytes), _VP(None))
+
+
+def test_backward_workspace_sizes(lib):
+    plain = _shape(wl.TINY_SISO_F32)
+    rot = _shape(wl.TINY_SISO_F32, has_theta=1)
+    assert lib.ssd_backward_workspace_bytes(ctypes.byref(plain)) > 0
+    assert (lib.ssd_backward_workspace_bytes(ctypes.byref(rot))
+            > lib.ssd_backward_workspace_bytes(ctypes.byref(plain)))
+    for bad in (_shape(wl.TINY_SISO_F32, headdim=128), _shape(wl.TINY_SISO_F32, dstate=18),
+                _shape(wl.TINY_SISO_F32, dstate=256), _shape(wl.TINY_SISO_F32, mimo_rank=128)):
+        assert lib.ssd_backward_workspace_bytes(ctypes.byref(bad)) == 0
+    trap = _shape(wl.TINY_SISO_F32, mimo_rank=2)
+    assert lib.ssd_trapezoidal_backward_workspace_bytes(ctypes.byref(trap)) > 0
+    wide = _shape(wl.TINY_SISO_F32, mimo_rank=64)   # 128 write channels after the expansion
+    assert lib.ssd_trapezoidal_backward_workspace_bytes(ctypes.byref(wide)) == 0
+
+
+@no_gpu_only
+def test_backward_host_rejections(lib):
+    """Rejected on the host before any launch (no GPU needed)."""
+    plain = _shape(wl.TINY_SISO_F32)
+    rot = _shape(wl.TINY_SISO_F32, has_theta=1)
+    assert _bwd(lib, plain, x=None) == 1                       # x missing
+    assert _bwd(lib, plain, ddA=None) == 1                     # ddA missing
+    assert _bwd(lib, plain, dx=A16 + 4) == 1                   # misaligned gradient
+    assert _bwd(lib, plain, theta=A16, dtheta=A16) == 1        # theta without has_theta
+    assert _bwd(lib, rot, theta=None, dtheta=A16) == 1         # has_theta without theta
+    assert _bwd(lib, rot, theta=A16, dtheta=None) == 1         # no dtheta for theta
+    assert _bwd(lib, plain, ws=None) == 4
+    assert _bwd(lib, plain, ws_bytes=64) == 4
+    assert _bwd(lib, plain, ws=A16 + 16) == 4
+    assert _bwd(lib, _shape(wl.TINY_SISO_F32, dstate=18), ws_bytes=1 << 30) == 2
+    f = lib.ssd_trapezoidal_backward
+    trap = _shape(wl.TINY_SISO_F32, mimo_rank=2)
+    need = lib.ssd_trapezoidal_backward_workspace_bytes(ctypes.byref(trap))
+    # x dA B C gamma beta | theta prev_x prev_B init | dy | dfinal | dx ddA dB dC dgamma dbeta |
+    # dtheta dinit dprev_x dprev_B | workspace
+    ptrs = ([_VP(A16)] * 6 + [_VP(None)] * 4 + [_VP(A16)] + [_VP(None)] + [_VP(A16)] * 6
+            + [_VP(None)] * 4 + [_VP(A16)])
+    assert len(ptrs) == 23
+    args = lambda p, nbytes: (ctypes.byref(trap), *p, ctypes.c_size_t(nbytes), _VP(None))
+    assert f(*args(ptrs, need - 1)) == 4                        # workspace too small
+    bad = list(ptrs)
+    bad[4] = _VP(None)                                          # gamma missing
+    assert f(*args(bad, need)) == 1
+    bad = list(ptrs)
+    bad[7] = _VP(A16)                                           # prev_x without prev_B
+    assert f(*args(bad, need)) == 1
