@@ -148,21 +148,23 @@ MAMBA3_MIMO_BF16 = SSDConfig("mamba3_mimo_bf16", 2, 8192, 32, 64, 128, 64, 4, 32
 LONG_ROT_F32 = SSDConfig("long_rotation_f32", 1, 131072, 24, 64, 64, 256, 1, 24, "f32",
                          theta=True)
 SELECTIVE_SCAN_F32 = SelectiveScanConfig("selective_scan_f32", 4, 4096, 512, 16)
-# Rotation variant: config 3's shape at T = 32768 with half of the state rotated, split-halves
-# pairing (a measured shape of the rotation-variant row; not one of the five workloads).
+# Rotation variant: the long-rotation shape (24 heads, P = N = 64) at T = 32768 with half of the
+# state rotated and the split-halves pairing; a measured shape, not one of the five workloads.
 ROT_VARIANT_F32 = SSDConfig("rotation_halves_rope32_f32", 1, 32768, 24, 64, 64, 256, 1, 24,
                             "f32", theta=True, rope_dim=32, halves=True)
-# Trapezoidal Mamba-3 (a measured shape of the trapezoidal row; not one of the five workloads).
+# Trapezoidal Mamba-3 (T = 16384, 16 heads, P = N = 64, R = 2, rotation); a measured shape, not
+# one of the five workloads.
 TRAP_MIMO_ROT_F32 = SSDConfig("mamba3_trapezoidal_f32", 1, 16384, 16, 64, 64, 64, 2, 16, "f32",
                               theta=True, trapezoidal=True)
 
-# Backward of the unrotated SSD on config 1's shape (a measured shape of the backward row).
+# Backward of the unrotated SSD on the Mamba-2 SISO shape (4 x 4096 steps, 32 heads, P = 64,
+# N = 128, bf16 inputs).
 MAMBA2_BWD_BF16 = SSDConfig("mamba2_backward_bf16", 4, 4096, 32, 64, 128, 64, 1, 1, "bf16",
                             backward=True)
-# Trapezoidal backward on the trapezoidal forward's measured shape.
+# Trapezoidal backward on the trapezoidal forward's shape above.
 TRAP_BWD_F32 = SSDConfig("mamba3_trapezoidal_backward_f32", 1, 16384, 16, 64, 64, 64, 2, 16,
                          "f32", theta=True, trapezoidal=True, backward=True)
-# Rotated backward on config 3's shape (a measured shape of the backward row).
+# Rotated backward on the long-rotation shape (T = 131072, 24 heads, P = N = 64, f32).
 LONG_ROT_BWD_F32 = SSDConfig("long_rotation_backward_f32", 1, 131072, 24, 64, 64, 256, 1, 24,
                              "f32", theta=True, backward=True)
 
