@@ -435,7 +435,7 @@ __global__ void __launch_bounds__(kSimtThreads, 3) simt_scan_kernel(GenericParam
       }
       __syncthreads();
       block_product<true>(bt, xs, ty, tx, yd, kmax);   // Yd[i][p] += sum_j M[i][j] x[j][p]
-      __syncthreads();
+      if (j0 < i0) __syncthreads();   // the next source tile overwrites B~^T / M^T and x
     }
     const int nvr = steps64(p, c) * R;
     const int64_t row0 = (b * p.T + c * p.l) * R;
@@ -450,6 +450,9 @@ __global__ void __launch_bounds__(kSimtThreads, 3) simt_scan_kernel(GenericParam
           make_float4(fmaf(sc, yo[r][0], yd[r][0]), fmaf(sc, yo[r][1], yd[r][1]),
                       fmaf(sc, yo[r][2], yd[r][2]), fmaf(sc, yo[r][3], yd[r][3]));
     }
+    // the next row tile restages C~^T, B~^T and x; after the last one the warps that finished
+    // their (shorter) masked product early retire without waiting
+    if (i0 + kT64 < l * R) __syncthreads();
   }
 }
 
