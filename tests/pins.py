@@ -456,5 +456,27 @@ def pin_trapezoidal_backward_finite_differences(mutation=0):
     return res
 
 
+def pin_trapezoidal_backward_reduces_to_plain(mutation=0):
+    """beta = 0, gamma = 1 and no previous write make the trapezoidal recurrence the plain
+    rotated one, so its reverse mode must give the plain reverse mode's gradients (two
+    separately written reverse modes agreeing), with and without the rotation."""
+    res = []
+    for rot in (False, True):
+        x, dA, B, C, _, bt, th, h0, _, _ = _trap_problem(81 + rot, 2, 70, 2, 2, 1, 3, 4,
+                                                         theta=rot, prev=False)
+        gm, bt = np.ones_like(bt), np.zeros_like(bt)
+        r = _rng(83 + rot)
+        dy = r.standard_normal(x.shape)
+        dfin = r.standard_normal(h0.shape)
+        gt = oracle.ssd_trap_backward(x, dA, B, C, gm, bt, dy, theta=th, init_state=h0,
+                                      dfinal=dfin, mutation=mutation)
+        gp = oracle.ssd_backward(x, dA, B, C, dy, h0, dfin, theta=th)
+        for k in ("dx", "ddA", "dB", "dC", "dinit") + (("dtheta",) if rot else ()):
+            tag = "rot_" if rot else ""
+            res.append((f"trap_as_plain_{tag}{k}", _maxerr(gt[k], gp[k]), 1e-10))
+    return res
+
+
 BWD_PINS = [pin_backward_finite_differences]
-TRAP_BWD_PINS = [pin_trapezoidal_backward_finite_differences]
+TRAP_BWD_PINS = [pin_trapezoidal_backward_finite_differences,
+                 pin_trapezoidal_backward_reduces_to_plain]
