@@ -104,3 +104,22 @@ def test_trapezoidal_backward_full_size_sampled():
                 check_close_inner(view[k], ref[k], TOL["f32"], f"{k} head {h}")
             else:
                 check_close(view[k], ref[k], TOL["f32"], f"{k} head {h}")
+
+
+def test_trapezoidal_backward_reduces_to_the_plain_backward():
+    """gamma = 1, beta = 0, no previous write: ssd_trapezoidal_backward equals
+    ssd_chunked_backward on the same data (rotated), through two different GPU paths."""
+    cfg = wl.SSDConfig("tbwd_plain", 1, 150, 4, 16, 32, 64, 2, 2, "f32", theta=True, **T)
+    inp = _draw(cfg, 53, "slow_decay_init_prev")
+    inp["gamma"] = torch.ones_like(inp["gamma"])
+    inp["beta"] = torch.zeros_like(inp["beta"])
+    inp["prev_x"] = inp["prev_B"] = None
+    got = _gpu(inp)
+    d = {k: (v.cuda() if v is not None else None) for k, v in inp.items()}
+    plain = pkg.ssd_chunked_backward(d["x"], d["dA"], d["B"], d["C"], d["dy"], theta=d["theta"],
+                                     init_state=d["init_state"], dfinal=d["dfinal"])
+    torch.cuda.synchronize()
+    # each path is within TOL of the oracle, so the two are within twice that of each other
+    for k in ("dx", "ddA", "dB", "dC", "dtheta", "dinit"):
+        gate = check_close_inner if k in ("ddA", "dtheta") else check_close
+        gate(got[k], to_np(plain[k]), 2 * TOL["f32"], f"trapezoid(beta=0) vs plain {k}")
