@@ -169,3 +169,94 @@ def trapezoidal_absorbed(x, dA, B, C, gamma, beta, theta=None, init_state=None, 
         y[:, t] = np.einsum("brhn,bhpn->brhp", Ch[:, t], h)
     final = rotate_pairs(g, phi[:, T - 1][:, :, None, :]) if T else g
     return y, final
+
+
+def chunked_backward(x, dA, B, C, dy, init_state=None, dfinal=None, chunk_len=64):
+    """Reverse mode of the unrotated SSD in the chunked form the GPU backward uses, fp64, for
+    the loss <dy, y> + <dfinal, final> (the pages give no backward formulas: this is the chain
+    rule through the K1..K5 decomposition, written out per chunk).  Per chunk c, with fused
+    rows i (step s(i) = i // R), cum the in-chunk prefix of dA, L_ij = exp(cum_s(i) - cum_s(j))
+    for s(j) <= s(i), CB = C B^T, DX = dy x^T, M = L o CB, A = L o DX, W = M o DX,
+    el_j = exp(cum_end - cum_s(j)), e_i = exp(cum_s(i)), h_in the chunk-input state and
+    G = dL/dh_out the gradient carried back from the later chunks (D_c = sum_i e_i dy_i C_i^T):
+      dx = M^T dy + diag(el) B G^T        dB = A^T C + diag(el) x G       dC = A B + diag(e) dy h_in
+      dL/dcum_s = sum over the step's rows of (rowsum W - colsum W + E_i - Q_i), with
+      E_i = e_i C_i . (h_in^T dy_i), Q_j = el_j x_j . (G B_j), plus at the chunk's last step
+      sum_j Q_j + exp(cum_end) <G, h_in>;  ddA_t = sum_{s >= t in the chunk} dL/dcum_s.
+    Returns dict dx, ddA, dB, dC, dinit."""
+    x, dA, B, C, dy = (np.asarray(v, np.float64) for v in (x, dA, B, C, dy))
+    b, T, R, H, P = x.shape
+    G, N = B.shape[3], B.shape[4]
+    l = int(chunk_len)
+    nch = -(-T // l)
+    Tp = nch * l
+    pad = Tp - T
+
+    def padt(v):
+        if pad == 0:
+            return v
+        w = [(0, 0)] * v.ndim
+        w[1] = (0, pad)
+        return np.pad(v, w)
+
+    xp, dAp, Bp, Cp, dyp = (padt(v) for v in (x, dA, B, C, dy))
+    L = l * R
+    step = np.arange(L) // R
+    out = {"dx": np.zeros_like(x), "ddA": np.zeros_like(dA), "dB": np.zeros_like(B),
+           "dC": np.zeros_like(C), "dinit": np.zeros((b, H, P, N))}
+    dBp = np.zeros_like(Bp)
+    dCp = np.zeros_like(Cp)
+    for bi in range(b):
+        for hi in range(H):
+            g = hi // (H // G)
+            X = xp[bi, :, :, hi, :].reshape(nch, L, P)
+            Bm = Bp[bi, :, :, g, :].reshape(nch, L, N)
+            Cm = Cp[bi, :, :, g, :].reshape(nch, L, N)
+            DY = dyp[bi, :, :, hi, :].reshape(nch, L, P)
+            cum = np.cumsum(dAp[bi, :, hi].reshape(nch, l), axis=1)
+            cumr = cum[:, step]
+            cend = cum[:, -1]
+            S = [(np.exp(cend[c] - cumr[c])[:, None] * X[c]).T @ Bm[c] for c in range(nch)]
+            D = [(np.exp(cumr[c])[:, None] * DY[c]).T @ Cm[c] for c in range(nch)]
+            hin = []
+            h = (np.zeros((P, N)) if init_state is None
+                 else np.asarray(init_state, np.float64)[bi, hi])
+            for c in range(nch):
+                hin.append(h)
+                h = np.exp(cend[c]) * h + S[c]
+            Gc = [None] * nch
+            gcur = (np.zeros((P, N)) if dfinal is None
+                    else np.asarray(dfinal, np.float64)[bi, hi])
+            for c in range(nch - 1, -1, -1):
+                Gc[c] = gcur
+                gcur = np.exp(cend[c]) * gcur + D[c]
+            out["dinit"][bi, hi] = gcur
+            for c in range(nch):
+                causal = step[:, None] >= step[None, :]
+                Lm = np.where(causal, np.exp(np.where(causal, cumr[c][:, None] - cumr[c][None, :],
+                                                      0.0)), 0.0)
+                CB = Cm[c] @ Bm[c].T
+                DX = DY[c] @ X[c].T
+                M, A = Lm * CB, Lm * DX
+                W = M * DX
+                el, e = np.exp(cend[c] - cumr[c]), np.exp(cumr[c])
+                U = el[:, None] * (Bm[c] @ Gc[c].T)            # [L, P]
+                V = DY[c] @ hin[c]                              # [L, N]
+                dxc = M.T @ DY[c] + U
+                dBc = A.T @ Cm[c] + el[:, None] * (X[c] @ Gc[c])
+                dCc = A @ Bm[c] + e[:, None] * V
+                E = e * np.sum(Cm[c] * V, axis=1)
+                Q = np.sum(X[c] * U, axis=1)
+                rows = W.sum(axis=1) - W.sum(axis=0) + E - Q
+                dcum = rows.reshape(l, R).sum(axis=1)
+                dcum[-1] += Q.sum() + np.exp(cend[c]) * np.sum(Gc[c] * hin[c])
+                ddA_c = np.cumsum(dcum[::-1])[::-1]
+                t0 = c * l
+                nv = min(l, T - t0)
+                out["dx"][bi, t0:t0 + nv, :, hi, :] = dxc.reshape(l, R, P)[:nv]
+                out["ddA"][bi, t0:t0 + nv, hi] = ddA_c[:nv]
+                dBp[bi, t0:t0 + l, :, g, :] += dBc.reshape(l, R, N)
+                dCp[bi, t0:t0 + l, :, g, :] += dCc.reshape(l, R, N)
+    out["dB"] = dBp[:, :T]
+    out["dC"] = dCp[:, :T]
+    return out

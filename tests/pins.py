@@ -477,6 +477,23 @@ def pin_trapezoidal_backward_reduces_to_plain(mutation=0):
     return res
 
 
-BWD_PINS = [pin_backward_finite_differences]
+def pin_backward_chunked_algebra(mutation=0):
+    """The sequential reverse mode against the chunked backward algebra (the per-chunk formulas
+    the GPU kernels use, restated in numpy fp64 in chunked_ref): ragged T, MIMO ranks, a group
+    shared by two heads, an initial state and dfinal, at several chunk lengths."""
+    res = []
+    x, dA, B, C, _, h0 = _problem(91, 2, 37, 2, 4, 2, 3, 4, init=True)
+    r = _rng(92)
+    dy = r.standard_normal(x.shape)
+    dfin = r.standard_normal(h0.shape)
+    g = oracle.ssd_backward(x, dA, B, C, dy, h0, dfin, mutation=mutation)
+    for l in (1, 8, 16, 37):
+        ref = chunked_ref.chunked_backward(x, dA, B, C, dy, h0, dfin, chunk_len=l)
+        for k in ("dx", "ddA", "dB", "dC", "dinit"):
+            res.append((f"chunked_bwd_l{l}_{k}", _maxerr(g[k], ref[k]), 1e-9))
+    return res
+
+
+BWD_PINS = [pin_backward_finite_differences, pin_backward_chunked_algebra]
 TRAP_BWD_PINS = [pin_trapezoidal_backward_finite_differences,
                  pin_trapezoidal_backward_reduces_to_plain]
