@@ -260,3 +260,101 @@ def chunked_backward(x, dA, B, C, dy, init_state=None, dfinal=None, chunk_len=64
     out["dB"] = dBp[:, :T]
     out["dC"] = dCp[:, :T]
     return out
+
+
+def chunked_backward_rotated(x, dA, B, C, theta, dy, init_state=None, dfinal=None, chunk_len=64):
+    """Reverse mode of the rotated SSD in chunk-local frames, fp64 (the form the GPU backward
+    uses).  Inside chunk c, phi_t is the angle accumulated since the chunk's start; the chunk is
+    the plain problem on B^ = R(-phi)B, C^ = R(-phi)C entered with the physical h_in(c) and left
+    through h_in(c+1) = R(phi_end) g_end.  The plain per-chunk gradients (chunked_backward's
+    formulas) on B^, C^ with G^_c = R(-phi_end) dL/dh_in(c+1) then give dB = R(phi) dB^,
+    dC = R(phi) dC^ and dL/dphi_t = sum over the step's rows of (dB^_0 B^_1 - dB^_1 B^_0 +
+    dC^_0 C^_1 - dC^_1 C^_0) plus, at the chunk's end, sum_p (G^_1 g_0 - G^_0 g_1) with
+    g = g_end; dtheta_t sums dL/dphi over the steps t .. chunk end.  Returns dict dx, ddA, dB,
+    dC, dtheta, dinit."""
+    x, dA, B, C, theta, dy = (np.asarray(v, np.float64) for v in (x, dA, B, C, theta, dy))
+    b, T, R, H, P = x.shape
+    G, N = B.shape[3], B.shape[4]
+    K = N // 2
+    l = int(chunk_len)
+    nch = -(-T // l)
+    pad = nch * l - T
+
+    def padt(v):
+        if pad == 0:
+            return v
+        w = [(0, 0)] * v.ndim
+        w[1] = (0, pad)
+        return np.pad(v, w)
+
+    xp, dAp, Bp, Cp, dyp, thp = (padt(v) for v in (x, dA, B, C, dy, theta))
+    L = l * R
+    step = np.arange(L) // R
+    out = {"dx": np.zeros_like(x), "ddA": np.zeros_like(dA), "dtheta": np.zeros_like(theta),
+           "dinit": np.zeros((b, H, P, N))}
+    dBp = np.zeros_like(Bp)
+    dCp = np.zeros_like(Cp)
+    cross = lambda d, v: d[..., 0::2] * v[..., 1::2] - d[..., 1::2] * v[..., 0::2]
+    for bi in range(b):
+        for hi in range(H):
+            g = hi // (H // G)
+            X = xp[bi, :, :, hi, :].reshape(nch, L, P)
+            DY = dyp[bi, :, :, hi, :].reshape(nch, L, P)
+            cum = np.cumsum(dAp[bi, :, hi].reshape(nch, l), axis=1)
+            cumr = cum[:, step]
+            cend = cum[:, -1]
+            phi = np.cumsum(thp[bi, :, hi, :].reshape(nch, l, K), axis=1)   # local angles
+            phir = phi[:, step, :]                                           # [nch, L, K]
+            Bh = rotate_pairs(Bp[bi, :, :, g, :].reshape(nch, L, N), -phir)
+            Ch = rotate_pairs(Cp[bi, :, :, g, :].reshape(nch, L, N), -phir)
+            pend = phi[:, -1, :]                                             # [nch, K]
+            S = [(np.exp(cend[c] - cumr[c])[:, None] * X[c]).T @ Bh[c] for c in range(nch)]
+            D = [(np.exp(cumr[c])[:, None] * DY[c]).T @ Ch[c] for c in range(nch)]
+            hin, gend = [], []
+            h = (np.zeros((P, N)) if init_state is None
+                 else np.asarray(init_state, np.float64)[bi, hi])
+            for c in range(nch):
+                hin.append(h)
+                ge = np.exp(cend[c]) * h + S[c]
+                gend.append(ge)
+                h = rotate_pairs(ge, np.broadcast_to(pend[c], (P, K)))
+            Gh = [None] * nch
+            v = (np.zeros((P, N)) if dfinal is None
+                 else np.asarray(dfinal, np.float64)[bi, hi])
+            for c in range(nch - 1, -1, -1):
+                Gh[c] = rotate_pairs(v, np.broadcast_to(-pend[c], (P, K)))
+                v = np.exp(cend[c]) * Gh[c] + D[c]
+            out["dinit"][bi, hi] = v
+            for c in range(nch):
+                causal = step[:, None] >= step[None, :]
+                Lm = np.where(causal, np.exp(np.where(causal, cumr[c][:, None] - cumr[c][None, :],
+                                                      0.0)), 0.0)
+                CB = Ch[c] @ Bh[c].T
+                DX = DY[c] @ X[c].T
+                M, A = Lm * CB, Lm * DX
+                W = M * DX
+                el, e = np.exp(cend[c] - cumr[c]), np.exp(cumr[c])
+                U = el[:, None] * (Bh[c] @ Gh[c].T)
+                V = DY[c] @ hin[c]
+                dxc = M.T @ DY[c] + U
+                dBh = A.T @ Ch[c] + el[:, None] * (X[c] @ Gh[c])
+                dCh = A @ Bh[c] + e[:, None] * V
+                E = e * np.sum(Ch[c] * V, axis=1)
+                Q = np.sum(X[c] * U, axis=1)
+                rows = W.sum(axis=1) - W.sum(axis=0) + E - Q
+                dcum = rows.reshape(l, R).sum(axis=1)
+                dcum[-1] += Q.sum() + np.exp(cend[c]) * np.sum(Gh[c] * hin[c])
+                ddA_c = np.cumsum(dcum[::-1])[::-1]
+                dphi = (cross(dBh, Bh[c]) + cross(dCh, Ch[c])).reshape(l, R, K).sum(axis=1)
+                dphi[-1] += cross(gend[c], Gh[c]).sum(axis=0)   # sum_p (G^_1 g_0 - G^_0 g_1)
+                dth = np.cumsum(dphi[::-1], axis=0)[::-1]
+                t0 = c * l
+                nv = min(l, T - t0)
+                out["dx"][bi, t0:t0 + nv, :, hi, :] = dxc.reshape(l, R, P)[:nv]
+                out["ddA"][bi, t0:t0 + nv, hi] = ddA_c[:nv]
+                out["dtheta"][bi, t0:t0 + nv, hi, :] = dth[:nv]
+                dBp[bi, t0:t0 + l, :, g, :] += rotate_pairs(dBh, phir[c]).reshape(l, R, N)
+                dCp[bi, t0:t0 + l, :, g, :] += rotate_pairs(dCh, phir[c]).reshape(l, R, N)
+    out["dB"] = dBp[:, :T]
+    out["dC"] = dCp[:, :T]
+    return out

@@ -494,6 +494,24 @@ def pin_backward_chunked_algebra(mutation=0):
     return res
 
 
-BWD_PINS = [pin_backward_finite_differences, pin_backward_chunked_algebra]
+def pin_rotated_backward_chunk_local_frames(mutation=0):
+    """The sequential rotated reverse mode against the chunk-local-frame restatement
+    (chunked_ref.chunked_backward_rotated, the form the GPU uses): ragged T, MIMO ranks, a
+    group shared by two differently turned heads, at several chunk lengths."""
+    res = []
+    x, dA, B, C, th, h0 = _problem(93, 2, 37, 2, 4, 2, 3, 4, theta=True, init=True)
+    r = _rng(94)
+    dy = r.standard_normal(x.shape)
+    dfin = r.standard_normal(h0.shape)
+    g = oracle.ssd_backward(x, dA, B, C, dy, h0, dfin, theta=th, mutation=mutation)
+    for l in (1, 8, 16, 37):
+        ref = chunked_ref.chunked_backward_rotated(x, dA, B, C, th, dy, h0, dfin, chunk_len=l)
+        for k in ("dx", "ddA", "dB", "dC", "dtheta", "dinit"):
+            res.append((f"rot_chunked_bwd_l{l}_{k}", _maxerr(g[k], ref[k]), 1e-9))
+    return res
+
+
+BWD_PINS = [pin_backward_finite_differences, pin_backward_chunked_algebra,
+            pin_rotated_backward_chunk_local_frames]
 TRAP_BWD_PINS = [pin_trapezoidal_backward_finite_differences,
                  pin_trapezoidal_backward_reduces_to_plain]
