@@ -14,6 +14,10 @@ that the pin tests can check the sequential oracle (``oracle.ssd``) against it:
   and the final state is turned back by R(Phi_{T-1}) (module docstring, "THE TRICK").
 - Ragged T: zero padding with dA = 0 and x = 0 (moments.rs page, module header: pads are
   identity decay and zero write, so the carried state passes through unchanged).
+- ``chunked_backward`` / ``chunked_backward_rotated``: the chain rule through that
+  decomposition (the pages ask for a trainable scan but print no backward formulas), per chunk,
+  plain and in chunk-local rotation frames, so the pins can check the sequential reverse mode
+  (``oracle.ssd_backward``) against the chunked algebra the GPU backward is built on.
 
 It is deliberately unfused and unblocked: every intermediate of the pages is materialised.
 """
