@@ -14,8 +14,8 @@ that the pin tests can check the sequential oracle (``oracle.ssd``) against it:
   and the final state is turned back by R(Phi_{T-1}) (module docstring, "THE TRICK").
 - Ragged T: zero padding with dA = 0 and x = 0 (moments.rs page, module header: pads are
   identity decay and zero write, so the carried state passes through unchanged).
-- ``chunked_backward`` / ``chunked_backward_rotated``: the chain rule through that
-  decomposition (the pages ask for a trainable scan but print no backward formulas), per chunk,
+- ``chunked_backward`` / ``chunked_backward_rotated`` / ``trapezoidal_backward_expanded``: the
+  chain rule through that decomposition (and through the trapezoid's 2R-channel expansion) (the pages ask for a trainable scan but print no backward formulas), per chunk,
   plain and in chunk-local rotation frames, so the pins can check the sequential reverse mode
   (``oracle.ssd_backward``) against the chunked algebra the GPU backward is built on.
 
@@ -361,4 +361,71 @@ def chunked_backward_rotated(x, dA, B, C, theta, dy, init_state=None, dfinal=Non
                 dCp[bi, t0:t0 + l, :, g, :] += rotate_pairs(dCh, phir[c]).reshape(l, R, N)
     out["dB"] = dBp[:, :T]
     out["dC"] = dCp[:, :T]
+    return out
+
+
+def trapezoidal_backward_expanded(x, dA, B, C, gamma, beta, dy, theta=None, init_state=None,
+                                  prev_x=None, prev_B=None, dfinal=None, chunk_len=64):
+    """Reverse mode of the trapezoidal SSD through its 2R-channel expansion (the form the GPU
+    uses), fp64: x^ = [gamma_t x_t, beta_t x_{t-1}], B^ = [B_t, R(theta_t) B_{t-1}] (per head
+    with theta), C^ = [C_t, 0], dy^ = [dy, 0]; the chunked backward of that plain (or rotated)
+    problem, then the chain rule back through the expansion:
+      dx_t = gamma_t dx^[t, r] + beta_{t+1} dx^[t+1, R+r],  dprev_x = beta_0 dx^[0, R+r]
+      dgamma_t = <dx^[t, :R], x_t>,  dbeta_t = <dx^[t, R:], x_{t-1}>
+      dB_t = sum_heads dB^[t, r] + R(theta_{t+1})^T dB^[t+1, R+r],  dprev_B likewise at t = 0
+      dC_t = sum_heads dC^[t, r],  dtheta_t = dtheta^_t + sum_r (dB^_1 B^_0 - dB^_0 B^_1)[t, R+r].
+    Returns the same dict as oracle.ssd_trap_backward."""
+    x, dA, B, C, gamma, beta, dy = (np.asarray(v, np.float64)
+                                    for v in (x, dA, B, C, gamma, beta, dy))
+    b, T, R, H, P = x.shape
+    G, N = B.shape[3], B.shape[4]
+    rot = theta is not None
+    th = np.asarray(theta, np.float64) if rot else None
+    G2 = H if rot else G
+    hof = (np.arange(H) // (H // G)) if rot else np.arange(G)   # group of each expanded row
+    xprev = np.zeros_like(x)
+    xprev[:, 1:] = x[:, :-1]
+    Bprev = np.zeros_like(B)
+    Bprev[:, 1:] = B[:, :-1]
+    if prev_x is not None:
+        xprev[:, 0] = np.asarray(prev_x, np.float64)
+        Bprev[:, 0] = np.asarray(prev_B, np.float64)
+    xh = np.concatenate([gamma[:, :, None, :, None] * x, beta[:, :, None, :, None] * xprev], axis=2)
+    Bcur, Bsh = B[:, :, :, hof, :], Bprev[:, :, :, hof, :]          # [b, T, R, G2, N]
+    if rot:
+        Bsh = rotate_pairs(Bsh, th[:, :, None, :, :])
+    Bh = np.concatenate([Bcur, Bsh], axis=2)
+    Ch = np.concatenate([C[:, :, :, hof, :], np.zeros_like(Bsh)], axis=2)
+    dyh = np.concatenate([dy, np.zeros_like(dy)], axis=2)
+    if rot:
+        g = chunked_backward_rotated(xh, dA, Bh, Ch, th, dyh, init_state, dfinal, chunk_len)
+    else:
+        g = chunked_backward(xh, dA, Bh, Ch, dyh, init_state, dfinal, chunk_len)
+    dxh, dBh, dCh = g["dx"], g["dB"], g["dC"]
+    out = {"ddA": g["ddA"], "dinit": g["dinit"]}
+    dx = gamma[:, :, None, :, None] * dxh[:, :, :R]
+    dx[:, :-1] += beta[:, 1:, None, :, None] * dxh[:, 1:, R:]
+    out["dx"] = dx
+    out["dgamma"] = np.sum(dxh[:, :, :R] * x, axis=(2, 4))
+    out["dbeta"] = np.sum(dxh[:, :, R:] * xprev, axis=(2, 4))
+    back = dBh[:, :, R:]                                             # shifted channels
+    if rot:
+        back = rotate_pairs(back, -th[:, :, None, :, :])             # R(theta_t)^T
+    dB = np.zeros_like(B)
+    dC = np.zeros_like(C)
+    dpB = np.zeros((b, R, G, N))
+    for j in range(G2):
+        gi = hof[j]
+        dB[:, :, :, gi] += dBh[:, :, :R, j]
+        dB[:, :-1, :, gi] += back[:, 1:, :, j]
+        dC[:, :, :, gi] += dCh[:, :, :R, j]
+        dpB[:, :, gi] += back[:, 0, :, j]
+    out["dB"], out["dC"] = dB, dC
+    if rot:
+        sh, dsh = Bh[:, :, R:], dBh[:, :, R:]
+        extra = dsh[..., 1::2] * sh[..., 0::2] - dsh[..., 0::2] * sh[..., 1::2]
+        out["dtheta"] = g["dtheta"] + extra.sum(axis=2)
+    if prev_x is not None:
+        out["dprev_x"] = beta[:, 0, None, :, None] * dxh[:, 0, R:]
+        out["dprev_B"] = dpB
     return out

@@ -513,5 +513,29 @@ def pin_rotated_backward_chunk_local_frames(mutation=0):
 
 BWD_PINS = [pin_backward_finite_differences, pin_backward_chunked_algebra,
             pin_rotated_backward_chunk_local_frames]
+def pin_trapezoidal_backward_expansion(mutation=0):
+    """The sequential trapezoidal reverse mode against the 2R-channel expansion, its chunked
+    backward and the chain rule back through it (chunked_ref.trapezoidal_backward_expanded, the
+    form the GPU uses), with and without the rotation, with a previous write."""
+    res = []
+    for rot in (False, True):
+        x, dA, B, C, gm, bt, th, h0, px, pb = _trap_problem(95 + rot, 2, 37, 2, 4, 2, 3, 4,
+                                                            theta=rot)
+        r = _rng(97 + rot)
+        dy = r.standard_normal(x.shape)
+        dfin = r.standard_normal(h0.shape)
+        g = oracle.ssd_trap_backward(x, dA, B, C, gm, bt, dy, theta=th, init_state=h0,
+                                     prev_x=px, prev_B=pb, dfinal=dfin, mutation=mutation)
+        for l in (8, 37):
+            ref = chunked_ref.trapezoidal_backward_expanded(x, dA, B, C, gm, bt, dy, theta=th,
+                                                            init_state=h0, prev_x=px, prev_B=pb,
+                                                            dfinal=dfin, chunk_len=l)
+            for k in sorted(g):
+                tag = "rot_" if rot else ""
+                res.append((f"trap_expanded_{tag}l{l}_{k}", _maxerr(g[k], ref[k]), 1e-9))
+    return res
+
+
 TRAP_BWD_PINS = [pin_trapezoidal_backward_finite_differences,
-                 pin_trapezoidal_backward_reduces_to_plain]
+                 pin_trapezoidal_backward_reduces_to_plain,
+                 pin_trapezoidal_backward_expansion]
