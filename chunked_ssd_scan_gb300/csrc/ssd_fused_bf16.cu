@@ -142,9 +142,10 @@ struct FusedArgs {
   float* seg_decay;        // [b*H*nseg]
 };
 
-__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatile int* abort,
-                                         WsHeader* hdr, int site) {
-  if (mbar_try_wait(bar, parity)) return true;
+// The loop of a wait that did not complete at once, kept out of line: the kernels wait at many
+// sites, and inlining this at each of them multiplies the code the warps must fetch.
+__device__ __noinline__ bool wait_bar_slow(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                           WsHeader* hdr, int site) {
   // bounded in cycles of this SM's clock, which only moves forward
   const long long t0 = clock64();
   while (true) {
@@ -156,6 +157,12 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatil
       return false;
     }
   }
+}
+
+__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                         WsHeader* hdr, int site) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return wait_bar_slow(bar, parity, abort, hdr, site);
 }
 
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
@@ -210,6 +217,82 @@ __device__ __forceinline__ void mask_block(const TileInfo& ti, int cb, bool exac
       split2(mul2(make_float2(w[k], w[k + 1]), l0), hi[k / 2], lo[k / 2]);
       split2(mul2(make_float2(w[k + 2], w[k + 3]), l1), hi[k / 2 + 1], lo[k / 2 + 1]);
     }
+  }
+}
+
+// K1 for one warp: reads dA straight from global memory (one tile ahead, into registers) and
+// publishes each tile's prefix sums and decay factors into a ring of kInfoSlots slots.
+__device__ __forceinline__ void k1_warp(const FusedArgs& a, TileInfo* info, uint64_t* info_ready,
+                                        uint64_t* info_empty, volatile int* abort, int b, int h,
+                                        int tbase, int nt, int lane) {
+  const int R = a.R, steps = a.steps;
+  const int per = (steps + 31) / 32;                 // steps per lane (<= 4)
+  const int beg = min(steps, lane * per), end = min(steps, beg + per);
+  const float* dsrc = a.dA + ((size_t)b * a.T + (size_t)tbase * steps) * a.H + h;
+  float dnext[4];
+  auto load_tile = [&](int t) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      dnext[k] = (beg + k < end && (tbase + t) * steps + beg + k < a.T)
+                     ? __ldg(dsrc + (size_t)(t * steps + beg + k) * a.H)
+                     : 0.f;
+  };
+  load_tile(0);
+  for (int t = 0; t < nt; ++t) {
+    float dcur[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) dcur[k] = dnext[k];
+    if (t + 1 < nt) load_tile(t + 1);
+    DF sum = {0.f, 0.f};
+    int pos = 0;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      pos |= (dcur[k] > 0.f);
+      sum = df_add(sum, DF{dcur[k], 0.f});
+    }
+    DF incl = sum;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const DF v = df_shfl_up(incl, off);
+      if (lane >= off) incl = df_add(incl, v);
+    }
+    const DF last = df_shfl(incl, 31);
+    DF acc = df_shfl_up(incl, 1);   // exclusive prefix of this lane's first step
+    if (lane == 0) acc = DF{0.f, 0.f};
+    const int monotone = __all_sync(0xffffffffu, pos == 0);
+    const int slot = t % kInfoSlots;
+    if (t >= kInfoSlots &&
+        !wait_bar(&info_empty[slot], ((t - kInfoSlots) / kInfoSlots) & 1, abort, a.hdr, 11))
+      break;
+    TileInfo& ti = info[slot];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      if (beg + k < end) {
+        acc = df_add(acc, DF{dcur[k], 0.f});
+        const float chi = acc.hi * kLog2e;
+        const float clo = fmaf(acc.hi, kLog2e, -chi) + acc.lo * kLog2e;
+        for (int r = 0; r < R; ++r) {
+          ti.cum_hi[(beg + k) * R + r] = chi;
+          ti.cum_lo[(beg + k) * R + r] = clo;
+        }
+      }
+    }
+    if (lane == 0) {
+      const float lhi = last.hi * kLog2e;
+      ti.last_hi = lhi;
+      ti.last_lo = fmaf(last.hi, kLog2e, -lhi) + last.lo * kLog2e;
+      ti.etile = ex2_approx(lhi + ti.last_lo);
+      ti.monotone = monotone;
+    }
+    __syncwarp();
+    // qf of the rank-one blocks: the reference of column block c is its last fused row
+#pragma unroll
+    for (int e = lane; e < kTileRows; e += 32) {
+      const int ref = (e >> 5) * 32 + 31;
+      ti.qf[e] = ex2_approx((ti.cum_hi[ref] - ti.cum_hi[e]) + (ti.cum_lo[ref] - ti.cum_lo[e]));
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&info_ready[slot]);
   }
 }
 
@@ -403,77 +486,7 @@ __global__ void __launch_bounds__(kThreadsFused, 1)
     }
     }
   } else if (warp == 2) {
-    // ------------------------------------------------------------------ K1 (one warp)
-    // Reads dA straight from global memory (one tile ahead, into registers) and publishes the
-    // tile's prefix sums and decay factors into a ring of kInfoSlots slots.
-    const int per = (steps + 31) / 32;                 // steps per lane (<= 4)
-    const int beg = min(steps, lane * per), end = min(steps, beg + per);
-    const float* dsrc = a.dA + ((size_t)b * a.T + (size_t)tbase * steps) * a.H + h;
-    float dnext[4];
-    auto load_tile = [&](int t) {
-#pragma unroll
-      for (int k = 0; k < 4; ++k)
-        dnext[k] = (beg + k < end && (tbase + t) * steps + beg + k < a.T)
-                       ? __ldg(dsrc + (size_t)(t * steps + beg + k) * a.H)
-                       : 0.f;
-    };
-    load_tile(0);
-    for (int t = 0; t < nt; ++t) {
-      float dcur[4];
-#pragma unroll
-      for (int k = 0; k < 4; ++k) dcur[k] = dnext[k];
-      if (t + 1 < nt) load_tile(t + 1);
-      DF sum = {0.f, 0.f};
-      int pos = 0;
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        pos |= (dcur[k] > 0.f);
-        sum = df_add(sum, DF{dcur[k], 0.f});
-      }
-      DF incl = sum;
-#pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const DF v = df_shfl_up(incl, off);
-        if (lane >= off) incl = df_add(incl, v);
-      }
-      const DF last = df_shfl(incl, 31);
-      DF acc = df_shfl_up(incl, 1);   // exclusive prefix of this lane's first step
-      if (lane == 0) acc = DF{0.f, 0.f};
-      const int monotone = __all_sync(0xffffffffu, pos == 0);
-      const int slot = t % kInfoSlots;
-      if (t >= kInfoSlots &&
-          !wait_bar(&bars->info_empty[slot], ((t - kInfoSlots) / kInfoSlots) & 1, abort, a.hdr, 11))
-        break;
-      TileInfo& ti = info[slot];
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        if (beg + k < end) {
-          acc = df_add(acc, DF{dcur[k], 0.f});
-          const float chi = acc.hi * kLog2e;
-          const float clo = fmaf(acc.hi, kLog2e, -chi) + acc.lo * kLog2e;
-          for (int r = 0; r < R; ++r) {
-            ti.cum_hi[(beg + k) * R + r] = chi;
-            ti.cum_lo[(beg + k) * R + r] = clo;
-          }
-        }
-      }
-      if (lane == 0) {
-        const float lhi = last.hi * kLog2e;
-        ti.last_hi = lhi;
-        ti.last_lo = fmaf(last.hi, kLog2e, -lhi) + last.lo * kLog2e;
-        ti.etile = ex2_approx(lhi + ti.last_lo);
-        ti.monotone = monotone;
-      }
-      __syncwarp();
-      // qf of the rank-one blocks: the reference of column block c is its last fused row
-#pragma unroll
-      for (int e = lane; e < kTileRows; e += 32) {
-        const int ref = (e >> 5) * 32 + 31;
-        ti.qf[e] = ex2_approx((ti.cum_hi[ref] - ti.cum_hi[e]) + (ti.cum_lo[ref] - ti.cum_lo[e]));
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->info_ready[slot]);
-    }
+    k1_warp(a, info, bars->info_ready, bars->info_empty, abort, b, h, tbase, nt, lane);
   } else {
     // ------------------------------------------------------------------ math warps (3-10)
     const int q = warp & 3;                 // TMEM lane quarter == SM sub-partition
@@ -740,6 +753,599 @@ __global__ void __launch_bounds__(kThreadsFused, 1)
   }
 }
 
+namespace full {
+
+// ============================================================================================
+// Full forward pass (one CTA per (batch, head) sequence or time segment of one).
+//
+// Per 128-row tile t the tensor core runs, in this order,
+//   Yo_t     = C_t h_t^T                      A = C_t (TMEM), B = [h_hi ; h_lo]   (K = 2 x 128)
+//   K3_t     = B_t^T [(dec o x)_hi ; lo]      A = B_t (MN-major smem)             (K = 2 x 128)
+//   CB_{t+1} = C_{t+1} B_{t+1}^T              A = C_{t+1} (TMEM), into mask buffer (t+1) & 1
+//   Yd_t    += (L o CB)_t x_t                 A = (L o CB) hi/lo (TMEM)           (K = 2 x 128)
+// where Yd_t starts from e^{cum_i} Yo_t, written into its accumulator by the out warps, so y_t
+// is one accumulator.  The mask of tile t+1 is computed while Yd_t, Yo_{t+1} and K3_{t+1} run
+// (two mask buffers), which gives the element-wise mask about one tile of tensor work to hide
+// behind.  The CUDA cores, around the tensor core:
+//   state warps  h_{t+1} = e^{cum_last} h_t + S_t in registers (the K4 step, fp32), written as
+//                bf16 hi/lo rows for Yo_{t+1}; the state never leaves the SM
+//   mask warps   (dec o x)_t into its own buffer, then the mask of tile t in place over CB_t
+//   out warps    e^{cum_i} Yo_t into the Yd accumulator; C_{t+1} from its shared-memory tile
+//                into TMEM; y_t -> bf16 -> the tile's x slot -> TMA store
+// The state recurrence never passes through the tensor core (K3 starts from zero).
+// ============================================================================================
+
+constexpr int kThreads = 512;
+constexpr int kXSlots = 3;                                  // x ring (a slot also stages y_t)
+constexpr uint32_t kOffX = 0;
+constexpr uint32_t kOffB = kOffX + kXSlots * kXBytes;        // two B stages
+constexpr uint32_t kOffC = kOffB + 2 * kBCBytes;             // one C slot (copied into TMEM)
+constexpr uint32_t kOffDxHi = kOffC + kBCBytes;              // (dec o x) hi  [rows][P]
+constexpr uint32_t kOffDxLo = kOffDxHi + kXBytes;            // (dec o x) lo
+constexpr uint32_t kOffHHi = kOffDxLo + kXBytes;             // h^T hi [N rows][P]
+constexpr uint32_t kOffHLo = kOffHHi + kXBytes;              // h^T lo
+constexpr uint32_t kOffInfo = kOffHLo + kXBytes;
+constexpr uint32_t kOffBar = kOffInfo + kInfoSlots * sizeof(TileInfo);
+constexpr uint32_t kSmem = kOffBar + 512;
+static_assert(kSmem <= 232448, "exceeds the 227 KB shared-memory limit per CTA");
+static_assert(kOffInfo % 1024 == 0, "operand buffers must stay 1024-byte aligned");
+
+// TMEM columns (128 lanes x 512 columns of 32 bit)
+constexpr uint32_t kColM = 0;      // two buffers of 128: CB fp32, rewritten as (L o CB) hi/lo
+                                   // per 32-column block (16 hi then 16 lo columns)
+constexpr uint32_t kColYd = 256;   // y accumulator: e^{cum_i} Yo_t, then + Yd_t
+constexpr uint32_t kColYo = 320;   // C h^T
+constexpr uint32_t kColS = 384;    // B^T (dec o x) (hi and lo stacked along K)
+constexpr uint32_t kColC = 448;    // C: 128 bf16 of the state axis, two per column
+
+// The MMA warp waits on few barriers (a wait costs a few hundred cycles of latency even when its
+// phase has completed, and the issuing thread runs only a few MMAs ahead of the tensor core),
+// and tests each of them before issuing the product before it:
+//   yo_go(t)     state warps wrote h_t; out warps read Yo_{t-1}
+//   k3_go(t)     (dec o x)_t written; state warps read S_{t-1}
+//   cb_go(t)     C_t copied into TMEM and B_t landed (the out warps wait for both)
+//   m_ready[b]   the mask of the tile in mask buffer b is in TMEM
+//   y_pre(t)     e^{cum_i} Yo_t written into the y accumulator (after y_{t-1} was read)
+// x_t needs no wait of its own: the (dec o x) warps waited for it before arriving on k3_go(t),
+// and Yd_t is issued after K3_t.  Barriers whose next phase can complete before a waiter has
+// seen the current one (CB_{t+1} and the mask of tile t+1 may both finish before Yd_t is
+// issued) come in pairs, one per mask buffer.
+struct Bars {
+  uint64_t x_full[kXSlots], x_empty[kXSlots], b_full[2], b_empty[2];
+  uint64_t c_full, c_empty, cb_go;
+  uint64_t info_ready[kInfoSlots], info_empty[kInfoSlots];
+  uint64_t cb_full[2], m_ready[2], yd_full, yo_full, s_full;
+  uint64_t yo_go, k3_go, y_pre, drain;
+};
+static_assert(sizeof(Bars) + 16 <= 512, "barrier block");
+
+// Mask blocks [cb0, cb1) of the tile's rows in quarter q = warp % 4 (the diagonal block q is
+// exact, the ones below it factorized), blocks [cb1, zero_end) set to zero.  Five warps share the
+// 1 + 2 + 3 + 4 blocks of the causal tile.
+struct MaskShare {
+  int cb0, cb1, zero_end;
+};
+__device__ __forceinline__ MaskShare mask_share(int warp) {
+  switch (warp) {
+    case 4: return {0, 1, 4};
+    case 5: return {0, 2, 4};
+    case 6: return {0, 3, 4};
+    case 7: return {2, 4, 4};
+    case 3: return {0, 2, 2};
+    default: return {0, 0, 0};
+  }
+}
+constexpr int kMaskWarps = 5;
+
+// (dec o x) work units (32 rows x 16 columns; 16 per tile) of the warps that compute it: most on
+// sub-partition 0 (the least mask work), none on sub-partition 2 (three mask blocks and K1).
+__device__ __forceinline__ int2 dx_units(int warp) {
+  switch (warp) {
+    case 4: return make_int2(0, 7);
+    case 5: return make_int2(7, 12);
+    case 7: return make_int2(12, 14);
+    case 3: return make_int2(14, 16);
+    default: return make_int2(0, 0);
+  }
+}
+constexpr int kDxWarps = 4;
+
+__global__ void __launch_bounds__(kThreads, 1)
+    ssd_fused_full_kernel(FusedArgs a, const __grid_constant__ CUtensorMap tm_x,
+                          const __grid_constant__ CUtensorMap tm_b,
+                          const __grid_constant__ CUtensorMap tm_c,
+                          const __grid_constant__ CUtensorMap tm_y) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  Bars* bars = reinterpret_cast<Bars*>(smem + kOffBar);
+  TileInfo* info = reinterpret_cast<TileInfo*>(smem + kOffInfo);
+  uint32_t& s_tmem = *reinterpret_cast<uint32_t*>(smem + kOffBar + sizeof(Bars));
+  int& s_abort = *reinterpret_cast<int*>(smem + kOffBar + sizeof(Bars) + 4);
+  int& s_keep_tmem = *reinterpret_cast<int*>(smem + kOffBar + sizeof(Bars) + 8);
+  if ((smem_u32(smem) & 1023u) != 0) {   // never expected; refuse rather than mis-swizzle
+    if (threadIdx.x == 0 && a.hdr) latch_error(a.hdr, SSD_ERR_CUDA, 99);
+    return;
+  }
+
+  const int warp = __shfl_sync(0xffffffffu, static_cast<int>(threadIdx.x / 32), 0);
+  const int lane = threadIdx.x % 32;
+  const int seq = blockIdx.x / a.nseg;   // (b, h)
+  const int seg = blockIdx.x % a.nseg;
+  const int b = seq / a.H, h = seq % a.H;
+  const int g = h / (a.H / a.G);
+  const int R = a.R;
+  const int tbase = seg * a.seg_tiles;
+  const int nt = min(a.ntiles - tbase, a.seg_tiles);
+  const int seg_row = tbase * kTileRows;
+  volatile int* abort = &s_abort;
+
+  if (threadIdx.x == 0) {
+    s_abort = 0;
+    s_keep_tmem = 0;
+    for (int s = 0; s < kXSlots; ++s) {
+      mbar_init(&bars->x_full[s], 1);
+      mbar_init(&bars->x_empty[s], 4);     // out warps, once their y store has read the slot
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&bars->b_full[s], 1);
+      mbar_init(&bars->b_empty[s], 1);     // MMA commit after K3 (CB of the tile came before)
+      mbar_init(&bars->cb_full[s], 1);
+      mbar_init(&bars->m_ready[s], kMaskWarps);
+    }
+    mbar_init(&bars->c_full, 1);
+    mbar_init(&bars->c_empty, 4);          // out warps, C row read into registers
+    mbar_init(&bars->cb_go, 4);            // out warps: C row in TMEM and B of the tile landed
+    for (int k = 0; k < kInfoSlots; ++k) {
+      mbar_init(&bars->info_ready[k], 1);
+      mbar_init(&bars->info_empty[k], 8);  // out and state warps
+    }
+    mbar_init(&bars->yd_full, 1);
+    mbar_init(&bars->yo_full, 1);
+    mbar_init(&bars->s_full, 1);
+    mbar_init(&bars->yo_go, 8);            // 4 state warps + 4 out warps
+    mbar_init(&bars->k3_go, kDxWarps + 4); // (dec o x) warps + 4 state warps
+    mbar_init(&bars->y_pre, 4);            // out warps
+    mbar_init(&bars->drain, 1);
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tm_x);
+    tma_prefetch_desc(&tm_b);
+    tma_prefetch_desc(&tm_c);
+    tma_prefetch_desc(&tm_y);
+  }
+  if (warp == 1) {
+    tmem_alloc(&s_tmem, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s_tmem;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------------ TMA producer
+    // Per tile: C (one slot, freed once the out warps hold it in registers), B (two stages,
+    // freed by K3), x (three slots, freed once y of the tile has been stored from the slot).
+    int nc = 0, nb = 0, nx = 0;   // tiles whose C, B, x loads were issued
+    for (int t = 0; t < nt; ++t) {
+      const int row = seg_row + t * kTileRows;   // rows past the sequence's end read as zeros
+      if (t >= 1 && !wait_bar(&bars->c_empty, (t - 1) & 1, abort, a.hdr, 31)) break;
+      mbar_arrive_expect_tx_elect(&bars->c_full, kBCBytes);
+      tma_load_4d_elect(smem + kOffC, &tm_c, &bars->c_full, 0, g, row, b);
+      tma_load_4d_elect(smem + kOffC + kBCBytes / 2, &tm_c, &bars->c_full, 64, g, row, b);
+      nc = t + 1;
+      const int sb = t & 1;
+      if (t >= 2 && !wait_bar(&bars->b_empty[sb], ((t - 2) >> 1) & 1, abort, a.hdr, 32)) break;
+      mbar_arrive_expect_tx_elect(&bars->b_full[sb], kBCBytes);
+      tma_load_4d_elect(smem + kOffB + sb * kBCBytes, &tm_b, &bars->b_full[sb], 0, g, row, b);
+      tma_load_4d_elect(smem + kOffB + sb * kBCBytes + kBCBytes / 2, &tm_b, &bars->b_full[sb], 64,
+                        g, row, b);
+      nb = t + 1;
+      const int sx = t % kXSlots;
+      if (t >= kXSlots &&
+          !wait_bar(&bars->x_empty[sx], ((t - kXSlots) / kXSlots) & 1, abort, a.hdr, 33))
+        break;
+      mbar_arrive_expect_tx_elect(&bars->x_full[sx], kXBytes);
+      tma_load_4d_elect(smem + kOffX + sx * kXBytes, &tm_x, &bars->x_full[sx], 0, h, row, b);
+      nx = t + 1;
+      if (t + 3 < nt) {   // pull a later tile into L2 so its load later finds it there
+        const int r3 = row + 3 * kTileRows;
+        tma_prefetch_l2_4d_elect(&tm_x, 0, h, r3, b);
+        tma_prefetch_l2_4d_elect(&tm_b, 0, g, r3, b);
+        tma_prefetch_l2_4d_elect(&tm_b, 64, g, r3, b);
+        tma_prefetch_l2_4d_elect(&tm_c, 0, g, r3, b);
+        tma_prefetch_l2_4d_elect(&tm_c, 64, g, r3, b);
+      }
+    }
+    // Drain: no TMA load may still be writing this CTA's shared memory when it exits.  In a
+    // normal run every load has been waited for by its consumer and these return at once.
+    // Slot s of an n-slot ring received the loads of tiles s, s + n, ... below the issued count;
+    // waiting for the parity of the last of them covers all of them.
+    bool drained = true;
+    for (int s = 0; s < kXSlots; ++s) {
+      const int k = nx > s ? (nx - 1 - s) / kXSlots + 1 : 0;
+      if (k > 0) drained &= mbar_wait_bounded(&bars->x_full[s], (k - 1) & 1, 2000000000ull);
+    }
+    for (int s = 0; s < 2; ++s) {
+      const int k = nb > s ? (nb - 1 - s) / 2 + 1 : 0;
+      if (k > 0) drained &= mbar_wait_bounded(&bars->b_full[s], (k - 1) & 1, 2000000000ull);
+    }
+    if (nc > 0) drained &= mbar_wait_bounded(&bars->c_full, (nc - 1) & 1, 2000000000ull);
+    if (!drained && lane == 0 && a.hdr) latch_error(a.hdr, SSD_ERR_TIMEOUT, 91);
+  } else if (warp == 1) {
+    // ------------------------------------------------------------------ MMA issuer
+    // The whole warp runs the loop and one elected lane issues each MMA; descriptors are
+    // precomputed 32-bit words plus constant offsets (a start-address step of s bytes adds
+    // s >> 4 to the low word).
+    constexpr uint32_t id_cb = idesc_bf16(128, 128, 0, 0);   // TS: A = C, B = B tile K-major
+    constexpr uint32_t id_n64 = idesc_bf16(128, 64, 0, 1);   // TS: A in TMEM, B MN-major
+    constexpr uint32_t id_k3 = idesc_bf16(128, 64, 1, 1);    // SS: A = B tile MN-major
+    constexpr uint32_t dhi = sdesc_sw128_hi(1024);
+    const uint32_t hlo = sdesc_sw128_lo(smem_u32(smem + kOffHHi), 0);
+    const uint32_t dxlo = sdesc_sw128_lo(smem_u32(smem + kOffDxHi), 0);
+    const uint32_t blo0 = sdesc_sw128_lo(smem_u32(smem + kOffB), 0);             // K-major
+    const uint32_t bmlo0 = sdesc_sw128_lo(smem_u32(smem + kOffB), kBCBytes / 2);  // MN-major
+    const uint32_t xlo0 = sdesc_sw128_lo(smem_u32(smem + kOffX), 0);
+    const uint32_t tC = tmem + kColC;
+    // A product's barrier is tested (non-blocking) before the previous product is issued; only
+    // if that test failed does the warp block on it afterwards.
+    auto gate = [&](uint32_t probed, uint64_t* bar, uint32_t parity, int site) -> bool {
+      if (!probed && !wait_bar(bar, parity, abort, a.hdr, site)) return false;
+      return true;
+    };
+    auto issue_cb = [&](int t) {
+      const uint32_t bl = blo0 + (t & 1) * (kBCBytes >> 4);
+      const uint32_t dm = tmem + kColM + (t & 1) * 128;
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks)
+        mma_ts_we(dm, tC + ks * 8, bl + (((ks >> 2) * (kBCBytes / 2) + (ks & 3) * 32) >> 4), dhi,
+                  id_cb, ks > 0);
+      mma_commit_elect(&bars->cb_full[t & 1]);
+    };
+    uint32_t p_yo = mbar_test_wait(&bars->yo_go, 0);
+    bool ok = gate(0, &bars->cb_go, 0, 35);
+    if (ok) {
+      tc_fence_after();
+      issue_cb(0);
+    }
+    for (int t = 0; ok && t < nt; ++t) {
+      const int sb = t & 1;
+      // Yo_t = C_t [h_hi ; h_lo]
+      const uint32_t p_k3 = mbar_test_wait(&bars->k3_go, t & 1);
+      if (!gate(p_yo, &bars->yo_go, t & 1, 36)) break;
+      tc_fence_after();
+#pragma unroll
+      for (int ks = 0; ks < 16; ++ks)
+        mma_ts_we(tmem + kColYo, tC + (ks & 7) * 8,
+                  hlo + (((ks < 8 ? 0u : kOffHLo - kOffHHi) + (ks & 7) * 2048) >> 4), dhi, id_n64,
+                  ks > 0);
+      mma_commit_elect(&bars->yo_full);
+      // K3_t = B_t^T [(dec o x)_hi ; (dec o x)_lo]
+      const uint32_t p_cb = t + 1 < nt ? mbar_test_wait(&bars->cb_go, (t + 1) & 1) : 1u;
+      if (!gate(p_k3, &bars->k3_go, t & 1, 38)) break;
+      tc_fence_after();
+      {
+        const uint32_t al = bmlo0 + sb * (kBCBytes >> 4);
+#pragma unroll
+        for (int ks = 0; ks < 16; ++ks)
+          mma_ss_we(tmem + kColS, al + (ks & 7) * (2048 >> 4), dhi,
+                    dxlo + (((ks < 8 ? 0u : kOffDxLo - kOffDxHi) + (ks & 7) * 2048) >> 4), dhi,
+                    id_k3, ks > 0);
+      }
+      mma_commit_elect(&bars->s_full);
+      mma_commit_elect(&bars->b_empty[sb]);
+      // CB of the next tile, into the other mask buffer
+      const uint32_t p_m = mbar_test_wait(&bars->m_ready[sb], (t >> 1) & 1);
+      const uint32_t p_pre = mbar_test_wait(&bars->y_pre, t & 1);
+      if (t + 1 < nt) {
+        if (!gate(p_cb, &bars->cb_go, (t + 1) & 1, 35)) break;
+        tc_fence_after();
+        issue_cb(t + 1);
+      }
+      // Yd_t += (L o CB)_hi x + (L o CB)_lo x onto e^{cum_i} Yo_t
+      p_yo = t + 1 < nt ? mbar_test_wait(&bars->yo_go, (t + 1) & 1) : 1u;
+      if (!gate(p_m, &bars->m_ready[sb], (t >> 1) & 1, 40)) break;
+      if (!gate(p_pre, &bars->y_pre, t & 1, 41)) break;
+      tc_fence_after();
+      {
+        const uint32_t xl = xlo0 + (t % kXSlots) * (kXBytes >> 4);
+        const uint32_t am = tmem + kColM + sb * 128;
+#pragma unroll
+        for (int ks = 0; ks < 16; ++ks) {
+          const int kk = ks & 7;
+          const uint32_t acol = (kk >> 1) * 32 + (kk & 1) * 8 + (ks < 8 ? 0 : 16);
+          mma_ts_we(tmem + kColYd, am + acol, xl + kk * (2048 >> 4), dhi, id_n64, 1);
+        }
+      }
+      mma_commit_elect(&bars->yd_full);
+    }
+    // Drain: every MMA issued has completed before TMEM is freed.
+    mma_commit_elect(&bars->drain);
+    if (!mbar_wait_bounded(&bars->drain, 0, 2000000000ull) && lane == 0) {
+      s_keep_tmem = 1;   // MMAs may still write TMEM: leave it allocated
+      if (a.hdr) latch_error(a.hdr, SSD_ERR_TIMEOUT, 92);
+    }
+  } else if (warp == 2) {
+    k1_warp(a, info, bars->info_ready, bars->info_empty, abort, b, h, tbase, nt, lane);
+  } else {
+    const int q = warp & 3;                 // TMEM lane quarter == SM sub-partition
+    const int i = q * 32 + lane;            // tile row / state row of this thread
+    const uint32_t lane_addr = static_cast<uint32_t>(q * 32) << 16;
+    if (warp == 3 || (warp >= 4 && warp < 8)) {
+      // ---------------------------------------------------------------- mask warps
+      const int jlim = (i / R + 1) * R;     // columns j < jlim are at or before row i's step
+      const MaskShare ms = mask_share(warp);
+      const int2 du = dx_units(warp);
+      const bool has_dx = du.y > du.x;
+      // (dec o x)_t split into hi and lo (own buffers; x_t stays for Yd_t).
+      auto dec_x = [&](int t) -> bool {
+        const int slot = t % kInfoSlots;
+        const TileInfo& ti = info[slot];
+        if (!wait_bar(&bars->info_ready[slot], (t / kInfoSlots) & 1, abort, a.hdr, 45))
+          return false;
+        if (!wait_bar(&bars->x_full[t % kXSlots], (t / kXSlots) & 1, abort, a.hdr, 46))
+          return false;
+        if (t >= 1 && !wait_bar(&bars->s_full, (t - 1) & 1, abort, a.hdr, 47)) return false;
+        const uint8_t* xs = smem + kOffX + (t % kXSlots) * kXBytes;
+        uint8_t* dhi = smem + kOffDxHi;
+        uint8_t* dlo = smem + kOffDxLo;
+#pragma unroll 1
+        for (int u = du.x; u < du.y; ++u) {
+          const int row = (u >> 2) * 32 + lane, c0 = (u & 3) * 16;
+          const float wd =
+              ex2_approx((ti.last_hi - ti.cum_hi[row]) + (ti.last_lo - ti.cum_lo[row]));
+          const float2 w2 = make_float2(wd, wd);
+          const uint32_t o0 = sw128_off16(row, c0), o1 = sw128_off16(row, c0 + 8);
+          const uint4 v0 = *reinterpret_cast<const uint4*>(xs + o0);
+          const uint4 v1 = *reinterpret_cast<const uint4*>(xs + o1);
+          uint4 h0, l0, h1, l1;
+          split2(mul2(unpack_bf16(v0.x), w2), h0.x, l0.x);
+          split2(mul2(unpack_bf16(v0.y), w2), h0.y, l0.y);
+          split2(mul2(unpack_bf16(v0.z), w2), h0.z, l0.z);
+          split2(mul2(unpack_bf16(v0.w), w2), h0.w, l0.w);
+          split2(mul2(unpack_bf16(v1.x), w2), h1.x, l1.x);
+          split2(mul2(unpack_bf16(v1.y), w2), h1.y, l1.y);
+          split2(mul2(unpack_bf16(v1.z), w2), h1.z, l1.z);
+          split2(mul2(unpack_bf16(v1.w), w2), h1.w, l1.w);
+          *reinterpret_cast<uint4*>(dhi + o0) = h0;
+          *reinterpret_cast<uint4*>(dhi + o1) = h1;
+          *reinterpret_cast<uint4*>(dlo + o0) = l0;
+          *reinterpret_cast<uint4*>(dlo + o1) = l1;
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->k3_go);
+        return true;
+      };
+      // Mask blocks of tile t for this thread's row, in place over CB_t (mask buffer t & 1).
+      auto mask_part = [&](int t) -> bool {
+        const int slot = t % kInfoSlots;
+        const TileInfo& ti = info[slot];
+        if (!wait_bar(&bars->info_ready[slot], (t / kInfoSlots) & 1, abort, a.hdr, 43))
+          return false;
+        if (!wait_bar(&bars->cb_full[t & 1], (t >> 1) & 1, abort, a.hdr, 44)) return false;
+        tc_fence_after();
+        const uint32_t mb = tmem + lane_addr + kColM + (t & 1) * 128;
+        const bool fact_ok = ti.monotone != 0;
+        const float chi = ti.cum_hi[i], clo = ti.cum_lo[i];
+#pragma unroll 1
+        for (int cb = ms.cb0; cb < ms.cb1; ++cb) {
+          float w[32];
+          tmem_ld32(mb + cb * 32, w);
+          tmem_ld_wait();
+          reg_tie(w);
+          uint32_t hi[16], lo[16];
+          mask_block(ti, cb, cb == q || !fact_ok, chi, clo, jlim, w, hi, lo);
+          tmem_st16u(mb + cb * 32, hi);
+          tmem_st16u(mb + cb * 32 + 16, lo);
+        }
+        if (ms.cb1 < ms.zero_end) {
+          uint32_t z[16];
+#pragma unroll
+          for (int k = 0; k < 16; ++k) z[k] = 0u;
+#pragma unroll 1
+          for (int cb = ms.cb1; cb < ms.zero_end; ++cb) {
+            tmem_st16u(mb + cb * 32, z);
+            tmem_st16u(mb + cb * 32 + 16, z);
+          }
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->m_ready[t & 1]);
+        return true;
+      };
+      for (int t = 0; t < nt; ++t) {
+        if (has_dx && !dec_x(t)) break;
+        if (!mask_part(t)) break;
+      }
+    } else if (warp < 12) {
+      // ---------------------------------------------------------------- state warps
+      // Thread = state row n = i; h^T[n][0..63] in registers across the whole sequence.
+      const size_t st_base = (size_t)seq * kP * kN;
+      const size_t seg_base = ((size_t)seq * a.nseg + seg) * kP * kN;
+      const float* init0 = seg == 0 ? (a.init ? a.init + st_base : nullptr) : a.seg_init + seg_base;
+      float hv[kP];
+#pragma unroll
+      for (int p = 0; p < kP; ++p) hv[p] = init0 ? init0[(size_t)p * kN + i] : 0.f;
+      if (lane == 0) mbar_arrive(&bars->k3_go);   // the S accumulator is free for K3_0
+      // t = -1 publishes h_0; iteration t folds S_t into the state and publishes h_{t+1}
+      for (int t = -1; t < nt; ++t) {
+        if (t >= 0) {
+          const int slot = t % kInfoSlots;
+          if (!wait_bar(&bars->info_ready[slot], (t / kInfoSlots) & 1, abort, a.hdr, 48)) break;
+          if (!wait_bar(&bars->s_full, t & 1, abort, a.hdr, 49)) break;
+          tc_fence_after();
+          const float e = info[slot].etile;
+          const float2 e2 = make_float2(e, e);
+#pragma unroll
+          for (int c = 0; c < kP; c += 32) {
+            float sv[32];
+            tmem_ld32(tmem + lane_addr + kColS + c, sv);
+            tmem_ld_wait();
+            reg_tie(sv);
+#pragma unroll
+            for (int k = 0; k < 32; k += 2) {
+              const float2 v = fma2(e2, make_float2(hv[c + k], hv[c + k + 1]),
+                                    make_float2(sv[k], sv[k + 1]));
+              hv[c + k] = v.x;
+              hv[c + k + 1] = v.y;
+            }
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) {
+            if (t + 1 < nt) mbar_arrive(&bars->k3_go);   // S_t read: K3_{t+1} may go
+            mbar_arrive(&bars->info_empty[slot]);
+          }
+          if (t + 1 == nt) break;
+          // Yo_t has read h_t from the operand buffer (it was issued before K3_t)
+          if (!wait_bar(&bars->yo_full, t & 1, abort, a.hdr, 50)) break;
+        }
+        // h^T row n as bf16 hi and lo rows of the Yo operand
+        uint8_t* hhi = smem + kOffHHi;
+        uint8_t* hlo = smem + kOffHLo;
+#pragma unroll
+        for (int k = 0; k < kP; k += 8) {
+          uint4 uh, ul;
+          split2(make_float2(hv[k], hv[k + 1]), uh.x, ul.x);
+          split2(make_float2(hv[k + 2], hv[k + 3]), uh.y, ul.y);
+          split2(make_float2(hv[k + 4], hv[k + 5]), uh.z, ul.z);
+          split2(make_float2(hv[k + 6], hv[k + 7]), uh.w, ul.w);
+          const uint32_t off = sw128_off16(i, k);
+          *reinterpret_cast<uint4*>(hhi + off) = uh;
+          *reinterpret_cast<uint4*>(hlo + off) = ul;
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->yo_go);
+      }
+      if (a.final_state && seg == a.nseg - 1 && !*abort) {
+#pragma unroll
+        for (int p = 0; p < kP; ++p) a.final_state[st_base + (size_t)p * kN + i] = hv[p];
+      }
+    } else {
+      // ---------------------------------------------------------------- out warps
+      // Per tile: e^{cum_i} Yo_t into the y accumulator; C_{t+1} into TMEM once Yo_t has read
+      // C_t; then y_t = the accumulator after Yd_t -> bf16 -> the tile's x slot -> TMA store.
+      auto copy_c = [&](int t) -> bool {
+        if (!wait_bar(&bars->c_full, t & 1, abort, a.hdr, 51)) return false;
+        const uint8_t* cs = smem + kOffC;
+#pragma unroll
+        for (int blk = 0; blk < 2; ++blk) {
+          uint32_t w[32];
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            const uint4 v = *reinterpret_cast<const uint4*>(cs + blk * (kBCBytes / 2) +
+                                                            sw128_off16(i, c * 8));
+            w[c * 4 + 0] = v.x;
+            w[c * 4 + 1] = v.y;
+            w[c * 4 + 2] = v.z;
+            w[c * 4 + 3] = v.w;
+          }
+          tmem_st32u(tmem + lane_addr + kColC + blk * 32, w);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->c_empty);
+        tmem_st_wait();
+        tc_fence_before();
+        // CB_t also needs B_t: the MMA warp waits for both on cb_go
+        if (!wait_bar(&bars->b_full[t & 1], (t >> 1) & 1, abort, a.hdr, 55)) return false;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->cb_go);
+        return true;
+      };
+      if (lane == 0) mbar_arrive(&bars->yo_go);   // no Yo to read before tile 0
+      int stored = 0;   // y stores issued by this warp (lane 0)
+      // t = -1 only copies C_0
+      for (int t = -1; t < nt; ++t) {
+        if (t < 0) {
+          if (!copy_c(0)) break;
+          continue;
+        }
+        const int slot = t % kInfoSlots;
+        if (!wait_bar(&bars->info_ready[slot], (t / kInfoSlots) & 1, abort, a.hdr, 54)) break;
+        if (!wait_bar(&bars->yo_full, t & 1, abort, a.hdr, 52)) break;
+        tc_fence_after();
+        const TileInfo& ti = info[slot];
+        {
+          // e^{cum_i} Yo_t into the y accumulator (y_{t-1} was read in the previous iteration)
+          const float sc = ex2_approx(ti.cum_hi[i] + ti.cum_lo[i]);
+          const float2 sc2 = make_float2(sc, sc);
+#pragma unroll
+          for (int c = 0; c < kP; c += 32) {
+            float vo[32];
+            tmem_ld32(tmem + lane_addr + kColYo + c, vo);
+            tmem_ld_wait();
+            reg_tie(vo);
+            uint32_t vu[32];
+#pragma unroll
+            for (int k = 0; k < 32; k += 2) {
+              const float2 v = mul2(sc2, make_float2(vo[k], vo[k + 1]));
+              vu[k] = __float_as_uint(v.x);
+              vu[k + 1] = __float_as_uint(v.y);
+            }
+            tmem_st32u(tmem + lane_addr + kColYd + c, vu);
+          }
+          tmem_st_wait();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) {
+            mbar_arrive(&bars->y_pre);
+            if (t + 1 < nt) mbar_arrive(&bars->yo_go);   // Yo_t read
+          }
+        }
+        if (t + 1 < nt && !copy_c(t + 1)) break;
+        if (!wait_bar(&bars->yd_full, t & 1, abort, a.hdr, 53)) break;
+        tc_fence_after();
+        uint8_t* ys = smem + kOffX + (t % kXSlots) * kXBytes;   // x_t is no longer needed
+#pragma unroll
+        for (int c = 0; c < kP; c += 32) {
+          float vy[32];
+          tmem_ld32(tmem + lane_addr + kColYd + c, vy);
+          tmem_ld_wait();
+          reg_tie(vy);
+          uint32_t pk[16];
+#pragma unroll
+          for (int k = 0; k < 16; ++k) pk[k] = pack_bf16(vy[2 * k], vy[2 * k + 1]);
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            *reinterpret_cast<uint4*>(ys + sw128_off16(i, c + 8 * k)) =
+                make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
+        }
+        tc_fence_before();
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&bars->info_empty[slot]);
+          tma_store_4d(&tm_y, ys + q * 4096, 0, h, seg_row + t * kTileRows + q * 32, b);
+          bulk_commit_group();
+          ++stored;
+          // the store of the previous tile has read its slot: hand it back to the producer
+          if (stored >= 2) {
+            bulk_wait_group_read<1>();
+            mbar_arrive(&bars->x_empty[(t - 1) % kXSlots]);
+          }
+        }
+        __syncwarp();
+      }
+      if (lane == 0) {
+        bulk_wait_group<0>();   // every y store complete before the CTA exits
+      }
+      __syncwarp();
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1 && !s_keep_tmem) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+}  // namespace full
+
 PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   static std::once_flag once;
@@ -768,16 +1374,16 @@ bool make_map(CUtensorMap* m, CUtensorMapDataType dt, uint32_t rank, const void*
 // Encoded tensor maps of the last few distinct (pointers, shape) keys per host thread: a call
 // with the same buffers skips the three encodes.
 struct MapKey {
-  const void *x, *B, *C;
+  const void *x, *B, *C, *y;
   int64_t batch, T, H, G, R, P, N;
   bool operator==(const MapKey& o) const {
-    return x == o.x && B == o.B && C == o.C && batch == o.batch && T == o.T && H == o.H &&
-           G == o.G && R == o.R && P == o.P && N == o.N;
+    return x == o.x && B == o.B && C == o.C && y == o.y && batch == o.batch && T == o.T &&
+           H == o.H && G == o.G && R == o.R && P == o.P && N == o.N;
   }
 };
 struct MapEntry {
   MapKey key;
-  CUtensorMap mx, mb, mc;
+  CUtensorMap mx, mb, mc, my;
   bool valid = false;
 };
 constexpr int kMapCacheSize = 4;
@@ -794,6 +1400,11 @@ bool encode_maps(const GenericParams& p, MapEntry& m) {
     if (!make_map(&m.mx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, p.x, dims, str, box,
                   CU_TENSOR_MAP_SWIZZLE_128B))
       return false;
+    // y has x's layout; each out warp stores its 32 rows of a tile
+    cuuint32_t ybox[4] = {64, 1, 32, 1};
+    if (!make_map(&m.my, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, p.y, dims, str, ybox,
+                  CU_TENSOR_MAP_SWIZZLE_128B))
+      return false;
   }
   cuuint64_t dims[4] = {(cuuint64_t)p.N, (cuuint64_t)p.G, (cuuint64_t)rows, (cuuint64_t)p.batch};
   cuuint64_t str[3] = {(cuuint64_t)p.N * 2, (cuuint64_t)p.G * p.N * 2,
@@ -808,7 +1419,7 @@ bool encode_maps(const GenericParams& p, MapEntry& m) {
 const MapEntry* cached_maps(const GenericParams& p) {
   thread_local MapEntry cache[kMapCacheSize];
   thread_local int next = 0;
-  const MapKey key{p.x, p.B, p.C, p.batch, p.T, p.H, p.G, p.R, p.P, p.N};
+  const MapKey key{p.x, p.B, p.C, p.y, p.batch, p.T, p.H, p.G, p.R, p.P, p.N};
   for (auto& m : cache)
     if (m.valid && m.key == key) return &m;
   MapEntry& m = cache[next];
@@ -828,8 +1439,8 @@ cudaError_t ensure_smem_attribute() {
   if (e != cudaSuccess) return e;
   const uint64_t bit = dev < 64 ? (1ull << dev) : 0ull;
   if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
-  e = cudaFuncSetAttribute(ssd_fused_bf16_kernel<false>,
-                           cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
+  e = cudaFuncSetAttribute(full::ssd_fused_full_kernel,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, full::kSmem);
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(ssd_fused_bf16_kernel<true>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
@@ -931,8 +1542,8 @@ cudaError_t fused_bf16_forward(const GenericParams& p, cudaStream_t st) {
     fused_seg_carry_kernel<<<(unsigned)((elems + 255) / 256), 256, 0, st>>>(a, elems);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
-  ssd_fused_bf16_kernel<false><<<seqs * a.nseg, kThreadsFused, kSmemAlloc, st>>>(a, m->mx, m->mb,
-                                                                                 m->mc);
+  full::ssd_fused_full_kernel<<<seqs * a.nseg, full::kThreads, full::kSmem, st>>>(
+      a, m->mx, m->mb, m->mc, m->my);
   return cudaGetLastError();
 }
 
