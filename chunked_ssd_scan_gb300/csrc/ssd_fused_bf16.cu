@@ -1,16 +1,16 @@
 // Fused tcgen05/TMEM chunked SSD forward for bf16 I/O (sm_103a).
 //
-// One CTA owns one (batch, head) sequence and walks it in tiles of 128 rank-fused rows
-// (fused row i = t*R + r, as in the serial.rs page's K2 reshape), carrying the state on chip
-// from tile to tile, so the inter-chunk state of K4 never goes to HBM.  Per tile:
+// One CTA owns one (batch, head) sequence (or a time segment of one) and walks it in tiles of
+// 128 rank-fused rows (fused row i = t*R + r, as in the serial.rs page's K2 reshape), carrying
+// the state on chip from tile to tile, so the inter-chunk state of K4 never goes to HBM.  Per
+// tile:
 //   K1  tile-local inclusive cumsum of dA (double-float), decay factors
-//   K2  CB = C B^T                                   tcgen05.mma  M128 N128 K128 -> TMEM
+//   K2  CB = C B^T                                       tcgen05.mma, A = C from TMEM
 //   K5a (L o CB), L[i,j] = exp(cum[i/R] - cum[j/R]) for j/R <= i/R else 0, split into bf16
-//       hi + lo and written back to TMEM;  Yd = (L o CB) x     tcgen05.mma (A from TMEM)
+//       hi + lo and written back to TMEM;  Yd = (L o CB) x     tcgen05.mma, A from TMEM
 //   K3  S^T = B^T (dec o x), dec_i = exp(cum_last - cum[i/R]), (dec o x) split hi + lo
-//   K5b Yo = C h_in, h_in split hi + lo;  y = Yd + exp(cum[i/R]) Yo -> bf16 -> global
-//   K4  h_out = exp(cum_last) h_in + S^T: the K3 accumulator is preloaded with
-//       exp(cum_last) h_in, so the tensor core adds S^T onto the decayed state.
+//   K5b Yo = C h_in, h_in split hi + lo;  y = Yd + exp(cum[i/R]) Yo -> bf16 -> TMA store
+//   K4  h_out = exp(cum_last) h_in + S^T in fp32 registers of the state warps
 // The serial.rs page runs K1..K5 per chunk with the K4 loop across chunks; a 128-row tile is a
 // sub-block of a chunk, and the part of a chunk's 1-semiseparable mask below a tile's diagonal
 // block has rank one (exp(cum_i - cum_j) = exp(cum_i) exp(-cum_j)), which is exactly what the
@@ -22,26 +22,14 @@
 // Operands that are products of inputs ((L o CB), dec o x and h_in) are carried as two bf16
 // terms (hi + lo, ~16 mantissa bits): one bf16 rounding of them is far too coarse for the
 // 2e-2 (1 + |y|) bound when decay is slow and y cancels.  Products of two bf16 inputs are exact
-// in the fp32 accumulators.
-//
-// Warp roles (352 threads; TMEM lane quarter q = warp % 4 is the SM sub-partition):
-//   warp 0      TMA producer (x, B, C tiles; two stages)
-//   warp 1      MMA issuer and TMEM owner; per tile: Yd_t, CB_{t+1}, Yo_t, K3_t
-//   warp 2      K1 for each tile as soon as its dA lands (runs ahead of the math warps)
-//   warps 3-6   "mask" warps, one per lane quarter q: (dec o x)_t for a share of the rows
-//               (larger shares on the quarters with less mask work), then the diagonal
-//               block q and the block q-1 of the mask of tile t+1
-//   warps 7-10  "state" warps, one per quarter: the mask blocks 0..q-2 of tile t+1, the output
-//               rows of quarter q of tile t, and state rows of quarter q (h_in split for Yo,
-//               decayed state preloaded into the K3 accumulator)
-// Each warp rewrites only TMEM columns that it has read itself, so the masked operand is
-// formed in place without a barrier between warps.  Every wait is bounded; a wait that gives
-// up latches SSD_ERR_TIMEOUT in the workspace header and the CTA stops issuing work.
+// in the fp32 accumulators.  Every wait is bounded; a wait that gives up latches
+// SSD_ERR_TIMEOUT in the workspace header and the CTA stops issuing work, drains the TMA loads
+// and MMAs it issued, and frees its TMEM.
 //
 // Ragged sequences: when seqlen * R is not a multiple of 128 the last tile is partial.  The
 // tensor maps carry the batch as their own dimension, so TMA fills the rows past the end of a
-// sequence with zeros (x = B = C = 0), K1 reads dA = 0 there, and no y is written for them:
-// zero padding, which leaves y of the real steps and the final state unchanged.
+// sequence with zeros (x = B = C = 0), K1 reads dA = 0 there, and the TMA store writes no y
+// there: zero padding, which leaves y of the real steps and the final state unchanged.
 //
 // Time segments: with fewer sequences than SMs, each sequence is cut into segments run by
 // separate CTAs.  The same kernel in its state-only form (kPre: K1, dec o x, K3 and K4; no C,
@@ -72,21 +60,12 @@ using namespace fp;
 constexpr int kTileRows = 128;
 constexpr int kP = 64;
 constexpr int kN = 128;
-constexpr int kThreadsFused = 352;
 constexpr long long kWaitCycles = 4000000000ll;   // per wait before giving up (~2 s at 2 GHz)
 constexpr float kLog2e = 1.4426950408889634f;
 
-// Shared-memory map (offsets from the 1024-aligned dynamic shared window).
 constexpr uint32_t kXBytes = kTileRows * kP * 2;          // 16 KB per stage
 constexpr uint32_t kBCBytes = kTileRows * kN * 2;         // 32 KB per stage (two 64-col blocks)
-constexpr uint32_t kOffX = 0;                              // 2 stages (x, then (dec o x) hi)
-constexpr uint32_t kOffXlo = kOffX + 2 * kXBytes;          // (dec o x) lo
-constexpr uint32_t kOffB = kOffXlo + kXBytes;              // 2 stages
-constexpr uint32_t kOffC = kOffB + 2 * kBCBytes;           // 2 stages
-constexpr uint32_t kOffHhi = kOffC + 2 * kBCBytes;         // h_in hi  [N rows][P]
-constexpr uint32_t kOffHlo = kOffHhi + kN * kP * 2;        // h_in lo
 constexpr int kInfoSlots = 4;                             // K1 runs up to this many tiles ahead
-constexpr uint32_t kOffInfo = kOffHlo + kN * kP * 2;       // ring of per-tile K1 results
 struct TileInfo {
   float cum_hi[kTileRows];   // log2-scaled prefix sum of dA at fused row j (hi part)
   float cum_lo[kTileRows];   // ... lo part
@@ -96,33 +75,7 @@ struct TileInfo {
   int monotone;              // 1 if every dA of the tile is <= 0 (factorized mask is safe)
   float pad[28];
 };
-constexpr uint32_t kOffBar = kOffInfo + kInfoSlots * sizeof(TileInfo);
-constexpr uint32_t kSmemUsed = kOffBar + 256;
-constexpr uint32_t kSmemAlloc = kSmemUsed;
-static_assert(kSmemAlloc <= 232448, "exceeds the 227 KB shared-memory limit per CTA");
-
-// TMEM columns (128 lanes x 512 columns of 32 bit).
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColM = 0;     // CB fp32 [0,128); each 32-column block cb is rewritten in
-                                  // place as 16 columns of (L o CB) hi then 16 columns of lo,
-                                  // two bf16 per column
-constexpr uint32_t kColYd = 128;  // Yd, two buffers: [128,192) and [192,256)
-constexpr uint32_t kColYo = 256;  // Yo from h_hi [256,320) and from h_lo [320,384)
-constexpr uint32_t kColS = 384;   // exp(cum_last) h_in + B^T (dec o x)_hi [384,448),
-                                  // B^T (dec o x)_lo [448,512)
-
-// (dec o x) work units (32 rows x 16 columns) per lane quarter: the quarters with fewer mask
-// blocks (and no other role on their sub-partition) take more.
-__device__ __forceinline__ int xs_unit_begin(int q) {
-  return q == 0 ? 0 : (q == 1 ? 7 : (q == 2 ? 12 : 13));
-}
-__device__ __forceinline__ int xs_unit_end(int q) { return q == 3 ? 16 : xs_unit_begin(q + 1); }
-
-struct Bars {
-  uint64_t full[2], empty[2], info_ready[kInfoSlots], info_empty[kInfoSlots];
-  uint64_t cb_full, m_ready, yd_full, xs_ready, yo_full, s_full, hb_full;
-};
-static_assert(sizeof(Bars) + 8 <= 256, "barrier block");
 
 struct FusedArgs {
   const float* dA;
@@ -296,465 +249,6 @@ __device__ __forceinline__ void k1_warp(const FusedArgs& a, TileInfo* info, uint
   }
 }
 
-// kPre = true: the state-only pre-pass of a segment (K1, (dec o x), K3, K4; no CB, mask, Yd, Yo
-// or output).  kPre = false: the full forward of a segment.
-template <bool kPre>
-__global__ void __launch_bounds__(kThreadsFused, 1)
-    ssd_fused_bf16_kernel(FusedArgs a, const __grid_constant__ CUtensorMap tm_x,
-                          const __grid_constant__ CUtensorMap tm_b,
-                          const __grid_constant__ CUtensorMap tm_c) {
-  // The dynamic shared window is declared 1024-byte aligned (required by the 128-byte swizzle
-  // atoms) and addressed directly, so every access stays a shared-memory access.
-  extern __shared__ __align__(1024) uint8_t smem[];
-  Bars* bars = reinterpret_cast<Bars*>(smem + kOffBar);
-  TileInfo* info = reinterpret_cast<TileInfo*>(smem + kOffInfo);
-  uint32_t& s_tmem = *reinterpret_cast<uint32_t*>(smem + kOffBar + sizeof(Bars));
-  int& s_abort = *reinterpret_cast<int*>(smem + kOffBar + sizeof(Bars) + 4);
-  if ((smem_u32(smem) & 1023u) != 0) {   // never expected; refuse rather than mis-swizzle
-    if (threadIdx.x == 0 && a.hdr) latch_error(a.hdr, SSD_ERR_CUDA, 99);
-    return;
-  }
-
-  // warp index broadcast from lane 0: provably uniform, so role branches stay convergent
-  const int warp = __shfl_sync(0xffffffffu, static_cast<int>(threadIdx.x / 32), 0);
-  const int lane = threadIdx.x % 32;
-  const int nrun = kPre ? a.nseg - 1 : a.nseg;   // segments this launch runs per sequence
-  const int seq = blockIdx.x / nrun;             // (b, h)
-  const int seg = blockIdx.x % nrun;
-  const int b = seq / a.H, h = seq % a.H;
-  const int g = h / (a.H / a.G);
-  const int R = a.R, steps = a.steps;
-  const int tbase = seg * a.seg_tiles;           // first tile of this segment
-  const int nt = min(a.ntiles - tbase, a.seg_tiles);
-  const int seg_row = tbase * kTileRows;                  // fused row (within the sequence)
-                                                         // of the segment's start
-  const int64_t row_base = (int64_t)b * a.T * R + seg_row;   // ... in the whole tensor
-  volatile int* abort = &s_abort;
-
-  if (threadIdx.x == 0) {
-    s_abort = 0;
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(&bars->full[s], 1);
-      mbar_init(&bars->empty[s], 1);                // MMA commit after the stage's last MMA
-    }
-    for (int k = 0; k < kInfoSlots; ++k) {
-      mbar_init(&bars->info_ready[k], 1);
-      mbar_init(&bars->info_empty[k], 4);   // state warps, after the tile's last use of its info
-    }
-    mbar_init(&bars->cb_full, 1);
-    mbar_init(&bars->m_ready, 6);            // 4 mask warps + the state warps of quarters 2, 3
-    mbar_init(&bars->yd_full, 1);
-    mbar_init(&bars->xs_ready, 4);
-    mbar_init(&bars->yo_full, 1);
-    mbar_init(&bars->s_full, 1);
-    mbar_init(&bars->hb_full, 4);
-    fence_mbar_init();
-  }
-  if (warp == 0 && lane == 0) {
-    tma_prefetch_desc(&tm_x);
-    tma_prefetch_desc(&tm_b);
-    tma_prefetch_desc(&tm_c);
-  }
-  if (warp == 1) {
-    tmem_alloc(&s_tmem, kTmemCols);
-    tmem_relinquish();
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = s_tmem;
-
-  if (warp == 0) {
-    // ------------------------------------------------------------------ TMA producer
-    const uint32_t tx = kPre ? kXBytes + kBCBytes : kXBytes + 2 * kBCBytes;
-    for (int t = 0; t < nt; ++t) {
-      const int s = t & 1;
-      if (t >= 2 && !wait_bar(&bars->empty[s], ((t - 2) >> 1) & 1, abort, a.hdr, 1)) break;
-      mbar_arrive_expect_tx_elect(&bars->full[s], tx);
-      const int row = seg_row + t * kTileRows;   // rows past the sequence's end read as zeros
-      tma_load_4d_elect(smem + kOffX + s * kXBytes, &tm_x, &bars->full[s], 0, h, row, b);
-      tma_load_4d_elect(smem + kOffB + s * kBCBytes, &tm_b, &bars->full[s], 0, g, row, b);
-      tma_load_4d_elect(smem + kOffB + s * kBCBytes + kBCBytes / 2, &tm_b, &bars->full[s], 64, g,
-                        row, b);
-      if (!kPre) {   // the pre-pass needs no C
-        tma_load_4d_elect(smem + kOffC + s * kBCBytes, &tm_c, &bars->full[s], 0, g, row, b);
-        tma_load_4d_elect(smem + kOffC + s * kBCBytes + kBCBytes / 2, &tm_c, &bars->full[s], 64,
-                          g, row, b);
-      }
-      // Tile t+2 reuses this stage only after K3_t; pulling it into L2 now takes the DRAM
-      // latency out of that later load.
-      if (t + 2 < nt) {
-        const int r2 = row + 2 * kTileRows;
-        tma_prefetch_l2_4d_elect(&tm_x, 0, h, r2, b);
-        tma_prefetch_l2_4d_elect(&tm_b, 0, g, r2, b);
-        tma_prefetch_l2_4d_elect(&tm_b, 64, g, r2, b);
-        if (!kPre) {
-          tma_prefetch_l2_4d_elect(&tm_c, 0, g, r2, b);
-          tma_prefetch_l2_4d_elect(&tm_c, 64, g, r2, b);
-        }
-      }
-    }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------------ MMA issuer
-    // Per tile t the issue order is  Yd_t, CB_{t+1}, Yo_t, K3_t.  CB_{t+1} overwrites the TMEM
-    // columns that Yd_t reads as its A operand; MMAs issued by one thread execute in order.
-    // Every MMA loop is straight-line code (no branch between two MMAs).
-    const uint32_t id_cb = idesc_bf16(128, 128, 0, 0);
-    const uint32_t id_yd = idesc_bf16(128, 64, 0, 1);
-    const uint32_t id_k3 = idesc_bf16(128, 128, 1, 1);
-    const uint32_t id_yo = idesc_bf16(128, 128, 0, 1);
-    const uint32_t sXlo = smem_u32(smem + kOffXlo);
-    const uint32_t sHhi = smem_u32(smem + kOffHhi);
-    auto issue_cb = [&](int t) {
-      const int s = t & 1;
-      const uint32_t sB = smem_u32(smem + kOffB + s * kBCBytes);
-      const uint32_t sC = smem_u32(smem + kOffC + s * kBCBytes);
-      tc_fence_after();
-#pragma unroll
-      for (int ks = 0; ks < 8; ++ks) {
-        const uint32_t off = (ks >> 2) * (kBCBytes / 2) + (ks & 3) * 32;
-        mma_bf16_elect(tmem + kColM, sdesc_sw128(sC + off, 0, 1024),
-                       sdesc_sw128(sB + off, 0, 1024), id_cb, ks > 0);
-      }
-      mma_commit_elect(&bars->cb_full);
-    };
-    if constexpr (kPre) {
-      // K3 only; (dec o x)_lo of tile t sits in the (unused) C stage t & 1
-      for (int t = 0; t < nt; ++t) {
-        const int s = t & 1;
-        const uint32_t sB = smem_u32(smem + kOffB + s * kBCBytes);
-        const uint32_t sX = smem_u32(smem + kOffX + s * kXBytes);
-        const uint32_t lbo_x = smem_u32(smem + kOffC + s * kXBytes) - sX;
-        if (!wait_bar(&bars->hb_full, t & 1, abort, a.hdr, 7)) break;
-        if (!wait_bar(&bars->xs_ready, t & 1, abort, a.hdr, 10)) break;
-        tc_fence_after();
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
-          mma_bf16_elect(tmem + kColS, sdesc_sw128(sB + ks * 2048, kBCBytes / 2, 1024),
-                         sdesc_sw128(sX + ks * 2048, lbo_x, 1024), id_k3, 1);
-        }
-        mma_commit_elect(&bars->s_full);
-        if (t + 2 < nt) mma_commit_elect(&bars->empty[s]);
-      }
-    } else {
-    bool ok = wait_bar(&bars->full[0], 0, abort, a.hdr, 2);
-    if (ok) issue_cb(0);
-    for (int t = 0; ok && t < nt; ++t) {
-      const int s = t & 1;
-      const uint32_t sB = smem_u32(smem + kOffB + s * kBCBytes);
-      const uint32_t sC = smem_u32(smem + kOffC + s * kBCBytes);
-      const uint32_t sX = smem_u32(smem + kOffX + s * kXBytes);
-      // Yd = (L o CB)_hi x + (L o CB)_lo x   (A from TMEM; K = 2 x 128).  Block cb of the
-      // operand holds hi in columns [32cb, 32cb+16) and lo in [32cb+16, 32cb+32).
-      if (!wait_bar(&bars->m_ready, t & 1, abort, a.hdr, 3)) break;
-      tc_fence_after();
-      const uint32_t yd = tmem + kColYd + (t & 1) * 64;
-#pragma unroll
-      for (int ks = 0; ks < 16; ++ks) {
-        const int kk = ks & 7;
-        const uint32_t acol = kColM + (kk >> 1) * 32 + (kk & 1) * 8 + (ks < 8 ? 0 : 16);
-        mma_bf16_ts_elect(yd, tmem + acol, sdesc_sw128(sX + kk * 2048, 0, 1024), id_yd, ks > 0);
-      }
-      mma_commit_elect(&bars->yd_full);
-      // CB of the next tile
-      if (t + 1 < nt) {
-        if (!wait_bar(&bars->full[(t + 1) & 1], ((t + 1) >> 1) & 1, abort, a.hdr, 5)) break;
-        issue_cb(t + 1);
-      }
-      // Yo = C [h_hi | h_lo]   (N = 128; the two halves are summed in the output step)
-      if (!wait_bar(&bars->hb_full, t & 1, abort, a.hdr, 7)) break;
-      tc_fence_after();
-#pragma unroll
-      for (int ks = 0; ks < 8; ++ks) {
-        const uint32_t offa = (ks >> 2) * (kBCBytes / 2) + (ks & 3) * 32;
-        mma_bf16_elect(tmem + kColYo, sdesc_sw128(sC + offa, 0, 1024),
-                       sdesc_sw128(sHhi + ks * 2048, kOffHlo - kOffHhi, 1024), id_yo, ks > 0);
-      }
-      mma_commit_elect(&bars->yo_full);
-      // K3: S^T += B^T [(dec o x)_hi | (dec o x)_lo]   (A = B as MN-major: M = state index);
-      // the accumulator holds [exp(cum_last) h_in | 0] written by the state warps
-      if (!wait_bar(&bars->xs_ready, t & 1, abort, a.hdr, 10)) break;
-      tc_fence_after();
-      const uint32_t lbo_x = sXlo - sX;   // distance from the hi block (in place of x) to lo
-#pragma unroll
-      for (int ks = 0; ks < 8; ++ks) {
-        mma_bf16_elect(tmem + kColS, sdesc_sw128(sB + ks * 2048, kBCBytes / 2, 1024),
-                       sdesc_sw128(sX + ks * 2048, lbo_x, 1024), id_k3, 1);
-      }
-      mma_commit_elect(&bars->s_full);
-      if (t + 2 < nt) mma_commit_elect(&bars->empty[s]);
-    }
-    }
-  } else if (warp == 2) {
-    k1_warp(a, info, bars->info_ready, bars->info_empty, abort, b, h, tbase, nt, lane);
-  } else {
-    // ------------------------------------------------------------------ math warps (3-10)
-    const int q = warp & 3;                 // TMEM lane quarter == SM sub-partition
-    const bool mask_role = warp < 7;        // warps 3-6: mask warps; 7-10: state warps
-    const int i = q * 32 + lane;            // tile row (and state row) owned by this thread
-    const uint32_t lane_addr = static_cast<uint32_t>(q * 32) << 16;
-    const int jlim = (i / R + 1) * R;       // columns j < jlim are at or before row i's step
-    // Mask blocks [cb0, cb1) of tile t for this thread's row, in place; blocks [cb1, zero_end)
-    // are above the diagonal and set to zero.  Waits for the tile's info and CB.
-    auto mask_part = [&](int t, int cb0, int cb1, int zero_end) -> bool {
-      const int slot = t % kInfoSlots;
-      const TileInfo& ti = info[slot];
-      if (!wait_bar(&bars->info_ready[slot], (t / kInfoSlots) & 1, abort, a.hdr, 12)) return false;
-      if (!wait_bar(&bars->cb_full, t & 1, abort, a.hdr, 13)) return false;
-      tc_fence_after();
-      const bool fact_ok = ti.monotone != 0;
-      const float chi = ti.cum_hi[i], clo = ti.cum_lo[i];
-#pragma unroll 1
-      for (int cb = cb0; cb < cb1; ++cb) {
-        float w[32];
-        tmem_ld32(tmem + lane_addr + kColM + cb * 32, w);
-        tmem_ld_wait();
-        reg_tie(w);
-        uint32_t hi[16], lo[16];
-        mask_block(ti, cb, cb == q || !fact_ok, chi, clo, jlim, w, hi, lo);
-        tmem_st16u(tmem + lane_addr + kColM + cb * 32, hi);
-        tmem_st16u(tmem + lane_addr + kColM + cb * 32 + 16, lo);
-      }
-      if (cb1 < zero_end) {
-        uint32_t z[16];
-#pragma unroll
-        for (int k = 0; k < 16; ++k) z[k] = 0u;
-#pragma unroll 1
-        for (int cb = cb1; cb < zero_end; ++cb) {
-          tmem_st16u(tmem + lane_addr + kColM + cb * 32, z);
-          tmem_st16u(tmem + lane_addr + kColM + cb * 32 + 16, z);
-        }
-      }
-      tmem_st_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->m_ready);
-      return true;
-    };
-    if (mask_role) {
-      // ---------------------------------------------------------------- mask warps
-      // mask blocks max(q-1, 0) .. q (the diagonal block is exact), zero blocks q+1 .. 3
-      const int cb0 = q >= 1 ? q - 1 : 0;
-      const int ub = xs_unit_begin(q), ue = xs_unit_end(q);
-      // (dec o x) of tile t, split: hi in place of x (after Yd_t has read x), lo in its own
-      // buffer (in the pre-pass, the unused C stage of the tile); this warp's units of 32 rows
-      // x 16 columns
-      auto scale_x = [&](int t) -> bool {
-        const TileInfo& ti = info[t % kInfoSlots];
-        if (kPre) {
-          if (!wait_bar(&bars->info_ready[t % kInfoSlots], (t / kInfoSlots) & 1, abort, a.hdr, 18))
-            return false;
-          if (!wait_bar(&bars->full[t & 1], (t >> 1) & 1, abort, a.hdr, 19)) return false;
-          // K3 of the previous tile first: without it these warps could complete two phases of
-          // xs_ready (tiles t-1 and t, both of whose loads are issued up front) before the MMA
-          // warp tests the first, and a parity wait cannot tell those phases apart
-          if (t >= 1 && !wait_bar(&bars->s_full, (t - 1) & 1, abort, a.hdr, 22)) return false;
-        } else if (!wait_bar(&bars->yd_full, t & 1, abort, a.hdr, 14)) {
-          return false;
-        }
-        uint8_t* xs = smem + kOffX + (t & 1) * kXBytes;
-        uint8_t* xlo = kPre ? smem + kOffC + (t & 1) * kXBytes : smem + kOffXlo;
-#pragma unroll 1
-        for (int u = ub; u < ue; ++u) {
-          const int row = (u >> 2) * 32 + lane, c0 = (u & 3) * 16;
-          const float wd =
-              ex2_approx((ti.last_hi - ti.cum_hi[row]) + (ti.last_lo - ti.cum_lo[row]));
-          const float2 w2 = make_float2(wd, wd);
-          const uint32_t o0 = sw128_off16(row, c0), o1 = sw128_off16(row, c0 + 8);
-          const uint4 v0 = *reinterpret_cast<const uint4*>(xs + o0);
-          const uint4 v1 = *reinterpret_cast<const uint4*>(xs + o1);
-          uint4 h0, l0, h1, l1;
-          split2(mul2(unpack_bf16(v0.x), w2), h0.x, l0.x);
-          split2(mul2(unpack_bf16(v0.y), w2), h0.y, l0.y);
-          split2(mul2(unpack_bf16(v0.z), w2), h0.z, l0.z);
-          split2(mul2(unpack_bf16(v0.w), w2), h0.w, l0.w);
-          split2(mul2(unpack_bf16(v1.x), w2), h1.x, l1.x);
-          split2(mul2(unpack_bf16(v1.y), w2), h1.y, l1.y);
-          split2(mul2(unpack_bf16(v1.z), w2), h1.z, l1.z);
-          split2(mul2(unpack_bf16(v1.w), w2), h1.w, l1.w);
-          *reinterpret_cast<uint4*>(xs + o0) = h0;
-          *reinterpret_cast<uint4*>(xs + o1) = h1;
-          *reinterpret_cast<uint4*>(xlo + o0) = l0;
-          *reinterpret_cast<uint4*>(xlo + o1) = l1;
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars->xs_ready);
-        return true;
-      };
-      // one loop with one call site per phase (t = -1 only masks tile 0)
-      for (int t = kPre ? 0 : -1; t < nt; ++t) {
-        if (t >= 0 && !scale_x(t)) break;
-        if (!kPre && t + 1 < nt && !mask_part(t + 1, cb0, q + 1, 4)) break;
-      }
-    } else {
-      // ---------------------------------------------------------------- state warps
-      // state row n = i: h_in split into [h_hi | h_lo] for Yo, exp(cum_last) h_in preloaded
-      // into the K3 accumulator (lo half zeroed); output rows i of every tile.
-      const size_t st_base = (size_t)seq * kP * kN;
-      const size_t seg_base = ((size_t)seq * a.nseg + seg) * kP * kN;
-      // initial state: the call's for segment 0; the carried one for later segments of the
-      // full pass; zero for later segments of the pre-pass
-      const float* init0 = seg == 0 ? (a.init ? a.init + st_base : nullptr)
-                                    : (kPre ? nullptr : a.seg_init + seg_base);
-      float seg_decay = 1.f;   // pre-pass: product of the tiles' exp(cum_last)
-      uint8_t* hbhi = smem + kOffHhi;
-      uint8_t* hblo = smem + kOffHlo;
-      // writes h (32 values of columns [c0, c0+32) of state row i) to the Yo operand and the
-      // decayed copy e*h into the K3 accumulator
-      auto put_state = [&](int c0, const float (&hv)[32], float e) {
-        float eh[32];
-#pragma unroll
-        for (int k = 0; k < 32; k += 8) {
-          if (kPre) break;   // the pre-pass has no Yo
-          uint4 uh, ul;
-          split2(make_float2(hv[k], hv[k + 1]), uh.x, ul.x);
-          split2(make_float2(hv[k + 2], hv[k + 3]), uh.y, ul.y);
-          split2(make_float2(hv[k + 4], hv[k + 5]), uh.z, ul.z);
-          split2(make_float2(hv[k + 6], hv[k + 7]), uh.w, ul.w);
-          const uint32_t off = sw128_off16(i, c0 + k);
-          *reinterpret_cast<uint4*>(hbhi + off) = uh;
-          *reinterpret_cast<uint4*>(hblo + off) = ul;
-        }
-        const float2 e2 = make_float2(e, e);
-#pragma unroll
-        for (int k = 0; k < 32; k += 2) {
-          const float2 v = mul2(make_float2(hv[k], hv[k + 1]), e2);
-          eh[k] = v.x;
-          eh[k + 1] = v.y;
-        }
-        float z[16];
-#pragma unroll
-        for (int k = 0; k < 16; ++k) z[k] = 0.f;
-        float e0[16], e1[16];
-#pragma unroll
-        for (int k = 0; k < 16; ++k) {
-          e0[k] = eh[k];
-          e1[k] = eh[16 + k];
-        }
-        tmem_st16(tmem + lane_addr + kColS + c0, e0);
-        tmem_st16(tmem + lane_addr + kColS + c0 + 16, e1);
-        tmem_st16(tmem + lane_addr + kColS + 64 + c0, z);
-        tmem_st16(tmem + lane_addr + kColS + 64 + c0 + 16, z);
-      };
-      auto publish_state = [&]() {
-        tmem_st_wait();
-        fence_proxy_async_smem();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars->hb_full);
-      };
-      bool ok = wait_bar(&bars->info_ready[0], 0, abort, a.hdr, 16);
-      if (ok) {
-        const float e0 = info[0].etile;
-#pragma unroll 1
-        for (int c0 = 0; c0 < kP; c0 += 32) {
-          float hv[32];
-#pragma unroll
-          for (int k = 0; k < 32; ++k)
-            hv[k] = init0 ? init0[(size_t)(c0 + k) * kN + i] : 0.f;
-          put_state(c0, hv, e0);
-        }
-        publish_state();
-      }
-      for (int t = -1; ok && t < nt; ++t) {
-        if (!kPre && q >= 2 && t + 1 < nt && !mask_part(t + 1, 0, q - 1, q - 1)) break;
-        if (t < 0) continue;
-        const int slot = t % kInfoSlots;
-        const TileInfo& ti = info[slot];
-        const bool next = t + 1 < nt;
-        if (kPre) seg_decay *= ti.etile;
-        // output: y = Yd + exp(cum[i/R]) (Yo_hi + Yo_lo)
-        if (!kPre) {
-        if (!wait_bar(&bars->yo_full, t & 1, abort, a.hdr, 21)) break;
-        tc_fence_after();
-        {
-          const float sc = ex2_approx(ti.cum_hi[i] + ti.cum_lo[i]);   // exp(cum_i)
-          const float2 sc2 = make_float2(sc, sc);
-          __nv_bfloat16* yrow = a.y + ((size_t)(row_base + t * kTileRows + i) * a.H + h) * kP;
-          const bool real = seg_row + t * kTileRows + i < a.T * R;   // else a padding row
-          const uint32_t yd = tmem + lane_addr + kColYd + (t & 1) * 64;
-#pragma unroll 1
-          for (int c = 0; c < kP; c += 32) {
-            float vd[32], vh[32], vl[32];
-            tmem_ld32(yd + c, vd);
-            tmem_ld32(tmem + lane_addr + kColYo + c, vh);
-            tmem_ld32(tmem + lane_addr + kColYo + 64 + c, vl);
-            tmem_ld_wait();
-            reg_tie(vd);
-            reg_tie(vh);
-            reg_tie(vl);
-            uint32_t pk[16];
-#pragma unroll
-            for (int k = 0; k < 16; ++k) {
-              const float2 o = fma2(sc2, add2(make_float2(vh[2 * k], vh[2 * k + 1]),
-                                              make_float2(vl[2 * k], vl[2 * k + 1])),
-                                    make_float2(vd[2 * k], vd[2 * k + 1]));
-              pk[k] = pack_bf16(o.x, o.y);
-            }
-            if (!real) continue;
-            uint4* dst = reinterpret_cast<uint4*>(yrow + c);
-            dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-            dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
-            dst[2] = make_uint4(pk[8], pk[9], pk[10], pk[11]);
-            dst[3] = make_uint4(pk[12], pk[13], pk[14], pk[15]);
-          }
-        }
-        }
-        // K4: h_in(t+1) = S_hi + S_lo (the accumulator already holds the decayed h_in(t))
-        if (!wait_bar(&bars->s_full, t & 1, abort, a.hdr, 20)) break;
-        float enext = 0.f;
-        if (next) {
-          const int ns = (t + 1) % kInfoSlots;
-          if (!wait_bar(&bars->info_ready[ns], ((t + 1) / kInfoSlots) & 1, abort, a.hdr, 17))
-            break;
-          enext = info[ns].etile;
-        }
-        tc_fence_after();
-#pragma unroll 1
-        for (int c0 = 0; c0 < kP; c0 += 32) {
-          float sh[32], sl[32];
-          tmem_ld32(tmem + lane_addr + kColS + c0, sh);
-          tmem_ld32(tmem + lane_addr + kColS + 64 + c0, sl);
-          tmem_ld_wait();
-          reg_tie(sh);
-          reg_tie(sl);
-          float hv[32];
-#pragma unroll
-          for (int k = 0; k < 32; k += 2) {
-            const float2 v = add2(make_float2(sh[k], sh[k + 1]), make_float2(sl[k], sl[k + 1]));
-            hv[k] = v.x;
-            hv[k + 1] = v.y;
-          }
-          if (next) {
-            put_state(c0, hv, enext);
-          } else if (kPre) {   // the segment's end state for the carry pass
-#pragma unroll
-            for (int k = 0; k < 32; ++k) a.seg_end[seg_base + (size_t)(c0 + k) * kN + i] = hv[k];
-          } else if (a.final_state && seg == a.nseg - 1) {
-#pragma unroll
-            for (int k = 0; k < 32; ++k) a.final_state[st_base + (size_t)(c0 + k) * kN + i] = hv[k];
-          }
-        }
-        if (next) publish_state();
-        if (kPre && !next && warp == 7 && lane == 0) a.seg_decay[(size_t)seq * a.nseg + seg] = seg_decay;
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars->info_empty[slot]);   // last use of this tile's info
-      }
-    }
-  }
-
-  tc_fence_before();
-  __syncthreads();
-  if (warp == 1) {
-    tc_fence_after();
-    tmem_dealloc(tmem, kTmemCols);
-  }
-}
-
-namespace full {
-
 // ============================================================================================
 // Full forward pass (one CTA per (batch, head) sequence or time segment of one).
 //
@@ -773,6 +267,12 @@ namespace full {
 //   out warps    e^{cum_i} Yo_t into the Yd accumulator; C_{t+1} from its shared-memory tile
 //                into TMEM; y_t -> bf16 -> the tile's x slot -> TMA store
 // The state recurrence never passes through the tensor core (K3 starts from zero).
+//
+// kPre = true is the state-only pre-pass of a sequence cut into time segments: per tile only
+// K1, (dec o x), K3 and the state step (no C, CB, mask, Yo, Yd or y).  Segment s (of the first
+// nseg - 1) runs from the true initial state when s = 0 and from zero otherwise, and writes its
+// end state and its decay product exp(sum dA); fused_seg_carry_kernel turns those into every
+// segment's true initial state for the full pass.
 // ============================================================================================
 
 constexpr int kThreads = 512;
@@ -850,8 +350,9 @@ __device__ __forceinline__ int2 dx_units(int warp) {
 }
 constexpr int kDxWarps = 4;
 
+template <bool kPre>
 __global__ void __launch_bounds__(kThreads, 1)
-    ssd_fused_full_kernel(FusedArgs a, const __grid_constant__ CUtensorMap tm_x,
+    ssd_fused_bf16_kernel(FusedArgs a, const __grid_constant__ CUtensorMap tm_x,
                           const __grid_constant__ CUtensorMap tm_b,
                           const __grid_constant__ CUtensorMap tm_c,
                           const __grid_constant__ CUtensorMap tm_y) {
@@ -868,8 +369,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = __shfl_sync(0xffffffffu, static_cast<int>(threadIdx.x / 32), 0);
   const int lane = threadIdx.x % 32;
-  const int seq = blockIdx.x / a.nseg;   // (b, h)
-  const int seg = blockIdx.x % a.nseg;
+  const int nrun = kPre ? a.nseg - 1 : a.nseg;   // segments this launch runs per sequence
+  const int seq = blockIdx.x / nrun;             // (b, h)
+  const int seg = blockIdx.x % nrun;
   const int b = seq / a.H, h = seq % a.H;
   const int g = h / (a.H / a.G);
   const int R = a.R;
@@ -883,7 +385,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     s_keep_tmem = 0;
     for (int s = 0; s < kXSlots; ++s) {
       mbar_init(&bars->x_full[s], 1);
-      mbar_init(&bars->x_empty[s], 4);     // out warps, once their y store has read the slot
+      // out warps once their y store has read the slot (the pre-pass: the (dec o x) warps)
+      mbar_init(&bars->x_empty[s], kPre ? kDxWarps : 4);
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&bars->b_full[s], 1);
@@ -896,7 +399,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars->cb_go, 4);            // out warps: C row in TMEM and B of the tile landed
     for (int k = 0; k < kInfoSlots; ++k) {
       mbar_init(&bars->info_ready[k], 1);
-      mbar_init(&bars->info_empty[k], 8);  // out and state warps
+      mbar_init(&bars->info_empty[k], kPre ? 4 : 8);   // state warps (and out warps)
     }
     mbar_init(&bars->yd_full, 1);
     mbar_init(&bars->yo_full, 1);
@@ -929,11 +432,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     int nc = 0, nb = 0, nx = 0;   // tiles whose C, B, x loads were issued
     for (int t = 0; t < nt; ++t) {
       const int row = seg_row + t * kTileRows;   // rows past the sequence's end read as zeros
-      if (t >= 1 && !wait_bar(&bars->c_empty, (t - 1) & 1, abort, a.hdr, 31)) break;
-      mbar_arrive_expect_tx_elect(&bars->c_full, kBCBytes);
-      tma_load_4d_elect(smem + kOffC, &tm_c, &bars->c_full, 0, g, row, b);
-      tma_load_4d_elect(smem + kOffC + kBCBytes / 2, &tm_c, &bars->c_full, 64, g, row, b);
-      nc = t + 1;
+      if (!kPre) {   // the pre-pass needs no C
+        if (t >= 1 && !wait_bar(&bars->c_empty, (t - 1) & 1, abort, a.hdr, 31)) break;
+        mbar_arrive_expect_tx_elect(&bars->c_full, kBCBytes);
+        tma_load_4d_elect(smem + kOffC, &tm_c, &bars->c_full, 0, g, row, b);
+        tma_load_4d_elect(smem + kOffC + kBCBytes / 2, &tm_c, &bars->c_full, 64, g, row, b);
+        nc = t + 1;
+      }
       const int sb = t & 1;
       if (t >= 2 && !wait_bar(&bars->b_empty[sb], ((t - 2) >> 1) & 1, abort, a.hdr, 32)) break;
       mbar_arrive_expect_tx_elect(&bars->b_full[sb], kBCBytes);
@@ -953,8 +458,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_prefetch_l2_4d_elect(&tm_x, 0, h, r3, b);
         tma_prefetch_l2_4d_elect(&tm_b, 0, g, r3, b);
         tma_prefetch_l2_4d_elect(&tm_b, 64, g, r3, b);
-        tma_prefetch_l2_4d_elect(&tm_c, 0, g, r3, b);
-        tma_prefetch_l2_4d_elect(&tm_c, 64, g, r3, b);
+        if (!kPre) {
+          tma_prefetch_l2_4d_elect(&tm_c, 0, g, r3, b);
+          tma_prefetch_l2_4d_elect(&tm_c, 64, g, r3, b);
+        }
       }
     }
     // Drain: no TMA load may still be writing this CTA's shared memory when it exits.  In a
@@ -1002,6 +509,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                   id_cb, ks > 0);
       mma_commit_elect(&bars->cb_full[t & 1]);
     };
+    if constexpr (kPre) {
+      // K3 only; B_t is waited for here (in the full pass the out warps wait for it)
+      for (int t = 0; t < nt; ++t) {
+        const int sb = t & 1;
+        if (!gate(0, &bars->b_full[sb], (t >> 1) & 1, 34)) break;
+        if (!gate(0, &bars->k3_go, t & 1, 38)) break;
+        tc_fence_after();
+        const uint32_t al = bmlo0 + sb * (kBCBytes >> 4);
+#pragma unroll
+        for (int ks = 0; ks < 16; ++ks)
+          mma_ss_we(tmem + kColS, al + (ks & 7) * (2048 >> 4), dhi,
+                    dxlo + (((ks < 8 ? 0u : kOffDxLo - kOffDxHi) + (ks & 7) * 2048) >> 4), dhi,
+                    id_k3, ks > 0);
+        mma_commit_elect(&bars->s_full);
+        mma_commit_elect(&bars->b_empty[sb]);
+      }
+    } else {
     uint32_t p_yo = mbar_test_wait(&bars->yo_go, 0);
     bool ok = gate(0, &bars->cb_go, 0, 35);
     if (ok) {
@@ -1058,6 +582,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       mma_commit_elect(&bars->yd_full);
+    }
     }
     // Drain: every MMA issued has completed before TMEM is freed.
     mma_commit_elect(&bars->drain);
@@ -1157,6 +682,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       for (int t = 0; t < nt; ++t) {
         if (has_dx && !dec_x(t)) break;
+        if (kPre) {
+          // x_t has no other reader in the pre-pass
+          if (has_dx && lane == 0) mbar_arrive(&bars->x_empty[t % kXSlots]);
+          continue;
+        }
         if (!mask_part(t)) break;
       }
     } else if (warp < 12) {
@@ -1164,7 +694,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       // Thread = state row n = i; h^T[n][0..63] in registers across the whole sequence.
       const size_t st_base = (size_t)seq * kP * kN;
       const size_t seg_base = ((size_t)seq * a.nseg + seg) * kP * kN;
-      const float* init0 = seg == 0 ? (a.init ? a.init + st_base : nullptr) : a.seg_init + seg_base;
+      // initial state: the call's for segment 0; the carried one for later segments of the full
+      // pass; zero for later segments of the pre-pass
+      const float* init0 = seg == 0 ? (a.init ? a.init + st_base : nullptr)
+                                    : (kPre ? nullptr : a.seg_init + seg_base);
+      float seg_decay = 1.f;   // pre-pass: product of the tiles' exp(cum_last)
       float hv[kP];
 #pragma unroll
       for (int p = 0; p < kP; ++p) hv[p] = init0 ? init0[(size_t)p * kN + i] : 0.f;
@@ -1178,6 +712,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           const float e = info[slot].etile;
           const float2 e2 = make_float2(e, e);
+          seg_decay *= e;
 #pragma unroll
           for (int c = 0; c < kP; c += 32) {
             float sv[32];
@@ -1199,8 +734,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_arrive(&bars->info_empty[slot]);
           }
           if (t + 1 == nt) break;
+          if (kPre) continue;   // the pre-pass has no Yo
           // Yo_t has read h_t from the operand buffer (it was issued before K3_t)
           if (!wait_bar(&bars->yo_full, t & 1, abort, a.hdr, 50)) break;
+        } else if (kPre) {
+          continue;
         }
         // h^T row n as bf16 hi and lo rows of the Yo operand
         uint8_t* hhi = smem + kOffHHi;
@@ -1220,119 +758,127 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars->yo_go);
       }
-      if (a.final_state && seg == a.nseg - 1 && !*abort) {
+      if (kPre) {   // the segment's end state and decay for the carry pass
+        if (!*abort) {
+#pragma unroll
+          for (int p = 0; p < kP; ++p) a.seg_end[seg_base + (size_t)p * kN + i] = hv[p];
+          if (warp == 8 && lane == 0) a.seg_decay[(size_t)seq * a.nseg + seg] = seg_decay;
+        }
+      } else if (a.final_state && seg == a.nseg - 1 && !*abort) {
 #pragma unroll
         for (int p = 0; p < kP; ++p) a.final_state[st_base + (size_t)p * kN + i] = hv[p];
       }
     } else {
       // ---------------------------------------------------------------- out warps
-      // Per tile: e^{cum_i} Yo_t into the y accumulator; C_{t+1} into TMEM once Yo_t has read
-      // C_t; then y_t = the accumulator after Yd_t -> bf16 -> the tile's x slot -> TMA store.
-      auto copy_c = [&](int t) -> bool {
-        if (!wait_bar(&bars->c_full, t & 1, abort, a.hdr, 51)) return false;
-        const uint8_t* cs = smem + kOffC;
-#pragma unroll
-        for (int blk = 0; blk < 2; ++blk) {
-          uint32_t w[32];
-#pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            const uint4 v = *reinterpret_cast<const uint4*>(cs + blk * (kBCBytes / 2) +
-                                                            sw128_off16(i, c * 8));
-            w[c * 4 + 0] = v.x;
-            w[c * 4 + 1] = v.y;
-            w[c * 4 + 2] = v.z;
-            w[c * 4 + 3] = v.w;
-          }
-          tmem_st32u(tmem + lane_addr + kColC + blk * 32, w);
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars->c_empty);
-        tmem_st_wait();
-        tc_fence_before();
-        // CB_t also needs B_t: the MMA warp waits for both on cb_go
-        if (!wait_bar(&bars->b_full[t & 1], (t >> 1) & 1, abort, a.hdr, 55)) return false;
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars->cb_go);
-        return true;
-      };
-      if (lane == 0) mbar_arrive(&bars->yo_go);   // no Yo to read before tile 0
-      int stored = 0;   // y stores issued by this warp (lane 0)
-      // t = -1 only copies C_0
-      for (int t = -1; t < nt; ++t) {
-        if (t < 0) {
-          if (!copy_c(0)) break;
-          continue;
-        }
-        const int slot = t % kInfoSlots;
-        if (!wait_bar(&bars->info_ready[slot], (t / kInfoSlots) & 1, abort, a.hdr, 54)) break;
-        if (!wait_bar(&bars->yo_full, t & 1, abort, a.hdr, 52)) break;
-        tc_fence_after();
-        const TileInfo& ti = info[slot];
-        {
-          // e^{cum_i} Yo_t into the y accumulator (y_{t-1} was read in the previous iteration)
-          const float sc = ex2_approx(ti.cum_hi[i] + ti.cum_lo[i]);
-          const float2 sc2 = make_float2(sc, sc);
-#pragma unroll
-          for (int c = 0; c < kP; c += 32) {
-            float vo[32];
-            tmem_ld32(tmem + lane_addr + kColYo + c, vo);
-            tmem_ld_wait();
-            reg_tie(vo);
-            uint32_t vu[32];
-#pragma unroll
-            for (int k = 0; k < 32; k += 2) {
-              const float2 v = mul2(sc2, make_float2(vo[k], vo[k + 1]));
-              vu[k] = __float_as_uint(v.x);
-              vu[k + 1] = __float_as_uint(v.y);
+      if constexpr (!kPre) {   // the pre-pass has no output
+        // Per tile: e^{cum_i} Yo_t into the y accumulator; C_{t+1} into TMEM once Yo_t has read
+        // C_t; then y_t = the accumulator after Yd_t -> bf16 -> the tile's x slot -> TMA store.
+        auto copy_c = [&](int t) -> bool {
+          if (!wait_bar(&bars->c_full, t & 1, abort, a.hdr, 51)) return false;
+          const uint8_t* cs = smem + kOffC;
+  #pragma unroll
+          for (int blk = 0; blk < 2; ++blk) {
+            uint32_t w[32];
+  #pragma unroll
+            for (int c = 0; c < 8; ++c) {
+              const uint4 v = *reinterpret_cast<const uint4*>(cs + blk * (kBCBytes / 2) +
+                                                              sw128_off16(i, c * 8));
+              w[c * 4 + 0] = v.x;
+              w[c * 4 + 1] = v.y;
+              w[c * 4 + 2] = v.z;
+              w[c * 4 + 3] = v.w;
             }
-            tmem_st32u(tmem + lane_addr + kColYd + c, vu);
+            tmem_st32u(tmem + lane_addr + kColC + blk * 32, w);
           }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars->c_empty);
           tmem_st_wait();
           tc_fence_before();
+          // CB_t also needs B_t: the MMA warp waits for both on cb_go
+          if (!wait_bar(&bars->b_full[t & 1], (t >> 1) & 1, abort, a.hdr, 55)) return false;
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars->cb_go);
+          return true;
+        };
+        if (lane == 0) mbar_arrive(&bars->yo_go);   // no Yo to read before tile 0
+        int stored = 0;   // y stores issued by this warp (lane 0)
+        // t = -1 only copies C_0
+        for (int t = -1; t < nt; ++t) {
+          if (t < 0) {
+            if (!copy_c(0)) break;
+            continue;
+          }
+          const int slot = t % kInfoSlots;
+          if (!wait_bar(&bars->info_ready[slot], (t / kInfoSlots) & 1, abort, a.hdr, 54)) break;
+          if (!wait_bar(&bars->yo_full, t & 1, abort, a.hdr, 52)) break;
+          tc_fence_after();
+          const TileInfo& ti = info[slot];
+          {
+            // e^{cum_i} Yo_t into the y accumulator (y_{t-1} was read in the previous iteration)
+            const float sc = ex2_approx(ti.cum_hi[i] + ti.cum_lo[i]);
+            const float2 sc2 = make_float2(sc, sc);
+  #pragma unroll
+            for (int c = 0; c < kP; c += 32) {
+              float vo[32];
+              tmem_ld32(tmem + lane_addr + kColYo + c, vo);
+              tmem_ld_wait();
+              reg_tie(vo);
+              uint32_t vu[32];
+  #pragma unroll
+              for (int k = 0; k < 32; k += 2) {
+                const float2 v = mul2(sc2, make_float2(vo[k], vo[k + 1]));
+                vu[k] = __float_as_uint(v.x);
+                vu[k + 1] = __float_as_uint(v.y);
+              }
+              tmem_st32u(tmem + lane_addr + kColYd + c, vu);
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+              mbar_arrive(&bars->y_pre);
+              if (t + 1 < nt) mbar_arrive(&bars->yo_go);   // Yo_t read
+            }
+          }
+          if (t + 1 < nt && !copy_c(t + 1)) break;
+          if (!wait_bar(&bars->yd_full, t & 1, abort, a.hdr, 53)) break;
+          tc_fence_after();
+          uint8_t* ys = smem + kOffX + (t % kXSlots) * kXBytes;   // x_t is no longer needed
+  #pragma unroll
+          for (int c = 0; c < kP; c += 32) {
+            float vy[32];
+            tmem_ld32(tmem + lane_addr + kColYd + c, vy);
+            tmem_ld_wait();
+            reg_tie(vy);
+            uint32_t pk[16];
+  #pragma unroll
+            for (int k = 0; k < 16; ++k) pk[k] = pack_bf16(vy[2 * k], vy[2 * k + 1]);
+  #pragma unroll
+            for (int k = 0; k < 4; ++k)
+              *reinterpret_cast<uint4*>(ys + sw128_off16(i, c + 8 * k)) =
+                  make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
+          }
+          tc_fence_before();
+          fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
-            mbar_arrive(&bars->y_pre);
-            if (t + 1 < nt) mbar_arrive(&bars->yo_go);   // Yo_t read
+            mbar_arrive(&bars->info_empty[slot]);
+            tma_store_4d(&tm_y, ys + q * 4096, 0, h, seg_row + t * kTileRows + q * 32, b);
+            bulk_commit_group();
+            ++stored;
+            // the store of the previous tile has read its slot: hand it back to the producer
+            if (stored >= 2) {
+              bulk_wait_group_read<1>();
+              mbar_arrive(&bars->x_empty[(t - 1) % kXSlots]);
+            }
           }
+          __syncwarp();
         }
-        if (t + 1 < nt && !copy_c(t + 1)) break;
-        if (!wait_bar(&bars->yd_full, t & 1, abort, a.hdr, 53)) break;
-        tc_fence_after();
-        uint8_t* ys = smem + kOffX + (t % kXSlots) * kXBytes;   // x_t is no longer needed
-#pragma unroll
-        for (int c = 0; c < kP; c += 32) {
-          float vy[32];
-          tmem_ld32(tmem + lane_addr + kColYd + c, vy);
-          tmem_ld_wait();
-          reg_tie(vy);
-          uint32_t pk[16];
-#pragma unroll
-          for (int k = 0; k < 16; ++k) pk[k] = pack_bf16(vy[2 * k], vy[2 * k + 1]);
-#pragma unroll
-          for (int k = 0; k < 4; ++k)
-            *reinterpret_cast<uint4*>(ys + sw128_off16(i, c + 8 * k)) =
-                make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
-        }
-        tc_fence_before();
-        fence_proxy_async_smem();
-        __syncwarp();
         if (lane == 0) {
-          mbar_arrive(&bars->info_empty[slot]);
-          tma_store_4d(&tm_y, ys + q * 4096, 0, h, seg_row + t * kTileRows + q * 32, b);
-          bulk_commit_group();
-          ++stored;
-          // the store of the previous tile has read its slot: hand it back to the producer
-          if (stored >= 2) {
-            bulk_wait_group_read<1>();
-            mbar_arrive(&bars->x_empty[(t - 1) % kXSlots]);
-          }
+          bulk_wait_group<0>();   // every y store complete before the CTA exits
         }
         __syncwarp();
       }
-      if (lane == 0) {
-        bulk_wait_group<0>();   // every y store complete before the CTA exits
-      }
-      __syncwarp();
     }
   }
 
@@ -1344,7 +890,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-}  // namespace full
 
 PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -1439,11 +984,11 @@ cudaError_t ensure_smem_attribute() {
   if (e != cudaSuccess) return e;
   const uint64_t bit = dev < 64 ? (1ull << dev) : 0ull;
   if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
-  e = cudaFuncSetAttribute(full::ssd_fused_full_kernel,
-                           cudaFuncAttributeMaxDynamicSharedMemorySize, full::kSmem);
+  e = cudaFuncSetAttribute(ssd_fused_bf16_kernel<false>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(ssd_fused_bf16_kernel<true>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
   if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_acq_rel);
   return e;
 }
@@ -1535,15 +1080,15 @@ cudaError_t fused_bf16_forward(const GenericParams& p, cudaStream_t st) {
   if (e != cudaSuccess) return e;
   const unsigned seqs = (unsigned)(p.batch * p.H);
   if (a.nseg > 1) {
-    ssd_fused_bf16_kernel<true><<<seqs * (a.nseg - 1), kThreadsFused, kSmemAlloc, st>>>(
-        a, m->mx, m->mb, m->mc);
+    ssd_fused_bf16_kernel<true><<<seqs * (a.nseg - 1), kThreads, kSmem, st>>>(
+        a, m->mx, m->mb, m->mc, m->my);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     const int64_t elems = (int64_t)seqs * kP * kN;
     fused_seg_carry_kernel<<<(unsigned)((elems + 255) / 256), 256, 0, st>>>(a, elems);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
-  full::ssd_fused_full_kernel<<<seqs * a.nseg, full::kThreads, full::kSmem, st>>>(
-      a, m->mx, m->mb, m->mc, m->my);
+  ssd_fused_bf16_kernel<false><<<seqs * a.nseg, kThreads, kSmem, st>>>(a, m->mx, m->mb, m->mc,
+                                                                        m->my);
   return cudaGetLastError();
 }
 

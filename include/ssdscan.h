@@ -250,15 +250,20 @@ ssd_status selective_scan_forward(const float* u, const float* delta, const floa
  * Allocation-free variant of selective_scan_forward.  The pages have no counterpart: this entry
  * point exists for callers that cannot allocate device memory (for example code that receives
  * only its input and output buffers through a fixed plugin interface, or code on a path where
- * cudaMalloc and the device synchronisation it can imply are not allowed).  It computes exactly
- * what selective_scan_forward computes, with the same kernels, but takes no workspace: its
- * scratch lives in one fixed device array of SSD_NOALLOC_SCRATCH_BYTES (16 MiB) inside this
- * library, which every GPU that loads the library holds until the process exits.
+ * cudaMalloc and the device synchronisation it can imply are not allowed).  It computes the same
+ * function as selective_scan_forward but always on the segmented three-kernel path (per-segment
+ * states, a carry pass, the output pass), whereas selective_scan_forward takes a one-pass kernel
+ * for d_state in {8, 16, 32, 64} with d_model % 4 == 0; the two agree within the fp32 parity
+ * bound |got - ref| <= 1e-4 (1 + |ref|), not bit for bit.  It takes no workspace: its scratch
+ * lives in one fixed device array of SSD_NOALLOC_SCRATCH_BYTES (16 MiB) inside this library,
+ * which every GPU that loads the library holds until the process exits.
  *   - Limit: (d_state + 1) * batch * ceil(seqlen / 64) * d_model floats must fit the array
  *     (the 4 x 4096 x 512 x 16 workload uses 8.9 MB); larger sizes return SSD_ERR_UNSUPPORTED
  *     before any launch.  Other argument errors are reported as in selective_scan_forward.
  *   - The first call on each device looks up the array's device address (cudaGetSymbolAddress)
- *     with that device current; make that first call before any stream capture.
+ *     with that device current, and the library keeps that address for the rest of the process;
+ *     make that first call before any stream capture, and do not use this entry point after a
+ *     cudaDeviceReset of that device (the kept address would belong to the destroyed context).
  *   - All calls on a device share the one array and it keeps the last call's contents.  Nothing
  *     in it has to start at zero (every call writes its scratch before reading it), but calls
  *     that can overlap on the GPU (different streams, or concurrent host threads) race on it and

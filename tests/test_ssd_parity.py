@@ -50,6 +50,26 @@ def test_full_size_sampled_heads(cfg):
         check_close(fin[b:b + 1, h:h + 1], fr, TOL[cfg.dtype], f"{cfg.name} final[b={b},h={h}]")
 
 
+def test_full_size_slow_decay_carries_state_across_all_tiles():
+    """The Mamba-2-shape workload at full size with slow decay and an initial state, in the one-
+    launch configuration the benchmark times (128 sequences on one SM each: every sequence's
+    state crosses all 32 tiles on chip).  Under the stated decay the carry between tiles is
+    ~e^-127 and invisible; here it dominates y.  Sampled (batch, head) problems, every output."""
+    cfg = wl.MAMBA2_SISO_BF16
+    shape = pkg.make_shape(cfg.batch, cfg.seqlen, cfg.nheads, cfg.headdim, cfg.dstate, cfg.ngroups,
+                           cfg.mimo_rank, cfg.chunk_len, cfg.dtype, cfg.theta)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    if cfg.batch * cfg.nheads * 2 > sms:   # the bench's configuration on this GPU: no segments
+        assert pkg.ssd_chunked_launches(shape) == 1
+    inp = wl.make_ssd_inputs(cfg, seed=0, slow_decay=True, init_state=True)
+    y, fin = gpu_ssd(inp, cfg.chunk_len)
+    for (b, h) in [(0, 0), (1, 9), (2, 22), (3, 31)]:
+        sub = slice_heads(inp, cfg, b, h)
+        yr, fr = oracle_ssd(sub)
+        check_close(y[b:b + 1, :, :, h:h + 1], yr, TOL[cfg.dtype], f"slow decay y[b={b},h={h}]")
+        check_close(fin[b:b + 1, h:h + 1], fr, TOL[cfg.dtype], f"slow decay final[b={b},h={h}]")
+
+
 EDGE = [
     # single chunk, one head, tiny dims
     wl.SSDConfig("one_chunk_f32", 1, 64, 1, 8, 8, 64, 1, 1, "f32"),

@@ -3,9 +3,10 @@
 ``selective_scan_forward_noalloc`` serves callers that cannot allocate device memory (for example
 code that receives only its input and output buffers through a fixed plugin interface): instead
 of a caller workspace it uses one fixed scratch array inside the library.  Called through the C
-ABI, it must give the same result as ``selective_scan_forward`` (the workspace entry point), on
-two calls in a row with different inputs, so that contents left in the shared array by one call
-cannot leak into the next.
+ABI, it must agree with ``selective_scan_forward`` (the workspace entry point) and with the fp64
+oracle, on calls in a row with different inputs.  The second call repeats the first call's sizes
+with other seeds, so the whole scratch region the first call filled is read again: any contents
+leaking from one call into the next would show.
 
 This file is named so that pytest collects it last.
 """
@@ -15,6 +16,7 @@ import pytest
 import torch
 
 import chunked_ssd_scan_gb300 as pkg
+import oracle
 from chunked_ssd_scan_gb300 import workloads as wl
 from tests.parity_util import check_close, to_np
 
@@ -36,10 +38,12 @@ def _p(t):
     return _VP(None) if t is None else _VP(t.data_ptr())
 
 
-def test_noalloc_matches_workspace_entry_point_on_two_calls():
+def test_noalloc_matches_workspace_entry_point_and_oracle_on_calls_in_a_row():
     f = _fn()
     stream = _VP(torch.cuda.current_stream().cuda_stream)
-    cases = [(wl.SELECTIVE_SCAN_F32, 0), (wl.SelectiveScanConfig("second", 2, 1000, 96, 7), 1)]
+    small = wl.SelectiveScanConfig("second", 2, 1000, 96, 7)
+    # the full workload twice (other seeds the second time), then a smaller odd shape
+    cases = [(wl.SELECTIVE_SCAN_F32, 0), (wl.SELECTIVE_SCAN_F32, 3), (small, 1)]
     for cfg, seed in cases:
         s = wl.make_selective_scan_inputs(cfg, seed=seed, device="cuda")
         ref = pkg.selective_scan_forward(s["u"], s["delta"], s["A"], s["B"], s["C"], s["skip"])
@@ -48,7 +52,10 @@ def test_noalloc_matches_workspace_entry_point_on_two_calls():
                _p(y), cfg.batch, cfg.seqlen, cfg.d_model, cfg.d_state, stream)
         assert st == 0, pkg.STATUS.get(st, st)
         torch.cuda.synchronize()
-        check_close(to_np(y), to_np(ref), TOL, f"noalloc vs workspace entry point ({cfg.name})")
+        what = f"{cfg.name}, seed {seed}"
+        check_close(to_np(y), to_np(ref), TOL, f"noalloc vs workspace entry point ({what})")
+        yo = oracle.selective_scan(*(to_np(s[k]) for k in ("u", "delta", "A", "B", "C", "skip")))
+        check_close(to_np(y), yo, TOL, f"noalloc vs oracle ({what})")
 
 
 def test_noalloc_rejects_sizes_beyond_its_scratch():
