@@ -32,6 +32,13 @@ METRIC = "SSD forward tokens/s and % of roofline (HBM GB/s / tensor-pipe) at 1 G
 L2_FLUSH_BYTES = 256 << 20
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
+# Dense tf32 tensor-core throughput of this GPU, measured the way the bf16 figure of
+# MEASURED_PEAKS.json is: torch.matmul of two 8192 x 8192 fp32 matrices with TF32 allowed, best
+# of 10 timed with CUDA events, 2 N^3 FLOP (`python bench.py --measure-peak tf32`;
+# profiles/peaks_tf32.md).  The roofline of an fp32-input workload takes its contraction FLOPs at
+# this rate.
+MEASURED_TF32_TFLOPS = 1043.5
+FALLBACK_TF32_TFLOPS = 1100.0   # nominal dense tf32, used only while no measurement is recorded
 # fp32 FMA peak of the CUDA cores: 152 SMs x 128 lanes x 2 FLOP x 2.07 GHz (maximum SM clock).
 ALU_FP32_TFLOPS = round(152 * 128 * 2 * 2.07e9 / 1e12, 1)
 
@@ -70,6 +77,8 @@ def parse_args():
     # smaller cases of a workload's shape, for profiler captures (not bench lines)
     ap.add_argument("--batch", type=int, default=0, help="override the workload's batch")
     ap.add_argument("--seqlen", type=int, default=0, help="override the workload's seqlen")
+    ap.add_argument("--measure-peak", choices=["tf32"], default=None,
+                    help="measure a tensor-core peak (torch.matmul) and print it instead")
     return ap.parse_args()
 
 
@@ -88,6 +97,35 @@ def measured_peaks():
         return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
     except Exception:
         return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
+
+
+def tf32_peak():
+    if MEASURED_TF32_TFLOPS:
+        return MEASURED_TF32_TFLOPS, "measured (torch.matmul 8192^3, TF32 allowed, best of 10)"
+    return FALLBACK_TF32_TFLOPS, "nominal (no measurement recorded)"
+
+
+def measure_matmul_peak(kind: str):
+    """Dense tensor-core throughput as torch.matmul of two 8192 x 8192 matrices achieves it:
+    best of 10 launches timed with CUDA events, 2 N^3 FLOP each (the method of the bf16 figure
+    in MEASURED_PEAKS.json)."""
+    n = 8192
+    torch.backends.cuda.matmul.allow_tf32 = kind == "tf32"
+    a = torch.randn(n, n, device="cuda", dtype=torch.float32)
+    b = torch.randn(n, n, device="cuda", dtype=torch.float32)
+    for _ in range(3):
+        torch.matmul(a, b)
+    best = float("inf")
+    for _ in range(10):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        torch.matmul(a, b)
+        e1.record()
+        torch.cuda.synchronize()
+        best = min(best, e0.elapsed_time(e1))
+    return {"peak": kind, "tflops": round(2 * n ** 3 / (best * 1e-3) / 1e12, 1), "ms": round(best, 4),
+            "how": "torch.matmul fp32 8192^3 with allow_tf32, best of 10, CUDA events",
+            "gpu": torch.cuda.get_device_name(0)}
 
 
 def workload(name, batch=0, seqlen=0):
@@ -375,50 +413,17 @@ def run_ours(args, rank, world, local):
     hbm, tf, peak_src = measured_peaks()
     # the capture's bytes belong to the workload's own shape, not to an overridden one
     traffic = None if (args.batch or args.seqlen) else NCU_TRAFFIC_BYTES.get(cfg.name)
-    achieved = io_bytes / (ms * 1e-3) / 1e9
-    roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
-            "frac": round(achieved / hbm, 4), "traffic": traffic,
-            "peak_source": peak_src,
-            "kernel": ("selective_scan_forward" if is_ss
-                       else "ssd_chunked_backward" if variant == "backward"
-                       else "ssd_trapezoidal_forward" if variant == "trapezoidal"
-                       else "ssd_rotation_variant_forward" if variant == "rotation_variant"
-                       else f"ssd_chunked_forward[{variant}]"),
-            "algorithmic_bytes_per_launch": io_bytes}
-    if variant == "backward":
-        # fp32 FMA work on CUDA cores: the bound is the SMs' fp32 lanes at the maximum clock
-        alu = ALU_FP32_TFLOPS
-        a_tf = flops / (ms * 1e-3) / 1e12
-        roof = {"bound": "alu", "achieved": round(a_tf, 2), "peak": alu, "unit": "TFLOP/s",
-                "frac": round(a_tf / alu, 4), "traffic": traffic,
-                "peak_source": "derived: 152 SMs x 128 fp32 lanes x 2 FLOP x 2.07 GHz",
-                "kernel": ("ssd_trapezoidal_backward" if cfg.trapezoidal
-                           else "ssd_chunked_backward"),
-                "algorithmic_flops_per_launch": flops,
-                "algorithmic_bytes_per_launch": io_bytes,
-                "hbm_gbs": round(io_bytes / (ms * 1e-3) / 1e9, 1),
-                "hbm_frac": round(io_bytes / (ms * 1e-3) / 1e9 / hbm, 4)}
-    elif flops and variant != "tc_bf16":
-        # fp32 paths run their contractions as fp32 FMAs on the CUDA cores (no tensor cores:
-        # the fp32 accumulator of the tensor core truncates); the tighter of the HBM and the
-        # fp32-lane bound is the roofline
-        alu = ALU_FP32_TFLOPS
-        t_hbm, t_alu = io_bytes / (hbm * 1e9), flops / (alu * 1e12)
-        a_tf = flops / (ms * 1e-3) / 1e12
-        roof["alu_tflops"] = round(a_tf, 2)
-        roof["alu_frac"] = round(a_tf / alu, 4)
-        if t_alu > t_hbm:
-            roof.update({"bound": "alu", "achieved": round(a_tf, 2), "peak": alu,
-                         "unit": "TFLOP/s", "frac": round(a_tf / alu, 4),
-                         "peak_source": "derived: 152 SMs x 128 fp32 lanes x 2 FLOP x 2.07 GHz",
-                         "algorithmic_flops_per_launch": flops,
-                         "hbm_gbs": round(achieved, 1), "hbm_frac": round(achieved / hbm, 4)})
-        roof["roofline_frac"] = round(max(t_hbm, t_alu) / (ms * 1e-3), 4)
-    elif flops:
-        roof["tensor_tflops"] = round(flops / (ms * 1e-3) / 1e12, 2)
-        roof["tensor_frac_of_bf16_peak"] = round(flops / (ms * 1e-3) / 1e12 / tf, 4)
-        t_roof = max(io_bytes / (hbm * 1e9), flops / (tf * 1e12))
-        roof["roofline_frac"] = round(t_roof / (ms * 1e-3), 4)
+    kernel = ("selective_scan_forward" if is_ss
+              else ("ssd_trapezoidal_backward" if cfg.trapezoidal else "ssd_chunked_backward")
+              if variant == "backward"
+              else "ssd_trapezoidal_forward" if variant == "trapezoidal"
+              else "ssd_rotation_variant_forward" if variant == "rotation_variant"
+              else f"ssd_chunked_forward[{variant}]")
+    roof = roofline(io_bytes, flops, ms * 1e-3, hbm, tf, peak_src, bf16_inputs=dtype == "bf16",
+                    tensor_path=variant == "tc_bf16")
+    roof.update({"traffic": traffic, "kernel": kernel, "algorithmic_bytes_per_launch": io_bytes})
+    if flops:
+        roof["algorithmic_flops_per_launch"] = flops
 
     out = {
         "metric": metric_name(cfg, is_ss),
@@ -453,6 +458,41 @@ def run_ours(args, rank, world, local):
         except Exception as ex:  # pragma: no cover
             out["cpu_baseline"] = {"error": repr(ex)}
     return out
+
+
+def roofline(io_bytes, flops, sec, hbm, tf_bf16, peak_src, bf16_inputs, tensor_path):
+    """The roofline of one call: the slower of the algorithmic bytes at the measured HBM
+    bandwidth and the contraction FLOPs at the tensor-core peak (bf16 for bf16 inputs, tf32 for
+    fp32 inputs), over the measured time.  `bound` names the slower one; `frac` is that
+    roofline time over the measured time.  Paths that run their contractions on the CUDA cores
+    (fp32 FMA) also report the fraction of the fp32-lane peak (`alu_frac`), as a second figure."""
+    t_hbm = io_bytes / (hbm * 1e9)
+    if bf16_inputs:
+        tc, tc_src = tf_bf16, f"bf16, {peak_src}"
+    else:
+        tc, tc_src = tf32_peak()
+        tc_src = "tf32, " + tc_src
+    t_tc = flops / (tc * 1e12) if flops else 0.0
+    gbs = io_bytes / sec / 1e9
+    if t_tc > t_hbm:
+        roof = {"bound": "tensor", "achieved": round(flops / sec / 1e12, 2), "peak": tc,
+                "unit": "TFLOP/s", "frac": round(t_tc / sec, 4), "peak_source": tc_src,
+                "hbm_gbs": round(gbs, 1), "hbm_frac": round(t_hbm / sec, 4)}
+    else:
+        roof = {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm, "unit": "GB/s",
+                "frac": round(t_hbm / sec, 4), "peak_source": peak_src}
+    if flops:
+        roof["tensor_peak"] = tc
+        roof["tensor_peak_source"] = tc_src
+        roof["tensor_tflops"] = round(flops / sec / 1e12, 2)
+        roof["tensor_frac"] = round(t_tc / sec, 4)
+        if not tensor_path:
+            a_tf = flops / sec / 1e12
+            roof["alu_tflops"] = round(a_tf, 2)
+            roof["alu_frac"] = round(a_tf / ALU_FP32_TFLOPS, 4)
+            roof["alu_peak_source"] = "derived: 152 SMs x 128 fp32 lanes x 2 FLOP x 2.07 GHz"
+    roof["roofline_frac"] = roof["frac"]
+    return roof
 
 
 def config_dict(cfg, is_ss):
@@ -585,9 +625,12 @@ def e2e_measure(args, cfg, is_ss, host, dev, stream):
         status = pkg.workspace_status(ws, stream)
         if status != ("SSD_OK", 0):
             raise RuntimeError(f"device-side error word after the end-to-end steps: {status}")
+    # the copies run in series with the call on one stream: their effective bandwidth shows how
+    # much of the end-to-end time is the host link rather than the kernels
     return {"value": round(cfg.tokens / (ms * 1e-3), 1), "unit": "tokens/s",
             "ms_per_step": round(ms, 4), "h2d_bytes_per_step": int(h2d),
-            "d2h_bytes_per_step": int(d2h), "steps": n}
+            "d2h_bytes_per_step": int(d2h), "steps": n,
+            "copy_gbs_effective": round((h2d + d2h) / (ms * 1e-3) / 1e9, 1)}
 
 
 def _ssd_sample(cfg, host, heads, batches=1):
@@ -662,6 +705,21 @@ def _time_oracle_ss(cfg, host, nthr, channels):
     return time.perf_counter() - t0
 
 
+def oracle_single_thread(cfg, is_ss, host):
+    """The oracle on one host thread: (tokens/s scaled to the full workload, description)."""
+    if is_ss:
+        ch = min(cfg.d_model, 64)
+        t = _time_oracle_ss(cfg, host, 1, ch)
+        frac = ch / (cfg.d_model * cfg.batch)
+        desc = f"one thread, batch 0, channels 0..{ch - 1}, full T"
+    else:
+        sub1, _ = _ssd_sample(cfg, host, 1)
+        t = _time_oracle_ssd(sub1, 1)
+        frac = 1.0 / (cfg.nheads * cfg.batch)
+        desc = "one thread, the (batch 0, head 0) problem, full T"
+    return round(cfg.tokens * frac / t, 1), desc + f"; {t:.2f} s wall"
+
+
 def oracle_sampler(cfg, is_ss, host, target_s):
     """Returns (step callable -> seconds, sampled fraction of the workload, cores, description):
     the oracle as it stands over whole independent problems of batch 0, sized to ~target_s."""
@@ -701,9 +759,11 @@ def cpu_baseline(cfg, is_ss, host, target_s: float = 12.0):
         total += step()
         reps += 1
     dt = total / reps
+    st_value, st_desc = oracle_single_thread(cfg, is_ss, host)
     return {"value": round(cfg.tokens * frac / dt, 1), "unit": "tokens/s", "cores": cores,
             "kind": "oracle",
-            "sample": desc + f"; {dt:.2f} s wall per repetition, {reps} repetitions"}
+            "sample": desc + f"; {dt:.2f} s wall per repetition, {reps} repetitions",
+            "single_thread_value": st_value, "single_thread_sample": st_desc}
 
 
 def run_reference(args, rank, world):
@@ -739,6 +799,9 @@ def run_reference(args, rank, world):
 
 def main():
     args = parse_args()
+    if args.measure_peak:
+        print(json.dumps(measure_matmul_peak(args.measure_peak)))
+        return
     rank, world, local = dist_env()
     if world > 1 and not torch.distributed.is_initialized():
         backend = "nccl" if torch.cuda.is_available() else "gloo"
