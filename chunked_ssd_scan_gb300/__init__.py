@@ -20,6 +20,7 @@ __all__ = [
     "ssd_chunked_launches", "ssd_chunked_forward", "SSDForwardPlan", "SelectiveScanPlan",
     "selective_scan_workspace_bytes", "selective_scan_forward", "ssd_trapezoidal_workspace_bytes",
     "ssd_trapezoidal_forward", "SSDTrapezoidalPlan", "ssd_rotation_variant_forward",
+    "ssd_quaternion_forward",
     "ssd_backward_workspace_bytes", "ssd_chunked_backward", "SSDBackwardPlan",
     "ssd_trapezoidal_backward", "ssd_trapezoidal_backward_workspace_bytes",
     "workspace_status", "wait_selftest", "STATUS", "VARIANTS",
@@ -76,6 +77,10 @@ def load_library(path: Optional[str] = None):
     lib.ssd_trapezoidal_workspace_bytes.argtypes = [SP]
     lib.ssd_trapezoidal_forward.restype = ctypes.c_int
     lib.ssd_trapezoidal_forward.argtypes = [SP] + [_VP] * 13 + [ctypes.c_size_t, _VP]
+    lib.ssd_quaternion_workspace_bytes.restype = ctypes.c_size_t
+    lib.ssd_quaternion_workspace_bytes.argtypes = [SP]
+    lib.ssd_quaternion_forward.restype = ctypes.c_int
+    lib.ssd_quaternion_forward.argtypes = [SP] + [_VP] * 9 + [ctypes.c_size_t, _VP]
     lib.ssd_rotation_variant_workspace_bytes.restype = ctypes.c_size_t
     lib.ssd_rotation_variant_workspace_bytes.argtypes = [SP, _I64, ctypes.c_int32]
     lib.ssd_rotation_variant_forward.restype = ctypes.c_int
@@ -300,6 +305,43 @@ def ssd_trapezoidal_forward(x, dA, B, C, gamma, beta, *, chunk_len: int, theta=N
                               prev_x=prev_x, prev_B=prev_B, init_state=init_state, y=y,
                               final_state=final_state, return_final_state=return_final_state,
                               workspace=workspace, stream=stream)()
+
+
+def ssd_quaternion_forward(x, dA, B, C, qcum, *, chunk_len: int, init_state=None, y=None,
+                           final_state=None, return_final_state: bool = True, workspace=None,
+                           stream=None):
+    """SSD forward with the quaternion rotation through ``ssd_quaternion_forward``: qcum
+    [b,T,H,N/4,4] f32 cumulative unit quaternions (w, x, y, z) of the state's 4-blocks.
+    Returns (y, final)."""
+    if x.dim() != 5 or B.dim() != 5:
+        raise ValueError("x must be [b,T,R,H,P] and B/C [b,T,R,G,N]")
+    b, T, R, H, P = x.shape
+    G, N = B.shape[3], B.shape[4]
+    _check_cuda("x", x)
+    _check_cuda("B", B, x.dtype, (b, T, R, G, N))
+    _check_cuda("C", C, x.dtype, (b, T, R, G, N))
+    _check_cuda("dA", dA, torch.float32, (b, T, H))
+    _check_cuda("qcum", qcum, torch.float32, (b, T, H, N // 4, 4))
+    if init_state is not None:
+        _check_cuda("init_state", init_state, torch.float32, (b, H, P, N))
+    shape = shape_of(x, B, chunk_len, False)
+    lib = load_library()
+    if y is None:
+        y = torch.empty_like(x)
+    if final_state is None and return_final_state:
+        final_state = torch.empty((b, H, P, N), dtype=torch.float32, device=x.device)
+    need = int(lib.ssd_quaternion_workspace_bytes(ctypes.byref(shape)))
+    if need == 0:
+        raise SSDError(2, "ssd_quaternion_workspace_bytes (shape not supported)")
+    if workspace is None:
+        workspace = torch.zeros(need, dtype=torch.uint8, device=x.device)
+    st = lib.ssd_quaternion_forward(ctypes.byref(shape), _ptr(x), _ptr(dA), _ptr(B), _ptr(C),
+                                    _ptr(qcum), _ptr(init_state), _ptr(y), _ptr(final_state),
+                                    _ptr(workspace), ctypes.c_size_t(workspace.numel()),
+                                    _stream_handle(stream))
+    if st != 0:
+        raise SSDError(st, "ssd_quaternion_forward")
+    return y, final_state
 
 
 def ssd_rotation_variant_forward(x, dA, B, C, theta, *, chunk_len: int, rope_dim: int = 0,

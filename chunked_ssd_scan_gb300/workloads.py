@@ -211,6 +211,19 @@ def make_ssd_inputs(cfg: SSDConfig, seed: int = 0, *, slow_decay: bool = False,
     return out
 
 
+def make_quaternions(batch: int, T: int, H: int, N: int, seed: int = 0,
+                     step: float = 0.05) -> torch.Tensor:
+    """Cumulative unit quaternions [batch, T, H, N/4, 4] (w, x, y, z) for the quaternion
+    rotation: a normalised random walk in R^4 started at the identity, so consecutive steps
+    differ by small turns (the per-step turn of a step is a few times `step` radians)."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed)
+    u = torch.randn((batch, T, H, N // 4, 4), generator=g, dtype=torch.float64) * step
+    u = torch.cumsum(u, dim=1)
+    u[..., 0] += 1.0
+    return (u / torch.linalg.vector_norm(u, dim=-1, keepdim=True)).to(torch.float32).contiguous()
+
+
 def make_trap_inputs(cfg: SSDConfig, seed: int = 0, *, slow_decay: bool = False,
                      init_state: bool = False, prev: bool = True,
                      device: Optional[str] = None) -> dict:

@@ -64,7 +64,7 @@ typedef enum ssd_kernel_variant {
   SSD_VARIANT_NONE = 0,    /* shape not supported                                    */
   SSD_VARIANT_GENERIC = 1, /* CUDA-core fp32 chunk pipeline (any supported shape)    */
   SSD_VARIANT_TC_BF16 = 2, /* fused tcgen05/TMEM kernel, bf16 operands, fp32 accum.  */
-  SSD_VARIANT_TILED_F32 = 3 /* register-tiled CUDA-core fp32 kernels, P = N = 64, R = 1  */
+  SSD_VARIANT_TILED_F32 = 3 /* register-tiled CUDA-core fp32 kernels, P = N = 64, R | 64 */
 } ssd_kernel_variant;
 
 /*
@@ -168,6 +168,29 @@ ssd_status ssd_rotation_variant_forward(const ssd_shape* shape, int64_t rope_dim
                                         const void* B, const void* C, const float* theta,
                                         const float* init_state, void* y, float* final_state,
                                         void* workspace, size_t workspace_bytes, void* stream);
+
+/* Bytes of device workspace ssd_quaternion_forward needs (0 if the shape is invalid or
+ * unsupported: has_theta must be 0 and dstate a multiple of 4). */
+size_t ssd_quaternion_workspace_bytes(const ssd_shape* shape);
+
+/*
+ * Quaternion rotation of the rotated SSD forward (moments.rs page, RotationSeq::Quaternion
+ * { cum_bshj4 }; named there, not defined, read plainly): qcum [batch, seqlen, nheads,
+ * dstate/4, 4] f32 holds the cumulative unit quaternion Q_t = (w, x, y, z) of every 4-dimension
+ * block of the state axis.  Block j of the state, the quaternion h[4j] + h[4j+1] i + h[4j+2] j
+ * + h[4j+3] k, is turned at step t (before the decay and the write, as the angle rotation) by
+ * left multiplication with Q_t Q_{t-1}^* (Q_{-1} = 1); with Q = cos(Phi) + i sin(Phi) this is
+ * the interleaved angle rotation with both pairs of a block turned alike.  init_state and
+ * final_state are in the physical frame.  shape->has_theta must be 0 and dstate % 4 == 0;
+ * qcum and final_state 16-byte aligned.  Runs as B and C turned by Q_t^* per head into fp32 in
+ * the workspace, ssd_chunked_forward on that fp32 problem (one group per head), and the final
+ * state turned back by Q_{T-1}.  Layouts of x, dA, B, C, y, the states, asynchrony, errors and
+ * the workspace header as ssd_chunked_forward.
+ */
+ssd_status ssd_quaternion_forward(const ssd_shape* shape, const void* x, const float* dA,
+                                  const void* B, const void* C, const float* qcum,
+                                  const float* init_state, void* y, float* final_state,
+                                  void* workspace, size_t workspace_bytes, void* stream);
 
 /* Bytes of device workspace ssd_chunked_backward needs for `shape` (0 if unsupported). */
 size_t ssd_backward_workspace_bytes(const ssd_shape* shape);

@@ -55,6 +55,8 @@ def _lib():
         lib.oracle_ssd_trap_backward_ex.argtypes = [_D] * 22 + [_I64] * 8 + [ctypes.c_int]
         lib.oracle_ssd_rot_ex.restype = ctypes.c_int
         lib.oracle_ssd_rot_ex.argtypes = [_D] * 8 + [_I64] * 8 + [ctypes.c_int, _I64, ctypes.c_int]
+        lib.oracle_ssd_quat_ex.restype = ctypes.c_int
+        lib.oracle_ssd_quat_ex.argtypes = [_D] * 8 + [_I64] * 8 + [ctypes.c_int]
         lib.oracle_ssd_trap_ex.restype = ctypes.c_int
         lib.oracle_ssd_trap_ex.argtypes = [_D] * 12 + [_I64] * 8 + [ctypes.c_int]
         lib.oracle_selective_scan_ex.restype = ctypes.c_int
@@ -181,6 +183,24 @@ def ssd_rotation_variant(x, dA, B, C, theta, init_state=None, rope_dim: int = 0,
     return y, fin
 
 
+def ssd_quaternion(x, dA, B, C, qcum, init_state=None, nthreads=None, mutation: int = 0):
+    """Sequential fp64 SSD recurrence with the quaternion rotation (see ssd_oracle.c): qcum
+    [b,T,H,N/4,4] cumulative unit quaternions (w, x, y, z); block j of the state is turned by
+    left multiplication with qcum_t qcum_{t-1}^* before the write.  Returns (y, final_state)."""
+    x, dA, B, C, qcum, init_state = (_f64(v) for v in (x, dA, B, C, qcum, init_state))
+    b, T, R, H, P = x.shape
+    G, N = B.shape[3], B.shape[4]
+    assert N % 4 == 0 and qcum.shape == (b, T, H, N // 4, 4)
+    y = np.zeros((b, T, R, H, P), np.float64)
+    fin = np.zeros((b, H, P, N), np.float64)
+    rc = _lib().oracle_ssd_quat_ex(_ptr(x), _ptr(dA), _ptr(B), _ptr(C), _ptr(qcum),
+                                   _ptr(init_state), _ptr(y), _ptr(fin), b, T, R, H, G, P, N,
+                                   nthreads or default_threads(), int(mutation))
+    if rc != 0:
+        raise ValueError(f"oracle_ssd_quat rejected its arguments (code {rc})")
+    return y, fin
+
+
 def ssd_trapezoidal(x, dA, B, C, gamma, beta, theta=None, init_state=None, prev_x=None,
                     prev_B=None, nthreads=None, mutation: int = 0):
     """Sequential fp64 trapezoidal SSD recurrence (see ssd_oracle.c).  Returns (y, final_state)."""
@@ -242,6 +262,10 @@ MUTATIONS_TRAP = {
 MUTATIONS_ROT = {
     "interleaved_instead_of_halves": 12,
     "rope_on_last_dims": 13,
+}
+MUTATIONS_QUAT = {
+    "quaternion_right_multiplication": 20,
+    "cumulative_quaternion_as_step": 21,
 }
 MUTATIONS_BWD = {
     "dy_added_after_decay": 14,

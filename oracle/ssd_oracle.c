@@ -31,6 +31,13 @@
  *     dimensions turn, theta then has rope_dim/2 angles per step, and the pair k is either the
  *     interleaved (2k, 2k+1) (rotate_pairwise, the default) or the split halves
  *     (k, k + rope_dim/2).
+ *   - Quaternion rotation (moments.rs page, RotationSeq::Quaternion { cum_bshj4 }, given as the
+ *     cumulative unit quaternion Q_t per (b, t, h) and 4-dimension block j of the state axis;
+ *     named, not defined, read plainly): in place of R(theta_t), block j (dimensions 4j..4j+3,
+ *     the quaternion h[4j] + h[4j+1] i + h[4j+2] j + h[4j+3] k) is multiplied on the left by
+ *     the step quaternion q_t = Q_t Q_{t-1}^* (Q_{-1} = 1), so the turns up to step t compose
+ *     to Q_t.  Left multiplication by a unit quaternion is orthogonal; with q = cos + i sin it
+ *     turns the pairs (4j, 4j+1) and (4j+2, 4j+3) both by the angle, as R does.
  *
  *   Trapezoidal SSD (Mamba-3; scan.py page, the trapezoidal forward: the beta term carries the
  *   PREVIOUS step's write and is turned by one step less of rotation), per (b, h):
@@ -73,6 +80,8 @@ typedef struct {
   /* rotation variant: rope_dim (0 = N) and halves (0 = interleaved pairs) */
   int64_t rope_dim;
   int halves;
+  /* quaternion rotation: cumulative unit quaternions [b, T, H, N/4, 4] (NULL = none) */
+  const double* qcum;
 } ssd_job;
 
 /* Planted-mistake codes, used only by the oracle's own pin tests. */
@@ -91,7 +100,51 @@ enum {
   MUT_TRAP_BETA_CURRENT = 11,     /* trapezoidal: beta multiplies S_t, not S_{t-1} */
   MUT_ROT_INTERLEAVED = 12,       /* rotation variant: ignores the split-halves pairing */
   MUT_ROPE_LAST_DIMS = 13,        /* rotation variant: turns the last rope_dim dims */
+  MUT_QUAT_RIGHT = 20,            /* quaternion: multiplies on the right, not the left */
+  MUT_QUAT_CUM_AS_STEP = 21,      /* quaternion: turns by Q_t instead of Q_t Q_{t-1}^* */
 };
+
+/* Hamilton product o = a b of quaternions stored (w, x, y, z) = w + x i + y j + z k. */
+static void quat_mul(const double* a, const double* b, double* o) {
+  const double w = a[0] * b[0] - a[1] * b[1] - a[2] * b[2] - a[3] * b[3];
+  const double x = a[0] * b[1] + a[1] * b[0] + a[2] * b[3] - a[3] * b[2];
+  const double y = a[0] * b[2] - a[1] * b[3] + a[2] * b[0] + a[3] * b[1];
+  const double z = a[0] * b[3] + a[1] * b[2] - a[2] * b[1] + a[3] * b[0];
+  o[0] = w;
+  o[1] = x;
+  o[2] = y;
+  o[3] = z;
+}
+
+/* Quaternion rotation of one step (moments.rs page, RotationSeq::Quaternion { cum_bshj4 }):
+ * block k of the state axis, dimensions (4k .. 4k+3) read as the quaternion
+ * h[4k] + h[4k+1] i + h[4k+2] j + h[4k+3] k, is turned by LEFT multiplication with the step's
+ * unit quaternion q_t = Q_t Q_{t-1}^* (Q the given cumulative quaternions, Q_{-1} = 1), so that
+ * the turns compose to Q_t over steps 0..t. */
+static void quat_turn_state(const ssd_job* j, int64_t b, int64_t hh, int64_t t, double* h) {
+  const int64_t T = j->T, H = j->H, P = j->P, N = j->N, K = N / 4;
+  const double* Qt = j->qcum + ((b * T + t) * H + hh) * K * 4;
+  const double* Qp = t > 0 ? j->qcum + ((b * T + t - 1) * H + hh) * K * 4 : NULL;
+  for (int64_t k = 0; k < K; ++k) {
+    double q[4];
+    if (j->mutation == MUT_QUAT_CUM_AS_STEP || !Qp) {
+      memcpy(q, Qt + 4 * k, sizeof(q));
+    } else {
+      const double conj[4] = {Qp[4 * k], -Qp[4 * k + 1], -Qp[4 * k + 2], -Qp[4 * k + 3]};
+      quat_mul(Qt + 4 * k, conj, q);
+    }
+    for (int64_t p = 0; p < P; ++p) {
+      double* v = h + p * N + 4 * k;
+      double o[4];
+      if (j->mutation == MUT_QUAT_RIGHT) {
+        quat_mul(v, q, o);
+      } else {
+        quat_mul(q, v, o);
+      }
+      memcpy(v, o, sizeof(o));
+    }
+  }
+}
 
 /* The pair of state dimensions that angle k of the rotation variant turns. */
 static void rot_pair(const ssd_job* j, int64_t k, int64_t* d0, int64_t* d1) {
@@ -186,6 +239,7 @@ static void ssd_one(const ssd_job* j, int64_t b, int64_t hh, double* h) {
   }
   for (int64_t t = 0; t < T; ++t) {
     const double a = (j->mutation == MUT_NO_DECAY) ? 1.0 : exp(j->dA[(b * T + t) * H + hh]);
+    if (j->qcum) quat_turn_state(j, b, hh, t, h);
     if (j->theta) {
       const int64_t K = (j->rope_dim > 0 ? j->rope_dim : N) / 2;
       const double* th = j->theta + ((b * T + t) * H + hh) * K;
@@ -269,8 +323,10 @@ static int run_ssd(const double* x, const double* dA, const double* B, const dou
                    const double* theta, const double* init_state, double* y, double* final_state,
                    int64_t batch, int64_t T, int64_t R, int64_t H, int64_t G, int64_t P, int64_t N,
                    int64_t nthreads, int mutation, const double* gamma, const double* beta,
-                   const double* prev_x, const double* prev_B, int64_t rope_dim, int halves) {
+                   const double* prev_x, const double* prev_B, int64_t rope_dim, int halves,
+                   const double* qcum) {
   if (!x || !dA || !B || !C || !y) return -1;
+  if (qcum && ((N % 4) != 0 || theta)) return -7;
   if (batch < 0 || T < 0 || R < 1 || H < 1 || G < 1 || P < 1 || N < 1) return -2;
   if (H % G != 0) return -3;
   if (theta && (N % 2 != 0)) return -4;
@@ -294,7 +350,7 @@ static int run_ssd(const double* x, const double* dA, const double* B, const dou
   for (int64_t i = 0; i < nt; ++i) {
     ssd_job j = {x,  dA, B,    C,     theta,  init_state, y,      final_state, batch, T,
                  R,  H,  G,    P,     N,      mutation,   nt,     i,           gamma, beta,
-                 prev_x, prev_B, rope_dim, halves};
+                 prev_x, prev_B, rope_dim, halves, qcum};
     jobs[i] = j;
   }
   for (int64_t i = 1; i < nt; ++i) pthread_create(&th[i], NULL, ssd_worker, &jobs[i]);
@@ -315,7 +371,7 @@ int oracle_ssd_ex(const double* x, const double* dA, const double* B, const doub
                   int64_t batch, int64_t T, int64_t R, int64_t H, int64_t G, int64_t P, int64_t N,
                   int64_t nthreads, int mutation) {
   return run_ssd(x, dA, B, C, theta, init_state, y, final_state, batch, T, R, H, G, P, N,
-                 nthreads, mutation, NULL, NULL, NULL, NULL, 0, 0);
+                 nthreads, mutation, NULL, NULL, NULL, NULL, 0, 0, NULL);
 }
 
 /* Rotation variants: theta [b,T,H,rope_dim/2] (rope_dim 0 = dstate); halves = 1 pairs the
@@ -326,7 +382,18 @@ int oracle_ssd_rot_ex(const double* x, const double* dA, const double* B, const 
                       int64_t G, int64_t P, int64_t N, int64_t rope_dim, int halves,
                       int64_t nthreads, int mutation) {
   return run_ssd(x, dA, B, C, theta, init_state, y, final_state, batch, T, R, H, G, P, N,
-                 nthreads, mutation, NULL, NULL, NULL, NULL, rope_dim, halves);
+                 nthreads, mutation, NULL, NULL, NULL, NULL, rope_dim, halves, NULL);
+}
+
+/* Quaternion rotation: qcum [b,T,H,N/4,4] cumulative unit quaternions (w, x, y, z); N % 4 == 0,
+ * no theta.  Block k of the state is turned by left multiplication with Q_t Q_{t-1}^* at step t. */
+int oracle_ssd_quat_ex(const double* x, const double* dA, const double* B, const double* C,
+                       const double* qcum, const double* init_state, double* y,
+                       double* final_state, int64_t batch, int64_t T, int64_t R, int64_t H,
+                       int64_t G, int64_t P, int64_t N, int64_t nthreads, int mutation) {
+  if (!qcum) return -1;
+  return run_ssd(x, dA, B, C, NULL, init_state, y, final_state, batch, T, R, H, G, P, N,
+                 nthreads, mutation, NULL, NULL, NULL, NULL, 0, 0, qcum);
 }
 
 /* Trapezoidal form: gamma, beta [b,T,H]; prev_x [b,R,H,P] and prev_B [b,R,G,N] may be NULL
@@ -338,7 +405,7 @@ int oracle_ssd_trap_ex(const double* x, const double* dA, const double* B, const
                        int64_t H, int64_t G, int64_t P, int64_t N, int64_t nthreads, int mutation) {
   if (!gamma || !beta) return -1;
   return run_ssd(x, dA, B, C, theta, init_state, y, final_state, batch, T, R, H, G, P, N,
-                 nthreads, mutation, gamma, beta, prev_x, prev_B, 0, 0);
+                 nthreads, mutation, gamma, beta, prev_x, prev_B, 0, 0, NULL);
 }
 
 int oracle_ssd(const double* x, const double* dA, const double* B, const double* C,

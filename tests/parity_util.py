@@ -1,6 +1,8 @@
 """Helpers shared by the GPU parity tests: run the library and the oracle on the same inputs."""
 from __future__ import annotations
 
+import ctypes
+
 import numpy as np
 import torch
 
@@ -16,16 +18,64 @@ def to_np(t):
     return None if t is None else t.detach().to("cpu", torch.float64).numpy()
 
 
-def gpu_ssd(inp: dict, chunk_len: int, dev: str = "cuda", final: bool = True):
+GUARD_BYTES = 4096
+GUARD_FILL = 0xFF   # every guard byte: 0xFFFF is a bf16 NaN, 0xFFFFFFFF an fp32 NaN
+
+
+class Guarded:
+    """A device buffer of `nbytes` carved out of a larger one with GUARD_BYTES of NaN pattern on
+    each side; check() asserts that nothing wrote into either guard band."""
+
+    def __init__(self, nbytes: int, dev: str, fill_inner: int = 0):
+        self.base = torch.full((GUARD_BYTES + nbytes + GUARD_BYTES,), GUARD_FILL,
+                               dtype=torch.uint8, device=dev)
+        self.inner = self.base[GUARD_BYTES:GUARD_BYTES + nbytes]
+        self.inner.fill_(fill_inner)
+
+    def view(self, dtype, shape):
+        return self.inner.view(dtype).view(shape)
+
+    def check(self, what: str):
+        lo = self.base[:GUARD_BYTES]
+        hi = self.base[-GUARD_BYTES:]
+        for name, band in (("before", lo), ("after", hi)):
+            bad = int((band != GUARD_FILL).sum().item())
+            assert bad == 0, f"{what}: {bad} bytes of the guard band {name} the buffer were written"
+
+
+def gpu_ssd(inp: dict, chunk_len: int, dev: str = "cuda", final: bool = True,
+            guard: bool = False):
     """One forward through the C ABI; the device-side error word of its workspace must be clean
-    (a bounded wait that gave up would otherwise only show as wrong numbers)."""
+    (a bounded wait that gave up would otherwise only show as wrong numbers).  With guard=True,
+    y, the final state and the workspace sit between NaN-pattern guard bands that must be intact
+    after the call (an out-of-bounds store that element-wise parity cannot see would show)."""
     d = {k: (v.to(dev) if v is not None else None) for k, v in inp.items()}
+    kw = {}
+    bands = []
+    if guard:
+        x, B = d["x"], d["B"]
+        b, T, R, H, P = x.shape
+        N = B.shape[4]
+        gy = Guarded(x.numel() * x.element_size(), dev, fill_inner=GUARD_FILL)
+        kw["y"] = gy.view(x.dtype, x.shape)
+        bands.append((gy, "y"))
+        if final:
+            gf = Guarded(b * H * P * N * 4, dev, fill_inner=GUARD_FILL)
+            kw["final_state"] = gf.view(torch.float32, (b, H, P, N))
+            bands.append((gf, "final_state"))
+        shape = pkg.shape_of(x, B, chunk_len, d["theta"] is not None)
+        nws = int(pkg.load_library().ssd_chunked_workspace_bytes(ctypes.byref(shape)))
+        gw = Guarded(nws, dev, fill_inner=0)   # a workspace starts with a zeroed header
+        kw["workspace"] = gw.inner
+        bands.append((gw, "workspace"))
     plan = pkg.SSDForwardPlan(d["x"], d["dA"], d["B"], d["C"], chunk_len=chunk_len,
                               theta=d["theta"], init_state=d["init_state"],
-                              return_final_state=final)
+                              return_final_state=final, **kw)
     y, fin = plan()
     assert pkg.workspace_status(plan.workspace) == ("SSD_OK", 0)
     torch.cuda.synchronize()
+    for g, what in bands:
+        g.check(what)
     return to_np(y), to_np(fin)
 
 

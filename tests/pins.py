@@ -388,6 +388,89 @@ def pin_rope_dim_superposition(mutation=0):
 ROT_PINS = [pin_rotation_variant_reductions, pin_rope_dim_superposition]
 
 
+# ------------------------------------------------------------------------ quaternion rotation
+def _quat_left_matrix(q):
+    """4 x 4 matrix of v -> q v (Hamilton product, components (w, x, y, z)), for q [..., 4]."""
+    w, x, y, z = (q[..., k] for k in range(4))
+    return np.stack([np.stack([w, -x, -y, -z], -1), np.stack([x, w, -z, y], -1),
+                     np.stack([y, z, w, -x], -1), np.stack([z, -y, x, w], -1)], -2)
+
+
+def _unit_quat_walk(seed, shape, step=0.15):
+    """Smooth cumulative unit quaternions: a normalised random walk in R^4 (no products)."""
+    r = _rng(seed)
+    u = np.cumsum(r.normal(0.0, step, shape + (4,)), axis=1)
+    u[..., 0] += 1.0
+    return u / np.linalg.norm(u, axis=-1, keepdims=True)
+
+
+def pin_quaternion_reductions(mutation=0):
+    """The quaternion form against closed forms: (1) cumulative quaternions cos Phi + i sin Phi
+    (Phi the cumulative angle) turn both pairs of each 4-block by the step angle, exactly the
+    interleaved angle rotation with each block's angle on its two pairs; (2) with no writes and
+    no decay the final state is Q_{T-1} h0 blockwise (the step turns compose to the cumulative
+    one), and for Q = cos phi + j sin phi that turns (h0, h2) by +phi and (h1, h3) by -phi (left
+    multiplication; on the right the second pair would turn by +phi); the norm of every block
+    is preserved."""
+    res = []
+    x, dA, B, C, _, h0 = _problem(61, 2, 27, 2, 2, 1, 3, 8, init=True)
+    th = _rng(62).uniform(-0.4, 0.4, (2, 27, 2, 2))
+    Phi = np.cumsum(th, axis=1)
+    Q = np.zeros((2, 27, 2, 2, 4))
+    Q[..., 0], Q[..., 1] = np.cos(Phi), np.sin(Phi)
+    yq, fq = oracle.ssd_quaternion(x, dA, B, C, Q, h0, mutation=mutation)
+    ya, fa = oracle.ssd(x, dA, B, C, np.repeat(th, 2, axis=3), h0)
+    res.append(("quat_i_axis_is_pairwise_angles", max(_maxerr(yq, ya), _maxerr(fq, fa)), 1e-12))
+    T = 11
+    z5 = lambda *s: np.zeros(s)
+    Qw = _unit_quat_walk(63, (1, T, 1, 2))
+    h0 = _rng(64).standard_normal((1, 1, 2, 8))
+    _, f = oracle.ssd_quaternion(z5(1, T, 1, 1, 2), z5(1, T, 1), z5(1, T, 1, 1, 8),
+                                 z5(1, T, 1, 1, 8), Qw, h0, mutation=mutation)
+    L = _quat_left_matrix(Qw[0, T - 1, 0])                     # [2 blocks, 4, 4]
+    want = np.einsum("kab,pkb->pka", L, h0[0, 0].reshape(2, 2, 4)).reshape(2, 8)
+    res.append(("quat_pure_turn_composes_to_cumulative", _maxerr(f[0, 0], want), 1e-12))
+    res.append(("quat_block_norms_preserved",
+                _maxerr(np.linalg.norm(f[0, 0].reshape(2, 2, 4), axis=-1),
+                        np.linalg.norm(h0[0, 0].reshape(2, 2, 4), axis=-1)), 1e-12))
+    phi = 0.7
+    Qj = np.zeros((1, 3, 1, 1, 4))
+    Qj[..., 0], Qj[..., 2] = math.cos(phi), math.sin(phi)      # constant: one turn at step 0
+    hv = np.array([1.0, 2.0, 3.0, 4.0]).reshape(1, 1, 1, 4)
+    _, f = oracle.ssd_quaternion(z5(1, 3, 1, 1, 1), z5(1, 3, 1), z5(1, 3, 1, 1, 4),
+                                 z5(1, 3, 1, 1, 4), Qj, hv, mutation=mutation)
+    c, s = math.cos(phi), math.sin(phi)
+    want = [c * 1 - s * 3, c * 2 + s * 4, s * 1 + c * 3, c * 4 - s * 2]
+    res.append(("quat_j_axis_left_multiplication", _maxerr(f.reshape(4), want), 1e-13))
+    return res
+
+
+def pin_quaternion_absorbed_frame(mutation=0):
+    """The rotation absorbed into B and C (left multiplication is orthogonal, so
+    C . (Q g) = (Q^* C) . g): the plain recurrence on B~ = Q_t^* B_t, C~ = Q_t^* C_t per head,
+    with the final state turned back by Q_{T-1}, equals the quaternion recurrence (MIMO, a group
+    shared by two heads, an initial state)."""
+    res = []
+    b, T, R, H, G, P, N = 1, 33, 2, 2, 1, 3, 8
+    x, dA, B, C, _, h0 = _problem(65, b, T, R, H, G, P, N, init=True, decay=(0.0, 0.2))
+    Q = _unit_quat_walk(66, (b, T, H, N // 4))
+    y, f = oracle.ssd_quaternion(x, dA, B, C, Q, h0, mutation=mutation)
+    Qc = Q * np.array([1.0, -1.0, -1.0, -1.0])
+    Lc = _quat_left_matrix(Qc)                                   # [b, T, H, N/4, 4, 4]
+    turn = lambda V: np.einsum("bthkij,btrhkj->btrhki", Lc,
+                               np.repeat(V, H // G, axis=3).reshape(b, T, R, H, N // 4, 4)
+                               ).reshape(b, T, R, H, N)
+    yp, g = oracle.ssd(x, dA, turn(B), turn(C), None, h0)
+    Lf = _quat_left_matrix(Q[:, T - 1])                          # [b, H, N/4, 4, 4]
+    fp = np.einsum("bhkij,bhpkj->bhpki", Lf, g.reshape(b, H, P, N // 4, 4)).reshape(b, H, P, N)
+    res.append(("quat_absorbed_frame_y", _maxerr(y, yp), 1e-10))
+    res.append(("quat_absorbed_frame_final", _maxerr(f, fp), 1e-10))
+    return res
+
+
+QUAT_PINS = [pin_quaternion_reductions, pin_quaternion_absorbed_frame]
+
+
 # ------------------------------------------------------------------------------------ backward
 def pin_backward_finite_differences(mutation=0):
     """The backward oracle against central differences of the forward oracle: for the loss

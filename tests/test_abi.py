@@ -40,6 +40,7 @@ def test_header_declares_the_abi():
                      "ssd_workspace_status", "ssd_status_string", "ssd_abi_version",
                      "ssd_trapezoidal_forward", "ssd_trapezoidal_workspace_bytes",
                      "ssd_rotation_variant_forward", "ssd_rotation_variant_workspace_bytes",
+                     "ssd_quaternion_forward", "ssd_quaternion_workspace_bytes",
                      "ssd_chunked_backward", "ssd_backward_workspace_bytes"):
         assert expected in names
 
@@ -220,3 +221,31 @@ def test_backward_host_rejections(lib):
     bad = list(ptrs)
     bad[7] = _VP(A16)                                           # prev_x without prev_B
     assert f(*args(bad, need)) == 1
+
+
+def declared_parameter_counts():
+    """Number of parameters of every function declared in the header."""
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    src = re.sub(r"//[^\n]*", "", src)
+    counts = {}
+    for m in re.finditer(r"^(?!typedef|#)[A-Za-z_][\w \t\*]*?\b([a-z_][a-z0-9_]*)\s*\(([^)]*)\)\s*;",
+                         src, flags=re.M):
+        params = m.group(2).strip()
+        counts[m.group(1)] = 0 if params in ("", "void") else len(params.split(","))
+    return counts
+
+
+def test_binding_argument_counts_match_the_header(lib):
+    """Every function the binding gives argtypes to takes as many arguments as the header
+    declares (a miscounted binding would fail only when called on a GPU)."""
+    counts = declared_parameter_counts()
+    assert counts, "no declarations parsed"
+    checked = 0
+    for name, n in counts.items():
+        argtypes = getattr(getattr(lib, name), "argtypes", None)
+        if argtypes is None:
+            continue
+        assert len(argtypes) == n, f"{name}: binding has {len(argtypes)} arguments, header {n}"
+        checked += 1
+    assert checked >= 10

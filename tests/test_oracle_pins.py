@@ -8,7 +8,7 @@ from tests import pins
 
 
 @pytest.mark.parametrize("pin", pins.SSD_PINS + pins.SS_PINS + pins.TRAP_PINS + pins.ROT_PINS
-                         + pins.BWD_PINS + pins.TRAP_BWD_PINS,
+                         + pins.QUAT_PINS + pins.BWD_PINS + pins.TRAP_BWD_PINS,
                          ids=lambda f: f.__name__)
 def test_pin_holds(pin):
     for name, err, tol in pin(0):
@@ -31,6 +31,12 @@ def test_planted_trapezoidal_mistake_is_caught(name, code):
 def test_planted_rotation_variant_mistake_is_caught(name, code):
     failed = [n for pin in pins.ROT_PINS for (n, err, tol) in pin(code) if not err <= tol]
     assert failed, f"planted mistake '{name}' passed every rotation-variant pin"
+
+
+@pytest.mark.parametrize("name,code", sorted(oracle.MUTATIONS_QUAT.items()))
+def test_planted_quaternion_mistake_is_caught(name, code):
+    failed = [n for pin in pins.QUAT_PINS for (n, err, tol) in pin(code) if not err <= tol]
+    assert failed, f"planted mistake '{name}' passed every quaternion pin"
 
 
 @pytest.mark.parametrize("name,code", sorted(oracle.MUTATIONS_BWD.items()))

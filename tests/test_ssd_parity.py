@@ -125,7 +125,7 @@ def test_ragged_sequence_lengths(cfg):
     assert pkg.ssd_chunked_variant(shape) == expect, cfg.name
     for kw in ({}, dict(slow_decay=True, init_state=True)):
         inp = wl.make_ssd_inputs(cfg, seed=8, **kw)
-        y, fin = gpu_ssd(inp, cfg.chunk_len)
+        y, fin = gpu_ssd(inp, cfg.chunk_len, guard=True)
         yr, fr = oracle_ssd(inp)
         check_close(y, yr, TOL[cfg.dtype], f"{cfg.name} y")
         check_close(fin, fr, TOL[cfg.dtype], f"{cfg.name} final_state")
@@ -181,7 +181,7 @@ def test_bf16_workloads_use_the_fused_kernel():
 @pytest.mark.parametrize("cfg", EDGE, ids=lambda c: c.name)
 def test_edge_shapes(cfg):
     inp = wl.make_ssd_inputs(cfg, seed=3, slow_decay=True, init_state=True)
-    y, fin = gpu_ssd(inp, cfg.chunk_len)
+    y, fin = gpu_ssd(inp, cfg.chunk_len, guard=True)
     yr, fr = oracle_ssd(inp)
     check_close(y, yr, TOL[cfg.dtype], f"{cfg.name} y")
     check_close(fin, fr, TOL[cfg.dtype], f"{cfg.name} final_state")
