@@ -73,10 +73,14 @@ def load_library(path: Optional[str] = None):
     lib.ssd_chunked_launches.argtypes = [SP]
     lib.ssd_chunked_forward.restype = ctypes.c_int
     lib.ssd_chunked_forward.argtypes = [SP] + [_VP] * 9 + [ctypes.c_size_t, _VP]
+    lib.ssd_chunked_forward_varlen.restype = ctypes.c_int
+    lib.ssd_chunked_forward_varlen.argtypes = [SP] + [_VP] * 10 + [ctypes.c_size_t, _VP]
     lib.ssd_trapezoidal_workspace_bytes.restype = ctypes.c_size_t
     lib.ssd_trapezoidal_workspace_bytes.argtypes = [SP]
     lib.ssd_trapezoidal_forward.restype = ctypes.c_int
     lib.ssd_trapezoidal_forward.argtypes = [SP] + [_VP] * 13 + [ctypes.c_size_t, _VP]
+    lib.ssd_trapezoidal_forward_varlen.restype = ctypes.c_int
+    lib.ssd_trapezoidal_forward_varlen.argtypes = [SP] + [_VP] * 14 + [ctypes.c_size_t, _VP]
     lib.ssd_quaternion_workspace_bytes.restype = ctypes.c_size_t
     lib.ssd_quaternion_workspace_bytes.argtypes = [SP]
     lib.ssd_quaternion_forward.restype = ctypes.c_int
@@ -163,14 +167,16 @@ def shape_of(x: torch.Tensor, B: torch.Tensor, chunk_len: int, has_theta: bool) 
 class SSDForwardPlan:
     """Arguments of ``ssd_chunked_forward`` validated once, for repeated calls on the same
     buffers.  Calling the plan makes only the C call (on the stream given here, or the stream
-    that is current at construction).  Shapes and dtypes are those of ``ssd_chunked_forward``.
+    that is current at construction).  Shapes and dtypes are those of ``ssd_chunked_forward``;
+    with ``valid_len`` (int64 [b] on the device) the plan calls ``ssd_chunked_forward_varlen``.
     """
 
     def __init__(self, x: torch.Tensor, dA: torch.Tensor, B: torch.Tensor, C: torch.Tensor, *,
                  chunk_len: int, theta: Optional[torch.Tensor] = None,
                  init_state: Optional[torch.Tensor] = None, y: Optional[torch.Tensor] = None,
                  final_state: Optional[torch.Tensor] = None, return_final_state: bool = True,
-                 workspace: Optional[torch.Tensor] = None, stream=None):
+                 workspace: Optional[torch.Tensor] = None, stream=None,
+                 valid_len: Optional[torch.Tensor] = None):
         if x.dim() != 5 or B.dim() != 5:
             raise ValueError("x must be [b,T,R,H,P] and B/C [b,T,R,G,N]")
         b, T, R, H, P = x.shape
@@ -185,6 +191,8 @@ class SSDForwardPlan:
             _check_cuda("theta", theta, torch.float32, (b, T, H, N // 2))
         if init_state is not None:
             _check_cuda("init_state", init_state, torch.float32, (b, H, P, N))
+        if valid_len is not None:
+            _check_cuda("valid_len", valid_len, torch.int64, (b,))
         self.shape = shape_of(x, B, chunk_len, theta is not None)
         self._lib = load_library()
         if y is None:
@@ -201,17 +209,19 @@ class SSDForwardPlan:
             workspace = torch.zeros(need, dtype=torch.uint8, device=x.device)   # zero header
         _check_cuda("workspace", workspace, torch.uint8)
         # keep every buffer alive as long as the plan
-        self.inputs = (x, dA, B, C, theta, init_state)
+        self.inputs = (x, dA, B, C, theta, init_state, valid_len)
         self.y, self.final_state, self.workspace = y, final_state, workspace
+        vl = () if valid_len is None else (_ptr(valid_len),)
         self._args = (ctypes.byref(self.shape), _ptr(x), _ptr(dA), _ptr(B), _ptr(C), _ptr(theta),
-                      _ptr(init_state), _ptr(y), _ptr(final_state), _ptr(workspace),
+                      *vl, _ptr(init_state), _ptr(y), _ptr(final_state), _ptr(workspace),
                       ctypes.c_size_t(workspace.numel()), _stream_handle(stream))
-        self._fn = self._lib.ssd_chunked_forward
+        self._name = "ssd_chunked_forward" + ("" if valid_len is None else "_varlen")
+        self._fn = getattr(self._lib, self._name)
 
     def __call__(self):
         st = self._fn(*self._args)
         if st != 0:
-            raise SSDError(st, "ssd_chunked_forward")
+            raise SSDError(st, self._name)
         return self.y, self.final_state
 
 
@@ -221,15 +231,18 @@ def ssd_chunked_forward(x: torch.Tensor, dA: torch.Tensor, B: torch.Tensor, C: t
                         y: Optional[torch.Tensor] = None,
                         final_state: Optional[torch.Tensor] = None,
                         return_final_state: bool = True,
-                        workspace: Optional[torch.Tensor] = None, stream=None):
-    """Chunked SSD forward scan through ``ssd_chunked_forward``.
+                        workspace: Optional[torch.Tensor] = None, stream=None,
+                        valid_len: Optional[torch.Tensor] = None):
+    """Chunked SSD forward scan through ``ssd_chunked_forward`` (``ssd_chunked_forward_varlen``
+    when ``valid_len`` is given).
 
     x [b,T,R,H,P], B/C [b,T,R,G,N] (all f32 or all bf16), dA [b,T,H] f32, theta [b,T,H,N/2] f32,
-    init_state [b,H,P,N] f32.  Returns (y, final_state) (final_state None if not requested).
+    init_state [b,H,P,N] f32, valid_len [b] int64 (steps from valid_len[b] on are padding; y is
+    not written there).  Returns (y, final_state) (final_state None if not requested).
     """
     return SSDForwardPlan(x, dA, B, C, chunk_len=chunk_len, theta=theta, init_state=init_state,
                           y=y, final_state=final_state, return_final_state=return_final_state,
-                          workspace=workspace, stream=stream)()
+                          workspace=workspace, stream=stream, valid_len=valid_len)()
 
 
 def ssd_trapezoidal_workspace_bytes(shape: ssd_shape) -> int:
@@ -246,7 +259,7 @@ class SSDTrapezoidalPlan:
 
     def __init__(self, x, dA, B, C, gamma, beta, *, chunk_len: int, theta=None, prev_x=None,
                  prev_B=None, init_state=None, y=None, final_state=None,
-                 return_final_state: bool = True, workspace=None, stream=None):
+                 return_final_state: bool = True, workspace=None, stream=None, valid_len=None):
         if x.dim() != 5 or B.dim() != 5:
             raise ValueError("x must be [b,T,R,H,P] and B/C [b,T,R,G,N]")
         b, T, R, H, P = x.shape
@@ -267,6 +280,8 @@ class SSDTrapezoidalPlan:
             _check_cuda("prev_B", prev_B, x.dtype, (b, R, G, N))
         if init_state is not None:
             _check_cuda("init_state", init_state, torch.float32, (b, H, P, N))
+        if valid_len is not None:
+            _check_cuda("valid_len", valid_len, torch.int64, (b,))
         self.shape = shape_of(x, B, chunk_len, theta is not None)
         self._lib = load_library()
         if y is None:
@@ -282,29 +297,33 @@ class SSDTrapezoidalPlan:
         if workspace is None:
             workspace = torch.zeros(need, dtype=torch.uint8, device=x.device)   # zero header
         _check_cuda("workspace", workspace, torch.uint8)
-        self.inputs = (x, dA, B, C, gamma, beta, theta, prev_x, prev_B, init_state)
+        self.inputs = (x, dA, B, C, gamma, beta, theta, prev_x, prev_B, init_state, valid_len)
         self.y, self.final_state, self.workspace = y, final_state, workspace
+        vl = () if valid_len is None else (_ptr(valid_len),)
         self._args = (ctypes.byref(self.shape), _ptr(x), _ptr(dA), _ptr(B), _ptr(C), _ptr(gamma),
-                      _ptr(beta), _ptr(theta), _ptr(prev_x), _ptr(prev_B), _ptr(init_state),
-                      _ptr(y), _ptr(final_state), _ptr(workspace),
+                      _ptr(beta), _ptr(theta), _ptr(prev_x), _ptr(prev_B), *vl,
+                      _ptr(init_state), _ptr(y), _ptr(final_state), _ptr(workspace),
                       ctypes.c_size_t(workspace.numel()), _stream_handle(stream))
-        self._fn = self._lib.ssd_trapezoidal_forward
+        self._name = "ssd_trapezoidal_forward" + ("" if valid_len is None else "_varlen")
+        self._fn = getattr(self._lib, self._name)
 
     def __call__(self):
         st = self._fn(*self._args)
         if st != 0:
-            raise SSDError(st, "ssd_trapezoidal_forward")
+            raise SSDError(st, self._name)
         return self.y, self.final_state
 
 
 def ssd_trapezoidal_forward(x, dA, B, C, gamma, beta, *, chunk_len: int, theta=None,
                             prev_x=None, prev_B=None, init_state=None, y=None, final_state=None,
-                            return_final_state: bool = True, workspace=None, stream=None):
-    """Trapezoidal Mamba-3 forward through ``ssd_trapezoidal_forward``; returns (y, final)."""
+                            return_final_state: bool = True, workspace=None, stream=None,
+                            valid_len=None):
+    """Trapezoidal Mamba-3 forward through ``ssd_trapezoidal_forward`` (the ``_varlen`` entry
+    point when ``valid_len`` [b] int64 is given); returns (y, final)."""
     return SSDTrapezoidalPlan(x, dA, B, C, gamma, beta, chunk_len=chunk_len, theta=theta,
                               prev_x=prev_x, prev_B=prev_B, init_state=init_state, y=y,
                               final_state=final_state, return_final_state=return_final_state,
-                              workspace=workspace, stream=stream)()
+                              workspace=workspace, stream=stream, valid_len=valid_len)()
 
 
 def ssd_quaternion_forward(x, dA, B, C, qcum, *, chunk_len: int, init_state=None, y=None,

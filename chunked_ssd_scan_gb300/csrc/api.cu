@@ -162,10 +162,15 @@ int32_t ssd_chunked_variant(const ssd_shape* shape) {
   return pick_variant(shape);
 }
 
-ssd_status ssd_chunked_forward(const ssd_shape* shape, const void* x, const float* dA,
-                               const void* B, const void* C, const float* theta,
-                               const float* init_state, void* y, float* final_state,
-                               void* workspace, size_t workspace_bytes, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// Both forward entry points; valid_len is null for ssd_chunked_forward.
+ssd_status chunked_forward(const ssd_shape* shape, const void* x, const float* dA, const void* B,
+                           const void* C, const float* theta, const int64_t* valid_len,
+                           const float* init_state, void* y, float* final_state, void* workspace,
+                           size_t workspace_bytes, void* stream) {
   const ssd_status sc = check_shape(shape);
   if (sc != SSD_OK) return sc;
   if (!x || !dA || !B || !C || !y) return SSD_ERR_INVALID_ARG;
@@ -203,6 +208,7 @@ ssd_status ssd_chunked_forward(const ssd_shape* shape, const void* x, const floa
   p.phi = theta ? reinterpret_cast<double*>(ws + lay.phi) : nullptr;
   p.phisum = theta ? reinterpret_cast<double*>(ws + lay.phisum) : nullptr;
   p.hdr = reinterpret_cast<WsHeader*>(ws);
+  p.valid_len = valid_len;
   cudaError_t e;
   const int32_t variant = pick_variant(shape);
   if (variant == SSD_VARIANT_TC_BF16) {
@@ -215,17 +221,44 @@ ssd_status ssd_chunked_forward(const ssd_shape* shape, const void* x, const floa
   return e == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
 }
 
+}  // namespace
+
+extern "C" {
+
+ssd_status ssd_chunked_forward(const ssd_shape* shape, const void* x, const float* dA,
+                               const void* B, const void* C, const float* theta,
+                               const float* init_state, void* y, float* final_state,
+                               void* workspace, size_t workspace_bytes, void* stream) {
+  return chunked_forward(shape, x, dA, B, C, theta, nullptr, init_state, y, final_state,
+                         workspace, workspace_bytes, stream);
+}
+
+ssd_status ssd_chunked_forward_varlen(const ssd_shape* shape, const void* x, const float* dA,
+                                      const void* B, const void* C, const float* theta,
+                                      const int64_t* valid_len, const float* init_state, void* y,
+                                      float* final_state, void* workspace,
+                                      size_t workspace_bytes, void* stream) {
+  if (!valid_len || reinterpret_cast<uintptr_t>(valid_len) % alignof(int64_t) != 0)
+    return SSD_ERR_INVALID_ARG;
+  return chunked_forward(shape, x, dA, B, C, theta, valid_len, init_state, y, final_state,
+                         workspace, workspace_bytes, stream);
+}
+
 size_t ssd_trapezoidal_workspace_bytes(const ssd_shape* shape) {
   if (check_trap_shape(shape) != SSD_OK) return 0;
   return trap_layout(shape).total;
 }
 
-ssd_status ssd_trapezoidal_forward(const ssd_shape* shape, const void* x, const float* dA,
-                                   const void* B, const void* C, const float* gamma,
-                                   const float* beta, const float* theta, const void* prev_x,
-                                   const void* prev_B, const float* init_state, void* y,
-                                   float* final_state, void* workspace, size_t workspace_bytes,
-                                   void* stream) {
+}  // extern "C"
+
+namespace {
+
+ssd_status trapezoidal_forward(const ssd_shape* shape, const void* x, const float* dA,
+                               const void* B, const void* C, const float* gamma,
+                               const float* beta, const float* theta, const void* prev_x,
+                               const void* prev_B, const int64_t* valid_len,
+                               const float* init_state, void* y, float* final_state,
+                               void* workspace, size_t workspace_bytes, void* stream) {
   const ssd_status sc = check_trap_shape(shape);
   if (sc != SSD_OK) return sc;
   if (!x || !dA || !B || !C || !gamma || !beta || !y) return SSD_ERR_INVALID_ARG;
@@ -266,6 +299,7 @@ ssd_status ssd_trapezoidal_forward(const ssd_shape* shape, const void* x, const 
   t.G2 = e.ngroups;
   t.P = shape->headdim;
   t.N = shape->dstate;
+  t.valid_len = valid_len;
   if (trap_expand(t, bf16, st) != cudaSuccess) return SSD_ERR_CUDA;
 
   GenericParams p;
@@ -292,10 +326,39 @@ ssd_status ssd_trapezoidal_forward(const ssd_shape* shape, const void* x, const 
   p.phi = theta ? reinterpret_cast<double*>(ws + lay.inner.phi) : nullptr;
   p.phisum = theta ? reinterpret_cast<double*>(ws + lay.inner.phisum) : nullptr;
   p.hdr = reinterpret_cast<WsHeader*>(ws);
+  p.valid_len = valid_len;
   const cudaError_t ce = pick_variant(&e) == SSD_VARIANT_TILED_F32 ? simt32_forward(p, st)
                                                                     : generic_forward(p, false, st);
   if (ce != cudaSuccess) return SSD_ERR_CUDA;
   return trap_compact(t, bf16, st) == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+ssd_status ssd_trapezoidal_forward(const ssd_shape* shape, const void* x, const float* dA,
+                                   const void* B, const void* C, const float* gamma,
+                                   const float* beta, const float* theta, const void* prev_x,
+                                   const void* prev_B, const float* init_state, void* y,
+                                   float* final_state, void* workspace, size_t workspace_bytes,
+                                   void* stream) {
+  return trapezoidal_forward(shape, x, dA, B, C, gamma, beta, theta, prev_x, prev_B, nullptr,
+                             init_state, y, final_state, workspace, workspace_bytes, stream);
+}
+
+ssd_status ssd_trapezoidal_forward_varlen(const ssd_shape* shape, const void* x,
+                                          const float* dA, const void* B, const void* C,
+                                          const float* gamma, const float* beta,
+                                          const float* theta, const void* prev_x,
+                                          const void* prev_B, const int64_t* valid_len,
+                                          const float* init_state, void* y, float* final_state,
+                                          void* workspace, size_t workspace_bytes,
+                                          void* stream) {
+  if (!valid_len || reinterpret_cast<uintptr_t>(valid_len) % alignof(int64_t) != 0)
+    return SSD_ERR_INVALID_ARG;
+  return trapezoidal_forward(shape, x, dA, B, C, gamma, beta, theta, prev_x, prev_B, valid_len,
+                             init_state, y, final_state, workspace, workspace_bytes, stream);
 }
 
 size_t selective_scan_workspace_bytes(int64_t batch, int64_t seqlen, int64_t d_model,

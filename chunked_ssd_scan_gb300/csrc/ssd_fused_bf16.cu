@@ -93,6 +93,12 @@ struct FusedArgs {
   const float* seg_init;   // [b*H*nseg][P][N] (segment 0 unused: it starts from init)
   float* seg_end;          // [b*H*nseg][P][N]
   float* seg_decay;        // [b*H*nseg]
+  // Per-sequence valid lengths [batch] (device, may be null): steps from valid_len[b] on are
+  // padding.  Tiles wholly inside it are not run (a segment past the end still runs one, so
+  // that it hands its state through); in the tile that straddles the end, K1 reads zero decay,
+  // the pad rows of x and B are zeroed in shared memory before any product reads them (so any
+  // pad contents, NaN included, stay out of the result) and y is stored for real rows only.
+  const int64_t* valid_len;
 };
 
 // The loop of a wait that did not complete at once, kept out of line: the kernels wait at many
@@ -177,7 +183,7 @@ __device__ __forceinline__ void mask_block(const TileInfo& ti, int cb, bool exac
 // publishes each tile's prefix sums and decay factors into a ring of kInfoSlots slots.
 __device__ __forceinline__ void k1_warp(const FusedArgs& a, TileInfo* info, uint64_t* info_ready,
                                         uint64_t* info_empty, volatile int* abort, int b, int h,
-                                        int tbase, int nt, int lane) {
+                                        int tbase, int nt, int Tb, int lane) {
   const int R = a.R, steps = a.steps;
   const int per = (steps + 31) / 32;                 // steps per lane (<= 4)
   const int beg = min(steps, lane * per), end = min(steps, beg + per);
@@ -186,7 +192,7 @@ __device__ __forceinline__ void k1_warp(const FusedArgs& a, TileInfo* info, uint
   auto load_tile = [&](int t) {
 #pragma unroll
     for (int k = 0; k < 4; ++k)
-      dnext[k] = (beg + k < end && (tbase + t) * steps + beg + k < a.T)
+      dnext[k] = (beg + k < end && (tbase + t) * steps + beg + k < Tb)
                      ? __ldg(dsrc + (size_t)(t * steps + beg + k) * a.H)
                      : 0.f;
   };
@@ -376,8 +382,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int g = h / (a.H / a.G);
   const int R = a.R;
   const int tbase = seg * a.seg_tiles;
-  const int nt = min(a.ntiles - tbase, a.seg_tiles);
   const int seg_row = tbase * kTileRows;
+  int Tb = a.T;   // real steps of the sequence
+  if (a.valid_len) {
+    const int64_t v = a.valid_len[b];
+    Tb = (int)(v < 0 ? 0 : (v > a.T ? a.T : v));
+  }
+  const int vrows = Tb * R;   // real fused rows of the sequence
+  const int nt = max(1, min(min(a.ntiles - tbase, a.seg_tiles),
+                            (vrows - seg_row + kTileRows - 1) / kTileRows));
+  // the out warps zero B's pad rows and, in the pre-pass, gate K3 on that
+  const bool zero_b = a.valid_len != nullptr;
   volatile int* abort = &s_abort;
 
   if (threadIdx.x == 0) {
@@ -405,7 +420,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars->yo_full, 1);
     mbar_init(&bars->s_full, 1);
     mbar_init(&bars->yo_go, 8);            // 4 state warps + 4 out warps
-    mbar_init(&bars->k3_go, kDxWarps + 4); // (dec o x) warps + 4 state warps
+    // (dec o x) warps + 4 state warps (+ 4 out warps zeroing B's pad rows in the pre-pass)
+    mbar_init(&bars->k3_go, kDxWarps + 4 + (kPre && zero_b ? 4 : 0));
     mbar_init(&bars->y_pre, 4);            // out warps
     mbar_init(&bars->drain, 1);
     fence_mbar_init();
@@ -591,7 +607,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (a.hdr) latch_error(a.hdr, SSD_ERR_TIMEOUT, 92);
     }
   } else if (warp == 2) {
-    k1_warp(a, info, bars->info_ready, bars->info_empty, abort, b, h, tbase, nt, lane);
+    k1_warp(a, info, bars->info_ready, bars->info_empty, abort, b, h, tbase, nt, Tb, lane);
   } else {
     const int q = warp & 3;                 // TMEM lane quarter == SM sub-partition
     const int i = q * 32 + lane;            // tile row / state row of this thread
@@ -611,12 +627,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!wait_bar(&bars->x_full[t % kXSlots], (t / kXSlots) & 1, abort, a.hdr, 46))
           return false;
         if (t >= 1 && !wait_bar(&bars->s_full, (t - 1) & 1, abort, a.hdr, 47)) return false;
-        const uint8_t* xs = smem + kOffX + (t % kXSlots) * kXBytes;
+        uint8_t* xs = smem + kOffX + (t % kXSlots) * kXBytes;
         uint8_t* dhi = smem + kOffDxHi;
         uint8_t* dlo = smem + kOffDxLo;
+        const int lim = vrows - (seg_row + t * kTileRows);   // rows from lim on are padding
 #pragma unroll 1
         for (int u = du.x; u < du.y; ++u) {
           const int row = (u >> 2) * 32 + lane, c0 = (u & 3) * 16;
+          if (row >= lim) {   // pad row: zero in x (for Yd) and in (dec o x)
+            const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+            const uint32_t o0 = sw128_off16(row, c0), o1 = sw128_off16(row, c0 + 8);
+            *reinterpret_cast<uint4*>(xs + o0) = z;
+            *reinterpret_cast<uint4*>(xs + o1) = z;
+            *reinterpret_cast<uint4*>(dhi + o0) = z;
+            *reinterpret_cast<uint4*>(dhi + o1) = z;
+            *reinterpret_cast<uint4*>(dlo + o0) = z;
+            *reinterpret_cast<uint4*>(dlo + o1) = z;
+            continue;
+          }
           const float wd =
               ex2_approx((ti.last_hi - ti.cum_hi[row]) + (ti.last_lo - ti.cum_lo[row]));
           const float2 w2 = make_float2(wd, wd);
@@ -770,6 +798,29 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     } else {
       // ---------------------------------------------------------------- out warps
+      // Row i of B_t zeroed when it is padding (both 64-column halves of the stage).
+      auto zero_b_pad = [&](int t) {
+        if (i < vrows - (seg_row + t * kTileRows)) return;
+        uint8_t* bs = smem + kOffB + (t & 1) * kBCBytes;
+        const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+        for (int blk = 0; blk < 2; ++blk)
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            *reinterpret_cast<uint4*>(bs + blk * (kBCBytes / 2) + sw128_off16(i, c * 8)) = z;
+      };
+      if constexpr (kPre) {
+        // K3_t waits for these warps once B_t's pad rows are zero; tile t is taken up only
+        // after K3_{t-1} completed, so no arrival runs a phase ahead
+        for (int t = 0; zero_b && t < nt; ++t) {
+          if (t >= 1 && !wait_bar(&bars->s_full, (t - 1) & 1, abort, a.hdr, 56)) break;
+          if (!wait_bar(&bars->b_full[t & 1], (t >> 1) & 1, abort, a.hdr, 57)) break;
+          zero_b_pad(t);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars->k3_go);
+        }
+      }
       if constexpr (!kPre) {   // the pre-pass has no output
         // Per tile: e^{cum_i} Yo_t into the y accumulator; C_{t+1} into TMEM once Yo_t has read
         // C_t; then y_t = the accumulator after Yd_t -> bf16 -> the tile's x slot -> TMA store.
@@ -796,12 +847,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_before();
           // CB_t also needs B_t: the MMA warp waits for both on cb_go
           if (!wait_bar(&bars->b_full[t & 1], (t >> 1) & 1, abort, a.hdr, 55)) return false;
+          if (zero_b && vrows - (seg_row + t * kTileRows) < kTileRows) {
+            zero_b_pad(t);
+            fence_proxy_async_smem();
+          }
           __syncwarp();
           if (lane == 0) mbar_arrive(&bars->cb_go);
           return true;
         };
         if (lane == 0) mbar_arrive(&bars->yo_go);   // no Yo to read before tile 0
-        int stored = 0;   // y stores issued by this warp (lane 0)
         // t = -1 only copies C_0
         for (int t = -1; t < nt; ++t) {
           if (t < 0) {
@@ -844,6 +898,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!wait_bar(&bars->yd_full, t & 1, abort, a.hdr, 53)) break;
           tc_fence_after();
           uint8_t* ys = smem + kOffX + (t % kXSlots) * kXBytes;   // x_t is no longer needed
+          // a quarter of whole real rows goes out by TMA from the slot; one that reaches the
+          // end of the real rows is stored row by row from registers (real rows only)
+          const int qrow = seg_row + t * kTileRows + q * 32;   // first fused row of the quarter
+          const int vq = vrows - qrow;
+          __nv_bfloat16* yrow = a.y + (((size_t)b * a.T * R + qrow + lane) * a.H + h) * kP;
   #pragma unroll
           for (int c = 0; c < kP; c += 32) {
             float vy[32];
@@ -853,22 +912,33 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t pk[16];
   #pragma unroll
             for (int k = 0; k < 16; ++k) pk[k] = pack_bf16(vy[2 * k], vy[2 * k + 1]);
+            if (vq >= 32) {
   #pragma unroll
-            for (int k = 0; k < 4; ++k)
-              *reinterpret_cast<uint4*>(ys + sw128_off16(i, c + 8 * k)) =
-                  make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
+              for (int k = 0; k < 4; ++k)
+                *reinterpret_cast<uint4*>(ys + sw128_off16(i, c + 8 * k)) =
+                    make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
+            } else if (lane < vq) {
+  #pragma unroll
+              for (int k = 0; k < 4; ++k)
+                *reinterpret_cast<uint4*>(yrow + c + 8 * k) =
+                    make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
+            }
           }
           tc_fence_before();
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
             mbar_arrive(&bars->info_empty[slot]);
-            tma_store_4d(&tm_y, ys + q * 4096, 0, h, seg_row + t * kTileRows + q * 32, b);
-            bulk_commit_group();
-            ++stored;
+            if (vq >= 32) {
+              tma_store_4d(&tm_y, ys + q * 4096, 0, h, qrow, b);
+              bulk_commit_group();
+            }
             // the store of the previous tile has read its slot: hand it back to the producer
-            if (stored >= 2) {
-              bulk_wait_group_read<1>();
+            if (t >= 1) {
+              if (vq >= 32)
+                bulk_wait_group_read<1>();
+              else
+                bulk_wait_group_read<0>();
               mbar_arrive(&bars->x_empty[(t - 1) % kXSlots]);
             }
           }
@@ -1061,6 +1131,7 @@ cudaError_t fused_bf16_forward(const GenericParams& p, cudaStream_t st) {
   a.final_state = p.final_state;
   a.y = static_cast<__nv_bfloat16*>(p.y);
   a.hdr = p.hdr;
+  a.valid_len = p.valid_len;
   a.T = (int32_t)p.T;
   a.R = (int32_t)p.R;
   a.H = (int32_t)p.H;

@@ -73,9 +73,10 @@ __device__ __forceinline__ float seg_exp(const float* hi, const float* lo, int i
   return expf((hi[i] - hi[j]) + (lo[i] - lo[j]));
 }
 
-// Real steps of chunk c (the last chunk may be short).
-__device__ __forceinline__ int chunk_steps(const GenericParams& p, int64_t c) {
-  return (int)min(p.l, p.T - c * p.l);
+// Real steps of chunk c of sequence b: the last chunk may be short, and with per-sequence valid
+// lengths the steps from valid_len[b] on are padding (none of them is read).
+__device__ __forceinline__ int chunk_steps(const GenericParams& p, int64_t b, int64_t c) {
+  return (int)max((int64_t)0, min(p.l, seq_steps(p, b) - c * p.l));
 }
 
 // x reduced to [-pi, pi] (fp64 in, fp32 out).
@@ -89,7 +90,7 @@ __device__ inline float reduce_two_pi(double a) {
 __device__ void chunk_angles(const GenericParams& p, int64_t b, int64_t c, int64_t h,
                              float* s_ang) {
   const int64_t K = p.N / 2;
-  const int nv = chunk_steps(p, c);
+  const int nv = chunk_steps(p, b, c);
   for (int64_t k = threadIdx.x; k < K; k += blockDim.x) {
     double acc = p.phi[((b * (p.nch + 1) + c) * p.H + h) * K + k];
     const float* th = p.theta + ((b * p.T + c * p.l) * p.H + h) * K + k;
@@ -105,7 +106,7 @@ template <typename T>
 __device__ void stage_bc_rows(const GenericParams& p, const T* __restrict__ src, int64_t b,
                               int64_t c, int64_t g, int64_t row0, int rows, const float* s_ang,
                               float* dst, int ld) {
-  const int64_t L = (int64_t)chunk_steps(p, c) * p.R;   // real rows of the chunk
+  const int64_t L = (int64_t)chunk_steps(p, b, c) * p.R;   // real rows of the chunk
   const int64_t N = p.N;
   const int64_t base = ((b * p.T + c * p.l) * p.R) * p.G + g;   // fused row 0, group g
   if (p.theta == nullptr) {
@@ -150,7 +151,7 @@ __global__ void __launch_bounds__(kPhiThreads) phi_chunk_sum_kernel(GenericParam
   for (int64_t k = threadIdx.x % 32; k < K; k += 32) {
     const float* th = p.theta + ((b * p.T + c * p.l) * p.H + h) * K + k;
     fp::DF s = {0.f, 0.f};
-    const int nv = chunk_steps(p, c);
+    const int nv = chunk_steps(p, b, c);
     for (int64_t t = 0; t < nv; ++t) s = fp::df_add(s, fp::DF{__ldg(th + t * p.H * K), 0.f});
     p.phisum[((b * p.nch + c) * p.H + h) * K + k] = (double)s.hi + (double)s.lo;
   }
@@ -200,7 +201,7 @@ __global__ void __launch_bounds__(kThreads) chunk_state_kernel(GenericParams p) 
   float* s_B = s_x + kStateRows * P;         // [kStateRows][N]
   float* s_ang = s_B + kStateRows * N;       // [l][N/2] when theta
 
-  const int Lv = chunk_steps(p, c) * R;     // real rows of the chunk
+  const int Lv = chunk_steps(p, b, c) * R;     // real rows of the chunk
   chunk_cumsum(p.dA + (b * p.T + c * p.l) * p.H + h, p.H, l, Lv / R, s_cum, s_lo);
   if (p.theta) chunk_angles(p, b, c, h, s_ang);
   __syncthreads();
@@ -321,7 +322,7 @@ __global__ void __launch_bounds__(kThreads) chunk_scan_kernel(GenericParams p) {
   float* s_M = s_x + kScanCols * P;                  // [kScanRows][kScanCols+1]
   float* s_ang = s_M + kScanRows * (kScanCols + 1);  // [l][N/2] when theta
 
-  const int Lv = chunk_steps(p, c) * R;     // real rows of the chunk
+  const int Lv = chunk_steps(p, b, c) * R;     // real rows of the chunk
   chunk_cumsum(p.dA + (b * p.T + c * p.l) * p.H + h, p.H, l, Lv / R, s_cum, s_lo);
   if (p.theta) chunk_angles(p, b, c, h, s_ang);
   __syncthreads();

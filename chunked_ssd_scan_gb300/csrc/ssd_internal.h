@@ -27,7 +27,19 @@ struct GenericParams {
   double* phi;      // [b, nch+1, H, N/2]: chunk-start angles (mod 2 pi); the last one is Phi_{T-1}
   double* phisum;   // [b, nch, H, N/2]: per-chunk angle sums
   WsHeader* hdr;
+  // Per-sequence valid lengths [batch] (device, may be null): steps t >= valid_len[b] are
+  // padding, read as zero decay, zero input and no turn; y there is not written.
+  const int64_t* valid_len;
 };
+
+#ifdef __CUDACC__
+// Real steps of sequence b: valid_len[b] clamped to [0, T], or T without valid lengths.
+__device__ __forceinline__ int64_t seq_steps(const GenericParams& p, int64_t b) {
+  if (p.valid_len == nullptr) return p.T;
+  const int64_t v = __ldg(p.valid_len + b);
+  return v < 0 ? 0 : (v > p.T ? p.T : v);
+}
+#endif
 
 size_t generic_state_smem(int64_t l, int64_t P, int64_t N, bool theta);
 size_t generic_scan_smem(int64_t l, int64_t P, int64_t N, bool theta);
@@ -51,6 +63,7 @@ struct TrapArgs {
   void* y;                                    // I/O dtype, R channels
   float *xh, *bh, *ch, *yh;                   // workspace: the expanded problem (fp32, 2R channels)
   int64_t batch, T, R, H, G, G2, P, N;        // G2: groups of the expanded B/C (H when theta)
+  const int64_t* valid_len;                   // [batch] device, or null (no padding)
 };
 cudaError_t trap_expand(const TrapArgs& a, bool bf16, cudaStream_t st);
 cudaError_t trap_compact(const TrapArgs& a, bool bf16, cudaStream_t st);

@@ -42,9 +42,9 @@ constexpr int kTileFloats = kT64 * kT64;
 // log2 of the rank (a power of two dividing 64): row i belongs to step i >> rank_shift.
 __device__ __forceinline__ int rank_shift(const GenericParams& p) { return __ffs((int)p.R) - 1; }
 
-// Real steps of chunk c (the last chunk may be short).
-__device__ __forceinline__ int steps64(const GenericParams& p, int64_t c) {
-  return (int)min(p.l, p.T - c * p.l);
+// Real steps of chunk c of sequence b (short last chunk; padding past valid_len[b] excluded).
+__device__ __forceinline__ int steps64(const GenericParams& p, int64_t b, int64_t c) {
+  return (int)max((int64_t)0, min(p.l, seq_steps(p, b) - c * p.l));
 }
 
 // log2-scaled double-float prefix sums of dA over steps [0, n) of a chunk, by warp 0 (steps at
@@ -86,7 +86,7 @@ __device__ void chunk_prefix64(const float* __restrict__ src, int64_t stride, in
 __device__ void issue_theta64(const GenericParams& p, int64_t b, int64_t c, int64_t h, int n,
                               float* ang) {
   const float* th = p.theta + ((b * p.T + c * p.l) * p.H + h) * kPairs64;
-  const int nv = steps64(p, c);
+  const int nv = steps64(p, b, c);
   for (int e = threadIdx.x; e < n * (kPairs64 / 4); e += blockDim.x) {
     const int t = e / (kPairs64 / 4), q = e % (kPairs64 / 4);
     const bool real = t < nv;
@@ -175,7 +175,7 @@ __device__ void stage_bc64(const GenericParams& p, const float* __restrict__ src
   const int tid = threadIdx.x;
   const int R = (int)p.R;
   const int64_t row0 = (b * p.T + c * p.l) * R;   // fused row of the chunk's first step
-  const int nvr = steps64(p, c) * R;              // real rows of the chunk
+  const int nvr = steps64(p, b, c) * R;              // real rows of the chunk
   if (!transpose) {
     // row-major: the 16 lanes of a half-warp read and write one row (coalesced loads,
     // conflict-free shared stores)
@@ -236,7 +236,7 @@ __device__ void stage_x64(const GenericParams& p, int64_t b, int64_t c, int64_t 
   const int ch = tid & 15;   // half-warps read and write whole rows
   const int R = (int)p.R;
   const int64_t row0 = (b * p.T + c * p.l) * R;
-  const int nvr = steps64(p, c) * R;
+  const int nvr = steps64(p, b, c) * R;
 #pragma unroll
   for (int r = 0; r < 4; ++r) {
     const int row = (tid >> 4) + 16 * r;
@@ -262,7 +262,7 @@ __device__ void issue_rows64(const GenericParams& p, int64_t b, int64_t c, int64
                              float* xs, float* bs) {
   const float* xsrc = static_cast<const float*>(p.x);
   const float* bsrc = static_cast<const float*>(p.B);
-  const int nvr = steps64(p, c) * (int)p.R;
+  const int nvr = steps64(p, b, c) * (int)p.R;
   const int64_t row0 = (b * p.T + c * p.l) * p.R;
   for (int e = threadIdx.x; e < kTileFloats / 4; e += kSimtThreads) {
     const int row = e / (kT64 / 4), q = e % (kT64 / 4);
@@ -287,7 +287,7 @@ __global__ void __launch_bounds__(kSimtThreads) simt_state_kernel(GenericParams 
   float* total = ang + (p.theta ? l * kPairs64 : 0);
   // the first block's raw rows are in flight while the prefix sums and the angles are formed
   issue_rows64(p, b, c, h, g, xs, bs);
-  chunk_prefix64(p.dA + (b * p.T + c * p.l) * p.H + h, p.H, l, steps64(p, c), cum_hi, cum_lo,
+  chunk_prefix64(p.dA + (b * p.T + c * p.l) * p.H + h, p.H, l, steps64(p, b, c), cum_hi, cum_lo,
                  total);
   if (p.theta) {
     chunk_angles64(p, b, c, h, l, ang);   // its wait covers the rows too
@@ -360,7 +360,7 @@ __global__ void __launch_bounds__(kSimtThreads, 3) simt_scan_kernel(GenericParam
   if (p.theta) issue_theta64(p, b, c, h, l, ang);
   {
     const float* xsrc = static_cast<const float*>(p.x);
-    const int nvr = steps64(p, c) * (int)p.R;
+    const int nvr = steps64(p, b, c) * (int)p.R;
     const int64_t row0 = (b * p.T + c * p.l) * p.R;
     for (int e = threadIdx.x; e < kTileFloats / 4; e += kSimtThreads) {
       const int row = e / (kT64 / 4), q = e % (kT64 / 4);
@@ -369,7 +369,7 @@ __global__ void __launch_bounds__(kSimtThreads, 3) simt_scan_kernel(GenericParam
                  xsrc + ((row0 + (real ? row : 0)) * p.H + h) * kT64 + 4 * q, real ? 16 : 0);
     }
   }
-  chunk_prefix64(p.dA + (b * p.T + c * p.l) * p.H + h, p.H, l, steps64(p, c), cum_hi, cum_lo,
+  chunk_prefix64(p.dA + (b * p.T + c * p.l) * p.H + h, p.H, l, steps64(p, b, c), cum_hi, cum_lo,
                  nullptr);
   {
     // h_in [p][n] (written over S by the state pass) -> h^T [n][p] with the 16-byte chunks of
@@ -437,7 +437,7 @@ __global__ void __launch_bounds__(kSimtThreads, 3) simt_scan_kernel(GenericParam
       block_product<true>(bt, xs, ty, tx, yd, kmax);   // Yd[i][p] += sum_j M[i][j] x[j][p]
       if (j0 < i0) __syncthreads();   // the next source tile overwrites B~^T / M^T and x
     }
-    const int nvr = steps64(p, c) * R;
+    const int nvr = steps64(p, b, c) * R;
     const int64_t row0 = (b * p.T + c * p.l) * R;
 #pragma unroll
     for (int r = 0; r < 4; ++r) {

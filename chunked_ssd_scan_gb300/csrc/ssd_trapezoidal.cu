@@ -27,6 +27,14 @@ namespace {
 // row's elements, so no index is recovered by division and the 32 lanes of a row are coalesced.
 constexpr int kRowLanes = 32, kRowsPerBlock = 8;
 
+// True if step t of sequence b is padding (t >= valid_len[b], clamped to [0, Tn]).
+__device__ __forceinline__ bool pad_step(const int64_t* valid_len, int64_t b, int64_t t,
+                                         int64_t Tn) {
+  if (valid_len == nullptr) return false;
+  const int64_t v = __ldg(valid_len + b);
+  return t >= (v < 0 ? 0 : (v > Tn ? Tn : v));
+}
+
 unsigned step_blocks(int64_t steps) {
   return (unsigned)(steps < 1 ? 1 : (steps > 0x7fffffff ? 0x7fffffff : steps));
 }
@@ -36,10 +44,11 @@ template <typename T>
 __global__ void __launch_bounds__(kRowLanes * kRowsPerBlock)
     trap_expand_x(const T* __restrict__ x, const float* __restrict__ gamma,
                   const float* __restrict__ beta, const T* __restrict__ prev_x,
-                  float* __restrict__ xh, int64_t batch, int64_t Tn, int64_t R, int64_t H,
-                  int64_t P) {
+                  float* __restrict__ xh, const int64_t* __restrict__ valid_len,
+                  int64_t batch, int64_t Tn, int64_t R, int64_t H, int64_t P) {
   for (int64_t bt = blockIdx.x; bt < batch * Tn; bt += gridDim.x) {
     const int64_t t = bt % Tn, b = bt / Tn;
+    if (pad_step(valid_len, b, t, Tn)) continue;   // padding: never read downstream
     for (int64_t m = 0; m < 2 * R; ++m) {
       for (int64_t h = threadIdx.y; h < H; h += kRowsPerBlock) {
         const T* src = nullptr;
@@ -69,12 +78,14 @@ template <typename T>
 __global__ void __launch_bounds__(kRowLanes * kRowsPerBlock)
     trap_expand_bc(const T* __restrict__ B, const T* __restrict__ C,
                    const float* __restrict__ theta, const T* __restrict__ prev_B,
-                   float* __restrict__ bh, float* __restrict__ ch, int64_t batch, int64_t Tn,
-                   int64_t R, int64_t H, int64_t G, int64_t G2, int64_t N) {
+                   float* __restrict__ bh, float* __restrict__ ch,
+                   const int64_t* __restrict__ valid_len, int64_t batch, int64_t Tn, int64_t R,
+                   int64_t H, int64_t G, int64_t G2, int64_t N) {
   const int64_t K = (N + 1) / 2;   // pairs (the last one single when N is odd, no theta)
   const int64_t hpg = H / G;
   for (int64_t bt = blockIdx.x; bt < batch * Tn; bt += gridDim.x) {
     const int64_t t = bt % Tn, b = bt / Tn;
+    if (pad_step(valid_len, b, t, Tn)) continue;
     for (int64_t m = 0; m < 2 * R; ++m) {
       for (int64_t g2 = threadIdx.y; g2 < G2; g2 += kRowsPerBlock) {
         const int64_t g = theta ? g2 / hpg : g2;
@@ -117,9 +128,11 @@ __global__ void __launch_bounds__(kRowLanes * kRowsPerBlock)
 // y[b,t,r,h,:] = y^[b,t,r,h,:] for the R real output channels (r < R of 2R).
 template <typename T>
 __global__ void __launch_bounds__(kRowLanes * kRowsPerBlock)
-    trap_compact_y(const float* __restrict__ yh, T* __restrict__ y, int64_t batch, int64_t Tn,
-                   int64_t R, int64_t H, int64_t P) {
+    trap_compact_y(const float* __restrict__ yh, T* __restrict__ y,
+                   const int64_t* __restrict__ valid_len, int64_t batch, int64_t Tn, int64_t R,
+                   int64_t H, int64_t P) {
   for (int64_t bt = blockIdx.x; bt < batch * Tn; bt += gridDim.x) {
+    if (pad_step(valid_len, bt / Tn, bt % Tn, Tn)) continue;   // y at padding is not written
     for (int64_t r = 0; r < R; ++r) {
       for (int64_t h = threadIdx.y; h < H; h += kRowsPerBlock) {
         const float* src = yh + ((bt * 2 * R + r) * H + h) * P;
@@ -135,19 +148,20 @@ cudaError_t expand_typed(const TrapArgs& a, cudaStream_t st) {
   const dim3 blk(kRowLanes, kRowsPerBlock);
   trap_expand_x<T><<<step_blocks(a.batch * a.T), blk, 0, st>>>(
       static_cast<const T*>(a.x), a.gamma, a.beta, static_cast<const T*>(a.prev_x), a.xh,
-      a.batch, a.T, a.R, a.H, a.P);
+      a.valid_len, a.batch, a.T, a.R, a.H, a.P);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   trap_expand_bc<T><<<step_blocks(a.batch * a.T), blk, 0, st>>>(
       static_cast<const T*>(a.B), static_cast<const T*>(a.C), a.theta,
-      static_cast<const T*>(a.prev_B), a.bh, a.ch, a.batch, a.T, a.R, a.H, a.G, a.G2, a.N);
+      static_cast<const T*>(a.prev_B), a.bh, a.ch, a.valid_len, a.batch, a.T, a.R, a.H, a.G,
+      a.G2, a.N);
   return cudaGetLastError();
 }
 
 template <typename T>
 cudaError_t compact_typed(const TrapArgs& a, cudaStream_t st) {
   trap_compact_y<T><<<step_blocks(a.batch * a.T), dim3(kRowLanes, kRowsPerBlock), 0,
-                      st>>>(a.yh, static_cast<T*>(a.y), a.batch, a.T, a.R, a.H, a.P);
+                      st>>>(a.yh, static_cast<T*>(a.y), a.valid_len, a.batch, a.T, a.R, a.H, a.P);
   return cudaGetLastError();
 }
 

@@ -119,6 +119,26 @@ ssd_status ssd_chunked_forward(const ssd_shape* shape, const void* x, const floa
                                const float* init_state, void* y, float* final_state,
                                void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * ssd_chunked_forward for sequences of different real lengths in one padded batch (moments.rs
+ * page: the valid-length mask of state_moments_phys and the pad rules of its module header).
+ * valid_len: device int64 [batch], 8-byte aligned, non-NULL; each value is read clamped to
+ * [0, seqlen].  Steps t >= valid_len[b] are padding and are treated as the page's zero pads:
+ * dA = 0 (identity decay), no write (x and B taken as zero), no rotation (theta taken as zero).
+ * So y at the real steps equals that of ssd_chunked_forward on the sequence cut at its length,
+ * final_state[b] is the state at step valid_len[b] - 1 (init_state when the length is 0), and
+ * y is not written at pad steps.  The inputs at pad steps may hold anything, NaN included:
+ * the CUDA-core kernels do not read them, and the tensor-core kernel, which loads whole tiles,
+ * zeroes the pad rows of x and B on chip before any product reads them.
+ * Other arguments, workspace size, asynchrony and errors as for ssd_chunked_forward (a NULL or
+ * misaligned valid_len is INVALID_ARG).
+ */
+ssd_status ssd_chunked_forward_varlen(const ssd_shape* shape, const void* x, const float* dA,
+                                      const void* B, const void* C, const float* theta,
+                                      const int64_t* valid_len, const float* init_state, void* y,
+                                      float* final_state, void* workspace,
+                                      size_t workspace_bytes, void* stream);
+
 /* Bytes of device workspace ssd_trapezoidal_forward needs for `shape` (0 if unsupported). */
 size_t ssd_trapezoidal_workspace_bytes(const ssd_shape* shape);
 
@@ -146,6 +166,23 @@ ssd_status ssd_trapezoidal_forward(const ssd_shape* shape, const void* x, const 
                                    const void* prev_B, const float* init_state, void* y,
                                    float* final_state, void* workspace, size_t workspace_bytes,
                                    void* stream);
+
+/*
+ * ssd_trapezoidal_forward with per-sequence valid lengths, under the rules of
+ * ssd_chunked_forward_varlen (moments.rs page: zero pads carry the state through unchanged;
+ * the chunk carry is read at the last real step).  Steps t >= valid_len[b] are padding: no
+ * decay, no gamma or beta write, no turn, no y written; final_state[b] is h at step
+ * valid_len[b] - 1.  Inputs at pad steps are not read.  Workspace, asynchrony and errors as for
+ * ssd_trapezoidal_forward.
+ */
+ssd_status ssd_trapezoidal_forward_varlen(const ssd_shape* shape, const void* x,
+                                          const float* dA, const void* B, const void* C,
+                                          const float* gamma, const float* beta,
+                                          const float* theta, const void* prev_x,
+                                          const void* prev_B, const int64_t* valid_len,
+                                          const float* init_state, void* y, float* final_state,
+                                          void* workspace, size_t workspace_bytes,
+                                          void* stream);
 
 /* Bytes of device workspace ssd_rotation_variant_forward needs (0 if unsupported/invalid). */
 size_t ssd_rotation_variant_workspace_bytes(const ssd_shape* shape, int64_t rope_dim,
