@@ -307,9 +307,10 @@ constexpr uint32_t kColC = 448;    // C: 128 bf16 of the state axis, two per col
 // The MMA warp waits on few barriers (a wait costs a few hundred cycles of latency even when its
 // phase has completed, and the issuing thread runs only a few MMAs ahead of the tensor core),
 // and tests each of them before issuing the product before it:
-//   yo_go(t)     state warps wrote h_t; out warps read Yo_{t-1}
+//   yo_go(t)     state warps wrote h_t; out warps read Yo_{t-1} and copied C_t into TMEM
 //   k3_go(t)     (dec o x)_t written; state warps read S_{t-1}
-//   cb_go(t)     C_t copied into TMEM and B_t landed (the out warps wait for both)
+//   c_full, b_full  CB_t reads C_t and B_t straight from shared memory (with valid lengths:
+//                cb_go(t), which the out warps arrive on once B_t's pad rows are zero)
 //   m_ready[b]   the mask of the tile in mask buffer b is in TMEM
 //   y_pre(t)     e^{cum_i} Yo_t written into the y accumulator (after y_{t-1} was read)
 // x_t needs no wait of its own: the (dec o x) warps waited for it before arriving on k3_go(t),
@@ -318,7 +319,7 @@ constexpr uint32_t kColC = 448;    // C: 128 bf16 of the state axis, two per col
 // issued) come in pairs, one per mask buffer.
 struct Bars {
   uint64_t x_full[kXSlots], x_empty[kXSlots], b_full[2], b_empty[2];
-  uint64_t c_full, c_empty, cb_go;
+  uint64_t c_full, cb_go;
   uint64_t info_ready[kInfoSlots], info_empty[kInfoSlots];
   uint64_t cb_full[2], m_ready[2], yd_full, yo_full, s_full;
   uint64_t yo_go, k3_go, y_pre, drain;
@@ -405,13 +406,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&bars->b_full[s], 1);
-      mbar_init(&bars->b_empty[s], 1);     // MMA commit after K3 (CB of the tile came before)
-      mbar_init(&bars->cb_full[s], 1);
+      mbar_init(&bars->b_empty[s], 1);     // a state warp once K3 of the tile is done
+      // CB_t done (MMA commit) and C_t held in TMEM (out warps): the mask may start and C_t's
+      // shared-memory slot is free
+      mbar_init(&bars->cb_full[s], 5);
       mbar_init(&bars->m_ready[s], kMaskWarps);
     }
     mbar_init(&bars->c_full, 1);
-    mbar_init(&bars->c_empty, 4);          // out warps, C row read into registers
-    mbar_init(&bars->cb_go, 4);            // out warps: C row in TMEM and B of the tile landed
+    mbar_init(&bars->cb_go, 4);            // out warps: B of the tile landed, pad rows zeroed
     for (int k = 0; k < kInfoSlots; ++k) {
       mbar_init(&bars->info_ready[k], 1);
       mbar_init(&bars->info_empty[k], kPre ? 4 : 8);   // state warps (and out warps)
@@ -449,7 +451,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int t = 0; t < nt; ++t) {
       const int row = seg_row + t * kTileRows;   // rows past the sequence's end read as zeros
       if (!kPre) {   // the pre-pass needs no C
-        if (t >= 1 && !wait_bar(&bars->c_empty, (t - 1) & 1, abort, a.hdr, 31)) break;
+        if (t >= 1 &&
+            !wait_bar(&bars->cb_full[(t - 1) & 1], ((t - 1) >> 1) & 1, abort, a.hdr, 31))
+          break;
         mbar_arrive_expect_tx_elect(&bars->c_full, kBCBytes);
         tma_load_4d_elect(smem + kOffC, &tm_c, &bars->c_full, 0, g, row, b);
         tma_load_4d_elect(smem + kOffC + kBCBytes / 2, &tm_c, &bars->c_full, 64, g, row, b);
@@ -509,6 +513,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t blo0 = sdesc_sw128_lo(smem_u32(smem + kOffB), 0);             // K-major
     const uint32_t bmlo0 = sdesc_sw128_lo(smem_u32(smem + kOffB), kBCBytes / 2);  // MN-major
     const uint32_t xlo0 = sdesc_sw128_lo(smem_u32(smem + kOffX), 0);
+    const uint32_t clo0 = sdesc_sw128_lo(smem_u32(smem + kOffC), 0);             // K-major
     const uint32_t tC = tmem + kColC;
     // A product's barrier is tested (non-blocking) before the previous product is issued; only
     // if that test failed does the warp block on it afterwards.
@@ -516,14 +521,30 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!probed && !wait_bar(bar, parity, abort, a.hdr, site)) return false;
       return true;
     };
+    // CB_t = C_t B_t^T with both operands K-major in shared memory (SS at N = 128 runs as fast
+    // as TS), so it waits only for the two TMA loads; C_t's slot is released by this commit and
+    // by the out warps once they hold C_t in TMEM for Yo_t
     auto issue_cb = [&](int t) {
       const uint32_t bl = blo0 + (t & 1) * (kBCBytes >> 4);
       const uint32_t dm = tmem + kColM + (t & 1) * 128;
 #pragma unroll
-      for (int ks = 0; ks < 8; ++ks)
-        mma_ts_we(dm, tC + ks * 8, bl + (((ks >> 2) * (kBCBytes / 2) + (ks & 3) * 32) >> 4), dhi,
-                  id_cb, ks > 0);
+      for (int ks = 0; ks < 8; ++ks) {
+        const uint32_t ko = ((ks >> 2) * (kBCBytes / 2) + (ks & 3) * 32) >> 4;
+        mma_ss_we(dm, clo0 + ko, dhi, bl + ko, dhi, id_cb, ks > 0);
+      }
       mma_commit_elect(&bars->cb_full[t & 1]);
+    };
+    // CB_t's inputs: probed without blocking, then waited for
+    auto probe_cb = [&](int t) -> uint32_t {
+      if (zero_b) return mbar_test_wait(&bars->cb_go, t & 1);
+      return mbar_test_wait(&bars->c_full, t & 1) &&
+             mbar_test_wait(&bars->b_full[t & 1], (t >> 1) & 1);
+    };
+    auto gate_cb = [&](uint32_t probed, int t) -> bool {
+      if (probed) return true;
+      if (zero_b) return wait_bar(&bars->cb_go, t & 1, abort, a.hdr, 35);
+      return wait_bar(&bars->c_full, t & 1, abort, a.hdr, 35) &&
+             wait_bar(&bars->b_full[t & 1], (t >> 1) & 1, abort, a.hdr, 37);
     };
     if constexpr (kPre) {
       // K3 only; B_t is waited for here (in the full pass the out warps wait for it)
@@ -539,11 +560,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     dxlo + (((ks < 8 ? 0u : kOffDxLo - kOffDxHi) + (ks & 7) * 2048) >> 4), dhi,
                     id_k3, ks > 0);
         mma_commit_elect(&bars->s_full);
-        mma_commit_elect(&bars->b_empty[sb]);
       }
     } else {
     uint32_t p_yo = mbar_test_wait(&bars->yo_go, 0);
-    bool ok = gate(0, &bars->cb_go, 0, 35);
+    bool ok = gate_cb(0, 0);
     if (ok) {
       tc_fence_after();
       issue_cb(0);
@@ -561,7 +581,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                   ks > 0);
       mma_commit_elect(&bars->yo_full);
       // K3_t = B_t^T [(dec o x)_hi ; (dec o x)_lo]
-      const uint32_t p_cb = t + 1 < nt ? mbar_test_wait(&bars->cb_go, (t + 1) & 1) : 1u;
+      const uint32_t p_cb = t + 1 < nt ? probe_cb(t + 1) : 1u;
       if (!gate(p_k3, &bars->k3_go, t & 1, 38)) break;
       tc_fence_after();
       {
@@ -573,12 +593,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     id_k3, ks > 0);
       }
       mma_commit_elect(&bars->s_full);
-      mma_commit_elect(&bars->b_empty[sb]);
       // CB of the next tile, into the other mask buffer
       const uint32_t p_m = mbar_test_wait(&bars->m_ready[sb], (t >> 1) & 1);
       const uint32_t p_pre = mbar_test_wait(&bars->y_pre, t & 1);
       if (t + 1 < nt) {
-        if (!gate(p_cb, &bars->cb_go, (t + 1) & 1, 35)) break;
+        if (!gate_cb(p_cb, t + 1)) break;
         tc_fence_after();
         issue_cb(t + 1);
       }
@@ -738,6 +757,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!wait_bar(&bars->info_ready[slot], (t / kInfoSlots) & 1, abort, a.hdr, 48)) break;
           if (!wait_bar(&bars->s_full, t & 1, abort, a.hdr, 49)) break;
           tc_fence_after();
+          if (warp == 8 && lane == 0) mbar_arrive(&bars->b_empty[t & 1]);   // K3_t read B_t
           const float e = info[slot].etile;
           const float2 e2 = make_float2(e, e);
           seg_decay *= e;
@@ -842,24 +862,26 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_st32u(tmem + lane_addr + kColC + blk * 32, w);
           }
           __syncwarp();
-          if (lane == 0) mbar_arrive(&bars->c_empty);
+          if (lane == 0) mbar_arrive(&bars->cb_full[t & 1]);
           tmem_st_wait();
           tc_fence_before();
-          // CB_t also needs B_t: the MMA warp waits for both on cb_go
-          if (!wait_bar(&bars->b_full[t & 1], (t >> 1) & 1, abort, a.hdr, 55)) return false;
-          if (zero_b && vrows - (seg_row + t * kTileRows) < kTileRows) {
-            zero_b_pad(t);
-            fence_proxy_async_smem();
+          if (zero_b) {   // CB_t waits for B_t's pad rows to be zero
+            if (!wait_bar(&bars->b_full[t & 1], (t >> 1) & 1, abort, a.hdr, 55)) return false;
+            if (vrows - (seg_row + t * kTileRows) < kTileRows) {
+              zero_b_pad(t);
+              fence_proxy_async_smem();
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->cb_go);
           }
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&bars->cb_go);
           return true;
         };
-        if (lane == 0) mbar_arrive(&bars->yo_go);   // no Yo to read before tile 0
-        // t = -1 only copies C_0
+        // t = -1 only copies C_0 (no Yo to read before tile 0)
         for (int t = -1; t < nt; ++t) {
           if (t < 0) {
             if (!copy_c(0)) break;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->yo_go);
             continue;
           }
           const int slot = t % kInfoSlots;
@@ -889,12 +911,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) {
-              mbar_arrive(&bars->y_pre);
-              if (t + 1 < nt) mbar_arrive(&bars->yo_go);   // Yo_t read
-            }
+            if (lane == 0) mbar_arrive(&bars->y_pre);
           }
-          if (t + 1 < nt && !copy_c(t + 1)) break;
+          if (t + 1 < nt) {   // Yo_t read and C_{t+1} in TMEM: Yo_{t+1} may go
+            if (!copy_c(t + 1)) break;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->yo_go);
+          }
           if (!wait_bar(&bars->yd_full, t & 1, abort, a.hdr, 53)) break;
           tc_fence_after();
           uint8_t* ys = smem + kOffX + (t % kXSlots) * kXBytes;   // x_t is no longer needed
