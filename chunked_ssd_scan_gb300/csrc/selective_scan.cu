@@ -25,6 +25,7 @@ namespace {
 constexpr int kSsThreads = 128;
 constexpr int64_t kSegLen = 64;
 
+
 template <int NB, bool kOutput>
 __global__ void __launch_bounds__(kSsThreads) ss_segment_kernel(SelectiveScanParams p) {
   const int64_t seg = blockIdx.x, b = blockIdx.z;
@@ -122,16 +123,24 @@ cudaError_t launch_nb(const SelectiveScanParams& p, cudaStream_t st) {
 // A warp owns 32 / LPC channels d of one batch row; the LPC lanes of a channel each carry SPL
 // of its N states, so every exp(delta * A) is evaluated on the special-function unit (2^x with
 // A pre-scaled by log2 e) and only segment boundary states go to memory.  T is cut into
-// segments (at least 256 steps) so that enough warps exist: a state-only pass gives each
+// segments (at least kSsMinSeg steps) so that enough warps exist: a state-only pass gives each
 // segment's end state from zero, a carry pass chains them, and the output pass runs each
 // segment from its true input state.  Every LPC steps the lanes of a channel sum their C . h
 // partials with a transpose-reduce (log2 LPC shuffle levels), after which lane l holds y of
 // step t0 + l.  The block's delta, u, B and C rows are staged through shared memory in a ring
-// of kSsStages stages of kSsSteps steps (16-byte cp.async, zero-filled past the segment and D).
+// of kSsStages stages of SsLayout::kSteps steps (16-byte cp.async, zero-filled past the segment
+// and D).
 // ------------------------------------------------------------------------------------------------
 constexpr int kSsWarps = 4;
-constexpr int kSsSteps = 16;
-constexpr int kSsStages = 2;
+// Steps per stage and stages in flight: short stages, four deep (measured on the 4 x 4096 x 512
+// x 16 workload: 8 x 4 beat 16 x 2 and 16 x 3 by about 15 %); a stage holds at least one step
+// per lane of a channel.
+constexpr int kSsStepsMin = 8;
+constexpr int kSsStages = 4;
+// Time segments: enough to give every SM this many blocks' worth of resident work (the scan is
+// latency bound, so more blocks than fit at once still help), each at least kSsMinSeg steps.
+constexpr int kSsWaveMult = 2;
+constexpr int64_t kSsMinSeg = 128;
 
 
 template <int SPL, int LPC>
@@ -139,8 +148,9 @@ struct SsLayout {
   static constexpr int kN = SPL * LPC;                   // d_state
   static constexpr int kCpw = 32 / LPC;                  // channels per warp
   static constexpr int kCpb = kCpw * kSsWarps;           // channels per block
-  static constexpr int kDtFloats = kSsSteps * kCpb;
-  static constexpr int kBFloats = kSsSteps * kN;
+  static constexpr int kSteps = LPC > kSsStepsMin ? LPC : kSsStepsMin;   // steps per stage
+  static constexpr int kDtFloats = kSteps * kCpb;
+  static constexpr int kBFloats = kSteps * kN;
   static constexpr int kStageFloats = 2 * kDtFloats + 2 * kBFloats;
   static constexpr size_t kSmemBytes = sizeof(float) * kStageFloats * kSsStages;
 };
@@ -204,6 +214,7 @@ __global__ void __launch_bounds__(32 * kSsWarps) ss_onepass_kernel(SelectiveScan
   const float sk = (dv && p.skip) ? p.skip[dd] : 0.f;
   const int64_t T = p.T, D = p.D;
   const int64_t t_beg = seg * p.seg_len, t_end = min(T, t_beg + p.seg_len);
+  constexpr int kSsSteps = Lay::kSteps;
   const int64_t nst = (t_end - t_beg + kSsSteps - 1) / kSsSteps;
 
   auto issue = [&](int64_t st) {
@@ -255,7 +266,7 @@ __global__ void __launch_bounds__(32 * kSsWarps) ss_onepass_kernel(SelectiveScan
     const float* sC = sm + 2 * Lay::kDtFloats + Lay::kBFloats + SPL * l;
     const int64_t t0 = t_beg + st * kSsSteps;
     if constexpr (!kOut) {
-#pragma unroll 16
+#pragma unroll
       for (int kk = 0; kk < kSsSteps; ++kk) {
         const float dt = sdt[kk * kCpb], uu = su[kk * kCpb];
         float bb[SPL];
@@ -364,10 +375,10 @@ cudaError_t launch_onepass(const SelectiveScanParams& p, cudaStream_t st) {
                                                           32 * kSsWarps, Lay::kSmemBytes)) !=
       cudaSuccess)
     return e;
-  int64_t nseg = std::max<int64_t>(1, (int64_t)sms * std::max(per_sm, 1) / groups);
-  nseg = std::max<int64_t>(1, std::min<int64_t>(nseg, p.T / 256));
+  int64_t nseg = std::max<int64_t>(1, (int64_t)sms * std::max(per_sm, 1) * kSsWaveMult / groups);
+  nseg = std::max<int64_t>(1, std::min<int64_t>(nseg, p.T / kSsMinSeg));
   int64_t seg_len = (p.T + nseg - 1) / nseg;
-  seg_len = (seg_len + kSsSteps - 1) / kSsSteps * kSsSteps;
+  seg_len = (seg_len + Lay::kSteps - 1) / Lay::kSteps * Lay::kSteps;
   SelectiveScanParams q = p;
   q.seg_len = seg_len;
   q.nseg = (p.T + seg_len - 1) / seg_len;   // <= ceil(T / 64): fits the workspace's segment arrays

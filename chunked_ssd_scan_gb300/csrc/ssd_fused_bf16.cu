@@ -33,9 +33,11 @@
 //
 // Time segments: with fewer sequences than SMs, each sequence is cut into segments run by
 // separate CTAs.  The same kernel in its state-only form (kPre: K1, dec o x, K3 and K4; no C,
-// CB, mask, Yd, Yo or output) gives each earlier segment's end state, fused_seg_carry_kernel
-// turns them into every segment's true initial state, and the full form then runs all segments
-// in parallel, writing every y once.
+// CB, mask, Yd, Yo or output) gives the end states of pieces of the sequence before its last
+// segment, fused_seg_carry_kernel chains them into every segment's true initial state, and the
+// full form then runs all segments in parallel, writing every y once.  The state-only pieces
+// are a whole number of times shorter than the segments, so that this pass, which costs about a
+// third of the full one per tile, still fills the SMs.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <math.h>
@@ -85,14 +87,15 @@ struct FusedArgs {
   WsHeader* hdr;
   int32_t T, R, H, G, ntiles, steps;   // steps = time steps per tile (128 / R)
   // Time segments: each (batch, head) sequence is cut into nseg segments of seg_tiles tiles
-  // (the last may be shorter), each run by its own CTA.  The state-only pre-pass writes the
-  // end state of every segment but the last (from the true initial state for segment 0, from
-  // zero otherwise) to seg_end and the segment's decay exp(sum dA) to seg_decay; a carry pass
-  // turns them into the true initial state of every segment (seg_init).
-  int32_t nseg, seg_tiles;
+  // (the last may be shorter), each run by its own CTA.  The state-only pre-pass cuts the
+  // tiles before the last segment into npre pieces of pre_tiles tiles (pre_tiles divides
+  // seg_tiles) and writes each piece's end state (from the true initial state for piece 0,
+  // from zero otherwise) to seg_end and its decay exp(sum dA) to seg_decay; a carry pass chains
+  // them into the true initial state of every segment (seg_init).
+  int32_t nseg, seg_tiles, npre, pre_tiles;
   const float* seg_init;   // [b*H*nseg][P][N] (segment 0 unused: it starts from init)
-  float* seg_end;          // [b*H*nseg][P][N]
-  float* seg_decay;        // [b*H*nseg]
+  float* seg_end;          // [b*H*npre][P][N]
+  float* seg_decay;        // [b*H*npre]
   // Per-sequence valid lengths [batch] (device, may be null): steps from valid_len[b] on are
   // padding.  Tiles wholly inside it are not run (a segment past the end still runs one, so
   // that it hands its state through); in the tile that straddles the end, K1 reads zero decay,
@@ -275,10 +278,10 @@ __device__ __forceinline__ void k1_warp(const FusedArgs& a, TileInfo* info, uint
 // The state recurrence never passes through the tensor core (K3 starts from zero).
 //
 // kPre = true is the state-only pre-pass of a sequence cut into time segments: per tile only
-// K1, (dec o x), K3 and the state step (no C, CB, mask, Yo, Yd or y).  Segment s (of the first
-// nseg - 1) runs from the true initial state when s = 0 and from zero otherwise, and writes its
-// end state and its decay product exp(sum dA); fused_seg_carry_kernel turns those into every
-// segment's true initial state for the full pass.
+// K1, (dec o x), K3 and the state step (no C, CB, mask, Yo, Yd or y).  Piece j (of the npre
+// pieces that cover the first nseg - 1 segments) runs from the true initial state when j = 0 and
+// from zero otherwise, and writes its end state and its decay product exp(sum dA);
+// fused_seg_carry_kernel turns those into every segment's true initial state for the full pass.
 // ============================================================================================
 
 constexpr int kThreads = 512;
@@ -376,13 +379,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = __shfl_sync(0xffffffffu, static_cast<int>(threadIdx.x / 32), 0);
   const int lane = threadIdx.x % 32;
-  const int nrun = kPre ? a.nseg - 1 : a.nseg;   // segments this launch runs per sequence
+  const int nrun = kPre ? a.npre : a.nseg;       // segments (pieces) run per sequence
   const int seq = blockIdx.x / nrun;             // (b, h)
   const int seg = blockIdx.x % nrun;
+  const int span = kPre ? a.pre_tiles : a.seg_tiles;
+  const int end_tile = kPre ? (a.nseg - 1) * a.seg_tiles : a.ntiles;
   const int b = seq / a.H, h = seq % a.H;
   const int g = h / (a.H / a.G);
   const int R = a.R;
-  const int tbase = seg * a.seg_tiles;
+  const int tbase = seg * span;
   const int seg_row = tbase * kTileRows;
   int Tb = a.T;   // real steps of the sequence
   if (a.valid_len) {
@@ -390,7 +395,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     Tb = (int)(v < 0 ? 0 : (v > a.T ? a.T : v));
   }
   const int vrows = Tb * R;   // real fused rows of the sequence
-  const int nt = max(1, min(min(a.ntiles - tbase, a.seg_tiles),
+  const int nt = max(1, min(min(end_tile - tbase, span),
                             (vrows - seg_row + kTileRows - 1) / kTileRows));
   // the out warps zero B's pad rows and, in the pre-pass, gate K3 on that
   const bool zero_b = a.valid_len != nullptr;
@@ -740,7 +745,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ---------------------------------------------------------------- state warps
       // Thread = state row n = i; h^T[n][0..63] in registers across the whole sequence.
       const size_t st_base = (size_t)seq * kP * kN;
-      const size_t seg_base = ((size_t)seq * a.nseg + seg) * kP * kN;
+      const size_t seg_base = ((size_t)seq * nrun + seg) * kP * kN;
       // initial state: the call's for segment 0; the carried one for later segments of the full
       // pass; zero for later segments of the pre-pass
       const float* init0 = seg == 0 ? (a.init ? a.init + st_base : nullptr)
@@ -810,7 +815,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!*abort) {
 #pragma unroll
           for (int p = 0; p < kP; ++p) a.seg_end[seg_base + (size_t)p * kN + i] = hv[p];
-          if (warp == 8 && lane == 0) a.seg_decay[(size_t)seq * a.nseg + seg] = seg_decay;
+          if (warp == 8 && lane == 0) a.seg_decay[(size_t)seq * nrun + seg] = seg_decay;
         }
       } else if (a.final_state && seg == a.nseg - 1 && !*abort) {
 #pragma unroll
@@ -1087,48 +1092,71 @@ cudaError_t ensure_smem_attribute() {
 }
 
 // True initial state of every segment after the first, one thread per (sequence, state element):
-// segment 0's pre-pass started from the true state, later ones from zero, so
-// h(1) = end_0 and h(s+1) = decay_s h(s) + end_s.
+// piece 0 of the pre-pass started from the true state, later ones from zero, so after piece j
+// h = end_0 (j = 0) or decay_j h + end_j; at the end of every per = seg_tiles / pre_tiles pieces
+// that is the initial state of the next segment.
 __global__ void fused_seg_carry_kernel(FusedArgs a, int64_t elems) {
   const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (idx >= elems) return;
   constexpr int64_t kPN = (int64_t)kP * kN;
   const int64_t seq = idx / kPN, e = idx % kPN;
   float* init = const_cast<float*>(a.seg_init);
+  const int per = a.seg_tiles / a.pre_tiles;   // pieces per segment
   float hcur = 0.f;
-  for (int s = 0; s + 1 < a.nseg; ++s) {
-    const float end = a.seg_end[(seq * a.nseg + s) * kPN + e];
-    hcur = s == 0 ? end : fmaf(a.seg_decay[seq * a.nseg + s], hcur, end);
-    init[(seq * a.nseg + s + 1) * kPN + e] = hcur;
+  for (int j = 0; j < a.npre; ++j) {
+    const float end = a.seg_end[(seq * a.npre + j) * kPN + e];
+    hcur = j == 0 ? end : fmaf(a.seg_decay[seq * a.npre + j], hcur, end);
+    if ((j + 1) % per == 0) init[(seq * a.nseg + (j + 1) / per) * kPN + e] = hcur;
   }
 }
 
 // Segments per sequence: enough CTAs to cover the SMs when there are fewer sequences than SMs
 // (each segment keeps at least four tiles).
-int fused_segments(int64_t batch, int64_t H, int64_t ntiles) {
+// Tiles of 128 fused rows per sequence (the last may be partial).
+int64_t fused_tiles(int64_t T, int64_t R) { return (T * R + kTileRows - 1) / kTileRows; }
+
+struct SegPlan {
+  int ntiles, nseg, seg_tiles, npre, pre_tiles;
+};
+
+// Segments per sequence: enough CTAs to cover the SMs when there are fewer sequences than SMs
+// (each segment keeps at least four tiles); then the state-only pieces: each segment before the
+// last is cut into the largest number k of equal pieces (k divides seg_tiles, each piece keeps
+// at least four tiles) with seqs * (nseg - 1) * k CTAs still within one wave.
+SegPlan fused_plan(int64_t batch, int64_t T, int64_t H, int64_t R) {
+  SegPlan pl;
+  pl.ntiles = (int)fused_tiles(T, R);
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-    return 1;
-  const int64_t seqs = batch * H;
-  int64_t n = sms / std::max<int64_t>(seqs, 1);
-  n = std::min<int64_t>(n, ntiles / 4);
+    sms = 1;
+  const int64_t seqs = std::max<int64_t>(batch * H, 1);
+  int64_t n = sms / seqs;
+  n = std::min<int64_t>(n, pl.ntiles / 4);
   n = std::min<int64_t>(n, 16);
-  return (int)std::max<int64_t>(n, 1);
+  pl.nseg = (int)std::max<int64_t>(n, 1);
+  pl.seg_tiles = (pl.ntiles + pl.nseg - 1) / pl.nseg;
+  pl.nseg = (pl.ntiles + pl.seg_tiles - 1) / pl.seg_tiles;   // no empty segment
+  int k = 1;
+  if (pl.nseg > 1) {
+    const int64_t pre_seqs = seqs * (pl.nseg - 1);
+    for (int c = 2; c <= 16; ++c)
+      if (pl.seg_tiles % c == 0 && pl.seg_tiles / c >= 4 && pre_seqs * c <= sms) k = c;
+  }
+  pl.pre_tiles = pl.seg_tiles / k;
+  pl.npre = (pl.nseg - 1) * k;
+  return pl;
 }
 
 }  // namespace
 
-// Tiles of 128 fused rows per sequence (the last may be partial).
-int64_t fused_tiles(int64_t T, int64_t R) { return (T * R + kTileRows - 1) / kTileRows; }
-
 size_t fused_bf16_workspace_bytes(int64_t batch, int64_t T, int64_t H, int64_t R) {
-  const int64_t ntiles = fused_tiles(T, R);
-  const int nseg = fused_segments(batch, H, ntiles);
+  const SegPlan pl = fused_plan(batch, T, H, R);
   size_t bytes = sizeof(WsHeader);
-  if (nseg > 1) {
-    const size_t seg_states = (size_t)batch * H * nseg * kP * kN;
-    bytes += 2 * seg_states * sizeof(float) + align_up((size_t)batch * H * nseg * sizeof(float), 256);
+  if (pl.nseg > 1) {
+    const size_t seqs = (size_t)batch * H;
+    bytes += seqs * (pl.nseg + pl.npre) * kP * kN * sizeof(float) +
+             align_up(seqs * pl.npre * sizeof(float), 256);
   }
   return bytes;
 }
@@ -1159,22 +1187,26 @@ cudaError_t fused_bf16_forward(const GenericParams& p, cudaStream_t st) {
   a.R = (int32_t)p.R;
   a.H = (int32_t)p.H;
   a.G = (int32_t)p.G;
-  a.ntiles = (int32_t)fused_tiles(p.T, p.R);
+  const SegPlan pl = fused_plan(p.batch, p.T, p.H, p.R);
+  a.ntiles = pl.ntiles;
   a.steps = steps;
-  a.nseg = fused_segments(p.batch, p.H, a.ntiles);
-  a.seg_tiles = (a.ntiles + a.nseg - 1) / a.nseg;
-  a.nseg = (a.ntiles + a.seg_tiles - 1) / a.seg_tiles;   // no empty segment
-  // workspace after the header: segment initial states, end states, decays
+  a.nseg = pl.nseg;
+  a.seg_tiles = pl.seg_tiles;
+  a.npre = pl.npre;
+  a.pre_tiles = pl.pre_tiles;
+  // workspace after the header: segment initial states, piece end states, piece decays
   char* ws = reinterpret_cast<char*>(p.hdr);
-  const size_t seg_states = (size_t)p.batch * p.H * a.nseg * kP * kN;
+  const size_t seqs_z = (size_t)p.batch * p.H;
+  const size_t init_bytes = seqs_z * a.nseg * kP * kN * sizeof(float);
+  const size_t end_bytes = seqs_z * a.npre * kP * kN * sizeof(float);
   a.seg_init = reinterpret_cast<const float*>(ws + sizeof(WsHeader));
-  a.seg_end = reinterpret_cast<float*>(ws + sizeof(WsHeader) + seg_states * sizeof(float));
-  a.seg_decay = reinterpret_cast<float*>(ws + sizeof(WsHeader) + 2 * seg_states * sizeof(float));
+  a.seg_end = reinterpret_cast<float*>(ws + sizeof(WsHeader) + init_bytes);
+  a.seg_decay = reinterpret_cast<float*>(ws + sizeof(WsHeader) + init_bytes + end_bytes);
   cudaError_t e = ensure_smem_attribute();
   if (e != cudaSuccess) return e;
   const unsigned seqs = (unsigned)(p.batch * p.H);
   if (a.nseg > 1) {
-    ssd_fused_bf16_kernel<true><<<seqs * (a.nseg - 1), kThreads, kSmem, st>>>(
+    ssd_fused_bf16_kernel<true><<<seqs * a.npre, kThreads, kSmem, st>>>(
         a, m->mx, m->mb, m->mc, m->my);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     const int64_t elems = (int64_t)seqs * kP * kN;
@@ -1187,7 +1219,7 @@ cudaError_t fused_bf16_forward(const GenericParams& p, cudaStream_t st) {
 }
 
 int fused_bf16_launches(int64_t batch, int64_t T, int64_t H, int64_t R) {
-  return fused_segments(batch, H, fused_tiles(T, R)) > 1 ? 3 : 1;
+  return fused_plan(batch, T, H, R).nseg > 1 ? 3 : 1;
 }
 
 }  // namespace ssd

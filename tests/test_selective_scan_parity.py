@@ -66,3 +66,19 @@ def test_worked_example_on_gpu():
     y = pkg.selective_scan_forward(t("u", (1, 4, 2)), t("delta", (1, 4, 2)), t("A", (2, 2)),
                                    t("B", (1, 4, 2)), t("C", (1, 4, 2)), t("skip", (2,)))
     np.testing.assert_allclose(y.cpu().numpy().reshape(-1), g["y"], atol=g["tolerance"][0] + 1e-6)
+
+
+def test_exponent_range_of_the_decay():
+    """Decay factors exp(delta A) from about e^-120 (underflowing to zero) up to nearly 1
+    (A from -20 to -0.5, delta doubled): every exponential over that range, on a problem whose
+    memory stays short enough for the fp32 recurrence to meet the gate."""
+    cfg = wl.SelectiveScanConfig("exp_range", 2, 700, 64, 16)
+    s = wl.make_selective_scan_inputs(cfg, seed=5)
+    g = torch.Generator().manual_seed(5)
+    s["A"] = -(torch.rand((cfg.d_model, cfg.d_state), generator=g) * 19.5 + 0.5)
+    s["delta"] = s["delta"] * 2.0
+    d = {k: v.cuda() for k, v in s.items()}
+    y = pkg.selective_scan_forward(d["u"], d["delta"], d["A"], d["B"], d["C"], d["skip"])
+    torch.cuda.synchronize()
+    ref = oracle.selective_scan(*(to_np(s[k]) for k in ("u", "delta", "A", "B", "C", "skip")))
+    check_close(to_np(y), ref, TOL, "exponent-range y")
