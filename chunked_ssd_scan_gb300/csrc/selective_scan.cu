@@ -176,7 +176,8 @@ __device__ __forceinline__ void ss_step(const float (&a)[SPL], float dt, float d
                                         const float (&bb)[SPL], float (&h)[SPL]) {
 #pragma unroll
   for (int j = 0; j < SPL; j += 2) {
-    const float2 e = make_float2(fp::ex2_approx(a[j] * dt), fp::ex2_approx(a[j + 1] * dt));
+    const float2 x = fp::mul2(make_float2(a[j], a[j + 1]), make_float2(dt, dt));
+    const float2 e = make_float2(fp::ex2_approx(x.x), fp::ex2_approx(x.y));
     const float2 r =
         fp::fma2(e, make_float2(h[j], h[j + 1]), fp::mul2(make_float2(du, du), make_float2(bb[j], bb[j + 1])));
     h[j] = r.x;
@@ -287,10 +288,12 @@ __global__ void __launch_bounds__(32 * kSsWarps) ss_onepass_kernel(SelectiveScan
           ld_states<SPL>(sB + kk * kN, bb);
           ld_states<SPL>(sC + kk * kN, cc);
           ss_step<SPL>(a, dt, dt * uu, bb, h);
-          float acc = cc[0] * h[0];
+          // C . h over the lane's states as paired products, the two halves added at the end
+          float2 acc = fp::mul2(make_float2(cc[0], cc[1]), make_float2(h[0], h[1]));
 #pragma unroll
-          for (int j = 1; j < SPL; ++j) acc = fmaf(cc[j], h[j], acc);
-          v[k] = acc;
+          for (int j = 2; j < SPL; j += 2)
+            acc = fp::fma2(make_float2(cc[j], cc[j + 1]), make_float2(h[j], h[j + 1]), acc);
+          v[k] = acc.x + acc.y;
         }
         // transpose-reduce over the LPC lanes of the channel: at the level with lane bit m
         // the lanes with that bit keep the upper half of their values, the others the lower
@@ -329,19 +332,24 @@ __global__ void __launch_bounds__(kSsThreads) ss_carry_states_kernel(SelectiveSc
   float* q = p.agg_h + ((b * p.nseg) * p.N + n) * p.D + d;
   const float* sd = p.agg_dt + (b * p.nseg) * p.D + d;
   float h = 0.f;
-  for (int64_t s0 = 0; s0 + 1 < p.nseg; s0 += 8) {   // loads eight segments ahead of the chain
-    float ev[8], dv[8];
+  // 32 segments per round: every load of the round is issued before the first is used and the
+  // decays are formed off the chain, so the serial part is one FMA per segment
+  constexpr int kRound = 32;
+  for (int64_t s0 = 0; s0 + 1 < p.nseg; s0 += kRound) {
+    float ev[kRound], dv[kRound];
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
+    for (int k = 0; k < kRound; ++k) {
       const bool in = s0 + k + 1 < p.nseg;
       ev[k] = in ? q[(s0 + k) * sstride] : 0.f;
       dv[k] = in ? sd[(s0 + k) * p.D] : 0.f;
     }
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
+    for (int k = 0; k < kRound; ++k) dv[k] = expf(a * dv[k]);
+#pragma unroll
+    for (int k = 0; k < kRound; ++k) {
       if (s0 + k + 1 < p.nseg) {
         q[(s0 + k) * sstride] = h;
-        h = expf(a * dv[k]) * h + ev[k];
+        h = dv[k] * h + ev[k];
       }
     }
   }
