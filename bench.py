@@ -47,8 +47,8 @@ ALU_FP32_TFLOPS = round(152 * 128 * 2 * 2.07e9 / 1e12, 1)
 # still held in L2 when the kernel ends are not counted.  Workloads without a capture report
 # null.
 NCU_TRAFFIC_BYTES = {
-    "mamba2_siso_bf16": 77_707_008 + 21_843_200,           # ssd_fused_bf16_kernel<false>
-    "mamba3_mimo_bf16": 1_353_165_824 + 253_219_328,       # ssd_fused_bf16_kernel<false>
+    "mamba2_siso_bf16": 77_673_216 + 27_691_520,           # ssd_fused_bf16_kernel<false>
+    "mamba3_mimo_bf16": 1_441_353_984 + 253_872_640,       # ssd_fused_bf16_kernel<false>
     "long_rotation_f32": 3_937_686_272 + 788_730_368,      # simt_scan_kernel
     "selective_scan_f32": 71_228_672 + 6_168_320,          # ss_onepass_kernel (output pass)
     # bwd_chunk_grad_kernel, captured at batch 1 and scaled by 4 (traffic grows with the batch)
