@@ -141,6 +141,8 @@ constexpr int kSsStages = 4;
 // latency bound, so more blocks than fit at once still help), each at least kSsMinSeg steps.
 constexpr int kSsWaveMult = 2;
 constexpr int64_t kSsMinSeg = 128;
+// the workspace holds ceil(T / kSegLen) segment states: segments may not be shorter
+static_assert(kSsMinSeg >= kSegLen, "segments shorter than the workspace's segment length");
 
 
 template <int SPL, int LPC>
