@@ -12,6 +12,7 @@
 
 #include <algorithm>
 
+#include <atomic>
 #include <mutex>
 
 #include "common.cuh"
@@ -190,33 +191,37 @@ __device__ __forceinline__ void ss_step(const float (&a)[SPL], float dt, float d
 // kOut = false: the segment's end state from a zero start and its summed delta (segments
 // 0 .. nseg-2; no C, no output).  kOut = true: the segment from its true input state (left in
 // agg_h by the carry pass) with y.  Lane l of a channel carries states SPL*l .. SPL*l+SPL-1.
+// Lane mapping of a block: a warp owns kCpw channels, lane l of a channel its states
+// SPL*l .. SPL*l+SPL-1.
+template <int SPL, int LPC>
+struct SsLane {
+  using Lay = SsLayout<SPL, LPC>;
+  int cl, l;       // channel within the block, lane within the channel
+  int64_t d, dd;   // channel (dd clamped to a valid one)
+  bool dv;         // d < D
+  __device__ SsLane(const SelectiveScanParams& p, int64_t d0) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    cl = warp * Lay::kCpw + lane / LPC;
+    l = lane % LPC;
+    d = d0 + cl;
+    dv = d < p.D;
+    dd = dv ? d : 0;
+  }
+};
+
+// Steps [t_beg, t_end) of batch row b for the block's channels d0 .. d0 + kCpb - 1, from the
+// state h (in registers; h is the end state afterwards).  kOut = false: state only, with the
+// summed delta of the lane's channel in sdt_sum.  kOut = true: y of every step too.
 template <int SPL, int LPC, bool kOut>
-__global__ void __launch_bounds__(32 * kSsWarps) ss_onepass_kernel(SelectiveScanParams p) {
+__device__ __forceinline__ void ss_segment(const SelectiveScanParams& p, int64_t b, int64_t d0,
+                                           const SsLane<SPL, LPC>& ln, int64_t t_beg,
+                                           int64_t t_end, const float (&a)[SPL], float sk,
+                                           float (&h)[SPL], float& sdt_sum) {
   using Lay = SsLayout<SPL, LPC>;
   constexpr int kN = Lay::kN, kCpb = Lay::kCpb;
   extern __shared__ __align__(16) float ss_sm[];
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int64_t groups = (p.D + kCpb - 1) / kCpb;
-  const int64_t nrun = kOut ? p.nseg : p.nseg - 1;      // segments this pass covers
-  const int64_t seg = blockIdx.x % nrun;
-  const int64_t bgrp = blockIdx.x / nrun;
-  const int64_t b = bgrp / groups;
-  const int64_t d0 = (bgrp % groups) * kCpb;
-  const int cl = warp * Lay::kCpw + lane / LPC;         // channel within the block
-  const int64_t d = d0 + cl;
-  const int l = lane % LPC;
-  const bool dv = d < p.D;
-  const int64_t dd = dv ? d : 0;
-  const float kLog2e = 1.4426950408889634f;
-  float a[SPL], h[SPL];
-#pragma unroll
-  for (int j = 0; j < SPL; ++j) {
-    a[j] = dv ? p.A[dd * kN + SPL * l + j] * kLog2e : 0.f;
-    h[j] = 0.f;
-  }
-  const float sk = (dv && p.skip) ? p.skip[dd] : 0.f;
   const int64_t T = p.T, D = p.D;
-  const int64_t t_beg = seg * p.seg_len, t_end = min(T, t_beg + p.seg_len);
+  const int cl = ln.cl, l = ln.l;
   constexpr int kSsSteps = Lay::kSteps;
   const int64_t nst = (t_end - t_beg + kSsSteps - 1) / kSsSteps;
 
@@ -249,13 +254,7 @@ __global__ void __launch_bounds__(32 * kSsWarps) ss_onepass_kernel(SelectiveScan
     if (s < nst) issue(s);
     cp_async_commit();
   }
-  float* yp = p.y + b * T * D + dd;
-  float* agg = p.agg_h + ((b * p.nseg + seg) * kN + SPL * l) * D + dd;   // [b, seg, n, d]
-  float sdt_sum = 0.f;
-  if (kOut && seg > 0 && dv) {   // segment-input state from the carry pass
-#pragma unroll
-    for (int j = 0; j < SPL; ++j) h[j] = agg[j * D];
-  }
+  float* yp = p.y + b * T * D + ln.dd;
 #pragma unroll 1
   for (int64_t st = 0; st < nst; ++st) {
     if (st + kSsStages - 1 < nst) issue(st + kSsStages - 1);
@@ -311,16 +310,177 @@ __global__ void __launch_bounds__(32 * kSsWarps) ss_onepass_kernel(SelectiveScan
           }
         }
         const int64_t t = t0 + k0 + l;
-        if (dv && t < t_end) yp[t * D] = fmaf(sk, su[(k0 + l) * kCpb], v[0]);   // + skip * u
+        if (ln.dv && t < t_end) yp[t * D] = fmaf(sk, su[(k0 + l) * kCpb], v[0]);   // + skip * u
       }
     }
     __syncthreads();   // the stage's buffer is refilled by a later issue
   }
-  if (!kOut && dv) {
+}
+
+// The lane's A row (pre-scaled by log2 e) and skip weight.
+template <int SPL, int LPC>
+__device__ __forceinline__ void ss_lane_params(const SelectiveScanParams& p,
+                                               const SsLane<SPL, LPC>& ln, float (&a)[SPL],
+                                               float& sk) {
+  constexpr int kN = SsLayout<SPL, LPC>::kN;
+  const float kLog2e = 1.4426950408889634f;
+#pragma unroll
+  for (int j = 0; j < SPL; ++j) a[j] = ln.dv ? p.A[ln.dd * kN + SPL * ln.l + j] * kLog2e : 0.f;
+  sk = (ln.dv && p.skip) ? p.skip[ln.dd] : 0.f;
+}
+
+template <int SPL, int LPC, bool kOut>
+__global__ void __launch_bounds__(32 * kSsWarps) ss_onepass_kernel(SelectiveScanParams p) {
+  using Lay = SsLayout<SPL, LPC>;
+  constexpr int kN = Lay::kN, kCpb = Lay::kCpb;
+  const int64_t groups = (p.D + kCpb - 1) / kCpb;
+  const int64_t nrun = kOut ? p.nseg : p.nseg - 1;      // segments this pass covers
+  const int64_t seg = blockIdx.x % nrun;
+  const int64_t bgrp = blockIdx.x / nrun;
+  const int64_t b = bgrp / groups;
+  const int64_t d0 = (bgrp % groups) * kCpb;
+  const SsLane<SPL, LPC> ln(p, d0);
+  const int64_t D = p.D;
+  float a[SPL], h[SPL], sk;
+  ss_lane_params(p, ln, a, sk);
+#pragma unroll
+  for (int j = 0; j < SPL; ++j) h[j] = 0.f;
+  const int64_t t_beg = seg * p.seg_len, t_end = min(p.T, t_beg + p.seg_len);
+  float* agg = p.agg_h + ((b * p.nseg + seg) * kN + SPL * ln.l) * D + ln.dd;   // [b, seg, n, d]
+  float sdt_sum = 0.f;
+  if (kOut && seg > 0 && ln.dv) {   // segment-input state from the carry pass
+#pragma unroll
+    for (int j = 0; j < SPL; ++j) h[j] = agg[j * D];
+  }
+  ss_segment<SPL, LPC, kOut>(p, b, d0, ln, t_beg, t_end, a, sk, h, sdt_sum);
+  if (!kOut && ln.dv) {
 #pragma unroll
     for (int j = 0; j < SPL; ++j) agg[j * D] = h[j];
-    if (l == 0) p.agg_dt[(b * p.nseg + seg) * D + dd] = sdt_sum;
+    if (ln.l == 0) p.agg_dt[(b * p.nseg + seg) * D + ln.dd] = sdt_sum;
   }
+}
+
+// ------------------------------------------------------------------------------------------------
+// The same scan in one cooperative launch with a decoupled look-back over time segments: every
+// block but the last segment's runs its segment state-only from zero and publishes that end
+// state (segment 0: the inclusive state itself), then finds its input state by walking back
+// over the published states of earlier segments until it meets an inclusive one
+// (h_in(s) = E_{s-1} + D_{s-1} (E_{s-2} + D_{s-2} ( ... I_j))), publishes its own inclusive
+// state I_s = D_s h_in(s) + E_s, and runs its segment again with the output.  All blocks are
+// resident at once (cooperative launch), and a block only waits for blocks of earlier segments,
+// which publish their end states without waiting for anything: every wait ends.  Each wait is
+// still bounded (1 s); one that gives up latches SSD_ERR_TIMEOUT and the block goes on from
+// what it has.
+// ------------------------------------------------------------------------------------------------
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// The state (1 = end state from zero, 2 = inclusive) a segment published in this call, or 0 if
+// nothing was published within the bound.
+__device__ int ss_wait_flag(const uint64_t* f, uint64_t epoch) {
+  const uint64_t t0 = global_ns();
+  for (;;) {
+    uint64_t v;
+    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(f) : "memory");
+    if ((v >> 2) == epoch) return (int)(v & 3u);
+    if (global_ns() - t0 > 1000000000ull) return 0;
+    __nanosleep(100);
+  }
+}
+
+__device__ __forceinline__ void ss_publish(uint64_t* f, uint64_t epoch, int state) {
+  const uint64_t v = epoch * 4 + (uint64_t)state;
+  asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(f), "l"(v) : "memory");
+}
+
+template <int SPL, int LPC>
+__global__ void __launch_bounds__(32 * kSsWarps) ss_lookback_kernel(SelectiveScanParams p) {
+  using Lay = SsLayout<SPL, LPC>;
+  constexpr int kN = Lay::kN, kCpb = Lay::kCpb;
+  __shared__ int s_state;
+  const int64_t groups = (p.D + kCpb - 1) / kCpb;
+  const int64_t seg = blockIdx.x % p.nseg;
+  const int64_t bgrp = blockIdx.x / p.nseg;
+  const int64_t b = bgrp / groups;
+  const int64_t d0 = (bgrp % groups) * kCpb;
+  const SsLane<SPL, LPC> ln(p, d0);
+  const int64_t D = p.D;
+  float a[SPL], h[SPL], sk;
+  ss_lane_params(p, ln, a, sk);
+  const int64_t t_beg = seg * p.seg_len, t_end = min(p.T, t_beg + p.seg_len);
+  const bool last = seg == p.nseg - 1;
+  // this lane's states of segment s in a [b, nseg, N, D] array
+  auto at = [&](float* base, int64_t s) {
+    return base + ((b * p.nseg + s) * kN + SPL * ln.l) * D + ln.dd;
+  };
+  uint64_t* flag = p.flags + bgrp * p.nseg;
+  float e_s[SPL], sdt = 0.f;
+  if (!last) {
+#pragma unroll
+    for (int j = 0; j < SPL; ++j) h[j] = 0.f;
+    ss_segment<SPL, LPC, false>(p, b, d0, ln, t_beg, t_end, a, sk, h, sdt);
+    float* dst = at(seg == 0 ? p.inc_h : p.agg_h, seg);
+#pragma unroll
+    for (int j = 0; j < SPL; ++j) {
+      e_s[j] = h[j];
+      if (ln.dv) dst[j * D] = h[j];
+    }
+    if (seg > 0 && ln.dv && ln.l == 0) p.agg_dt[(b * p.nseg + seg) * D + ln.dd] = sdt;
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) ss_publish(flag + seg, p.epoch, seg == 0 ? 2 : 1);
+  }
+  // input state of the segment
+  float hin[SPL];
+#pragma unroll
+  for (int j = 0; j < SPL; ++j) hin[j] = 0.f;
+  if (seg > 0) {
+    float acc[SPL], dec[SPL];
+#pragma unroll
+    for (int j = 0; j < SPL; ++j) {
+      acc[j] = 0.f;
+      dec[j] = 1.f;
+    }
+    for (int64_t s = seg - 1; s >= 0; --s) {
+      if (threadIdx.x == 0) s_state = ss_wait_flag(flag + s, p.epoch);
+      __syncthreads();
+      const int state = s_state;
+      __syncthreads();
+      if (state == 0) {   // gave up: latch and go on from the partial sum
+        if (threadIdx.x == 0 && p.hdr) latch_error(p.hdr, SSD_ERR_TIMEOUT, 300 + (int)(s & 63));
+#pragma unroll
+        for (int j = 0; j < SPL; ++j) hin[j] = acc[j];
+        break;
+      }
+      const float* src = at(state == 2 ? p.inc_h : p.agg_h, s);
+#pragma unroll
+      for (int j = 0; j < SPL; ++j) acc[j] = fmaf(dec[j], ln.dv ? __ldcg(src + j * D) : 0.f, acc[j]);
+      if (state == 2) {
+#pragma unroll
+        for (int j = 0; j < SPL; ++j) hin[j] = acc[j];
+        break;
+      }
+      const float sd = ln.dv ? __ldcg(p.agg_dt + (b * p.nseg + s) * D + ln.dd) : 0.f;
+#pragma unroll
+      for (int j = 0; j < SPL; ++j) dec[j] *= fp::ex2_approx(a[j] * sd);
+    }
+    if (!last) {   // the inclusive state of this segment for later ones
+      float* dst = at(p.inc_h, seg);
+#pragma unroll
+      for (int j = 0; j < SPL; ++j)
+        if (ln.dv) dst[j * D] = fmaf(fp::ex2_approx(a[j] * sdt), hin[j], e_s[j]);
+      __threadfence();
+      __syncthreads();
+      if (threadIdx.x == 0) ss_publish(flag + seg, p.epoch, 2);
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < SPL; ++j) h[j] = hin[j];
+  float unused = 0.f;
+  ss_segment<SPL, LPC, true>(p, b, d0, ln, t_beg, t_end, a, sk, h, unused);
 }
 
 // Segment-input states for the one-pass path, one thread per (b, state n, d): h_in(0) = 0,
@@ -358,8 +518,66 @@ __global__ void __launch_bounds__(kSsThreads) ss_carry_states_kernel(SelectiveSc
   q[(p.nseg - 1) * sstride] = h;
 }
 
+// Calls of the look-back form draw distinct epochs, so flags left in a workspace by an earlier
+// call never pass for this call's.
+std::atomic<uint64_t> g_ss_epoch{0};
+
+// One cooperative launch over as many segments as fit resident at once with the whole grid
+// (at least kSsMinSeg steps each); the look-back arrays live in the workspace's segment arrays,
+// which are sized for ceil(T / kSegLen) segments (p.nseg): inclusive states after the end
+// states, flags after the summed deltas.  Returns cudaErrorNotSupported (nothing launched) when
+// the form does not apply, and the caller runs the three-launch form.
+template <int SPL, int LPC>
+cudaError_t launch_lookback(const SelectiveScanParams& p, cudaStream_t st) {
+  using Lay = SsLayout<SPL, LPC>;
+  auto kern = ss_lookback_kernel<SPL, LPC>;
+  int dev = 0, sms = 0, coop = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev);
+  if (e != cudaSuccess) return e;
+  if (!coop) return cudaErrorNotSupported;
+  if (Lay::kSmemBytes > 48 * 1024 &&
+      (e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)Lay::kSmemBytes)) != cudaSuccess)
+    return e;
+  int per_sm = 0;
+  if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 32 * kSsWarps,
+                                                          Lay::kSmemBytes)) != cudaSuccess)
+    return e;
+  const int64_t bgroups = (p.D + Lay::kCpb - 1) / Lay::kCpb;   // channel blocks per batch row
+  const int64_t groups = p.batch * bgroups;
+  int64_t nseg = (int64_t)sms * per_sm / groups;
+  nseg = std::min<int64_t>(nseg, p.T / kSsMinSeg);
+  if (nseg < 2) return cudaErrorNotSupported;
+  int64_t seg_len = (p.T + nseg - 1) / nseg;
+  seg_len = (seg_len + Lay::kSteps - 1) / Lay::kSteps * Lay::kSteps;
+  nseg = (p.T + seg_len - 1) / seg_len;
+  // room in the workspace (p.nseg segments of end states and summed deltas)
+  const int64_t flags_floats = 2 * groups * nseg + 2;
+  if (2 * nseg > p.nseg || p.batch * nseg * p.D + flags_floats > p.batch * p.nseg * p.D)
+    return cudaErrorNotSupported;
+  SelectiveScanParams q = p;
+  q.seg_len = seg_len;
+  q.nseg = nseg;
+  q.inc_h = p.agg_h + p.batch * nseg * p.N * p.D;
+  const int64_t fo = (p.batch * nseg * p.D + 1) / 2 * 2;   // 8-byte aligned
+  q.flags = reinterpret_cast<uint64_t*>(p.agg_dt + fo);
+  q.epoch = g_ss_epoch.fetch_add(1, std::memory_order_relaxed) + 1;
+  void* args[] = {&q};
+  return cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(kern),
+                                     dim3((unsigned)(groups * nseg)), dim3(32 * kSsWarps), args,
+                                     Lay::kSmemBytes, st);
+}
+
 template <int SPL, int LPC>
 cudaError_t launch_onepass(const SelectiveScanParams& p, cudaStream_t st) {
+#ifndef SS_THREE_PASS
+  {
+    const cudaError_t e = launch_lookback<SPL, LPC>(p, st);
+    if (e != cudaErrorNotSupported) return e;
+  }
+#endif
   using Lay = SsLayout<SPL, LPC>;
   const int64_t groups = p.batch * ((p.D + Lay::kCpb - 1) / Lay::kCpb);
   // Segments of T (each at least 256 steps, a multiple of the staging step) until the output

@@ -82,6 +82,11 @@ struct SelectiveScanParams {
   float* agg_h;     // [b, nseg, N, D]: segment-local end states, then segment-input states
   float* agg_dt;    // [b, nseg, D]: summed delta per segment
   WsHeader* hdr;
+  // One-launch look-back form (set by its launcher): inclusive states [b, nseg, N, D] and one
+  // flag per (channel block, segment), tagged with the call's epoch.
+  float* inc_h;
+  uint64_t* flags;
+  uint64_t epoch;
 };
 
 int64_t ss_segment_length(int64_t T);
