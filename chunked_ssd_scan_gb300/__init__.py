@@ -17,7 +17,7 @@ from . import workloads  # noqa: F401  (seeded synthetic inputs; no scan arithme
 
 __all__ = [
     "SSDError", "load_library", "ssd_shape", "ssd_chunked_workspace_bytes", "ssd_chunked_variant",
-    "ssd_chunked_launches", "ssd_chunked_forward", "SSDForwardPlan", "SelectiveScanPlan",
+    "ssd_chunked_launches", "ssd_chunked_forward", "ssd_trapezoidal_variant", "SSDForwardPlan", "SelectiveScanPlan",
     "selective_scan_workspace_bytes", "selective_scan_forward", "ssd_trapezoidal_workspace_bytes",
     "ssd_trapezoidal_forward", "SSDTrapezoidalPlan", "ssd_rotation_variant_forward",
     "ssd_quaternion_forward",
@@ -77,6 +77,8 @@ def load_library(path: Optional[str] = None):
     lib.ssd_chunked_forward_varlen.argtypes = [SP] + [_VP] * 10 + [ctypes.c_size_t, _VP]
     lib.ssd_trapezoidal_workspace_bytes.restype = ctypes.c_size_t
     lib.ssd_trapezoidal_workspace_bytes.argtypes = [SP]
+    lib.ssd_trapezoidal_variant.restype = ctypes.c_int32
+    lib.ssd_trapezoidal_variant.argtypes = [SP]
     lib.ssd_trapezoidal_forward.restype = ctypes.c_int
     lib.ssd_trapezoidal_forward.argtypes = [SP] + [_VP] * 13 + [ctypes.c_size_t, _VP]
     lib.ssd_trapezoidal_forward_varlen.restype = ctypes.c_int
@@ -247,6 +249,10 @@ def ssd_chunked_forward(x: torch.Tensor, dA: torch.Tensor, B: torch.Tensor, C: t
 
 def ssd_trapezoidal_workspace_bytes(shape: ssd_shape) -> int:
     return int(load_library().ssd_trapezoidal_workspace_bytes(ctypes.byref(shape)))
+
+
+def ssd_trapezoidal_variant(shape: ssd_shape) -> str:
+    return VARIANTS.get(int(load_library().ssd_trapezoidal_variant(ctypes.byref(shape))), "none")
 
 
 class SSDTrapezoidalPlan:

@@ -105,12 +105,24 @@ ssd_shape trap_expanded(const ssd_shape* s) {
 struct TrapLayout {
   SsdLayout inner;   // the generic pipeline's buffers (offsets from the workspace start)
   size_t xh = 0, bh = 0, ch = 0, yh = 0, total = 0;
+  // the bf16 tensor-core form: the fused kernel's workspace first, then x^, B^, C^, w^, y^
+  bool fused = false;
+  size_t xq = 0, bq = 0, cq = 0, wq = 0, yq = 0;
 };
+
+// bf16 without rotation on a shape the fused kernel takes at 2R channels: the trapezoid runs
+// there, with gamma and beta as per-row write weights.
+bool trap_fused(const ssd_shape* s) {
+  return s->io_dtype == SSD_BF16 && !s->has_theta && s->mimo_rank <= 16 &&
+         fused_bf16_supported(s->seqlen, s->nheads, s->headdim, s->dstate, 2 * s->mimo_rank,
+                              s->chunk_len, true, false);
+}
 
 ssd_status check_trap_shape(const ssd_shape* s) {
   ssd_status st = check_shape(s);
   if (st != SSD_OK) return st;
   if (s->mimo_rank > (int64_t(1) << 30)) return SSD_ERR_UNSUPPORTED;
+  if (trap_fused(s)) return SSD_OK;
   const ssd_shape e = trap_expanded(s);
   if ((st = check_shape(&e)) != SSD_OK) return st;
   const int32_t v = pick_variant(&e);
@@ -118,8 +130,27 @@ ssd_status check_trap_shape(const ssd_shape* s) {
 }
 
 TrapLayout trap_layout(const ssd_shape* s) {
-  const ssd_shape e = trap_expanded(s);
   TrapLayout L;
+  if (trap_fused(s)) {
+    L.fused = true;
+    const size_t rows = (size_t)(s->batch * s->seqlen * 2 * s->mimo_rank);
+    size_t off = align_up(fused_bf16_workspace_bytes(s->batch, s->seqlen, s->nheads,
+                                                     2 * s->mimo_rank),
+                          kWsAlign);
+    L.xq = off;
+    off = align_up(off + 2 * rows * s->nheads * s->headdim, kWsAlign);
+    L.bq = off;
+    off = align_up(off + 2 * rows * s->ngroups * s->dstate, kWsAlign);
+    L.cq = off;
+    off = align_up(off + 2 * rows * s->ngroups * s->dstate, kWsAlign);
+    L.wq = off;
+    off = align_up(off + sizeof(float) * rows * s->nheads, kWsAlign);
+    L.yq = off;
+    off = align_up(off + 2 * rows * s->nheads * s->headdim, kWsAlign);
+    L.total = off;
+    return L;
+  }
+  const ssd_shape e = trap_expanded(s);
   L.inner = ssd_layout(&e);
   const size_t xs = sizeof(float) * (size_t)(e.batch * e.seqlen * e.mimo_rank * e.nheads * e.headdim);
   const size_t bs = sizeof(float) * (size_t)(e.batch * e.seqlen * e.mimo_rank * e.ngroups * e.dstate);
@@ -244,6 +275,13 @@ ssd_status ssd_chunked_forward_varlen(const ssd_shape* shape, const void* x, con
                          workspace, workspace_bytes, stream);
 }
 
+int32_t ssd_trapezoidal_variant(const ssd_shape* shape) {
+  if (check_trap_shape(shape) != SSD_OK) return SSD_VARIANT_NONE;
+  if (trap_fused(shape)) return SSD_VARIANT_TC_BF16;
+  const ssd_shape e = trap_expanded(shape);
+  return pick_variant(&e);
+}
+
 size_t ssd_trapezoidal_workspace_bytes(const ssd_shape* shape) {
   if (check_trap_shape(shape) != SSD_OK) return 0;
   return trap_layout(shape).total;
@@ -271,10 +309,60 @@ ssd_status trapezoidal_forward(const ssd_shape* shape, const void* x, const floa
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) % kWsAlign) != 0 ||
       workspace_bytes < lay.total)
     return SSD_ERR_WORKSPACE;
-  const ssd_shape e = trap_expanded(shape);
   char* ws = static_cast<char*>(workspace);
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
   const bool bf16 = shape->io_dtype == SSD_BF16;
+  if (lay.fused) {
+    if (!al16(prev_x) || !al16(prev_B)) return SSD_ERR_INVALID_ARG;   // copied as 16-byte words
+    TrapFusedArgs f;
+    memset(&f, 0, sizeof(f));
+    f.x = x;
+    f.B = B;
+    f.C = C;
+    f.prev_x = prev_x;
+    f.prev_B = prev_B;
+    f.gamma = gamma;
+    f.beta = beta;
+    f.y = y;
+    f.xq = ws + lay.xq;
+    f.bq = ws + lay.bq;
+    f.cq = ws + lay.cq;
+    f.wq = reinterpret_cast<float*>(ws + lay.wq);
+    f.yq = ws + lay.yq;
+    f.valid_len = valid_len;
+    f.batch = shape->batch;
+    f.T = shape->seqlen;
+    f.R = shape->mimo_rank;
+    f.H = shape->nheads;
+    f.G = shape->ngroups;
+    f.P = shape->headdim;
+    f.N = shape->dstate;
+    if (trap_fused_expand(f, st) != cudaSuccess) return SSD_ERR_CUDA;
+    GenericParams p;
+    memset(&p, 0, sizeof(p));
+    p.x = f.xq;
+    p.dA = dA;
+    p.B = f.bq;
+    p.C = f.cq;
+    p.init = init_state;
+    p.y = f.yq;
+    p.final_state = final_state;
+    p.batch = shape->batch;
+    p.T = shape->seqlen;
+    p.H = shape->nheads;
+    p.P = shape->headdim;
+    p.N = shape->dstate;
+    p.G = shape->ngroups;
+    p.R = 2 * shape->mimo_rank;
+    p.l = shape->chunk_len;
+    p.nch = (shape->seqlen + p.l - 1) / p.l;
+    p.hdr = reinterpret_cast<WsHeader*>(ws);
+    p.valid_len = valid_len;
+    p.wrow = f.wq;
+    if (fused_bf16_forward(p, st) != cudaSuccess) return SSD_ERR_CUDA;
+    return trap_fused_compact(f, st) == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
+  }
+  const ssd_shape e = trap_expanded(shape);
 
   TrapArgs t;
   memset(&t, 0, sizeof(t));

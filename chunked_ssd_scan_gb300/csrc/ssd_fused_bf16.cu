@@ -71,7 +71,9 @@ constexpr int kInfoSlots = 4;                             // K1 runs up to this 
 struct TileInfo {
   float cum_hi[kTileRows];   // log2-scaled prefix sum of dA at fused row j (hi part)
   float cum_lo[kTileRows];   // ... lo part
-  float qf[kTileRows];       // exp(cum_ref(block of j) - cum_j), cum_ref at the block's end
+  float qf[kTileRows];       // exp(cum_ref(block of j) - cum_j) (times w_j), cum_ref at the
+                             // block's end
+  float w[kTileRows];        // write weight of fused row j (with per-row weights only)
   float last_hi, last_lo;    // log2-scaled total of the tile
   float etile;               // exp(cum_last)
   int monotone;              // 1 if every dA of the tile is <= 0 (factorized mask is safe)
@@ -102,6 +104,11 @@ struct FusedArgs {
   // the pad rows of x and B are zeroed in shared memory before any product reads them (so any
   // pad contents, NaN included, stay out of the result) and y is stored for real rows only.
   const int64_t* valid_len;
+  // Per fused row write weights [b][T * R][H] (device, may be null): row i's write x_i (x) B_i
+  // enters the state and every later output scaled by w_i.  They are folded into the column
+  // factors of the mask and into (dec o x), so x and B stay exact bf16 operands (the
+  // trapezoidal form runs on this kernel this way, its gamma and beta as the weights).
+  const float* wrow;
 };
 
 // The loop of a wait that did not complete at once, kept out of line: the kernels wait at many
@@ -147,6 +154,7 @@ __device__ __forceinline__ void split2(float2 v, uint32_t& hi, uint32_t& lo) {
 // One 32-column block cb of the masked operand for the calling thread's row (w = its CB
 // values): below the diagonal block and with a monotone tile the factorized form
 // exp(cum_i - cum_ref) * qf_j, else one exponential per element with the causal cut at jlim.
+template <bool kW>
 __device__ __forceinline__ void mask_block(const TileInfo& ti, int cb, bool exact, float chi,
                                            float clo, int jlim, const float (&w)[32],
                                            uint32_t (&hi)[16], uint32_t (&lo)[16]) {
@@ -172,10 +180,15 @@ __device__ __forceinline__ void mask_block(const TileInfo& ti, int cb, bool exac
       const float2 e0 = add2(sub2(ch2, make_float2(ch.x, ch.y)), sub2(cl2, make_float2(cl.x, cl.y)));
       const float2 e1 = add2(sub2(ch2, make_float2(ch.z, ch.w)), sub2(cl2, make_float2(cl.z, cl.w)));
       // future columns (j >= jlim) are cut after the exponential, which may overflow there
-      const float2 l0 = make_float2(j < jlim ? ex2_approx(e0.x) : 0.f,
-                                    j + 1 < jlim ? ex2_approx(e0.y) : 0.f);
-      const float2 l1 = make_float2(j + 2 < jlim ? ex2_approx(e1.x) : 0.f,
-                                    j + 3 < jlim ? ex2_approx(e1.y) : 0.f);
+      float2 l0 = make_float2(j < jlim ? ex2_approx(e0.x) : 0.f,
+                              j + 1 < jlim ? ex2_approx(e0.y) : 0.f);
+      float2 l1 = make_float2(j + 2 < jlim ? ex2_approx(e1.x) : 0.f,
+                              j + 3 < jlim ? ex2_approx(e1.y) : 0.f);
+      if constexpr (kW) {   // the column's write weight
+        const float4 wj = *reinterpret_cast<const float4*>(&ti.w[j]);
+        l0 = mul2(l0, make_float2(wj.x, wj.y));
+        l1 = mul2(l1, make_float2(wj.z, wj.w));
+      }
       split2(mul2(make_float2(w[k], w[k + 1]), l0), hi[k / 2], lo[k / 2]);
       split2(mul2(make_float2(w[k + 2], w[k + 3]), l1), hi[k / 2 + 1], lo[k / 2 + 1]);
     }
@@ -184,6 +197,7 @@ __device__ __forceinline__ void mask_block(const TileInfo& ti, int cb, bool exac
 
 // K1 for one warp: reads dA straight from global memory (one tile ahead, into registers) and
 // publishes each tile's prefix sums and decay factors into a ring of kInfoSlots slots.
+template <bool kW>
 __device__ __forceinline__ void k1_warp(const FusedArgs& a, TileInfo* info, uint64_t* info_ready,
                                         uint64_t* info_empty, volatile int* abort, int b, int h,
                                         int tbase, int nt, int Tb, int lane) {
@@ -199,12 +213,28 @@ __device__ __forceinline__ void k1_warp(const FusedArgs& a, TileInfo* info, uint
                      ? __ldg(dsrc + (size_t)(t * steps + beg + k) * a.H)
                      : 0.f;
   };
+  // per-row write weights: rows lane + 32 k of the tile, one tile ahead
+  const float* wsrc = kW ? a.wrow + (size_t)b * a.T * R * a.H + h : nullptr;
+  float wnext[4], wcur[4];
+  auto load_w = [&](int t) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int row = (tbase + t) * kTileRows + lane + 32 * k;
+      wnext[k] = row < Tb * R ? __ldg(wsrc + (size_t)row * a.H) : 0.f;
+    }
+  };
   load_tile(0);
+  if constexpr (kW) load_w(0);
   for (int t = 0; t < nt; ++t) {
     float dcur[4];
 #pragma unroll
     for (int k = 0; k < 4; ++k) dcur[k] = dnext[k];
     if (t + 1 < nt) load_tile(t + 1);
+    if constexpr (kW) {
+#pragma unroll
+      for (int k = 0; k < 4; ++k) wcur[k] = wnext[k];
+      if (t + 1 < nt) load_w(t + 1);
+    }
     DF sum = {0.f, 0.f};
     int pos = 0;
 #pragma unroll
@@ -248,10 +278,21 @@ __device__ __forceinline__ void k1_warp(const FusedArgs& a, TileInfo* info, uint
     }
     __syncwarp();
     // qf of the rank-one blocks: the reference of column block c is its last fused row
+    if constexpr (kW) {   // times the column's write weight
 #pragma unroll
-    for (int e = lane; e < kTileRows; e += 32) {
-      const int ref = (e >> 5) * 32 + 31;
-      ti.qf[e] = ex2_approx((ti.cum_hi[ref] - ti.cum_hi[e]) + (ti.cum_lo[ref] - ti.cum_lo[e]));
+      for (int k = 0; k < 4; ++k) {
+        const int e = lane + 32 * k;
+        const int ref = (e >> 5) * 32 + 31;
+        ti.qf[e] = wcur[k] * ex2_approx((ti.cum_hi[ref] - ti.cum_hi[e]) +
+                                        (ti.cum_lo[ref] - ti.cum_lo[e]));
+        ti.w[e] = wcur[k];
+      }
+    } else {
+#pragma unroll
+      for (int e = lane; e < kTileRows; e += 32) {
+        const int ref = (e >> 5) * 32 + 31;
+        ti.qf[e] = ex2_approx((ti.cum_hi[ref] - ti.cum_hi[e]) + (ti.cum_lo[ref] - ti.cum_lo[e]));
+      }
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&info_ready[slot]);
@@ -360,7 +401,7 @@ __device__ __forceinline__ int2 dx_units(int warp) {
 }
 constexpr int kDxWarps = 4;
 
-template <bool kPre>
+template <bool kPre, bool kW>
 __global__ void __launch_bounds__(kThreads, 1)
     ssd_fused_bf16_kernel(FusedArgs a, const __grid_constant__ CUtensorMap tm_x,
                           const __grid_constant__ CUtensorMap tm_b,
@@ -631,7 +672,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (a.hdr) latch_error(a.hdr, SSD_ERR_TIMEOUT, 92);
     }
   } else if (warp == 2) {
-    k1_warp(a, info, bars->info_ready, bars->info_empty, abort, b, h, tbase, nt, Tb, lane);
+    k1_warp<kW>(a, info, bars->info_ready, bars->info_empty, abort, b, h, tbase, nt, Tb, lane);
   } else {
     const int q = warp & 3;                 // TMEM lane quarter == SM sub-partition
     const int i = q * 32 + lane;            // tile row / state row of this thread
@@ -669,8 +710,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             *reinterpret_cast<uint4*>(dlo + o1) = z;
             continue;
           }
-          const float wd =
-              ex2_approx((ti.last_hi - ti.cum_hi[row]) + (ti.last_lo - ti.cum_lo[row]));
+          float wd = ex2_approx((ti.last_hi - ti.cum_hi[row]) + (ti.last_lo - ti.cum_lo[row]));
+          if constexpr (kW) wd *= ti.w[row];
           const float2 w2 = make_float2(wd, wd);
           const uint32_t o0 = sw128_off16(row, c0), o1 = sw128_off16(row, c0 + 8);
           const uint4 v0 = *reinterpret_cast<const uint4*>(xs + o0);
@@ -712,7 +753,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld_wait();
           reg_tie(w);
           uint32_t hi[16], lo[16];
-          mask_block(ti, cb, cb == q || !fact_ok, chi, clo, jlim, w, hi, lo);
+          mask_block<kW>(ti, cb, cb == q || !fact_ok, chi, clo, jlim, w, hi, lo);
           tmem_st16u(mb + cb * 32, hi);
           tmem_st16u(mb + cb * 32 + 16, lo);
         }
@@ -1082,11 +1123,13 @@ cudaError_t ensure_smem_attribute() {
   if (e != cudaSuccess) return e;
   const uint64_t bit = dev < 64 ? (1ull << dev) : 0ull;
   if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
-  e = cudaFuncSetAttribute(ssd_fused_bf16_kernel<false>,
-                           cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(ssd_fused_bf16_kernel<true>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+  const void* kernels[] = {reinterpret_cast<const void*>(ssd_fused_bf16_kernel<false, false>),
+                           reinterpret_cast<const void*>(ssd_fused_bf16_kernel<true, false>),
+                           reinterpret_cast<const void*>(ssd_fused_bf16_kernel<false, true>),
+                           reinterpret_cast<const void*>(ssd_fused_bf16_kernel<true, true>)};
+  for (const void* k : kernels)
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
   if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_acq_rel);
   return e;
 }
@@ -1183,6 +1226,7 @@ cudaError_t fused_bf16_forward(const GenericParams& p, cudaStream_t st) {
   a.y = static_cast<__nv_bfloat16*>(p.y);
   a.hdr = p.hdr;
   a.valid_len = p.valid_len;
+  a.wrow = p.wrow;
   a.T = (int32_t)p.T;
   a.R = (int32_t)p.R;
   a.H = (int32_t)p.H;
@@ -1206,15 +1250,23 @@ cudaError_t fused_bf16_forward(const GenericParams& p, cudaStream_t st) {
   if (e != cudaSuccess) return e;
   const unsigned seqs = (unsigned)(p.batch * p.H);
   if (a.nseg > 1) {
-    ssd_fused_bf16_kernel<true><<<seqs * a.npre, kThreads, kSmem, st>>>(
-        a, m->mx, m->mb, m->mc, m->my);
+    if (a.wrow)
+      ssd_fused_bf16_kernel<true, true><<<seqs * a.npre, kThreads, kSmem, st>>>(
+          a, m->mx, m->mb, m->mc, m->my);
+    else
+      ssd_fused_bf16_kernel<true, false><<<seqs * a.npre, kThreads, kSmem, st>>>(
+          a, m->mx, m->mb, m->mc, m->my);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     const int64_t elems = (int64_t)seqs * kP * kN;
     fused_seg_carry_kernel<<<(unsigned)((elems + 255) / 256), 256, 0, st>>>(a, elems);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
-  ssd_fused_bf16_kernel<false><<<seqs * a.nseg, kThreads, kSmem, st>>>(a, m->mx, m->mb, m->mc,
-                                                                        m->my);
+  if (a.wrow)
+    ssd_fused_bf16_kernel<false, true><<<seqs * a.nseg, kThreads, kSmem, st>>>(
+        a, m->mx, m->mb, m->mc, m->my);
+  else
+    ssd_fused_bf16_kernel<false, false><<<seqs * a.nseg, kThreads, kSmem, st>>>(
+        a, m->mx, m->mb, m->mc, m->my);
   return cudaGetLastError();
 }
 

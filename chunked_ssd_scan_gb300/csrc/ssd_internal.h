@@ -30,6 +30,9 @@ struct GenericParams {
   // Per-sequence valid lengths [batch] (device, may be null): steps t >= valid_len[b] are
   // padding, read as zero decay, zero input and no turn; y there is not written.
   const int64_t* valid_len;
+  // Per fused row write weights [b, T*R, H] f32 (device, may be null; tensor-core kernel only):
+  // row i's write enters the state and every later output scaled by w_i.
+  const float* wrow;
 };
 
 #ifdef __CUDACC__
@@ -67,6 +70,21 @@ struct TrapArgs {
 };
 cudaError_t trap_expand(const TrapArgs& a, bool bf16, cudaStream_t st);
 cudaError_t trap_compact(const TrapArgs& a, bool bf16, cudaStream_t st);
+
+// Trapezoidal form on the bf16 tensor-core kernel (no theta): the 2R channels hold exact bf16
+// copies (x^ = [x_t, x_{t-1}], B^ = [B_t, B_{t-1}], C^ = [C_t, 0]) and gamma / beta become the
+// kernel's per-row write weights.
+struct TrapFusedArgs {
+  const void *x, *B, *C, *prev_x, *prev_B;   // bf16
+  const float *gamma, *beta;
+  void* y;                                    // bf16, R channels
+  void *xq, *bq, *cq, *yq;                    // workspace, bf16, 2R channels
+  float* wq;                                  // workspace [b, T, 2R, H]
+  const int64_t* valid_len;
+  int64_t batch, T, R, H, G, P, N;
+};
+cudaError_t trap_fused_expand(const TrapFusedArgs& a, cudaStream_t st);
+cudaError_t trap_fused_compact(const TrapFusedArgs& a, cudaStream_t st);
 
 // Selective scan.
 struct SelectiveScanParams {

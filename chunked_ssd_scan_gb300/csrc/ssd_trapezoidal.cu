@@ -165,7 +165,76 @@ cudaError_t compact_typed(const TrapArgs& a, cudaStream_t st) {
   return cudaGetLastError();
 }
 
+// Rows of 16-byte words: copy n words from src (zeros if src is null) to dst, lanes along the row.
+__device__ __forceinline__ void copy_row16(uint4* __restrict__ dst, const uint4* __restrict__ src,
+                                           int64_t n) {
+  for (int64_t k = threadIdx.x; k < n; k += kRowLanes)
+    dst[k] = src ? __ldg(src + k) : make_uint4(0u, 0u, 0u, 0u);
+}
+
+// x^, B^, C^ (exact bf16 copies) and the write weights w^ = [gamma_t, beta_t] of step (b, t).
+__global__ void __launch_bounds__(kRowLanes * kRowsPerBlock)
+    trap_fused_expand_kernel(TrapFusedArgs a) {
+  const int64_t Tn = a.T, R = a.R, R2 = 2 * a.R;
+  const int64_t xw = a.P / 8, bw = a.N / 8;   // 16-byte words per row
+  const uint4* x = static_cast<const uint4*>(a.x);
+  const uint4* B = static_cast<const uint4*>(a.B);
+  const uint4* C = static_cast<const uint4*>(a.C);
+  const uint4* px = static_cast<const uint4*>(a.prev_x);
+  const uint4* pB = static_cast<const uint4*>(a.prev_B);
+  uint4* xq = static_cast<uint4*>(a.xq);
+  uint4* bq = static_cast<uint4*>(a.bq);
+  uint4* cq = static_cast<uint4*>(a.cq);
+  for (int64_t bt = blockIdx.x; bt < a.batch * Tn; bt += gridDim.x) {
+    const int64_t t = bt % Tn, b = bt / Tn;
+    if (pad_step(a.valid_len, b, t, Tn)) continue;   // padding: never read downstream
+    for (int64_t m = 0; m < R2; ++m) {
+      const bool cur = m < R;
+      for (int64_t h = threadIdx.y; h < a.H; h += kRowsPerBlock) {
+        const uint4* src = cur ? x + ((bt * R + m) * a.H + h) * xw
+                               : (t > 0 ? x + (((bt - 1) * R + (m - R)) * a.H + h) * xw
+                                        : (px ? px + ((b * R + (m - R)) * a.H + h) * xw : nullptr));
+        copy_row16(xq + ((bt * R2 + m) * a.H + h) * xw, src, xw);
+        if (threadIdx.x == 0)
+          a.wq[(bt * R2 + m) * a.H + h] = cur ? a.gamma[bt * a.H + h] : a.beta[bt * a.H + h];
+      }
+      for (int64_t g = threadIdx.y; g < a.G; g += kRowsPerBlock) {
+        const uint4* bsrc = cur ? B + ((bt * R + m) * a.G + g) * bw
+                                : (t > 0 ? B + (((bt - 1) * R + (m - R)) * a.G + g) * bw
+                                         : (pB ? pB + ((b * R + (m - R)) * a.G + g) * bw : nullptr));
+        copy_row16(bq + ((bt * R2 + m) * a.G + g) * bw, bsrc, bw);
+        copy_row16(cq + ((bt * R2 + m) * a.G + g) * bw, cur ? C + ((bt * R + m) * a.G + g) * bw : nullptr,
+                   bw);
+      }
+    }
+  }
+}
+
+// y[b, t, r] = y^[b, t, r] for the R real output channels (bf16 rows copied as 16-byte words).
+__global__ void __launch_bounds__(kRowLanes * kRowsPerBlock)
+    trap_fused_compact_kernel(TrapFusedArgs a) {
+  const int64_t Tn = a.T, R = a.R, R2 = 2 * a.R, xw = a.P / 8;
+  const uint4* yq = static_cast<const uint4*>(a.yq);
+  uint4* y = static_cast<uint4*>(a.y);
+  for (int64_t bt = blockIdx.x; bt < a.batch * Tn; bt += gridDim.x) {
+    if (pad_step(a.valid_len, bt / Tn, bt % Tn, Tn)) continue;   // y at padding is not written
+    for (int64_t r = 0; r < R; ++r)
+      for (int64_t h = threadIdx.y; h < a.H; h += kRowsPerBlock)
+        copy_row16(y + ((bt * R + r) * a.H + h) * xw, yq + ((bt * R2 + r) * a.H + h) * xw, xw);
+  }
+}
+
 }  // namespace
+
+cudaError_t trap_fused_expand(const TrapFusedArgs& a, cudaStream_t st) {
+  trap_fused_expand_kernel<<<step_blocks(a.batch * a.T), dim3(kRowLanes, kRowsPerBlock), 0, st>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t trap_fused_compact(const TrapFusedArgs& a, cudaStream_t st) {
+  trap_fused_compact_kernel<<<step_blocks(a.batch * a.T), dim3(kRowLanes, kRowsPerBlock), 0, st>>>(a);
+  return cudaGetLastError();
+}
 
 cudaError_t trap_expand(const TrapArgs& a, bool bf16, cudaStream_t st) {
   return bf16 ? expand_typed<__nv_bfloat16>(a, st) : expand_typed<float>(a, st);

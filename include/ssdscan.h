@@ -143,6 +143,14 @@ ssd_status ssd_chunked_forward_varlen(const ssd_shape* shape, const void* x, con
 size_t ssd_trapezoidal_workspace_bytes(const ssd_shape* shape);
 
 /*
+ * Which kernel family ssd_trapezoidal_forward runs for `shape` (SSD_VARIANT_NONE if none):
+ * SSD_VARIANT_TC_BF16 for bf16 I/O without rotation when the fused tensor-core kernel takes the
+ * shape at 2·mimo_rank channels (P = 64, N = 128, 2R dividing 128 and at most 32, nheads % 4 = 0),
+ * otherwise the family of the fp32 2R-channel expansion (TILED_F32 or GENERIC).
+ */
+int32_t ssd_trapezoidal_variant(const ssd_shape* shape);
+
+/*
  * Trapezoidal Mamba-3 SSD forward (scan.py page, the trapezoidal forward; moments.rs page,
  * combined injections).  Per (batch b, head h), g = h / (H/G), with the step write
  * S_t = sum_r x[b,t,r,h,:] (outer) B[b,t,r,g,:]:
@@ -157,8 +165,13 @@ size_t ssd_trapezoidal_workspace_bytes(const ssd_shape* shape);
  * io_dtype; both or neither).  The shape is the caller's (R = mimo_rank output and write
  * channels); the library runs it as one scalar-decay scan with 2R write channels
  * (x^ = [gamma x_t, beta x_{t-1}], B^ = [B_t, Rot(theta_t) B_{t-1}]) built in fp32 in the
- * workspace, on the CUDA-core chunk pipeline.  Errors, asynchrony and the workspace header as
- * for ssd_chunked_forward; UNSUPPORTED when the expanded shape exceeds that pipeline's limits.
+ * workspace, on the CUDA-core chunk pipeline; for bf16 without rotation on a shape the fused
+ * tensor-core kernel takes (ssd_trapezoidal_variant), the 2R channels are exact bf16 copies
+ * (x^ = [x_t, x_{t-1}], B^ = [B_t, B_{t-1}], C^ = [C_t, 0]) and gamma, beta enter that kernel as
+ * per-row write weights, so no product of two inputs is rounded to bf16.  Errors, asynchrony
+ * and the workspace header as for ssd_chunked_forward; UNSUPPORTED when the expanded shape
+ * exceeds the kernels' limits.  With the tensor-core form prev_x and prev_B must be 16-byte
+ * aligned.
  */
 ssd_status ssd_trapezoidal_forward(const ssd_shape* shape, const void* x, const float* dA,
                                    const void* B, const void* C, const float* gamma,

@@ -42,7 +42,8 @@ def test_header_declares_the_abi():
                      "ssd_rotation_variant_forward", "ssd_rotation_variant_workspace_bytes",
                      "ssd_quaternion_forward", "ssd_quaternion_workspace_bytes",
                      "ssd_chunked_backward", "ssd_backward_workspace_bytes",
-                     "ssd_chunked_forward_varlen", "ssd_trapezoidal_forward_varlen"):
+                     "ssd_chunked_forward_varlen", "ssd_trapezoidal_forward_varlen",
+                     "ssd_trapezoidal_variant"):
         assert expected in names
 
 

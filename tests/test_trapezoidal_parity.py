@@ -18,7 +18,13 @@ CASES = [
     wl.SSDConfig("trap_bf16", 1, 256, 4, 64, 64, 64, 2, 2, "bf16", **T),
     wl.SSDConfig("trap_rot_bf16", 1, 190, 2, 32, 32, 64, 1, 1, "bf16", theta=True, **T),
     wl.TRAP_MIMO_ROT_F32.with_(seqlen=512),
+    # bf16 without rotation at P = 64, N = 128: the fused tensor-core kernel with gamma and beta
+    # as per-row write weights (ragged T; MIMO rank 4 with time segments and pre-pass pieces)
+    wl.SSDConfig("trap_fused_bf16", 2, 300, 4, 64, 128, 64, 2, 2, "bf16", **T),
+    wl.SSDConfig("trap_fused_mimo_bf16", 1, 1000, 4, 64, 128, 64, 4, 4, "bf16", **T),
 ]
+
+FUSED = {"trap_fused_bf16", "trap_fused_mimo_bf16"}
 
 
 @pytest.mark.parametrize("cfg", CASES, ids=lambda c: c.name)
@@ -26,6 +32,11 @@ CASES = [
 def test_trapezoidal_parity(cfg, variant):
     kw = dict(slow_decay=True, init_state=True) if variant == "slow_decay_init_prev" else {}
     inp = wl.make_trap_inputs(cfg, seed=21, prev=variant != "no_prev", **kw)
+    x, B = inp["x"], inp["B"]
+    shape = pkg.shape_of(x, B, cfg.chunk_len, inp["theta"] is not None)
+    want = "tc_bf16" if cfg.name in FUSED else ("tiled_f32", "generic")
+    got = pkg.ssd_trapezoidal_variant(shape)
+    assert got == want if isinstance(want, str) else got in want, (cfg.name, got)
     y, fin = gpu_trap(inp, cfg.chunk_len)
     yr, fr = oracle_trap(inp)
     check_close(y, yr, TOL[cfg.dtype], f"{cfg.name}/{variant} y")

@@ -50,6 +50,9 @@ TRAP_CASES = [
     (wl.SSDConfig("vl_trap_rot_f32", 3, 300, 4, 16, 32, 64, 2, 2, "f32", theta=True, **T),
      [300, 129, 0]),
     (wl.SSDConfig("vl_trap_bf16", 2, 256, 4, 64, 64, 64, 2, 2, "bf16", **T), [77, 256]),
+    # the tensor-core form of the trapezoid
+    (wl.SSDConfig("vl_trap_fused_bf16", 3, 300, 4, 64, 128, 64, 2, 2, "bf16", **T),
+     [300, 129, 1]),
 ]
 
 SSD_KEYS = ("x", "dA", "B", "C", "theta")
