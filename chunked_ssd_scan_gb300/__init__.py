@@ -30,7 +30,7 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libssdscan.so")
 
 STATUS = {0: "SSD_OK", 1: "SSD_ERR_INVALID_ARG", 2: "SSD_ERR_UNSUPPORTED", 3: "SSD_ERR_CUDA",
-          4: "SSD_ERR_WORKSPACE", 5: "SSD_ERR_TIMEOUT"}
+          4: "SSD_ERR_WORKSPACE", 5: "SSD_ERR_TIMEOUT", 6: "SSD_ERR_INDEX"}
 VARIANTS = {0: "none", 1: "generic", 2: "tc_bf16", 3: "tiled_f32"}
 SSD_F32, SSD_BF16 = 0, 1
 

@@ -337,6 +337,7 @@ ssd_status trapezoidal_forward(const ssd_shape* shape, const void* x, const floa
     f.G = shape->ngroups;
     f.P = shape->headdim;
     f.N = shape->dstate;
+    f.hdr = reinterpret_cast<WsHeader*>(ws);
     if (trap_fused_expand(f, st) != cudaSuccess) return SSD_ERR_CUDA;
     GenericParams p;
     memset(&p, 0, sizeof(p));
@@ -388,6 +389,7 @@ ssd_status trapezoidal_forward(const ssd_shape* shape, const void* x, const floa
   t.P = shape->headdim;
   t.N = shape->dstate;
   t.valid_len = valid_len;
+  t.hdr = reinterpret_cast<WsHeader*>(ws);
   if (trap_expand(t, bf16, st) != cudaSuccess) return SSD_ERR_CUDA;
 
   GenericParams p;
@@ -531,6 +533,7 @@ const char* ssd_status_string(ssd_status status) {
     case SSD_ERR_CUDA: return "SSD_ERR_CUDA";
     case SSD_ERR_WORKSPACE: return "SSD_ERR_WORKSPACE";
     case SSD_ERR_TIMEOUT: return "SSD_ERR_TIMEOUT";
+    case SSD_ERR_INDEX: return "SSD_ERR_INDEX";
   }
   return "SSD_ERR_UNKNOWN";
 }

@@ -11,15 +11,13 @@ namespace ssd {
 
 // ----------------------------------------------------------------------------------------------
 // Workspace header: the first 256 bytes of every workspace.  Kernels latch device-side errors
-// here instead of trapping, and the fused kernel keeps its work-ticket counters here.
+// here instead of trapping.
 // ----------------------------------------------------------------------------------------------
 struct WsHeader {
   int32_t error;     // 0 = ok, otherwise an ssd_status value latched by a kernel
   int32_t pad0;
   int64_t detail;    // kernel-specific detail word of the first latched error
-  uint32_t ticket;   // dynamic work-ticket counter (fused kernel)
-  uint32_t done;     // finished-CTA counter (fused kernel)
-  uint32_t reserved[58];
+  uint32_t reserved[60];
 };
 static_assert(sizeof(WsHeader) == 256, "workspace header must be 256 bytes");
 
@@ -33,6 +31,20 @@ __device__ inline void latch_error(WsHeader* hdr, int32_t code, int64_t detail) 
     hdr->detail = detail;
   }
 }
+
+// Index checks of the debug build (compiled with SSD_INDEX_CHECKS): an output access whose
+// element index lies outside its buffer is skipped and SSD_ERR_INDEX is latched with the
+// access's site number as detail.  In the normal build the check is the constant true.
+#ifdef SSD_INDEX_CHECKS
+__device__ inline bool index_ok(WsHeader* hdr, int64_t idx, int64_t extent, int site) {
+  if (idx >= 0 && idx < extent) return true;
+  if (hdr) latch_error(hdr, SSD_ERR_INDEX, site);
+  return false;
+}
+#define SSD_INDEX_OK(hdr, idx, extent, site) ::ssd::index_ok((hdr), (int64_t)(idx), (int64_t)(extent), (site))
+#else
+#define SSD_INDEX_OK(hdr, idx, extent, site) true
+#endif
 
 // Load one element of an I/O tensor as fp32.
 template <typename T>

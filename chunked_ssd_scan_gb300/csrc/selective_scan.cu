@@ -61,7 +61,7 @@ __global__ void __launch_bounds__(kSsThreads) ss_segment_kernel(SelectiveScanPar
           acc += __ldg(Ct + n) * h[n];
         }
       }
-      p.y[row * p.D + d] = acc + sk * uu;
+      if (SSD_INDEX_OK(p.hdr, row * p.D + d, p.batch * p.T * p.D, 30)) p.y[row * p.D + d] = acc + sk * uu;
     } else {
 #pragma unroll
       for (int n = 0; n < NB; ++n) {
@@ -72,8 +72,11 @@ __global__ void __launch_bounds__(kSsThreads) ss_segment_kernel(SelectiveScanPar
   if (!kOutput) {
 #pragma unroll
     for (int n = 0; n < NB; ++n)
-      if (n < N) p.agg_h[((b * p.nseg + seg) * p.N + n) * p.D + d] = h[n];
-    p.agg_dt[(b * p.nseg + seg) * p.D + d] = sdt;
+      if (n < N && SSD_INDEX_OK(p.hdr, ((b * p.nseg + seg) * p.N + n) * p.D + d,
+                                p.batch * p.nseg * p.N * p.D, 31))
+        p.agg_h[((b * p.nseg + seg) * p.N + n) * p.D + d] = h[n];
+    if (SSD_INDEX_OK(p.hdr, (b * p.nseg + seg) * p.D + d, p.batch * p.nseg * p.D, 32))
+      p.agg_dt[(b * p.nseg + seg) * p.D + d] = sdt;
   }
 }
 
@@ -96,7 +99,7 @@ __global__ void __launch_bounds__(kSsThreads) ss_carry_kernel(SelectiveScanParam
       if (n < N) {
         float* q = p.agg_h + ((b * p.nseg + s) * p.N + n) * p.D + d;
         const float end = *q;
-        *q = h[n];
+        if (SSD_INDEX_OK(p.hdr, q - p.agg_h, p.batch * p.nseg * p.N * p.D, 33)) *q = h[n];
         h[n] = expf(a[n] * sdt) * h[n] + end;
       }
     }
@@ -310,7 +313,8 @@ __device__ __forceinline__ void ss_segment(const SelectiveScanParams& p, int64_t
           }
         }
         const int64_t t = t0 + k0 + l;
-        if (ln.dv && t < t_end) yp[t * D] = fmaf(sk, su[(k0 + l) * kCpb], v[0]);   // + skip * u
+        if (ln.dv && t < t_end && SSD_INDEX_OK(p.hdr, (yp - p.y) + t * D, p.batch * T * D, 34))
+          yp[t * D] = fmaf(sk, su[(k0 + l) * kCpb], v[0]);   // + skip * u
       }
     }
     __syncthreads();   // the stage's buffer is refilled by a later issue
@@ -355,8 +359,12 @@ __global__ void __launch_bounds__(32 * kSsWarps) ss_onepass_kernel(SelectiveScan
   ss_segment<SPL, LPC, kOut>(p, b, d0, ln, t_beg, t_end, a, sk, h, sdt_sum);
   if (!kOut && ln.dv) {
 #pragma unroll
-    for (int j = 0; j < SPL; ++j) agg[j * D] = h[j];
-    if (ln.l == 0) p.agg_dt[(b * p.nseg + seg) * D + ln.dd] = sdt_sum;
+    for (int j = 0; j < SPL; ++j)
+      if (SSD_INDEX_OK(p.hdr, (agg - p.agg_h) + j * D, p.batch * p.nseg * kN * D, 35))
+        agg[j * D] = h[j];
+    if (ln.l == 0 &&
+        SSD_INDEX_OK(p.hdr, (b * p.nseg + seg) * D + ln.dd, p.batch * p.nseg * D, 36))
+      p.agg_dt[(b * p.nseg + seg) * D + ln.dd] = sdt_sum;
   }
 }
 
@@ -426,9 +434,12 @@ __global__ void __launch_bounds__(32 * kSsWarps) ss_lookback_kernel(SelectiveSca
 #pragma unroll
     for (int j = 0; j < SPL; ++j) {
       e_s[j] = h[j];
-      if (ln.dv) dst[j * D] = h[j];
+      if (ln.dv && SSD_INDEX_OK(p.hdr, (dst - p.agg_h) + j * D, 2 * p.batch * p.nseg * kN * D, 38))
+        dst[j * D] = h[j];
     }
-    if (seg > 0 && ln.dv && ln.l == 0) p.agg_dt[(b * p.nseg + seg) * D + ln.dd] = sdt;
+    if (seg > 0 && ln.dv && ln.l == 0 &&
+        SSD_INDEX_OK(p.hdr, (b * p.nseg + seg) * D + ln.dd, p.batch * p.nseg * D, 39))
+      p.agg_dt[(b * p.nseg + seg) * D + ln.dd] = sdt;
     __threadfence();
     __syncthreads();
     if (threadIdx.x == 0) ss_publish(flag + seg, p.epoch, seg == 0 ? 2 : 1);
@@ -471,7 +482,8 @@ __global__ void __launch_bounds__(32 * kSsWarps) ss_lookback_kernel(SelectiveSca
       float* dst = at(p.inc_h, seg);
 #pragma unroll
       for (int j = 0; j < SPL; ++j)
-        if (ln.dv) dst[j * D] = fmaf(fp::ex2_approx(a[j] * sdt), hin[j], e_s[j]);
+        if (ln.dv && SSD_INDEX_OK(p.hdr, (dst - p.agg_h) + j * D, 2 * p.batch * p.nseg * kN * D, 38))
+          dst[j * D] = fmaf(fp::ex2_approx(a[j] * sdt), hin[j], e_s[j]);
       __threadfence();
       __syncthreads();
       if (threadIdx.x == 0) ss_publish(flag + seg, p.epoch, 2);
@@ -510,12 +522,14 @@ __global__ void __launch_bounds__(kSsThreads) ss_carry_states_kernel(SelectiveSc
 #pragma unroll
     for (int k = 0; k < kRound; ++k) {
       if (s0 + k + 1 < p.nseg) {
-        q[(s0 + k) * sstride] = h;
+        if (SSD_INDEX_OK(p.hdr, (q - p.agg_h) + (s0 + k) * sstride, p.batch * p.nseg * p.N * p.D, 37))
+          q[(s0 + k) * sstride] = h;
         h = dv[k] * h + ev[k];
       }
     }
   }
-  q[(p.nseg - 1) * sstride] = h;
+  if (SSD_INDEX_OK(p.hdr, (q - p.agg_h) + (p.nseg - 1) * sstride, p.batch * p.nseg * p.N * p.D, 37))
+    q[(p.nseg - 1) * sstride] = h;
 }
 
 // Calls of the look-back form draw distinct epochs, so flags left in a workspace by an earlier

@@ -109,6 +109,8 @@ struct FusedArgs {
   // factors of the mask and into (dec o x), so x and B stay exact bf16 operands (the
   // trapezoidal form runs on this kernel this way, its gamma and beta as the weights).
   const float* wrow;
+  // element counts of the outputs (index checks of the debug build)
+  int64_t y_elems, st_elems, seqs;
 };
 
 // The loop of a wait that did not complete at once, kept out of line: the kernels wait at many
@@ -855,12 +857,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (kPre) {   // the segment's end state and decay for the carry pass
         if (!*abort) {
 #pragma unroll
-          for (int p = 0; p < kP; ++p) a.seg_end[seg_base + (size_t)p * kN + i] = hv[p];
-          if (warp == 8 && lane == 0) a.seg_decay[(size_t)seq * nrun + seg] = seg_decay;
+          for (int p = 0; p < kP; ++p)
+            if (SSD_INDEX_OK(a.hdr, seg_base + (size_t)p * kN + i, a.seqs * a.npre * kP * kN, 3))
+              a.seg_end[seg_base + (size_t)p * kN + i] = hv[p];
+          if (warp == 8 && lane == 0 &&
+              SSD_INDEX_OK(a.hdr, (size_t)seq * nrun + seg, a.seqs * a.npre, 4))
+            a.seg_decay[(size_t)seq * nrun + seg] = seg_decay;
         }
       } else if (a.final_state && seg == a.nseg - 1 && !*abort) {
 #pragma unroll
-        for (int p = 0; p < kP; ++p) a.final_state[st_base + (size_t)p * kN + i] = hv[p];
+        for (int p = 0; p < kP; ++p)
+          if (SSD_INDEX_OK(a.hdr, st_base + (size_t)p * kN + i, a.st_elems, 2))
+            a.final_state[st_base + (size_t)p * kN + i] = hv[p];
       }
     } else {
       // ---------------------------------------------------------------- out warps
@@ -989,6 +997,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             } else if (lane < vq) {
   #pragma unroll
               for (int k = 0; k < 4; ++k)
+                if (SSD_INDEX_OK(a.hdr, (yrow - a.y) + c + 8 * k + 7, a.y_elems, 1))
                 *reinterpret_cast<uint4*>(yrow + c + 8 * k) =
                     make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
             }
@@ -1149,7 +1158,8 @@ __global__ void fused_seg_carry_kernel(FusedArgs a, int64_t elems) {
   for (int j = 0; j < a.npre; ++j) {
     const float end = a.seg_end[(seq * a.npre + j) * kPN + e];
     hcur = j == 0 ? end : fmaf(a.seg_decay[seq * a.npre + j], hcur, end);
-    if ((j + 1) % per == 0) init[(seq * a.nseg + (j + 1) / per) * kPN + e] = hcur;
+    const int64_t o = (seq * a.nseg + (j + 1) / per) * kPN + e;
+    if ((j + 1) % per == 0 && SSD_INDEX_OK(a.hdr, o, a.seqs * a.nseg * kPN, 5)) init[o] = hcur;
   }
 }
 
@@ -1227,6 +1237,9 @@ cudaError_t fused_bf16_forward(const GenericParams& p, cudaStream_t st) {
   a.hdr = p.hdr;
   a.valid_len = p.valid_len;
   a.wrow = p.wrow;
+  a.seqs = p.batch * p.H;
+  a.y_elems = p.batch * p.T * p.R * p.H * p.P;
+  a.st_elems = a.seqs * p.P * p.N;
   a.T = (int32_t)p.T;
   a.R = (int32_t)p.R;
   a.H = (int32_t)p.H;

@@ -153,7 +153,9 @@ __global__ void __launch_bounds__(kPhiThreads) phi_chunk_sum_kernel(GenericParam
     fp::DF s = {0.f, 0.f};
     const int nv = chunk_steps(p, b, c);
     for (int64_t t = 0; t < nv; ++t) s = fp::df_add(s, fp::DF{__ldg(th + t * p.H * K), 0.f});
-    p.phisum[((b * p.nch + c) * p.H + h) * K + k] = (double)s.hi + (double)s.lo;
+    const int64_t o = ((b * p.nch + c) * p.H + h) * K + k;
+    if (SSD_INDEX_OK(p.hdr, o, p.batch * p.nch * p.H * K, 16))
+      p.phisum[o] = (double)s.hi + (double)s.lo;
   }
 }
 
@@ -180,11 +182,14 @@ __global__ void phi_prefix_kernel(GenericParams p) {
     if (lane >= off) incl += v;
   }
   double acc = incl - run;   // exclusive prefix of this lane's first chunk
+  const int64_t phi_elems = p.batch * (p.nch + 1) * p.H * K;
   for (int64_t c = c0; c < c1; ++c) {
-    dst[c * cs] = acc - kTwoPi * rint(acc * (1.0 / kTwoPi));
+    if (SSD_INDEX_OK(p.hdr, (dst - p.phi) + c * cs, phi_elems, 15))
+      dst[c * cs] = acc - kTwoPi * rint(acc * (1.0 / kTwoPi));
     acc += src[c * cs];
   }
-  if (lane == 31) dst[p.nch * cs] = incl - kTwoPi * rint(incl * (1.0 / kTwoPi));
+  if (lane == 31 && SSD_INDEX_OK(p.hdr, (dst - p.phi) + p.nch * cs, phi_elems, 15))
+    dst[p.nch * cs] = incl - kTwoPi * rint(incl * (1.0 / kTwoPi));
 }
 
 template <typename T, int OPT>
@@ -238,9 +243,12 @@ __global__ void __launch_bounds__(kThreads) chunk_state_kernel(GenericParams p) 
 #pragma unroll
   for (int k = 0; k < OPT; ++k) {
     const int o = threadIdx.x + k * kThreads;
-    if (o < P * N) dst[o] = acc[k];
+    if (o < P * N && SSD_INDEX_OK(p.hdr, (dst - p.states) + o, p.batch * p.nch * p.H * P * N, 10))
+      dst[o] = acc[k];
   }
-  if (threadIdx.x == 0) p.cend[(b * p.nch + c) * p.H + h] = cum_end;
+  if (threadIdx.x == 0 &&
+      SSD_INDEX_OK(p.hdr, (b * p.nch + c) * p.H + h, p.batch * p.nch * p.H, 11))
+    p.cend[(b * p.nch + c) * p.H + h] = cum_end;
 }
 
 // One thread carries one state element (or, with rotation, one interleaved pair) of one
@@ -280,7 +288,9 @@ __global__ void __launch_bounds__(kThreads) state_pass_kernel(GenericParams p) {
         const float a = expf(av[k]);
 #pragma unroll
         for (int w = 0; w < W; ++w) {
-          sp[(c0 + k) * cstride + w] = hv[w];
+          if (SSD_INDEX_OK(p.hdr, (sp - p.states) + (c0 + k) * cstride + w,
+                           p.batch * p.nch * p.H * PN, 12))
+            sp[(c0 + k) * cstride + w] = hv[w];
           hv[w] = a * hv[w] + sv[k][w];
         }
       }
@@ -298,7 +308,9 @@ __global__ void __launch_bounds__(kThreads) state_pass_kernel(GenericParams p) {
   }
   if (p.final_state) {
 #pragma unroll
-    for (int w = 0; w < W; ++w) p.final_state[(b * p.H + h) * PN + off + w] = hv[w];
+    for (int w = 0; w < W; ++w)
+      if (SSD_INDEX_OK(p.hdr, (b * p.H + h) * PN + off + w, p.batch * p.H * PN, 13))
+        p.final_state[(b * p.H + h) * PN + off + w] = hv[w];
   }
 }
 
@@ -390,7 +402,8 @@ __global__ void __launch_bounds__(kThreads) chunk_scan_kernel(GenericParams p) {
 #pragma unroll
     for (int k = 0; k < PPT; ++k) {
       const int pp = pg + 4 * k;
-      if (pp < P) st_from_f32(yrow + pp, acc[k]);
+      if (pp < P && SSD_INDEX_OK(p.hdr, (yrow - ys) + pp, p.batch * p.T * p.R * p.H * p.P, 14))
+        st_from_f32(yrow + pp, acc[k]);
     }
   }
 }

@@ -67,6 +67,7 @@ struct TrapArgs {
   float *xh, *bh, *ch, *yh;                   // workspace: the expanded problem (fp32, 2R channels)
   int64_t batch, T, R, H, G, G2, P, N;        // G2: groups of the expanded B/C (H when theta)
   const int64_t* valid_len;                   // [batch] device, or null (no padding)
+  WsHeader* hdr;                              // error word (index checks of the debug build)
 };
 cudaError_t trap_expand(const TrapArgs& a, bool bf16, cudaStream_t st);
 cudaError_t trap_compact(const TrapArgs& a, bool bf16, cudaStream_t st);
@@ -82,6 +83,7 @@ struct TrapFusedArgs {
   float* wq;                                  // workspace [b, T, 2R, H]
   const int64_t* valid_len;
   int64_t batch, T, R, H, G, P, N;
+  WsHeader* hdr;
 };
 cudaError_t trap_fused_expand(const TrapFusedArgs& a, cudaStream_t st);
 cudaError_t trap_fused_compact(const TrapFusedArgs& a, cudaStream_t st);

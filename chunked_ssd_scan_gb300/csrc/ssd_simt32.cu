@@ -332,9 +332,13 @@ __global__ void __launch_bounds__(kSimtThreads) simt_state_kernel(GenericParams 
   float* dst = p.states + ((b * p.nch + c) * p.H + h) * kTileFloats;
 #pragma unroll
   for (int r = 0; r < 4; ++r)
-    *reinterpret_cast<float4*>(dst + (4 * ty + r) * kT64 + 4 * tx) =
-        make_float4(acc[r][0], acc[r][1], acc[r][2], acc[r][3]);
-  if (threadIdx.x == 0) p.cend[(b * p.nch + c) * p.H + h] = *total;
+    if (SSD_INDEX_OK(p.hdr, (dst - p.states) + (4 * ty + r) * kT64 + 4 * tx + 3,
+                     p.batch * p.nch * p.H * kTileFloats, 20))
+      *reinterpret_cast<float4*>(dst + (4 * ty + r) * kT64 + 4 * tx) =
+          make_float4(acc[r][0], acc[r][1], acc[r][2], acc[r][3]);
+  if (threadIdx.x == 0 &&
+      SSD_INDEX_OK(p.hdr, (b * p.nch + c) * p.H + h, p.batch * p.nch * p.H, 22))
+    p.cend[(b * p.nch + c) * p.H + h] = *total;
 }
 
 // ---------------------------------------------------------------------------------- K2 + K5
@@ -446,6 +450,8 @@ __global__ void __launch_bounds__(kSimtThreads, 3) simt_scan_kernel(GenericParam
       const int ti = si >> rs;
       const float sc = exp2f(cum_hi[ti] + cum_lo[ti]);   // exp(cum of row i's step)
       float* yrow = static_cast<float*>(p.y) + ((row0 + si) * p.H + h) * kT64;
+      if (SSD_INDEX_OK(p.hdr, ((row0 + si) * p.H + h) * kT64 + 4 * tx + 3,
+                       p.batch * p.T * p.R * p.H * kT64, 21))
       *reinterpret_cast<float4*>(yrow + 4 * tx) =
           make_float4(fmaf(sc, yo[r][0], yd[r][0]), fmaf(sc, yo[r][1], yd[r][1]),
                       fmaf(sc, yo[r][2], yd[r][2]), fmaf(sc, yo[r][3], yd[r][3]));

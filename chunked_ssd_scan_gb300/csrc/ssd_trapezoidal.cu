@@ -45,7 +45,7 @@ __global__ void __launch_bounds__(kRowLanes * kRowsPerBlock)
     trap_expand_x(const T* __restrict__ x, const float* __restrict__ gamma,
                   const float* __restrict__ beta, const T* __restrict__ prev_x,
                   float* __restrict__ xh, const int64_t* __restrict__ valid_len,
-                  int64_t batch, int64_t Tn, int64_t R, int64_t H, int64_t P) {
+                  int64_t batch, int64_t Tn, int64_t R, int64_t H, int64_t P, WsHeader* hdr) {
   for (int64_t bt = blockIdx.x; bt < batch * Tn; bt += gridDim.x) {
     const int64_t t = bt % Tn, b = bt / Tn;
     if (pad_step(valid_len, b, t, Tn)) continue;   // padding: never read downstream
@@ -66,7 +66,8 @@ __global__ void __launch_bounds__(kRowLanes * kRowsPerBlock)
         }
         float* dst = xh + ((bt * 2 * R + m) * H + h) * P;
         for (int64_t p = threadIdx.x; p < P; p += kRowLanes)
-          dst[p] = src ? w * ld_f32(src + p) : 0.f;
+          if (SSD_INDEX_OK(hdr, (dst - xh) + p, batch * Tn * 2 * R * H * P, 40))
+            dst[p] = src ? w * ld_f32(src + p) : 0.f;
       }
     }
   }
@@ -80,7 +81,7 @@ __global__ void __launch_bounds__(kRowLanes * kRowsPerBlock)
                    const float* __restrict__ theta, const T* __restrict__ prev_B,
                    float* __restrict__ bh, float* __restrict__ ch,
                    const int64_t* __restrict__ valid_len, int64_t batch, int64_t Tn, int64_t R,
-                   int64_t H, int64_t G, int64_t G2, int64_t N) {
+                   int64_t H, int64_t G, int64_t G2, int64_t N, WsHeader* hdr) {
   const int64_t K = (N + 1) / 2;   // pairs (the last one single when N is odd, no theta)
   const int64_t hpg = H / G;
   for (int64_t bt = blockIdx.x; bt < batch * Tn; bt += gridDim.x) {
@@ -113,6 +114,8 @@ __global__ void __launch_bounds__(kRowLanes * kRowsPerBlock)
             b0 = e;
             b1 = od;
           }
+          if (!SSD_INDEX_OK(hdr, (bd - bh) + n0 + (two ? 1 : 0), batch * Tn * 2 * R * G2 * N, 41))
+            continue;
           bd[n0] = b0;
           cd[n0] = csrc ? ld_f32(csrc + n0) : 0.f;
           if (two) {
@@ -130,14 +133,15 @@ template <typename T>
 __global__ void __launch_bounds__(kRowLanes * kRowsPerBlock)
     trap_compact_y(const float* __restrict__ yh, T* __restrict__ y,
                    const int64_t* __restrict__ valid_len, int64_t batch, int64_t Tn, int64_t R,
-                   int64_t H, int64_t P) {
+                   int64_t H, int64_t P, WsHeader* hdr) {
   for (int64_t bt = blockIdx.x; bt < batch * Tn; bt += gridDim.x) {
     if (pad_step(valid_len, bt / Tn, bt % Tn, Tn)) continue;   // y at padding is not written
     for (int64_t r = 0; r < R; ++r) {
       for (int64_t h = threadIdx.y; h < H; h += kRowsPerBlock) {
         const float* src = yh + ((bt * 2 * R + r) * H + h) * P;
         T* dst = y + ((bt * R + r) * H + h) * P;
-        for (int64_t p = threadIdx.x; p < P; p += kRowLanes) st_from_f32(dst + p, src[p]);
+        for (int64_t p = threadIdx.x; p < P; p += kRowLanes)
+          if (SSD_INDEX_OK(hdr, (dst - y) + p, batch * Tn * R * H * P, 42)) st_from_f32(dst + p, src[p]);
       }
     }
   }
@@ -148,28 +152,30 @@ cudaError_t expand_typed(const TrapArgs& a, cudaStream_t st) {
   const dim3 blk(kRowLanes, kRowsPerBlock);
   trap_expand_x<T><<<step_blocks(a.batch * a.T), blk, 0, st>>>(
       static_cast<const T*>(a.x), a.gamma, a.beta, static_cast<const T*>(a.prev_x), a.xh,
-      a.valid_len, a.batch, a.T, a.R, a.H, a.P);
+      a.valid_len, a.batch, a.T, a.R, a.H, a.P, a.hdr);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   trap_expand_bc<T><<<step_blocks(a.batch * a.T), blk, 0, st>>>(
       static_cast<const T*>(a.B), static_cast<const T*>(a.C), a.theta,
       static_cast<const T*>(a.prev_B), a.bh, a.ch, a.valid_len, a.batch, a.T, a.R, a.H, a.G,
-      a.G2, a.N);
+      a.G2, a.N, a.hdr);
   return cudaGetLastError();
 }
 
 template <typename T>
 cudaError_t compact_typed(const TrapArgs& a, cudaStream_t st) {
   trap_compact_y<T><<<step_blocks(a.batch * a.T), dim3(kRowLanes, kRowsPerBlock), 0,
-                      st>>>(a.yh, static_cast<T*>(a.y), a.valid_len, a.batch, a.T, a.R, a.H, a.P);
+                      st>>>(a.yh, static_cast<T*>(a.y), a.valid_len, a.batch, a.T, a.R, a.H, a.P, a.hdr);
   return cudaGetLastError();
 }
 
 // Rows of 16-byte words: copy n words from src (zeros if src is null) to dst, lanes along the row.
 __device__ __forceinline__ void copy_row16(uint4* __restrict__ dst, const uint4* __restrict__ src,
-                                           int64_t n) {
+                                           int64_t n, WsHeader* hdr, const uint4* base,
+                                           int64_t extent, int site) {
   for (int64_t k = threadIdx.x; k < n; k += kRowLanes)
-    dst[k] = src ? __ldg(src + k) : make_uint4(0u, 0u, 0u, 0u);
+    if (SSD_INDEX_OK(hdr, (dst - base) + k, extent, site))
+      dst[k] = src ? __ldg(src + k) : make_uint4(0u, 0u, 0u, 0u);
 }
 
 // x^, B^, C^ (exact bf16 copies) and the write weights w^ = [gamma_t, beta_t] of step (b, t).
@@ -194,17 +200,20 @@ __global__ void __launch_bounds__(kRowLanes * kRowsPerBlock)
         const uint4* src = cur ? x + ((bt * R + m) * a.H + h) * xw
                                : (t > 0 ? x + (((bt - 1) * R + (m - R)) * a.H + h) * xw
                                         : (px ? px + ((b * R + (m - R)) * a.H + h) * xw : nullptr));
-        copy_row16(xq + ((bt * R2 + m) * a.H + h) * xw, src, xw);
-        if (threadIdx.x == 0)
+        copy_row16(xq + ((bt * R2 + m) * a.H + h) * xw, src, xw, a.hdr, xq,
+                   a.batch * Tn * R2 * a.H * xw, 43);
+        if (threadIdx.x == 0 &&
+            SSD_INDEX_OK(a.hdr, (bt * R2 + m) * a.H + h, a.batch * Tn * R2 * a.H, 44))
           a.wq[(bt * R2 + m) * a.H + h] = cur ? a.gamma[bt * a.H + h] : a.beta[bt * a.H + h];
       }
       for (int64_t g = threadIdx.y; g < a.G; g += kRowsPerBlock) {
         const uint4* bsrc = cur ? B + ((bt * R + m) * a.G + g) * bw
                                 : (t > 0 ? B + (((bt - 1) * R + (m - R)) * a.G + g) * bw
                                          : (pB ? pB + ((b * R + (m - R)) * a.G + g) * bw : nullptr));
-        copy_row16(bq + ((bt * R2 + m) * a.G + g) * bw, bsrc, bw);
-        copy_row16(cq + ((bt * R2 + m) * a.G + g) * bw, cur ? C + ((bt * R + m) * a.G + g) * bw : nullptr,
-                   bw);
+        const int64_t bext = a.batch * Tn * R2 * a.G * bw;
+        copy_row16(bq + ((bt * R2 + m) * a.G + g) * bw, bsrc, bw, a.hdr, bq, bext, 45);
+        copy_row16(cq + ((bt * R2 + m) * a.G + g) * bw,
+                   cur ? C + ((bt * R + m) * a.G + g) * bw : nullptr, bw, a.hdr, cq, bext, 46);
       }
     }
   }
@@ -220,7 +229,8 @@ __global__ void __launch_bounds__(kRowLanes * kRowsPerBlock)
     if (pad_step(a.valid_len, bt / Tn, bt % Tn, Tn)) continue;   // y at padding is not written
     for (int64_t r = 0; r < R; ++r)
       for (int64_t h = threadIdx.y; h < a.H; h += kRowsPerBlock)
-        copy_row16(y + ((bt * R + r) * a.H + h) * xw, yq + ((bt * R2 + r) * a.H + h) * xw, xw);
+        copy_row16(y + ((bt * R + r) * a.H + h) * xw, yq + ((bt * R2 + r) * a.H + h) * xw, xw,
+                   a.hdr, y, a.batch * Tn * R * a.H * xw, 47);
   }
 }
 

@@ -290,6 +290,7 @@ ssd_status ssd_trapezoidal_backward(
   t.G2 = G2;
   t.P = P;
   t.N = N;
+  t.hdr = reinterpret_cast<WsHeader*>(ws);   // this call's own header (offset 0)
   if (trap_expand(t, bf16, st) != cudaSuccess) return SSD_ERR_CUDA;
   const dim3 blk(kLanes, kRows);
   tbwd_expand_dy<<<tb_blocks(steps), blk, 0, st>>>(dy, dyh, steps, R, H, P);

@@ -41,7 +41,9 @@ typedef enum ssd_status {
   SSD_ERR_UNSUPPORTED = 2, /* valid arguments outside what the kernels implement             */
   SSD_ERR_CUDA = 3,        /* a CUDA runtime call or kernel launch failed                    */
   SSD_ERR_WORKSPACE = 4,   /* workspace missing, misaligned or smaller than required         */
-  SSD_ERR_TIMEOUT = 5      /* a device-side wait gave up (latched in the workspace)          */
+  SSD_ERR_TIMEOUT = 5,     /* a device-side wait gave up (latched in the workspace)          */
+  SSD_ERR_INDEX = 6        /* index-checked build only: a kernel skipped an access outside its
+                              buffer (latched in the workspace, detail = the access's site)   */
 } ssd_status;
 
 typedef enum ssd_dtype { SSD_F32 = 0, SSD_BF16 = 1 } ssd_dtype;
