@@ -50,7 +50,7 @@ NCU_TRAFFIC_BYTES = {
     "mamba2_siso_bf16": 77_673_216 + 27_691_520,           # ssd_fused_bf16_kernel<false>
     "mamba3_mimo_bf16": 1_441_353_984 + 253_872_640,       # ssd_fused_bf16_kernel<false>
     "long_rotation_f32": 3_937_686_272 + 788_730_368,      # simt_scan_kernel
-    "selective_scan_f32": 73_327_616 + 4_809_728,          # ss_onepass_kernel (output pass)
+    "selective_scan_f32": 77_815_552 + 8_036_864,          # ss_lookback_kernel
     # bwd_chunk_grad_kernel, captured at batch 1 and scaled by 4 (traffic grows with the batch)
     "mamba2_backward_bf16": (191_560_192 + 22_935_552) * 4,
 }
