@@ -69,16 +69,17 @@ constexpr uint32_t kXBytes = kTileRows * kP * 2;          // 16 KB per stage
 constexpr uint32_t kBCBytes = kTileRows * kN * 2;         // 32 KB per stage (two 64-col blocks)
 constexpr int kInfoSlots = 4;                             // K1 runs up to this many tiles ahead
 struct TileInfo {
-  float cum_hi[kTileRows];   // log2-scaled prefix sum of dA at fused row j (hi part)
-  float cum_lo[kTileRows];   // ... lo part
+  float cum_hi[kTileRows];   // log2-scaled prefix sum of dA at fused row j
   float qf[kTileRows];       // exp(cum_ref(block of j) - cum_j) (times w_j), cum_ref at the
                              // block's end
   float w[kTileRows];        // write weight of fused row j (with per-row weights only)
-  float last_hi, last_lo;    // log2-scaled total of the tile
+  float last_hi;             // log2-scaled total of the tile
   float etile;               // exp(cum_last)
   int monotone;              // 1 if every dA of the tile is <= 0 (factorized mask is safe)
-  float pad[28];
+  float pad[29];
 };
+// the rows are read as float4 from every slot of the ring
+static_assert(sizeof(TileInfo) % 16 == 0, "TileInfo slots must keep 16-byte alignment");
 constexpr uint32_t kTmemCols = 512;
 
 struct FusedArgs {
@@ -158,11 +159,11 @@ __device__ __forceinline__ void split2(float2 v, uint32_t& hi, uint32_t& lo) {
 // exp(cum_i - cum_ref) * qf_j, else one exponential per element with the causal cut at jlim.
 template <bool kW>
 __device__ __forceinline__ void mask_block(const TileInfo& ti, int cb, bool exact, float chi,
-                                           float clo, int jlim, const float (&w)[32],
+                                           int jlim, const float (&w)[32],
                                            uint32_t (&hi)[16], uint32_t (&lo)[16]) {
   if (!exact) {
     const int ref = cb * 32 + 31;
-    const float r = ex2_approx((chi - ti.cum_hi[ref]) + (clo - ti.cum_lo[ref]));
+    const float r = ex2_approx(chi - ti.cum_hi[ref]);
     const float2 rr = make_float2(r, r);
 #pragma unroll
     for (int k = 0; k < 32; k += 4) {
@@ -173,14 +174,13 @@ __device__ __forceinline__ void mask_block(const TileInfo& ti, int cb, bool exac
              hi[k / 2 + 1], lo[k / 2 + 1]);
     }
   } else {
-    const float2 ch2 = make_float2(chi, chi), cl2 = make_float2(clo, clo);
+    const float2 ch2 = make_float2(chi, chi);
 #pragma unroll
     for (int k = 0; k < 32; k += 4) {
       const int j = cb * 32 + k;
       const float4 ch = *reinterpret_cast<const float4*>(&ti.cum_hi[j]);
-      const float4 cl = *reinterpret_cast<const float4*>(&ti.cum_lo[j]);
-      const float2 e0 = add2(sub2(ch2, make_float2(ch.x, ch.y)), sub2(cl2, make_float2(cl.x, cl.y)));
-      const float2 e1 = add2(sub2(ch2, make_float2(ch.z, ch.w)), sub2(cl2, make_float2(cl.z, cl.w)));
+      const float2 e0 = sub2(ch2, make_float2(ch.x, ch.y));
+      const float2 e1 = sub2(ch2, make_float2(ch.z, ch.w));
       // future columns (j >= jlim) are cut after the exponential, which may overflow there
       float2 l0 = make_float2(j < jlim ? ex2_approx(e0.x) : 0.f,
                               j + 1 < jlim ? ex2_approx(e0.y) : 0.f);
@@ -237,63 +237,78 @@ __device__ __forceinline__ void k1_warp(const FusedArgs& a, TileInfo* info, uint
       for (int k = 0; k < 4; ++k) wcur[k] = wnext[k];
       if (t + 1 < nt) load_w(t + 1);
     }
-    DF sum = {0.f, 0.f};
+    // fp32 prefix sums: within a 128-row tile |cum| stays far below the range where fp32
+    // rounding would show at the bf16 output's precision
+    float sum = 0.f;
     int pos = 0;
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       pos |= (dcur[k] > 0.f);
-      sum = df_add(sum, DF{dcur[k], 0.f});
+      sum += dcur[k];
     }
-    DF incl = sum;
+    float incl = sum;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
-      const DF v = df_shfl_up(incl, off);
-      if (lane >= off) incl = df_add(incl, v);
+      const float v = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += v;
     }
-    const DF last = df_shfl(incl, 31);
-    DF acc = df_shfl_up(incl, 1);   // exclusive prefix of this lane's first step
-    if (lane == 0) acc = DF{0.f, 0.f};
+    const float last = __shfl_sync(0xffffffffu, incl, 31);
+    float acc = __shfl_up_sync(0xffffffffu, incl, 1);   // exclusive prefix of the lane's first step
+    if (lane == 0) acc = 0.f;
     const int monotone = __all_sync(0xffffffffu, pos == 0);
     const int slot = t % kInfoSlots;
     if (t >= kInfoSlots &&
         !wait_bar(&info_empty[slot], ((t - kInfoSlots) / kInfoSlots) & 1, abort, a.hdr, 11))
       break;
     TileInfo& ti = info[slot];
+    float chv[4];
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-      if (beg + k < end) {
-        acc = df_add(acc, DF{dcur[k], 0.f});
-        const float chi = acc.hi * kLog2e;
-        const float clo = fmaf(acc.hi, kLog2e, -chi) + acc.lo * kLog2e;
-        for (int r = 0; r < R; ++r) {
-          ti.cum_hi[(beg + k) * R + r] = chi;
-          ti.cum_lo[(beg + k) * R + r] = clo;
-        }
-      }
+      acc += dcur[k];   // dcur is 0 past the lane's steps
+      chv[k] = acc * kLog2e;
+    }
+    // with R in {1, 2, 4} the lane's steps cover exactly the rows 4 lane .. 4 lane + 3 (row
+    // 4 lane + m belongs to the lane's step m / R): one 16-byte store
+    const bool quad = R == 1 || R == 2 || R == 4;
+    float4 c4 = make_float4(chv[0], chv[0], chv[0], chv[0]);
+    if (R == 1) c4 = make_float4(chv[0], chv[1], chv[2], chv[3]);
+    if (R == 2) c4 = make_float4(chv[0], chv[0], chv[1], chv[1]);
+    if (quad) {
+      *reinterpret_cast<float4*>(&ti.cum_hi[4 * lane]) = c4;
+    } else {
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        if (beg + k < end)
+          for (int r = 0; r < R; ++r) ti.cum_hi[(beg + k) * R + r] = chv[k];
     }
     if (lane == 0) {
-      const float lhi = last.hi * kLog2e;
+      const float lhi = last * kLog2e;
       ti.last_hi = lhi;
-      ti.last_lo = fmaf(last.hi, kLog2e, -lhi) + last.lo * kLog2e;
-      ti.etile = ex2_approx(lhi + ti.last_lo);
+      ti.etile = ex2_approx(lhi);
       ti.monotone = monotone;
     }
-    __syncwarp();
     // qf of the rank-one blocks: the reference of column block c is its last fused row
-    if constexpr (kW) {   // times the column's write weight
+    if (!kW && quad) {
+      // the reference row 32 (lane / 8) + 31 of the lane's rows is row 3 of lane 8 (lane / 8) + 7
+      const float cref = __shfl_sync(0xffffffffu, c4.w, (lane & ~7) | 7);
+      *reinterpret_cast<float4*>(&ti.qf[4 * lane]) =
+          make_float4(ex2_approx(cref - c4.x), ex2_approx(cref - c4.y), ex2_approx(cref - c4.z),
+                      ex2_approx(cref - c4.w));
+    } else if constexpr (kW) {   // times the column's write weight
+      __syncwarp();
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         const int e = lane + 32 * k;
         const int ref = (e >> 5) * 32 + 31;
-        ti.qf[e] = wcur[k] * ex2_approx((ti.cum_hi[ref] - ti.cum_hi[e]) +
-                                        (ti.cum_lo[ref] - ti.cum_lo[e]));
+        ti.qf[e] = wcur[k] * ex2_approx(ti.cum_hi[ref] - ti.cum_hi[e]);
         ti.w[e] = wcur[k];
       }
     } else {
+      __syncwarp();
 #pragma unroll
       for (int e = lane; e < kTileRows; e += 32) {
         const int ref = (e >> 5) * 32 + 31;
-        ti.qf[e] = ex2_approx((ti.cum_hi[ref] - ti.cum_hi[e]) + (ti.cum_lo[ref] - ti.cum_lo[e]));
+        ti.qf[e] = ex2_approx(ti.cum_hi[ref] - ti.cum_hi[e]);
       }
     }
     __syncwarp();
@@ -712,7 +727,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             *reinterpret_cast<uint4*>(dlo + o1) = z;
             continue;
           }
-          float wd = ex2_approx((ti.last_hi - ti.cum_hi[row]) + (ti.last_lo - ti.cum_lo[row]));
+          float wd = ex2_approx(ti.last_hi - ti.cum_hi[row]);
           if constexpr (kW) wd *= ti.w[row];
           const float2 w2 = make_float2(wd, wd);
           const uint32_t o0 = sw128_off16(row, c0), o1 = sw128_off16(row, c0 + 8);
@@ -747,7 +762,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const uint32_t mb = tmem + lane_addr + kColM + (t & 1) * 128;
         const bool fact_ok = ti.monotone != 0;
-        const float chi = ti.cum_hi[i], clo = ti.cum_lo[i];
+        const float chi = ti.cum_hi[i];
 #pragma unroll 1
         for (int cb = ms.cb0; cb < ms.cb1; ++cb) {
           float w[32];
@@ -755,7 +770,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld_wait();
           reg_tie(w);
           uint32_t hi[16], lo[16];
-          mask_block<kW>(ti, cb, cb == q || !fact_ok, chi, clo, jlim, w, hi, lo);
+          mask_block<kW>(ti, cb, cb == q || !fact_ok, chi, jlim, w, hi, lo);
           tmem_st16u(mb + cb * 32, hi);
           tmem_st16u(mb + cb * 32 + 16, lo);
         }
@@ -945,7 +960,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const TileInfo& ti = info[slot];
           {
             // e^{cum_i} Yo_t into the y accumulator (y_{t-1} was read in the previous iteration)
-            const float sc = ex2_approx(ti.cum_hi[i] + ti.cum_lo[i]);
+            const float sc = ex2_approx(ti.cum_hi[i]);
             const float2 sc2 = make_float2(sc, sc);
   #pragma unroll
             for (int c = 0; c < kP; c += 32) {
