@@ -77,6 +77,9 @@ def parse_args():
     # smaller cases of a workload's shape, for profiler captures (not bench lines)
     ap.add_argument("--batch", type=int, default=0, help="override the workload's batch")
     ap.add_argument("--seqlen", type=int, default=0, help="override the workload's seqlen")
+    ap.add_argument("--tf32", action="store_true",
+                    help="fp32 workloads with P = N = 64: run ssd_chunked_forward_tf32 (the chunk "
+                         "scan on the tensor core) instead of ssd_chunked_forward")
     ap.add_argument("--measure-peak", choices=["tf32"], default=None,
                     help="measure a tensor-core peak (torch.matmul) and print it instead")
     return ap.parse_args()
@@ -252,11 +255,13 @@ def job_tokens(tokens_per_replica: int, world: int) -> int:
     return tokens_per_replica * world
 
 
-def kernel_chunk(pkg, shape, R, chunk_len):
+def kernel_chunk(pkg, shape, R, chunk_len, variant=None):
     """Steps per chunk the kernels actually tile by: the register-tiled fp32 path uses 64 fused
-    rows (64 / R steps) whatever chunk_len says; every other path tiles by chunk_len (the fused
-    bf16 kernel's FLOPs are not its bound, so its count keeps chunk_len)."""
-    return 64 // R if pkg.ssd_chunked_variant(shape) == "tiled_f32" else chunk_len
+    rows (64 / R steps) and the tf32 tensor-core path 128 fused rows (128 / R) whatever
+    chunk_len says; every other path tiles by chunk_len (the fused bf16 kernel's FLOPs are not
+    its bound, so its count keeps chunk_len)."""
+    v = variant or pkg.ssd_chunked_variant(shape)
+    return {"tiled_f32": 64 // R, "tc_tf32": 128 // R}.get(v, chunk_len)
 
 
 def run_ours(args, rank, world, local):
@@ -385,13 +390,13 @@ def run_ours(args, rank, world, local):
         # validated once; each step is only the C-ABI call
         fn = pkg.SSDForwardPlan(d["x"], d["dA"], d["B"], d["C"], chunk_len=cfg.chunk_len,
                                 theta=d["theta"], init_state=d["init_state"], y=y,
-                                final_state=fin, workspace=ws, stream=stream)
-        variant = pkg.ssd_chunked_variant(shape)
+                                final_state=fin, workspace=ws, stream=stream, tf32=args.tf32)
+        variant = "tc_tf32" if args.tf32 else pkg.ssd_chunked_variant(shape)
         launches_per_call = pkg.ssd_chunked_launches(shape)
         dtype = cfg.dtype
         io_bytes = cfg.io_bytes()
-        flops = cfg.with_(chunk_len=kernel_chunk(pkg, shape, cfg.mimo_rank,
-                                                 cfg.chunk_len)).causal_flops()
+        flops = cfg.with_(chunk_len=kernel_chunk(pkg, shape, cfg.mimo_rank, cfg.chunk_len,
+                                                 variant)).causal_flops()
 
     if world > 1:
         torch.distributed.barrier()
@@ -411,8 +416,9 @@ def run_ours(args, rank, world, local):
     ms = slowest_replica_ms(sum(step_ms) / len(step_ms), world, dev)
     tokens = job_tokens(cfg.tokens, world)
     hbm, tf, peak_src = measured_peaks()
-    # the capture's bytes belong to the workload's own shape, not to an overridden one
-    traffic = None if (args.batch or args.seqlen) else NCU_TRAFFIC_BYTES.get(cfg.name)
+    # the capture's bytes belong to the workload's own shape and default kernels
+    traffic = (None if (args.batch or args.seqlen or args.tf32)
+               else NCU_TRAFFIC_BYTES.get(cfg.name))
     kernel = ("selective_scan_forward" if is_ss
               else ("ssd_trapezoidal_backward" if cfg.trapezoidal else "ssd_chunked_backward")
               if variant == "backward"
@@ -420,7 +426,7 @@ def run_ours(args, rank, world, local):
               else "ssd_rotation_variant_forward" if variant == "rotation_variant"
               else f"ssd_chunked_forward[{variant}]")
     roof = roofline(io_bytes, flops, ms * 1e-3, hbm, tf, peak_src, bf16_inputs=dtype == "bf16",
-                    tensor_path=variant == "tc_bf16")
+                    tensor_path=variant in ("tc_bf16", "tc_tf32"))
     roof.update({"traffic": traffic, "kernel": kernel, "algorithmic_bytes_per_launch": io_bytes})
     if flops:
         roof["algorithmic_flops_per_launch"] = flops
@@ -596,7 +602,7 @@ def e2e_measure(args, cfg, is_ss, host, dev, stream):
                 pkg.ssd_chunked_forward(dbuf["x"], dbuf["dA"], dbuf["B"], dbuf["C"],
                                         chunk_len=cfg.chunk_len, theta=dbuf["theta"],
                                         init_state=dbuf["init_state"], y=y, final_state=fin,
-                                        workspace=ws)
+                                        workspace=ws, tf32=args.tf32)
 
     h2d = sum(v.numel() * v.element_size() for v in pin.values() if v is not None)
     d2h = sum(o.numel() * o.element_size() for o, _ in outs)

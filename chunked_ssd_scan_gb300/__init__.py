@@ -31,7 +31,7 @@ LIB_PATH = os.path.join(_PKG, "libssdscan.so")
 
 STATUS = {0: "SSD_OK", 1: "SSD_ERR_INVALID_ARG", 2: "SSD_ERR_UNSUPPORTED", 3: "SSD_ERR_CUDA",
           4: "SSD_ERR_WORKSPACE", 5: "SSD_ERR_TIMEOUT", 6: "SSD_ERR_INDEX"}
-VARIANTS = {0: "none", 1: "generic", 2: "tc_bf16", 3: "tiled_f32"}
+VARIANTS = {0: "none", 1: "generic", 2: "tc_bf16", 3: "tiled_f32", 4: "tc_tf32"}
 SSD_F32, SSD_BF16 = 0, 1
 
 
@@ -75,6 +75,8 @@ def load_library(path: Optional[str] = None):
     lib.ssd_chunked_forward.argtypes = [SP] + [_VP] * 9 + [ctypes.c_size_t, _VP]
     lib.ssd_chunked_forward_varlen.restype = ctypes.c_int
     lib.ssd_chunked_forward_varlen.argtypes = [SP] + [_VP] * 10 + [ctypes.c_size_t, _VP]
+    lib.ssd_chunked_forward_tf32.restype = ctypes.c_int
+    lib.ssd_chunked_forward_tf32.argtypes = [SP] + [_VP] * 10 + [ctypes.c_size_t, _VP]
     lib.ssd_trapezoidal_workspace_bytes.restype = ctypes.c_size_t
     lib.ssd_trapezoidal_workspace_bytes.argtypes = [SP]
     lib.ssd_trapezoidal_variant.restype = ctypes.c_int32
@@ -170,7 +172,9 @@ class SSDForwardPlan:
     """Arguments of ``ssd_chunked_forward`` validated once, for repeated calls on the same
     buffers.  Calling the plan makes only the C call (on the stream given here, or the stream
     that is current at construction).  Shapes and dtypes are those of ``ssd_chunked_forward``;
-    with ``valid_len`` (int64 [b] on the device) the plan calls ``ssd_chunked_forward_varlen``.
+    with ``valid_len`` (int64 [b] on the device) the plan calls ``ssd_chunked_forward_varlen``;
+    with ``tf32=True`` (fp32, P = N = 64) it calls ``ssd_chunked_forward_tf32`` (valid_len
+    optional), whose chunk scan runs on the tensor core.
     """
 
     def __init__(self, x: torch.Tensor, dA: torch.Tensor, B: torch.Tensor, C: torch.Tensor, *,
@@ -178,7 +182,7 @@ class SSDForwardPlan:
                  init_state: Optional[torch.Tensor] = None, y: Optional[torch.Tensor] = None,
                  final_state: Optional[torch.Tensor] = None, return_final_state: bool = True,
                  workspace: Optional[torch.Tensor] = None, stream=None,
-                 valid_len: Optional[torch.Tensor] = None):
+                 valid_len: Optional[torch.Tensor] = None, tf32: bool = False):
         if x.dim() != 5 or B.dim() != 5:
             raise ValueError("x must be [b,T,R,H,P] and B/C [b,T,R,G,N]")
         b, T, R, H, P = x.shape
@@ -213,11 +217,12 @@ class SSDForwardPlan:
         # keep every buffer alive as long as the plan
         self.inputs = (x, dA, B, C, theta, init_state, valid_len)
         self.y, self.final_state, self.workspace = y, final_state, workspace
-        vl = () if valid_len is None else (_ptr(valid_len),)
+        vl = (_ptr(valid_len),) if (tf32 or valid_len is not None) else ()
         self._args = (ctypes.byref(self.shape), _ptr(x), _ptr(dA), _ptr(B), _ptr(C), _ptr(theta),
                       *vl, _ptr(init_state), _ptr(y), _ptr(final_state), _ptr(workspace),
                       ctypes.c_size_t(workspace.numel()), _stream_handle(stream))
-        self._name = "ssd_chunked_forward" + ("" if valid_len is None else "_varlen")
+        self._name = "ssd_chunked_forward" + ("_tf32" if tf32 else
+                                              "" if valid_len is None else "_varlen")
         self._fn = getattr(self._lib, self._name)
 
     def __call__(self):
@@ -234,9 +239,9 @@ def ssd_chunked_forward(x: torch.Tensor, dA: torch.Tensor, B: torch.Tensor, C: t
                         final_state: Optional[torch.Tensor] = None,
                         return_final_state: bool = True,
                         workspace: Optional[torch.Tensor] = None, stream=None,
-                        valid_len: Optional[torch.Tensor] = None):
+                        valid_len: Optional[torch.Tensor] = None, tf32: bool = False):
     """Chunked SSD forward scan through ``ssd_chunked_forward`` (``ssd_chunked_forward_varlen``
-    when ``valid_len`` is given).
+    when ``valid_len`` is given, ``ssd_chunked_forward_tf32`` with ``tf32=True``).
 
     x [b,T,R,H,P], B/C [b,T,R,G,N] (all f32 or all bf16), dA [b,T,H] f32, theta [b,T,H,N/2] f32,
     init_state [b,H,P,N] f32, valid_len [b] int64 (steps from valid_len[b] on are padding; y is
@@ -244,7 +249,7 @@ def ssd_chunked_forward(x: torch.Tensor, dA: torch.Tensor, B: torch.Tensor, C: t
     """
     return SSDForwardPlan(x, dA, B, C, chunk_len=chunk_len, theta=theta, init_state=init_state,
                           y=y, final_state=final_state, return_final_state=return_final_state,
-                          workspace=workspace, stream=stream, valid_len=valid_len)()
+                          workspace=workspace, stream=stream, valid_len=valid_len, tf32=tf32)()
 
 
 def ssd_trapezoidal_workspace_bytes(shape: ssd_shape) -> int:

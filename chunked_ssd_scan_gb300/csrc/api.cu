@@ -1,5 +1,6 @@
 // C ABI of the library: argument validation, workspace layout and kernel launches.
 // Declarations and the contract of every entry point are in include/ssdscan.h.
+#include <algorithm>
 #include <string.h>
 
 #include "common.cuh"
@@ -64,13 +65,9 @@ int64_t kernel_chunk_len(const ssd_shape* s) {
   return pick_variant(s) == SSD_VARIANT_TILED_F32 ? 64 / s->mimo_rank : s->chunk_len;
 }
 
-SsdLayout ssd_layout(const ssd_shape* s) {
+// Workspace of the chunk pipeline run with chunks of l steps.
+SsdLayout chunk_layout(const ssd_shape* s, int64_t l) {
   SsdLayout L;
-  if (pick_variant(s) == SSD_VARIANT_TC_BF16) {   // the fused kernel keeps its state on chip
-    L.total = fused_bf16_workspace_bytes(s->batch, s->seqlen, s->nheads, s->mimo_rank);
-    return L;
-  }
-  const int64_t l = kernel_chunk_len(s);
   const int64_t nch = (s->seqlen + l - 1) / l;   // the last chunk may be short
   size_t off = sizeof(WsHeader);
   L.states = off;
@@ -88,6 +85,15 @@ SsdLayout ssd_layout(const ssd_shape* s) {
   }
   L.total = off;
   return L;
+}
+
+SsdLayout ssd_layout(const ssd_shape* s) {
+  if (pick_variant(s) == SSD_VARIANT_TC_BF16) {   // the fused kernel keeps its state on chip
+    SsdLayout L;
+    L.total = fused_bf16_workspace_bytes(s->batch, s->seqlen, s->nheads, s->mimo_rank);
+    return L;
+  }
+  return chunk_layout(s, kernel_chunk_len(s));
 }
 
 bool al16(const void* p) { return p == nullptr || aligned16(p); }
@@ -177,7 +183,12 @@ extern "C" {
 
 size_t ssd_chunked_workspace_bytes(const ssd_shape* shape) {
   if (check_shape(shape) != SSD_OK) return 0;
-  return ssd_layout(shape).total;
+  size_t n = ssd_layout(shape).total;
+  // one size serves ssd_chunked_forward_tf32 as well (its chunks of 128 fused rows)
+  if (tc32_supported(shape->headdim, shape->dstate, shape->mimo_rank,
+                     shape->io_dtype == SSD_BF16))
+    n = std::max(n, chunk_layout(shape, tc32_chunk_len(shape->mimo_rank)).total);
+  return n;
 }
 
 int32_t ssd_chunked_launches(const ssd_shape* shape) {
@@ -197,19 +208,25 @@ int32_t ssd_chunked_variant(const ssd_shape* shape) {
 
 namespace {
 
-// Both forward entry points; valid_len is null for ssd_chunked_forward.
+// The forward entry points; valid_len is null for ssd_chunked_forward, and tf32 selects the
+// tensor-core chunk scan of ssd_chunked_forward_tf32 (its chunks of 128 fused rows need a
+// smaller workspace than the register-tiled path's, which the common size covers).
 ssd_status chunked_forward(const ssd_shape* shape, const void* x, const float* dA, const void* B,
                            const void* C, const float* theta, const int64_t* valid_len,
                            const float* init_state, void* y, float* final_state, void* workspace,
-                           size_t workspace_bytes, void* stream) {
+                           size_t workspace_bytes, void* stream, bool tf32 = false) {
   const ssd_status sc = check_shape(shape);
   if (sc != SSD_OK) return sc;
+  if (tf32 && !tc32_supported(shape->headdim, shape->dstate, shape->mimo_rank,
+                              shape->io_dtype == SSD_BF16))
+    return SSD_ERR_UNSUPPORTED;
   if (!x || !dA || !B || !C || !y) return SSD_ERR_INVALID_ARG;
   if ((shape->has_theta != 0) != (theta != nullptr)) return SSD_ERR_INVALID_ARG;
   if (!al16(x) || !al16(dA) || !al16(B) || !al16(C) || !al16(y) || !al16(theta) ||
       !al16(init_state) || !al16(final_state))
     return SSD_ERR_INVALID_ARG;
-  const SsdLayout lay = ssd_layout(shape);
+  const int64_t l = tf32 ? tc32_chunk_len(shape->mimo_rank) : kernel_chunk_len(shape);
+  const SsdLayout lay = tf32 ? chunk_layout(shape, l) : ssd_layout(shape);
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) % kWsAlign) != 0 ||
       workspace_bytes < lay.total)
     return SSD_ERR_WORKSPACE;
@@ -232,7 +249,7 @@ ssd_status chunked_forward(const ssd_shape* shape, const void* x, const float* d
   p.N = shape->dstate;
   p.G = shape->ngroups;
   p.R = shape->mimo_rank;
-  p.l = kernel_chunk_len(shape);
+  p.l = l;
   p.nch = (shape->seqlen + p.l - 1) / p.l;   // the last chunk may be short
   p.states = reinterpret_cast<float*>(ws + lay.states);
   p.cend = reinterpret_cast<float*>(ws + lay.cend);
@@ -241,11 +258,11 @@ ssd_status chunked_forward(const ssd_shape* shape, const void* x, const float* d
   p.hdr = reinterpret_cast<WsHeader*>(ws);
   p.valid_len = valid_len;
   cudaError_t e;
-  const int32_t variant = pick_variant(shape);
+  const int32_t variant = tf32 ? SSD_VARIANT_TC_TF32 : pick_variant(shape);
   if (variant == SSD_VARIANT_TC_BF16) {
     e = fused_bf16_forward(p, static_cast<cudaStream_t>(stream));
-  } else if (variant == SSD_VARIANT_TILED_F32) {
-    e = simt32_forward(p, static_cast<cudaStream_t>(stream));
+  } else if (variant == SSD_VARIANT_TILED_F32 || variant == SSD_VARIANT_TC_TF32) {
+    e = simt32_forward(p, static_cast<cudaStream_t>(stream), variant == SSD_VARIANT_TC_TF32);
   } else {
     e = generic_forward(p, shape->io_dtype == SSD_BF16, static_cast<cudaStream_t>(stream));
   }
@@ -273,6 +290,17 @@ ssd_status ssd_chunked_forward_varlen(const ssd_shape* shape, const void* x, con
     return SSD_ERR_INVALID_ARG;
   return chunked_forward(shape, x, dA, B, C, theta, valid_len, init_state, y, final_state,
                          workspace, workspace_bytes, stream);
+}
+
+ssd_status ssd_chunked_forward_tf32(const ssd_shape* shape, const void* x, const float* dA,
+                                    const void* B, const void* C, const float* theta,
+                                    const int64_t* valid_len, const float* init_state, void* y,
+                                    float* final_state, void* workspace, size_t workspace_bytes,
+                                    void* stream) {
+  if (valid_len && reinterpret_cast<uintptr_t>(valid_len) % alignof(int64_t) != 0)
+    return SSD_ERR_INVALID_ARG;
+  return chunked_forward(shape, x, dA, B, C, theta, valid_len, init_state, y, final_state,
+                         workspace, workspace_bytes, stream, true);
 }
 
 int32_t ssd_trapezoidal_variant(const ssd_shape* shape) {
@@ -417,7 +445,7 @@ ssd_status trapezoidal_forward(const ssd_shape* shape, const void* x, const floa
   p.phisum = theta ? reinterpret_cast<double*>(ws + lay.inner.phisum) : nullptr;
   p.hdr = reinterpret_cast<WsHeader*>(ws);
   p.valid_len = valid_len;
-  const cudaError_t ce = pick_variant(&e) == SSD_VARIANT_TILED_F32 ? simt32_forward(p, st)
+  const cudaError_t ce = pick_variant(&e) == SSD_VARIANT_TILED_F32 ? simt32_forward(p, st, false)
                                                                     : generic_forward(p, false, st);
   if (ce != cudaSuccess) return SSD_ERR_CUDA;
   return trap_compact(t, bf16, st) == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;

@@ -463,5 +463,28 @@ __device__ __forceinline__ void mma_ts_we(uint32_t d_tmem, uint32_t a_tmem, uint
       : "memory");
 }
 
+// kind::tf32 forms of the two above (fp32 operands read as tf32, fp32 accumulate).
+__device__ __forceinline__ void mma_ss_we_tf32(uint32_t d_tmem, uint32_t alo, uint32_t ahi,
+                                               uint32_t blo, uint32_t bhi, uint32_t idesc,
+                                               uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t.reg .b64 ad, bd;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+      "mov.b64 ad, {%1, %2};\n\tmov.b64 bd, {%3, %4};\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::tf32 [%0], ad, bd, %5, p;\n\t}" ::"r"(d_tmem),
+      "r"(alo), "r"(ahi), "r"(blo), "r"(bhi), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_ts_we_tf32(uint32_t d_tmem, uint32_t a_tmem, uint32_t blo,
+                                               uint32_t bhi, uint32_t idesc,
+                                               uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t.reg .b64 bd;\n\tsetp.ne.b32 p, %5, 0;\n\t"
+      "mov.b64 bd, {%2, %3};\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], bd, %4, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "r"(blo), "r"(bhi), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 }  // namespace tc
 }  // namespace ssd

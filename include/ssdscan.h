@@ -66,7 +66,10 @@ typedef enum ssd_kernel_variant {
   SSD_VARIANT_NONE = 0,    /* shape not supported                                    */
   SSD_VARIANT_GENERIC = 1, /* CUDA-core fp32 chunk pipeline (any supported shape)    */
   SSD_VARIANT_TC_BF16 = 2, /* fused tcgen05/TMEM kernel, bf16 operands, fp32 accum.  */
-  SSD_VARIANT_TILED_F32 = 3 /* register-tiled CUDA-core fp32 kernels, P = N = 64, R | 64 */
+  SSD_VARIANT_TILED_F32 = 3, /* register-tiled CUDA-core fp32 kernels, P = N = 64, R | 64 */
+  SSD_VARIANT_TC_TF32 = 4    /* the family ssd_chunked_forward_tf32 runs (not chosen by
+                                ssd_chunked_forward): the tiled path with the chunk scan as
+                                tcgen05 kind::tf32 products */
 } ssd_kernel_variant;
 
 /*
@@ -140,6 +143,26 @@ ssd_status ssd_chunked_forward_varlen(const ssd_shape* shape, const void* x, con
                                       const int64_t* valid_len, const float* init_state, void* y,
                                       float* final_state, void* workspace,
                                       size_t workspace_bytes, void* stream);
+
+/*
+ * ssd_chunked_forward for fp32 I/O with headdim = dstate = 64 and mimo_rank a power of two up to
+ * 64, with the chunk scan (the serial.rs page's K2 and K5: CB = C B^T, the decay mask, (L o CB) x
+ * and C h_in, the scan.py page's rotation absorbed into B and C) on the tensor core as
+ * tcgen05.mma kind::tf32 over chunks of 128 fused rows (128 / mimo_rank steps, whatever
+ * chunk_len says: the result does not depend on it).  Every fp32 operand is split into a tf32
+ * high part and its remainder and each pair takes three products (hi.lo, lo.hi, then hi.hi),
+ * accumulated in TMEM over one 32-deep K block at a time and summed in fp32 round-to-nearest, so
+ * the tensor core's truncating accumulation stays within the fp32 gate 1e-4 (1 + |y|).  K1, K3
+ * and K4 run on the CUDA cores as in ssd_chunked_forward (SSD_VARIANT_TILED_F32).
+ * valid_len: NULL, or as for ssd_chunked_forward_varlen.  Other arguments, the workspace size
+ * (ssd_chunked_workspace_bytes covers both fp32 scans), asynchrony and errors as for
+ * ssd_chunked_forward; UNSUPPORTED for any other shape or dtype.
+ */
+ssd_status ssd_chunked_forward_tf32(const ssd_shape* shape, const void* x, const float* dA,
+                                    const void* B, const void* C, const float* theta,
+                                    const int64_t* valid_len, const float* init_state, void* y,
+                                    float* final_state, void* workspace, size_t workspace_bytes,
+                                    void* stream);
 
 /* Bytes of device workspace ssd_trapezoidal_forward needs for `shape` (0 if unsupported). */
 size_t ssd_trapezoidal_workspace_bytes(const ssd_shape* shape);

@@ -44,9 +44,10 @@ class Guarded:
 
 
 def gpu_ssd(inp: dict, chunk_len: int, dev: str = "cuda", final: bool = True,
-            guard: bool = False):
-    """One forward through the C ABI; the device-side error word of its workspace must be clean
-    (a bounded wait that gave up would otherwise only show as wrong numbers).  With guard=True,
+            guard: bool = False, tf32: bool = False, valid_len=None):
+    """One forward through the C ABI (ssd_chunked_forward_tf32 with tf32=True; valid lengths per
+    sequence if given); the device-side error word of its workspace must be clean (a bounded
+    wait that gave up would otherwise only show as wrong numbers).  With guard=True,
     y, the final state and the workspace sit between NaN-pattern guard bands that must be intact
     after the call (an out-of-bounds store that element-wise parity cannot see would show)."""
     d = {k: (v.to(dev) if v is not None else None) for k, v in inp.items()}
@@ -68,9 +69,11 @@ def gpu_ssd(inp: dict, chunk_len: int, dev: str = "cuda", final: bool = True,
         gw = Guarded(nws, dev, fill_inner=0)   # a workspace starts with a zeroed header
         kw["workspace"] = gw.inner
         bands.append((gw, "workspace"))
+    if valid_len is not None:
+        kw["valid_len"] = torch.as_tensor(valid_len, dtype=torch.int64, device=dev)
     plan = pkg.SSDForwardPlan(d["x"], d["dA"], d["B"], d["C"], chunk_len=chunk_len,
                               theta=d["theta"], init_state=d["init_state"],
-                              return_final_state=final, **kw)
+                              return_final_state=final, tf32=tf32, **kw)
     y, fin = plan()
     assert pkg.workspace_status(plan.workspace) == ("SSD_OK", 0)
     torch.cuda.synchronize()
