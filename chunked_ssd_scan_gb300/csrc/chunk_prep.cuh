@@ -1,7 +1,8 @@
 // Per-chunk preparation shared by the fp32 chunk kernels with P = N = 64 (the register-tiled
 // CUDA-core kernels and the tf32 tensor-core chunk scan): the rank shift of fused rows, the real
 // steps of a chunk, the double-float prefix sums of dA (K1) and the rotation angles Phi_t of a
-// chunk's steps.  Every function here assumes blockDim.x == kPrepThreads.
+// chunk's steps.  chunk_prefix64 runs on warp 0; issue_theta64 on any block; chunk_angles64
+// takes the block size as its template argument (kPrepThreads by default).
 #pragma once
 
 #include "common.cuh"
@@ -29,15 +30,18 @@ __device__ __forceinline__ int steps64(const GenericParams& p, int64_t b, int64_
 
 // log2-scaled double-float prefix sums of dA over steps [0, n) of a chunk, by warp 0 (steps at
 // or after nv read as zero): cum_hi/cum_lo[t] is the inclusive sum up to step t; *total
-// (natural units) if non-null.
+// (natural units) if non-null.  With kShared the steps are read from shared memory (a staged
+// copy) instead of through the read-only global path.
+template <bool kShared = false>
 __device__ inline void chunk_prefix64(const float* __restrict__ src, int64_t stride, int n, int nv,
                                float* cum_hi, float* cum_lo, float* total) {
+  auto ld = [&](int t) { return kShared ? src[(int64_t)t * stride] : __ldg(src + (int64_t)t * stride); };
   if (threadIdx.x >= 32) return;
   const int lane = threadIdx.x;
   const int per = (n + 31) / 32;
   const int beg = min(n, lane * per), end = min(n, beg + per);
   DF s = {0.f, 0.f};
-  for (int t = beg; t < min(end, nv); ++t) s = df_add(s, DF{__ldg(src + (int64_t)t * stride), 0.f});
+  for (int t = beg; t < min(end, nv); ++t) s = df_add(s, DF{ld(t), 0.f});
   DF incl = s;
 #pragma unroll
   for (int off = 1; off < 32; off <<= 1) {
@@ -48,7 +52,7 @@ __device__ inline void chunk_prefix64(const float* __restrict__ src, int64_t str
   DF acc = df_shfl_up(incl, 1);
   if (lane == 0) acc = DF{0.f, 0.f};
   for (int t = beg; t < end; ++t) {
-    if (t < nv) acc = df_add(acc, DF{__ldg(src + (int64_t)t * stride), 0.f});
+    if (t < nv) acc = df_add(acc, DF{ld(t), 0.f});
     const float chi = acc.hi * kLog2e64;
     cum_hi[t] = chi;
     cum_lo[t] = fmaf(acc.hi, kLog2e64, -chi) + acc.lo * kLog2e64;
@@ -76,14 +80,16 @@ __device__ inline void issue_theta64(const GenericParams& p, int64_t b, int64_t 
 }
 
 // With staged = true the theta rows were issued earlier by issue_theta64 (and are waited for
-// here).
+// here).  kThreads = blockDim.x (a multiple of 32).  phi0: the chunk's 32 start angles staged in
+// shared memory, or null to read them from p.phi.
+template <int kThreads = kPrepThreads>
 __device__ inline void chunk_angles64(const GenericParams& p, int64_t b, int64_t c, int64_t h, int n,
-                               float* ang, bool staged = false) {
-  __shared__ float part_hi[kPrepThreads], part_lo[kPrepThreads];
+                               float* ang, bool staged = false, const double* phi0 = nullptr) {
+  __shared__ float part_hi[kThreads], part_lo[kThreads];
   if (!staged) issue_theta64(p, b, c, h, n, ang);
   cp_async_wait_all();
   __syncthreads();
-  constexpr int kGroups = kPrepThreads / kPairs64;        // 8 step groups per pair
+  constexpr int kGroups = kThreads / kPairs64;            // step groups per pair
   const int k = threadIdx.x % kPairs64, gr = threadIdx.x / kPairs64;
   const int per = (n + kGroups - 1) / kGroups;
   const int beg = min(n, gr * per), end = min(n, beg + per);
@@ -92,7 +98,8 @@ __device__ inline void chunk_angles64(const GenericParams& p, int64_t b, int64_t
   part_hi[threadIdx.x] = run.hi;
   part_lo[threadIdx.x] = run.lo;
   __syncthreads();
-  const double a0 = p.phi[((b * (p.nch + 1) + c) * p.H + h) * kPairs64 + k];   // in [-pi, pi]
+  const double a0 = phi0 ? phi0[k]   // in [-pi, pi]
+                          : p.phi[((b * (p.nch + 1) + c) * p.H + h) * kPairs64 + k];
   const float s_hi = (float)a0;
   DF acc = {s_hi, (float)(a0 - (double)s_hi)};
   for (int g = 0; g < gr; ++g)

@@ -29,6 +29,8 @@
 // writes no y there.
 #include <math.h>
 
+#include <algorithm>
+
 #include "chunk_prep.cuh"
 #include "common.cuh"
 #include "fp_helpers.cuh"
@@ -44,7 +46,7 @@ using namespace tc;
 
 constexpr int kRows = 128;                       // fused rows per chunk = MMA M
 constexpr int kD = 64;                           // P = N
-constexpr int kThreads = kPrepThreads;           // 8 warps
+constexpr int kThreads = 512;                    // 16 warps: 4 per TMEM lane quarter
 constexpr uint32_t kOpBytes = kRows * kD * 4;    // one 128 x 64 fp32 operand: 32 KB
 constexpr uint32_t kAtom128 = kRows * 128;       // a 32-column atom of a 128-row operand
 constexpr uint32_t kAtom64 = kD * 128;           // a 32-column atom of a 64-row operand
@@ -59,7 +61,10 @@ constexpr uint32_t kOffHLo = kOffHHi + kOpBytes / 2;
 constexpr uint32_t kOffAng = kOffHLo + kOpBytes / 2;           // angles [step][pair]
 constexpr uint32_t kOffCum = kOffAng + kRows * kPairs64 * 4;   // cum_hi, cum_lo [step]
 constexpr uint32_t kOffXRaw = kOffCum + 2 * kRows * 4;         // raw x rows [j][p]
-constexpr uint32_t kOffBar = kOffXRaw + kOpBytes;              // 2 mbarriers + TMEM base
+// raw C, B and h_in rows land in the B~ hi, B~ lo and h lo buffers before staging
+constexpr uint32_t kOffPhi0 = kOffXRaw + kOpBytes;             // the 32 chunk-start angles
+constexpr uint32_t kOffDA = kOffPhi0 + kPairs64 * 8;            // dA of the chunk's steps
+constexpr uint32_t kOffBar = kOffDA + kRows * 4;                // 2 mbarriers + TMEM base
 constexpr uint32_t kSmemUsed = kOffBar + 32;
 constexpr uint32_t kSmemAlloc = kSmemUsed + 1024;              // the base is aligned up to 1 KB
 constexpr uint32_t kTmemCols = 512;
@@ -91,7 +96,71 @@ __device__ __forceinline__ float comp(const float4& v, int e) {
   return e == 0 ? v.x : (e == 1 ? v.y : (e == 2 ? v.z : v.w));
 }
 
-__global__ void __launch_bounds__(kThreads, 1) tc32_scan_kernel(GenericParams p) {
+// Tile u of the grid-stride loop: chunk c fastest, then head h, then batch b.
+struct Tile {
+  int64_t c, h, b;
+};
+__device__ __forceinline__ Tile tile_of(const GenericParams& p, int64_t u) {
+  Tile t;
+  t.c = u % p.nch;
+  const int64_t r = u / p.nch;
+  t.h = r % p.H;
+  t.b = r / p.H;
+  return t;
+}
+
+// cp.async copies of tile t's dA, chunk-start angles and theta, raw C rows (into the B~ hi
+// buffer), raw B rows (into the B~ lo buffer) and h_in (into the h lo buffer), rows past the
+// chunk's real ones zero-filled.  Their buffers are free once the previous tile's phase-1
+// products completed and its prefix sums and angles were formed.
+__device__ void issue_main(const GenericParams& p, const Tile& t, uint8_t* smem, float* ang) {
+  const int R = (int)p.R;
+  const int64_t g = t.h / (p.H / p.G);
+  const int nv = steps64(p, t.b, t.c);
+  const int nvr = nv * R;
+  const int64_t row0 = (t.b * p.T + t.c * p.l) * R;
+  const float* dA = p.dA + (t.b * p.T + t.c * p.l) * p.H + t.h;
+  for (int k = threadIdx.x; k < nv; k += kThreads)
+    cp_async4(smem + kOffDA + 4 * k, dA + (int64_t)k * p.H);
+  if (p.theta) {
+    issue_theta64(p, t.b, t.c, t.h, (int)p.l, ang);
+    const double* ph = p.phi + ((t.b * (p.nch + 1) + t.c) * p.H + t.h) * kPairs64;
+    for (int k = threadIdx.x; k < kPairs64 / 2; k += kThreads)
+      cp_async16(smem + kOffPhi0 + 16 * k, ph + 2 * k, 16);
+  }
+  const float* Cg = static_cast<const float*>(p.C);
+  const float* Bg = static_cast<const float*>(p.B);
+  for (int e = threadIdx.x; e < kRows * kD / 4; e += kThreads) {
+    const int row = e >> 4, q4 = e & 15;
+    const bool real = row < nvr;
+    const int64_t r = row0 + (real ? row : 0);
+    cp_async16(smem + kOffBHi + 16 * e, Cg + (r * p.G + g) * kD + 4 * q4, real ? 16 : 0);
+    cp_async16(smem + kOffBLo + 16 * e, Bg + (r * p.G + g) * kD + 4 * q4, real ? 16 : 0);
+  }
+  const float* hin = p.states + ((t.b * p.nch + t.c) * p.H + t.h) * (kD * kD);
+  for (int e = threadIdx.x; e < kD * kD / 4; e += kThreads)
+    cp_async16(smem + kOffHLo + 16 * e, hin + 4 * e, 16);
+}
+
+// cp.async copies of tile t's raw x rows; their buffer is free once the previous tile's x^T
+// was formed.
+__device__ void issue_x(const GenericParams& p, const Tile& t, uint8_t* smem) {
+  const int R = (int)p.R;
+  const int nvr = steps64(p, t.b, t.c) * R;
+  const int64_t row0 = (t.b * p.T + t.c * p.l) * R;
+  const float* Xg = static_cast<const float*>(p.x);
+  for (int e = threadIdx.x; e < kRows * kD / 4; e += kThreads) {
+    const int row = e >> 4, q4 = e & 15;
+    const bool real = row < nvr;
+    cp_async16(smem + kOffXRaw + 16 * e, Xg + ((row0 + (real ? row : 0)) * p.H + t.h) * kD + 4 * q4,
+               real ? 16 : 0);
+  }
+}
+
+// One CTA per SM walks the tiles u = blockIdx.x, + gridDim.x, ...; the copies of tile u + grid
+// are issued while tile u's mask, x^T, phase 2 and output run, so the loads of one tile overlap
+// the arithmetic of the previous one.
+__global__ void __launch_bounds__(kThreads, 1) tc32_scan_kernel(GenericParams p, int64_t ntiles) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   float* ang = reinterpret_cast<float*>(smem + kOffAng);
@@ -101,13 +170,13 @@ __global__ void __launch_bounds__(kThreads, 1) tc32_scan_kernel(GenericParams p)
   uint64_t* drain = bar + 1;                                          // abort path
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + kOffBar + 16);
 
-  const int64_t c = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
-  const int64_t g = h / (p.H / p.G);
   const int l = (int)p.l;                        // steps per chunk (128 / R)
   const int R = (int)p.R, rs = rank_shift(p);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nvr = steps64(p, b, c) * R;          // real fused rows of the chunk
-  const int64_t row0 = (b * p.T + c * p.l) * R;  // fused row of the chunk's first step
+  const int q = warp & 3, cw = warp >> 2;        // TMEM lane quarter; column quarter of the warp
+  const int i = 32 * q + lane;                   // the row this thread reads out
+  const int ti = i >> rs;
+  const uint32_t lane_addr = static_cast<uint32_t>(32 * q) << 16;
 
   if (threadIdx.x == 0) {
     mbar_init(bar, 1);
@@ -118,80 +187,13 @@ __global__ void __launch_bounds__(kThreads, 1) tc32_scan_kernel(GenericParams p)
     tmem_alloc(s_tmem, kTmemCols);
     tmem_relinquish();
   }
-  // Every global read of the chunk is issued here, before any of them is waited for: theta,
-  // and the raw rows of C, B (into the lo halves of their operands, read back below before
-  // they are overwritten), h_in (into the lo half of its operand) and x, zero-filled past the
-  // chunk's real rows; warp 0 meanwhile forms the prefix sums of dA.
-  if (p.theta) issue_theta64(p, b, c, h, l, ang);
-  {
-    const float* Cg = static_cast<const float*>(p.C);
-    const float* Bg = static_cast<const float*>(p.B);
-    const float* Xg = static_cast<const float*>(p.x);
-    for (int e = threadIdx.x; e < kRows * kD / 4; e += kThreads) {
-      const int row = e >> 4, q4 = e & 15;
-      const bool real = row < nvr;
-      const int64_t r = row0 + (real ? row : 0);
-      cp_async16(smem + kOffCLo + 16 * e, Cg + (r * p.G + g) * kD + 4 * q4, real ? 16 : 0);
-      cp_async16(smem + kOffBLo + 16 * e, Bg + (r * p.G + g) * kD + 4 * q4, real ? 16 : 0);
-      cp_async16(smem + kOffXRaw + 16 * e, Xg + (r * p.H + h) * kD + 4 * q4, real ? 16 : 0);
-    }
-    const float* hin = p.states + ((b * p.nch + c) * p.H + h) * (kD * kD);
-    for (int e = threadIdx.x; e < kD * kD / 4; e += kThreads)
-      cp_async16(smem + kOffHLo + 16 * e, hin + 4 * e, 16);
-    cp_async_commit();
+  int64_t u = blockIdx.x;
+  if (u < ntiles) {
+    const Tile t = tile_of(p, u);
+    issue_main(p, t, smem, ang);
+    issue_x(p, t, smem);
   }
-  chunk_prefix64(p.dA + (b * p.T + c * p.l) * p.H + h, p.H, l, steps64(p, b, c), cum_hi, cum_lo,
-                 nullptr);
-  if (p.theta) {
-    chunk_angles64(p, b, c, h, l, ang, true);   // waits for every copy above
-  } else {
-    cp_async_wait_all();
-    __syncthreads();
-  }
-
-  // ------------------------------------------------------------------ staging
-  {
-    // C~ and B~: the half-warps of a row read it whole; both are turned by the same angle.  All
-    // raw values are read into registers before the first hi / lo store overwrites them.
-    const int ch = threadIdx.x & 15;   // k = 4 ch .. 4 ch + 3 (rotation pairs 2 ch, 2 ch + 1)
-    float4 cv[kRows / 16], bv[kRows / 16], hv[kD / 16];
-#pragma unroll
-    for (int r = 0; r < kRows / 16; ++r) {
-      const int e = threadIdx.x + kThreads * r;   // row (threadIdx.x >> 4) + 16 r, chunk ch
-      cv[r] = *reinterpret_cast<const float4*>(smem + kOffCLo + 16 * e);
-      bv[r] = *reinterpret_cast<const float4*>(smem + kOffBLo + 16 * e);
-    }
-#pragma unroll
-    for (int r = 0; r < kD / 16; ++r)
-      hv[r] = *reinterpret_cast<const float4*>(smem + kOffHLo + 16 * (threadIdx.x + kThreads * r));
-    __syncthreads();
-#pragma unroll
-    for (int r = 0; r < kRows / 16; ++r) {
-      const int row = (threadIdx.x >> 4) + 16 * r;
-      float4 cr = cv[r], br = bv[r];
-      if (p.theta) {
-        const float* ar = ang + (row >> rs) * kPairs64 + 2 * ch;
-        float s0, c0, s1, c1;
-        sincosf(ar[0], &s0, &c0);
-        sincosf(ar[1], &s1, &c1);
-        cr = make_float4(c0 * cr.x + s0 * cr.y, -s0 * cr.x + c0 * cr.y, c1 * cr.z + s1 * cr.w,
-                         -s1 * cr.z + c1 * cr.w);
-        br = make_float4(c0 * br.x + s0 * br.y, -s0 * br.x + c0 * br.y, c1 * br.z + s1 * br.w,
-                         -s1 * br.z + c1 * br.w);
-      }
-      const uint32_t o = kmaj_off(kRows, row, 4 * ch);
-      store_split(smem + kOffCHi + o, smem + kOffCLo + o, cr);
-      store_split(smem + kOffBHi + o, smem + kOffBLo + o, br);
-    }
-    // h_in [p][n] is K-major for Yo as it stands (rows p, K = n)
-#pragma unroll
-    for (int r = 0; r < kD / 16; ++r) {
-      const int pp = (threadIdx.x >> 4) + 16 * r;
-      const uint32_t o = kmaj_off(kD, pp, 4 * ch);
-      store_split(smem + kOffHHi + o, smem + kOffHLo + o, hv[r]);
-    }
-  }
-  fence_proxy_async_smem();
+  cp_async_commit();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -200,77 +202,141 @@ __global__ void __launch_bounds__(kThreads, 1) tc32_scan_kernel(GenericParams p)
   constexpr uint32_t id_n128 = idesc_tf32(128, 128, 0, 0);
   constexpr uint32_t id_n64 = idesc_tf32(128, 64, 0, 0);
   constexpr uint32_t dh = sdesc_sw128_hi(1024);
-  // ------------------------------------------------------------------ phase 1: CB, Yo
-  if (warp == 1) {
-    const uint32_t c_lo[2] = {sdesc_sw128_lo(smem_u32(smem + kOffCHi), 0),
-                              sdesc_sw128_lo(smem_u32(smem + kOffCLo), 0)};
-    const uint32_t b_lo[2] = {sdesc_sw128_lo(smem_u32(smem + kOffBHi), 0),
-                              sdesc_sw128_lo(smem_u32(smem + kOffBLo), 0)};
-    const uint32_t h_lo[2] = {sdesc_sw128_lo(smem_u32(smem + kOffHHi), 0),
-                              sdesc_sw128_lo(smem_u32(smem + kOffHLo), 0)};
-    // products (hi, lo), (lo, hi), (hi, hi) in this order (A part pr == 1, B part pr == 0 or
-    // 1): the two small correction products go in first, so the accumulator truncates at their
-    // magnitude and only the last four steps truncate at the block's own
-#pragma unroll
-    for (int kb = 0; kb < 2; ++kb)
-#pragma unroll
-      for (int pr = 0; pr < 3; ++pr)
-#pragma unroll
-        for (int ks = 0; ks < 4; ++ks) {
-          const uint32_t ko = (kb * kAtom128 + ks * 32) >> 4;
-          mma_ss_we_tf32(tmem + kColCB + kb * 128, c_lo[pr == 1] + ko, dh, b_lo[pr == 0] + ko, dh,
-                         id_n128, (pr | ks) != 0);
-        }
-#pragma unroll
-    for (int kb = 0; kb < 2; ++kb)
-#pragma unroll
-      for (int pr = 0; pr < 3; ++pr)
-#pragma unroll
-        for (int ks = 0; ks < 4; ++ks) {
-          const uint32_t ka = (kb * kAtom128 + ks * 32) >> 4, kh = (kb * kAtom64 + ks * 32) >> 4;
-          mma_ss_we_tf32(tmem + kColYo + kb * 64, c_lo[pr == 1] + ka, dh, h_lo[pr == 0] + kh, dh,
-                         id_n64, (pr | ks) != 0);
-        }
-    mma_commit_elect(bar);
-  }
-  const int q = warp & 3, hf = warp >> 2;   // TMEM lane quarter; column half
-  const int i = 32 * q + lane;              // the row this thread reads out
-  const int ti = i >> rs;
-  const uint32_t lane_addr = static_cast<uint32_t>(32 * q) << 16;
-  const int jc = lane & 3;
-  bool ok = mbar_wait_bounded(bar, 0, kWaitNs);
-  ok = __syncthreads_and(ok) != 0;
-  float yo[32];
-  if (ok) {
-    tc_fence_after();
-    // ---------------------------------------------------------------- Yo, mask, x^T
+  bool ok = true;
+  for (; u < ntiles; u += gridDim.x) {
+    const Tile t = tile_of(p, u);
+    const int64_t nx = u + gridDim.x;
+    const int nvr = steps64(p, t.b, t.c) * R;          // real fused rows of the chunk
+    const int64_t row0 = (t.b * p.T + t.c * p.l) * R;  // fused row of the chunk's first step
+    // prefix sums of dA (warp 0) and the rotation angles, from this tile's staged copies
+    cp_async_wait_all();
+    __syncthreads();
+    chunk_prefix64<true>(reinterpret_cast<const float*>(smem + kOffDA), 1, l, steps64(p, t.b, t.c),
+                         cum_hi, cum_lo, nullptr);
+    if (p.theta) {
+      chunk_angles64<kThreads>(p, t.b, t.c, t.h, l, ang, true,
+                               reinterpret_cast<const double*>(smem + kOffPhi0));
+    } else {
+      __syncthreads();
+    }
+
+    // ---------------------------------------------------------------- staging
     {
-      float a0[32], a1[32];
-      tmem_ld32(tmem + lane_addr + kColYo + 32 * hf, a0);
-      tmem_ld32(tmem + lane_addr + kColYo + 64 + 32 * hf, a1);
+      // C~ and B~: the half-warps of a row read it whole; both are turned by the same angle.
+      // All raw values are read into registers before the first hi / lo store overwrites them.
+      constexpr int kRowStep = kThreads / 16;   // rows per pass of the block
+      const int ch = threadIdx.x & 15;   // k = 4 ch .. 4 ch + 3 (rotation pairs 2 ch, 2 ch + 1)
+      float4 cv[kRows / kRowStep], bv[kRows / kRowStep], hv[kD / kRowStep];
+#pragma unroll
+      for (int r = 0; r < kRows / kRowStep; ++r) {
+        const int e = threadIdx.x + kThreads * r;   // row (threadIdx.x >> 4) + kRowStep r
+        cv[r] = *reinterpret_cast<const float4*>(smem + kOffBHi + 16 * e);
+        bv[r] = *reinterpret_cast<const float4*>(smem + kOffBLo + 16 * e);
+      }
+#pragma unroll
+      for (int r = 0; r < kD / kRowStep; ++r)
+        hv[r] = *reinterpret_cast<const float4*>(smem + kOffHLo + 16 * (threadIdx.x + kThreads * r));
+      __syncthreads();
+#pragma unroll
+      for (int r = 0; r < kRows / kRowStep; ++r) {
+        const int row = (threadIdx.x >> 4) + kRowStep * r;
+        float4 cr = cv[r], br = bv[r];
+        if (p.theta) {
+          const float* ar = ang + (row >> rs) * kPairs64 + 2 * ch;
+          float s0, c0, s1, c1;
+          sincosf(ar[0], &s0, &c0);
+          sincosf(ar[1], &s1, &c1);
+          cr = make_float4(c0 * cr.x + s0 * cr.y, -s0 * cr.x + c0 * cr.y, c1 * cr.z + s1 * cr.w,
+                           -s1 * cr.z + c1 * cr.w);
+          br = make_float4(c0 * br.x + s0 * br.y, -s0 * br.x + c0 * br.y, c1 * br.z + s1 * br.w,
+                           -s1 * br.z + c1 * br.w);
+        }
+        const uint32_t o = kmaj_off(kRows, row, 4 * ch);
+        store_split(smem + kOffCHi + o, smem + kOffCLo + o, cr);
+        store_split(smem + kOffBHi + o, smem + kOffBLo + o, br);
+      }
+      // h_in [p][n] is K-major for Yo as it stands (rows p, K = n)
+#pragma unroll
+      for (int r = 0; r < kD / kRowStep; ++r) {
+        const int pp = (threadIdx.x >> 4) + kRowStep * r;
+        const uint32_t o = kmaj_off(kD, pp, 4 * ch);
+        store_split(smem + kOffHHi + o, smem + kOffHLo + o, hv[r]);
+      }
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+
+    // ---------------------------------------------------------------- phase 1: CB, Yo
+    if (warp == 1) {
+      const uint32_t c_lo[2] = {sdesc_sw128_lo(smem_u32(smem + kOffCHi), 0),
+                                sdesc_sw128_lo(smem_u32(smem + kOffCLo), 0)};
+      const uint32_t b_lo[2] = {sdesc_sw128_lo(smem_u32(smem + kOffBHi), 0),
+                                sdesc_sw128_lo(smem_u32(smem + kOffBLo), 0)};
+      const uint32_t h_lo[2] = {sdesc_sw128_lo(smem_u32(smem + kOffHHi), 0),
+                                sdesc_sw128_lo(smem_u32(smem + kOffHLo), 0)};
+      // products (hi, lo), (lo, hi), (hi, hi) in this order (A part pr == 1, B part pr == 0):
+      // the two small correction products go in first, so the accumulator truncates at their
+      // magnitude and only the last four steps truncate at the block's own
+#pragma unroll
+      for (int kb = 0; kb < 2; ++kb)
+#pragma unroll
+        for (int pr = 0; pr < 3; ++pr)
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks) {
+            const uint32_t ko = (kb * kAtom128 + ks * 32) >> 4;
+            mma_ss_we_tf32(tmem + kColCB + kb * 128, c_lo[pr == 1] + ko, dh, b_lo[pr == 0] + ko,
+                           dh, id_n128, (pr | ks) != 0);
+          }
+#pragma unroll
+      for (int kb = 0; kb < 2; ++kb)
+#pragma unroll
+        for (int pr = 0; pr < 3; ++pr)
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks) {
+            const uint32_t ka = (kb * kAtom128 + ks * 32) >> 4;
+            const uint32_t kh = (kb * kAtom64 + ks * 32) >> 4;
+            mma_ss_we_tf32(tmem + kColYo + kb * 64, c_lo[pr == 1] + ka, dh, h_lo[pr == 0] + kh,
+                           dh, id_n64, (pr | ks) != 0);
+          }
+      mma_commit_elect(bar);
+    }
+    ok = mbar_wait_bounded(bar, 0, kWaitNs);
+    ok = __syncthreads_and(ok) != 0;
+    if (!ok) break;
+    tc_fence_after();
+
+    // ---------------------------------------------------------------- Yo, mask, x^T
+    float yo[16];   // Yo of row i, columns p = 16 cw .. 16 cw + 15
+    {
+      float a0[16], a1[16];
+      tmem_ld16(tmem + lane_addr + kColYo + 16 * cw, a0);
+      tmem_ld16(tmem + lane_addr + kColYo + 64 + 16 * cw, a1);
       tmem_ld_wait();
       reg_tie(a0);
       reg_tie(a1);
 #pragma unroll
-      for (int k = 0; k < 32; ++k) yo[k] = a0[k] + a1[k];
+      for (int k = 0; k < 16; ++k) yo[k] = a0[k] + a1[k];
     }
+    // the mask of columns j = 32 cw .. 32 cw + 31, 16 at a time
     const float chi = cum_hi[ti], clo = cum_lo[ti];
 #pragma unroll 1
-    for (int cb = 2 * hf; cb < 2 * hf + 2; ++cb) {
-      const int j0 = 32 * cb;
-      uint32_t mh[32], ml[32];
+    for (int hb = 0; hb < 2; ++hb) {
+      const int j0 = 32 * cw + 16 * hb;
+      uint32_t mh[16], ml[16];
       if ((j0 >> rs) > ((32 * q + 31) >> rs)) {   // every column after every row's step
 #pragma unroll
-        for (int k = 0; k < 32; ++k) mh[k] = ml[k] = 0u;
+        for (int k = 0; k < 16; ++k) mh[k] = ml[k] = 0u;
       } else {
-        float v0[32], v1[32];
-        tmem_ld32(tmem + lane_addr + kColCB + j0, v0);
-        tmem_ld32(tmem + lane_addr + kColCB + 128 + j0, v1);
+        float v0[16], v1[16];
+        tmem_ld16(tmem + lane_addr + kColCB + j0, v0);
+        tmem_ld16(tmem + lane_addr + kColCB + 128 + j0, v1);
         tmem_ld_wait();
         reg_tie(v0);
         reg_tie(v1);
 #pragma unroll
-        for (int k = 0; k < 32; ++k) {
+        for (int k = 0; k < 16; ++k) {
           const int tj = (j0 + k) >> rs;
           const float m = tj <= ti
                               ? exp2f((chi - cum_hi[tj]) + (clo - cum_lo[tj])) * (v0[k] + v1[k])
@@ -280,17 +346,15 @@ __global__ void __launch_bounds__(kThreads, 1) tc32_scan_kernel(GenericParams p)
           ml[k] = __float_as_uint(m - mhi);
         }
       }
-      tmem_st32u(tmem + lane_addr + kColCB + j0, mh);
-      tmem_st32u(tmem + lane_addr + kColCB + 128 + j0, ml);
+      tmem_st16u(tmem + lane_addr + kColCB + j0, mh);
+      tmem_st16u(tmem + lane_addr + kColCB + 128 + j0, ml);
     }
-    // x^T [p][j] hi / lo from the raw rows (task k of the warp: rows 16 jg .. 16 jg + 15,
-    // columns 32 ph .. 32 ph + 31; lane: 4 rows from 4 jc, columns 4 cq ..): per store the 8
-    // lanes of a quarter warp cover 4 j chunks x 2 p rows of different parity, i.e. 8 distinct
-    // swizzled chunk positions (conflict-free)
-#pragma unroll
-    for (int tk = 0; tk < 2; ++tk) {
-      const int task = warp + 8 * tk, jg = task & 7, cq = 8 * (task >> 3) + (lane >> 2);
-#pragma unroll
+    // x^T [p][j] hi / lo from the raw rows (the warp's task: rows 16 jg .. 16 jg + 15, columns
+    // 32 ph .. 32 ph + 31; lane: 4 rows from 4 jc, columns 4 cq ..): per store the 8 lanes of a
+    // quarter warp cover 4 j chunks x 2 p rows of different parity, i.e. 8 distinct swizzled
+    // chunk positions (conflict-free)
+    {
+      const int jc = lane & 3, jg = warp & 7, cq = 8 * (warp >> 3) + (lane >> 2);
       float4 xr[4];   // rows 16 jg + 4 jc + r, columns 4 cq .. 4 cq + 3
 #pragma unroll
       for (int r = 0; r < 4; ++r)
@@ -298,66 +362,80 @@ __global__ void __launch_bounds__(kThreads, 1) tc32_scan_kernel(GenericParams p)
                                                  16 * ((16 * jg + 4 * jc + r) * (kD / 4) + cq));
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const float4 v = make_float4(comp(xr[0], e), comp(xr[1], e), comp(xr[2], e), comp(xr[3], e));
+        const float4 v =
+            make_float4(comp(xr[0], e), comp(xr[1], e), comp(xr[2], e), comp(xr[3], e));
         const uint32_t o = kmaj_off(kD, 4 * cq + e, 16 * jg + 4 * jc);
         store_split(smem + kOffXHi + o, smem + kOffXLo + o, v);
       }
     }
     tmem_st_wait();
-  }
-  fence_proxy_async_smem();
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  // ------------------------------------------------------------------ phase 2: Yd
-  if (ok && warp == 1) {
-    const uint32_t x_lo[2] = {sdesc_sw128_lo(smem_u32(smem + kOffXHi), 0),
-                              sdesc_sw128_lo(smem_u32(smem + kOffXLo), 0)};
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    // the next tile's inputs: phase 1 read B~ and h_in, staging read the angles, the raw x rows
+    // were transposed; these copies overlap phase 2, the output and the next prefix sums
+    if (nx < ntiles) {
+      const Tile tn = tile_of(p, nx);
+      issue_main(p, tn, smem, ang);
+      issue_x(p, tn, smem);
+    }
+    cp_async_commit();
+
+    // ---------------------------------------------------------------- phase 2: Yd
+    if (warp == 1) {
+      const uint32_t x_lo[2] = {sdesc_sw128_lo(smem_u32(smem + kOffXHi), 0),
+                                sdesc_sw128_lo(smem_u32(smem + kOffXLo), 0)};
 #pragma unroll
-    for (int kb = 0; kb < 4; ++kb)
+      for (int kb = 0; kb < 4; ++kb)
 #pragma unroll
-      for (int pr = 0; pr < 3; ++pr)
+        for (int pr = 0; pr < 3; ++pr)
 #pragma unroll
-        for (int ks = 0; ks < 4; ++ks)
-          mma_ts_we_tf32(tmem + kColYd + kb * 64,
-                         tmem + kColCB + (pr == 1 ? 128 : 0) + kb * 32 + ks * 8,
-                         x_lo[pr == 0] + ((kb * kAtom64 + ks * 32) >> 4), dh, id_n64,
-                         (pr | ks) != 0);
-    mma_commit_elect(bar);
-  }
-  if (ok) {
+          for (int ks = 0; ks < 4; ++ks)
+            mma_ts_we_tf32(tmem + kColYd + kb * 64,
+                           tmem + kColCB + (pr == 1 ? 128 : 0) + kb * 32 + ks * 8,
+                           x_lo[pr == 0] + ((kb * kAtom64 + ks * 32) >> 4), dh, id_n64,
+                           (pr | ks) != 0);
+      mma_commit_elect(bar);
+    }
     ok = mbar_wait_bounded(bar, 1, kWaitNs);
     ok = __syncthreads_and(ok) != 0;
-  }
-  if (ok) {
+    if (!ok) break;
     tc_fence_after();
-    float yd[32];
+    {
+      float yd[16];
 #pragma unroll
-    for (int k = 0; k < 32; ++k) yd[k] = 0.f;
+      for (int k = 0; k < 16; ++k) yd[k] = 0.f;
 #pragma unroll
-    for (int kb = 0; kb < 4; kb += 2) {
-      float a0[32], a1[32];
-      tmem_ld32(tmem + lane_addr + kColYd + kb * 64 + 32 * hf, a0);
-      tmem_ld32(tmem + lane_addr + kColYd + (kb + 1) * 64 + 32 * hf, a1);
-      tmem_ld_wait();
-      reg_tie(a0);
-      reg_tie(a1);
+      for (int kb = 0; kb < 4; kb += 2) {
+        float a0[16], a1[16];
+        tmem_ld16(tmem + lane_addr + kColYd + kb * 64 + 16 * cw, a0);
+        tmem_ld16(tmem + lane_addr + kColYd + (kb + 1) * 64 + 16 * cw, a1);
+        tmem_ld_wait();
+        reg_tie(a0);
+        reg_tie(a1);
 #pragma unroll
-      for (int k = 0; k < 32; ++k) yd[k] = (yd[k] + a0[k]) + a1[k];
-    }
-    if (i < nvr) {
-      const float sc = exp2f(cum_hi[ti] + cum_lo[ti]);   // e^{cum of row i's step}
-      const int64_t yoff = ((row0 + i) * p.H + h) * kD + 32 * hf;
-      if (SSD_INDEX_OK(p.hdr, yoff + 31, p.batch * p.T * p.R * p.H * kD, 24)) {
-        float4* y4 = reinterpret_cast<float4*>(static_cast<float*>(p.y) + yoff);
+        for (int k = 0; k < 16; ++k) yd[k] = (yd[k] + a0[k]) + a1[k];
+      }
+      if (i < nvr) {
+        const float sc = exp2f(chi + clo);   // e^{cum of row i's step}
+        const int64_t yoff = ((row0 + i) * p.H + t.h) * kD + 16 * cw;
+        if (SSD_INDEX_OK(p.hdr, yoff + 15, p.batch * p.T * p.R * p.H * kD, 24)) {
+          float4* y4 = reinterpret_cast<float4*>(static_cast<float*>(p.y) + yoff);
 #pragma unroll
-        for (int k = 0; k < 8; ++k)
-          y4[k] = make_float4(fmaf(sc, yo[4 * k], yd[4 * k]), fmaf(sc, yo[4 * k + 1], yd[4 * k + 1]),
-                              fmaf(sc, yo[4 * k + 2], yd[4 * k + 2]),
-                              fmaf(sc, yo[4 * k + 3], yd[4 * k + 3]));
+          for (int k = 0; k < 4; ++k)
+            y4[k] = make_float4(fmaf(sc, yo[4 * k], yd[4 * k]),
+                                fmaf(sc, yo[4 * k + 1], yd[4 * k + 1]),
+                                fmaf(sc, yo[4 * k + 2], yd[4 * k + 2]),
+                                fmaf(sc, yo[4 * k + 3], yd[4 * k + 3]));
+        }
       }
     }
-  } else {
+    // this tile's TMEM columns and cum arrays are read; the next tile may overwrite them
+    tc_fence_before();
+    __syncthreads();
+  }
+  if (!ok) {
     // a bounded wait gave up: latch it, then wait (bounded again) until every MMA issued so
     // far has completed before TMEM is released
     if (threadIdx.x == 0 && p.hdr) latch_error(p.hdr, SSD_ERR_TIMEOUT, 25);
@@ -365,6 +443,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc32_scan_kernel(GenericParams p)
     if (!mbar_wait_bounded(drain, 0, kWaitNs) && threadIdx.x == 0 && p.hdr)
       latch_error(p.hdr, SSD_ERR_TIMEOUT, 26);
   }
+  cp_async_wait_all();   // no copy may still be landing in shared memory at exit
   tc_fence_before();
   __syncthreads();
   if (warp == 0) {
@@ -387,8 +466,14 @@ cudaError_t tc32_scan(const GenericParams& p, cudaStream_t st) {
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)kSmemAlloc);
   if (e != cudaSuccess) return e;
-  const dim3 grid((unsigned)p.nch, (unsigned)p.H, (unsigned)p.batch);
-  tc32_scan_kernel<<<grid, kThreads, kSmemAlloc, st>>>(p);
+  int dev = 0, sms = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+    return e;
+  const int64_t ntiles = p.nch * p.H * p.batch;
+  const unsigned grid = (unsigned)std::min<int64_t>(ntiles, std::max(sms, 1));
+  if (grid == 0) return cudaSuccess;
+  tc32_scan_kernel<<<grid, kThreads, kSmemAlloc, st>>>(p, ntiles);
   return cudaGetLastError();
 }
 
