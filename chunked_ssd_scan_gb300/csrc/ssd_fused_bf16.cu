@@ -405,18 +405,33 @@ __device__ __forceinline__ MaskShare mask_share(int warp) {
 }
 constexpr int kMaskWarps = 5;
 
-// (dec o x) work units (32 rows x 16 columns; 16 per tile) of the warps that compute it: most on
-// sub-partition 0 (the least mask work), none on sub-partition 2 (three mask blocks and K1).
+// (dec o x) work units (32 rows x 16 columns; 16 per tile) of the warps that compute it.  In the
+// full pass most go to sub-partition 0 (the least mask work) and none to sub-partition 2 (three
+// mask blocks and K1); the pre-pass has no mask, so there the five mask warps share them evenly.
+template <bool kPre>
 __device__ __forceinline__ int2 dx_units(int warp) {
-  switch (warp) {
-    case 4: return make_int2(0, 7);
-    case 5: return make_int2(7, 12);
-    case 7: return make_int2(12, 14);
-    case 3: return make_int2(14, 16);
-    default: return make_int2(0, 0);
+  if constexpr (kPre) {
+    switch (warp) {
+      case 4: return make_int2(0, 4);
+      case 5: return make_int2(4, 7);
+      case 6: return make_int2(7, 10);
+      case 7: return make_int2(10, 13);
+      case 3: return make_int2(13, 16);
+      default: return make_int2(0, 0);
+    }
+  } else {
+    switch (warp) {
+      case 4: return make_int2(0, 7);
+      case 5: return make_int2(7, 12);
+      case 7: return make_int2(12, 14);
+      case 3: return make_int2(14, 16);
+      default: return make_int2(0, 0);
+    }
   }
 }
-constexpr int kDxWarps = 4;
+// warps with (dec o x) units (each arrives on k3_go, and in the pre-pass on x_empty)
+template <bool kPre>
+constexpr int kDxWarps = kPre ? 5 : 4;
 
 template <bool kPre, bool kW>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -465,7 +480,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < kXSlots; ++s) {
       mbar_init(&bars->x_full[s], 1);
       // out warps once their y store has read the slot (the pre-pass: the (dec o x) warps)
-      mbar_init(&bars->x_empty[s], kPre ? kDxWarps : 4);
+      mbar_init(&bars->x_empty[s], kPre ? kDxWarps<true> : 4);
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&bars->b_full[s], 1);
@@ -486,7 +501,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars->s_full, 1);
     mbar_init(&bars->yo_go, 8);            // 4 state warps + 4 out warps
     // (dec o x) warps + 4 state warps (+ 4 out warps zeroing B's pad rows in the pre-pass)
-    mbar_init(&bars->k3_go, kDxWarps + 4 + (kPre && zero_b ? 4 : 0));
+    mbar_init(&bars->k3_go, kDxWarps<kPre> + 4 + (kPre && zero_b ? 4 : 0));
     mbar_init(&bars->y_pre, 4);            // out warps
     mbar_init(&bars->drain, 1);
     fence_mbar_init();
@@ -698,7 +713,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ---------------------------------------------------------------- mask warps
       const int jlim = (i / R + 1) * R;     // columns j < jlim are at or before row i's step
       const MaskShare ms = mask_share(warp);
-      const int2 du = dx_units(warp);
+      const int2 du = dx_units<kPre>(warp);
       const bool has_dx = du.y > du.x;
       // (dec o x)_t split into hi and lo (own buffers; x_t stays for Yd_t).
       auto dec_x = [&](int t) -> bool {
