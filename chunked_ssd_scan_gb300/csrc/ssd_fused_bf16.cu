@@ -4,8 +4,8 @@
 // 128 rank-fused rows (fused row i = t*R + r, as in the serial.rs page's K2 reshape), carrying
 // the state on chip from tile to tile, so the inter-chunk state of K4 never goes to HBM.  Per
 // tile:
-//   K1  tile-local inclusive cumsum of dA (double-float), decay factors
-//   K2  CB = C B^T                                       tcgen05.mma, A = C from TMEM
+//   K1  tile-local inclusive cumsum of dA (fp32 over warp shuffles), decay factors
+//   K2  CB = C B^T                                       tcgen05.mma, both from shared memory
 //   K5a (L o CB), L[i,j] = exp(cum[i/R] - cum[j/R]) for j/R <= i/R else 0, split into bf16
 //       hi + lo and written back to TMEM;  Yd = (L o CB) x     tcgen05.mma, A from TMEM
 //   K3  S^T = B^T (dec o x), dec_i = exp(cum_last - cum[i/R]), (dec o x) split hi + lo
@@ -322,7 +322,7 @@ __device__ __forceinline__ void k1_warp(const FusedArgs& a, TileInfo* info, uint
 // Per 128-row tile t the tensor core runs, in this order,
 //   Yo_t     = C_t h_t^T                      A = C_t (TMEM), B = [h_hi ; h_lo]   (K = 2 x 128)
 //   K3_t     = B_t^T [(dec o x)_hi ; lo]      A = B_t (MN-major smem)             (K = 2 x 128)
-//   CB_{t+1} = C_{t+1} B_{t+1}^T              A = C_{t+1} (TMEM), into mask buffer (t+1) & 1
+//   CB_{t+1} = C_{t+1} B_{t+1}^T              both K-major in smem, into mask buffer (t+1) & 1
 //   Yd_t    += (L o CB)_t x_t                 A = (L o CB) hi/lo (TMEM)           (K = 2 x 128)
 // where Yd_t starts from e^{cum_i} Yo_t, written into its accumulator by the out warps, so y_t
 // is one accumulator.  The mask of tile t+1 is computed while Yd_t, Yo_{t+1} and K3_{t+1} run
