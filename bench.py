@@ -47,8 +47,8 @@ ALU_FP32_TFLOPS = round(152 * 128 * 2 * 2.07e9 / 1e12, 1)
 # still held in L2 when the kernel ends are not counted.  Workloads without a capture report
 # null.
 NCU_TRAFFIC_BYTES = {
-    "mamba2_siso_bf16": 77_673_216 + 27_691_520,           # ssd_fused_bf16_kernel<false>
-    "mamba3_mimo_bf16": 1_441_353_984 + 253_872_640,       # ssd_fused_bf16_kernel<false>
+    "mamba2_siso_bf16": 77_669_632 + 27_295_744,           # ssd_fused_bf16_kernel<false>
+    "mamba3_mimo_bf16": 1_441_407_232 + 253_506_816,       # ssd_fused_bf16_kernel<false>
     "long_rotation_f32": 3_937_686_272 + 788_730_368,      # simt_scan_kernel
     "selective_scan_f32": 77_815_552 + 8_036_864,          # ss_lookback_kernel
     # bwd_chunk_grad_kernel, captured at batch 1 and scaled by 4 (traffic grows with the batch)
@@ -256,12 +256,11 @@ def job_tokens(tokens_per_replica: int, world: int) -> int:
 
 
 def kernel_chunk(pkg, shape, R, chunk_len, variant=None):
-    """Steps per chunk the kernels actually tile by: the register-tiled fp32 path uses 64 fused
-    rows (64 / R steps) and the tf32 tensor-core path 128 fused rows (128 / R) whatever
-    chunk_len says; every other path tiles by chunk_len (the fused bf16 kernel's FLOPs are not
-    its bound, so its count keeps chunk_len)."""
+    """Steps per chunk the kernels actually tile by: the fp32 path with the tf32 chunk scan uses
+    128 fused rows (128 / R steps) whatever chunk_len says; every other path tiles by chunk_len
+    (the fused bf16 kernel's FLOPs are not its bound, so its count keeps chunk_len)."""
     v = variant or pkg.ssd_chunked_variant(shape)
-    return {"tiled_f32": 64 // R, "tc_tf32": 128 // R}.get(v, chunk_len)
+    return 128 // R if v == "tc_tf32" else chunk_len
 
 
 def run_ours(args, rank, world, local):

@@ -1,6 +1,5 @@
 // C ABI of the library: argument validation, workspace layout and kernel launches.
 // Declarations and the contract of every entry point are in include/ssdscan.h.
-#include <algorithm>
 #include <string.h>
 
 #include "common.cuh"
@@ -51,18 +50,16 @@ int32_t pick_variant(const ssd_shape* s) {
   if (fused_bf16_supported(s->seqlen, s->nheads, s->headdim, s->dstate, s->mimo_rank,
                            s->chunk_len, s->io_dtype == SSD_BF16, s->has_theta != 0))
     return SSD_VARIANT_TC_BF16;
-  if (simt32_supported(s->headdim, s->dstate, s->mimo_rank, s->chunk_len, s->io_dtype == SSD_BF16,
-                       s->has_theta != 0))
-    return SSD_VARIANT_TILED_F32;
+  if (tc32_supported(s->headdim, s->dstate, s->mimo_rank, s->io_dtype == SSD_BF16))
+    return SSD_VARIANT_TC_TF32;
   return SSD_VARIANT_GENERIC;
 }
 
 // Chunk length the kernels tile time by.  The decomposition is exact for any chunk length, so
-// this is a tiling choice: the register-tiled fp32 kernels use 64 rank-fused rows, i.e. 64 / R
-// steps (their quadratic work per row grows with the chunk, the chunk-state traffic shrinks
-// with it; 64 rows is the faster trade on GB300), every other path the caller's chunk_len.
+// this is a tiling choice: the fp32 path with the tensor-core chunk scan uses 128 rank-fused
+// rows (128 / R steps, one MMA tile), every other path the caller's chunk_len.
 int64_t kernel_chunk_len(const ssd_shape* s) {
-  return pick_variant(s) == SSD_VARIANT_TILED_F32 ? 64 / s->mimo_rank : s->chunk_len;
+  return pick_variant(s) == SSD_VARIANT_TC_TF32 ? tc32_chunk_len(s->mimo_rank) : s->chunk_len;
 }
 
 // Workspace of the chunk pipeline run with chunks of l steps.
@@ -132,7 +129,7 @@ ssd_status check_trap_shape(const ssd_shape* s) {
   const ssd_shape e = trap_expanded(s);
   if ((st = check_shape(&e)) != SSD_OK) return st;
   const int32_t v = pick_variant(&e);
-  return (v == SSD_VARIANT_GENERIC || v == SSD_VARIANT_TILED_F32) ? SSD_OK : SSD_ERR_UNSUPPORTED;
+  return (v == SSD_VARIANT_GENERIC || v == SSD_VARIANT_TC_TF32) ? SSD_OK : SSD_ERR_UNSUPPORTED;
 }
 
 TrapLayout trap_layout(const ssd_shape* s) {
@@ -183,12 +180,7 @@ extern "C" {
 
 size_t ssd_chunked_workspace_bytes(const ssd_shape* shape) {
   if (check_shape(shape) != SSD_OK) return 0;
-  size_t n = ssd_layout(shape).total;
-  // one size serves ssd_chunked_forward_tf32 as well (its chunks of 128 fused rows)
-  if (tc32_supported(shape->headdim, shape->dstate, shape->mimo_rank,
-                     shape->io_dtype == SSD_BF16))
-    n = std::max(n, chunk_layout(shape, tc32_chunk_len(shape->mimo_rank)).total);
-  return n;
+  return ssd_layout(shape).total;   // ssd_chunked_forward_tf32 runs the same layout
 }
 
 int32_t ssd_chunked_launches(const ssd_shape* shape) {
@@ -208,9 +200,9 @@ int32_t ssd_chunked_variant(const ssd_shape* shape) {
 
 namespace {
 
-// The forward entry points; valid_len is null for ssd_chunked_forward, and tf32 selects the
-// tensor-core chunk scan of ssd_chunked_forward_tf32 (its chunks of 128 fused rows need a
-// smaller workspace than the register-tiled path's, which the common size covers).
+// The forward entry points; valid_len is null for ssd_chunked_forward, and tf32 (the
+// ssd_chunked_forward_tf32 entry) insists on the fp32 path with the tensor-core chunk scan
+// instead of falling back to the generic pipeline for other shapes.
 ssd_status chunked_forward(const ssd_shape* shape, const void* x, const float* dA, const void* B,
                            const void* C, const float* theta, const int64_t* valid_len,
                            const float* init_state, void* y, float* final_state, void* workspace,
@@ -261,8 +253,8 @@ ssd_status chunked_forward(const ssd_shape* shape, const void* x, const float* d
   const int32_t variant = tf32 ? SSD_VARIANT_TC_TF32 : pick_variant(shape);
   if (variant == SSD_VARIANT_TC_BF16) {
     e = fused_bf16_forward(p, static_cast<cudaStream_t>(stream));
-  } else if (variant == SSD_VARIANT_TILED_F32 || variant == SSD_VARIANT_TC_TF32) {
-    e = simt32_forward(p, static_cast<cudaStream_t>(stream), variant == SSD_VARIANT_TC_TF32);
+  } else if (variant == SSD_VARIANT_TC_TF32) {
+    e = fp32_forward(p, static_cast<cudaStream_t>(stream));
   } else {
     e = generic_forward(p, shape->io_dtype == SSD_BF16, static_cast<cudaStream_t>(stream));
   }
@@ -445,8 +437,8 @@ ssd_status trapezoidal_forward(const ssd_shape* shape, const void* x, const floa
   p.phisum = theta ? reinterpret_cast<double*>(ws + lay.inner.phisum) : nullptr;
   p.hdr = reinterpret_cast<WsHeader*>(ws);
   p.valid_len = valid_len;
-  const cudaError_t ce = pick_variant(&e) == SSD_VARIANT_TILED_F32 ? simt32_forward(p, st, false)
-                                                                    : generic_forward(p, false, st);
+  const cudaError_t ce = pick_variant(&e) == SSD_VARIANT_TC_TF32 ? fp32_forward(p, st)
+                                                                  : generic_forward(p, false, st);
   if (ce != cudaSuccess) return SSD_ERR_CUDA;
   return trap_compact(t, bf16, st) == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
 }

@@ -52,14 +52,12 @@ cudaError_t generic_forward(const GenericParams& p, bool bf16, cudaStream_t st);
 // (phi, phisum) and the K4 pass over chunks (states -> h_in in place, final state).
 cudaError_t generic_phi(const GenericParams& p, cudaStream_t st);
 cudaError_t generic_state_pass(const GenericParams& p, cudaStream_t st);
-// fp32 I/O with P = N = 64, mimo_rank 1, 64 | chunk_len <= 512: register-tiled CUDA-core kernels.
-bool simt32_supported(int64_t P, int64_t N, int64_t R, int64_t l, bool bf16, bool theta);
-// With tc_scan the chunk scan (K2 + K5) runs as the tf32 tensor-core kernel (p.l * p.R = 128).
-cudaError_t simt32_forward(const GenericParams& p, cudaStream_t st, bool tc_scan);
-// fp32 I/O with P = N = 64 and R a power of two up to 64: K2 + K5 as tcgen05 kind::tf32 products
-// over chunks of 128 fused rows (three split products, 32-deep K blocks).
+// fp32 I/O with P = N = 64 and R a power of two up to 64, over chunks of 128 fused rows
+// (p.l * p.R = 128): the chunk states on the CUDA cores (K1, K3), the K4 pass, and the chunk
+// scan (K2 + K5) as tcgen05 kind::tf32 products with split operands and 32-deep K blocks.
 bool tc32_supported(int64_t P, int64_t N, int64_t R, bool bf16);
 int64_t tc32_chunk_len(int64_t R);
+cudaError_t fp32_forward(const GenericParams& p, cudaStream_t st);
 cudaError_t tc32_scan(const GenericParams& p, cudaStream_t st);
 
 // Host-side validation of an SSD shape (the ssd_chunked_* rules).

@@ -66,10 +66,11 @@ typedef enum ssd_kernel_variant {
   SSD_VARIANT_NONE = 0,    /* shape not supported                                    */
   SSD_VARIANT_GENERIC = 1, /* CUDA-core fp32 chunk pipeline (any supported shape)    */
   SSD_VARIANT_TC_BF16 = 2, /* fused tcgen05/TMEM kernel, bf16 operands, fp32 accum.  */
-  SSD_VARIANT_TILED_F32 = 3, /* register-tiled CUDA-core fp32 kernels, P = N = 64, R | 64 */
-  SSD_VARIANT_TC_TF32 = 4    /* the family ssd_chunked_forward_tf32 runs (not chosen by
-                                ssd_chunked_forward): the tiled path with the chunk scan as
-                                tcgen05 kind::tf32 products */
+  SSD_VARIANT_TILED_F32 = 3, /* not returned by this library: the all-CUDA-core fp32 path that
+                                SSD_VARIANT_TC_TF32 replaced (value kept for the ABI)        */
+  SSD_VARIANT_TC_TF32 = 4    /* fp32, P = N = 64, R | 64: CUDA-core chunk states + K4 pass, the
+                                chunk scan as tcgen05 kind::tf32 (split operands, 32-deep K
+                                blocks)                                                      */
 } ssd_kernel_variant;
 
 /*
@@ -145,18 +146,19 @@ ssd_status ssd_chunked_forward_varlen(const ssd_shape* shape, const void* x, con
                                       size_t workspace_bytes, void* stream);
 
 /*
- * ssd_chunked_forward for fp32 I/O with headdim = dstate = 64 and mimo_rank a power of two up to
- * 64, with the chunk scan (the serial.rs page's K2 and K5: CB = C B^T, the decay mask, (L o CB) x
- * and C h_in, the scan.py page's rotation absorbed into B and C) on the tensor core as
- * tcgen05.mma kind::tf32 over chunks of 128 fused rows (128 / mimo_rank steps, whatever
- * chunk_len says: the result does not depend on it).  Every fp32 operand is split into a tf32
- * high part and its remainder and each pair takes three products (hi.lo, lo.hi, then hi.hi),
- * accumulated in TMEM over one 32-deep K block at a time and summed in fp32 round-to-nearest, so
- * the tensor core's truncating accumulation stays within the fp32 gate 1e-4 (1 + |y|).  K1, K3
- * and K4 run on the CUDA cores as in ssd_chunked_forward (SSD_VARIANT_TILED_F32).
- * valid_len: NULL, or as for ssd_chunked_forward_varlen.  Other arguments, the workspace size
- * (ssd_chunked_workspace_bytes covers both fp32 scans), asynchrony and errors as for
- * ssd_chunked_forward; UNSUPPORTED for any other shape or dtype.
+ * The fp32 path with the chunk scan on the tensor core, which ssd_chunked_forward itself runs
+ * for fp32 I/O with headdim = dstate = 64 and mimo_rank a power of two up to 64
+ * (SSD_VARIANT_TC_TF32); this entry returns UNSUPPORTED for any other shape or dtype instead of
+ * falling back to the generic CUDA-core pipeline.  The chunk scan (the serial.rs page's K2 and
+ * K5: CB = C B^T, the decay mask, (L o CB) x and C h_in, the scan.py page's rotation absorbed
+ * into B and C) runs as tcgen05.mma kind::tf32 over chunks of 128 fused rows (128 / mimo_rank
+ * steps, whatever chunk_len says: the result does not depend on it).  Every fp32 operand is
+ * split into a tf32 high part and its remainder and each pair takes three products (hi.lo,
+ * lo.hi, then hi.hi), accumulated in TMEM over one 32-deep K block at a time and summed in fp32
+ * round-to-nearest, so the tensor core's truncating accumulation stays within the fp32 gate
+ * 1e-4 (1 + |y|).  K1 and K3 (chunk states) run as fp32 FMAs on the CUDA cores, K4 as the state
+ * pass.  valid_len: NULL, or as for ssd_chunked_forward_varlen.  Other arguments, the workspace
+ * size, asynchrony and errors as for ssd_chunked_forward.
  */
 ssd_status ssd_chunked_forward_tf32(const ssd_shape* shape, const void* x, const float* dA,
                                     const void* B, const void* C, const float* theta,
@@ -171,7 +173,7 @@ size_t ssd_trapezoidal_workspace_bytes(const ssd_shape* shape);
  * Which kernel family ssd_trapezoidal_forward runs for `shape` (SSD_VARIANT_NONE if none):
  * SSD_VARIANT_TC_BF16 for bf16 I/O without rotation when the fused tensor-core kernel takes the
  * shape at 2·mimo_rank channels (P = 64, N = 128, 2R dividing 128 and at most 32, nheads % 4 = 0),
- * otherwise the family of the fp32 2R-channel expansion (TILED_F32 or GENERIC).
+ * otherwise the family of the fp32 2R-channel expansion (TC_TF32 or GENERIC).
  */
 int32_t ssd_trapezoidal_variant(const ssd_shape* shape);
 

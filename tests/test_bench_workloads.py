@@ -1,5 +1,5 @@
 """bench.py's workload plumbing on CPU: every named workload resolves, its algorithmic bytes and
-FLOPs are positive, the FLOP count of the register-tiled fp32 path uses the 64-row chunks the
+FLOPs are positive, the FLOP count of the fp32 tensor-core path uses the 128-row chunks the
 kernels tile by, and the backward's bytes grow with the gradients it writes (no GPU involved)."""
 import pytest
 
@@ -36,8 +36,8 @@ def test_fp32_flops_counted_at_the_kernel_chunk():
     cfg = wl.LONG_ROT_F32
     shape = pkg.make_shape(cfg.batch, cfg.seqlen, cfg.nheads, cfg.headdim, cfg.dstate,
                            cfg.ngroups, cfg.mimo_rank, cfg.chunk_len, "f32", cfg.theta)
-    assert pkg.ssd_chunked_variant(shape) == "tiled_f32"
-    assert bench.kernel_chunk(pkg, shape, 1, cfg.chunk_len) == 64
+    assert pkg.ssd_chunked_variant(shape) == "tc_tf32"
+    assert bench.kernel_chunk(pkg, shape, 1, cfg.chunk_len) == 128
     bf = wl.MAMBA2_SISO_BF16
     bshape = pkg.make_shape(bf.batch, bf.seqlen, bf.nheads, bf.headdim, bf.dstate, bf.ngroups,
                             bf.mimo_rank, bf.chunk_len, "bf16", False)

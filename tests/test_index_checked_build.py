@@ -23,12 +23,12 @@ SSD_SHAPES = [
     (wl.SSDConfig("ck_fused_ragged", 2, 700, 4, 64, 128, 256, 1, 1, "bf16"), None),
     (wl.SSDConfig("ck_fused_mimo_segments", 1, 1000, 4, 64, 128, 64, 4, 4, "bf16"), None),
     (wl.SSDConfig("ck_fused_varlen", 3, 300, 4, 64, 128, 64, 2, 2, "bf16"), [300, 97, 1]),
-    (wl.SSDConfig("ck_tiled_rot_ragged", 2, 333, 4, 64, 64, 256, 1, 4, "f32", theta=True), None),
+    (wl.SSDConfig("ck_tc32_rot_ragged", 2, 333, 4, 64, 64, 256, 1, 4, "f32", theta=True), None),
     (wl.SSDConfig("ck_generic_mimo", 2, 150, 3, 16, 32, 64, 2, 3, "f32", theta=True), [150, 77]),
 ]
 TRAP_SHAPES = [
     wl.SSDConfig("ck_trap_fused", 2, 300, 4, 64, 128, 64, 2, 2, "bf16", **T),
-    wl.SSDConfig("ck_trap_tiled_rot", 1, 200, 4, 64, 64, 64, 2, 4, "f32", theta=True, **T),
+    wl.SSDConfig("ck_trap_tc32_rot", 1, 200, 4, 64, 64, 64, 2, 4, "f32", theta=True, **T),
 ]
 SS_SHAPES = [
     wl.SelectiveScanConfig("ck_ss_lookback", 2, 1000, 20, 16),

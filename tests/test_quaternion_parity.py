@@ -14,8 +14,8 @@ from tests.parity_util import TOL, check_close, to_np
 pytestmark = pytest.mark.gpu
 
 CASES = [
-    # register-tiled fp32 path after the turn (P = N = 64), several chunks
-    wl.SSDConfig("quat_tiled_f32", 2, 600, 4, 64, 64, 128, 1, 2, "f32"),
+    # fp32 P = N = 64 path after the turn (tf32 tensor-core chunk scan), several chunks
+    wl.SSDConfig("quat_tc32_f32", 2, 600, 4, 64, 64, 128, 1, 2, "f32"),
     # generic path: MIMO rank 2, a group shared by three heads, ragged T, small odd P
     wl.SSDConfig("quat_generic_mimo_f32", 1, 203, 3, 5, 12, 32, 2, 1, "f32"),
     # bf16 I/O: widened around the fp32 problem

@@ -13,8 +13,8 @@ pytestmark = pytest.mark.gpu
 CASES = [
     # generic path (P, N small), MIMO with groups, ragged T
     wl.SSDConfig("rot_generic_f32", 2, 150, 4, 16, 16, 64, 2, 2, "f32", theta=True),
-    # register-tiled fp32 path (P = N = 64)
-    wl.SSDConfig("rot_tiled_f32", 1, 256, 3, 64, 64, 64, 1, 1, "f32", theta=True),
+    # fp32 P = N = 64 path (tf32 tensor-core chunk scan)
+    wl.SSDConfig("rot_tc32_f32", 1, 256, 3, 64, 64, 64, 1, 1, "f32", theta=True),
     # bf16 I/O (rotation runs on the generic path)
     wl.SSDConfig("rot_bf16", 1, 128, 2, 32, 32, 32, 1, 2, "bf16", theta=True),
 ]

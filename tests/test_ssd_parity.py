@@ -90,14 +90,15 @@ EDGE = [
     wl.SSDConfig("fused_r8_g4", 1, 256, 4, 64, 128, 16, 8, 4, "bf16"),
     # fused kernel with time segments of unequal length (9 tiles on 8 sequences: 5 + 4)
     wl.SSDConfig("fused_uneven_segments", 1, 1152, 8, 64, 128, 128, 1, 1, "bf16"),
-    # register-tiled fp32 path: one 64-row tile per chunk without rotation, two groups; six
-    # tiles per chunk with rotation and one group shared by three heads
-    wl.SSDConfig("tiled_f32_l64_g2", 2, 512, 4, 64, 64, 64, 1, 2, "f32"),
-    wl.SSDConfig("tiled_f32_l384_theta_shared", 1, 768, 3, 64, 64, 384, 1, 1, "f32", theta=True),
-    # register-tiled fp32 path with MIMO rank-fused rows (64 / R steps per chunk): rank 2 with
-    # rotation and a ragged tail; rank 4 with two groups
-    wl.SSDConfig("tiled_f32_mimo_r2_theta", 1, 200, 2, 64, 64, 64, 2, 1, "f32", theta=True),
-    wl.SSDConfig("tiled_f32_mimo_r4_groups", 2, 96, 4, 64, 64, 128, 4, 2, "f32"),
+    # fp32 path with the tf32 tensor-core chunk scan (128 fused rows per chunk whatever
+    # chunk_len says): four chunks without rotation, two groups; six chunks with rotation and
+    # one group shared by three heads
+    wl.SSDConfig("tc32_f32_l64_g2", 2, 512, 4, 64, 64, 64, 1, 2, "f32"),
+    wl.SSDConfig("tc32_f32_l384_theta_shared", 1, 768, 3, 64, 64, 384, 1, 1, "f32", theta=True),
+    # the same with MIMO rank-fused rows (128 / R steps per chunk): rank 2 with rotation and a
+    # ragged tail; rank 4 with two groups
+    wl.SSDConfig("tc32_f32_mimo_r2_theta", 1, 200, 2, 64, 64, 64, 2, 1, "f32", theta=True),
+    wl.SSDConfig("tc32_f32_mimo_r4_groups", 2, 96, 4, 64, 64, 128, 4, 2, "f32"),
 ]
 
 
@@ -111,15 +112,15 @@ RAGGED = [
     wl.SSDConfig("ragged_fused_bf16", 2, 300, 4, 64, 128, 256, 1, 1, "bf16"),
     wl.SSDConfig("ragged_fused_mimo_bf16", 1, 90, 4, 64, 128, 32, 4, 2, "bf16"),
     wl.SSDConfig("ragged_fused_segments_bf16", 1, 1000, 8, 64, 128, 128, 1, 1, "bf16"),
-    wl.SSDConfig("ragged_tiled_f32", 1, 200, 2, 64, 64, 64, 1, 1, "f32"),
-    wl.SSDConfig("ragged_tiled_theta_f32", 2, 130, 3, 64, 64, 128, 1, 1, "f32", theta=True),
+    wl.SSDConfig("ragged_tc32_f32", 1, 200, 2, 64, 64, 64, 1, 1, "f32"),
+    wl.SSDConfig("ragged_tc32_theta_f32", 2, 130, 3, 64, 64, 128, 1, 1, "f32", theta=True),
 ]
 
 
 @pytest.mark.parametrize("cfg", RAGGED, ids=lambda c: c.name)
 def test_ragged_sequence_lengths(cfg):
     assert cfg.seqlen % cfg.chunk_len != 0
-    expect = {"generic": "generic", "fused": "tc_bf16", "tiled": "tiled_f32"}[cfg.name.split("_")[1]]
+    expect = {"generic": "generic", "fused": "tc_bf16", "tc32": "tc_tf32"}[cfg.name.split("_")[1]]
     shape = pkg.make_shape(cfg.batch, cfg.seqlen, cfg.nheads, cfg.headdim, cfg.dstate,
                            cfg.ngroups, cfg.mimo_rank, cfg.chunk_len, cfg.dtype, cfg.theta)
     assert pkg.ssd_chunked_variant(shape) == expect, cfg.name
@@ -153,11 +154,11 @@ def test_per_sequence_valid_length_by_zero_padding(cfg):
         check_close(fin[b:b + 1], fr, TOL[cfg.dtype], f"{cfg.name} final[b={b}]")
 
 
-def test_f32_workloads_use_the_tiled_kernels():
+def test_f32_workloads_use_the_tf32_tensor_core_scan():
     for cfg in (wl.LONG_ROT_F32, EDGE[-1], EDGE[-2], EDGE[-3], EDGE[-4]):
         shape = pkg.make_shape(cfg.batch, cfg.seqlen, cfg.nheads, cfg.headdim, cfg.dstate,
                                cfg.ngroups, cfg.mimo_rank, cfg.chunk_len, cfg.dtype, cfg.theta)
-        assert pkg.ssd_chunked_variant(shape) == "tiled_f32", cfg.name
+        assert pkg.ssd_chunked_variant(shape) == "tc_tf32", cfg.name
 
 
 def test_fused_launches_follow_the_segmentation():

@@ -34,7 +34,7 @@ def test_trapezoidal_parity(cfg, variant):
     inp = wl.make_trap_inputs(cfg, seed=21, prev=variant != "no_prev", **kw)
     x, B = inp["x"], inp["B"]
     shape = pkg.shape_of(x, B, cfg.chunk_len, inp["theta"] is not None)
-    want = "tc_bf16" if cfg.name in FUSED else ("tiled_f32", "generic")
+    want = "tc_bf16" if cfg.name in FUSED else ("tc_tf32", "generic")
     got = pkg.ssd_trapezoidal_variant(shape)
     assert got == want if isinstance(want, str) else got in want, (cfg.name, got)
     y, fin = gpu_trap(inp, cfg.chunk_len)

@@ -35,10 +35,10 @@ SSD_CASES = [
     # sequence ends in its third segment, so later segments run on padding only
     (wl.SSDConfig("vl_fused_segmented_bf16", 2, 4096, 4, 64, 128, 256, 1, 1, "bf16"),
      [4096, 1234], "tc_bf16"),
-    (wl.SSDConfig("vl_tiled_f32", 3, 600, 4, 64, 64, 256, 1, 2, "f32"),
-     [600, 300, 37], "tiled_f32"),
-    (wl.SSDConfig("vl_tiled_rot_f32", 2, 700, 4, 64, 64, 256, 1, 4, "f32", theta=True),
-     [513, 700], "tiled_f32"),
+    (wl.SSDConfig("vl_tc32_f32", 3, 600, 4, 64, 64, 256, 1, 2, "f32"),
+     [600, 300, 37], "tc_tf32"),
+    (wl.SSDConfig("vl_tc32_rot_f32", 2, 700, 4, 64, 64, 256, 1, 4, "f32", theta=True),
+     [513, 700], "tc_tf32"),
     (wl.SSDConfig("vl_generic_rot_mimo_f32", 3, 333, 3, 16, 32, 64, 2, 3, "f32", theta=True),
      [333, 200, 64], "generic"),
     (wl.SSDConfig("vl_generic_bf16", 2, 257, 2, 32, 32, 128, 1, 1, "bf16"),
