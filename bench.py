@@ -49,7 +49,8 @@ ALU_FP32_TFLOPS = round(152 * 128 * 2 * 2.07e9 / 1e12, 1)
 NCU_TRAFFIC_BYTES = {
     "mamba2_siso_bf16": 77_669_632 + 27_295_744,           # ssd_fused_bf16_kernel<false>
     "mamba3_mimo_bf16": 1_441_407_232 + 253_506_816,       # ssd_fused_bf16_kernel<false>
-    "long_rotation_f32": 3_937_686_272 + 788_730_368,      # simt_scan_kernel
+    # tc32_scan_kernel, captured at T = 16384 and scaled by 8 (its traffic grows with T)
+    "long_rotation_f32": (407_444_736 + 79_954_432) * 8,
     "selective_scan_f32": 77_815_552 + 8_036_864,          # ss_lookback_kernel
     # bwd_chunk_grad_kernel, captured at batch 1 and scaled by 4 (traffic grows with the batch)
     "mamba2_backward_bf16": (191_560_192 + 22_935_552) * 4,
@@ -415,9 +416,8 @@ def run_ours(args, rank, world, local):
     ms = slowest_replica_ms(sum(step_ms) / len(step_ms), world, dev)
     tokens = job_tokens(cfg.tokens, world)
     hbm, tf, peak_src = measured_peaks()
-    # the capture's bytes belong to the workload's own shape and default kernels
-    traffic = (None if (args.batch or args.seqlen or args.tf32)
-               else NCU_TRAFFIC_BYTES.get(cfg.name))
+    # the capture's bytes belong to the workload's own shape, not to an overridden one
+    traffic = None if (args.batch or args.seqlen) else NCU_TRAFFIC_BYTES.get(cfg.name)
     kernel = ("selective_scan_forward" if is_ss
               else ("ssd_trapezoidal_backward" if cfg.trapezoidal else "ssd_chunked_backward")
               if variant == "backward"
