@@ -319,9 +319,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc32_scan_kernel(GenericParams p,
 #pragma unroll
       for (int k = 0; k < 16; ++k) yo[k] = a0[k] + a1[k];
     }
-    // the mask of columns j = 32 cw .. 32 cw + 31, 16 at a time
+    // the mask of columns j = 32 cw .. 32 cw + 31, 16 at a time; 2^x on the special-function
+    // unit (relative error ~2^-22, results below 2^-126 flushed to zero: far below the gate)
     const float chi = cum_hi[ti], clo = cum_lo[ti];
-#pragma unroll 1
+#pragma unroll
     for (int hb = 0; hb < 2; ++hb) {
       const int j0 = 32 * cw + 16 * hb;
       uint32_t mh[16], ml[16];
@@ -339,7 +340,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc32_scan_kernel(GenericParams p,
         for (int k = 0; k < 16; ++k) {
           const int tj = (j0 + k) >> rs;
           const float m = tj <= ti
-                              ? exp2f((chi - cum_hi[tj]) + (clo - cum_lo[tj])) * (v0[k] + v1[k])
+                              ? fp::ex2_approx((chi - cum_hi[tj]) + (clo - cum_lo[tj])) *
+                                    (v0[k] + v1[k])
                               : 0.f;
           const float mhi = tf32_hi(m);
           mh[k] = __float_as_uint(mhi);
