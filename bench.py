@@ -50,7 +50,7 @@ NCU_TRAFFIC_BYTES = {
     "mamba2_siso_bf16": 77_669_632 + 27_295_744,           # ssd_fused_bf16_kernel<false>
     "mamba3_mimo_bf16": 1_441_407_232 + 253_506_816,       # ssd_fused_bf16_kernel<false>
     # tc32_scan_kernel, captured at T = 16384 and scaled by 8 (its traffic grows with T)
-    "long_rotation_f32": (407_444_736 + 79_954_432) * 8,
+    "long_rotation_f32": (407_122_688 + 79_207_168) * 8,
     "selective_scan_f32": 77_815_552 + 8_036_864,          # ss_lookback_kernel
     # bwd_chunk_grad_kernel, captured at batch 1 and scaled by 4 (traffic grows with the batch)
     "mamba2_backward_bf16": (191_560_192 + 22_935_552) * 4,
