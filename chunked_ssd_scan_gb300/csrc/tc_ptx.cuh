@@ -30,13 +30,6 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
                : "memory");
 }
 
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
-  asm volatile(
-      "{\n\t.reg .b64 st;\n\tmbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(
-          smem_u32(bar)),
-      "r"(bytes)
-      : "memory");
-}
 
 // Waits (suspended in hardware, not polling) until the phase with `parity` completes or about
 // `suspend_ns` nanoseconds pass; returns whether it completed.
@@ -83,23 +76,7 @@ __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
-__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar,
-                                            int32_t x, int32_t y) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y)
-      : "memory");
-}
 
-__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, uint64_t* bar,
-                                            int32_t x, int32_t y, int32_t z) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z)
-      : "memory");
-}
 
 // Generic-proxy shared-memory writes -> visible to the async proxy (tcgen05.mma operands).
 __device__ __forceinline__ void fence_proxy_async_smem() {
@@ -133,35 +110,8 @@ __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// ---------------------------------------------------------------------------------- MMA
-// D[tmem] (+)= A[smem desc] * B[smem desc]^T-as-described, kind::f16 (bf16 in, f32 accumulate),
-// issued by one thread.
-__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                         uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
 
-// Same with kind::tf32 (fp32 storage, tf32 multiply, f32 accumulate).
-__device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                         uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
 
-// Arrive on `bar` once all previously issued tcgen05.mma of this thread have completed.
-__device__ __forceinline__ void mma_commit(uint64_t* bar) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-          smem_u32(bar))
-      : "memory");
-}
 
 // Instruction descriptor, kind::f16 with bf16 A/B and f32 D.  a_mn / b_mn select MN-major
 // (transposed) operands.
@@ -174,16 +124,6 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int a_mn, int b_
 __host__ __device__ constexpr uint32_t idesc_tf32(int M, int N, int a_mn, int b_mn) {
   return (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)a_mn << 15) | ((uint32_t)b_mn << 16) |
          ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
-}
-
-// Shared-memory matrix descriptor with 128-byte swizzling.
-//  K-major operand: rows of 128 B (64 bf16 of K), 8-row atoms of 1024 B; sbo = byte stride
-//    between 8-row groups (1024 when packed); lbo unused.
-//  MN-major operand: rows of 128 B (64 elements of M/N) indexed by K, 8 K-rows per 1024-B atom;
-//    lbo = byte stride between 64-wide M/N blocks, sbo = byte stride between 8-row K groups.
-__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t smem_addr, uint32_t lbo, uint32_t sbo) {
-  return (uint64_t)((smem_addr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
-         ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
 }
 
 // ---------------------------------------------------------------------------------- TMEM ld/st
@@ -213,37 +153,8 @@ __device__ __forceinline__ void reg_tie(float (&v)[N]) {
   for (int i = 0; i < N; ++i) asm volatile("" : "+f"(v[i]));
 }
 
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const float (&v)[16]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
-      "%14,%15,%16};" ::"r"(taddr),
-      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
-      "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
-      "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
-      "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
-      "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
-      "r"(__float_as_uint(v[15]))
-      : "memory");
-}
 
-// 32 lanes x 32 bits, 8 consecutive columns per thread.
-__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&v)[8]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr),
-      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
-      : "memory");
-}
 
-// D[tmem] (+)= A[tmem] * B[smem desc], kind::f16.  A is M rows (TMEM lanes) by 16 bf16 of K
-// packed two per 32-bit column (8 columns per instruction), even K index in the low half.
-__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                            uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
 
 __device__ __forceinline__ void tmem_st_wait() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
@@ -260,28 +171,7 @@ __host__ __device__ __forceinline__ uint32_t sw128_off32(uint32_t row, uint32_t 
   return row * 128u + ((((col >> 2) ^ row) & 7u) << 4) + ((col & 3u) << 2);
 }
 
-// ---------------------------------------------------------------------------------- elected issue
-// The variants below are executed by a whole converged warp; one lane (elect.sync) performs the
-// operation.  Keeping the election inside the same asm statement keeps the operands warp-uniform,
-// which is what makes back-to-back tcgen05.mma issue cheap.
-__device__ __forceinline__ void mma_bf16_elect(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                               uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p, e;\n\tsetp.ne.b32 p, %4, 0;\n\telect.sync _|e, 0xffffffff;\n\t"
-      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
 
-__device__ __forceinline__ void mma_bf16_ts_elect(uint32_t d_tmem, uint32_t a_tmem,
-                                                  uint64_t b_desc, uint32_t idesc,
-                                                  uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p, e;\n\tsetp.ne.b32 p, %4, 0;\n\telect.sync _|e, 0xffffffff;\n\t"
-      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
 
 __device__ __forceinline__ void mma_commit_elect(uint64_t* bar) {
   asm volatile(
@@ -299,26 +189,7 @@ __device__ __forceinline__ void mbar_arrive_expect_tx_elect(uint64_t* bar, uint3
       : "memory");
 }
 
-__device__ __forceinline__ void tma_load_2d_elect(void* dst, const CUtensorMap* map,
-                                                  uint64_t* bar, int32_t x, int32_t y) {
-  asm volatile(
-      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
-      "@e cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%3, %4}], [%2];\n\t}" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y)
-      : "memory");
-}
 
-__device__ __forceinline__ void tma_load_3d_elect(void* dst, const CUtensorMap* map,
-                                                  uint64_t* bar, int32_t x, int32_t y,
-                                                  int32_t z) {
-  asm volatile(
-      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
-      "@e cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%3, %4, %5}], [%2];\n\t}" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z)
-      : "memory");
-}
 
 __device__ __forceinline__ void tma_load_4d_elect(void* dst, const CUtensorMap* map,
                                                   uint64_t* bar, int32_t x, int32_t y,
@@ -411,9 +282,14 @@ __device__ __forceinline__ void tmem_st32u(uint32_t taddr, const uint32_t (&v)[3
 }
 
 // ---------------------------------------------------------------------------------- lean issue
-// Issue forms for a single issuing thread: the 64-bit smem descriptors are passed as their two
-// 32-bit words (the high word is constant for a whole operand; the low word carries the start
-// address), so a group of MMAs costs about three instructions per MMA.
+// Shared-memory matrix descriptors with 128-byte swizzling, passed to the MMA as their two 32-bit
+// words: the high word is constant for a whole operand, the low word carries the start address
+// (a start-address step of s bytes adds s >> 4 to it), so a group of MMAs costs about three
+// instructions per MMA.
+//  K-major operand: rows of 128 B (64 bf16 or 32 tf32 of K), 8-row atoms of 1024 B; sbo = byte
+//    stride between 8-row groups (1024 when packed); lbo unused.
+//  MN-major operand: rows of 128 B (64 elements of M/N) indexed by K, 8 K-rows per 1024-B atom;
+//    lbo = byte stride between 64-wide M/N blocks, sbo = byte stride between 8-row K groups.
 __host__ __device__ constexpr uint32_t sdesc_sw128_hi(uint32_t sbo) {
   return ((sbo >> 4) & 0x3FFFu) | (1u << 14) | (2u << 29);
 }
@@ -421,27 +297,10 @@ __device__ __forceinline__ uint32_t sdesc_sw128_lo(uint32_t smem_addr, uint32_t 
   return ((smem_addr & 0x3FFFFu) >> 4) | (((lbo >> 4) & 0x3FFFu) << 16);
 }
 
-__device__ __forceinline__ void mma_ss_w(uint32_t d_tmem, uint32_t alo, uint32_t ahi, uint32_t blo,
-                                         uint32_t bhi, uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t.reg .b64 ad, bd;\n\tsetp.ne.b32 p, %6, 0;\n\t"
-      "mov.b64 ad, {%1, %2};\n\tmov.b64 bd, {%3, %4};\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], ad, bd, %5, p;\n\t}" ::"r"(d_tmem),
-      "r"(alo), "r"(ahi), "r"(blo), "r"(bhi), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
 
-__device__ __forceinline__ void mma_ts_w(uint32_t d_tmem, uint32_t a_tmem, uint32_t blo,
-                                         uint32_t bhi, uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t.reg .b64 bd;\n\tsetp.ne.b32 p, %5, 0;\n\t"
-      "mov.b64 bd, {%2, %3};\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], bd, %4, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "r"(blo), "r"(bhi), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
 
-// Elected forms of the two above: executed by a whole converged warp, one lane issues.
+// MMA issue, executed by a whole converged warp: one lane (elect.sync) issues.  SS: A and B
+// from shared memory; TS: A from TMEM.  kind::f16 with bf16 A and B, f32 D.
 __device__ __forceinline__ void mma_ss_we(uint32_t d_tmem, uint32_t alo, uint32_t ahi,
                                           uint32_t blo, uint32_t bhi, uint32_t idesc,
                                           uint32_t accumulate) {
